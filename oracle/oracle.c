@@ -1,0 +1,362 @@
+/*
+ * Float64 CPU oracle for the indexer-selected sparse attention step.
+ *
+ * TEST INFRASTRUCTURE ONLY: the tests, the package smoke check and the
+ * benchmark's CPU-baseline leg call it; the product path never does.  It is
+ * plain and slow on purpose: one loop nest per definition, no blocking, no
+ * fusion, every value decoded from its storage format and combined in IEEE
+ * double.  The only parallelism is an OpenMP loop over independent query
+ * tokens.
+ *
+ * Sources (page title, section):
+ *  - "DeepSeek-V4.1-Flash-NVFP4 inference/model.py", Indexer.forward: the
+ *    index score einsum, its ReLU and the weighted sum over index heads; the
+ *    visibility rule for compressed positions; the top-k kept per query,
+ *    re-sorted into position order, with -1 for unreachable picks.
+ *  - same page, get_window_topk_idxs and Attention._window_kv: the raw
+ *    sliding window (a ring of window_size slots, the query's own token
+ *    included) and Attention.forward: one sparse attention over the window
+ *    rows concatenated with the selected compressed rows.
+ *  - "DeepSeek-V3.2-Exp inference/model.py", Indexer.forward: fp8-e4m3 index
+ *    keys with one fp32 scale per position (head_dim 128 = one block), and
+ *    fp8 queries with a per-(token, head) scale folded into the weights.
+ *
+ * Readings where the pages are silent (each listed in the design notes):
+ *  - scales are dequantisation multipliers: q_hat = q * q_scale[t,h],
+ *    k_hat = k * k_scale[b,s]; w is used as given (callers fold softmax and
+ *    head-count scaling into it, as both pages do);
+ *  - ties in the top-k go to the lower position;
+ *  - the optional attention sink adds exp(sink_h - m) to the softmax
+ *    denominator only (parity unpinned: the formula is not on the pages);
+ *  - window rows and compressed rows are concatenated, never de-duplicated.
+ *
+ * Compile-time ORC_MUTANT=n builds deliberately wrong variants; the pin tests
+ * build them to show that each plausible mistake fails at least one pin.  The
+ * default build (ORC_MUTANT undefined) is the oracle.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#include "oracle.h"
+
+#ifndef ORC_MUTANT
+#define ORC_MUTANT 0
+#endif
+
+/* ---- storage formats ---------------------------------------------------- */
+
+/* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 mantissa bits. */
+double orc_bf16_value(uint16_t bits) {
+  int sign = bits >> 15;
+  int e = (bits >> 7) & 0xFF;
+  int m = bits & 0x7F;
+  double v;
+  if (e == 0xFF)
+    v = m ? NAN : INFINITY;
+  else if (e == 0)
+    v = ldexp((double)m, -126 - 7); /* subnormal: 0.m * 2^-126 */
+  else
+    v = ldexp(128.0 + m, e - 127 - 7); /* 1.m * 2^(e-127) */
+  return sign ? -v : v;
+}
+
+/* float8 e4m3fn: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits, no
+ * infinities, S.1111.111 is NaN, exponent 0 holds the subnormals. */
+double orc_e4m3_value(uint8_t bits) {
+  int sign = bits >> 7;
+  int e = (bits >> 3) & 0xF;
+  int m = bits & 0x7;
+  double v;
+  if (e == 0xF && m == 0x7)
+    v = NAN;
+  else if (e == 0)
+    v = ldexp((double)m, -6 - 3); /* subnormal: 0.m * 2^-6 */
+  else
+    v = ldexp(8.0 + m, e - 7 - 3); /* 1.m * 2^(e-7) */
+  return sign ? -v : v;
+}
+
+static double elem(const void *base, int32_t dtype, int64_t i) {
+  if (dtype == ORC_BF16) return orc_bf16_value(((const uint16_t *)base)[i]);
+  return orc_e4m3_value(((const uint8_t *)base)[i]);
+}
+
+/* ---- visibility and window ---------------------------------------------- */
+
+/* Compressed entry j stands for tokens [j*r, (j+1)*r) and becomes visible once
+ * the query has passed its last token: the query at absolute position p sees
+ * the entries j < floor((p + 1) / r).  (Prefill: compress_lens =
+ * arange(1, seqlen + 1) // ratio; decode: end_pos // ratio with
+ * end_pos = p + 1.) */
+int32_t orc_n_vis(int32_t pos, int32_t r) {
+#if ORC_MUTANT == 4
+  return pos / r;
+#else
+  return (pos + 1) / r;
+#endif
+}
+
+/* The raw window of the query at position p: positions max(0, p-W+1) .. p,
+ * its own token included (decode writes the token into its ring slot before
+ * attending).  Each lives in ring slot position mod R.  Oldest first. */
+int32_t orc_window_slots(int32_t pos, int32_t W, int32_t R, int32_t *slots) {
+  int32_t n = 0;
+#if ORC_MUTANT == 6
+  for (int32_t p = pos - W; p <= pos - 1; ++p)
+#else
+  for (int32_t p = pos - W + 1; p <= pos; ++p)
+#endif
+  {
+    if (p < 0) continue;
+    slots[n++] = p % R;
+  }
+  return n;
+}
+
+static int valid_token(const orc_problem *P, int32_t t) {
+  if (t < 0 || t >= P->T) return 0;
+  int32_t b = P->q_seq[t];
+  if (b < 0 || b >= P->B) return 0;
+  if (P->q_pos[t] < 0) return 0;
+  if (orc_n_vis(P->q_pos[t], P->r) > P->N_c) return 0;
+  return 1;
+}
+
+/* ---- index scores -------------------------------------------------------- */
+
+/* S[t,s] = sum_h w[t,h] * ReLU( sum_d q_hat[t,h,d] * k_hat[b,s,d] ) for the
+ * visible positions s < n_vis(t); -inf elsewhere.  A[t,s] is the condition
+ * magnitude sum_h |w[t,h]| * sum_d |q_hat[t,h,d] * k_hat[b,s,d]| that bounds
+ * any rounding error of a finite-precision evaluation. */
+static void score_token(const orc_problem *P, int32_t t, double *S, double *A) {
+  const int64_t N_c = P->N_c, H_I = P->H_I, D_I = P->D_I;
+  const int32_t b = P->q_seq[t];
+  const int32_t nv = orc_n_vis(P->q_pos[t], P->r);
+  for (int64_t s = 0; s < N_c; ++s) {
+    double sum = 0.0, mag = 0.0;
+    if (s >= nv) {
+      S[s] = -INFINITY;
+      if (A) A[s] = 0.0;
+      continue;
+    }
+#if ORC_MUTANT == 3
+    const int64_t krow = (int64_t)0 * N_c + s;
+#else
+    const int64_t krow = (int64_t)b * N_c + s;
+#endif
+#if ORC_MUTANT == 2
+    const double ks = 1.0;
+#else
+    const double ks = P->k_scale ? (double)P->k_scale[krow] : 1.0;
+#endif
+    for (int64_t h = 0; h < H_I; ++h) {
+#if ORC_MUTANT == 11
+      const double qs = 1.0;
+#else
+      const double qs = P->q_scale ? (double)P->q_scale[t * H_I + h] : 1.0;
+#endif
+      double dot = 0.0, adot = 0.0;
+#if ORC_MUTANT == 7
+      for (int64_t d = 0; d < D_I - 1; ++d) {
+#else
+      for (int64_t d = 0; d < D_I; ++d) {
+#endif
+        const double qv = elem(P->q_I, P->q_dtype, (t * H_I + h) * D_I + d) * qs;
+        const double kv = elem(P->k_I, P->k_dtype, krow * D_I + d) * ks;
+        dot += qv * kv;
+        adot += fabs(qv * kv);
+      }
+      const double wh = (double)P->w[t * H_I + h];
+#if ORC_MUTANT == 1
+      sum += wh * dot;
+#elif ORC_MUTANT == 10
+      sum += (dot > 0.0 ? dot : 0.0);
+#else
+      sum += wh * (dot > 0.0 ? dot : 0.0);
+#endif
+      mag += fabs(wh) * adot;
+    }
+    S[s] = sum;
+    if (A) A[s] = mag;
+  }
+}
+
+int32_t orc_index_scores(const orc_problem *P, const int32_t *rows, int32_t n_rows,
+                         double *S, double *A) {
+  for (int32_t i = 0; i < n_rows; ++i)
+    if (!valid_token(P, rows[i])) return -1;
+  const int64_t N_c = P->N_c;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int32_t i = 0; i < n_rows; ++i)
+    score_token(P, rows[i], S + i * N_c, A ? A + i * N_c : NULL);
+  return 0;
+}
+
+/* ---- top-k --------------------------------------------------------------- */
+
+typedef struct {
+  double score;
+  int32_t pos;
+} scored_pos;
+
+/* Higher score first; among equal scores the lower position first. */
+static int by_score_then_pos(const void *a, const void *b) {
+  const scored_pos *x = (const scored_pos *)a, *y = (const scored_pos *)b;
+  if (x->score > y->score) return -1;
+  if (x->score < y->score) return 1;
+#if ORC_MUTANT == 5
+  return (x->pos > y->pos) ? -1 : (x->pos < y->pos);
+#else
+  return (x->pos < y->pos) ? -1 : (x->pos > y->pos);
+#endif
+}
+
+static int ascending_int(const void *a, const void *b) {
+  int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+  return (x < y) ? -1 : (x > y);
+}
+
+/* Keeps K_eff = min(K, n_vis) of the visible positions 0 .. n_vis-1, the
+ * highest scores first with ties to the lower position, and writes them in
+ * ascending position order followed by K - K_eff entries of -1.  Returns
+ * K_eff. */
+int32_t orc_topk_row(const double *S, int32_t n_vis, int32_t K, int32_t *idx) {
+  if (n_vis < 0 || K < 0) return -1;
+  int32_t k_eff = K < n_vis ? K : n_vis;
+  scored_pos *all = (scored_pos *)malloc(sizeof(scored_pos) * (size_t)(n_vis > 0 ? n_vis : 1));
+  for (int32_t s = 0; s < n_vis; ++s) {
+    all[s].score = S[s];
+    all[s].pos = s;
+  }
+  qsort(all, (size_t)n_vis, sizeof(scored_pos), by_score_then_pos);
+  for (int32_t i = 0; i < k_eff; ++i) idx[i] = all[i].pos;
+  qsort(idx, (size_t)k_eff, sizeof(int32_t), ascending_int);
+  for (int32_t i = k_eff; i < K; ++i) idx[i] = -1;
+  free(all);
+  return k_eff;
+}
+
+/* ---- sparse attention ---------------------------------------------------- */
+
+/* For query token t (sequence b, position p) the key set J is the window rows
+ * (ring slots of Kw/Vw) followed by the compressed rows idx[t, :] that are not
+ * -1.  For each head h: l_j = scale * Q[t,h] . K_j, a_j = exp(l_j - m) / Z with
+ * m = max_j l_j and Z = sum_j exp(l_j - m) (+ exp(sink_h - m) when a sink is
+ * given), and O[t,h] = sum_j a_j V_j. */
+static void attn_token(const orc_problem *P, int32_t t, const int32_t *idx_row, int32_t K,
+                       double *O) {
+  const int64_t H = P->H, D = P->D, R = P->R, N_c = P->N_c;
+  const int32_t b = P->q_seq[t];
+  int32_t *slots = (int32_t *)malloc(sizeof(int32_t) * (size_t)(P->W > 0 ? P->W : 1));
+  const int32_t nw = orc_window_slots(P->q_pos[t], P->W, P->R, slots);
+  const int32_t nj = nw + K;
+  const uint16_t **krows = (const uint16_t **)malloc(sizeof(void *) * (size_t)(nj > 0 ? nj : 1));
+  const uint16_t **vrows = (const uint16_t **)malloc(sizeof(void *) * (size_t)(nj > 0 ? nj : 1));
+  double *logit = (double *)malloc(sizeof(double) * (size_t)(nj > 0 ? nj : 1));
+  int32_t n = 0;
+  for (int32_t j = 0; j < nw; ++j) {
+    krows[n] = P->Kw + ((int64_t)b * R + slots[j]) * D;
+    vrows[n] = P->Vw + ((int64_t)b * R + slots[j]) * D;
+    ++n;
+  }
+  for (int32_t k = 0; k < K; ++k) {
+    const int32_t c = idx_row[k];
+    if (c < 0) continue;
+    krows[n] = P->Kc + ((int64_t)b * N_c + c) * D;
+    vrows[n] = P->Vc + ((int64_t)b * N_c + c) * D;
+    ++n;
+  }
+  for (int64_t h = 0; h < H; ++h) {
+    const uint16_t *q = P->Q + ((int64_t)t * H + h) * D;
+    double m = -INFINITY;
+    for (int32_t j = 0; j < n; ++j) {
+      double dot = 0.0;
+      for (int64_t d = 0; d < D; ++d) dot += orc_bf16_value(q[d]) * orc_bf16_value(krows[j][d]);
+#if ORC_MUTANT == 9
+      logit[j] = -(double)P->scale * dot;
+#else
+      logit[j] = (double)P->scale * dot;
+#endif
+      if (logit[j] > m) m = logit[j];
+    }
+    if (P->sink && (double)P->sink[h] > m) m = (double)P->sink[h];
+    double Z = 0.0;
+    for (int32_t j = 0; j < n; ++j) Z += exp(logit[j] - m);
+    if (P->sink) Z += exp((double)P->sink[h] - m);
+    double *o = O + h * D;
+    for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+    for (int32_t j = 0; j < n; ++j) {
+      const double a = exp(logit[j] - m) / Z;
+#if ORC_MUTANT == 8
+      const uint16_t *v = krows[j];
+#else
+      const uint16_t *v = vrows[j];
+#endif
+      for (int64_t d = 0; d < D; ++d) o[d] += a * orc_bf16_value(v[d]);
+    }
+  }
+  free(logit);
+  free(vrows);
+  free(krows);
+  free(slots);
+}
+
+static int valid_idx_row(const orc_problem *P, int32_t t, const int32_t *idx_row, int32_t K) {
+  const int32_t nv = orc_n_vis(P->q_pos[t], P->r);
+  for (int32_t k = 0; k < K; ++k)
+    if (idx_row[k] < -1 || idx_row[k] >= nv) return 0;
+  return 1;
+}
+
+int32_t orc_sparse_attn(const orc_problem *P, const int32_t *idx, int32_t K,
+                        const int32_t *rows, int32_t n_rows, double *O) {
+  for (int32_t i = 0; i < n_rows; ++i)
+    if (!valid_token(P, rows[i]) || !valid_idx_row(P, rows[i], idx + (int64_t)rows[i] * K, K))
+      return -1;
+  const int64_t HD = (int64_t)P->H * P->D;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int32_t i = 0; i < n_rows; ++i)
+    attn_token(P, rows[i], idx + (int64_t)rows[i] * K, K, O + i * HD);
+  return 0;
+}
+
+/* ---- the whole step --------------------------------------------------------
+ * Scores, top-k and attention for the tokens rows[0..n_rows), one token at a
+ * time.  idx and O are written compactly (row i for token rows[i]). */
+int32_t orc_fused(const orc_problem *P, int32_t K, const int32_t *rows, int32_t n_rows,
+                  int32_t *idx, double *O) {
+  for (int32_t i = 0; i < n_rows; ++i)
+    if (!valid_token(P, rows[i])) return -1;
+  const int64_t HD = (int64_t)P->H * P->D;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int32_t i = 0; i < n_rows; ++i) {
+    const int32_t t = rows[i];
+    double *S = (double *)malloc(sizeof(double) * (size_t)(P->N_c > 0 ? P->N_c : 1));
+    score_token(P, t, S, NULL);
+    orc_topk_row(S, orc_n_vis(P->q_pos[t], P->r), K, idx + (int64_t)i * K);
+    attn_token(P, t, idx + (int64_t)i * K, K, O + i * HD);
+    free(S);
+  }
+  return 0;
+}
+
+void orc_set_threads(int32_t n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
+int32_t orc_get_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
