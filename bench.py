@@ -1,0 +1,401 @@
+#!/usr/bin/env python
+"""Throughput of the fused sparse attention step (index scores -> top-k ->
+windowed + sparse MQA) on GB300, as one JSON line.
+
+Default workload: decode, batch 64, positions U[32768, 65535], r=4, index
+64x128 fp8 keys + per-position scale, topk 2048, attention 64x128, window
+128 (the first workload with an HBM-roofline target); ``--workload`` picks
+another.  One step = one sa_fused_decode call over the whole batch with its
+inputs resident in HBM.  Three copies of every input rotate between steps, so
+each step reads data evicted from L2 by the two before it.
+
+``--impl reference`` times the float64 CPU oracle on the host cores instead
+(the baseline arm); it never touches the GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "query-tokens/s of fused indexer+top-k+sparse attn; % of HBM roofline"
+UNIT = "query-tokens/s"
+STAGES = ("idx_score", "idx_topk", "sparse_mqa")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="c2", choices=("c0", "c1", "c2", "c3", "c4"))
+    ap.add_argument("--copies", type=int, default=3)
+    ap.add_argument("--soak-seconds", type=float, default=1.5)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+# ------------------------------------------------------------- accounting ---
+
+def algorithmic_bytes(w):
+    """Per-step algorithmic bytes of each stage (the roofline numerators)."""
+    pos = w.q_pos.astype(np.int64)
+    nv = np.minimum((pos + 1) // w.r, w.N_c)
+    kb = 1 if w.k_dtype == 1 else 2
+    key_row = w.D_I * kb + (4 if w.k_scale is not None else 0)
+    n_w = np.minimum(w.W, pos + 1)
+    k_eff = np.minimum(w.K, nv)
+    kv_row = 2 * w.D * 2  # K and V rows, bf16
+    return {
+        "idx_score": int(np.sum(nv) * key_row),
+        "idx_topk": int(np.sum(nv) * 4 + w.T * w.K * 4),
+        "sparse_mqa": int(np.sum(n_w + k_eff) * kv_row),
+        "step": int(np.sum(nv) * key_row + np.sum(n_w + k_eff) * kv_row),
+    }
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash(stage):
+    src = {"idx_score": "idx_score.cu", "idx_topk": "idx_topk.cu", "sparse_mqa": "sparse_mqa.cu"}[stage]
+    path = os.path.join(ROOT, "indexer_selected_sparse_score_gb300", "csrc", src)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(stage, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of that kernel (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(f"{stage}:{workload}")
+    except Exception:
+        return None
+    if not rec or rec.get("source_sha256_16") != kernel_source_hash(stage):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------- clocks ---
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.rows = []
+        self.proc = None
+        sel = []
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            if vis:
+                sel = ["-i", vis.split(",")[device_index]]
+        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", "200", *sel]
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 7:
+                self.rows.append((time.time(), parts))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [p for (ts, p) in self.rows if t0 <= ts <= t1]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(p[0]) for p in rows if p[0].replace(".", "", 1).isdigit()]
+        mx = [float(p[1]) for p in rows if p[1].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in rows for i in range(4) if p[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------- reference arm ---
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from indexer_selected_sparse_score_gb300 import workloads as wl
+    oracle.build()
+    threads = os.cpu_count() or 1
+    oracle.set_threads(threads)
+    w = wl.generate(wl.CONFIGS[args.workload])
+    p = oracle.Problem(**w.problem_fields())
+    # size each step's sample so that the whole run stays within ~150 s
+    t0 = time.perf_counter()
+    oracle.fused(p, w.K, rows=[0])
+    one = time.perf_counter() - t0
+    per_step_budget = 150.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(w.T, math.floor(per_step_budget * threads / max(one, 1e-6)))))
+    cursor = 0
+
+    def step():
+        nonlocal cursor
+        rows = [(cursor + i) % w.T for i in range(n)]
+        cursor = (cursor + n) % w.T
+        oracle.fused(p, w.K, rows=rows)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = n * args.steps / el
+    sample = f"{n} of the {w.T} query tokens per step (rotating), float64 oracle, {threads} threads"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": f"{w.spec.name}: {w.spec.description}",
+                                          "global_batch": n, "seed": w.seed},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+# ---------------------------------------------------------------- our arm ---
+
+def cpu_baseline(w, seconds):
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    oracle.set_threads(threads)
+    p = oracle.Problem(**w.problem_fields())
+    t0 = time.perf_counter()
+    oracle.fused(p, w.K, rows=[0])
+    one = time.perf_counter() - t0
+    n = int(max(1, min(w.T, math.floor(seconds * threads / max(one, 1e-6)))))
+    rows = list(range(n))
+    t0 = time.perf_counter()
+    oracle.fused(p, w.K, rows=rows)
+    el = time.perf_counter() - t0
+    return {"value": n / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"query tokens 0..{n - 1} of the {w.T}-token batch (same seeded workload), "
+                      f"float64 oracle, one OpenMP thread per host core, {el:.1f} s"}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    from indexer_selected_sparse_score_gb300 import binding, build
+    from indexer_selected_sparse_score_gb300 import workloads as wl
+
+    if local_rank == 0:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    binding.load()
+
+    spec = wl.CONFIGS[args.workload]
+    w = wl.generate(spec, seed=wl.SEEDS[spec.name] + 1000 * rank)
+    copies = [binding.upload(w, device="cuda") for _ in range(max(1, args.copies))]
+    K = w.K
+    ws = binding.new_workspace(copies[0])
+    out = torch.empty((w.T, w.H, w.D), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((w.T, max(K, 1)), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    launches_per_step = binding.sa_fused_decode_launch_count(copies[0].ia, copies[0].aa, K)
+
+    def step(i):
+        dp = copies[i % len(copies)]
+        binding.sa_fused_decode(dp.ia, dp.aa, K, idx, out, ws, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if binding.sa_check_device_status(ws) != binding.SA_OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    t_soak = time.time()
+    i = 0
+    while time.time() - t_soak < args.soak_seconds:  # same steps, untimed, to read clocks under load
+        step(i)
+        i += 1
+        if i % 16 == 0:
+            torch.cuda.synchronize()
+    # ---- timed region: exactly K steps
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_end = time.time()
+    sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_per_step = ms / args.steps
+    value = w.T * world * args.steps / (ms / 1000.0)
+
+    # ---- per-stage device time, same launches with events between stages
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for row in evs:
+        for e in row:
+            e.record(stream)  # materialise the CUDA event handles
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        dp = copies[i % len(copies)]
+        binding.sa_fused_decode_staged(dp.ia, dp.aa, K, idx, out, ws, [e.cuda_event for e in evs[i]], stream)
+    torch.cuda.synchronize()
+    stage_ms = {s: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)) / args.steps
+                for j, s in enumerate(STAGES)}
+    if binding.sa_check_device_status(ws) != binding.SA_OK:
+        raise RuntimeError("device status not OK after the timed steps")
+
+    # ---- end to end through the C ABI with host buffers
+    names = ("q_seq", "q_pos", "q_I", "q_scale", "w", "Q")
+    host = {n: getattr(w, n) for n in names if getattr(w, n) is not None}
+    pinned = {n: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
+              for n, a in host.items()}
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    idx_h = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
+    d2h = out_h.numel() * out_h.element_size() + idx_h.numel() * idx_h.element_size()
+
+    def e2e_step(i):
+        dp = copies[i % len(copies)]
+        for n, t in pinned.items():
+            dp.tensors[n].copy_(t, non_blocking=True)
+        binding.sa_fused_decode(dp.ia, dp.aa, K, idx, out, ws, stream)
+        out_h.copy_(out, non_blocking=True)
+        idx_h.copy_(idx, non_blocking=True)
+
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = w.T * world * args.steps / (e2e_ms / 1000.0)
+
+    # ---- roofline of the dominant kernel
+    nbytes = algorithmic_bytes(w)
+    peak, peak_src = peaks()
+    dom = max(STAGES, key=lambda s: stage_ms[s])
+    achieved = nbytes[dom] / (stage_ms[dom] / 1000.0) / 1e9
+    traffic = recorded_traffic(dom, spec.name)
+    stages = {s: {"ms": round(stage_ms[s], 5), "algorithmic_bytes": nbytes[s],
+                  "GB_s": round(nbytes[s] / (stage_ms[s] / 1000.0) / 1e9, 1) if stage_ms[s] > 0 else None}
+              for s in STAGES}
+    step_frac = nbytes["step"] / (ms_per_step / 1000.0) / 1e9 / peak
+
+    clocks = sampler.summary(t_soak, t_end)
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8/bf16 in, fp32 accumulate",
+        "data": "synthetic (seeded, shapes and distributions of the workload)",
+        "config": {"workload": f"{spec.name}: {spec.description}", "global_batch": w.T * world,
+                   "per_gpu_batch": w.T, "seed": w.seed,
+                   "l2": f"{len(copies)} rotating input copies; each step's {nbytes['step'] / 1e6:.1f} MB "
+                         f"is evicted by the others (L2 129 MB)",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_roofline": {"step_bytes": nbytes["step"], "frac_of_peak": round(step_frac, 4),
+                         "frac_of_8TBps": round(nbytes["step"] / (ms_per_step / 1000.0) / 8e12, 4)},
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else peak_src,
+                     "algorithmic_bytes_per_launch": nbytes[dom]},
+        "stages": stages,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "per-step query inputs copied from pinned host memory, index/KV caches resident"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,190 @@
+/*
+ * sa.h -- C ABI of the GB300 (sm_103a) sparse attention step:
+ *
+ *   index scores  ->  per-query top-k  ->  windowed + sparse MQA  (+ split-KV combine)
+ *
+ * The step is the one of "DeepSeek-V4.1-Flash-NVFP4 inference/model.py"
+ * (Indexer.forward, get_window_topk_idxs, Attention._window_kv,
+ * Attention.forward) with the fp8 index keys and per-position key scales of
+ * "DeepSeek-V3.2-Exp inference/model.py" (Indexer.forward, fp8_index).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Notation: B sequences, T query tokens, token t belongs to sequence
+ * q_seq[t] and sits at absolute position q_pos[t].  Compressed entry j of a
+ * sequence stands for its tokens [j*r, (j+1)*r); token t can see the entries
+ * j < n_vis(t) = floor((q_pos[t] + 1) / r) (Indexer.forward, "compress_lens").
+ * Its raw window is the positions max(0, p-W+1) .. p, its own token included
+ * (Attention._window_kv writes the token before attending), stored in a ring
+ * of R slots per sequence at slot = position mod R.
+ *
+ * Memory: every pointer argument except the argument structs themselves is a
+ * DEVICE pointer owned by the caller, 16-byte aligned, holding a dense
+ * row-major array of the stated shape.  The library never allocates or frees
+ * device memory: scratch comes from a caller workspace of
+ * sa_workspace_size() bytes, which must be zero-filled once before its first
+ * use (sa_workspace_init).  All work is enqueued on the caller's stream; no
+ * call synchronises except sa_check_device_status.  Calls that share a
+ * workspace must not run concurrently.
+ *
+ * Errors: arguments are checked on the host before anything is enqueued; a
+ * bad argument returns an error and enqueues nothing.  sa_last_error_detail()
+ * gives a one-line reason for the last error of the calling thread.  Values
+ * that only the device sees (q_seq out of range, a position whose n_vis
+ * exceeds N_c, an index >= n_vis) are never dereferenced: the kernels skip
+ * them and set a sticky flag in the workspace, which sa_check_device_status
+ * reports (SA_ERR_DEVICE_DATA) and clears.  No kernel traps or spins without
+ * a bound.
+ */
+#ifndef SA_H
+#define SA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SA_API __attribute__((visibility("default")))
+#else
+#define SA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream); NULL is the legacy default stream. */
+typedef struct CUstream_st *sa_stream_t;
+
+typedef enum {
+  SA_OK = 0,
+  SA_ERR_INVALID_ARG = 1, /* null, negative, misaligned, or inconsistent argument */
+  SA_ERR_UNSUPPORTED = 2, /* a shape or dtype combination outside the compiled kernels */
+  SA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than sa_workspace_size() */
+  SA_ERR_CUDA = 4,        /* a CUDA launch or runtime call failed */
+  SA_ERR_TIMEOUT = 5,     /* a bounded device wait gave up (reported by sa_check_device_status) */
+  SA_ERR_DEVICE_DATA = 6  /* device-resident data was out of range and skipped */
+} sa_status;
+
+typedef enum { SA_BF16 = 0, SA_FP8_E4M3 = 1 } sa_dtype;
+
+/* Indexer inputs ("DeepSeek-V3.2-Exp inference/model.py", Indexer.forward:
+ * fp8 q with a per-(token, head) scale, fp8 k_cache with a per-position
+ * fp32 k_scale_cache; "DeepSeek-V4.1-Flash-NVFP4 inference/model.py",
+ * Indexer.forward: bf16-valued q and k). */
+typedef struct {
+  int32_t B, T;        /* sequences, query tokens (T >= 0, B >= 1) */
+  int32_t H_I, D_I;    /* index heads (1..128), index head dim (64 or 128) */
+  int32_t N_c;         /* compressed rows stored per sequence (>= 1) */
+  int32_t r;           /* compression ratio (>= 1) */
+  const int32_t *q_seq; /* [T] sequence id of each token, in [0, B) */
+  const int32_t *q_pos; /* [T] absolute position of each token, >= 0 */
+  const void *q_I;     /* [T, H_I, D_I] index queries, bf16 or fp8-e4m3fn */
+  int32_t q_dtype;     /* sa_dtype of q_I */
+  const float *q_scale; /* [T, H_I] dequantisation scale of q_I (> 0), or NULL for 1 */
+  const float *w;      /* [T, H_I] head weights, used as given (callers fold
+                          softmax_scale * H_I^-0.5 and any q scale into them
+                          or pass q_scale) */
+  const void *k_I;     /* [B, N_c, D_I] index keys, bf16 or fp8-e4m3fn */
+  int32_t k_dtype;     /* sa_dtype of k_I */
+  const float *k_scale; /* [B, N_c] dequantisation scale of each key row (> 0), or NULL for 1 */
+} sa_index_args;
+
+/* Attention inputs: one shared KV head across H query heads
+ * ("DeepSeek-V4.1-Flash-NVFP4 inference/model.py", Attention.forward:
+ * sparse_attn(q, kv, attn_sink, topk_idxs, softmax_scale) over the window KV
+ * concatenated with the compressed KV). */
+typedef struct {
+  int32_t H, D;        /* query heads (H*D a multiple of 256, H <= 128), head dim (128) */
+  int32_t W;           /* window length (>= 1) */
+  int32_t R;           /* raw ring slots per sequence (>= W; a prefill chunk of n
+                          tokens needs R >= n + W - 1) */
+  const void *Q;       /* [T, H, D] bf16 queries */
+  const void *Kw;      /* [B, R, D] bf16 raw window keys, slot = position mod R */
+  const void *Vw;      /* [B, R, D] bf16 raw window values (may equal Kw) */
+  const void *Kc;      /* [B, N_c, D] bf16 compressed keys */
+  const void *Vc;      /* [B, N_c, D] bf16 compressed values (may equal Kc) */
+  const float *sink;   /* [H] per-head attention sink logit, or NULL for none */
+  float scale;         /* softmax scale applied to Q.K (e.g. D^-0.5) */
+} sa_attn_args;
+
+/* Bytes of workspace the calls below need for these shapes and this K
+ * (attn may be NULL for sa_indexer_scores / sa_topk alone).  Returns 0 when
+ * the arguments are invalid. */
+SA_API size_t sa_workspace_size(const sa_index_args *ia, const sa_attn_args *aa, int32_t K);
+
+/* Zero-fills the workspace header (the sticky device status word).  Call it
+ * once on a new workspace.  Enqueued on `stream`. */
+SA_API sa_status sa_workspace_init(void *ws, size_t ws_bytes, sa_stream_t stream);
+
+/* Index scores ("DeepSeek-V4.1-Flash-NVFP4 inference/model.py",
+ * Indexer.forward: einsum over the head dim, ReLU, times weights, sum over
+ * index heads; "DeepSeek-V3.2-Exp inference/model.py", fp8_index):
+ *
+ *   scores[t, s] = sum_h w[t,h] * ReLU( sum_d q[t,h,d] q_scale[t,h] * k[b,s,d] k_scale[b,s] )
+ *
+ * for s < n_vis(t) (b = q_seq[t]) and -inf for n_vis(t) <= s < N_c.
+ * scores: [T, N_c] fp32, device, written in full.  Arithmetic: the products
+ * are exact in fp32 and accumulated in fp32. */
+SA_API sa_status sa_indexer_scores(const sa_index_args *ia, float *scores, void *ws, size_t ws_bytes,
+                            sa_stream_t stream);
+
+/* Per-query top-k ("DeepSeek-V4.1-Flash-NVFP4 inference/model.py",
+ * Indexer.forward: topk = min(index_topk, n_vis); the picks re-sorted into
+ * position order; unreachable picks are -1).  For each token t keeps
+ * K_eff = min(K, n_vis(t)) positions s < n_vis(t) with the highest
+ * scores[t, s] (ties: the lower position wins) and writes them in ascending
+ * order to idx[t, 0 .. K_eff), then -1 to idx[t, K_eff .. K).
+ * scores: [T, N_c] fp32 (only s < n_vis(t) is read); idx: [T, K] int32.
+ * K may be 0.  The selection is exact on the fp32 values (no tolerance). */
+SA_API sa_status sa_topk(const float *scores, const sa_index_args *ia, int32_t K, int32_t *idx, void *ws,
+                  size_t ws_bytes, sa_stream_t stream);
+
+/* Sparse MQA over the window and the selected compressed rows
+ * ("DeepSeek-V4.1-Flash-NVFP4 inference/model.py", Attention.forward and
+ * sparse_attn): for token t and head h the keys are the window rows then the
+ * compressed rows idx[t, k] != -1 (concatenated, not de-duplicated);
+ * l_j = scale * Q[t,h] . K_j; out[t,h] = sum_j softmax(l)_j V_j, where the
+ * softmax denominator also holds exp(sink[h]) when sink is given.
+ * idx: [T, K] int32, each entry -1 or in [0, n_vis(t)); out: [T, H, D] bf16
+ * (round to nearest even).  Only ia->B, T, N_c, r, q_seq and q_pos are read
+ * from ia. */
+SA_API sa_status sa_sparse_attn(const sa_index_args *ia, const sa_attn_args *aa, const int32_t *idx,
+                         int32_t K, void *out, void *ws, size_t ws_bytes, sa_stream_t stream);
+
+/* The whole step in one call, no host synchronisation: index scores into the
+ * workspace, top-k, sparse MQA with the split-KV combine.  idx_out: [T, K]
+ * int32 or NULL (then the indices stay in the workspace); out: [T, H, D]
+ * bf16.  Serves decode (one token per sequence) and prefill chunks alike. */
+SA_API sa_status sa_fused_decode(const sa_index_args *ia, const sa_attn_args *aa, int32_t K,
+                          int32_t *idx_out, void *out, void *ws, size_t ws_bytes,
+                          sa_stream_t stream);
+
+/* sa_fused_decode with timing marks: the same launches on the same stream,
+ * with the caller's CUDA events (cudaEvent_t handles) recorded on `stream`
+ * before the index-score kernel, before the top-k kernel, before the
+ * attention kernel(s) and after the last kernel: stage_events[0..3].  For
+ * measuring each stage's device time inside a timed loop. */
+SA_API sa_status sa_fused_decode_staged(const sa_index_args *ia, const sa_attn_args *aa, int32_t K,
+                                        int32_t *idx_out, void *out, void *ws, size_t ws_bytes,
+                                        sa_stream_t stream, void *const *stage_events);
+
+/* Number of kernel launches one sa_fused_decode call makes for these shapes
+ * (0 when the arguments are invalid). */
+SA_API int32_t sa_fused_decode_launch_count(const sa_index_args *ia, const sa_attn_args *aa,
+                                            int32_t K);
+
+/* Synchronises `stream`, then reads and clears the workspace's sticky device
+ * status: SA_OK, SA_ERR_DEVICE_DATA (out-of-range device data was skipped)
+ * or SA_ERR_TIMEOUT. */
+SA_API sa_status sa_check_device_status(void *ws, sa_stream_t stream);
+
+/* Text for a status code (static storage). */
+SA_API const char *sa_status_string(sa_status s);
+
+/* One-line reason for the calling thread's most recent non-OK return. */
+SA_API const char *sa_last_error_detail(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SA_H */

@@ -1,0 +1,217 @@
+"""ctypes binding of libsa.so (include/sa.h), with the same entry-point names.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  Tensors are passed as raw device pointers (``tensor.data_ptr()``)
+and streams as ``torch.cuda.Stream.cuda_stream`` handles; torch provides device
+memory and streams, nothing else.  If libsa.so is missing the first call
+raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+import torch
+
+from .build import LIB
+
+SA_OK = 0
+SA_ERR_INVALID_ARG = 1
+SA_ERR_UNSUPPORTED = 2
+SA_ERR_WORKSPACE = 3
+SA_ERR_CUDA = 4
+SA_ERR_TIMEOUT = 5
+SA_ERR_DEVICE_DATA = 6
+
+SA_BF16 = 0
+SA_FP8_E4M3 = 1
+
+
+class SAError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"sa status {status}: {detail}")
+        self.status = status
+        self.detail = detail
+
+
+class IndexArgs(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("T", ctypes.c_int32), ("H_I", ctypes.c_int32), ("D_I", ctypes.c_int32),
+        ("N_c", ctypes.c_int32), ("r", ctypes.c_int32),
+        ("q_seq", ctypes.c_void_p), ("q_pos", ctypes.c_void_p),
+        ("q_I", ctypes.c_void_p), ("q_dtype", ctypes.c_int32), ("q_scale", ctypes.c_void_p),
+        ("w", ctypes.c_void_p),
+        ("k_I", ctypes.c_void_p), ("k_dtype", ctypes.c_int32), ("k_scale", ctypes.c_void_p),
+    ]
+
+
+class AttnArgs(ctypes.Structure):
+    _fields_ = [
+        ("H", ctypes.c_int32), ("D", ctypes.c_int32), ("W", ctypes.c_int32), ("R", ctypes.c_int32),
+        ("Q", ctypes.c_void_p), ("Kw", ctypes.c_void_p), ("Vw", ctypes.c_void_p),
+        ("Kc", ctypes.c_void_p), ("Vc", ctypes.c_void_p),
+        ("sink", ctypes.c_void_p), ("scale", ctypes.c_float),
+    ]
+
+
+EXPORTED = ("sa_workspace_size", "sa_workspace_init", "sa_indexer_scores", "sa_topk",
+            "sa_sparse_attn", "sa_fused_decode", "sa_fused_decode_staged",
+            "sa_fused_decode_launch_count", "sa_check_device_status", "sa_status_string",
+            "sa_last_error_detail")
+
+_LIB = None
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libsa.so (built by ``build.build()``); raises if it is absent."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    path = path or LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run indexer_selected_sparse_score_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    IA, AA = ctypes.POINTER(IndexArgs), ctypes.POINTER(AttnArgs)
+    lib.sa_workspace_size.argtypes = [IA, AA, i32]
+    lib.sa_workspace_size.restype = sz
+    lib.sa_workspace_init.argtypes = [vp, sz, vp]
+    lib.sa_indexer_scores.argtypes = [IA, vp, vp, sz, vp]
+    lib.sa_topk.argtypes = [vp, IA, i32, vp, vp, sz, vp]
+    lib.sa_sparse_attn.argtypes = [IA, AA, vp, i32, vp, vp, sz, vp]
+    lib.sa_fused_decode.argtypes = [IA, AA, i32, vp, vp, vp, sz, vp]
+    lib.sa_fused_decode_staged.argtypes = [IA, AA, i32, vp, vp, vp, sz, vp, ctypes.POINTER(vp)]
+    lib.sa_fused_decode_launch_count.argtypes = [IA, AA, i32]
+    lib.sa_fused_decode_launch_count.restype = i32
+    lib.sa_check_device_status.argtypes = [vp, vp]
+    lib.sa_status_string.argtypes = [i32]
+    lib.sa_status_string.restype = ctypes.c_char_p
+    lib.sa_last_error_detail.restype = ctypes.c_char_p
+    for name in ("sa_workspace_init", "sa_indexer_scores", "sa_topk", "sa_sparse_attn",
+                 "sa_fused_decode", "sa_fused_decode_staged", "sa_check_device_status"):
+        getattr(lib, name).restype = i32
+    if path == LIB:
+        _LIB = lib
+    return lib
+
+
+def _p(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _s(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int) -> None:
+    if status != SA_OK:
+        raise SAError(status, load().sa_last_error_detail().decode())
+
+
+def _ws(ws):
+    return _p(ws), (ws.numel() * ws.element_size() if ws is not None else 0)
+
+
+# ----------------------------------------------------------- entry points ---
+
+def sa_workspace_size(ia: IndexArgs, aa: Optional[AttnArgs], K: int) -> int:
+    return int(load().sa_workspace_size(ctypes.byref(ia), ctypes.byref(aa) if aa is not None else None, K))
+
+
+def sa_workspace_init(ws, stream=None) -> None:
+    p, n = _ws(ws)
+    _check(load().sa_workspace_init(p, n, _s(stream)))
+
+
+def sa_indexer_scores(ia: IndexArgs, scores, ws, stream=None) -> None:
+    p, n = _ws(ws)
+    _check(load().sa_indexer_scores(ctypes.byref(ia), _p(scores), p, n, _s(stream)))
+
+
+def sa_topk(scores, ia: IndexArgs, K: int, idx, ws, stream=None) -> None:
+    p, n = _ws(ws)
+    _check(load().sa_topk(_p(scores), ctypes.byref(ia), K, _p(idx), p, n, _s(stream)))
+
+
+def sa_sparse_attn(ia: IndexArgs, aa: AttnArgs, idx, K: int, out, ws, stream=None) -> None:
+    p, n = _ws(ws)
+    _check(load().sa_sparse_attn(ctypes.byref(ia), ctypes.byref(aa), _p(idx), K, _p(out), p, n, _s(stream)))
+
+
+def sa_fused_decode(ia: IndexArgs, aa: AttnArgs, K: int, idx_out, out, ws, stream=None) -> None:
+    p, n = _ws(ws)
+    _check(load().sa_fused_decode(ctypes.byref(ia), ctypes.byref(aa), K, _p(idx_out), _p(out), p, n,
+                                  _s(stream)))
+
+
+def sa_fused_decode_staged(ia: IndexArgs, aa: AttnArgs, K: int, idx_out, out, ws, events,
+                           stream=None) -> None:
+    """``events``: four raw cudaEvent_t handles (ints) recorded between stages."""
+    p, n = _ws(ws)
+    arr = (ctypes.c_void_p * 4)(*events)
+    _check(load().sa_fused_decode_staged(ctypes.byref(ia), ctypes.byref(aa), K, _p(idx_out), _p(out),
+                                         p, n, _s(stream), arr))
+
+
+def sa_fused_decode_launch_count(ia: IndexArgs, aa: AttnArgs, K: int) -> int:
+    return int(load().sa_fused_decode_launch_count(ctypes.byref(ia), ctypes.byref(aa), K))
+
+
+def sa_check_device_status(ws, stream=None) -> int:
+    """Synchronise, read and clear the sticky device status; returns the sa status."""
+    return int(load().sa_check_device_status(_p(ws), _s(stream)))
+
+
+# ------------------------------------------------------ device marshalling ---
+
+def _dev(a: Optional[np.ndarray], device) -> Optional[torch.Tensor]:
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).to(device)
+
+
+@dataclass
+class DeviceProblem:
+    """Device copies of a workload's arrays plus the C argument structs."""
+    tensors: dict
+    ia: IndexArgs
+    aa: AttnArgs
+    K: int
+    T: int
+    H: int
+    D: int
+
+
+def upload(w, device="cuda", K: Optional[int] = None) -> DeviceProblem:
+    """Copy a workload (host numpy arrays in storage formats) to the device."""
+    names = ("q_seq", "q_pos", "q_I", "q_scale", "w", "k_I", "k_scale", "Q", "Kw", "Vw", "Kc", "Vc", "sink")
+    t = {n: _dev(getattr(w, n), device) for n in names}
+    ia = IndexArgs(w.B, w.T, w.H_I, w.D_I, w.N_c, w.r, _p(t["q_seq"]), _p(t["q_pos"]),
+                   _p(t["q_I"]), w.q_dtype, _p(t["q_scale"]), _p(t["w"]),
+                   _p(t["k_I"]), w.k_dtype, _p(t["k_scale"]))
+    aa = AttnArgs(w.H, w.D, w.W, w.R, _p(t["Q"]), _p(t["Kw"]), _p(t["Vw"]), _p(t["Kc"]), _p(t["Vc"]),
+                  _p(t["sink"]), float(w.scale))
+    return DeviceProblem(t, ia, aa, w.K if K is None else K, w.T, w.H, w.D)
+
+
+def new_workspace(dp: DeviceProblem, device="cuda", stream=None) -> torch.Tensor:
+    n = sa_workspace_size(dp.ia, dp.aa, dp.K)
+    if n == 0:
+        raise SAError(SA_ERR_INVALID_ARG, "workspace size query rejected the arguments")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    sa_workspace_init(ws, stream)
+    return ws

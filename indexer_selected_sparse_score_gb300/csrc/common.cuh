@@ -1,0 +1,74 @@
+// Device helpers shared by the kernels of the sparse attention step.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sa {
+
+// Sticky device status flags, OR-ed into the first word of the workspace.
+enum : uint32_t {
+  kFlagBadSeq = 1u,     // q_seq[t] outside [0, B)
+  kFlagBadPos = 2u,     // q_pos[t] < 0 or n_vis(t) > N_c
+  kFlagBadIndex = 4u,   // an index outside [-1, n_vis(t))
+  kFlagTimeout = 8u,    // a bounded wait gave up
+};
+
+__device__ __forceinline__ void raise_flag(uint32_t *status, uint32_t f) {
+  if (status) atomicOr(status, f);
+}
+
+// Visible compressed entries of a token at absolute position p: compressed
+// entry j covers tokens [j*r, (j+1)*r) and is visible once p >= (j+1)*r - 1.
+__device__ __forceinline__ int n_vis_of(int pos, int r) { return (pos + 1) / r; }
+
+// Validated (sequence, position, n_vis) of token t; returns false (and flags)
+// when the token must be skipped.
+struct Token {
+  int b, pos, nv;
+};
+
+__device__ __forceinline__ bool load_token(const int32_t *q_seq, const int32_t *q_pos, int t,
+                                           int B, int N_c, int r, uint32_t *status, Token &tk,
+                                           bool report) {
+  tk.b = q_seq[t];
+  tk.pos = q_pos[t];
+  if (tk.b < 0 || tk.b >= B) {
+    if (report) raise_flag(status, kFlagBadSeq);
+    return false;
+  }
+  if (tk.pos < 0) {
+    if (report) raise_flag(status, kFlagBadPos);
+    return false;
+  }
+  tk.nv = n_vis_of(tk.pos, r);
+  if (tk.nv > N_c) {
+    if (report) raise_flag(status, kFlagBadPos);
+    tk.nv = N_c;
+  }
+  return true;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ float e4m3_bits_to_float(uint8_t b) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(b), __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+// Order-preserving map of an fp32 score to uint32 (larger float -> larger
+// key); -0 is folded onto +0 so that the two compare equal, as they do in
+// floating point.
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace sa

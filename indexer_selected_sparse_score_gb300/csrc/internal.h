@@ -1,0 +1,42 @@
+// Host-side launchers behind the C ABI (one per kernel family).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sa.h"
+
+namespace sa {
+
+// Attention split-KV plan: each token's key list (window rows then its K
+// index slots) is cut into `splits` chunks of `split_keys` keys.
+struct SplitPlan {
+  int splits;
+  int split_keys;
+};
+SplitPlan plan_splits(int T, int W, int K);
+
+// Workspace carve-up (byte offsets, 256-byte aligned).
+struct WsLayout {
+  size_t status, scores, idx, part_m, part_l, part_o, total;
+};
+WsLayout ws_layout(const sa_index_args &ia, const sa_attn_args *aa, int K);
+
+cudaError_t launch_idx_score(const sa_index_args &ia, float *scores, int64_t ld,
+                             bool write_masked, uint32_t *status, cudaStream_t stream);
+
+cudaError_t launch_topk(const float *scores, int64_t ld, const sa_index_args &ia, int K,
+                        int32_t *idx, uint32_t *status, cudaStream_t stream);
+
+cudaError_t launch_sparse_mqa(const sa_index_args &ia, const sa_attn_args &aa, const int32_t *idx,
+                              int K, void *out, float *part_m, float *part_l, float *part_o,
+                              const SplitPlan &plan, uint32_t *status, cudaStream_t stream);
+
+// Kernel launches of one fused call (index score, top-k, attention, combine).
+int fused_launch_count(const sa_index_args &ia, const sa_attn_args &aa, int K,
+                       const SplitPlan &plan);
+
+bool attn_shape_supported(int H, int D);
+bool index_shape_supported(int H_I, int D_I);
+
+}  // namespace sa

@@ -1,0 +1,265 @@
+// The C ABI declared in include/sa.h: argument checks on the host, workspace
+// carve-up, and the launch sequence of each entry point.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+thread_local std::string g_detail;
+
+sa_status fail(sa_status s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+sa_status fail(sa_status s, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_detail = buf;
+  return s;
+}
+
+sa_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(SA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+size_t round_up(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+sa_status check_index(const sa_index_args *ia, bool need_index_inputs) {
+  if (!ia) return fail(SA_ERR_INVALID_ARG, "index args pointer is NULL");
+  if (ia->B < 1 || ia->T < 0 || ia->N_c < 1 || ia->r < 1)
+    return fail(SA_ERR_INVALID_ARG, "need B >= 1, T >= 0, N_c >= 1, r >= 1 (got B=%d T=%d N_c=%d r=%d)",
+                ia->B, ia->T, ia->N_c, ia->r);
+  if (ia->T > 0 && (!ia->q_seq || !ia->q_pos))
+    return fail(SA_ERR_INVALID_ARG, "q_seq and q_pos must be device pointers");
+  if (!aligned4(ia->q_seq) || !aligned4(ia->q_pos))
+    return fail(SA_ERR_INVALID_ARG, "q_seq / q_pos must be 4-byte aligned");
+  if (!need_index_inputs) return SA_OK;
+  if (ia->q_dtype != SA_BF16 && ia->q_dtype != SA_FP8_E4M3)
+    return fail(SA_ERR_INVALID_ARG, "q_dtype %d is not a sa_dtype", ia->q_dtype);
+  if (ia->k_dtype != SA_BF16 && ia->k_dtype != SA_FP8_E4M3)
+    return fail(SA_ERR_INVALID_ARG, "k_dtype %d is not a sa_dtype", ia->k_dtype);
+  if (!sa::index_shape_supported(ia->H_I, ia->D_I))
+    return fail(SA_ERR_UNSUPPORTED, "index heads %d x dim %d: need 1..128 heads of dim 64 or 128",
+                ia->H_I, ia->D_I);
+  if (ia->T > 0 && (!ia->q_I || !ia->w || !ia->k_I))
+    return fail(SA_ERR_INVALID_ARG, "q_I, w and k_I must be device pointers");
+  if (!aligned16(ia->q_I) || !aligned16(ia->k_I))
+    return fail(SA_ERR_INVALID_ARG, "q_I and k_I must be 16-byte aligned");
+  if (!aligned4(ia->w) || !aligned4(ia->q_scale) || !aligned4(ia->k_scale))
+    return fail(SA_ERR_INVALID_ARG, "w, q_scale and k_scale must be 4-byte aligned");
+  return SA_OK;
+}
+
+sa_status check_attn(const sa_attn_args *aa, int T) {
+  if (!aa) return fail(SA_ERR_INVALID_ARG, "attention args pointer is NULL");
+  if (!sa::attn_shape_supported(aa->H, aa->D))
+    return fail(SA_ERR_UNSUPPORTED, "attention %d heads x dim %d: need dim 128 and 16/32/64/128 heads",
+                aa->H, aa->D);
+  if (aa->W < 1 || aa->R < aa->W)
+    return fail(SA_ERR_INVALID_ARG, "need W >= 1 and R >= W (got W=%d R=%d)", aa->W, aa->R);
+  if (!std::isfinite(aa->scale)) return fail(SA_ERR_INVALID_ARG, "softmax scale is not finite");
+  if (T > 0 && (!aa->Q || !aa->Kw || !aa->Vw || !aa->Kc || !aa->Vc))
+    return fail(SA_ERR_INVALID_ARG, "Q, Kw, Vw, Kc, Vc must be device pointers");
+  if (!aligned16(aa->Q) || !aligned16(aa->Kw) || !aligned16(aa->Vw) || !aligned16(aa->Kc) ||
+      !aligned16(aa->Vc))
+    return fail(SA_ERR_INVALID_ARG, "Q, Kw, Vw, Kc, Vc must be 16-byte aligned");
+  if (!aligned4(aa->sink)) return fail(SA_ERR_INVALID_ARG, "sink must be 4-byte aligned");
+  return SA_OK;
+}
+
+sa_status check_ws(void *ws, size_t ws_bytes, size_t need) {
+  if (!ws) return fail(SA_ERR_WORKSPACE, "workspace pointer is NULL");
+  if (!aligned16(ws)) return fail(SA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  if (ws_bytes < need)
+    return fail(SA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  return SA_OK;
+}
+
+template <typename T>
+T *at(void *ws, size_t off) {
+  return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
+}  // namespace
+
+namespace sa {
+
+WsLayout ws_layout(const sa_index_args &ia, const sa_attn_args *aa, int K) {
+  WsLayout L{};
+  size_t off = 0;
+  L.status = off;
+  off += 256;
+  L.scores = off;
+  off += round_up(sizeof(float) * static_cast<size_t>(ia.T) * ia.N_c);
+  L.idx = off;
+  off += round_up(sizeof(int32_t) * static_cast<size_t>(ia.T) * (K > 0 ? K : 0));
+  L.part_m = L.part_l = L.part_o = off;
+  if (aa) {
+    const SplitPlan plan = plan_splits(ia.T, aa->W, K);
+    const size_t th = static_cast<size_t>(ia.T) * aa->H * plan.splits;
+    L.part_m = off;
+    off += round_up(sizeof(float) * th);
+    L.part_l = off;
+    off += round_up(sizeof(float) * th);
+    L.part_o = off;
+    off += round_up(sizeof(float) * th * aa->D);
+  }
+  L.total = off;
+  return L;
+}
+
+}  // namespace sa
+
+extern "C" {
+
+size_t sa_workspace_size(const sa_index_args *ia, const sa_attn_args *aa, int32_t K) {
+  if (check_index(ia, false) != SA_OK || K < 0) return 0;
+  if (aa && check_attn(aa, 0) != SA_OK) return 0;
+  return sa::ws_layout(*ia, aa, K).total;
+}
+
+sa_status sa_workspace_init(void *ws, size_t ws_bytes, sa_stream_t stream) {
+  if (sa_status s = check_ws(ws, ws_bytes, 256)) return s;
+  cudaError_t e = cudaMemsetAsync(ws, 0, 256, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SA_OK : cuda_fail(e, "cudaMemsetAsync");
+}
+
+sa_status sa_indexer_scores(const sa_index_args *ia, float *scores, void *ws, size_t ws_bytes,
+                            sa_stream_t stream) {
+  if (sa_status s = check_index(ia, true)) return s;
+  if (ia->T > 0 && !scores) return fail(SA_ERR_INVALID_ARG, "scores must be a device pointer");
+  if (!aligned4(scores)) return fail(SA_ERR_INVALID_ARG, "scores must be 4-byte aligned");
+  if (sa_status s = check_ws(ws, ws_bytes, 256)) return s;
+  cudaError_t e = sa::launch_idx_score(*ia, scores, ia->N_c, true, at<uint32_t>(ws, 0),
+                                       reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SA_OK : cuda_fail(e, "index score launch");
+}
+
+sa_status sa_topk(const float *scores, const sa_index_args *ia, int32_t K, int32_t *idx, void *ws,
+                  size_t ws_bytes, sa_stream_t stream) {
+  if (sa_status s = check_index(ia, false)) return s;
+  if (K < 0) return fail(SA_ERR_INVALID_ARG, "K must be >= 0 (got %d)", K);
+  if (ia->T > 0 && K > 0 && (!scores || !idx))
+    return fail(SA_ERR_INVALID_ARG, "scores and idx must be device pointers");
+  if (!aligned4(scores) || !aligned4(idx))
+    return fail(SA_ERR_INVALID_ARG, "scores and idx must be 4-byte aligned");
+  if (sa_status s = check_ws(ws, ws_bytes, 256)) return s;
+  cudaError_t e = sa::launch_topk(scores, ia->N_c, *ia, K, idx, at<uint32_t>(ws, 0),
+                                  reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SA_OK : cuda_fail(e, "top-k launch");
+}
+
+sa_status sa_sparse_attn(const sa_index_args *ia, const sa_attn_args *aa, const int32_t *idx,
+                         int32_t K, void *out, void *ws, size_t ws_bytes, sa_stream_t stream) {
+  if (sa_status s = check_index(ia, false)) return s;
+  if (sa_status s = check_attn(aa, ia->T)) return s;
+  if (K < 0) return fail(SA_ERR_INVALID_ARG, "K must be >= 0 (got %d)", K);
+  if (ia->T > 0 && (!out || (K > 0 && !idx)))
+    return fail(SA_ERR_INVALID_ARG, "out and idx must be device pointers");
+  if (!aligned4(idx) || !aligned16(out))
+    return fail(SA_ERR_INVALID_ARG, "idx must be 4-byte and out 16-byte aligned");
+  const sa::WsLayout L = sa::ws_layout(*ia, aa, K);
+  if (sa_status s = check_ws(ws, ws_bytes, L.total)) return s;
+  const sa::SplitPlan plan = sa::plan_splits(ia->T, aa->W, K);
+  cudaError_t e = sa::launch_sparse_mqa(*ia, *aa, idx, K, out, at<float>(ws, L.part_m),
+                                        at<float>(ws, L.part_l), at<float>(ws, L.part_o), plan,
+                                        at<uint32_t>(ws, 0), reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SA_OK : cuda_fail(e, "sparse attention launch");
+}
+
+static sa_status fused_impl(const sa_index_args *ia, const sa_attn_args *aa, int32_t K,
+                            int32_t *idx_out, void *out, void *ws, size_t ws_bytes,
+                            sa_stream_t stream, void *const *ev) {
+  if (sa_status s = check_index(ia, true)) return s;
+  if (sa_status s = check_attn(aa, ia->T)) return s;
+  if (K < 0) return fail(SA_ERR_INVALID_ARG, "K must be >= 0 (got %d)", K);
+  if (ia->T > 0 && !out) return fail(SA_ERR_INVALID_ARG, "out must be a device pointer");
+  if (!aligned4(idx_out) || !aligned16(out))
+    return fail(SA_ERR_INVALID_ARG, "idx_out must be 4-byte and out 16-byte aligned");
+  const sa::WsLayout L = sa::ws_layout(*ia, aa, K);
+  if (sa_status s = check_ws(ws, ws_bytes, L.total)) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  auto mark = [&](int i) -> cudaError_t {
+    return ev ? cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st) : cudaSuccess;
+  };
+  uint32_t *status = at<uint32_t>(ws, 0);
+  float *scores = at<float>(ws, L.scores);
+  int32_t *idx = idx_out ? idx_out : at<int32_t>(ws, L.idx);
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess) e = sa::launch_idx_score(*ia, scores, ia->N_c, false, status, st);
+  if (e != cudaSuccess) return cuda_fail(e, "index score launch");
+  e = mark(1);
+  if (e == cudaSuccess) e = sa::launch_topk(scores, ia->N_c, *ia, K, idx, status, st);
+  if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+  const sa::SplitPlan plan = sa::plan_splits(ia->T, aa->W, K);
+  e = mark(2);
+  if (e == cudaSuccess)
+    e = sa::launch_sparse_mqa(*ia, *aa, idx, K, out, at<float>(ws, L.part_m), at<float>(ws, L.part_l),
+                              at<float>(ws, L.part_o), plan, status, st);
+  if (e == cudaSuccess) e = mark(3);
+  return e == cudaSuccess ? SA_OK : cuda_fail(e, "sparse attention launch");
+}
+
+sa_status sa_fused_decode(const sa_index_args *ia, const sa_attn_args *aa, int32_t K,
+                          int32_t *idx_out, void *out, void *ws, size_t ws_bytes,
+                          sa_stream_t stream) {
+  return fused_impl(ia, aa, K, idx_out, out, ws, ws_bytes, stream, nullptr);
+}
+
+sa_status sa_fused_decode_staged(const sa_index_args *ia, const sa_attn_args *aa, int32_t K,
+                                 int32_t *idx_out, void *out, void *ws, size_t ws_bytes,
+                                 sa_stream_t stream, void *const *stage_events) {
+  if (!stage_events) return fail(SA_ERR_INVALID_ARG, "stage_events is NULL");
+  for (int i = 0; i < 4; ++i)
+    if (!stage_events[i]) return fail(SA_ERR_INVALID_ARG, "stage event %d is NULL", i);
+  return fused_impl(ia, aa, K, idx_out, out, ws, ws_bytes, stream, stage_events);
+}
+
+int32_t sa_fused_decode_launch_count(const sa_index_args *ia, const sa_attn_args *aa, int32_t K) {
+  if (check_index(ia, true) != SA_OK || check_attn(aa, 0) != SA_OK || K < 0) return 0;
+  if (ia->T == 0) return 0;
+  const sa::SplitPlan plan = sa::plan_splits(ia->T, aa->W, K);
+  return sa::fused_launch_count(*ia, *aa, K, plan);
+}
+
+sa_status sa_check_device_status(void *ws, sa_stream_t stream) {
+  if (!ws) return fail(SA_ERR_WORKSPACE, "workspace pointer is NULL");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  uint32_t flags = 0;
+  e = cudaMemcpy(&flags, ws, sizeof(flags), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy (status word)");
+  if (flags == 0) return SA_OK;
+  e = cudaMemset(ws, 0, sizeof(flags));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemset (status word)");
+  if (flags & sa::kFlagTimeout) return fail(SA_ERR_TIMEOUT, "a bounded device wait gave up (flags 0x%x)", flags);
+  return fail(SA_ERR_DEVICE_DATA, "device data out of range was skipped (flags 0x%x:%s%s%s)", flags,
+              (flags & sa::kFlagBadSeq) ? " q_seq" : "", (flags & sa::kFlagBadPos) ? " q_pos" : "",
+              (flags & sa::kFlagBadIndex) ? " idx" : "");
+}
+
+const char *sa_status_string(sa_status s) {
+  switch (s) {
+    case SA_OK: return "ok";
+    case SA_ERR_INVALID_ARG: return "invalid argument";
+    case SA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case SA_ERR_WORKSPACE: return "workspace missing or too small";
+    case SA_ERR_CUDA: return "CUDA error";
+    case SA_ERR_TIMEOUT: return "bounded device wait timed out";
+    case SA_ERR_DEVICE_DATA: return "out-of-range device data skipped";
+  }
+  return "unknown status";
+}
+
+const char *sa_last_error_detail(void) { return g_detail.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,314 @@
+// Sparse MQA over the raw window plus the selected compressed rows, with a
+// split-KV combine ("DeepSeek-V4.1-Flash-NVFP4 inference/model.py",
+// Attention.forward: kv = cat(window_kv, compress_kv), topk_idxs =
+// cat(window_idxs, compress_idxs + offset), sparse_attn(q, kv, attn_sink,
+// topk_idxs, softmax_scale); one shared KV head serves every query head).
+//
+// CUDA-core kernel: one CTA per (token, split).  The token's key list is its
+// window rows (oldest first) followed by its K index slots; a split takes a
+// contiguous chunk of that list.  Rows are gathered 16 bytes per thread,
+// logits and the online softmax run in fp32 in the log2 domain (logits are
+// pre-multiplied by scale * log2(e)), and each split leaves (m, l, o) partials
+// that the combine kernel merges.  A single split writes the output directly.
+#include "common.cuh"
+#include "internal.h"
+
+namespace sa {
+namespace {
+
+constexpr int kAttnThreads = 256;
+constexpr int kKeyTile = 32;
+
+struct AttnParams {
+  int B, T, N_c, r;
+  const int32_t *q_seq, *q_pos;
+  int W, R;
+  const uint16_t *Q, *Kw, *Vw, *Kc, *Vc;
+  const float *sink;
+  float qk_scale;  // scale * log2(e)
+  const int32_t *idx;
+  int K;
+  int splits, split_keys;
+  float *part_m, *part_l, *part_o;
+  __nv_bfloat16 *out;
+  uint32_t *status;
+};
+
+template <int H, int D>
+constexpr size_t attn_smem_bytes() {
+  return sizeof(float) * (static_cast<size_t>(H) * (D + 1) + kKeyTile * (D + 1) + kKeyTile * D +
+                          H * (kKeyTile + 1) + 3 * H) +
+         sizeof(int) * 2 * kKeyTile;
+}
+
+template <int H, int D>
+__global__ void __launch_bounds__(kAttnThreads) sparse_mqa_simt_kernel(AttnParams p) {
+  constexpr int NPT = H * D / kAttnThreads;
+  constexpr int DP = D + 1;
+  constexpr int PP = kKeyTile + 1;
+  static_assert(NPT * kAttnThreads == H * D, "H*D must be a multiple of the CTA size");
+  extern __shared__ float4 smem4[];
+  float *Qs = reinterpret_cast<float *>(smem4);  // [H][DP]
+  float *Ks = Qs + H * DP;                       // [kKeyTile][DP]
+  float *Vs = Ks + kKeyTile * DP;                // [kKeyTile][D]
+  float *Ps = Vs + kKeyTile * D;                 // [H][PP]
+  float *m_s = Ps + H * PP;
+  float *l_s = m_s + H;
+  float *c_s = l_s + H;
+  int *row_of = reinterpret_cast<int *>(c_s + H);  // [kKeyTile] row in its source, -1 = none
+  int *src_of = row_of + kKeyTile;                 // [kKeyTile] 0 = window ring, 1 = compressed
+
+  const int t = blockIdx.y, split = blockIdx.x, tid = threadIdx.x;
+  Token tk;
+  const bool ok = load_token(p.q_seq, p.q_pos, t, p.B, p.N_c, p.r, p.status, tk,
+                             split == 0 && tid == 0);
+  const int n_w = ok ? min(p.W, tk.pos + 1) : 0;
+  const int n_keys = ok ? n_w + p.K : 0;
+  const int k_begin = split * p.split_keys;
+  const int k_end = min(k_begin + p.split_keys, n_keys);
+
+  const int64_t qbase = static_cast<int64_t>(t) * H * D;
+  for (int i = tid; i < H * D; i += kAttnThreads)
+    Qs[(i / D) * DP + (i % D)] = bf16_bits_to_float(p.Q[qbase + i]) * p.qk_scale;
+  for (int h = tid; h < H; h += kAttnThreads) {
+    m_s[h] = -INFINITY;
+    l_s[h] = 0.f;
+  }
+  float acc[NPT];
+#pragma unroll
+  for (int e = 0; e < NPT; ++e) acc[e] = 0.f;
+  __syncthreads();
+
+  for (int tile = k_begin; tile < k_end; tile += kKeyTile) {
+    if (tid < kKeyTile) {
+      const int kk = tile + tid;
+      int row = -1, src = 0;
+      if (kk < k_end) {
+        if (kk < n_w) {
+          const int pos = tk.pos - n_w + 1 + kk;
+          row = tk.b * p.R + pos % p.R;
+        } else {
+          const int c = p.idx[static_cast<int64_t>(t) * p.K + (kk - n_w)];
+          if (c >= 0 && c < tk.nv) {
+            row = tk.b * p.N_c + c;
+            src = 1;
+          } else if (c != -1) {
+            raise_flag(p.status, kFlagBadIndex);
+          }
+        }
+      }
+      row_of[tid] = row;
+      src_of[tid] = src;
+    }
+    __syncthreads();
+    constexpr int CH = D / 8;  // 16-byte chunks per row
+    for (int i = tid; i < kKeyTile * CH; i += kAttnThreads) {
+      const int j = i / CH, c = i % CH;
+      const int row = row_of[j];
+      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+      if (row >= 0) {
+        const uint16_t *kb = src_of[j] ? p.Kc : p.Kw;
+        const uint16_t *vb = src_of[j] ? p.Vc : p.Vw;
+        kv = __ldg(reinterpret_cast<const uint4 *>(kb + static_cast<int64_t>(row) * D) + c);
+        vv = __ldg(reinterpret_cast<const uint4 *>(vb + static_cast<int64_t>(row) * D) + c);
+      }
+      const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
+      const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        Ks[j * DP + 8 * c + 2 * e] = __uint_as_float(kw[e] << 16);
+        Ks[j * DP + 8 * c + 2 * e + 1] = __uint_as_float(kw[e] & 0xFFFF0000u);
+        Vs[j * D + 8 * c + 2 * e] = __uint_as_float(vw[e] << 16);
+        Vs[j * D + 8 * c + 2 * e + 1] = __uint_as_float(vw[e] & 0xFFFF0000u);
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < H * kKeyTile; i += kAttnThreads) {
+      const int h = i / kKeyTile, j = i % kKeyTile;
+      float v = -INFINITY;
+      if (row_of[j] >= 0) {
+        float dot = 0.f;
+        const float *qh = Qs + h * DP;
+        const float *kj = Ks + j * DP;
+#pragma unroll 16
+        for (int d = 0; d < D; ++d) dot = fmaf(qh[d], kj[d], dot);
+        v = dot;
+      }
+      Ps[h * PP + j] = v;
+    }
+    __syncthreads();
+    for (int h = tid; h < H; h += kAttnThreads) {
+      float mx = -INFINITY;
+      for (int j = 0; j < kKeyTile; ++j) mx = fmaxf(mx, Ps[h * PP + j]);
+      const float m_old = m_s[h];
+      const float m_new = fmaxf(m_old, mx);
+      float corr = 1.f, sum = 0.f;
+      if (m_new != -INFINITY) {
+        corr = exp2f(m_old - m_new);
+        for (int j = 0; j < kKeyTile; ++j) {
+          const float pj = exp2f(Ps[h * PP + j] - m_new);
+          Ps[h * PP + j] = pj;
+          sum += pj;
+        }
+      } else {
+        for (int j = 0; j < kKeyTile; ++j) Ps[h * PP + j] = 0.f;
+      }
+      l_s[h] = l_s[h] * corr + sum;
+      m_s[h] = m_new;
+      c_s[h] = corr;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < NPT; ++e) {
+      const int el = tid + e * kAttnThreads;
+      const int h = el / D, d = el % D;
+      float a = acc[e] * c_s[h];
+#pragma unroll 8
+      for (int j = 0; j < kKeyTile; ++j) a = fmaf(Ps[h * PP + j], Vs[j * D + d], a);
+      acc[e] = a;
+    }
+    __syncthreads();
+  }
+
+  if (p.splits == 1) {
+#pragma unroll
+    for (int e = 0; e < NPT; ++e) {
+      const int el = tid + e * kAttnThreads;
+      const int h = el / D;
+      const float m = m_s[h];
+      const float s2 = p.sink ? p.sink[h] * kLog2e : -INFINITY;
+      const float M = fmaxf(m, s2);
+      float o = 0.f;
+      if (M != -INFINITY) {
+        const float a = exp2f(m - M);
+        const float L = l_s[h] * a + (p.sink ? exp2f(s2 - M) : 0.f);
+        o = acc[e] * a / L;
+      }
+      p.out[qbase + el] = __float2bfloat16_rn(o);
+    }
+  } else {
+    for (int h = tid; h < H; h += kAttnThreads) {
+      const int64_t pi = (static_cast<int64_t>(t) * H + h) * p.splits + split;
+      p.part_m[pi] = m_s[h];
+      p.part_l[pi] = l_s[h];
+    }
+#pragma unroll
+    for (int e = 0; e < NPT; ++e) {
+      const int el = tid + e * kAttnThreads;
+      const int h = el / D, d = el % D;
+      const int64_t pi = (static_cast<int64_t>(t) * H + h) * p.splits + split;
+      p.part_o[pi * D + d] = acc[e];
+    }
+  }
+}
+
+// out[t,h,:] = sum_s 2^(m_s - M) o_s / (sum_s 2^(m_s - M) l_s + 2^(sink - M)),
+// M the largest of the m_s and the sink (all in the log2 domain).
+template <int D>
+__global__ void __launch_bounds__(D) combine_kernel(int H, int S, const float *__restrict__ part_m,
+                                                    const float *__restrict__ part_l,
+                                                    const float *__restrict__ part_o,
+                                                    const float *__restrict__ sink,
+                                                    __nv_bfloat16 *__restrict__ out) {
+  const int th = blockIdx.x;  // t * H + h
+  const int h = th % H, d = threadIdx.x;
+  const float *pm = part_m + static_cast<int64_t>(th) * S;
+  const float *pl = part_l + static_cast<int64_t>(th) * S;
+  const float *po = part_o + static_cast<int64_t>(th) * S * D;
+  const float s2 = sink ? sink[h] * kLog2e : -INFINITY;
+  float M = s2;
+  for (int s = 0; s < S; ++s) M = fmaxf(M, pm[s]);
+  float o = 0.f;
+  if (M != -INFINITY) {
+    float L = sink ? exp2f(s2 - M) : 0.f, acc = 0.f;
+    for (int s = 0; s < S; ++s) {
+      const float a = exp2f(pm[s] - M);  // 0 for an empty split (m = -inf)
+      L = fmaf(a, pl[s], L);
+      acc = fmaf(a, po[static_cast<int64_t>(s) * D + d], acc);
+    }
+    o = acc / L;
+  }
+  out[static_cast<int64_t>(th) * D + d] = __float2bfloat16_rn(o);
+}
+
+template <int H, int D>
+cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
+  auto kern = sparse_mqa_simt_kernel<H, D>;
+  constexpr size_t smem = attn_smem_bytes<H, D>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.splits, p.T);
+  kern<<<grid, kAttnThreads, smem, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.splits == 1) return e;
+  combine_kernel<D><<<p.T * H, D, 0, stream>>>(H, p.splits, p.part_m, p.part_l, p.part_o, p.sink,
+                                               p.out);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attn_shape_supported(int H, int D) {
+  return D == 128 && (H == 16 || H == 32 || H == 64 || H == 128);
+}
+
+int fused_launch_count(const sa_index_args &ia, const sa_attn_args &aa, int K,
+                       const SplitPlan &plan) {
+  (void)aa;
+  const int topk = K > 0 ? 1 : 0;
+  const int attn = plan.splits > 1 ? 2 : 1;
+  return ia.T > 0 ? 1 + topk + attn : 0;
+}
+
+SplitPlan plan_splits(int T, int W, int K) {
+  const int n_keys = W + K;
+  const int max_splits = (n_keys + kKeyTile - 1) / kKeyTile;
+  const int target_ctas = 2 * 152;
+  int splits = T > 0 ? (target_ctas + T - 1) / T : 1;
+  splits = splits < 1 ? 1 : (splits > max_splits ? max_splits : splits);
+  int split_keys = (n_keys + splits - 1) / splits;
+  split_keys = (split_keys + kKeyTile - 1) / kKeyTile * kKeyTile;
+  splits = (n_keys + split_keys - 1) / split_keys;
+  return SplitPlan{splits < 1 ? 1 : splits, split_keys < kKeyTile ? kKeyTile : split_keys};
+}
+
+cudaError_t launch_sparse_mqa(const sa_index_args &ia, const sa_attn_args &aa, const int32_t *idx,
+                              int K, void *out, float *part_m, float *part_l, float *part_o,
+                              const SplitPlan &plan, uint32_t *status, cudaStream_t stream) {
+  if (ia.T == 0) return cudaSuccess;
+  AttnParams p;
+  p.B = ia.B;
+  p.T = ia.T;
+  p.N_c = ia.N_c;
+  p.r = ia.r;
+  p.q_seq = ia.q_seq;
+  p.q_pos = ia.q_pos;
+  p.W = aa.W;
+  p.R = aa.R;
+  p.Q = static_cast<const uint16_t *>(aa.Q);
+  p.Kw = static_cast<const uint16_t *>(aa.Kw);
+  p.Vw = static_cast<const uint16_t *>(aa.Vw);
+  p.Kc = static_cast<const uint16_t *>(aa.Kc);
+  p.Vc = static_cast<const uint16_t *>(aa.Vc);
+  p.sink = aa.sink;
+  p.qk_scale = aa.scale * kLog2e;
+  p.idx = idx;
+  p.K = K;
+  p.splits = plan.splits;
+  p.split_keys = plan.split_keys;
+  p.part_m = part_m;
+  p.part_l = part_l;
+  p.part_o = part_o;
+  p.out = static_cast<__nv_bfloat16 *>(out);
+  p.status = status;
+  switch (aa.H) {
+    case 16: return launch_attn<16, 128>(p, stream);
+    case 32: return launch_attn<32, 128>(p, stream);
+    case 64: return launch_attn<64, 128>(p, stream);
+    case 128: return launch_attn<128, 128>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace sa

@@ -1,0 +1,103 @@
+"""The C ABI on the host (no GPU needed): the library builds and loads, it
+exports every entry point include/sa.h declares, argument checks return their
+error codes before anything touches a device, and the product package never
+reaches the oracle."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from indexer_selected_sparse_score_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_symbols():
+    names = []
+    for hdr in os.listdir(os.path.join(ROOT, "include")):
+        if hdr.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", hdr)).read()
+            names += re.findall(r"SA_API\s+[\w\s\*]+?\b(sa_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert "sa_fused_decode" in names and len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(binding.EXPORTED) <= set(names)
+
+
+def _ia(**kw):
+    base = dict(B=2, T=3, H_I=16, D_I=64, N_c=100, r=2, q_seq=16, q_pos=16, q_I=16, q_dtype=0,
+                q_scale=None, w=16, k_I=16, k_dtype=1, k_scale=16)
+    base.update(kw)
+    return binding.IndexArgs(*[base[f] for f, _ in binding.IndexArgs._fields_])
+
+
+def _aa(**kw):
+    base = dict(H=16, D=128, W=8, R=8, Q=16, Kw=16, Vw=16, Kc=16, Vc=16, sink=None, scale=0.088)
+    base.update(kw)
+    return binding.AttnArgs(*[base[f] for f, _ in binding.AttnArgs._fields_])
+
+
+def _call_fused(lib, ia, aa, K=8, ws=256, ws_bytes=1 << 20, out=256):
+    return lib.sa_fused_decode(ctypes.byref(ia) if ia is not None else None,
+                               ctypes.byref(aa) if aa is not None else None, K, None, out, ws,
+                               ws_bytes, None)
+
+
+def test_workspace_size(lib):
+    n = lib.sa_workspace_size(ctypes.byref(_ia()), ctypes.byref(_aa()), 8)
+    assert n > 256 and n % 256 == 0
+    assert lib.sa_workspace_size(ctypes.byref(_ia(B=0)), None, 8) == 0
+    assert lib.sa_workspace_size(ctypes.byref(_ia()), None, -1) == 0
+
+
+@pytest.mark.parametrize("ia,aa,K,status", [
+    (None, _aa(), 8, binding.SA_ERR_INVALID_ARG),
+    (_ia(T=-1), _aa(), 8, binding.SA_ERR_INVALID_ARG),
+    (_ia(r=0), _aa(), 8, binding.SA_ERR_INVALID_ARG),
+    (_ia(D_I=96), _aa(), 8, binding.SA_ERR_UNSUPPORTED),
+    (_ia(H_I=129), _aa(), 8, binding.SA_ERR_UNSUPPORTED),
+    (_ia(q_dtype=7), _aa(), 8, binding.SA_ERR_INVALID_ARG),
+    (_ia(k_I=24), _aa(), 8, binding.SA_ERR_INVALID_ARG),        # misaligned
+    (_ia(), _aa(H=24), 8, binding.SA_ERR_UNSUPPORTED),
+    (_ia(), _aa(D=64), 8, binding.SA_ERR_UNSUPPORTED),
+    (_ia(), _aa(R=4), 8, binding.SA_ERR_INVALID_ARG),           # R < W
+    (_ia(), _aa(scale=float("nan")), 8, binding.SA_ERR_INVALID_ARG),
+    (_ia(), _aa(Q=None), 8, binding.SA_ERR_INVALID_ARG),
+    (_ia(), _aa(), -1, binding.SA_ERR_INVALID_ARG),
+])
+def test_fused_rejects_bad_arguments(lib, ia, aa, K, status):
+    assert _call_fused(lib, ia, aa, K) == status
+    assert lib.sa_last_error_detail()
+
+
+def test_workspace_checks(lib):
+    assert _call_fused(lib, _ia(), _aa(), ws=None) == binding.SA_ERR_WORKSPACE
+    assert _call_fused(lib, _ia(), _aa(), ws_bytes=300) == binding.SA_ERR_WORKSPACE
+    assert _call_fused(lib, _ia(), _aa(), ws=264) == binding.SA_ERR_INVALID_ARG
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert lib.sa_status_string(s)
+
+
+def test_product_package_never_reaches_the_oracle():
+    pkg = os.path.join(ROOT, "indexer_selected_sparse_score_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "oracle.h" not in text and "liboracle" not in text, f

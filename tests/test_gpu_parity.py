@@ -1,0 +1,163 @@
+"""CUDA path vs the float64 oracle, element by element, on small seeded
+workloads that span several tiles and a ragged tail (GPU only)."""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_run import run_attn, run_fused, run_scores, run_topk
+from helpers import n_vis, problem
+from indexer_selected_sparse_score_gb300 import binding
+from indexer_selected_sparse_score_gb300 import workloads as wl
+from tolerances import check_attn, check_scores, check_topk_sets
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    # index 16 x 64 (V4.1 defaults), fp8 keys with scales, r=2
+    "i16x64_fp8k": wl.small("i16x64_fp8k"),
+    # bf16 keys, no scales (V4.1 bf16-valued keys)
+    "i16x64_bf16k": wl.small("i16x64_bf16k", k_dtype=wl.BF16, k_scale=False),
+    # index 64 x 128, fp8 keys, r=4, topk 100, attention 64 heads
+    "i64x128_fp8k": wl.small("i64x128_fp8k", H_I=64, D_I=128, r=4, N_c=700, K=100, H=64,
+                             pos_lo=900, pos_hi=2799, w_div=64.0),
+    # fp8 queries with per-token scale and fp8 keys (prefill-style dtypes)
+    "i64x128_fp8qk": wl.small("i64x128_fp8qk", H_I=64, D_I=128, r=4, N_c=700, K=100, H=64,
+                              q_dtype=wl.FP8_E4M3, q_scale=True, pos_lo=900, pos_hi=2799,
+                              w_div=64.0),
+    # r = 1 (no compression), one index head, sink present
+    "r1_h1_sink": wl.small("r1_h1_sink", r=1, N_c=520, H_I=1, K=33, sink=True, pos_lo=100,
+                           pos_hi=519),
+    # positions below the window (ring still filling) and n_vis < K, = K
+    "early": wl.small("early", B=4, T=4, r=2, N_c=64, K=40, W=32, R=32, pos_lo=0, pos_hi=100),
+    # prefill chunk: 96 causal tokens of one sequence, ring of T + W - 1 slots
+    "prefill": wl.small("prefill", B=1, T=96, r=4, N_c=160, H_I=64, D_I=128, K=48, H=64, W=16,
+                        R=112, q_dtype=wl.FP8_E4M3, q_scale=True, pos_mode="prefill",
+                        pos_lo=540, pos_hi=635, w_div=64.0),
+}
+
+
+# fixed positions where the edge cases must appear: n_vis = 0 (position 0),
+# n_vis < K, n_vis == K (79 -> 40 with r=2, K=40), window not yet full
+POSITIONS = {"early": (np.arange(4, dtype=np.int32), np.array([0, 5, 79, 100], dtype=np.int32))}
+
+
+@pytest.fixture(scope="module", params=sorted(SMALL))
+def case(request):
+    w = wl.generate(SMALL[request.param], seed=1000 + sorted(SMALL).index(request.param),
+                    positions=POSITIONS.get(request.param))
+    S, A = oracle.index_scores(problem(w), with_magnitude=True)
+    return request.param, w, S, A
+
+
+def test_scores(case):
+    name, w, S, A = case
+    g = run_scores(w)
+    check_scores(g, S, A)
+
+
+def test_topk_exact_on_gpu_scores(case):
+    """Top-k is integer work: on the same fp32 scores it must equal the
+    oracle's selection exactly."""
+    name, w, S, A = case
+    g_scores = run_scores(w)
+    idx = run_topk(w, g_scores, w.K)
+    for t in range(w.T):
+        nv = n_vis(int(w.q_pos[t]), w.r)
+        ref = oracle.topk_row(g_scores[t].astype(np.float64), nv, w.K)
+        assert idx[t].tolist() == ref.tolist(), (name, t)
+
+
+def test_attn_on_oracle_indices(case):
+    name, w, S, A = case
+    o_idx = oracle.topk(problem(w), S, w.K)
+    g = run_attn(w, o_idx)
+    o = oracle.sparse_attn(problem(w), o_idx)
+    check_attn(g, o)
+
+
+def test_fused(case):
+    name, w, S, A = case
+    g_idx, g_out = run_fused(w)
+    o_idx = oracle.topk(problem(w), S, w.K)
+    for t in range(w.T):
+        check_topk_sets(g_idx[t], o_idx[t], S[t], A[t], n_vis(int(w.q_pos[t]), w.r), w.K)
+    # attention parity on the GPU's own selection
+    check_attn(g_out, oracle.sparse_attn(problem(w), g_idx))
+
+
+def test_fused_without_idx_out(case):
+    name, w, S, A = case
+    _, g_out = run_fused(w, with_idx=False)
+    g_idx, g_out2 = run_fused(w)
+    assert np.array_equal(g_out, g_out2)
+
+
+def test_topk_ties_and_sizes():
+    """Planted ties across chunk boundaries: exact match with the oracle's
+    lower-position tie rule."""
+    spec = wl.small("ties", B=5, T=5, r=1, N_c=5000, K=700, pos_mode="fixed", pos_lo=0, pos_hi=0)
+    w = wl.generate(spec, seed=77, positions=(np.arange(5, dtype=np.int32),
+                                              np.array([4999, 2500, 700, 699, 1500], dtype=np.int32)))
+    rng = np.random.default_rng(8)
+    scores = np.round(rng.normal(size=(5, 5000)) * 4).astype(np.float32) / 4
+    scores[4, :] = 1.0  # a row of equal scores: the lowest positions win
+    scores[3, 10:20] = -0.0
+    idx = run_topk(w, scores, spec.K)
+    for t in range(5):
+        nv = n_vis(int(w.q_pos[t]), w.r)
+        ref = oracle.topk_row(scores[t].astype(np.float64), nv, spec.K)
+        assert idx[t].tolist() == ref.tolist(), t
+
+
+def test_k_zero_is_window_only():
+    w = wl.generate(wl.small("k0", K=0), seed=5)
+    _, g = run_fused(w, K=0)
+    o = oracle.sparse_attn(problem(w), np.zeros((w.T, 0), dtype=np.int32))
+    check_attn(g, o)
+
+
+def test_shared_kv_tensor():
+    """K and V given as one tensor (the V4.1 page's single kv): pointers equal."""
+    w = wl.generate(wl.small("kv_same"), seed=6)
+    w.Vw = w.Kw
+    w.Vc = w.Kc
+    S, A = oracle.index_scores(problem(w), with_magnitude=True)
+    o_idx = oracle.topk(problem(w), S, w.K)
+    dp = binding.upload(w)
+    dp.tensors["Vw"], dp.tensors["Vc"] = dp.tensors["Kw"], dp.tensors["Kc"]
+    dp.aa.Vw, dp.aa.Vc = dp.aa.Kw, dp.aa.Kc
+    g_idx, g = run_fused(w, dp=dp)
+    check_attn(g, oracle.sparse_attn(problem(w), g_idx))
+
+
+def test_empty_batch():
+    w = wl.generate(wl.small("empty", T=0, B=1), seed=9, positions=(np.zeros(0, np.int32), np.zeros(0, np.int32)))
+    idx, out = run_fused(w)
+    assert idx.shape == (0, w.K) and out.shape == (0, w.H, w.D)
+
+
+def test_bad_device_indices_are_skipped_and_flagged():
+    w = wl.generate(wl.small("badidx"), seed=10)
+    S = oracle.index_scores(problem(w))
+    o_idx = oracle.topk(problem(w), S, w.K)
+    bad = o_idx.copy()
+    bad[0, 3] = n_vis(int(w.q_pos[0]), w.r) + 5   # past n_vis
+    bad[1, 0] = -9                                  # not -1
+    g = run_attn(w, bad, expect_status=binding.SA_ERR_DEVICE_DATA)
+    clean = bad.copy()
+    clean[0, 3] = -1
+    clean[1, 0] = -1
+    check_attn(g, oracle.sparse_attn(problem(w), clean))
+
+
+def test_bad_sequence_id_is_flagged():
+    w = wl.generate(wl.small("badseq"), seed=11)
+    w.q_seq = w.q_seq.copy()
+    w.q_seq[1] = 99
+    dp = binding.upload(w)
+    ws = binding.new_workspace(dp)
+    import torch
+    scores = torch.empty((w.T, w.N_c), dtype=torch.float32, device="cuda")
+    binding.sa_indexer_scores(dp.ia, scores, ws)
+    assert binding.sa_check_device_status(ws) == binding.SA_ERR_DEVICE_DATA
+    assert binding.sa_check_device_status(ws) == binding.SA_OK  # read-and-clear
