@@ -173,6 +173,41 @@ SA_API sa_status sa_fused_decode_staged(const sa_index_args *ia, const sa_attn_a
 SA_API int32_t sa_fused_decode_launch_count(const sa_index_args *ia, const sa_attn_args *aa,
                                             int32_t K);
 
+/* Bytes of the fixed device scratch array behind sa_fused_decode_noalloc. */
+#define SA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/* sa_fused_decode for callers that cannot allocate device memory.  (The model
+ * pages have no counterpart: this is a deployment variant of the fused step.)
+ *
+ * Who needs it: code that has no device allocator at hand or must not
+ * allocate on its execution path -- a plugin host that hands its kernels no
+ * workspace, or a serving loop that fixes its memory budget at start-up and
+ * treats any allocation while serving a request as a failure.  Such a caller
+ * cannot obtain the workspace the other entry points ask for.
+ *
+ * Same inputs, outputs and results as sa_fused_decode (idx_out may be NULL;
+ * out is [T, H, D] bf16), but the scratch lives in one library-owned device
+ * array of SA_NOALLOC_SCRATCH_BYTES bytes: every GPU that loads the library
+ * holds that array until the process exits.  Nothing is allocated or freed:
+ * no cudaMalloc, cudaFree or allocating library routine is called.
+ *
+ * - Size limit: a problem whose scratch (sa_workspace_size for the same
+ *   arguments) exceeds SA_NOALLOC_SCRATCH_BYTES is rejected with
+ *   SA_ERR_UNSUPPORTED and enqueues nothing.
+ * - Set-up: the first call on each device (with that device current) looks
+ *   up the array's device address once (cudaGetSymbolAddress); make that
+ *   first call before any stream capture.
+ * - Sharing: every call on a device uses the same array, which keeps the last
+ *   call's contents (no part of it needs to start at zero).  Calls whose work
+ *   overlaps on the GPU -- on different streams, or from different host
+ *   threads -- race on it and give undefined results; serialise them.
+ * - device_status: optional 4-byte device word that the kernels OR their
+ *   out-of-range-data flags into (see sa_check_device_status for their
+ *   meaning); NULL to skip reporting.  The caller zeroes and reads it. */
+SA_API sa_status sa_fused_decode_noalloc(const sa_index_args *ia, const sa_attn_args *aa,
+                                         int32_t K, int32_t *idx_out, void *out,
+                                         uint32_t *device_status, sa_stream_t stream);
+
 /* Synchronises `stream`, then reads and clears the workspace's sticky device
  * status: SA_OK, SA_ERR_DEVICE_DATA (out-of-range device data was skipped)
  * or SA_ERR_TIMEOUT. */

@@ -86,6 +86,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.sa_fused_decode_staged.argtypes = [IA, AA, i32, vp, vp, vp, sz, vp, ctypes.POINTER(vp)]
     lib.sa_fused_decode_launch_count.argtypes = [IA, AA, i32]
     lib.sa_fused_decode_launch_count.restype = i32
+    lib.sa_fused_decode_noalloc.argtypes = [IA, AA, i32, vp, vp, vp, vp]
+    lib.sa_fused_decode_noalloc.restype = i32
     lib.sa_check_device_status.argtypes = [vp, vp]
     lib.sa_status_string.argtypes = [i32]
     lib.sa_status_string.restype = ctypes.c_char_p
@@ -166,6 +168,14 @@ def sa_fused_decode_staged(ia: IndexArgs, aa: AttnArgs, K: int, idx_out, out, ws
 
 def sa_fused_decode_launch_count(ia: IndexArgs, aa: AttnArgs, K: int) -> int:
     return int(load().sa_fused_decode_launch_count(ctypes.byref(ia), ctypes.byref(aa), K))
+
+
+def sa_fused_decode_noalloc(ia: IndexArgs, aa: AttnArgs, K: int, idx_out, out, device_status=None,
+                            stream=None) -> None:
+    """The fused step on the library's fixed device scratch (no workspace, no
+    allocation); see include/sa.h for its size limit and sharing rules."""
+    _check(load().sa_fused_decode_noalloc(ctypes.byref(ia), ctypes.byref(aa), K, _p(idx_out), _p(out),
+                                          _p(device_status), _s(stream)))
 
 
 def sa_check_device_status(ws, stream=None) -> int:

@@ -36,6 +36,15 @@ cudaError_t launch_sparse_mqa(const sa_index_args &ia, const sa_attn_args &aa, c
 int fused_launch_count(const sa_index_args &ia, const sa_attn_args &aa, int K,
                        const SplitPlan &plan);
 
+// Records a one-line error detail for sa_last_error_detail() and returns s.
+sa_status set_error(sa_status s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+
+// The fused launch sequence on a caller-chosen scratch region (laid out by
+// ws_layout) with a caller-chosen status word (may be NULL).
+sa_status fused_with_scratch(const sa_index_args *ia, const sa_attn_args *aa, int K,
+                             int32_t *idx_out, void *out, void *scratch, size_t scratch_bytes,
+                             uint32_t *status, cudaStream_t stream);
+
 bool attn_shape_supported(int H, int D);
 bool index_shape_supported(int H_I, int D_I);
 

@@ -118,6 +118,43 @@ WsLayout ws_layout(const sa_index_args &ia, const sa_attn_args *aa, int K) {
 
 }  // namespace sa
 
+namespace sa {
+
+sa_status set_error(sa_status s, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_detail = buf;
+  return s;
+}
+
+sa_status fused_with_scratch(const sa_index_args *ia, const sa_attn_args *aa, int K,
+                             int32_t *idx_out, void *out, void *scratch, size_t scratch_bytes,
+                             uint32_t *status, cudaStream_t st) {
+  if (sa_status s = check_index(ia, true)) return s;
+  if (sa_status s = check_attn(aa, ia->T)) return s;
+  if (K < 0) return fail(SA_ERR_INVALID_ARG, "K must be >= 0 (got %d)", K);
+  if (ia->T > 0 && !out) return fail(SA_ERR_INVALID_ARG, "out must be a device pointer");
+  if (!aligned4(idx_out) || !aligned16(out))
+    return fail(SA_ERR_INVALID_ARG, "idx_out must be 4-byte and out 16-byte aligned");
+  const WsLayout L = ws_layout(*ia, aa, K);
+  if (sa_status s = check_ws(scratch, scratch_bytes, L.total)) return s;
+  float *scores = at<float>(scratch, L.scores);
+  int32_t *idx = idx_out ? idx_out : at<int32_t>(scratch, L.idx);
+  cudaError_t e = launch_idx_score(*ia, scores, ia->N_c, false, status, st);
+  if (e != cudaSuccess) return cuda_fail(e, "index score launch");
+  e = launch_topk(scores, ia->N_c, *ia, K, idx, status, st);
+  if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+  const SplitPlan plan = plan_splits(ia->T, aa->W, K);
+  e = launch_sparse_mqa(*ia, *aa, idx, K, out, at<float>(scratch, L.part_m),
+                        at<float>(scratch, L.part_l), at<float>(scratch, L.part_o), plan, status, st);
+  return e == cudaSuccess ? SA_OK : cuda_fail(e, "sparse attention launch");
+}
+
+}  // namespace sa
+
 extern "C" {
 
 size_t sa_workspace_size(const sa_index_args *ia, const sa_attn_args *aa, int32_t K) {
