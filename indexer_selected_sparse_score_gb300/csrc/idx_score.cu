@@ -4,7 +4,9 @@
 // "DeepSeek-V3.2-Exp inference/model.py", fp8_index with fp8 keys and one
 // fp32 scale per position).
 //
-// This file holds the CUDA-core kernel: one thread per key row, the token's
+// This file holds the CUDA-core kernel (index heads of dim 64, bf16 keys and
+// any shape the tensor-core kernel in idx_score_umma.cu does not take): one
+// thread per key row, the token's
 // index queries dequantised once into shared memory (fp32) and broadcast to
 // all threads.  The products of a bf16/fp8 query element and an fp8/bf16 key
 // element are exact in fp32; each head's dot product accumulates in fp32 in
@@ -134,9 +136,16 @@ bool index_shape_supported(int H_I, int D_I) {
   return H_I >= 1 && H_I <= 128 && (D_I == 64 || D_I == 128);
 }
 
+size_t idx_score_scratch(const sa_index_args &ia) {
+  return idx_score_umma_supported(ia) ? idx_score_umma_scratch(ia) : 0;
+}
+
 cudaError_t launch_idx_score(const sa_index_args &ia, float *scores, int64_t ld,
-                             bool write_masked, uint32_t *status, cudaStream_t stream) {
+                             bool write_masked, void *scratch, uint32_t *status,
+                             cudaStream_t stream) {
   if (ia.T == 0) return cudaSuccess;
+  if (idx_score_umma_supported(ia))
+    return launch_idx_score_umma(ia, scores, ld, write_masked, scratch, status, stream);
   const bool qf8 = ia.q_dtype == SA_FP8_E4M3, kf8 = ia.k_dtype == SA_FP8_E4M3;
 #define SA_SCORE_CASE(DI, QF, KF)                                              \
   if (ia.D_I == DI && qf8 == QF && kf8 == KF)                                  \

@@ -1,0 +1,447 @@
+// Index scores on the 5th-generation tensor cores (tcgen05), for fp8-e4m3
+// keys of dim 128 ("DeepSeek-V3.2-Exp inference/model.py", Indexer.forward /
+// fp8_index: fp8 k_cache with one fp32 scale per position;
+// "DeepSeek-V4.1-Flash-NVFP4 inference/model.py", Indexer.forward: einsum,
+// relu_(), times weights, sum over heads).
+//
+// Per key tile of 128 positions the tensor core forms D[key, head] =
+// sum_d k[key, d] * q[head, d] (M = 128 keys, N = H_I heads, K = 128) with
+// e4m3 operands and an fp32 accumulator in tensor memory; the epilogue applies
+// ReLU, the head weights and the key scale.
+//
+// Queries that are bf16 are split exactly into two e4m3 pieces per head:
+// with a power-of-two head scale 2^e (max|q_h| 2^-e in (224, 448]),
+// q 2^-e = p1 + p2 where p1 = e4m3(q 2^-e) and p2 = e4m3(q 2^-e - p1).  Every
+// element within 2^-10.8 of the head's largest is represented exactly (its
+// 8 significant bits split 4 + 4); smaller ones carry an error below
+// 2^-10 * 2^e, i.e. below 2^-18.8 of the head's largest element.  Both pieces
+// accumulate into the same tensor-memory columns (two passes of K = 128), so
+// D = q 2^-e . k, and 2^e moves into the head weight.  fp8 queries need one
+// piece.  The products of e4m3 values are exact and the tensor core
+// accumulates them in fp32.
+//
+// The main kernel is persistent: every CTA takes a contiguous range of the
+// flattened (token, key tile) list, and four roles run as warps:
+//   warp 0     TMA producer: key tiles (6-stage ring) and each token's packed
+//              queries and weights (double buffered);
+//   warp 1     MMA issuer (one thread) and tensor-memory owner;
+//   warps 2-5  epilogue: tensor memory -> registers -> score.
+// Every wait is bounded (about a second); on expiry the kernel flags the
+// workspace status word and drains its in-flight copies and MMAs before it
+// returns.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "umma.cuh"
+
+namespace sa {
+namespace {
+
+using namespace umma;
+
+constexpr int kTileKeys = 128;                   // M
+constexpr int kKeyTileBytes = kTileKeys * 128;   // 128 keys x 128 fp8
+constexpr int kStages = 6;
+constexpr int kAccStages = 4;
+constexpr int kMainThreads = 192;
+constexpr int kMaxTokens = 8192;                 // tile prefix kept in shared memory
+
+template <int NH, int P>
+struct ScoreSmem {
+  static constexpr int kQBytes = P * NH * 128;
+  static constexpr size_t keys = 0;
+  static constexpr size_t qbuf = keys + static_cast<size_t>(kStages) * kKeyTileBytes;
+  static constexpr size_t wq = qbuf + 2 * static_cast<size_t>(kQBytes);
+  static constexpr size_t prefix = wq + 2 * NH * sizeof(float);
+  static constexpr size_t part = prefix + (kMaxTokens + 1) * sizeof(int);
+  static constexpr size_t bars = (part + kMainThreads * sizeof(int) + 7) & ~static_cast<size_t>(7);
+  static constexpr int kBars = 2 * kStages + 4 + 2 * kAccStages + 1;
+  static constexpr size_t misc = bars + kBars * sizeof(uint64_t);
+  static constexpr size_t total = misc + 64;
+};
+
+// ---------------------------------------------------------------- prep ----
+
+// Packs token t's index queries into the K-major 128-byte-swizzled layout the
+// MMA reads (piece p, head h at rows p*H_I + h), writes the folded head
+// weights wq[t, h] = w * q_scale * 2^e, and (optionally) -inf into the
+// masked tail of the score row.
+template <int NH, bool QFP8>
+__global__ void __launch_bounds__(128)
+idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq,
+                 const int32_t *__restrict__ q_pos, const void *__restrict__ q_I,
+                 const float *__restrict__ q_scale, const float *__restrict__ w,
+                 uint8_t *__restrict__ qpack, float *__restrict__ wq, float *__restrict__ scores,
+                 int64_t ld, int write_masked, uint32_t *status) {
+  constexpr int P = QFP8 ? 1 : 2;
+  const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t *dst = qpack + static_cast<size_t>(t) * P * NH * 128;
+  for (int h = warp; h < NH; h += 4) {
+    const int64_t qrow = (static_cast<int64_t>(t) * NH + h) * 128;
+    const float qsc = q_scale ? q_scale[static_cast<int64_t>(t) * NH + h] : 1.f;
+    const float wt = w[static_cast<int64_t>(t) * NH + h] * qsc;
+    if (QFP8) {
+      const uint32_t v = reinterpret_cast<const uint32_t *>(static_cast<const uint8_t *>(q_I) + qrow)[lane];
+      *reinterpret_cast<uint32_t *>(dst + umma::sw128_offset(h, 4 * lane)) = v;
+      if (lane == 0) wq[static_cast<int64_t>(t) * NH + h] = wt;
+    } else {
+      const uint2 raw = reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(q_I) + qrow)[lane];
+      float x[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                    __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
+      float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      int e = 0;
+      if (amax > 0.f) {
+        int ex;
+        frexpf(amax, &ex);  // amax = m 2^ex, m in [0.5, 1)
+        e = ex - 9;         // amax 2^-e in [256, 512)
+        if (ldexpf(amax, -e) > 448.f) ++e;
+      }
+      uint32_t w1 = 0, w2 = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float y = ldexpf(x[i], -e);
+        const __nv_fp8_storage_t p1 = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
+        const float rest = y - e4m3_bits_to_float(p1);
+        const __nv_fp8_storage_t p2 = __nv_cvt_float_to_fp8(rest, __NV_SATFINITE, __NV_E4M3);
+        w1 |= static_cast<uint32_t>(p1) << (8 * i);
+        w2 |= static_cast<uint32_t>(p2) << (8 * i);
+      }
+      *reinterpret_cast<uint32_t *>(dst + umma::sw128_offset(h, 4 * lane)) = w1;
+      *reinterpret_cast<uint32_t *>(dst + NH * 128 + umma::sw128_offset(h, 4 * lane)) = w2;
+      if (lane == 0) wq[static_cast<int64_t>(t) * NH + h] = ldexpf(wt, e);
+    }
+  }
+  if (write_masked) {
+    Token tk;
+    const bool ok = load_token(q_seq, q_pos, t, B, N_c, r, status, tk, threadIdx.x == 0);
+    const int nv = ok ? tk.nv : 0;
+    float *row = scores + static_cast<int64_t>(t) * ld;
+    for (int s = nv + threadIdx.x; s < N_c; s += 128) row[s] = -INFINITY;
+  }
+}
+
+// --------------------------------------------------------------- main -----
+
+struct ScoreParams {
+  int B, T, N_c, r;
+  const int32_t *q_seq, *q_pos;
+  const uint8_t *qpack;
+  const float *wq;
+  const float *k_scale;
+  float *scores;
+  int64_t ld;
+  uint32_t *status;
+};
+
+__device__ __forceinline__ int token_tiles(const ScoreParams &p, int t, int *b_out, int *nv_out) {
+  const int b = p.q_seq[t], pos = p.q_pos[t];
+  if (b < 0 || b >= p.B || pos < 0) return 0;
+  const int nv = min(n_vis_of(pos, p.r), p.N_c);
+  if (b_out) *b_out = b;
+  if (nv_out) *nv_out = nv;
+  return (nv + kTileKeys - 1) / kTileKeys;
+}
+
+template <int NH, int P>
+__global__ void __launch_bounds__(kMainThreads, 1)
+idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParams p) {
+  using L = ScoreSmem<NH, P>;
+  constexpr int kQBytes = L::kQBytes;
+  constexpr uint32_t kTmemCols = kAccStages * NH;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the swizzle atoms need 1024-byte alignment: align the base explicitly
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t *keys = smem + L::keys;
+  uint8_t *qbuf = smem + L::qbuf;
+  float *wqs = reinterpret_cast<float *>(smem + L::wq);
+  int *prefix = reinterpret_cast<int *>(smem + L::prefix);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bars);
+  uint64_t *kfull = bars, *kempty = bars + kStages;
+  uint64_t *qfull = bars + 2 * kStages, *qempty = qfull + 2;
+  uint64_t *afull = qempty + 2, *aempty = afull + kAccStages;
+  uint64_t *done = aempty + kAccStages;
+  uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem + L::misc);
+  int *abort_s = reinterpret_cast<int *>(smem + L::misc + 8);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- set-up: tile prefix over tokens, barriers, tensor memory
+  {
+    const int per = (p.T + kMainThreads - 1) / kMainThreads;
+    const int t0 = tid * per, t1 = min(p.T, t0 + per);
+    int sum = 0;
+    for (int t = t0; t < t1; ++t) sum += token_tiles(p, t, nullptr, nullptr);
+    // inclusive scan of the per-thread sums across the block
+    int *part = reinterpret_cast<int *>(smem + L::part);
+    part[tid] = sum;
+    __syncthreads();
+    for (int o = 1; o < kMainThreads; o <<= 1) {
+      const int v = tid >= o ? part[tid - o] : 0;
+      __syncthreads();
+      part[tid] += v;
+      __syncthreads();
+    }
+    int run = part[tid] - sum;
+    for (int t = t0; t < t1; ++t) {
+      prefix[t] = run;
+      run += token_tiles(p, t, nullptr, nullptr);
+    }
+    if (tid == kMainThreads - 1) prefix[p.T] = part[tid];
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&kempty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&qfull[i], 1);
+      mbar_init(&qempty[i], 1 + 4);  // MMA commit + four epilogue warps
+    }
+    for (int i = 0; i < kAccStages; ++i) {
+      mbar_init(&afull[i], 1);
+      mbar_init(&aempty[i], 4);
+    }
+    mbar_init(done, 1);
+    *abort_s = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_base_s, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_s;
+
+  const int total = prefix[p.T];
+  const int begin = static_cast<int>((static_cast<long long>(total) * blockIdx.x) / gridDim.x);
+  const int end = static_cast<int>((static_cast<long long>(total) * (blockIdx.x + 1)) / gridDim.x);
+
+  // first token whose tiles contain `begin`
+  auto locate = [&](int i) {
+    int lo = 0, hi = p.T - 1;
+    while (lo < hi) {  // largest t with prefix[t] <= i
+      const int mid = (lo + hi + 1) >> 1;
+      if (prefix[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  };
+  auto fail = [&]() {
+    raise_flag(p.status, kFlagTimeout);
+    atomicExch(abort_s, 1);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0 && begin < end) {
+      prefetch_tmap(&kmap);
+      int t = locate(begin), prev_t = -1, qn = -1, b = 0, nv = 0;
+      int issued = 0;
+      for (int i = begin; i < end && !*(volatile int *)abort_s; ++i) {
+        while (prefix[t + 1] <= i) ++t;
+        if (t != prev_t) {
+          token_tiles(p, t, &b, &nv);
+          ++qn;
+          const int qb = qn & 1;
+          if (!mbar_wait(&qempty[qb], ((qn >> 1) & 1) ^ 1)) { fail(); break; }
+          mbar_expect_tx(&qfull[qb], kQBytes + NH * 4);
+          bulk_load(qbuf + qb * kQBytes, p.qpack + static_cast<size_t>(t) * kQBytes, kQBytes, &qfull[qb]);
+          bulk_load(wqs + qb * NH, p.wq + static_cast<size_t>(t) * NH, NH * 4, &qfull[qb]);
+          prev_t = t;
+        }
+        const int j = i - prefix[t];
+        const int n = i - begin, s = n % kStages;
+        if (!mbar_wait(&kempty[s], ((n / kStages) & 1) ^ 1)) { fail(); break; }
+        mbar_expect_tx(&kfull[s], kKeyTileBytes);
+        tma_load_2d(keys + s * kKeyTileBytes, &kmap, &kfull[s], 0, b * p.N_c + j * kTileKeys);
+        ++issued;
+      }
+      // drain: every issued copy must land before the CTA may exit
+      for (int n = max(0, issued - kStages); n < issued; ++n)
+        mbar_wait(&kfull[n % kStages], (n / kStages) & 1);
+      if (qn >= 0) mbar_wait(&qfull[qn & 1], (qn >> 1) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0 && begin < end) {
+      constexpr uint32_t idesc = idesc_e4m3(kTileKeys, NH);
+      int t = locate(begin), prev_t = -1, qn = -1;
+      for (int i = begin; i < end && !*(volatile int *)abort_s; ++i) {
+        while (prefix[t + 1] <= i) ++t;
+        if (t != prev_t) {
+          if (qn >= 0) mma_commit(&qempty[qn & 1]);
+          ++qn;
+          if (!mbar_wait(&qfull[qn & 1], (qn >> 1) & 1)) { fail(); break; }
+          prev_t = t;
+        }
+        const int n = i - begin, s = n % kStages, a = n % kAccStages;
+        if (!mbar_wait(&kfull[s], (n / kStages) & 1)) { fail(); break; }
+        if (!mbar_wait(&aempty[a], ((n / kAccStages) & 1) ^ 1)) { fail(); break; }
+        tc_fence_after();
+        const uint32_t d = tmem + a * NH;
+        const uint32_t a0 = smem_u32(keys + s * kKeyTileBytes);
+        const uint32_t b0 = smem_u32(qbuf + (qn & 1) * kQBytes);
+#pragma unroll
+        for (int pc = 0; pc < P; ++pc)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f8f6f4(d, desc_sw128_kmajor(a0 + 32 * k), desc_sw128_kmajor(b0 + pc * NH * 128 + 32 * k),
+                       idesc, (pc | k) != 0);
+        mma_commit(&kempty[s]);
+        mma_commit(&afull[a]);
+      }
+      if (qn >= 0) mma_commit(&qempty[qn & 1]);
+      mma_commit(done);
+      if (!mbar_wait(done, 0)) raise_flag(p.status, kFlagTimeout);
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    if (begin < end) {
+      int t = locate(begin), prev_t = -1, qn = -1, b = 0, nv = 0;
+      for (int i = begin; i < end && !*(volatile int *)abort_s; ++i) {
+        while (prefix[t + 1] <= i) ++t;
+        if (t != prev_t) {
+          if (qn >= 0) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&qempty[qn & 1]);
+          }
+          ++qn;
+          token_tiles(p, t, &b, &nv);
+          if (!mbar_wait(&qfull[qn & 1], (qn >> 1) & 1)) { fail(); break; }
+          prev_t = t;
+        }
+        const int n = i - begin, a = n % kAccStages;
+        if (!mbar_wait(&afull[a], (n / kAccStages) & 1)) { fail(); break; }
+        tc_fence_after();
+        uint32_t v[NH];
+#pragma unroll
+        for (int c = 0; c < NH / 32; ++c)
+          tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * NH + 32 * c,
+                             *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&aempty[a]);
+        const int s = (i - prefix[t]) * kTileKeys + row;
+        if (s < nv) {
+          const float *wv = wqs + (qn & 1) * NH;
+          float acc = 0.f;
+#pragma unroll
+          for (int h = 0; h < NH; ++h) acc = fmaf(wv[h], fmaxf(__uint_as_float(v[h]), 0.f), acc);
+          const int64_t krow = static_cast<int64_t>(b) * p.N_c + s;
+          const float ks = p.k_scale ? p.k_scale[krow] : 1.f;
+          p.scores[static_cast<int64_t>(t) * p.ld + s] = acc * ks;
+        }
+      }
+      if (qn >= 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qempty[qn & 1]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host --
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  return n;
+}
+
+template <int NH, bool QFP8>
+cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld, bool write_masked,
+                             uint8_t *qpack, float *wq, uint32_t *status, cudaStream_t stream) {
+  constexpr int P = QFP8 ? 1 : 2;
+  using L = ScoreSmem<NH, P>;
+  idx_qprep_kernel<NH, QFP8><<<ia.T, 128, 0, stream>>>(ia.B, ia.T, ia.N_c, ia.r, ia.q_seq, ia.q_pos,
+                                                        ia.q_I, ia.q_scale, ia.w, qpack, wq, scores,
+                                                        ld, write_masked ? 1 : 0, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  auto encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap kmap;
+  const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(ia.B) * ia.N_c};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {128, kTileKeys};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult cr = encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ia.k_I), dims,
+                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+
+  ScoreParams sp{ia.B, ia.T, ia.N_c, ia.r, ia.q_seq, ia.q_pos, qpack, wq, ia.k_scale, scores, ld, status};
+  auto kern = idx_score_umma_kernel<NH, P>;
+  const size_t smem = L::total + 1024;  // + alignment slack for the 1024-byte swizzle atoms
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<sm_count(), kMainThreads, smem, stream>>>(kmap, sp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool idx_score_umma_supported(const sa_index_args &ia) {
+  return ia.k_dtype == SA_FP8_E4M3 && ia.D_I == 128 && (ia.H_I == 32 || ia.H_I == 64 || ia.H_I == 128) &&
+         ia.T <= kMaxTokens;
+}
+
+size_t idx_score_umma_scratch(const sa_index_args &ia) {
+  const int P = ia.q_dtype == SA_FP8_E4M3 ? 1 : 2;
+  return static_cast<size_t>(ia.T) * P * ia.H_I * 128 + static_cast<size_t>(ia.T) * ia.H_I * 4 + 256;
+}
+
+cudaError_t launch_idx_score_umma(const sa_index_args &ia, float *scores, int64_t ld, bool write_masked,
+                                  void *scratch, uint32_t *status, cudaStream_t stream) {
+  if (ia.T == 0) return cudaSuccess;
+  const int P = ia.q_dtype == SA_FP8_E4M3 ? 1 : 2;
+  uint8_t *qpack = static_cast<uint8_t *>(scratch);
+  float *wq = reinterpret_cast<float *>(qpack + ((static_cast<size_t>(ia.T) * P * ia.H_I * 128 + 255) & ~size_t(255)));
+  const bool qf8 = ia.q_dtype == SA_FP8_E4M3;
+#define SA_UMMA_CASE(NH, QF)                                                                   \
+  if (ia.H_I == NH && qf8 == QF)                                                               \
+    return launch_umma_impl<NH, QF>(ia, scores, ld, write_masked, qpack, wq, status, stream);
+  SA_UMMA_CASE(32, false)
+  SA_UMMA_CASE(32, true)
+  SA_UMMA_CASE(64, false)
+  SA_UMMA_CASE(64, true)
+  SA_UMMA_CASE(128, false)
+  SA_UMMA_CASE(128, true)
+#undef SA_UMMA_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace sa

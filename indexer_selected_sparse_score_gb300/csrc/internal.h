@@ -18,12 +18,23 @@ SplitPlan plan_splits(int T, int W, int K);
 
 // Workspace carve-up (byte offsets, 256-byte aligned).
 struct WsLayout {
-  size_t status, scores, idx, part_m, part_l, part_o, total;
+  size_t status, scores, idx, score_scratch, part_m, part_l, part_o, total;
 };
 WsLayout ws_layout(const sa_index_args &ia, const sa_attn_args *aa, int K);
 
+// Index scores.  `scratch` (idx_score_scratch(ia) bytes, 256-byte aligned)
+// holds the tensor-core kernel's packed queries and folded head weights.
 cudaError_t launch_idx_score(const sa_index_args &ia, float *scores, int64_t ld,
-                             bool write_masked, uint32_t *status, cudaStream_t stream);
+                             bool write_masked, void *scratch, uint32_t *status,
+                             cudaStream_t stream);
+size_t idx_score_scratch(const sa_index_args &ia);
+
+// Tensor-core (tcgen05) variant: fp8 keys of dim 128, 32/64/128 index heads.
+bool idx_score_umma_supported(const sa_index_args &ia);
+size_t idx_score_umma_scratch(const sa_index_args &ia);
+cudaError_t launch_idx_score_umma(const sa_index_args &ia, float *scores, int64_t ld,
+                                  bool write_masked, void *scratch, uint32_t *status,
+                                  cudaStream_t stream);
 
 cudaError_t launch_topk(const float *scores, int64_t ld, const sa_index_args &ia, int K,
                         int32_t *idx, uint32_t *status, cudaStream_t stream);

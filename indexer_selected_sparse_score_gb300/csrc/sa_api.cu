@@ -101,6 +101,8 @@ WsLayout ws_layout(const sa_index_args &ia, const sa_attn_args *aa, int K) {
   off += round_up(sizeof(float) * static_cast<size_t>(ia.T) * ia.N_c);
   L.idx = off;
   off += round_up(sizeof(int32_t) * static_cast<size_t>(ia.T) * (K > 0 ? K : 0));
+  L.score_scratch = off;
+  off += round_up(idx_score_scratch(ia));
   L.part_m = L.part_l = L.part_o = off;
   if (aa) {
     const SplitPlan plan = plan_splits(ia.T, aa->W, K);
@@ -143,7 +145,8 @@ sa_status fused_with_scratch(const sa_index_args *ia, const sa_attn_args *aa, in
   if (sa_status s = check_ws(scratch, scratch_bytes, L.total)) return s;
   float *scores = at<float>(scratch, L.scores);
   int32_t *idx = idx_out ? idx_out : at<int32_t>(scratch, L.idx);
-  cudaError_t e = launch_idx_score(*ia, scores, ia->N_c, false, status, st);
+  cudaError_t e =
+      launch_idx_score(*ia, scores, ia->N_c, false, at<void>(scratch, L.score_scratch), status, st);
   if (e != cudaSuccess) return cuda_fail(e, "index score launch");
   e = launch_topk(scores, ia->N_c, *ia, K, idx, status, st);
   if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
@@ -174,9 +177,10 @@ sa_status sa_indexer_scores(const sa_index_args *ia, float *scores, void *ws, si
   if (sa_status s = check_index(ia, true)) return s;
   if (ia->T > 0 && !scores) return fail(SA_ERR_INVALID_ARG, "scores must be a device pointer");
   if (!aligned4(scores)) return fail(SA_ERR_INVALID_ARG, "scores must be 4-byte aligned");
-  if (sa_status s = check_ws(ws, ws_bytes, 256)) return s;
-  cudaError_t e = sa::launch_idx_score(*ia, scores, ia->N_c, true, at<uint32_t>(ws, 0),
-                                       reinterpret_cast<cudaStream_t>(stream));
+  const sa::WsLayout L = sa::ws_layout(*ia, nullptr, 0);
+  if (sa_status s = check_ws(ws, ws_bytes, L.total)) return s;
+  cudaError_t e = sa::launch_idx_score(*ia, scores, ia->N_c, true, at<void>(ws, L.score_scratch),
+                                       at<uint32_t>(ws, 0), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SA_OK : cuda_fail(e, "index score launch");
 }
 
@@ -231,7 +235,8 @@ static sa_status fused_impl(const sa_index_args *ia, const sa_attn_args *aa, int
   float *scores = at<float>(ws, L.scores);
   int32_t *idx = idx_out ? idx_out : at<int32_t>(ws, L.idx);
   cudaError_t e = mark(0);
-  if (e == cudaSuccess) e = sa::launch_idx_score(*ia, scores, ia->N_c, false, status, st);
+  if (e == cudaSuccess)
+    e = sa::launch_idx_score(*ia, scores, ia->N_c, false, at<void>(ws, L.score_scratch), status, st);
   if (e != cudaSuccess) return cuda_fail(e, "index score launch");
   e = mark(1);
   if (e == cudaSuccess) e = sa::launch_topk(scores, ia->N_c, *ia, K, idx, status, st);

@@ -256,9 +256,10 @@ bool attn_shape_supported(int H, int D) {
 int fused_launch_count(const sa_index_args &ia, const sa_attn_args &aa, int K,
                        const SplitPlan &plan) {
   (void)aa;
+  const int score = idx_score_umma_supported(ia) ? 2 : 1;  // (query packing +) scoring
   const int topk = K > 0 ? 1 : 0;
   const int attn = plan.splits > 1 ? 2 : 1;
-  return ia.T > 0 ? 1 + topk + attn : 0;
+  return ia.T > 0 ? score + topk + attn : 0;
 }
 
 SplitPlan plan_splits(int T, int W, int K) {

@@ -29,6 +29,15 @@ SMALL = {
                            pos_hi=519),
     # positions below the window (ring still filling) and n_vis < K, = K
     "early": wl.small("early", B=4, T=4, r=2, N_c=64, K=40, W=32, R=32, pos_lo=0, pos_hi=100),
+    # tensor-core index path with 32 and 128 index heads (V4.1 released: 32 x 128)
+    "i32x128_fp8k": wl.small("i32x128_fp8k", H_I=32, D_I=128, r=2, N_c=900, K=128, H=32,
+                             pos_lo=300, pos_hi=1799, w_div=32.0),
+    "i128x128_fp8qk": wl.small("i128x128_fp8qk", H_I=128, D_I=128, r=4, N_c=700, K=100, H=128,
+                               q_dtype=wl.FP8_E4M3, q_scale=True, pos_lo=900, pos_hi=2799,
+                               w_div=128.0),
+    # tensor-core path with tokens that see no compressed row between long ones
+    "umma_early": wl.small("umma_early", B=6, T=6, H_I=64, D_I=128, r=4, N_c=700, K=100, H=64,
+                           W=32, R=32, w_div=64.0),
     # prefill chunk: 96 causal tokens of one sequence, ring of T + W - 1 slots
     "prefill": wl.small("prefill", B=1, T=96, r=4, N_c=160, H_I=64, D_I=128, K=48, H=64, W=16,
                         R=112, q_dtype=wl.FP8_E4M3, q_scale=True, pos_mode="prefill",
@@ -38,7 +47,9 @@ SMALL = {
 
 # fixed positions where the edge cases must appear: n_vis = 0 (position 0),
 # n_vis < K, n_vis == K (79 -> 40 with r=2, K=40), window not yet full
-POSITIONS = {"early": (np.arange(4, dtype=np.int32), np.array([0, 5, 79, 100], dtype=np.int32))}
+POSITIONS = {"early": (np.arange(4, dtype=np.int32), np.array([0, 5, 79, 100], dtype=np.int32)),
+             "umma_early": (np.arange(6, dtype=np.int32),
+                            np.array([2, 2799, 0, 510, 3, 127], dtype=np.int32))}
 
 
 @pytest.fixture(scope="module", params=sorted(SMALL))
