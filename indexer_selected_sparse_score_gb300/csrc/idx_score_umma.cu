@@ -315,11 +315,11 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
           }
           ++qn;
           token_tiles(p, t, &b, &nv);
-          if (!mbar_wait(&qfull[qn & 1], (qn >> 1) & 1)) { fail(); break; }
+          if (!mbar_wait_warp(&qfull[qn & 1], (qn >> 1) & 1)) { fail(); break; }
           prev_t = t;
         }
         const int n = i - begin, a = n % kAccStages;
-        if (!mbar_wait(&afull[a], (n / kAccStages) & 1)) { fail(); break; }
+        if (!mbar_wait_warp(&afull[a], (n / kAccStages) & 1)) { fail(); break; }
         tc_fence_after();
         uint32_t v[NH];
 #pragma unroll
@@ -359,27 +359,6 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
 
 // ------------------------------------------------------------------ host --
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
-  return n;
-}
-
 template <int NH, bool QFP8>
 cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld, bool write_masked,
                              uint8_t *qpack, float *wq, uint32_t *status, cudaStream_t stream) {
@@ -413,6 +392,27 @@ cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld,
 }
 
 }  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  return n;
+}
 
 bool idx_score_umma_supported(const sa_index_args &ia) {
   return ia.k_dtype == SA_FP8_E4M3 && ia.D_I == 128 && (ia.H_I == 32 || ia.H_I == 64 || ia.H_I == 128) &&

@@ -1,6 +1,8 @@
 // Host-side launchers behind the C ABI (one per kernel family).
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -18,8 +20,13 @@ SplitPlan plan_splits(int T, int W, int K);
 
 // Workspace carve-up (byte offsets, 256-byte aligned).
 struct WsLayout {
-  size_t status, scores, idx, score_scratch, part_m, part_l, part_o, total;
+  size_t status, scores, idx, score_scratch, attn_scratch, part_m, part_l, part_o, total;
 };
+
+// Driver entry point cuTensorMapEncodeTiled (NULL if unavailable) and the
+// current device's SM count.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+int sm_count();
 WsLayout ws_layout(const sa_index_args &ia, const sa_attn_args *aa, int K);
 
 // Index scores.  `scratch` (idx_score_scratch(ia) bytes, 256-byte aligned)
@@ -39,9 +46,18 @@ cudaError_t launch_idx_score_umma(const sa_index_args &ia, float *scores, int64_
 cudaError_t launch_topk(const float *scores, int64_t ld, const sa_index_args &ia, int K,
                         int32_t *idx, uint32_t *status, cudaStream_t stream);
 
+// Attention + combine.  The tensor-core kernel (64 heads of dim 128) uses
+// `attn_scratch` (attn_umma_scratch bytes); the CUDA-core kernel uses the
+// split partials part_m/part_l/part_o laid out by `plan`.
 cudaError_t launch_sparse_mqa(const sa_index_args &ia, const sa_attn_args &aa, const int32_t *idx,
                               int K, void *out, float *part_m, float *part_l, float *part_o,
-                              const SplitPlan &plan, uint32_t *status, cudaStream_t stream);
+                              void *attn_scratch, const SplitPlan &plan, uint32_t *status,
+                              cudaStream_t stream);
+bool attn_umma_supported(const sa_attn_args &aa);
+size_t attn_umma_scratch(const sa_index_args &ia, const sa_attn_args &aa, int K);
+cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &aa, const int32_t *idx,
+                                   int K, void *out, void *scratch, uint32_t *status,
+                                   cudaStream_t stream);
 
 // Kernel launches of one fused call (index score, top-k, attention, combine).
 int fused_launch_count(const sa_index_args &ia, const sa_attn_args &aa, int K,

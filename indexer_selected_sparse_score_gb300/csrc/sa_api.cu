@@ -103,8 +103,10 @@ WsLayout ws_layout(const sa_index_args &ia, const sa_attn_args *aa, int K) {
   off += round_up(sizeof(int32_t) * static_cast<size_t>(ia.T) * (K > 0 ? K : 0));
   L.score_scratch = off;
   off += round_up(idx_score_scratch(ia));
-  L.part_m = L.part_l = L.part_o = off;
-  if (aa) {
+  L.attn_scratch = L.part_m = L.part_l = L.part_o = off;
+  if (aa && attn_umma_supported(*aa)) {
+    off += round_up(attn_umma_scratch(ia, aa ? *aa : sa_attn_args{}, K));
+  } else if (aa) {
     const SplitPlan plan = plan_splits(ia.T, aa->W, K);
     const size_t th = static_cast<size_t>(ia.T) * aa->H * plan.splits;
     L.part_m = off;
@@ -152,7 +154,8 @@ sa_status fused_with_scratch(const sa_index_args *ia, const sa_attn_args *aa, in
   if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
   const SplitPlan plan = plan_splits(ia->T, aa->W, K);
   e = launch_sparse_mqa(*ia, *aa, idx, K, out, at<float>(scratch, L.part_m),
-                        at<float>(scratch, L.part_l), at<float>(scratch, L.part_o), plan, status, st);
+                        at<float>(scratch, L.part_l), at<float>(scratch, L.part_o),
+                        at<void>(scratch, L.attn_scratch), plan, status, st);
   return e == cudaSuccess ? SA_OK : cuda_fail(e, "sparse attention launch");
 }
 
@@ -211,7 +214,7 @@ sa_status sa_sparse_attn(const sa_index_args *ia, const sa_attn_args *aa, const 
   if (sa_status s = check_ws(ws, ws_bytes, L.total)) return s;
   const sa::SplitPlan plan = sa::plan_splits(ia->T, aa->W, K);
   cudaError_t e = sa::launch_sparse_mqa(*ia, *aa, idx, K, out, at<float>(ws, L.part_m),
-                                        at<float>(ws, L.part_l), at<float>(ws, L.part_o), plan,
+                                        at<float>(ws, L.part_l), at<float>(ws, L.part_o), at<void>(ws, L.attn_scratch), plan,
                                         at<uint32_t>(ws, 0), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SA_OK : cuda_fail(e, "sparse attention launch");
 }
@@ -245,7 +248,7 @@ static sa_status fused_impl(const sa_index_args *ia, const sa_attn_args *aa, int
   e = mark(2);
   if (e == cudaSuccess)
     e = sa::launch_sparse_mqa(*ia, *aa, idx, K, out, at<float>(ws, L.part_m), at<float>(ws, L.part_l),
-                              at<float>(ws, L.part_o), plan, status, st);
+                              at<float>(ws, L.part_o), at<void>(ws, L.attn_scratch), plan, status, st);
   if (e == cudaSuccess) e = mark(3);
   return e == cudaSuccess ? SA_OK : cuda_fail(e, "sparse attention launch");
 }

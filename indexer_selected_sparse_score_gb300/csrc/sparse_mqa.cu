@@ -4,7 +4,8 @@
 // cat(window_idxs, compress_idxs + offset), sparse_attn(q, kv, attn_sink,
 // topk_idxs, softmax_scale); one shared KV head serves every query head).
 //
-// CUDA-core kernel: one CTA per (token, split).  The token's key list is its
+// CUDA-core kernel (head counts other than 64; the tensor-core kernel for 64
+// heads is in sparse_mqa_umma.cu): one CTA per (token, split).  The token's key list is its
 // window rows (oldest first) followed by its K index slots; a split takes a
 // contiguous chunk of that list.  Rows are gathered 16 bytes per thread,
 // logits and the online softmax run in fp32 in the log2 domain (logits are
@@ -255,10 +256,9 @@ bool attn_shape_supported(int H, int D) {
 
 int fused_launch_count(const sa_index_args &ia, const sa_attn_args &aa, int K,
                        const SplitPlan &plan) {
-  (void)aa;
   const int score = idx_score_umma_supported(ia) ? 2 : 1;  // (query packing +) scoring
   const int topk = K > 0 ? 1 : 0;
-  const int attn = plan.splits > 1 ? 2 : 1;
+  const int attn = attn_umma_supported(aa) ? 2 : (plan.splits > 1 ? 2 : 1);
   return ia.T > 0 ? score + topk + attn : 0;
 }
 
@@ -276,8 +276,11 @@ SplitPlan plan_splits(int T, int W, int K) {
 
 cudaError_t launch_sparse_mqa(const sa_index_args &ia, const sa_attn_args &aa, const int32_t *idx,
                               int K, void *out, float *part_m, float *part_l, float *part_o,
-                              const SplitPlan &plan, uint32_t *status, cudaStream_t stream) {
+                              void *attn_scratch, const SplitPlan &plan, uint32_t *status,
+                              cudaStream_t stream) {
   if (ia.T == 0) return cudaSuccess;
+  if (attn_umma_supported(aa))
+    return launch_sparse_mqa_umma(ia, aa, idx, K, out, attn_scratch, status, stream);
   AttnParams p;
   p.B = ia.B;
   p.T = ia.T;

@@ -63,6 +63,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   return true;
 }
 
+// Every lane of the warp waits; the result is the same in every lane (false
+// if any lane ran out of budget), so a warp never splits before a
+// .sync.aligned instruction.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity) {
+  const bool ok = mbar_wait(bar, parity);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // --------------------------------------------------------------------- TMA --
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {

@@ -27,6 +27,9 @@ SMALL = {
     # r = 1 (no compression), one index head, sink present
     "r1_h1_sink": wl.small("r1_h1_sink", r=1, N_c=520, H_I=1, K=33, sink=True, pos_lo=100,
                            pos_hi=519),
+    # 64 attention heads (tensor-core attention) with a sink and a window over 128
+    "h64_sink_w200": wl.small("h64_sink_w200", H_I=64, D_I=128, r=4, N_c=700, K=300, H=64, W=200,
+                              R=200, sink=True, pos_lo=900, pos_hi=2799, w_div=64.0),
     # positions below the window (ring still filling) and n_vis < K, = K
     "early": wl.small("early", B=4, T=4, r=2, N_c=64, K=40, W=32, R=32, pos_lo=0, pos_hi=100),
     # tensor-core index path with 32 and 128 index heads (V4.1 released: 32 x 128)
@@ -120,8 +123,9 @@ def test_topk_ties_and_sizes():
         assert idx[t].tolist() == ref.tolist(), t
 
 
-def test_k_zero_is_window_only():
-    w = wl.generate(wl.small("k0", K=0), seed=5)
+@pytest.mark.parametrize("H", [16, 64])
+def test_k_zero_is_window_only(H):
+    w = wl.generate(wl.small("k0", K=0, H=H, W=130, R=130), seed=5)
     _, g = run_fused(w, K=0)
     o = oracle.sparse_attn(problem(w), np.zeros((w.T, 0), dtype=np.int32))
     check_attn(g, o)
