@@ -82,11 +82,17 @@ def peaks():
         return 6800.0, "fallback"
 
 
+STAGE_SOURCES = {"idx_score": ("idx_score.cu", "idx_score_umma.cu", "umma.cuh"),
+                 "idx_topk": ("idx_topk.cu",),
+                 "sparse_mqa": ("sparse_mqa.cu", "sparse_mqa_umma.cu", "umma.cuh")}
+
+
 def kernel_source_hash(stage):
-    src = {"idx_score": "idx_score.cu", "idx_topk": "idx_topk.cu", "sparse_mqa": "sparse_mqa.cu"}[stage]
-    path = os.path.join(ROOT, "indexer_selected_sparse_score_gb300", "csrc", src)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for src in STAGE_SOURCES[stage]:
+        with open(os.path.join(ROOT, "indexer_selected_sparse_score_gb300", "csrc", src), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(stage, workload):
@@ -257,15 +263,41 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     launches_per_step = binding.sa_fused_decode_launch_count(copies[0].ia, copies[0].aa, K)
 
-    def step(i):
+    def eager_step(i):
         dp = copies[i % len(copies)]
         binding.sa_fused_decode(dp.ia, dp.aa, K, idx, out, ws, stream)
 
     for i in range(args.warmup):
-        step(i)
+        eager_step(i)
     torch.cuda.synchronize()
     if binding.sa_check_device_status(ws) != binding.SA_OK:
         raise RuntimeError("device status not OK after warm-up")
+
+    # One CUDA graph per input copy: the step as a decode loop would replay it.
+    graphs = []
+    for dp in copies:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            binding.sa_fused_decode(dp.ia, dp.aa, K, idx, out, ws)
+        graphs.append(g)
+    # and one per copy with CUDA events between the stages (per-kernel timing)
+    stage_events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in copies]
+    for row in stage_events:
+        for e in row:
+            e.record(stream)  # materialise the CUDA event handles
+    torch.cuda.synchronize()
+    staged_graphs = []
+    for dp, evs in zip(copies, stage_events):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            binding.sa_fused_decode_staged(dp.ia, dp.aa, K, idx, out, ws, [e.cuda_event for e in evs])
+        staged_graphs.append(g)
+    for i in range(max(3, args.warmup)):
+        graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+
+    def step(i):
+        graphs[i % len(graphs)].replay()
 
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -274,9 +306,9 @@ def run_ours(args):
     while time.time() - t_soak < args.soak_seconds:  # same steps, untimed, to read clocks under load
         step(i)
         i += 1
-        if i % 16 == 0:
+        if i % 64 == 0:
             torch.cuda.synchronize()
-    # ---- timed region: exactly K steps
+    # ---- timed region: exactly K steps (graph replays)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -298,18 +330,26 @@ def run_ours(args):
     ms_per_step = ms / args.steps
     value = w.T * world * args.steps / (ms / 1000.0)
 
-    # ---- per-stage device time, same launches with events between stages
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    for row in evs:
-        for e in row:
-            e.record(stream)  # materialise the CUDA event handles
+    # ---- the same K steps launched eagerly through the C ABI (no graph)
     torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
     for i in range(args.steps):
-        dp = copies[i % len(copies)]
-        binding.sa_fused_decode_staged(dp.ia, dp.aa, K, idx, out, ws, [e.cuda_event for e in evs[i]], stream)
+        eager_step(i)
+    e1.record(stream)
     torch.cuda.synchronize()
-    stage_ms = {s: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)) / args.steps
-                for j, s in enumerate(STAGES)}
+    eager_ms_per_step = e0.elapsed_time(e1) / args.steps
+
+    # ---- per-stage device time: staged graphs, events between the stages
+    sums = {s_: 0.0 for s_ in STAGES}
+    for i in range(args.steps):
+        k = i % len(staged_graphs)
+        staged_graphs[k].replay()
+        torch.cuda.synchronize()
+        evs = stage_events[k]
+        for j, s_ in enumerate(STAGES):
+            sums[s_] += evs[j].elapsed_time(evs[j + 1])
+    stage_ms = {s_: sums[s_] / args.steps for s_ in STAGES}
     if binding.sa_check_device_status(ws) != binding.SA_OK:
         raise RuntimeError("device status not OK after the timed steps")
 
@@ -379,6 +419,10 @@ def run_ours(args):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "per-step query inputs copied from pinned host memory, index/KV caches resident"},
         "gpu_launches": launches_per_step * args.steps,
+        "launch": "CUDA graph replay of one sa_fused_decode call per step",
+        "eager": {"ms_per_step": round(eager_ms_per_step, 5),
+                  "value": w.T * world / (eager_ms_per_step / 1000.0),
+                  "note": "the same steps launched through the C ABI without a graph"},
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

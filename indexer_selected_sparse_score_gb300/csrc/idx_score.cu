@@ -119,8 +119,8 @@ cudaError_t launch_simt(const sa_index_args &ia, float *scores, int64_t ld, bool
   auto kern = idx_score_simt_kernel<DI, QFP8, KFP8>;
   const size_t smem = (static_cast<size_t>(ia.H_I) * DI + ia.H_I) * sizeof(float);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    static bool attr_done[64] = {};
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), 64 * 1024 + 1024, attr_done);
     if (e != cudaSuccess) return e;
   }
   dim3 grid((ia.N_c + kScoreThreads - 1) / kScoreThreads, ia.T);

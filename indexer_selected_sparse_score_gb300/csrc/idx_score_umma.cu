@@ -385,7 +385,8 @@ cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld,
   ScoreParams sp{ia.B, ia.T, ia.N_c, ia.r, ia.q_seq, ia.q_pos, qpack, wq, ia.k_scale, scores, ld, status};
   auto kern = idx_score_umma_kernel<NH, P>;
   const size_t smem = L::total + 1024;  // + alignment slack for the 1024-byte swizzle atoms
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  static bool attr_done[64] = {};
+  e = set_smem_once(reinterpret_cast<const void *>(kern), smem, attr_done);
   if (e != cudaSuccess) return e;
   kern<<<sm_count(), kMainThreads, smem, stream>>>(kmap, sp);
   return cudaGetLastError();
@@ -408,10 +409,24 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 int sm_count() {
-  int dev = 0, n = 0;
+  static int cached[64] = {};
+  int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
   return n;
+}
+
+cudaError_t set_smem_once(const void *func, size_t bytes, bool *done_per_device) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done_per_device[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done_per_device[dev] = true;
+  return e;
 }
 
 bool idx_score_umma_supported(const sa_index_args &ia) {

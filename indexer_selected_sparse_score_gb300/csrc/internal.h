@@ -27,6 +27,9 @@ struct WsLayout {
 // current device's SM count.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 int sm_count();
+// Sets a kernel's dynamic shared-memory limit once per device (flag array of
+// 64 devices owned by the caller).
+cudaError_t set_smem_once(const void *func, size_t bytes, bool *done_per_device);
 WsLayout ws_layout(const sa_index_args &ia, const sa_attn_args *aa, int K);
 
 // Index scores.  `scratch` (idx_score_scratch(ia) bytes, 256-byte aligned)

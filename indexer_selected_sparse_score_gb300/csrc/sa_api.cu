@@ -232,7 +232,10 @@ static sa_status fused_impl(const sa_index_args *ia, const sa_attn_args *aa, int
   if (sa_status s = check_ws(ws, ws_bytes, L.total)) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   auto mark = [&](int i) -> cudaError_t {
-    return ev ? cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st) : cudaSuccess;
+    // external record nodes: the events are really recorded when the call is
+    // captured into a CUDA graph and replayed
+    return ev ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev[i]), st, cudaEventRecordExternal)
+              : cudaSuccess;
   };
   uint32_t *status = at<uint32_t>(ws, 0);
   float *scores = at<float>(ws, L.scores);

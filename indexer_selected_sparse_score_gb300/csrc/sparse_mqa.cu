@@ -236,8 +236,8 @@ template <int H, int D>
 cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
   auto kern = sparse_mqa_simt_kernel<H, D>;
   constexpr size_t smem = attn_smem_bytes<H, D>();
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  static bool attr_done[64] = {};
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), smem, attr_done);
   if (e != cudaSuccess) return e;
   dim3 grid(p.splits, p.T);
   kern<<<grid, kAttnThreads, smem, stream>>>(p);

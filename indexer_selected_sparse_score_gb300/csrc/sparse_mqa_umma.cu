@@ -20,8 +20,11 @@
 // instruction) into the 128-byte-swizzled layout both MMAs read.
 //
 // Warps: 0, 1, 4, 5 softmax (heads 0-31 / 32-63 x key halves 0-63 / 64-127);
-// 2 producer (row ids, gathers, per-token Q); 3 MMA issuer and tensor-memory
-// owner.  A token whose tiles all fall in one CTA is finished there; a token
+// 3 MMA issuer and tensor-memory owner; 2 and 6-11 producers: each of these
+// seven warps resolves the rows of its share of a tile's 128 gather4 copies
+// and issues them (one warp alone issues gathers at well under the HBM rate,
+// seven together come close to it); warp 2 also loads each token's Q and
+// writes the tile's key mask.  A token whose tiles all fall in one CTA is finished there; a token
 // split across CTAs leaves one (m, l, O) record per piece for the combine
 // kernel.  Every wait is bounded; on expiry the kernel flags the status word,
 // drains its copies and MMAs, and returns.
@@ -40,7 +43,8 @@ constexpr int kH = 64;            // query heads handled by this kernel
 constexpr int kD = 128;           // head dim
 constexpr int kTile = 128;        // keys per tile
 constexpr int kStages = 2;        // K/V tile stages
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
+constexpr int kGatherWarps = 7;   // warp 2 and warps 6..11
 constexpr float kLazyRescale = 8.f;  // log2 units
 constexpr int kRecFloats = 2 * kH + kH * kD;
 
@@ -154,7 +158,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
     reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&kvfull[i], 1);
+      mbar_init(&kvfull[i], kGatherWarps);
       mbar_init(&kvempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -188,10 +192,11 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
   };
   auto aborted = [&]() { return *reinterpret_cast<volatile int *>(abort_s) != 0; };
 
-  if (warp == 2) {
-    // ---------------------------------------------------------------- producer
+  if (warp == 2 || warp >= 6) {
+    // --------------------------------------------------------------- producers
+    const int pw = (warp == 2) ? 0 : warp - 5;  // 0 .. 6
     if (begin < end) {
-      if (lane == 0) {
+      if (warp == 2 && lane == 0) {
         prefetch_tmap(&qmap);
         prefetch_tmap(&kwmap);
         prefetch_tmap(&vwmap);
@@ -202,91 +207,95 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
       Token tk{0, 0, 0};
       bool tok_ok = false;
       int n_w = 0;
+      // the key of slot kk (0..127) of tile j: its row and whether it exists
+      auto resolve = [&](int t, int j, int kk, int &row) -> bool {
+        if (!tok_ok) return false;
+        if (j < p.WT) {
+          const int q = j * kTile + kk;
+          if (q >= n_w) return false;
+          const int pos = tk.pos - n_w + 1 + q;
+          row = tk.b * p.R + pos % p.R;
+          return true;
+        }
+        const int k = (j - p.WT) * kTile + kk;
+        if (k >= p.K) return false;
+        const int cidx = p.idx[static_cast<int64_t>(t) * p.K + k];
+        if (cidx >= 0 && cidx < tk.nv) {
+          row = tk.b * p.N_c + cidx;
+          return true;
+        }
+        if (cidx != -1 && warp == 2) raise_flag(p.status, kFlagBadIndex);
+        return false;
+      };
       for (int i = begin; i < end && !aborted(); ++i) {
         const int t = i / p.TPT, j = i % p.TPT, n = i - begin;
         if (t != prev_t) {
-          tok_ok = load_token(p.q_seq, p.q_pos, t, p.B, p.N_c, p.r, p.status, tk, lane == 0 && j == 0);
+          tok_ok = load_token(p.q_seq, p.q_pos, t, p.B, p.N_c, p.r, p.status, tk,
+                              warp == 2 && lane == 0 && j == 0);
           n_w = tok_ok ? min(p.W, tk.pos + 1) : 0;
           ++qn;
-          const int qb = qn & 1;
-          bool ok = true;
-          if (lane == 0) {
-            ok = mbar_wait(&qempty[qb], ((qn >> 1) & 1) ^ 1);
-            if (ok) {
-              mbar_expect_tx(&qfull[qb], 2 * kH * 128);
-              tma_load_2d(qs + qb * 32768, &qmap, &qfull[qb], 0, t * kH);
-              tma_load_2d(qs + qb * 32768 + 16384, &qmap, &qfull[qb], 64, t * kH);
-            } else {
-              fail();
+          if (warp == 2) {
+            const int qb = qn & 1;
+            bool ok = true;
+            if (lane == 0) {
+              ok = mbar_wait(&qempty[qb], ((qn >> 1) & 1) ^ 1);
+              if (ok) {
+                mbar_expect_tx(&qfull[qb], 2 * kH * 128);
+                tma_load_2d(qs + qb * 32768, &qmap, &qfull[qb], 0, t * kH);
+                tma_load_2d(qs + qb * 32768 + 16384, &qmap, &qfull[qb], 64, t * kH);
+              } else {
+                fail();
+              }
             }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
           }
-          if (!__shfl_sync(0xffffffffu, ok, 0)) break;
           prev_t = t;
         }
         const int s = n % kStages;
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait(&kvempty[s], ((n / kStages) & 1) ^ 1);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        if (!mbar_wait_warp(&kvempty[s], ((n / kStages) & 1) ^ 1)) {
           if (lane == 0) fail();
           break;
         }
-        // row ids of keys 4*lane .. 4*lane+3 of this tile
         const bool window = j < p.WT;
-        int rows[4];
-        bool valid[4];
+        if (warp == 2) {  // key mask of the tile: bit g of word e = key 4g+e exists
+          int row_unused = 0;
+          uint32_t m4[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          valid[e] = false;
-          rows[e] = 0;
-          if (!tok_ok) continue;
-          if (window) {
-            const int kk = j * kTile + 4 * lane + e;
-            if (kk < n_w) {
-              const int pos = tk.pos - n_w + 1 + kk;
-              rows[e] = tk.b * p.R + pos % p.R;
-              valid[e] = true;
-            }
-          } else {
-            const int k = (j - p.WT) * kTile + 4 * lane + e;
-            if (k < p.K) {
-              const int cidx = p.idx[static_cast<int64_t>(t) * p.K + k];
-              if (cidx >= 0 && cidx < tk.nv) {
-                rows[e] = tk.b * p.N_c + cidx;
-                valid[e] = true;
-              } else if (cidx != -1) {
-                raise_flag(p.status, kFlagBadIndex);
-              }
-            }
+          for (int e = 0; e < 4; ++e) m4[e] = __ballot_sync(0xffffffffu, resolve(t, j, 4 * lane + e, row_unused));
+          if (lane == 0) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mask_s[s * 4 + e] = m4[e];
           }
         }
-        const bool any = valid[0] || valid[1] || valid[2] || valid[3];
-        int fill = valid[0] ? rows[0] : valid[1] ? rows[1] : valid[2] ? rows[2] : rows[3];
+        // this warp's share of the 128 copies: copy c = (part, group), part =
+        // K lo / K hi / V lo / V hi, group g = keys 4g..4g+3
+        uint32_t bytes = 0;
+        const int c0 = lane * kGatherWarps + pw;
+        int rows[4] = {0, 0, 0, 0};
+        bool any = false;
+        if (c0 < 128) {
+          const int g = c0 & 31;
+          bool valid[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (!valid[e]) rows[e] = fill;
-        uint32_t m4[4];
+          for (int e = 0; e < 4; ++e) valid[e] = resolve(t, j, 4 * g + e, rows[e]);
+          any = valid[0] || valid[1] || valid[2] || valid[3];
+          const int fill = valid[0] ? rows[0] : valid[1] ? rows[1] : valid[2] ? rows[2] : rows[3];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) m4[e] = __ballot_sync(0xffffffffu, valid[e]);
-        const uint32_t groups = __popc(__ballot_sync(0xffffffffu, any));
-        if (lane == 0) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) mask_s[s * 4 + e] = m4[e];
-          mbar_expect_tx(&kvfull[s], groups * 4 * 256 * 2);
+          for (int e = 0; e < 4; ++e)
+            if (!valid[e]) rows[e] = fill;
         }
+        bytes = __popc(__ballot_sync(0xffffffffu, any)) * 512u;
+        if (lane == 0) mbar_expect_tx(&kvfull[s], bytes);
         __syncwarp();
         if (any) {
-          const CUtensorMap *km = window ? &kwmap : &kcmap;
-          const CUtensorMap *vm = window ? &vwmap : &vcmap;
-          uint8_t *kd = ks + s * 32768 + 4 * lane * 128;
-          uint8_t *vd = vs + s * 32768 + 4 * lane * 128;
-          gather4(kd, km, &kvfull[s], 0, rows[0], rows[1], rows[2], rows[3]);
-          gather4(kd + 16384, km, &kvfull[s], 64, rows[0], rows[1], rows[2], rows[3]);
-          gather4(vd, vm, &kvfull[s], 0, rows[0], rows[1], rows[2], rows[3]);
-          gather4(vd + 16384, vm, &kvfull[s], 64, rows[0], rows[1], rows[2], rows[3]);
+          const int g = c0 & 31, part = c0 >> 5;
+          const CUtensorMap *map = (part < 2) ? (window ? &kwmap : &kcmap) : (window ? &vwmap : &vcmap);
+          uint8_t *dst = ((part < 2) ? ks : vs) + s * 32768 + (part & 1) * 16384 + 4 * g * 128;
+          gather4(dst, map, &kvfull[s], (part & 1) * 64, rows[0], rows[1], rows[2], rows[3]);
         }
         ++issued;
       }
-      if (lane == 0) {  // drain: every issued copy lands before the CTA exits
+      if (warp == 2 && lane == 0) {  // drain: every issued copy lands before the CTA exits
         for (int n = max(0, issued - kStages); n < issued; ++n) mbar_wait(&kvfull[n % kStages], (n / kStages) & 1);
         for (int q = max(0, qn - 1); q <= qn; ++q) mbar_wait(&qfull[q & 1], (q >> 1) & 1);
       }
@@ -542,10 +551,11 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
   }
 }
 
-// Merges the records of every token split across CTAs:
-// out = sum_r 2^(m_r - M) O_r / (sum_r 2^(m_r - M) l_r + 2^(sink - M)).
+// Merges the records of every token split across CTAs, one block per
+// (token, head): out = sum_r 2^(m_r - M) O_r / (sum_r 2^(m_r - M) l_r +
+// 2^(sink - M)).
 __global__ void __launch_bounds__(kD) attn_umma_combine_kernel(const AttnUmmaParams p, int G) {
-  const int t = blockIdx.x, d = threadIdx.x;
+  const int t = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
   const long long total = static_cast<long long>(p.T) * p.TPT;
   const long long first_tile = static_cast<long long>(t) * p.TPT, last_tile = first_tile + p.TPT - 1;
   auto cta_of = [&](long long i) {
@@ -556,26 +566,21 @@ __global__ void __launch_bounds__(kD) attn_umma_combine_kernel(const AttnUmmaPar
   };
   const int c0 = cta_of(first_tile), c1 = cta_of(last_tile);
   if (c0 == c1) return;  // finished inside one CTA
-  for (int h = 0; h < kH; ++h) {
-    float M = p.sink ? p.sink[h] * kLog2e : -INFINITY;
+  auto slot_of = [&](int cc) { return (cc == c0 && tile_begin(total, cc, G) < first_tile) ? 1 : 0; };
+  float M = p.sink ? p.sink[h] * kLog2e : -INFINITY;
+  for (int cc = c0; cc <= c1; ++cc) M = fmaxf(M, record(p, cc, slot_of(cc))[h]);
+  float o = 0.f;
+  if (M != -INFINITY) {
+    float Lden = p.sink ? exp2f(p.sink[h] * kLog2e - M) : 0.f, acc = 0.f;
     for (int cc = c0; cc <= c1; ++cc) {
-      const int slot = (cc == c0 && tile_begin(total, cc, G) < first_tile) ? 1 : 0;
-      M = fmaxf(M, record(p, cc, slot)[h]);
+      const float *rec = record(p, cc, slot_of(cc));
+      const float a = exp2f(rec[h] - M);
+      Lden = fmaf(a, rec[kH + h], Lden);
+      acc = fmaf(a, rec[2 * kH + h * kD + d], acc);
     }
-    float o = 0.f;
-    if (M != -INFINITY) {
-      float Lden = p.sink ? exp2f(p.sink[h] * kLog2e - M) : 0.f, acc = 0.f;
-      for (int cc = c0; cc <= c1; ++cc) {
-        const int slot = (cc == c0 && tile_begin(total, cc, G) < first_tile) ? 1 : 0;
-        const float *rec = record(p, cc, slot);
-        const float a = exp2f(rec[h] - M);
-        Lden = fmaf(a, rec[kH + h], Lden);
-        acc = fmaf(a, rec[2 * kH + h * kD + d], acc);
-      }
-      o = Lden > 0.f ? acc / Lden : 0.f;
-    }
-    p.out[(static_cast<int64_t>(t) * kH + h) * kD + d] = __float2bfloat16_rn(o);
+    o = Lden > 0.f ? acc / Lden : 0.f;
   }
+  p.out[(static_cast<int64_t>(t) * kH + h) * kD + d] = __float2bfloat16_rn(o);
 }
 
 bool encode_rows(CUtensorMap *m, const void *base, uint64_t rows, uint32_t box_rows) {
@@ -635,13 +640,13 @@ cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &
     return cudaErrorInvalidValue;
   const int G = attn_umma_grid(ia, aa, K);
   const size_t smem = AttnSmem::total + 1024;
-  cudaError_t e = cudaFuncSetAttribute(sparse_mqa_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  static bool attr_done[64] = {};
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(sparse_mqa_umma_kernel), smem, attr_done);
   if (e != cudaSuccess) return e;
   sparse_mqa_umma_kernel<<<G, kThreads, smem, stream>>>(qmap, kwmap, vwmap, kcmap, vcmap, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_umma_combine_kernel<<<ia.T, kD, 0, stream>>>(p, G);
+  attn_umma_combine_kernel<<<dim3(ia.T, kH), kD, 0, stream>>>(p, G);
   return cudaGetLastError();
 }
 
