@@ -3,10 +3,12 @@
 // picks re-sorted into position order, -1 for unreachable picks).
 //
 // One CTA per query token.  The k-th largest score is found exactly by a
-// most-significant-digit-first radix select over order-preserving 32-bit keys
-// (four 8-bit digits), then one ordered compaction pass writes every position
-// whose key is above that threshold plus the lowest-positioned ones equal to
-// it, so ties go to the lower position and the output comes out ascending.
+// most-significant-digit-first radix select over order-preserving 32-bit keys,
+// then an ordered compaction writes every position whose key is above that
+// threshold plus the lowest-positioned ones equal to it, so ties go to the
+// lower position and the output comes out ascending.  Rows of up to 32768
+// scores are held in registers (topk_reg_kernel); longer rows stream from
+// global memory in four 8-bit passes (topk_radix_kernel).
 #include "common.cuh"
 #include "internal.h"
 
@@ -125,13 +127,171 @@ topk_radix_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, 
   }
 }
 
+// ---------------------------------------------------------------------------
+// Register-resident variant for rows of up to kRegMax scores: each thread
+// holds a contiguous block of E = ceil(n / 1024) keys, the K-th largest key is
+// found by three radix passes of 11, 11 and 10 bits (warp-aggregated
+// shared-memory histograms, one block-wide scan each), and the output offsets
+// come from a single block scan of packed (greater, equal) counts: the number
+// of picks before a thread is greater_before + min(equal_before, needed).
+
+constexpr int kRegMax = 32768;
+constexpr int kRegE = kRegMax / kTopkThreads;  // 32 keys per thread at most
+
+// Block-wide exclusive scan of one uint32 per thread; returns the prefix and
+// writes the total to *total.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_sums, uint32_t *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = warp_sums[lane];
+    uint32_t wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    warp_sums[lane] = wi - w;        // exclusive prefix of the warp totals
+    if (lane == 31) warp_sums[32] = wi;
+  }
+  __syncthreads();
+  const uint32_t r = warp_sums[warp] + incl - v;
+  *total = warp_sums[32];
+  __syncthreads();
+  return r;
+}
+
+// One radix pass: histogram of digit (key >> shift) & (nbins-1) over the keys
+// that match `prefix` under `mask`, then locate the bin holding the
+// `remaining`-th largest.  Returns the digit; `remaining` becomes the rank
+// within that bin.
+template <int E>
+__device__ __forceinline__ uint32_t radix_pass(const uint32_t (&key)[E], int cnt, uint32_t prefix, uint32_t mask,
+                                               int shift, int nbins, uint32_t *hist, uint32_t *warp_sums,
+                                               int &remaining) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  for (int i = tid; i < nbins; i += kTopkThreads) hist[i] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const bool in = e < cnt && (key[e] & mask) == prefix;
+    const uint32_t active = __ballot_sync(0xffffffffu, in);
+    if (in) {
+      const uint32_t bin = (key[e] >> shift) & static_cast<uint32_t>(nbins - 1);
+      const uint32_t peers = __match_any_sync(active, bin);
+      if ((__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], __popc(peers));
+    }
+  }
+  __syncthreads();
+  // bins in descending order: thread t owns ranks r = 2t, 2t+1 (bin = nbins-1-r)
+  uint32_t c0 = 0, c1 = 0;
+  const int r0 = 2 * tid;
+  if (r0 < nbins) c0 = hist[nbins - 1 - r0];
+  if (r0 + 1 < nbins) c1 = hist[nbins - 2 - r0];
+  uint32_t total;
+  const uint32_t before = block_excl_scan(c0 + c1, warp_sums, &total);
+  __shared__ uint32_t sel_digit, sel_above;
+  const uint32_t rem = static_cast<uint32_t>(remaining);
+  if (before < rem && rem <= before + c0 + c1) {
+    if (rem <= before + c0) {
+      sel_digit = nbins - 1 - r0;
+      sel_above = before;
+    } else {
+      sel_digit = nbins - 2 - r0;
+      sel_above = before + c0;
+    }
+  }
+  __syncthreads();
+  remaining -= static_cast<int>(sel_above);
+  const uint32_t d = sel_digit;
+  __syncthreads();
+  return d;
+}
+
+template <int E>
+__global__ void __launch_bounds__(kTopkThreads)
+topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, int r,
+                const int32_t *__restrict__ q_seq, const int32_t *__restrict__ q_pos, int K,
+                int32_t *__restrict__ idx, uint32_t *status) {
+  __shared__ uint32_t hist[2048];
+  __shared__ uint32_t warp_sums[33];
+  const int t = blockIdx.x, tid = threadIdx.x;
+  Token tk;
+  const bool ok = load_token(q_seq, q_pos, t, B, N_c, r, status, tk, tid == 0);
+  const int nv = ok ? tk.nv : 0;
+  int32_t *out = idx + static_cast<int64_t>(t) * K;
+  if (nv <= K) {  // every visible position is kept
+    for (int i = tid; i < K; i += kTopkThreads) out[i] = i < nv ? i : -1;
+    return;
+  }
+  const float *row = scores + static_cast<int64_t>(t) * ld;
+  const int per = (nv + kTopkThreads - 1) / kTopkThreads;  // <= E
+  const int lo = tid * per;
+  const int cnt = max(0, min(per, nv - lo));
+  uint32_t key[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) key[e] = e < cnt ? ordered_key(row[lo + e]) : 0u;
+
+  int remaining = K;
+  const uint32_t d1 = radix_pass<E>(key, cnt, 0u, 0u, 21, 2048, hist, warp_sums, remaining);
+  const uint32_t p1 = d1 << 21, m1 = 0xFFE00000u;
+  const uint32_t d2 = radix_pass<E>(key, cnt, p1, m1, 10, 2048, hist, warp_sums, remaining);
+  const uint32_t p2 = p1 | (d2 << 10), m2 = 0xFFFFFC00u;
+  const uint32_t d3 = radix_pass<E>(key, cnt, p2, m2, 0, 1024, hist, warp_sums, remaining);
+  const uint32_t thr = p2 | d3;
+  const uint32_t need_eq = static_cast<uint32_t>(remaining);
+
+  uint32_t gt = 0, eq = 0;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if (e < cnt) {
+      gt += key[e] > thr;
+      eq += key[e] == thr;
+    }
+  }
+  uint32_t tot;
+  const uint32_t pre = block_excl_scan((gt << 16) | eq, warp_sums, &tot);
+  const uint32_t gt_before = pre >> 16, eq_before = pre & 0xFFFFu;
+  uint32_t pos = gt_before + min(eq_before, need_eq);
+  uint32_t eq_seen = eq_before;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if (e < cnt) {
+      bool take = key[e] > thr;
+      if (key[e] == thr) {
+        take = eq_seen < need_eq;
+        ++eq_seen;
+      }
+      if (take && pos < static_cast<uint32_t>(K)) out[pos++] = lo + e;
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const float *scores, int64_t ld, const sa_index_args &ia, int K,
                         int32_t *idx, uint32_t *status, cudaStream_t stream) {
   if (ia.T == 0 || K == 0) return cudaSuccess;
-  topk_radix_kernel<<<ia.T, kTopkThreads, 0, stream>>>(scores, ld, ia.B, ia.N_c, ia.r, ia.q_seq,
-                                                       ia.q_pos, K, idx, status);
+  // a row holds at most N_c visible scores
+  if (ia.N_c <= kRegMax / 4)
+    topk_reg_kernel<kRegE / 4><<<ia.T, kTopkThreads, 0, stream>>>(scores, ld, ia.B, ia.N_c, ia.r, ia.q_seq,
+                                                                   ia.q_pos, K, idx, status);
+  else if (ia.N_c <= kRegMax / 2)
+    topk_reg_kernel<kRegE / 2><<<ia.T, kTopkThreads, 0, stream>>>(scores, ld, ia.B, ia.N_c, ia.r, ia.q_seq,
+                                                                   ia.q_pos, K, idx, status);
+  else if (ia.N_c <= kRegMax)
+    topk_reg_kernel<kRegE><<<ia.T, kTopkThreads, 0, stream>>>(scores, ld, ia.B, ia.N_c, ia.r, ia.q_seq,
+                                                               ia.q_pos, K, idx, status);
+  else
+    topk_radix_kernel<<<ia.T, kTopkThreads, 0, stream>>>(scores, ld, ia.B, ia.N_c, ia.r, ia.q_seq,
+                                                         ia.q_pos, K, idx, status);
   return cudaGetLastError();
 }
 

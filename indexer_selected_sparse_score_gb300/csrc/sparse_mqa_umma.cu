@@ -42,7 +42,7 @@ using namespace umma;
 constexpr int kH = 64;            // query heads handled by this kernel
 constexpr int kD = 128;           // head dim
 constexpr int kTile = 128;        // keys per tile
-constexpr int kStages = 2;        // K/V tile stages
+constexpr int kStages = 3;        // K/V tile stages
 constexpr int kThreads = 384;
 constexpr int kGatherWarps = 7;   // warp 2 and warps 6..11
 constexpr float kLazyRescale = 8.f;  // log2 units
@@ -50,11 +50,15 @@ constexpr int kRecFloats = 2 * kH + kH * kD;
 
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP = 384;  // tensor-memory columns
 
+// Q: two token buffers of 64 rows share one 32 KB region, [kblk][buf][64 rows
+// x 128 B]: the MMA reads 128 rows (M = 128) from each buffer's base, and rows
+// 64..127 (the other buffer, or the first K stage right after) only feed the
+// unused accumulator rows 64..127.
 struct AttnSmem {
-  static constexpr size_t k = 0;                                   // [stage][2 kblk][128 rows][128 B]
+  static constexpr size_t q = 0;                                   // [2 kblk][2 buf][64 rows][128 B]
+  static constexpr size_t k = q + 32768;                           // [stage][2 kblk][128 rows][128 B]
   static constexpr size_t v = k + kStages * 32768;
-  static constexpr size_t q = v + kStages * 32768;                 // [2 buf][2 kblk][128 rows][128 B]
-  static constexpr size_t mask = q + 2 * 32768;                    // [stage][4] u32
+  static constexpr size_t mask = v + kStages * 32768;              // [stage][4] u32
   static constexpr size_t xchg = mask + kStages * 4 * 4;           // [2 parity][2 halves][64] f32
   static constexpr size_t bars = (xchg + 4 * kH * 4 + 7) & ~size_t(7);
   static constexpr int kBars = 2 * kStages + 4 + 4 + 2 + 2 + 1 + 2;
@@ -104,6 +108,14 @@ __device__ __forceinline__ void gather4(void *dst, const CUtensorMap *map, uint6
       " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
       : "memory");
+}
+
+// 2^x by the hardware approximation (relative error about 2^-22; results
+// below 2^-126 flush to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // MN-major 128-byte-swizzled operand: rows = K (8-row atoms 1024 B apart),
@@ -156,6 +168,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
   // zero the operand buffers once: rows never written by a copy stay finite
   for (int i = tid; i < static_cast<int>(L::mask / 16); i += kThreads)
     reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
+  static_assert(L::total + 1024 <= 232448, "shared memory budget");
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&kvfull[i], kGatherWarps);
@@ -241,8 +254,8 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
               ok = mbar_wait(&qempty[qb], ((qn >> 1) & 1) ^ 1);
               if (ok) {
                 mbar_expect_tx(&qfull[qb], 2 * kH * 128);
-                tma_load_2d(qs + qb * 32768, &qmap, &qfull[qb], 0, t * kH);
-                tma_load_2d(qs + qb * 32768 + 16384, &qmap, &qfull[qb], 64, t * kH);
+                tma_load_2d(qs + qb * 8192, &qmap, &qfull[qb], 0, t * kH);
+                tma_load_2d(qs + 16384 + qb * 8192, &qmap, &qfull[qb], 64, t * kH);
               } else {
                 fail();
               }
@@ -302,67 +315,80 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
     }
   } else if (warp == 3) {
     // ------------------------------------------------------------- MMA issuer
+    // Issues S for tile n+1 and P.V for tile n in whichever order their inputs
+    // become ready (polling), so P.V never waits for the next tile's data.
     if (lane == 0 && begin < end) {
       constexpr uint32_t idesc_s = idesc_bf16(128, kTile);              // K-major A, K-major B
       constexpr uint32_t idesc_o = idesc_bf16(128, kD) | (1u << 16);     // K-major A (tmem), MN-major B
       const int count = end - begin;
+      int ns = 0, np = 0;            // next S to issue, next P.V to issue
       int qn_s = -1, prev_t_s = -1;  // token ordinal as seen by the S stage
-      int sg = -1;                   // segment ordinal as seen by the PV stage
-      auto issue_s = [&](int n) -> bool {
-        const int i = begin + n, t = i / p.TPT, j = i % p.TPT;
-        if (t != prev_t_s) {
-          ++qn_s;
-          if (!mbar_wait(&qfull[qn_s & 1], (qn_s >> 1) & 1)) return false;
-          prev_t_s = t;
-        }
-        const int s = n % kStages, sb = n & 1;
-        if (!mbar_wait(&kvfull[s], (n / kStages) & 1)) return false;
-        if (!mbar_wait(&sempty[sb], ((n >> 1) & 1) ^ 1)) return false;
-        tc_fence_after();
-        const uint32_t a0 = smem_u32(qs + (qn_s & 1) * 32768), b0 = smem_u32(ks + s * 32768);
-        const uint32_t d = tmem + (sb ? kColS1 : kColS0);
+      int sg = -1;                   // segment ordinal as seen by the P.V stage
+      bool q_ready = false;
+      long long idle_since = clock64();
+      bool ok = true;
+      while (np < count) {
+        if (aborted()) { ok = false; break; }
+        bool progressed = false;
+        // ---- S(ns): Q of its token, its K tile and a free S buffer
+        if (ns < count && ns <= np + 1) {
+          const int i = begin + ns, t = i / p.TPT, j = i % p.TPT;
+          if (t != prev_t_s) {
+            if (!q_ready && mbar_try_wait(&qfull[(qn_s + 1) & 1], ((qn_s + 1) >> 1) & 1)) q_ready = true;
+          }
+          const bool q_ok = (t == prev_t_s) || q_ready;
+          const int s = ns % kStages, sb = ns & 1;
+          if (q_ok && mbar_try_wait(&kvfull[s], (ns / kStages) & 1) &&
+              mbar_try_wait(&sempty[sb], ((ns >> 1) & 1) ^ 1)) {
+            if (t != prev_t_s) {
+              ++qn_s;
+              prev_t_s = t;
+              q_ready = false;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(qs + (qn_s & 1) * 8192), b0 = smem_u32(ks + s * 32768);
+            const uint32_t d = tmem + (sb ? kColS1 : kColS0);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_f16(d, desc_sw128_kmajor(a0 + off), desc_sw128_kmajor(b0 + off), idesc_s, kk > 0);
-        }
-        mma_commit(&sfull[sb]);
-        const bool last_of_token = (j == p.TPT - 1) || (i == end - 1);
-        if (last_of_token) mma_commit(&qempty[qn_s & 1]);
-        return true;
-      };
-      bool ok = issue_s(0);
-      for (int n = 0; n < count && ok && !aborted(); ++n) {
-        if (n + 1 < count && !issue_s(n + 1)) {
-          ok = false;
-          break;
-        }
-        const int i = begin + n, j = i % p.TPT;
-        const bool first = (j == 0) || (n == 0);
-        const bool last = (j == p.TPT - 1) || (i == end - 1);
-        if (first) {
-          ++sg;
-          if (sg > 0 && !mbar_wait(oempty, (sg - 1) & 1)) {
-            ok = false;
-            break;
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+              mma_f16(d, desc_sw128_kmajor(a0 + off), desc_sw128_kmajor(b0 + off), idesc_s, kk > 0);
+            }
+            mma_commit(&sfull[sb]);
+            if ((j == p.TPT - 1) || (i == end - 1)) mma_commit(&qempty[qn_s & 1]);
+            ++ns;
+            progressed = true;
           }
         }
-        if (!mbar_wait(pfull, n & 1)) {
+        // ---- P.V(np): P from the softmax (and O read out after the previous segment)
+        if (np < ns) {
+          const int i = begin + np, j = i % p.TPT;
+          const bool first = (j == 0) || (np == 0);
+          const bool last = (j == p.TPT - 1) || (i == end - 1);
+          const bool o_ok = !first || sg < 0 || mbar_try_wait(oempty, sg & 1);
+          if (o_ok && mbar_try_wait(pfull, np & 1)) {
+            if (first) ++sg;
+            tc_fence_after();
+            const int s = np % kStages;
+            const uint32_t v0 = smem_u32(vs + s * 32768);
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_f16_ta(tmem + kColO, tmem + kColP + 64 * half + 8 * kk,
+                           desc_sw128_mnmajor(v0 + kk * 2048, 16384), idesc_o, !(first && half == 0 && kk == 0));
+            mma_commit(&kvempty[s]);
+            mma_commit(pempty);
+            if (last) mma_commit(ofull);
+            ++np;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          idle_since = clock64();
+        } else if (clock64() - idle_since > kWaitBudgetCycles) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const int s = n % kStages;
-        const uint32_t v0 = smem_u32(vs + s * 32768);
-#pragma unroll
-        for (int half = 0; half < 2; ++half)
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ta(tmem + kColO, tmem + kColP + 64 * half + 8 * kk,
-                       desc_sw128_mnmajor(v0 + kk * 2048, 16384), idesc_o, !(first && half == 0 && kk == 0));
-        mma_commit(&kvempty[s]);
-        mma_commit(pempty);
-        if (last) mma_commit(ofull);
       }
       if (!ok) fail();
       mma_commit(done);
@@ -405,7 +431,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         break;
       }
       tc_fence_after();
-      uint32_t v[64];
+      uint32_t v[64];  // raw dot products Q.K of this thread's head and keys
       tmem_ld_32x32b_x32(tmem + lane_base + (sb ? kColS1 : kColS0) + 64 * kh,
                          *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
       tmem_ld_32x32b_x32(tmem + lane_base + (sb ? kColS1 : kColS0) + 64 * kh + 32,
@@ -417,15 +443,23 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[sb]);
-      float x[64];
+      // Masked keys -> -inf.  The max runs on the raw dot products (the
+      // softmax scale is positive) and each logit is scaled and shifted by one
+      // FMA inside exp2.  Mask words stride by 4 keys: bit g of word e is key
+      // 4g+e; a half of the tile whose 16 groups are all present skips it.
       float mx = -INFINITY;
+      const uint32_t all4 = m4[0] & m4[1] & m4[2] & m4[3];
+      const uint32_t half_mask = kh ? 0xFFFF0000u : 0x0000FFFFu;
+      if ((all4 & half_mask) != half_mask) {
 #pragma unroll
-      for (int q = 0; q < 64; ++q) {
-        const int key = 64 * kh + q;
-        const bool valid = (m4[key & 3] >> (key >> 2)) & 1u;
-        x[q] = valid ? __uint_as_float(v[q]) * p.qk_scale : -INFINITY;
-        mx = fmaxf(mx, x[q]);
+        for (int q = 0; q < 64; ++q) {
+          const int key = 64 * kh + q;
+          if (!((m4[key & 3] >> (key >> 2)) & 1u)) v[q] = 0xFF800000u;  // -inf
+        }
       }
+#pragma unroll
+      for (int q = 0; q < 64; ++q) mx = fmaxf(mx, __uint_as_float(v[q]));
+      mx *= p.qk_scale;
       float other;
       if (!swap(mx, other)) {
         if (lane == 0) fail();
@@ -441,21 +475,26 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         m_ref = tile_max;
         rescale = true;
       }
+      // p = 2^(scale * s - m_ref); P = hi + lo with hi = p truncated to bf16
+      // and lo = (p - hi) truncated to bf16 (|p - hi - lo| < 2^-14 p), packed
+      // in pairs with byte permutes: no conversion instructions.
       float sum = 0.f;
       uint32_t phi[32], plo[32];
+      const float neg_m = -m_ref;
+      const bool live = m_ref != -INFINITY;
 #pragma unroll
       for (int q = 0; q < 32; ++q) {
         float pa = 0.f, pb = 0.f;
-        if (m_ref != -INFINITY) {
-          pa = exp2f(x[2 * q] - m_ref);
-          pb = exp2f(x[2 * q + 1] - m_ref);
+        if (live) {
+          pa = ex2_approx(fmaf(__uint_as_float(v[2 * q]), p.qk_scale, neg_m));
+          pb = ex2_approx(fmaf(__uint_as_float(v[2 * q + 1]), p.qk_scale, neg_m));
         }
         sum += pa + pb;
-        const __nv_bfloat16 ha = __float2bfloat16_rn(pa), hb = __float2bfloat16_rn(pb);
-        const __nv_bfloat16 la = __float2bfloat16_rn(pa - __bfloat162float(ha));
-        const __nv_bfloat16 lb = __float2bfloat16_rn(pb - __bfloat162float(hb));
-        phi[q] = static_cast<uint32_t>(__bfloat16_as_ushort(ha)) | (static_cast<uint32_t>(__bfloat16_as_ushort(hb)) << 16);
-        plo[q] = static_cast<uint32_t>(__bfloat16_as_ushort(la)) | (static_cast<uint32_t>(__bfloat16_as_ushort(lb)) << 16);
+        const uint32_t ua = __float_as_uint(pa), ub = __float_as_uint(pb);
+        const float la = pa - __uint_as_float(ua & 0xFFFF0000u);
+        const float lb = pb - __uint_as_float(ub & 0xFFFF0000u);
+        phi[q] = __byte_perm(ua, ub, 0x7632);
+        plo[q] = __byte_perm(__float_as_uint(la), __float_as_uint(lb), 0x7632);
       }
       l_part = l_part * factor + sum;
       // the previous P.V must be finished before P is overwritten or O rescaled

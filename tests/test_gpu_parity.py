@@ -106,18 +106,20 @@ def test_fused_without_idx_out(case):
     assert np.array_equal(g_out, g_out2)
 
 
-def test_topk_ties_and_sizes():
-    """Planted ties across chunk boundaries: exact match with the oracle's
-    lower-position tie rule."""
-    spec = wl.small("ties", B=5, T=5, r=1, N_c=5000, K=700, pos_mode="fixed", pos_lo=0, pos_hi=0)
-    w = wl.generate(spec, seed=77, positions=(np.arange(5, dtype=np.int32),
-                                              np.array([4999, 2500, 700, 699, 1500], dtype=np.int32)))
+@pytest.mark.parametrize("N_c", [5000, 12000, 30000, 40000])
+def test_topk_ties_and_sizes(N_c):
+    """Planted ties across chunk boundaries, for rows held in registers (up to
+    32768 scores, three block sizes) and rows streamed from memory: exact match
+    with the oracle's lower-position tie rule."""
+    spec = wl.small("ties", B=5, T=5, r=1, N_c=N_c, K=700, D=128, H=16, pos_mode="fixed", pos_lo=0, pos_hi=0)
+    pos = np.array([N_c - 1, N_c // 2, 700, 699, 1500], dtype=np.int32)
+    w = wl.generate(spec, seed=77, positions=(np.arange(5, dtype=np.int32), pos))
     rng = np.random.default_rng(8)
-    scores = np.round(rng.normal(size=(5, 5000)) * 4).astype(np.float32) / 4
+    scores = np.round(rng.normal(size=(5, N_c)) * 4).astype(np.float32) / 4
     scores[4, :] = 1.0  # a row of equal scores: the lowest positions win
     scores[3, 10:20] = -0.0
     idx = run_topk(w, scores, spec.K)
-    for t in range(5):
+    for t in range(5):  # noqa: B007
         nv = n_vis(int(w.q_pos[t]), w.r)
         ref = oracle.topk_row(scores[t].astype(np.float64), nv, spec.K)
         assert idx[t].tolist() == ref.tolist(), t
