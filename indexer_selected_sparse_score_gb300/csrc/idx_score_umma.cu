@@ -44,10 +44,12 @@ using namespace umma;
 
 constexpr int kTileKeys = 128;                   // M
 constexpr int kKeyTileBytes = kTileKeys * 128;   // 128 keys x 128 fp8
-constexpr int kStages = 6;
+constexpr int kStages = 8;
 constexpr int kAccStages = 4;
 constexpr int kMainThreads = 192;
-constexpr int kMaxTokens = 8192;                 // tile prefix kept in shared memory
+constexpr int kPrepThreads = 256;
+constexpr int kPlanPer = 32;  // tokens per thread per chunk of the plan scan
+constexpr int kPlanSmemTokens = 8192;
 
 template <int NH, int P>
 struct ScoreSmem {
@@ -55,9 +57,7 @@ struct ScoreSmem {
   static constexpr size_t keys = 0;
   static constexpr size_t qbuf = keys + static_cast<size_t>(kStages) * kKeyTileBytes;
   static constexpr size_t wq = qbuf + 2 * static_cast<size_t>(kQBytes);
-  static constexpr size_t prefix = wq + 2 * NH * sizeof(float);
-  static constexpr size_t part = prefix + (kMaxTokens + 1) * sizeof(int);
-  static constexpr size_t bars = (part + kMainThreads * sizeof(int) + 7) & ~static_cast<size_t>(7);
+  static constexpr size_t bars = wq + 2 * NH * sizeof(float);
   static constexpr int kBars = 2 * kStages + 4 + 2 * kAccStages + 1;
   static constexpr size_t misc = bars + kBars * sizeof(uint64_t);
   static constexpr size_t total = misc + 64;
@@ -65,32 +65,139 @@ struct ScoreSmem {
 
 // ---------------------------------------------------------------- prep ----
 
-// Packs token t's index queries into the K-major 128-byte-swizzled layout the
-// MMA reads (piece p, head h at rows p*H_I + h), writes the folded head
-// weights wq[t, h] = w * q_scale * 2^e, and (optionally) -inf into the
-// masked tail of the score row.
+__device__ __forceinline__ int tiles_of_token(int B, int N_c, int r, const int32_t *q_seq, const int32_t *q_pos,
+                                              int t) {
+  const int b = q_seq[t], pos = q_pos[t];
+  if (b < 0 || b >= B || pos < 0) return 0;
+  const int nv = min(n_vis_of(pos, r), N_c);
+  return (nv + kTileKeys - 1) / kTileKeys;
+}
+
+// Block-wide inclusive scan (kPrepThreads threads) of one int per thread.
+__device__ __forceinline__ int plan_block_scan(int v, int *warp_sums) {
+  constexpr int kWarps = kPrepThreads / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kWarps ? warp_sums[lane] : 0, wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    if (lane < kWarps) warp_sums[lane] = wi - w;
+  }
+  __syncthreads();
+  const int r = warp_sums[warp] + incl;
+  __syncthreads();
+  return r;
+}
+
+// Blocks 0..T-1: pack token t's index queries into the K-major
+// 128-byte-swizzled layout the MMA reads (piece p, head h at rows p*H_I + h),
+// write the folded head weights wq[t, h] = w * q_scale * 2^e, and (optionally)
+// -inf into the masked tail of the score row.
+// Block T: the work plan of the main kernel -- prefix[t] = key tiles of the
+// tokens before t (prefix[T] = all tiles) and start[c] = the token holding the
+// first tile of CTA c of `grid` (each CTA takes tiles [total*c/grid,
+// total*(c+1)/grid)).
 template <int NH, bool QFP8>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kPrepThreads)
 idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq,
                  const int32_t *__restrict__ q_pos, const void *__restrict__ q_I,
                  const float *__restrict__ q_scale, const float *__restrict__ w,
                  uint8_t *__restrict__ qpack, float *__restrict__ wq, float *__restrict__ scores,
-                 int64_t ld, int write_masked, uint32_t *status) {
+                 int64_t ld, int write_masked, int32_t *__restrict__ prefix, int32_t *__restrict__ start,
+                 int grid, uint32_t *status) {
   constexpr int P = QFP8 ? 1 : 2;
+  constexpr int kHeadsPerWarp = NH / (kPrepThreads / 32);
   const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (t == T) {
+    __shared__ int warp_sums[32];
+    __shared__ int carry;
+    __shared__ int pre_s[kPlanSmemTokens + 1];  // prefix kept on chip for the searches below
+    const bool on_chip = T <= kPlanSmemTokens;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < T; base += kPrepThreads * kPlanPer) {
+      const int t0 = base + threadIdx.x * kPlanPer;
+      int tl[kPlanPer];
+      int sum = 0;
+#pragma unroll
+      for (int k = 0; k < kPlanPer; ++k) {
+        tl[k] = (t0 + k < T) ? tiles_of_token(B, N_c, r, q_seq, q_pos, t0 + k) : 0;
+        sum += tl[k];
+      }
+      const int incl = plan_block_scan(sum, warp_sums);
+      int run = carry + incl - sum;
+#pragma unroll
+      for (int k = 0; k < kPlanPer; ++k) {
+        if (t0 + k < T) {
+          prefix[t0 + k] = run;
+          if (on_chip) pre_s[t0 + k] = run;
+        }
+        run += tl[k];
+      }
+      __syncthreads();
+      if (threadIdx.x == kPrepThreads - 1) carry += incl;
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+      prefix[T] = carry;
+      if (on_chip) pre_s[T] = carry;
+    }
+    __syncthreads();
+    const long long total = carry;
+    for (int c = threadIdx.x; c < grid; c += kPrepThreads) {
+      const long long first = total * c / grid;
+      int lo = 0, hi = T - 1;  // largest token whose prefix <= first
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((on_chip ? pre_s[mid] : prefix[mid]) <= first) lo = mid; else hi = mid - 1;
+      }
+      start[c] = lo;
+    }
+    return;
+  }
+
   uint8_t *dst = qpack + static_cast<size_t>(t) * P * NH * 128;
-  for (int h = warp; h < NH; h += 4) {
-    const int64_t qrow = (static_cast<int64_t>(t) * NH + h) * 128;
-    const float qsc = q_scale ? q_scale[static_cast<int64_t>(t) * NH + h] : 1.f;
-    const float wt = w[static_cast<int64_t>(t) * NH + h] * qsc;
-    if (QFP8) {
-      const uint32_t v = reinterpret_cast<const uint32_t *>(static_cast<const uint8_t *>(q_I) + qrow)[lane];
-      *reinterpret_cast<uint32_t *>(dst + umma::sw128_offset(h, 4 * lane)) = v;
-      if (lane == 0) wq[static_cast<int64_t>(t) * NH + h] = wt;
-    } else {
-      const uint2 raw = reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(q_I) + qrow)[lane];
-      float x[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
-                    __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
+  if (QFP8) {
+    uint32_t v[kHeadsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kHeadsPerWarp; ++i) {
+      const int h = warp + (kPrepThreads / 32) * i;
+      v[i] = reinterpret_cast<const uint32_t *>(static_cast<const uint8_t *>(q_I) +
+                                                (static_cast<int64_t>(t) * NH + h) * 128)[lane];
+    }
+#pragma unroll
+    for (int i = 0; i < kHeadsPerWarp; ++i) {
+      const int h = warp + (kPrepThreads / 32) * i;
+      *reinterpret_cast<uint32_t *>(dst + umma::sw128_offset(h, 4 * lane)) = v[i];
+      if (lane == 0) {
+        const float qsc = q_scale ? q_scale[static_cast<int64_t>(t) * NH + h] : 1.f;
+        wq[static_cast<int64_t>(t) * NH + h] = w[static_cast<int64_t>(t) * NH + h] * qsc;
+      }
+    }
+  } else {
+    uint2 raw[kHeadsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kHeadsPerWarp; ++i) {
+      const int h = warp + (kPrepThreads / 32) * i;
+      raw[i] = reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(q_I) +
+                                               (static_cast<int64_t>(t) * NH + h) * 128)[lane];
+    }
+#pragma unroll
+    for (int i = 0; i < kHeadsPerWarp; ++i) {
+      const int h = warp + (kPrepThreads / 32) * i;
+      const float x[4] = {__uint_as_float(raw[i].x << 16), __uint_as_float(raw[i].x & 0xFFFF0000u),
+                          __uint_as_float(raw[i].y << 16), __uint_as_float(raw[i].y & 0xFFFF0000u)};
       float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -103,17 +210,20 @@ idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq
       }
       uint32_t w1 = 0, w2 = 0;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float y = ldexpf(x[i], -e);
+      for (int k = 0; k < 4; ++k) {
+        const float y = ldexpf(x[k], -e);
         const __nv_fp8_storage_t p1 = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
         const float rest = y - e4m3_bits_to_float(p1);
         const __nv_fp8_storage_t p2 = __nv_cvt_float_to_fp8(rest, __NV_SATFINITE, __NV_E4M3);
-        w1 |= static_cast<uint32_t>(p1) << (8 * i);
-        w2 |= static_cast<uint32_t>(p2) << (8 * i);
+        w1 |= static_cast<uint32_t>(p1) << (8 * k);
+        w2 |= static_cast<uint32_t>(p2) << (8 * k);
       }
       *reinterpret_cast<uint32_t *>(dst + umma::sw128_offset(h, 4 * lane)) = w1;
       *reinterpret_cast<uint32_t *>(dst + NH * 128 + umma::sw128_offset(h, 4 * lane)) = w2;
-      if (lane == 0) wq[static_cast<int64_t>(t) * NH + h] = ldexpf(wt, e);
+      if (lane == 0) {
+        const float qsc = q_scale ? q_scale[static_cast<int64_t>(t) * NH + h] : 1.f;
+        wq[static_cast<int64_t>(t) * NH + h] = ldexpf(w[static_cast<int64_t>(t) * NH + h] * qsc, e);
+      }
     }
   }
   if (write_masked) {
@@ -121,7 +231,7 @@ idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq
     const bool ok = load_token(q_seq, q_pos, t, B, N_c, r, status, tk, threadIdx.x == 0);
     const int nv = ok ? tk.nv : 0;
     float *row = scores + static_cast<int64_t>(t) * ld;
-    for (int s = nv + threadIdx.x; s < N_c; s += 128) row[s] = -INFINITY;
+    for (int s2 = nv + threadIdx.x; s2 < N_c; s2 += kPrepThreads) row[s2] = -INFINITY;
   }
 }
 
@@ -130,6 +240,7 @@ idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq
 struct ScoreParams {
   int B, T, N_c, r;
   const int32_t *q_seq, *q_pos;
+  const int32_t *prefix, *start;  // work plan written by the prep kernel
   const uint8_t *qpack;
   const float *wq;
   const float *k_scale;
@@ -147,6 +258,30 @@ __device__ __forceinline__ int token_tiles(const ScoreParams &p, int t, int *b_o
   return (nv + kTileKeys - 1) / kTileKeys;
 }
 
+// Walks a CTA's tile range token by token; the token boundary and the
+// token's sequence / visible count are read from memory only when a token
+// starts, never per tile.
+struct TileCursor {
+  int t, first, next, b, nv;  // token, its first tile, first tile of the next token
+  __device__ void start(const ScoreParams &p, int t0) {
+    t = t0;
+    first = p.prefix[t];
+    next = p.prefix[t + 1];
+    token_tiles(p, t, &b, &nv);
+  }
+  // moves to the token holding tile i (i never decreases); true if it changed
+  __device__ bool seek(const ScoreParams &p, int i) {
+    if (i < next) return false;
+    do {
+      ++t;
+      first = next;
+      next = p.prefix[t + 1];
+    } while (i >= next);
+    token_tiles(p, t, &b, &nv);
+    return true;
+  }
+};
+
 template <int NH, int P>
 __global__ void __launch_bounds__(kMainThreads, 1)
 idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParams p) {
@@ -159,7 +294,6 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
   uint8_t *keys = smem + L::keys;
   uint8_t *qbuf = smem + L::qbuf;
   float *wqs = reinterpret_cast<float *>(smem + L::wq);
-  int *prefix = reinterpret_cast<int *>(smem + L::prefix);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bars);
   uint64_t *kfull = bars, *kempty = bars + kStages;
   uint64_t *qfull = bars + 2 * kStages, *qempty = qfull + 2;
@@ -170,29 +304,7 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // ---- set-up: tile prefix over tokens, barriers, tensor memory
-  {
-    const int per = (p.T + kMainThreads - 1) / kMainThreads;
-    const int t0 = tid * per, t1 = min(p.T, t0 + per);
-    int sum = 0;
-    for (int t = t0; t < t1; ++t) sum += token_tiles(p, t, nullptr, nullptr);
-    // inclusive scan of the per-thread sums across the block
-    int *part = reinterpret_cast<int *>(smem + L::part);
-    part[tid] = sum;
-    __syncthreads();
-    for (int o = 1; o < kMainThreads; o <<= 1) {
-      const int v = tid >= o ? part[tid - o] : 0;
-      __syncthreads();
-      part[tid] += v;
-      __syncthreads();
-    }
-    int run = part[tid] - sum;
-    for (int t = t0; t < t1; ++t) {
-      prefix[t] = run;
-      run += token_tiles(p, t, nullptr, nullptr);
-    }
-    if (tid == kMainThreads - 1) prefix[p.T] = part[tid];
-  }
+  // ---- set-up: barriers, tensor memory
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&kfull[i], 1);
@@ -219,19 +331,10 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
   tc_fence_after();
   const uint32_t tmem = *tmem_base_s;
 
-  const int total = prefix[p.T];
+  const int total = p.prefix[p.T];
   const int begin = static_cast<int>((static_cast<long long>(total) * blockIdx.x) / gridDim.x);
   const int end = static_cast<int>((static_cast<long long>(total) * (blockIdx.x + 1)) / gridDim.x);
-
-  // first token whose tiles contain `begin`
-  auto locate = [&](int i) {
-    int lo = 0, hi = p.T - 1;
-    while (lo < hi) {  // largest t with prefix[t] <= i
-      const int mid = (lo + hi + 1) >> 1;
-      if (prefix[mid] <= i) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-  };
+  const int t_first = p.start[blockIdx.x];  // token holding tile `begin`
   auto fail = [&]() {
     raise_flag(p.status, kFlagTimeout);
     atomicExch(abort_s, 1);
@@ -241,12 +344,14 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
     // ------------------------------------------------------ TMA producer
     if (lane == 0 && begin < end) {
       prefetch_tmap(&kmap);
-      int t = locate(begin), prev_t = -1, qn = -1, b = 0, nv = 0;
+      TileCursor cur;
+      cur.start(p, t_first);
+      int prev_t = -1, qn = -1;
       int issued = 0;
       for (int i = begin; i < end && !*(volatile int *)abort_s; ++i) {
-        while (prefix[t + 1] <= i) ++t;
+        cur.seek(p, i);
+        const int t = cur.t, b = cur.b;
         if (t != prev_t) {
-          token_tiles(p, t, &b, &nv);
           ++qn;
           const int qb = qn & 1;
           if (!mbar_wait(&qempty[qb], ((qn >> 1) & 1) ^ 1)) { fail(); break; }
@@ -255,7 +360,7 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
           bulk_load(wqs + qb * NH, p.wq + static_cast<size_t>(t) * NH, NH * 4, &qfull[qb]);
           prev_t = t;
         }
-        const int j = i - prefix[t];
+        const int j = i - cur.first;
         const int n = i - begin, s = n % kStages;
         if (!mbar_wait(&kempty[s], ((n / kStages) & 1) ^ 1)) { fail(); break; }
         mbar_expect_tx(&kfull[s], kKeyTileBytes);
@@ -271,9 +376,12 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
     // ------------------------------------------------------- MMA issuer
     if (lane == 0 && begin < end) {
       constexpr uint32_t idesc = idesc_e4m3(kTileKeys, NH);
-      int t = locate(begin), prev_t = -1, qn = -1;
+      TileCursor cur;
+      cur.start(p, t_first);
+      int prev_t = -1, qn = -1;
       for (int i = begin; i < end && !*(volatile int *)abort_s; ++i) {
-        while (prefix[t + 1] <= i) ++t;
+        cur.seek(p, i);
+        const int t = cur.t;
         if (t != prev_t) {
           if (qn >= 0) mma_commit(&qempty[qn & 1]);
           ++qn;
@@ -302,19 +410,36 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
     }
   } else {
     // --------------------------------------------------------- epilogue
+    // The key scales of the next tile are loaded while this tile is reduced
+    // (their latency would otherwise stall every tile).
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     if (begin < end) {
-      int t = locate(begin), prev_t = -1, qn = -1, b = 0, nv = 0;
+      TileCursor cur, ahead;  // `ahead` runs one tile in front for the scale prefetch
+      cur.start(p, t_first);
+      ahead.start(p, t_first);
+      int prev_t = -1, qn = -1;
+      auto scale_at = [&](const TileCursor &c, int ii) -> float {
+        const int ss = (ii - c.first) * kTileKeys + row;
+        if (!p.k_scale || ss >= c.nv) return 1.f;
+        return p.k_scale[static_cast<int64_t>(c.b) * p.N_c + ss];
+      };
+      float ks_next = scale_at(ahead, begin);
       for (int i = begin; i < end && !*(volatile int *)abort_s; ++i) {
-        while (prefix[t + 1] <= i) ++t;
+        cur.seek(p, i);
+        const int t = cur.t, b = cur.b, nv = cur.nv;
+        (void)b;
+        const float ks = ks_next;
+        if (i + 1 < end) {
+          ahead.seek(p, i + 1);
+          ks_next = scale_at(ahead, i + 1);
+        }
         if (t != prev_t) {
           if (qn >= 0) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&qempty[qn & 1]);
           }
           ++qn;
-          token_tiles(p, t, &b, &nv);
           if (!mbar_wait_warp(&qfull[qn & 1], (qn >> 1) & 1)) { fail(); break; }
           prev_t = t;
         }
@@ -330,14 +455,12 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&aempty[a]);
-        const int s = (i - prefix[t]) * kTileKeys + row;
+        const int s = (i - cur.first) * kTileKeys + row;
         if (s < nv) {
           const float *wv = wqs + (qn & 1) * NH;
           float acc = 0.f;
 #pragma unroll
           for (int h = 0; h < NH; ++h) acc = fmaf(wv[h], fmaxf(__uint_as_float(v[h]), 0.f), acc);
-          const int64_t krow = static_cast<int64_t>(b) * p.N_c + s;
-          const float ks = p.k_scale ? p.k_scale[krow] : 1.f;
           p.scores[static_cast<int64_t>(t) * p.ld + s] = acc * ks;
         }
       }
@@ -361,12 +484,14 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
 
 template <int NH, bool QFP8>
 cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld, bool write_masked,
-                             uint8_t *qpack, float *wq, uint32_t *status, cudaStream_t stream) {
+                             uint8_t *qpack, float *wq, int32_t *prefix, int32_t *start, uint32_t *status,
+                             cudaStream_t stream) {
   constexpr int P = QFP8 ? 1 : 2;
   using L = ScoreSmem<NH, P>;
-  idx_qprep_kernel<NH, QFP8><<<ia.T, 128, 0, stream>>>(ia.B, ia.T, ia.N_c, ia.r, ia.q_seq, ia.q_pos,
-                                                        ia.q_I, ia.q_scale, ia.w, qpack, wq, scores,
-                                                        ld, write_masked ? 1 : 0, status);
+  const int grid = sm_count();
+  idx_qprep_kernel<NH, QFP8><<<ia.T + 1, kPrepThreads, 0, stream>>>(
+      ia.B, ia.T, ia.N_c, ia.r, ia.q_seq, ia.q_pos, ia.q_I, ia.q_scale, ia.w, qpack, wq, scores, ld,
+      write_masked ? 1 : 0, prefix, start, grid, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -382,13 +507,14 @@ cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
-  ScoreParams sp{ia.B, ia.T, ia.N_c, ia.r, ia.q_seq, ia.q_pos, qpack, wq, ia.k_scale, scores, ld, status};
+  ScoreParams sp{ia.B, ia.T, ia.N_c, ia.r, ia.q_seq, ia.q_pos, prefix, start, qpack, wq, ia.k_scale, scores,
+                 ld, status};
   auto kern = idx_score_umma_kernel<NH, P>;
   const size_t smem = L::total + 1024;  // + alignment slack for the 1024-byte swizzle atoms
   static bool attr_done[64] = {};
   e = set_smem_once(reinterpret_cast<const void *>(kern), smem, attr_done);
   if (e != cudaSuccess) return e;
-  kern<<<sm_count(), kMainThreads, smem, stream>>>(kmap, sp);
+  kern<<<grid, kMainThreads, smem, stream>>>(kmap, sp);
   return cudaGetLastError();
 }
 
@@ -430,25 +556,41 @@ cudaError_t set_smem_once(const void *func, size_t bytes, bool *done_per_device)
 }
 
 bool idx_score_umma_supported(const sa_index_args &ia) {
-  return ia.k_dtype == SA_FP8_E4M3 && ia.D_I == 128 && (ia.H_I == 32 || ia.H_I == 64 || ia.H_I == 128) &&
-         ia.T <= kMaxTokens;
+  return ia.k_dtype == SA_FP8_E4M3 && ia.D_I == 128 && (ia.H_I == 32 || ia.H_I == 64 || ia.H_I == 128);
 }
 
-size_t idx_score_umma_scratch(const sa_index_args &ia) {
+namespace {
+struct UmmaScratch {
+  size_t qpack, wq, prefix, start, total;
+};
+UmmaScratch umma_scratch_layout(const sa_index_args &ia) {
   const int P = ia.q_dtype == SA_FP8_E4M3 ? 1 : 2;
-  return static_cast<size_t>(ia.T) * P * ia.H_I * 128 + static_cast<size_t>(ia.T) * ia.H_I * 4 + 256;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  UmmaScratch L{};
+  L.qpack = 0;
+  L.wq = up(static_cast<size_t>(ia.T) * P * ia.H_I * 128);
+  L.prefix = L.wq + up(static_cast<size_t>(ia.T) * ia.H_I * 4);
+  L.start = L.prefix + up(static_cast<size_t>(ia.T + 1) * 4);
+  L.total = L.start + up(static_cast<size_t>(sm_count() + 1) * 4);
+  return L;
 }
+}  // namespace
+
+size_t idx_score_umma_scratch(const sa_index_args &ia) { return umma_scratch_layout(ia).total; }
 
 cudaError_t launch_idx_score_umma(const sa_index_args &ia, float *scores, int64_t ld, bool write_masked,
                                   void *scratch, uint32_t *status, cudaStream_t stream) {
   if (ia.T == 0) return cudaSuccess;
-  const int P = ia.q_dtype == SA_FP8_E4M3 ? 1 : 2;
-  uint8_t *qpack = static_cast<uint8_t *>(scratch);
-  float *wq = reinterpret_cast<float *>(qpack + ((static_cast<size_t>(ia.T) * P * ia.H_I * 128 + 255) & ~size_t(255)));
+  const UmmaScratch L = umma_scratch_layout(ia);
+  uint8_t *base = static_cast<uint8_t *>(scratch);
+  uint8_t *qpack = base + L.qpack;
+  float *wq = reinterpret_cast<float *>(base + L.wq);
+  int32_t *prefix = reinterpret_cast<int32_t *>(base + L.prefix);
+  int32_t *start = reinterpret_cast<int32_t *>(base + L.start);
   const bool qf8 = ia.q_dtype == SA_FP8_E4M3;
-#define SA_UMMA_CASE(NH, QF)                                                                   \
-  if (ia.H_I == NH && qf8 == QF)                                                               \
-    return launch_umma_impl<NH, QF>(ia, scores, ld, write_masked, qpack, wq, status, stream);
+#define SA_UMMA_CASE(NH, QF)                                                                              \
+  if (ia.H_I == NH && qf8 == QF)                                                                          \
+    return launch_umma_impl<NH, QF>(ia, scores, ld, write_masked, qpack, wq, prefix, start, status, stream);
   SA_UMMA_CASE(32, false)
   SA_UMMA_CASE(32, true)
   SA_UMMA_CASE(64, false)

@@ -258,7 +258,7 @@ int fused_launch_count(const sa_index_args &ia, const sa_attn_args &aa, int K,
                        const SplitPlan &plan) {
   const int score = idx_score_umma_supported(ia) ? 2 : 1;  // (query packing +) scoring
   const int topk = K > 0 ? 1 : 0;
-  const int attn = attn_umma_supported(aa) ? 2 : (plan.splits > 1 ? 2 : 1);
+  const int attn = attn_umma_supported(aa) ? 1 : (plan.splits > 1 ? 2 : 1);
   return ia.T > 0 ? score + topk + attn : 0;
 }
 

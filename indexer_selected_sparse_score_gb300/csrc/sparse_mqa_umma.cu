@@ -4,30 +4,34 @@
 // and the index-selected compressed rows).
 //
 // Each token's key list is its window (padded to a multiple of 128) followed
-// by its K index slots (padded likewise); every token therefore has the same
-// number of 128-key tiles, and the persistent CTAs split the flattened
-// (token, tile) list evenly.  Per tile:
-//   S = Q K^T      M = 128 (the 64 heads; rows 64..127 unused), N = 128 keys,
-//                  K = 128, bf16 x bf16 -> f32 in tensor memory;
-//   softmax        one thread per (head, half of the keys), exp2 in fp32 with a
-//                  lazily raised running maximum (rescale O only when the
-//                  tile maximum exceeds the reference by more than 2^8);
-//   O += P V       P from tensor memory as a bf16 hi + lo pair (two MMAs into
-//                  the same accumulator, p = hi + lo to 2^-16), V read
-//                  MN-major from the gathered tile, M = 128, N = 128 (d),
-//                  K = 128 keys.
+// by its K index slots (padded likewise), i.e. TPT tiles of 128 keys.  Every
+// CTA takes whole tokens (a contiguous token range), so no token is split.
+// Per tile:
+//   S = Q K^T      M = 128, N = 128 keys, K = 128, bf16 x bf16 -> f32 in
+//                  tensor memory.  Head 16w+i (w = 0..3, i = 0..15) is A row
+//                  and accumulator lane 32w+i, so each quarter of tensor
+//                  memory (one per SM sub-partition) holds 16 heads; the
+//                  other 64 rows are not used;
+//   softmax        four warps, one per sub-partition; a thread takes one head
+//                  and 64 of the tile's 128 keys (the 16x32bx2 access shape:
+//                  threads 0-15 keys 0-63, threads 16-31 keys 64-127 of the
+//                  same 16 heads): the tile max, then p = 2^(scale s - m) with
+//                  a lazily raised reference max (O is rescaled only when a
+//                  tile's max exceeds it by more than 2^8);
+//   O += P V       P written over the logits it came from, as a bf16 hi + lo
+//                  pair (two MMAs into the same accumulator); V read MN-major
+//                  from the gathered tile; M = 128, N = 128 (d), K = 128 keys.
+// Three S/P buffers let S run two tiles ahead of P.V, so the softmax waits for
+// the tensor core only to rescale O and at a token's end.
 // K and V rows are gathered by index with TMA gather4 (4 rows of 128 bytes per
-// instruction) into the 128-byte-swizzled layout both MMAs read.
+// instruction) into the 128-byte-swizzled layout both MMAs read, in two
+// separate rings: a K slot is free once S is done, a V slot once P.V is done.
 //
-// Warps: 0, 1, 4, 5 softmax (heads 0-31 / 32-63 x key halves 0-63 / 64-127);
-// 3 MMA issuer and tensor-memory owner; 2 and 6-11 producers: each of these
-// seven warps resolves the rows of its share of a tile's 128 gather4 copies
-// and issues them (one warp alone issues gathers at well under the HBM rate,
-// seven together come close to it); warp 2 also loads each token's Q and
-// writes the tile's key mask.  A token whose tiles all fall in one CTA is finished there; a token
-// split across CTAs leaves one (m, l, O) record per piece for the combine
-// kernel.  Every wait is bounded; on expiry the kernel flags the status word,
-// drains its copies and MMAs, and returns.
+// Warps: 0-3 softmax; 4 MMA issuer and tensor-memory owner; 5-10 copy K rows
+// (warp 5 also loads each token's Q and writes the tile's key mask); 11-15
+// copy V rows.  Issuing gather4 copies is the limit of a single warp, hence
+// eleven issuers.  Every wait is bounded; on expiry the kernel flags the
+// status word, drains its copies and MMAs, and returns.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -42,26 +46,33 @@ using namespace umma;
 constexpr int kH = 64;            // query heads handled by this kernel
 constexpr int kD = 128;           // head dim
 constexpr int kTile = 128;        // keys per tile
-constexpr int kStages = 3;        // K/V tile stages
-constexpr int kThreads = 384;
-constexpr int kGatherWarps = 7;   // warp 2 and warps 6..11
+constexpr int kStages = 3;        // slots of the K ring and of the V ring
+constexpr int kMaskSlots = 6;     // key masks; written up to 3 tiles ahead of their reader
+constexpr int kThreads = 512;
+constexpr int kMmaWarp = 4;
+constexpr int kKWarp0 = 5, kKWarps = 6;   // warps 5-10
+constexpr int kVWarp0 = 11, kVWarps = 5;  // warps 11-15
 constexpr float kLazyRescale = 8.f;  // log2 units
-constexpr int kRecFloats = 2 * kH + kH * kD;
+// Registers per thread: the kernel is built for 128 (512 threads on 64K
+// registers); the softmax warpgroup (warps 0-3) raises its limit and the other
+// three lower theirs, 184 + 3 * 104 <= 4 * 128 so the raise can always be met.
+constexpr int kLaunchRegs = 128, kSoftmaxRegs = 184, kOtherRegs = 104;
+static_assert(kSoftmaxRegs + 3 * kOtherRegs <= 4 * kLaunchRegs, "register split exceeds the launch allocation");
 
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP = 384;  // tensor-memory columns
+constexpr int kSBufs = 3;          // S/P buffers in tensor memory (P overwrites its S in place)
+constexpr uint32_t kColO = 384;    // tensor-memory columns: S/P buffer b at 128 b, O at 384
 
-// Q: two token buffers of 64 rows share one 32 KB region, [kblk][buf][64 rows
-// x 128 B]: the MMA reads 128 rows (M = 128) from each buffer's base, and rows
-// 64..127 (the other buffer, or the first K stage right after) only feed the
-// unused accumulator rows 64..127.
+// Q: two token buffers share one 32 KB region [kblk][128 rows][128 B]: head
+// 16w+i of buffer qb is row 32w+16qb+i.  The S MMA of buffer qb reads 128 rows
+// from row 16qb, so A row 32w+i is head 16w+i; the rows in between (the other
+// buffer, or past the region) only feed unused accumulator rows.
 struct AttnSmem {
-  static constexpr size_t q = 0;                                   // [2 kblk][2 buf][64 rows][128 B]
-  static constexpr size_t k = q + 32768;                           // [stage][2 kblk][128 rows][128 B]
+  static constexpr size_t q = 0;                                   // [2 kblk][128 rows][128 B]
+  static constexpr size_t k = q + 32768;                           // [slot][2 kblk][128 rows][128 B]
   static constexpr size_t v = k + kStages * 32768;
-  static constexpr size_t mask = v + kStages * 32768;              // [stage][4] u32
-  static constexpr size_t xchg = mask + kStages * 4 * 4;           // [2 parity][2 halves][64] f32
-  static constexpr size_t bars = (xchg + 4 * kH * 4 + 7) & ~size_t(7);
-  static constexpr int kBars = 2 * kStages + 4 + 4 + 2 + 2 + 1 + 2;
+  static constexpr size_t mask = v + kStages * 32768;              // [slot][4] u32
+  static constexpr size_t bars = (mask + kMaskSlots * 16 + 7) & ~size_t(7);
+  static constexpr int kBars = 4 * kStages + 4 + 3 * kSBufs + 2 + kMaskSlots;
   static constexpr size_t misc = bars + kBars * 8;
   static constexpr size_t total = misc + 64;
 };
@@ -70,16 +81,33 @@ struct AttnUmmaParams {
   int B, T, N_c, r, W, R, K;
   int WT, TPT;                    // window tiles per token, tiles per token
   const int32_t *q_seq, *q_pos, *idx;
+  const __nv_bfloat16 *Vw, *Vc;   // V rows (window ring, compressed), 128 bf16 each
   const float *sink;
   float qk_scale;                 // scale * log2(e)
   __nv_bfloat16 *out;
-  float *rec;                     // [grid][2][kRecFloats]
   uint32_t *status;
 };
 
-__device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 16x32bx2 shape with a half offset of 64 columns: thread t of the warp
+// accesses lane (warp quarter) + t % 16, columns col + 64 (t / 16) + j.
+__device__ __forceinline__ void tmem_ld_16x2_x32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32], 64;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_16x2_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x32.b32 [%0], 64, "
       "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
       "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
@@ -89,7 +117,22 @@ __device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st_16x2_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.16x32bx2.x8.b32 [%0], 64, {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
+// 16-byte global -> shared copy (L2 only), tracked by cp_async_mbar_arrive.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// Arrives on `bar` (without raising its expected count) once every cp.async
+// this thread issued before has completed.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 
 // O[tmem] (+)= A[tmem] . B[smem]
 __device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -130,40 +173,104 @@ __device__ __forceinline__ uint64_t desc_sw128_mnmajor(uint32_t addr, uint32_t l
   return d;
 }
 
-__device__ __forceinline__ int tile_begin(long long total, int c, int G) {
-  return static_cast<int>(total * c / G);
+// Key q (0..63) of a thread's 64 keys is present iff bit q/4 of mw[q%4] is
+// set, mw = the tile's mask words shifted to the thread's half (bit g of word
+// e = key 4g+e of the tile).
+__device__ __forceinline__ bool key_present(const uint32_t (&mw)[4], int q) {
+  return ((mw[q & 3] >> (q >> 2)) & 1u) != 0;
 }
 
-// Record slot of the piece of token-range [t0, t1) that CTA c processed.
-__device__ __forceinline__ float *record(const AttnUmmaParams &p, int c, int slot) {
-  return p.rec + (static_cast<size_t>(c) * 2 + slot) * kRecFloats;
+// Max of the present logits among 64 (eight independent partial maxima, so
+// the compare chain is eight deep instead of 64).
+template <bool MASKED>
+__device__ __forceinline__ float max64(const uint32_t (&v)[64], const uint32_t (&mw)[4]) {
+  float m[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m[i] = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < 64; ++q) {
+    float x = __uint_as_float(v[q]);
+    if (MASKED) x = key_present(mw, q) ? x : -INFINITY;
+    m[q & 7] = fmaxf(m[q & 7], x);
+  }
+#pragma unroll
+  for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+  return m[0];
+}
+
+// p = 2^(c s - m) of the 16 logits v[16G .. 16G+15] (absent keys give 0),
+// added into four partial sums, and split into P = hi + lo: hi = p truncated
+// to bf16, lo = (p - hi) truncated to bf16 (|p - hi - lo| < 2^-16 p); pairs of
+// keys packed per 32-bit word by byte permutes.
+template <bool MASKED, int G>
+__device__ __forceinline__ void exp_split16(const uint32_t (&v)[64], const uint32_t (&mw)[4], float c, float neg_m,
+                                            uint32_t (&hi)[8], uint32_t (&lo)[8], float (&s4)[4]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int k = 16 * G + 2 * q;
+    float pa = ex2_approx(fmaf(__uint_as_float(v[k]), c, neg_m));
+    float pb = ex2_approx(fmaf(__uint_as_float(v[k + 1]), c, neg_m));
+    if (MASKED) {
+      pa = key_present(mw, k) ? pa : 0.f;
+      pb = key_present(mw, k + 1) ? pb : 0.f;
+    }
+    s4[q & 3] += pa + pb;
+    const uint32_t ua = __float_as_uint(pa), ub = __float_as_uint(pb);
+    const float la = pa - __uint_as_float(ua & 0xFFFF0000u);
+    const float lb = pb - __uint_as_float(ub & 0xFFFF0000u);
+    hi[q] = __byte_perm(ua, ub, 0x7632);
+    lo[q] = __byte_perm(__float_as_uint(la), __float_as_uint(lb), 0x7632);
+  }
+}
+
+// The thread's 64 keys, 16 at a time: group G (keys 16G .. 16G+15 of the
+// thread's half) goes to columns 32(G/2) + 8(G%2) (hi) and 16 more (lo) of the
+// thread's half of the S/P buffer, over logits already in registers.
+template <bool MASKED>
+__device__ __forceinline__ void exp_store64(const uint32_t (&v)[64], const uint32_t (&mw)[4], float c, float neg_m,
+                                            uint32_t s_col, float (&s4)[4]) {
+  uint32_t hi[8], lo[8];
+  exp_split16<MASKED, 0>(v, mw, c, neg_m, hi, lo, s4);
+  tmem_st_16x2_x8(s_col + 0, hi);
+  tmem_st_16x2_x8(s_col + 16, lo);
+  exp_split16<MASKED, 1>(v, mw, c, neg_m, hi, lo, s4);
+  tmem_st_16x2_x8(s_col + 8, hi);
+  tmem_st_16x2_x8(s_col + 24, lo);
+  exp_split16<MASKED, 2>(v, mw, c, neg_m, hi, lo, s4);
+  tmem_st_16x2_x8(s_col + 32, hi);
+  tmem_st_16x2_x8(s_col + 48, lo);
+  exp_split16<MASKED, 3>(v, mw, c, neg_m, hi, lo, s4);
+  tmem_st_16x2_x8(s_col + 40, hi);
+  tmem_st_16x2_x8(s_col + 56, lo);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
 sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kwmap,
-                       const __grid_constant__ CUtensorMap vwmap, const __grid_constant__ CUtensorMap kcmap,
-                       const __grid_constant__ CUtensorMap vcmap, const AttnUmmaParams p) {
+                       const __grid_constant__ CUtensorMap kcmap, const AttnUmmaParams p) {
   using L = AttnSmem;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *ks = smem + L::k, *vs = smem + L::v, *qs = smem + L::q;
   uint32_t *mask_s = reinterpret_cast<uint32_t *>(smem + L::mask);
-  float *xchg = reinterpret_cast<float *>(smem + L::xchg);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bars);
-  uint64_t *kvfull = bars, *kvempty = bars + kStages;
-  uint64_t *qfull = bars + 2 * kStages, *qempty = qfull + 2;
-  uint64_t *sfull = qempty + 2, *sempty = sfull + 2;
-  uint64_t *pfull = sempty + 2, *pempty = pfull + 1;
-  uint64_t *ofull = pempty + 1, *oempty = ofull + 1;
+  uint64_t *kfull = bars, *kempty = bars + kStages;
+  uint64_t *vfull = bars + 2 * kStages, *vempty = bars + 3 * kStages;
+  uint64_t *qfull = bars + 4 * kStages, *qempty = qfull + 2;
+  // per S/P buffer: S written (sfull), P written (pfull), P.V done = buffer free (sempty)
+  uint64_t *sfull = qempty + 2, *pfull = sfull + kSBufs, *sempty = pfull + kSBufs;
+  uint64_t *oempty = sempty + kSBufs;  // O of the previous token read out
   uint64_t *done = oempty + 1;
-  uint64_t *xbar = done + 1;  // [2]: one per head quarter, pairs the two key-half warps
+  uint64_t *mfull = done + 1;  // [kMaskSlots]: the slot's key mask is written
   uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem + L::misc);
   int *abort_s = reinterpret_cast<int *>(smem + L::misc + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const long long total = static_cast<long long>(p.T) * p.TPT;
   const int G = gridDim.x, c = blockIdx.x;
-  const int begin = tile_begin(total, c, G), end = tile_begin(total, c + 1, G);
+  // whole tokens per CTA: tokens [T*c/G, T*(c+1)/G)
+  const int begin = static_cast<int>(static_cast<long long>(p.T) * c / G) * p.TPT;
+  const int end = static_cast<int>(static_cast<long long>(p.T) * (c + 1) / G) * p.TPT;
 
   // zero the operand buffers once: rows never written by a copy stay finite
   for (int i = tid; i < static_cast<int>(L::mask / 16); i += kThreads)
@@ -171,26 +278,27 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
   static_assert(L::total + 1024 <= 232448, "shared memory budget");
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&kvfull[i], kGatherWarps);
-      mbar_init(&kvempty[i], 1);
+      mbar_init(&kfull[i], kKWarps);
+      mbar_init(&kempty[i], 1);
+      mbar_init(&vfull[i], 32 * kVWarps);  // one cp.async arrival per V-producer thread
+      mbar_init(&vempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qfull[i], 1);
       mbar_init(&qempty[i], 1);
-      mbar_init(&sfull[i], 1);
-      mbar_init(&sempty[i], 4);
     }
-    mbar_init(pfull, 4);
-    mbar_init(pempty, 1);
-    mbar_init(ofull, 1);
+    for (int i = 0; i < kSBufs; ++i) {
+      mbar_init(&sfull[i], 1);
+      mbar_init(&pfull[i], 4);
+      mbar_init(&sempty[i], 1);
+    }
     mbar_init(oempty, 4);
     mbar_init(done, 1);
-    mbar_init(&xbar[0], 2);
-    mbar_init(&xbar[1], 2);
+    for (int i = 0; i < kMaskSlots; ++i) mbar_init(&mfull[i], 1);
     *abort_s = 0;
     fence_barrier_init();
   }
-  if (warp == 3) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_base_s, 512);
     tmem_relinquish();
   }
@@ -205,355 +313,343 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
   };
   auto aborted = [&]() { return *reinterpret_cast<volatile int *>(abort_s) != 0; };
 
-  if (warp == 2 || warp >= 6) {
-    // --------------------------------------------------------------- producers
-    const int pw = (warp == 2) ? 0 : warp - 5;  // 0 .. 6
-    if (begin < end) {
-      if (warp == 2 && lane == 0) {
-        prefetch_tmap(&qmap);
-        prefetch_tmap(&kwmap);
-        prefetch_tmap(&vwmap);
-        prefetch_tmap(&kcmap);
-        prefetch_tmap(&vcmap);
-      }
-      int qn = -1, prev_t = -1, issued = 0;
-      Token tk{0, 0, 0};
-      bool tok_ok = false;
-      int n_w = 0;
-      // the key of slot kk (0..127) of tile j: its row and whether it exists
-      auto resolve = [&](int t, int j, int kk, int &row) -> bool {
-        if (!tok_ok) return false;
-        if (j < p.WT) {
-          const int q = j * kTile + kk;
-          if (q >= n_w) return false;
-          const int pos = tk.pos - n_w + 1 + q;
-          row = tk.b * p.R + pos % p.R;
-          return true;
+  if (warp >= 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
+    if (warp >= kKWarp0) {
+      // --------------------------------------------------------------- producers
+      const bool is_k = warp < kVWarp0;
+      const int pw = is_k ? warp - kKWarp0 : warp - kVWarp0;  // rank among its ring's warps
+      const int nw = is_k ? kKWarps : kVWarps;
+      uint64_t *ring_full = is_k ? kfull : vfull;
+      uint64_t *ring_empty = is_k ? kempty : vempty;
+      uint8_t *ring = is_k ? ks : vs;
+      if (begin < end) {
+        if (warp == kKWarp0 && lane == 0) {
+          prefetch_tmap(&qmap);
+          prefetch_tmap(&kwmap);
+          prefetch_tmap(&kcmap);
         }
-        const int k = (j - p.WT) * kTile + kk;
-        if (k >= p.K) return false;
-        const int cidx = p.idx[static_cast<int64_t>(t) * p.K + k];
-        if (cidx >= 0 && cidx < tk.nv) {
-          row = tk.b * p.N_c + cidx;
-          return true;
-        }
-        if (cidx != -1 && warp == 2) raise_flag(p.status, kFlagBadIndex);
-        return false;
-      };
-      for (int i = begin; i < end && !aborted(); ++i) {
-        const int t = i / p.TPT, j = i % p.TPT, n = i - begin;
-        if (t != prev_t) {
-          tok_ok = load_token(p.q_seq, p.q_pos, t, p.B, p.N_c, p.r, p.status, tk,
-                              warp == 2 && lane == 0 && j == 0);
-          n_w = tok_ok ? min(p.W, tk.pos + 1) : 0;
-          ++qn;
-          if (warp == 2) {
-            const int qb = qn & 1;
-            bool ok = true;
-            if (lane == 0) {
-              ok = mbar_wait(&qempty[qb], ((qn >> 1) & 1) ^ 1);
-              if (ok) {
-                mbar_expect_tx(&qfull[qb], 2 * kH * 128);
-                tma_load_2d(qs + qb * 8192, &qmap, &qfull[qb], 0, t * kH);
-                tma_load_2d(qs + 16384 + qb * 8192, &qmap, &qfull[qb], 64, t * kH);
-              } else {
-                fail();
+        int qn = -1, prev_t = -1, issued = 0;
+        Token tk{0, 0, 0};
+        bool tok_ok = false;
+        int n_w = 0;
+        // idx entries of keys 4*lane .. 4*lane+3 of a compressed tile, loaded one
+        // tile ahead so their latency overlaps the current tile's copies
+        auto load_idx = [&](int i, int32_t (&cc)[4]) {
+          const int t = i / p.TPT, j = i % p.TPT;
+  #pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            cc[e] = -1;
+            const int k = (j - p.WT) * kTile + 4 * lane + e;
+            if (j >= p.WT && k < p.K) cc[e] = p.idx[static_cast<int64_t>(t) * p.K + k];
+          }
+        };
+        int32_t cnext[4];
+        load_idx(begin, cnext);
+        for (int i = begin; i < end; ++i) {
+          if (__any_sync(0xffffffffu, aborted())) break;
+          const int t = i / p.TPT, j = i % p.TPT, n = i - begin;
+          int32_t cidx[4] = {cnext[0], cnext[1], cnext[2], cnext[3]};
+          if (i + 1 < end) load_idx(i + 1, cnext);
+          if (t != prev_t) {
+            tok_ok = load_token(p.q_seq, p.q_pos, t, p.B, p.N_c, p.r, p.status, tk,
+                                warp == kKWarp0 && lane == 0 && j == 0);
+            n_w = tok_ok ? min(p.W, tk.pos + 1) : 0;
+            ++qn;
+            if (warp == kKWarp0) {
+              const int qb = qn & 1;
+              bool ok = true;
+              if (lane == 0) {
+                ok = mbar_wait(&qempty[qb], ((qn >> 1) & 1) ^ 1);
+                if (ok) {
+                  // heads 16w..16w+15 -> rows 32w+16qb .. +15, both 64-column halves
+                  mbar_expect_tx(&qfull[qb], 2 * kH * 128);
+  #pragma unroll
+                  for (int w = 0; w < 4; ++w)
+  #pragma unroll
+                    for (int kb = 0; kb < 2; ++kb)
+                      tma_load_2d(qs + kb * 16384 + (32 * w + 16 * qb) * 128, &qmap, &qfull[qb], 64 * kb,
+                                  t * kH + 16 * w);
+                } else {
+                  fail();
+                }
               }
+              if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             }
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            prev_t = t;
           }
-          prev_t = t;
-        }
-        const int s = n % kStages;
-        if (!mbar_wait_warp(&kvempty[s], ((n / kStages) & 1) ^ 1)) {
-          if (lane == 0) fail();
-          break;
-        }
-        const bool window = j < p.WT;
-        if (warp == 2) {  // key mask of the tile: bit g of word e = key 4g+e exists
-          int row_unused = 0;
-          uint32_t m4[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) m4[e] = __ballot_sync(0xffffffffu, resolve(t, j, 4 * lane + e, row_unused));
-          if (lane == 0) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) mask_s[s * 4 + e] = m4[e];
-          }
-        }
-        // this warp's share of the 128 copies: copy c = (part, group), part =
-        // K lo / K hi / V lo / V hi, group g = keys 4g..4g+3
-        uint32_t bytes = 0;
-        const int c0 = lane * kGatherWarps + pw;
-        int rows[4] = {0, 0, 0, 0};
-        bool any = false;
-        if (c0 < 128) {
-          const int g = c0 & 31;
+          // rows and presence of keys 4*lane .. 4*lane+3
+          const bool window = j < p.WT;
+          int rows[4];
           bool valid[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) valid[e] = resolve(t, j, 4 * g + e, rows[e]);
-          any = valid[0] || valid[1] || valid[2] || valid[3];
-          const int fill = valid[0] ? rows[0] : valid[1] ? rows[1] : valid[2] ? rows[2] : rows[3];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (!valid[e]) rows[e] = fill;
+  #pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            rows[e] = 0;
+            valid[e] = false;
+            if (!tok_ok) continue;
+            if (window) {
+              const int q = j * kTile + 4 * lane + e;
+              if (q < n_w) {
+                const int pos = tk.pos - n_w + 1 + q;
+                rows[e] = tk.b * p.R + pos % p.R;
+                valid[e] = true;
+              }
+            } else if (cidx[e] >= 0 && cidx[e] < tk.nv) {
+              rows[e] = tk.b * p.N_c + cidx[e];
+              valid[e] = true;
+            } else if (cidx[e] != -1 && warp == kKWarp0) {
+              raise_flag(p.status, kFlagBadIndex);
+            }
+          }
+          const int s = n % kStages;
+          if (!mbar_wait_warp(&ring_empty[s], ((n / kStages) & 1) ^ 1)) {
+            if (lane == 0) fail();
+            break;
+          }
+          if (warp == kKWarp0) {  // key mask of the tile: bit g of word e = key 4g+e exists
+            uint32_t m4[4];
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) m4[e] = __ballot_sync(0xffffffffu, valid[e]);
+            if (lane == 0) {
+  #pragma unroll
+              for (int e = 0; e < 4; ++e) mask_s[(n % kMaskSlots) * 4 + e] = m4[e];
+              mbar_arrive(&mfull[n % kMaskSlots]);
+            }
+          }
+          if (is_k) {
+            // K rows by TMA gather4.  This warp's share of the tile's 64
+            // copies: copy c = (half, group): half = columns 0-63 / 64-127 of
+            // the rows, group g = keys 4g..4g+3 (absent keys of a group read a
+            // present key's row; a group with none is not copied)
+            const bool any4 = valid[0] || valid[1] || valid[2] || valid[3];
+            const int fill = valid[0] ? rows[0] : valid[1] ? rows[1] : valid[2] ? rows[2] : rows[3];
+            const int c0 = lane * nw + pw;
+            const int g = c0 & 31, half = c0 >> 5;
+            int gr[4];
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) gr[e] = __shfl_sync(0xffffffffu, valid[e] ? rows[e] : fill, g);
+            const bool gany = __shfl_sync(0xffffffffu, any4, g);
+            const bool mine = c0 < 64 && gany;
+            const uint32_t bytes = __popc(__ballot_sync(0xffffffffu, mine)) * 512u;
+            if (lane == 0) mbar_expect_tx(&ring_full[s], bytes);
+            __syncwarp();
+            if (mine) {
+              const CUtensorMap *map = window ? &kwmap : &kcmap;
+              uint8_t *dst = ring + s * 32768 + half * 16384 + 4 * g * 128;
+              gather4(dst, map, &ring_full[s], half * 64, gr[0], gr[1], gr[2], gr[3]);
+            }
+          } else {
+            // V rows by 16-byte cp.async: a warp instruction copies two rows
+            // (keys 2pr, 2pr+1; 16 lanes x 16 B each) into the same swizzled
+            // layout TMA would write (16-byte chunk c of a 128-byte row r at
+            // chunk c ^ (r & 7)); absent keys are not copied.  Each lane's
+            // arrival on the slot's barrier fires once its copies have landed.
+            const uint8_t *vbase = reinterpret_cast<const uint8_t *>(window ? p.Vw : p.Vc);
+            const int hr = lane >> 4, ch = lane & 15;
+            uint8_t *slot = ring + s * 32768 + (ch >> 3) * 16384;
+            for (int pr = pw; pr < kTile / 2; pr += kVWarps) {
+              // keys 2pr, 2pr+1 live in lane pr/2 as entries 2(pr&1), 2(pr&1)+1
+              const bool odd = pr & 1;
+              const int a0 = odd ? (valid[2] ? rows[2] : -1) : (valid[0] ? rows[0] : -1);
+              const int a1 = odd ? (valid[3] ? rows[3] : -1) : (valid[1] ? rows[1] : -1);
+              const int r0 = __shfl_sync(0xffffffffu, a0, pr >> 1);
+              const int r1 = __shfl_sync(0xffffffffu, a1, pr >> 1);
+              const int row = hr ? r1 : r0, key = 2 * pr + hr;
+              if (row >= 0)
+                cp_async16(slot + key * 128 + (((ch & 7) ^ (key & 7)) << 4),
+                           vbase + static_cast<int64_t>(row) * (kD * 2) + ch * 16);
+            }
+            cp_async_mbar_arrive(&ring_full[s]);
+          }
+          ++issued;
         }
-        bytes = __popc(__ballot_sync(0xffffffffu, any)) * 512u;
-        if (lane == 0) mbar_expect_tx(&kvfull[s], bytes);
-        __syncwarp();
-        if (any) {
-          const int g = c0 & 31, part = c0 >> 5;
-          const CUtensorMap *map = (part < 2) ? (window ? &kwmap : &kcmap) : (window ? &vwmap : &vcmap);
-          uint8_t *dst = ((part < 2) ? ks : vs) + s * 32768 + (part & 1) * 16384 + 4 * g * 128;
-          gather4(dst, map, &kvfull[s], (part & 1) * 64, rows[0], rows[1], rows[2], rows[3]);
+        if ((warp == kKWarp0 || warp == kVWarp0) && lane == 0) {  // drain: every issued copy lands before the CTA exits
+          for (int n = max(0, issued - kStages); n < issued; ++n)
+            mbar_wait(&ring_full[n % kStages], (n / kStages) & 1);
+          if (warp == kKWarp0)
+            for (int q = max(0, qn - 1); q <= qn; ++q) mbar_wait(&qfull[q & 1], (q >> 1) & 1);
         }
-        ++issued;
       }
-      if (warp == 2 && lane == 0) {  // drain: every issued copy lands before the CTA exits
-        for (int n = max(0, issued - kStages); n < issued; ++n) mbar_wait(&kvfull[n % kStages], (n / kStages) & 1);
-        for (int q = max(0, qn - 1); q <= qn; ++q) mbar_wait(&qfull[q & 1], (q >> 1) & 1);
-      }
-    }
-  } else if (warp == 3) {
-    // ------------------------------------------------------------- MMA issuer
-    // Issues S for tile n+1 and P.V for tile n in whichever order their inputs
-    // become ready (polling), so P.V never waits for the next tile's data.
-    if (lane == 0 && begin < end) {
-      constexpr uint32_t idesc_s = idesc_bf16(128, kTile);              // K-major A, K-major B
-      constexpr uint32_t idesc_o = idesc_bf16(128, kD) | (1u << 16);     // K-major A (tmem), MN-major B
-      const int count = end - begin;
-      int ns = 0, np = 0;            // next S to issue, next P.V to issue
-      int qn_s = -1, prev_t_s = -1;  // token ordinal as seen by the S stage
-      int sg = -1;                   // segment ordinal as seen by the P.V stage
-      bool q_ready = false;
-      long long idle_since = clock64();
-      bool ok = true;
-      while (np < count) {
-        if (aborted()) { ok = false; break; }
-        bool progressed = false;
-        // ---- S(ns): Q of its token, its K tile and a free S buffer
-        if (ns < count && ns <= np + 1) {
-          const int i = begin + ns, t = i / p.TPT, j = i % p.TPT;
+    } else if (warp == kMmaWarp) {
+      // ------------------------------------------------------------- MMA issuer
+      // Fixed order S(0), S(1), P.V(0), S(2), P.V(1), S(3), ...: S runs two
+      // tiles ahead of P.V, and S(n+2) (which waits for P.V(n-1) to free its
+      // buffer) is issued after P.V(n), so the tensor core always has P.V(n)
+      // queued while the issuer waits.  Every input of each step is produced by
+      // work issued earlier in this order, so the blocking waits cannot deadlock.
+      if (lane == 0 && begin < end) {
+        constexpr uint32_t idesc_s = idesc_bf16(128, kTile);              // K-major A, K-major B
+        constexpr uint32_t idesc_o = idesc_bf16(128, kD) | (1u << 16);     // K-major A (tmem), MN-major B
+        const int count = end - begin;
+        int qn_s = -1, prev_t_s = -1;  // token ordinal as seen by the S stage
+        int tok_pv = -1;               // tokens started by the P.V stage
+        bool ok = true;
+        // S(n): Q of its token, its K tile and a free S/P buffer
+        auto issue_s = [&](int n) -> bool {
+          const int i = begin + n, t = i / p.TPT, j = i % p.TPT;
+          const int s = n % kStages, b = n % kSBufs;
           if (t != prev_t_s) {
-            if (!q_ready && mbar_try_wait(&qfull[(qn_s + 1) & 1], ((qn_s + 1) >> 1) & 1)) q_ready = true;
+            ++qn_s;
+            prev_t_s = t;
+            if (!mbar_wait(&qfull[qn_s & 1], (qn_s >> 1) & 1)) return false;
           }
-          const bool q_ok = (t == prev_t_s) || q_ready;
-          const int s = ns % kStages, sb = ns & 1;
-          if (q_ok && mbar_try_wait(&kvfull[s], (ns / kStages) & 1) &&
-              mbar_try_wait(&sempty[sb], ((ns >> 1) & 1) ^ 1)) {
-            if (t != prev_t_s) {
-              ++qn_s;
-              prev_t_s = t;
-              q_ready = false;
-            }
-            tc_fence_after();
-            const uint32_t a0 = smem_u32(qs + (qn_s & 1) * 8192), b0 = smem_u32(ks + s * 32768);
-            const uint32_t d = tmem + (sb ? kColS1 : kColS0);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-              mma_f16(d, desc_sw128_kmajor(a0 + off), desc_sw128_kmajor(b0 + off), idesc_s, kk > 0);
-            }
-            mma_commit(&sfull[sb]);
-            if ((j == p.TPT - 1) || (i == end - 1)) mma_commit(&qempty[qn_s & 1]);
-            ++ns;
-            progressed = true;
+          if (!mbar_wait(&kfull[s], (n / kStages) & 1) || !mbar_wait(&sempty[b], ((n / kSBufs) & 1) ^ 1))
+            return false;
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(qs + (qn_s & 1) * 2048), b0 = smem_u32(ks + s * 32768);
+          const uint32_t d = tmem + 128 * b;
+  #pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_f16(d, desc_sw128_kmajor(a0 + off), desc_sw128_kmajor(b0 + off), idesc_s, kk > 0);
           }
-        }
-        // ---- P.V(np): P from the softmax (and O read out after the previous segment)
-        if (np < ns) {
-          const int i = begin + np, j = i % p.TPT;
-          const bool first = (j == 0) || (np == 0);
-          const bool last = (j == p.TPT - 1) || (i == end - 1);
-          const bool o_ok = !first || sg < 0 || mbar_try_wait(oempty, sg & 1);
-          if (o_ok && mbar_try_wait(pfull, np & 1)) {
-            if (first) ++sg;
-            tc_fence_after();
-            const int s = np % kStages;
-            const uint32_t v0 = smem_u32(vs + s * 32768);
-#pragma unroll
-            for (int half = 0; half < 2; ++half)
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                mma_f16_ta(tmem + kColO, tmem + kColP + 64 * half + 8 * kk,
-                           desc_sw128_mnmajor(v0 + kk * 2048, 16384), idesc_o, !(first && half == 0 && kk == 0));
-            mma_commit(&kvempty[s]);
-            mma_commit(pempty);
-            if (last) mma_commit(ofull);
-            ++np;
-            progressed = true;
+          mma_commit(&sfull[b]);
+          mma_commit(&kempty[s]);
+          if (j == p.TPT - 1) mma_commit(&qempty[qn_s & 1]);
+          return true;
+        };
+        // P.V(n): P of the tile (in its S/P buffer: keys 32c..32c+31 as hi in
+        // columns 32c..32c+15 and lo in 32c+16..32c+31), its V tile, and O read
+        // out after the previous token
+        auto issue_pv = [&](int n) -> bool {
+          const int i = begin + n, j = i % p.TPT;
+          const bool first = j == 0;
+          const int s = n % kStages, b = n % kSBufs;
+          if (first && tok_pv >= 0 && !mbar_wait(oempty, tok_pv & 1)) return false;
+          if (!mbar_wait(&pfull[b], (n / kSBufs) & 1) || !mbar_wait(&vfull[s], (n / kStages) & 1)) return false;
+          if (first) ++tok_pv;
+          fence_proxy_async();  // V arrived through the generic proxy; the MMA reads it through the async one
+          tc_fence_after();
+          const uint32_t v0 = smem_u32(vs + s * 32768), pb = tmem + 128 * b;
+  #pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {  // keys 16kk .. 16kk+15
+            const uint64_t bdesc = desc_sw128_mnmajor(v0 + kk * 2048, 16384);
+            const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
+            mma_f16_ta(tmem + kColO, pb + col, bdesc, idesc_o, !(first && kk == 0));
+            mma_f16_ta(tmem + kColO, pb + col + 16, bdesc, idesc_o, 1);
           }
+          mma_commit(&vempty[s]);
+          mma_commit(&sempty[b]);
+          return true;
+        };
+        for (int n = 0; ok && n < 2 && n < count; ++n) ok = issue_s(n);
+        for (int n = 0; ok && n < count; ++n) {
+          if (aborted() || !issue_pv(n) || (n + 2 < count && !issue_s(n + 2))) ok = false;
         }
-        if (progressed) {
-          idle_since = clock64();
-        } else if (clock64() - idle_since > kWaitBudgetCycles) {
-          ok = false;
-          break;
-        }
+        if (!ok) fail();
+        mma_commit(done);
+        if (!mbar_wait(done, 0)) raise_flag(p.status, kFlagTimeout);
       }
-      if (!ok) fail();
-      mma_commit(done);
-      if (!mbar_wait(done, 0)) raise_flag(p.status, kFlagTimeout);
     }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     // ----------------------------------------------------------------- softmax
-    const int hq = warp & 1;                 // head quarter: 0 -> heads 0..31, 1 -> 32..63
-    const int kh = warp >> 2;                // key half: 0 -> keys 0..63, 1 -> 64..127
-    const int h = 32 * hq + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(32 * hq) << 16;
-    // value exchange with the partner warp (same heads, other key half):
-    // double-buffered slots, one mbarrier phase per exchange, bounded wait
-    int xk = 0;
-    auto swap = [&](float val, float &partner) -> bool {
-      xchg[((xk & 1) * 2 + kh) * kH + h] = val;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&xbar[hq]);
-      const bool ok = mbar_wait_warp(&xbar[hq], xk & 1);
-      partner = xchg[((xk & 1) * 2 + (kh ^ 1)) * kH + h];
-      ++xk;
-      return ok;
-    };
-    float m_ref = -INFINITY, l_part = 0.f;
-    int sg = -1, seg_start = 0;
+    // Warp w, thread t: head 16w + t%16 (tensor-memory lane 32w + t%16),
+    // keys 64u .. 64u+63 of each tile with u = t/16 (also O columns 64u ..
+    // 64u+63).  The two threads of a head combine their maxima by one shuffle
+    // per tile and their sums at the token's end.  P overwrites the logits it
+    // came from; O is touched only to rescale it (after waiting for the
+    // previous P.V) and to read it out at a token's end.
+    const int hq = lane & 15, u = lane >> 4;
+    const int h = 16 * warp + hq;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+    float m_ref = -INFINITY, l = 0.f;
     for (int i = begin; i < end; ++i) {
       const int n = i - begin, t = i / p.TPT, j = i % p.TPT;
-      const bool first = (j == 0) || (n == 0);
-      const bool last = (j == p.TPT - 1) || (i == end - 1);
+      const bool first = j == 0, last = j == p.TPT - 1;
       if (first) {
-        ++sg;
-        seg_start = i;
         m_ref = -INFINITY;
-        l_part = 0.f;
+        l = 0.f;
       }
-      const int s = n % kStages, sb = n & 1;
-      const bool ok = mbar_wait_warp(&kvfull[s], (n / kStages) & 1) && mbar_wait_warp(&sfull[sb], (n >> 1) & 1);
-      if (!ok) {
+      const int b = n % kSBufs;
+      if (!(mbar_wait_warp(&mfull[n % kMaskSlots], (n / kMaskSlots) & 1) &&
+            mbar_wait_warp(&sfull[b], (n / kSBufs) & 1))) {
         if (lane == 0) fail();
         break;
       }
       tc_fence_after();
-      uint32_t v[64];  // raw dot products Q.K of this thread's head and keys
-      tmem_ld_32x32b_x32(tmem + lane_base + (sb ? kColS1 : kColS0) + 64 * kh,
-                         *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-      tmem_ld_32x32b_x32(tmem + lane_base + (sb ? kColS1 : kColS0) + 64 * kh + 32,
-                         *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      const uint32_t s_col = tmem + lane_base + 128 * b;
+      uint32_t v[64];
+      tmem_ld_16x2_x32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld_16x2_x32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      uint32_t mw[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) mw[e] = mask_s[(n % kMaskSlots) * 4 + e];
+      const bool all_keys = (mw[0] & mw[1] & mw[2] & mw[3]) == 0xFFFFFFFFu;  // warp-uniform
+#pragma unroll
+      for (int e = 0; e < 4; ++e) mw[e] >>= 16 * u;
       tmem_ld_wait();
-      uint32_t m4[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) m4[e] = mask_s[s * 4 + e];
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sempty[sb]);
-      // Masked keys -> -inf.  The max runs on the raw dot products (the
-      // softmax scale is positive) and each logit is scaled and shifted by one
-      // FMA inside exp2.  Mask words stride by 4 keys: bit g of word e is key
-      // 4g+e; a half of the tile whose 16 groups are all present skips it.
-      float mx = -INFINITY;
-      const uint32_t all4 = m4[0] & m4[1] & m4[2] & m4[3];
-      const uint32_t half_mask = kh ? 0xFFFF0000u : 0x0000FFFFu;
-      if ((all4 & half_mask) != half_mask) {
-#pragma unroll
-        for (int q = 0; q < 64; ++q) {
-          const int key = 64 * kh + q;
-          if (!((m4[key & 3] >> (key >> 2)) & 1u)) v[q] = 0xFF800000u;  // -inf
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 64; ++q) mx = fmaxf(mx, __uint_as_float(v[q]));
+      // ---- the tile's max over the raw dot products (scale > 0)
+      float mx = all_keys ? max64<false>(v, mw) : max64<true>(v, mw);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
       mx *= p.qk_scale;
-      float other;
-      if (!swap(mx, other)) {
-        if (lane == 0) fail();
-        break;
-      }
-      const float tile_max = fmaxf(mx, other);
       float factor = 1.f;
       bool rescale = false;
       if (first) {
-        m_ref = tile_max;
-      } else if (tile_max > m_ref + kLazyRescale) {
-        factor = exp2f(m_ref - tile_max);
-        m_ref = tile_max;
+        m_ref = mx;
+      } else if (mx > m_ref + kLazyRescale) {
+        factor = exp2f(m_ref - mx);
+        m_ref = mx;
         rescale = true;
       }
-      // p = 2^(scale * s - m_ref); P = hi + lo with hi = p truncated to bf16
-      // and lo = (p - hi) truncated to bf16 (|p - hi - lo| < 2^-14 p), packed
-      // in pairs with byte permutes: no conversion instructions.
-      float sum = 0.f;
-      uint32_t phi[32], plo[32];
-      const float neg_m = -m_ref;
-      const bool live = m_ref != -INFINITY;
-#pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        float pa = 0.f, pb = 0.f;
-        if (live) {
-          pa = ex2_approx(fmaf(__uint_as_float(v[2 * q]), p.qk_scale, neg_m));
-          pb = ex2_approx(fmaf(__uint_as_float(v[2 * q + 1]), p.qk_scale, neg_m));
-        }
-        sum += pa + pb;
-        const uint32_t ua = __float_as_uint(pa), ub = __float_as_uint(pb);
-        const float la = pa - __uint_as_float(ua & 0xFFFF0000u);
-        const float lb = pb - __uint_as_float(ub & 0xFFFF0000u);
-        phi[q] = __byte_perm(ua, ub, 0x7632);
-        plo[q] = __byte_perm(__float_as_uint(la), __float_as_uint(lb), 0x7632);
-      }
-      l_part = l_part * factor + sum;
-      // the previous P.V must be finished before P is overwritten or O rescaled
-      if (!mbar_wait_warp(pempty, (n & 1) ^ 1)) {
-        if (lane == 0) fail();
-        break;
-      }
-      tc_fence_after();
       if (__any_sync(0xffffffffu, rescale)) {
-        uint32_t o[64];
-        tmem_ld_32x32b_x32(tmem + lane_base + kColO + 64 * kh, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-        tmem_ld_32x32b_x32(tmem + lane_base + kColO + 64 * kh + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
-        tmem_ld_wait();
-#pragma unroll
-        for (int q = 0; q < 64; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * factor);
-        tmem_st_x32(tmem + lane_base + kColO + 64 * kh, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-        tmem_st_x32(tmem + lane_base + kColO + 64 * kh + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
-      }
-      tmem_st_x32(tmem + lane_base + kColP + 32 * kh, phi);
-      tmem_st_x32(tmem + lane_base + kColP + 64 + 32 * kh, plo);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(pfull);
-
-      if (last) {
-        if (!mbar_wait_warp(ofull, sg & 1)) {
+        // O holds P.V of tiles up to n-1: wait for P.V(n-1), then scale this
+        // warp's rows (factor 1 for heads that keep their reference)
+        const int pn = n - 1;
+        if (!mbar_wait_warp(&sempty[pn % kSBufs], (pn / kSBufs) & 1)) {
           if (lane == 0) fail();
           break;
         }
         tc_fence_after();
-        uint32_t o[64];
-        tmem_ld_32x32b_x32(tmem + lane_base + kColO + 64 * kh, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-        tmem_ld_32x32b_x32(tmem + lane_base + kColO + 64 * kh + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(oempty);
-        float l_other;
-        if (!swap(l_part, l_other)) {
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t o[32];
+          tmem_ld_16x2_x32(tmem + lane_base + kColO + 32 * c2, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * factor);
+          tmem_st_16x2_x32(tmem + lane_base + kColO + 32 * c2, o);
+        }
+      }
+      // with no key seen yet (m_ref = -inf) every key of the tile is absent
+      // and masked to 0; any finite reference serves
+      const float neg_m = m_ref != -INFINITY ? -m_ref : 0.f;
+      // ---- P = 2^(scale * s - m_ref) as bf16 hi + lo, written over the logits
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+      if (all_keys)
+        exp_store64<false>(v, mw, p.qk_scale, neg_m, s_col, s4);
+      else
+        exp_store64<true>(v, mw, p.qk_scale, neg_m, s_col, s4);
+      tmem_st_wait();
+      l = l * factor + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pfull[b]);
+
+      if (last) {
+        // O is complete once P.V(n) is done
+        if (!mbar_wait_warp(&sempty[b], (n / kSBufs) & 1)) {
           if (lane == 0) fail();
           break;
         }
-        const float l = l_part + l_other;
-        const int t0 = t * p.TPT;
-        const bool whole = (seg_start == t0) && (i == t0 + p.TPT - 1);
-        if (whole) {
-          float Lden = l;
-          float a = 1.f;
-          if (p.sink) {
-            const float s2 = p.sink[h] * kLog2e;
-            const float M = fmaxf(m_ref, s2);
-            a = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - M);
-            Lden = l * a + exp2f(s2 - M);
-          }
-          const float inv = Lden > 0.f ? a / Lden : 0.f;
-          uint4 *dst = reinterpret_cast<uint4 *>(p.out + (static_cast<int64_t>(t) * kH + h) * kD + 64 * kh);
+        tc_fence_after();
+        const float l_all = l + __shfl_xor_sync(0xffffffffu, l, 16);
+        float Lden = l_all, a = 1.f;
+        if (p.sink) {
+          const float s2 = p.sink[h] * kLog2e;
+          const float M = fmaxf(m_ref, s2);
+          a = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - M);
+          Lden = l_all * a + exp2f(s2 - M);
+        }
+        const float inv = Lden > 0.f ? a / Lden : 0.f;
+        uint4 *dst = reinterpret_cast<uint4 *>(p.out + (static_cast<int64_t>(t) * kH + h) * kD + 64 * u);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t o[32];
+          tmem_ld_16x2_x32(tmem + lane_base + kColO + 32 * c2, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
             uint32_t pk[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -562,64 +658,23 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
               pk[e] = static_cast<uint32_t>(__bfloat16_as_ushort(lo)) |
                       (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
             }
-            dst[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[4 * c2 + q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
-        } else {
-          const int slot = (seg_start == begin) ? 0 : 1;
-          float *rec = record(p, c, slot);
-          if (kh == 0) {
-            rec[h] = m_ref;
-            rec[kH + h] = l;
-          }
-          float4 *od = reinterpret_cast<float4 *>(rec + 2 * kH + h * kD + 64 * kh);
-#pragma unroll
-          for (int q = 0; q < 16; ++q)
-            od[q] = make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
-                                __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(oempty);
       }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 3) {
+  if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-}
-
-// Merges the records of every token split across CTAs, one block per
-// (token, head): out = sum_r 2^(m_r - M) O_r / (sum_r 2^(m_r - M) l_r +
-// 2^(sink - M)).
-__global__ void __launch_bounds__(kD) attn_umma_combine_kernel(const AttnUmmaParams p, int G) {
-  const int t = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
-  const long long total = static_cast<long long>(p.T) * p.TPT;
-  const long long first_tile = static_cast<long long>(t) * p.TPT, last_tile = first_tile + p.TPT - 1;
-  auto cta_of = [&](long long i) {
-    int cc = static_cast<int>(i * G / total);
-    while (cc + 1 < G && tile_begin(total, cc + 1, G) <= i) ++cc;
-    while (cc > 0 && tile_begin(total, cc, G) > i) --cc;
-    return cc;
-  };
-  const int c0 = cta_of(first_tile), c1 = cta_of(last_tile);
-  if (c0 == c1) return;  // finished inside one CTA
-  auto slot_of = [&](int cc) { return (cc == c0 && tile_begin(total, cc, G) < first_tile) ? 1 : 0; };
-  float M = p.sink ? p.sink[h] * kLog2e : -INFINITY;
-  for (int cc = c0; cc <= c1; ++cc) M = fmaxf(M, record(p, cc, slot_of(cc))[h]);
-  float o = 0.f;
-  if (M != -INFINITY) {
-    float Lden = p.sink ? exp2f(p.sink[h] * kLog2e - M) : 0.f, acc = 0.f;
-    for (int cc = c0; cc <= c1; ++cc) {
-      const float *rec = record(p, cc, slot_of(cc));
-      const float a = exp2f(rec[h] - M);
-      Lden = fmaf(a, rec[kH + h], Lden);
-      acc = fmaf(a, rec[2 * kH + h * kD + d], acc);
-    }
-    o = Lden > 0.f ? acc / Lden : 0.f;
-  }
-  p.out[(static_cast<int64_t>(t) * kH + h) * kD + d] = __float2bfloat16_rn(o);
 }
 
 bool encode_rows(CUtensorMap *m, const void *base, uint64_t rows, uint32_t box_rows) {
@@ -634,23 +689,22 @@ bool encode_rows(CUtensorMap *m, const void *base, uint64_t rows, uint32_t box_r
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One CTA per SM, each over whole tokens (G <= T); a batch smaller than the
+// SM count leaves SMs idle rather than splitting tokens.
+int attn_umma_grid(const sa_index_args &ia) {
+  const int sms = sm_count();
+  return ia.T < sms ? ia.T : sms;
+}
+
 }  // namespace
 
 bool attn_umma_supported(const sa_attn_args &aa) { return aa.H == kH && aa.D == kD; }
 
-int attn_umma_grid(const sa_index_args &ia, const sa_attn_args &aa, int K) {
-  const int WT = (aa.W + kTile - 1) / kTile, KT = (K + kTile - 1) / kTile;
-  const long long total = static_cast<long long>(ia.T) * (WT + KT);
-  const int sms = sm_count();
-  return static_cast<int>(total < sms ? total : sms);
-}
-
-size_t attn_umma_scratch(const sa_index_args &ia, const sa_attn_args &aa, int K) {
-  return static_cast<size_t>(attn_umma_grid(ia, aa, K)) * 2 * kRecFloats * sizeof(float);
-}
+// The tensor-core attention keeps no scratch in global memory.
+size_t attn_umma_scratch(const sa_index_args &, const sa_attn_args &, int) { return 0; }
 
 cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &aa, const int32_t *idx, int K,
-                                   void *out, void *scratch, uint32_t *status, cudaStream_t stream) {
+                                   void *out, void *, uint32_t *status, cudaStream_t stream) {
   if (ia.T == 0) return cudaSuccess;
   AttnUmmaParams p;
   p.B = ia.B;
@@ -668,24 +722,30 @@ cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &
   p.sink = aa.sink;
   p.qk_scale = aa.scale * kLog2e;
   p.out = static_cast<__nv_bfloat16 *>(out);
-  p.rec = static_cast<float *>(scratch);
+  p.Vw = static_cast<const __nv_bfloat16 *>(aa.Vw);
+  p.Vc = static_cast<const __nv_bfloat16 *>(aa.Vc);
   p.status = status;
-  CUtensorMap qmap, kwmap, vwmap, kcmap, vcmap;
-  if (!encode_rows(&qmap, aa.Q, static_cast<uint64_t>(ia.T) * kH, kH) ||
+  CUtensorMap qmap, kwmap, kcmap;
+  if (!encode_rows(&qmap, aa.Q, static_cast<uint64_t>(ia.T) * kH, 16) ||
       !encode_rows(&kwmap, aa.Kw, static_cast<uint64_t>(ia.B) * aa.R, 1) ||
-      !encode_rows(&vwmap, aa.Vw, static_cast<uint64_t>(ia.B) * aa.R, 1) ||
-      !encode_rows(&kcmap, aa.Kc, static_cast<uint64_t>(ia.B) * ia.N_c, 1) ||
-      !encode_rows(&vcmap, aa.Vc, static_cast<uint64_t>(ia.B) * ia.N_c, 1))
+      !encode_rows(&kcmap, aa.Kc, static_cast<uint64_t>(ia.B) * ia.N_c, 1))
     return cudaErrorInvalidValue;
-  const int G = attn_umma_grid(ia, aa, K);
+  const int G = attn_umma_grid(ia);
   const size_t smem = AttnSmem::total + 1024;
+  // the register split above assumes the kernel launches with kLaunchRegs
+  // registers per thread; anything else could leave a raise waiting forever
+  static int regs = -1;
+  if (regs < 0) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void *>(sparse_mqa_umma_kernel));
+    if (e != cudaSuccess) return e;
+    regs = fa.numRegs;
+  }
+  if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   static bool attr_done[64] = {};
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(sparse_mqa_umma_kernel), smem, attr_done);
   if (e != cudaSuccess) return e;
-  sparse_mqa_umma_kernel<<<G, kThreads, smem, stream>>>(qmap, kwmap, vwmap, kcmap, vcmap, p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  attn_umma_combine_kernel<<<dim3(ia.T, kH), kD, 0, stream>>>(p, G);
+  sparse_mqa_umma_kernel<<<G, kThreads, smem, stream>>>(qmap, kwmap, kcmap, p);
   return cudaGetLastError();
 }
 
