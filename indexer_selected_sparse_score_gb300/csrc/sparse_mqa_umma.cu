@@ -72,7 +72,7 @@ struct AttnSmem {
   static constexpr size_t v = k + kStages * 32768;
   static constexpr size_t mask = v + kStages * 32768;              // [slot][4] u32
   static constexpr size_t bars = (mask + kMaskSlots * 16 + 7) & ~size_t(7);
-  static constexpr int kBars = 4 * kStages + 4 + 3 * kSBufs + 2 + kMaskSlots;
+  static constexpr int kBars = 4 * kStages + 4 + 3 * kSBufs + 2 + kMaskSlots + 2;
   static constexpr size_t misc = bars + kBars * 8;
   static constexpr size_t total = misc + 64;
 };
@@ -80,6 +80,7 @@ struct AttnSmem {
 struct AttnUmmaParams {
   int B, T, N_c, r, W, R, K;
   int WT, TPT;                    // window tiles per token, tiles per token
+  int split, PT0;                 // CTAs per token (1, or a 2-CTA cluster with one token), tiles of rank 0's part
   const int32_t *q_seq, *q_pos, *idx;
   const __nv_bfloat16 *Vw, *Vc;   // V rows (window ring, compressed), 128 bf16 each
   const float *sink;
@@ -101,6 +102,16 @@ __device__ __forceinline__ void tmem_ld_16x2_x32(uint32_t taddr, uint32_t (&r)[3
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
         "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_16x2_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16], 64;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
 }
@@ -171,6 +182,61 @@ __device__ __forceinline__ uint64_t desc_sw128_mnmajor(uint32_t addr, uint32_t l
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
   return d;
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster: a barrier with release/acquire
+// ordering at cluster scope.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrives (release, cluster scope) on the mbarrier at the same shared-memory
+// offset as `bar` in the cluster's CTA `rank`.
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t *bar, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(bar)), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
+// Shared-memory address of the same offset in the cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_map(const void *p, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+  return remote;
+}
+
+__device__ __forceinline__ void st_cluster_f4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// Bounded wait with acquire at cluster scope (for phases completed by the
+// other CTA of the cluster); the result is the same in every lane.
+__device__ __forceinline__ bool mbar_wait_cluster_warp(uint64_t *bar, uint32_t parity) {
+  auto test = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return ok != 0;
+  };
+  bool ok = test();
+  if (!ok) {
+    const long long t0 = clock64();
+    while (!(ok = test()))
+      if (clock64() - t0 > kWaitBudgetCycles) break;
+  }
+  return __all_sync(0xffffffffu, ok);
 }
 
 // Key q (0..63) of a thread's 64 keys is present iff bit q/4 of mw[q%4] is
@@ -263,18 +329,24 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
   uint64_t *oempty = sempty + kSBufs;  // O of the previous token read out
   uint64_t *done = oempty + 1;
   uint64_t *mfull = done + 1;  // [kMaskSlots]: the slot's key mask is written
+  // split handoff: xempty (rank 1) = rank 0's K ring is free to take rank 1's partial;
+  // xfull (rank 0) = the partial is there
+  uint64_t *xfull = mfull + kMaskSlots, *xempty = xfull + 1;
   uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem + L::misc);
   int *abort_s = reinterpret_cast<int *>(smem + L::misc + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = gridDim.x, c = blockIdx.x;
-  // whole tokens per CTA: tokens [T*c/G, T*(c+1)/G)
-  const int begin = static_cast<int>(static_cast<long long>(p.T) * c / G) * p.TPT;
-  const int end = static_cast<int>(static_cast<long long>(p.T) * (c + 1) / G) * p.TPT;
+  // Work: cluster c (of G) takes whole tokens [T*c/G, T*(c+1)/G); with a
+  // 2-CTA cluster, rank 0 takes tiles [0, PT0) of each and rank 1 the rest.
+  const int split = p.split;
+  const int rank = split > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int G = gridDim.x / split, c = blockIdx.x / split;
+  const int t0 = static_cast<int>(static_cast<long long>(p.T) * c / G);
+  const int t1 = static_cast<int>(static_cast<long long>(p.T) * (c + 1) / G);
+  const int J0 = rank * p.PT0;
+  const int PT = split == 1 ? p.TPT : (rank == 0 ? p.PT0 : p.TPT - p.PT0);
+  const int count = (t1 - t0) * PT;  // tiles of this CTA; tile n is tile J0 + n % PT of token t0 + n / PT
 
-  // zero the operand buffers once: rows never written by a copy stay finite
-  for (int i = tid; i < static_cast<int>(L::mask / 16); i += kThreads)
-    reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
   static_assert(L::total + 1024 <= 232448, "shared memory budget");
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -295,6 +367,8 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
     mbar_init(oempty, 4);
     mbar_init(done, 1);
     for (int i = 0; i < kMaskSlots; ++i) mbar_init(&mfull[i], 1);
+    mbar_init(xfull, 4);
+    mbar_init(xempty, 4);
     *abort_s = 0;
     fence_barrier_init();
   }
@@ -305,6 +379,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();
+  if (split > 1) cluster_sync();  // the partner's barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem = *tmem_base_s;
   auto fail = [&]() {
@@ -323,11 +398,21 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
       uint64_t *ring_full = is_k ? kfull : vfull;
       uint64_t *ring_empty = is_k ? kempty : vempty;
       uint8_t *ring = is_k ? ks : vs;
-      if (begin < end) {
+      if (count > 0) {
         if (warp == kKWarp0 && lane == 0) {
           prefetch_tmap(&qmap);
           prefetch_tmap(&kwmap);
           prefetch_tmap(&kcmap);
+        }
+        if (!is_k) {
+          // V rows of absent keys are never copied but are multiplied by P = 0:
+          // the ring starts zeroed so that they are finite.  (Absent K rows
+          // only reach logits the softmax masks; unused Q rows only reach
+          // accumulator lanes nobody reads.)
+          for (int i = pw * 32 + lane; i < kStages * 32768 / 16; i += 32 * kVWarps)
+            reinterpret_cast<uint4 *>(vs)[i] = make_uint4(0, 0, 0, 0);
+          fence_proxy_async();
+          asm volatile("bar.sync 1, %0;" ::"n"(32 * kVWarps) : "memory");
         }
         int qn = -1, prev_t = -1, issued = 0;
         Token tk{0, 0, 0};
@@ -335,8 +420,8 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         int n_w = 0;
         // idx entries of keys 4*lane .. 4*lane+3 of a compressed tile, loaded one
         // tile ahead so their latency overlaps the current tile's copies
-        auto load_idx = [&](int i, int32_t (&cc)[4]) {
-          const int t = i / p.TPT, j = i % p.TPT;
+        auto load_idx = [&](int n, int32_t (&cc)[4]) {
+          const int t = t0 + n / PT, j = J0 + n % PT;
   #pragma unroll
           for (int e = 0; e < 4; ++e) {
             cc[e] = -1;
@@ -345,15 +430,15 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
           }
         };
         int32_t cnext[4];
-        load_idx(begin, cnext);
-        for (int i = begin; i < end; ++i) {
+        load_idx(0, cnext);
+        for (int n = 0; n < count; ++n) {
           if (__any_sync(0xffffffffu, aborted())) break;
-          const int t = i / p.TPT, j = i % p.TPT, n = i - begin;
+          const int t = t0 + n / PT, j = J0 + n % PT;
           int32_t cidx[4] = {cnext[0], cnext[1], cnext[2], cnext[3]};
-          if (i + 1 < end) load_idx(i + 1, cnext);
+          if (n + 1 < count) load_idx(n + 1, cnext);
           if (t != prev_t) {
             tok_ok = load_token(p.q_seq, p.q_pos, t, p.B, p.N_c, p.r, p.status, tk,
-                                warp == kKWarp0 && lane == 0 && j == 0);
+                                warp == kKWarp0 && lane == 0 && j == J0);
             n_w = tok_ok ? min(p.W, tk.pos + 1) : 0;
             ++qn;
             if (warp == kKWarp0) {
@@ -477,16 +562,15 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
       // buffer) is issued after P.V(n), so the tensor core always has P.V(n)
       // queued while the issuer waits.  Every input of each step is produced by
       // work issued earlier in this order, so the blocking waits cannot deadlock.
-      if (lane == 0 && begin < end) {
+      if (lane == 0 && count > 0) {
         constexpr uint32_t idesc_s = idesc_bf16(128, kTile);              // K-major A, K-major B
         constexpr uint32_t idesc_o = idesc_bf16(128, kD) | (1u << 16);     // K-major A (tmem), MN-major B
-        const int count = end - begin;
         int qn_s = -1, prev_t_s = -1;  // token ordinal as seen by the S stage
         int tok_pv = -1;               // tokens started by the P.V stage
         bool ok = true;
         // S(n): Q of its token, its K tile and a free S/P buffer
         auto issue_s = [&](int n) -> bool {
-          const int i = begin + n, t = i / p.TPT, j = i % p.TPT;
+          const int t = t0 + n / PT, j = J0 + n % PT;
           const int s = n % kStages, b = n % kSBufs;
           if (t != prev_t_s) {
             ++qn_s;
@@ -505,15 +589,14 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
           }
           mma_commit(&sfull[b]);
           mma_commit(&kempty[s]);
-          if (j == p.TPT - 1) mma_commit(&qempty[qn_s & 1]);
+          if (j == J0 + PT - 1) mma_commit(&qempty[qn_s & 1]);
           return true;
         };
         // P.V(n): P of the tile (in its S/P buffer: keys 32c..32c+31 as hi in
         // columns 32c..32c+15 and lo in 32c+16..32c+31), its V tile, and O read
         // out after the previous token
         auto issue_pv = [&](int n) -> bool {
-          const int i = begin + n, j = i % p.TPT;
-          const bool first = j == 0;
+          const bool first = n % PT == 0;
           const int s = n % kStages, b = n % kSBufs;
           if (first && tok_pv >= 0 && !mbar_wait(oempty, tok_pv & 1)) return false;
           if (!mbar_wait(&pfull[b], (n / kSBufs) & 1) || !mbar_wait(&vfull[s], (n / kStages) & 1)) return false;
@@ -554,9 +637,9 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
     const int h = 16 * warp + hq;
     const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
     float m_ref = -INFINITY, l = 0.f;
-    for (int i = begin; i < end; ++i) {
-      const int n = i - begin, t = i / p.TPT, j = i % p.TPT;
-      const bool first = j == 0, last = j == p.TPT - 1;
+    int jj = 0, tok = 0;  // tile within the token's part, token ordinal
+    for (int n = 0; n < count; ++n, jj = (jj + 1 == PT) ? 0 : jj + 1, tok += jj == 0) {
+      const bool first = jj == 0, last = jj == PT - 1;
       if (first) {
         m_ref = -INFINITY;
         l = 0.f;
@@ -568,6 +651,8 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         break;
       }
       tc_fence_after();
+      // rank 0, last tile: S is done, so the K ring is free to take rank 1's part
+      if (split > 1 && rank == 0 && last && lane == 0) mbar_arrive_remote(xempty, 1);
       const uint32_t s_col = tmem + lane_base + 128 * b;
       uint32_t v[64];
       tmem_ld_16x2_x32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
@@ -634,42 +719,104 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         }
         tc_fence_after();
         const float l_all = l + __shfl_xor_sync(0xffffffffu, l, 16);
-        float Lden = l_all, a = 1.f;
-        if (p.sink) {
-          const float s2 = p.sink[h] * kLog2e;
-          const float M = fmaxf(m_ref, s2);
-          a = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - M);
-          Lden = l_all * a + exp2f(s2 - M);
-        }
-        const float inv = Lden > 0.f ? a / Lden : 0.f;
-        uint4 *dst = reinterpret_cast<uint4 *>(p.out + (static_cast<int64_t>(t) * kH + h) * kD + 64 * u);
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t o[32];
-          tmem_ld_16x2_x32(tmem + lane_base + kColO + 32 * c2, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const __nv_bfloat16 lo = __float2bfloat16_rn(__uint_as_float(o[8 * q + 2 * e]) * inv);
-              const __nv_bfloat16 hi = __float2bfloat16_rn(__uint_as_float(o[8 * q + 2 * e + 1]) * inv);
-              pk[e] = static_cast<uint32_t>(__bfloat16_as_ushort(lo)) |
-                      (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
-            }
-            dst[4 * c2 + q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        const int64_t row = static_cast<int64_t>(t0 + tok) * kH + h;
+        if (rank == 1) {
+          // second part of a split token: (m, l, O) go to rank 0's K ring
+          // (O as [64 heads][128] f32, then (m, l) per head) once it is free
+          if (!mbar_wait_cluster_warp(xempty, 0)) {
+            if (lane == 0) fail();
+            break;
           }
+          const uint32_t xo = cluster_map(ks + h * (kD * 4) + 64 * u * 4, 0);
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t o[16];
+            tmem_ld_16x2_x16(tmem + lane_base + kColO + 16 * c4, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_cluster_f4(xo + (16 * c4 + 4 * q) * 4, __uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+                            __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
+          }
+          if (u == 0) {
+            const uint32_t xml = cluster_map(ks + kH * kD * 4 + h * 8, 0);
+            asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(xml), "f"(m_ref), "f"(l_all) : "memory");
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive_remote(xfull, 0);
+            mbar_arrive(oempty);
+          }
+        } else {
+          // whole token, or the first part merged with rank 1's:
+          // O = a0 O0 + a1 O1, l = a0 l0 + a1 l1 against M = max(m0, m1)
+          float m1 = -INFINITY, l1 = 0.f;
+          const float4 *xo = reinterpret_cast<const float4 *>(ks + h * (kD * 4) + 64 * u * 4);
+          if (split > 1) {
+            if (!mbar_wait_cluster_warp(xfull, 0)) {
+              if (lane == 0) fail();
+              break;
+            }
+            const float2 ml = *reinterpret_cast<const float2 *>(ks + kH * kD * 4 + h * 8);
+            m1 = ml.x;
+            l1 = ml.y;
+          }
+          const float M = fmaxf(m_ref, m1);
+          const float a0 = m_ref == -INFINITY ? 0.f : exp2f(m_ref - M);
+          const float a1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
+          const float Lsum = l_all * a0 + l1 * a1;
+          float Lden = Lsum, a = 1.f;
+          if (p.sink) {
+            const float s2 = p.sink[h] * kLog2e;
+            const float Mf = fmaxf(M, s2);
+            a = (M == -INFINITY) ? 0.f : exp2f(M - Mf);
+            Lden = Lsum * a + exp2f(s2 - Mf);
+          }
+          const float inv = Lden > 0.f ? a / Lden : 0.f;
+          const float f0 = a0 * inv, f1 = a1 * inv;
+          uint4 *dst = reinterpret_cast<uint4 *>(p.out + row * kD + 64 * u);
+          // 16 of the thread's 64 columns at a time (columns 64u + 16c4 ..)
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t o[16];
+            tmem_ld_16x2_x16(tmem + lane_base + kColO + 16 * c4, o);
+            float x[16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 v4 = split > 1 ? xo[4 * c4 + q] : make_float4(0.f, 0.f, 0.f, 0.f);
+              x[4 * q] = v4.x;
+              x[4 * q + 1] = v4.y;
+              x[4 * q + 2] = v4.z;
+              x[4 * q + 3] = v4.w;
+            }
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              uint32_t pk[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int d = 8 * q + 2 * e;
+                const float y0 = fmaf(__uint_as_float(o[d]), f0, x[d] * f1);
+                const float y1 = fmaf(__uint_as_float(o[d + 1]), f0, x[d + 1] * f1);
+                pk[e] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(y0))) |
+                        (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(y1))) << 16);
+              }
+              dst[2 * c4 + q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(oempty);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(oempty);
       }
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  // neither CTA of a cluster leaves while the other may still arrive on its barriers
+  if (split > 1) cluster_sync();
   if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();
@@ -689,18 +836,51 @@ bool encode_rows(CUtensorMap *m, const void *base, uint64_t rows, uint32_t box_r
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// One CTA per SM, each over whole tokens (G <= T); a batch smaller than the
-// SM count leaves SMs idle rather than splitting tokens.
-int attn_umma_grid(const sa_index_args &ia) {
-  const int sms = sm_count();
-  return ia.T < sms ? ia.T : sms;
+size_t attn_smem_bytes() { return AttnSmem::total + 1024; }
+
+// 2-CTA clusters of this kernel that fit on the GPU at once (0 if unknown).
+int max_pair_clusters() {
+  static int cached[64];
+  static bool done[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!done[dev]) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = attn_smem_bytes();
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, sparse_mqa_umma_kernel, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    cached[dev] = n;
+    done[dev] = true;
+  }
+  return cached[dev];
+}
+
+// CTAs per token: 2 (a cluster pair, each CTA half of the token's tiles) when
+// every token can have its own pair at once, else 1 (whole tokens, one CTA per
+// SM at most).
+int attn_split(const sa_index_args &ia, int TPT) {
+  if (TPT < 2) return 1;
+  return ia.T <= max_pair_clusters() ? 2 : 1;
 }
 
 }  // namespace
 
 bool attn_umma_supported(const sa_attn_args &aa) { return aa.H == kH && aa.D == kD; }
 
-// The tensor-core attention keeps no scratch in global memory.
+// The tensor-core attention keeps no scratch in global memory (split tokens
+// hand their partials over in distributed shared memory).
 size_t attn_umma_scratch(const sa_index_args &, const sa_attn_args &, int) { return 0; }
 
 cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &aa, const int32_t *idx, int K,
@@ -730,8 +910,7 @@ cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &
       !encode_rows(&kwmap, aa.Kw, static_cast<uint64_t>(ia.B) * aa.R, 1) ||
       !encode_rows(&kcmap, aa.Kc, static_cast<uint64_t>(ia.B) * ia.N_c, 1))
     return cudaErrorInvalidValue;
-  const int G = attn_umma_grid(ia);
-  const size_t smem = AttnSmem::total + 1024;
+  const size_t smem = attn_smem_bytes();
   // the register split above assumes the kernel launches with kLaunchRegs
   // registers per thread; anything else could leave a raise waiting forever
   static int regs = -1;
@@ -745,8 +924,28 @@ cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &
   static bool attr_done[64] = {};
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(sparse_mqa_umma_kernel), smem, attr_done);
   if (e != cudaSuccess) return e;
-  sparse_mqa_umma_kernel<<<G, kThreads, smem, stream>>>(qmap, kwmap, kcmap, p);
-  return cudaGetLastError();
+  p.split = attn_split(ia, p.TPT);
+  p.PT0 = (p.TPT + 1) / 2;
+  const int sms = sm_count();
+  if (p.split == 1) {
+    const int G = ia.T < sms ? ia.T : sms;
+    sparse_mqa_umma_kernel<<<G, kThreads, smem, stream>>>(qmap, kwmap, kcmap, p);
+    return cudaGetLastError();
+  }
+  // one cluster pair per token
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * ia.T);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, sparse_mqa_umma_kernel, qmap, kwmap, kcmap, p);
 }
 
 }  // namespace sa
