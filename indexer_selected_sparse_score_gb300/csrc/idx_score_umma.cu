@@ -43,9 +43,19 @@ namespace {
 using namespace umma;
 
 constexpr int kTileKeys = 128;                   // M
-constexpr int kKeyTileBytes = kTileKeys * 128;   // 128 keys x 128 fp8
-constexpr int kStages = 8;
 constexpr int kAccStages = 4;
+constexpr int kKeyTileBytes = kTileKeys * 128;   // 128 keys x 128 fp8
+constexpr int kMaxStages = 8;                    // key-tile ring depth, as far as shared memory allows
+
+// Two CTAs share an SM when their tensor memory fits (kAccStages * NH columns
+// each): one CTA's MMA and epilogue latency then overlaps the other's copies.
+template <int NH>
+constexpr int kCtasPerSm = kAccStages * NH <= 256 ? 2 : 1;
+// Shared memory a CTA may lay out (less the 1 KB the driver reserves per CTA
+// and the 1 KB alignment slack): 228 KB per SM, 227 KB per CTA.
+template <int NH>
+constexpr size_t kSmemBudget = kCtasPerSm<NH> == 2 ? 233472 / 2 - 2048 : 232448 - 1024;
+constexpr int kScaleAhead = 8;                   // key-scale prefetch distance, in tiles
 constexpr int kMainThreads = 192;
 constexpr int kPrepThreads = 256;
 constexpr int kPlanPer = 32;  // tokens per thread per chunk of the plan scan
@@ -54,6 +64,13 @@ constexpr int kPlanSmemTokens = 8192;
 template <int NH, int P>
 struct ScoreSmem {
   static constexpr int kQBytes = P * NH * 128;
+  // everything but the key ring: two query buffers, two weight vectors, barriers (at most
+  // 2 * kMaxStages + 13 of them) and the misc words
+  static constexpr size_t kFixed = 2 * static_cast<size_t>(kQBytes) + 2 * NH * sizeof(float) +
+                                   (2 * kMaxStages + 13) * sizeof(uint64_t) + 64 + 8;
+  static constexpr int kStages = static_cast<int>(
+      (kSmemBudget<NH> - kFixed) / kKeyTileBytes < kMaxStages ? (kSmemBudget<NH> - kFixed) / kKeyTileBytes
+                                                                : kMaxStages);
   static constexpr size_t keys = 0;
   static constexpr size_t qbuf = keys + static_cast<size_t>(kStages) * kKeyTileBytes;
   static constexpr size_t wq = qbuf + 2 * static_cast<size_t>(kQBytes);
@@ -61,6 +78,7 @@ struct ScoreSmem {
   static constexpr int kBars = 2 * kStages + 4 + 2 * kAccStages + 1;
   static constexpr size_t misc = bars + kBars * sizeof(uint64_t);
   static constexpr size_t total = misc + 64;
+  static_assert(total <= kSmemBudget<NH>, "shared memory budget");
 };
 
 // ---------------------------------------------------------------- prep ----
@@ -287,6 +305,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParams p) {
   using L = ScoreSmem<NH, P>;
   constexpr int kQBytes = L::kQBytes;
+  constexpr int kStages = L::kStages;
   constexpr uint32_t kTmemCols = kAccStages * NH;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the swizzle atoms need 1024-byte alignment: align the base explicitly
@@ -374,48 +393,61 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
-    if (lane == 0 && begin < end) {
+    // The whole warp walks the tiles and waits; one elected lane issues the
+    // MMAs and commits from operands the warp computed uniformly.
+    if (begin < end) {
       constexpr uint32_t idesc = idesc_e4m3(kTileKeys, NH);
+      const bool leader = elect_one();
       TileCursor cur;
       cur.start(p, t_first);
       int prev_t = -1, qn = -1;
-      for (int i = begin; i < end && !*(volatile int *)abort_s; ++i) {
+      bool ok = true;
+      for (int i = begin; i < end; ++i) {
+        if (__any_sync(0xffffffffu, *(volatile int *)abort_s != 0)) break;
         cur.seek(p, i);
         const int t = cur.t;
         if (t != prev_t) {
-          if (qn >= 0) mma_commit(&qempty[qn & 1]);
+          if (qn >= 0 && leader) mma_commit(&qempty[qn & 1]);
           ++qn;
-          if (!mbar_wait(&qfull[qn & 1], (qn >> 1) & 1)) { fail(); break; }
+          if (!mbar_wait_warp(&qfull[qn & 1], (qn >> 1) & 1)) { ok = false; break; }
           prev_t = t;
         }
         const int n = i - begin, s = n % kStages, a = n % kAccStages;
-        if (!mbar_wait(&kfull[s], (n / kStages) & 1)) { fail(); break; }
-        if (!mbar_wait(&aempty[a], ((n / kAccStages) & 1) ^ 1)) { fail(); break; }
+        if (!mbar_wait_warp(&kfull[s], (n / kStages) & 1) ||
+            !mbar_wait_warp(&aempty[a], ((n / kAccStages) & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + a * NH;
         const uint32_t a0 = smem_u32(keys + s * kKeyTileBytes);
         const uint32_t b0 = smem_u32(qbuf + (qn & 1) * kQBytes);
+        if (leader) {
 #pragma unroll
-        for (int pc = 0; pc < P; ++pc)
+          for (int pc = 0; pc < P; ++pc)
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_f8f6f4(d, desc_sw128_kmajor(a0 + 32 * k), desc_sw128_kmajor(b0 + pc * NH * 128 + 32 * k),
-                       idesc, (pc | k) != 0);
-        mma_commit(&kempty[s]);
-        mma_commit(&afull[a]);
+            for (int k = 0; k < 4; ++k)
+              mma_f8f6f4(d, desc_sw128_kmajor(a0 + 32 * k), desc_sw128_kmajor(b0 + pc * NH * 128 + 32 * k),
+                         idesc, (pc | k) != 0);
+          mma_commit(&kempty[s]);
+          mma_commit(&afull[a]);
+        }
+        __syncwarp();
       }
-      if (qn >= 0) mma_commit(&qempty[qn & 1]);
-      mma_commit(done);
-      if (!mbar_wait(done, 0)) raise_flag(p.status, kFlagTimeout);
+      if (!ok && lane == 0) fail();
+      if (leader) {
+        if (qn >= 0) mma_commit(&qempty[qn & 1]);
+        mma_commit(done);
+        if (!mbar_wait(done, 0)) raise_flag(p.status, kFlagTimeout);
+      }
+      __syncwarp();
     }
   } else {
     // --------------------------------------------------------- epilogue
-    // The key scales of the next tile are loaded while this tile is reduced
-    // (their latency would otherwise stall every tile).
+    // The key scales are loaded kScaleAhead tiles ahead into a register
+    // queue: under a full memory stream their latency spans several tiles and
+    // would otherwise pace the whole pipeline.
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     if (begin < end) {
-      TileCursor cur, ahead;  // `ahead` runs one tile in front for the scale prefetch
+      TileCursor cur, ahead;  // `ahead` runs kScaleAhead tiles in front for the scale prefetch
       cur.start(p, t_first);
       ahead.start(p, t_first);
       int prev_t = -1, qn = -1;
@@ -424,15 +456,25 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
         if (!p.k_scale || ss >= c.nv) return 1.f;
         return p.k_scale[static_cast<int64_t>(c.b) * p.N_c + ss];
       };
-      float ks_next = scale_at(ahead, begin);
+      float ksq[kScaleAhead];  // scales of tiles i .. i + kScaleAhead - 1
+#pragma unroll
+      for (int k = 0; k < kScaleAhead; ++k) {
+        ksq[k] = 1.f;
+        if (begin + k < end) {
+          ahead.seek(p, begin + k);
+          ksq[k] = scale_at(ahead, begin + k);
+        }
+      }
       for (int i = begin; i < end && !*(volatile int *)abort_s; ++i) {
         cur.seek(p, i);
-        const int t = cur.t, b = cur.b, nv = cur.nv;
-        (void)b;
-        const float ks = ks_next;
-        if (i + 1 < end) {
-          ahead.seek(p, i + 1);
-          ks_next = scale_at(ahead, i + 1);
+        const int t = cur.t, nv = cur.nv;
+        const float ks = ksq[0];
+#pragma unroll
+        for (int k = 0; k + 1 < kScaleAhead; ++k) ksq[k] = ksq[k + 1];
+        ksq[kScaleAhead - 1] = 1.f;
+        if (i + kScaleAhead < end) {
+          ahead.seek(p, i + kScaleAhead);
+          ksq[kScaleAhead - 1] = scale_at(ahead, i + kScaleAhead);
         }
         if (t != prev_t) {
           if (qn >= 0) {
@@ -488,7 +530,7 @@ cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld,
                              cudaStream_t stream) {
   constexpr int P = QFP8 ? 1 : 2;
   using L = ScoreSmem<NH, P>;
-  const int grid = sm_count();
+  const int grid = sm_count() * kCtasPerSm<NH>;
   idx_qprep_kernel<NH, QFP8><<<ia.T + 1, kPrepThreads, 0, stream>>>(
       ia.B, ia.T, ia.N_c, ia.r, ia.q_seq, ia.q_pos, ia.q_I, ia.q_scale, ia.w, qpack, wq, scores, ld,
       write_masked ? 1 : 0, prefix, start, grid, status);
@@ -571,7 +613,7 @@ UmmaScratch umma_scratch_layout(const sa_index_args &ia) {
   L.wq = up(static_cast<size_t>(ia.T) * P * ia.H_I * 128);
   L.prefix = L.wq + up(static_cast<size_t>(ia.T) * ia.H_I * 4);
   L.start = L.prefix + up(static_cast<size_t>(ia.T + 1) * 4);
-  L.total = L.start + up(static_cast<size_t>(sm_count() + 1) * 4);
+  L.total = L.start + up(static_cast<size_t>(2 * sm_count() + 1) * 4);  // up to two CTAs per SM
   return L;
 }
 }  // namespace
