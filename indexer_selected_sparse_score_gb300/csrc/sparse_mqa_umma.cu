@@ -422,7 +422,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         // tile ahead so their latency overlaps the current tile's copies
         auto load_idx = [&](int n, int32_t (&cc)[4]) {
           const int t = t0 + n / PT, j = J0 + n % PT;
-  #pragma unroll
+#pragma unroll
           for (int e = 0; e < 4; ++e) {
             cc[e] = -1;
             const int k = (j - p.WT) * kTile + 4 * lane + e;
@@ -449,9 +449,9 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
                 if (ok) {
                   // heads 16w..16w+15 -> rows 32w+16qb .. +15, both 64-column halves
                   mbar_expect_tx(&qfull[qb], 2 * kH * 128);
-  #pragma unroll
+#pragma unroll
                   for (int w = 0; w < 4; ++w)
-  #pragma unroll
+#pragma unroll
                     for (int kb = 0; kb < 2; ++kb)
                       tma_load_2d(qs + kb * 16384 + (32 * w + 16 * qb) * 128, &qmap, &qfull[qb], 64 * kb,
                                   t * kH + 16 * w);
@@ -467,7 +467,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
           const bool window = j < p.WT;
           int rows[4];
           bool valid[4];
-  #pragma unroll
+#pragma unroll
           for (int e = 0; e < 4; ++e) {
             rows[e] = 0;
             valid[e] = false;
@@ -493,10 +493,10 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
           }
           if (warp == kKWarp0) {  // key mask of the tile: bit g of word e = key 4g+e exists
             uint32_t m4[4];
-  #pragma unroll
+#pragma unroll
             for (int e = 0; e < 4; ++e) m4[e] = __ballot_sync(0xffffffffu, valid[e]);
             if (lane == 0) {
-  #pragma unroll
+#pragma unroll
               for (int e = 0; e < 4; ++e) mask_s[(n % kMaskSlots) * 4 + e] = m4[e];
               mbar_arrive(&mfull[n % kMaskSlots]);
             }
@@ -511,7 +511,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
             const int c0 = lane * nw + pw;
             const int g = c0 & 31, half = c0 >> 5;
             int gr[4];
-  #pragma unroll
+#pragma unroll
             for (int e = 0; e < 4; ++e) gr[e] = __shfl_sync(0xffffffffu, valid[e] ? rows[e] : fill, g);
             const bool gany = __shfl_sync(0xffffffffu, any4, g);
             const bool mine = c0 < 64 && gany;
@@ -562,7 +562,9 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
       // buffer) is issued after P.V(n), so the tensor core always has P.V(n)
       // queued while the issuer waits.  Every input of each step is produced by
       // work issued earlier in this order, so the blocking waits cannot deadlock.
-      if (lane == 0 && count > 0) {
+      // The whole warp waits; one elected lane issues from warp-uniform operands.
+      if (count > 0) {
+        const bool leader = elect_one();
         constexpr uint32_t idesc_s = idesc_bf16(128, kTile);              // K-major A, K-major B
         constexpr uint32_t idesc_o = idesc_bf16(128, kD) | (1u << 16);     // K-major A (tmem), MN-major B
         int qn_s = -1, prev_t_s = -1;  // token ordinal as seen by the S stage
@@ -575,21 +577,25 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
           if (t != prev_t_s) {
             ++qn_s;
             prev_t_s = t;
-            if (!mbar_wait(&qfull[qn_s & 1], (qn_s >> 1) & 1)) return false;
+            if (!mbar_wait_warp(&qfull[qn_s & 1], (qn_s >> 1) & 1)) return false;
           }
-          if (!mbar_wait(&kfull[s], (n / kStages) & 1) || !mbar_wait(&sempty[b], ((n / kSBufs) & 1) ^ 1))
+          if (!mbar_wait_warp(&kfull[s], (n / kStages) & 1) ||
+              !mbar_wait_warp(&sempty[b], ((n / kSBufs) & 1) ^ 1))
             return false;
           tc_fence_after();
           const uint32_t a0 = smem_u32(qs + (qn_s & 1) * 2048), b0 = smem_u32(ks + s * 32768);
           const uint32_t d = tmem + 128 * b;
-  #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_f16(d, desc_sw128_kmajor(a0 + off), desc_sw128_kmajor(b0 + off), idesc_s, kk > 0);
+          if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+              mma_f16(d, desc_sw128_kmajor(a0 + off), desc_sw128_kmajor(b0 + off), idesc_s, kk > 0);
+            }
+            mma_commit(&sfull[b]);
+            mma_commit(&kempty[s]);
+            if (j == J0 + PT - 1) mma_commit(&qempty[qn_s & 1]);
           }
-          mma_commit(&sfull[b]);
-          mma_commit(&kempty[s]);
-          if (j == J0 + PT - 1) mma_commit(&qempty[qn_s & 1]);
+          __syncwarp();
           return true;
         };
         // P.V(n): P of the tile (in its S/P buffer: keys 32c..32c+31 as hi in
@@ -598,30 +604,37 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         auto issue_pv = [&](int n) -> bool {
           const bool first = n % PT == 0;
           const int s = n % kStages, b = n % kSBufs;
-          if (first && tok_pv >= 0 && !mbar_wait(oempty, tok_pv & 1)) return false;
-          if (!mbar_wait(&pfull[b], (n / kSBufs) & 1) || !mbar_wait(&vfull[s], (n / kStages) & 1)) return false;
+          if (first && tok_pv >= 0 && !mbar_wait_warp(oempty, tok_pv & 1)) return false;
+          if (!mbar_wait_warp(&pfull[b], (n / kSBufs) & 1) || !mbar_wait_warp(&vfull[s], (n / kStages) & 1))
+            return false;
           if (first) ++tok_pv;
           fence_proxy_async();  // V arrived through the generic proxy; the MMA reads it through the async one
           tc_fence_after();
           const uint32_t v0 = smem_u32(vs + s * 32768), pb = tmem + 128 * b;
-  #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // keys 16kk .. 16kk+15
-            const uint64_t bdesc = desc_sw128_mnmajor(v0 + kk * 2048, 16384);
-            const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
-            mma_f16_ta(tmem + kColO, pb + col, bdesc, idesc_o, !(first && kk == 0));
-            mma_f16_ta(tmem + kColO, pb + col + 16, bdesc, idesc_o, 1);
+          if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {  // keys 16kk .. 16kk+15
+              const uint64_t bdesc = desc_sw128_mnmajor(v0 + kk * 2048, 16384);
+              const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
+              mma_f16_ta(tmem + kColO, pb + col, bdesc, idesc_o, !(first && kk == 0));
+              mma_f16_ta(tmem + kColO, pb + col + 16, bdesc, idesc_o, 1);
+            }
+            mma_commit(&vempty[s]);
+            mma_commit(&sempty[b]);
           }
-          mma_commit(&vempty[s]);
-          mma_commit(&sempty[b]);
+          __syncwarp();
           return true;
         };
         for (int n = 0; ok && n < 2 && n < count; ++n) ok = issue_s(n);
         for (int n = 0; ok && n < count; ++n) {
-          if (aborted() || !issue_pv(n) || (n + 2 < count && !issue_s(n + 2))) ok = false;
+          if (__any_sync(0xffffffffu, aborted()) || !issue_pv(n) || (n + 2 < count && !issue_s(n + 2))) ok = false;
         }
-        if (!ok) fail();
-        mma_commit(done);
-        if (!mbar_wait(done, 0)) raise_flag(p.status, kFlagTimeout);
+        if (!ok && lane == 0) fail();
+        if (leader) {
+          mma_commit(done);
+          if (!mbar_wait(done, 0)) raise_flag(p.status, kFlagTimeout);
+        }
+        __syncwarp();
       }
     }
   } else {
