@@ -20,6 +20,18 @@ __device__ __forceinline__ void raise_flag(uint32_t *status, uint32_t f) {
   if (status) atomicOr(status, f);
 }
 
+// Programmatic dependent launch.  The kernels of one call run in a chain
+// (query prep -> index scores -> top-k -> attention); each kernel after the
+// first is launched so that it may start while its predecessor runs, does its
+// set-up, and then pdl_wait()s: that returns once the predecessor has
+// completed and its writes are visible (a no-op for an ordinary launch).
+// pdl_trigger() lets the successor start; a successor only starts once every
+// CTA of this kernel has triggered or exited, i.e. is already resident, so it
+// can never hold resources this kernel still needs.  Every CTA of a waiting
+// kernel waits, so completion is transitive along the chain.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Visible compressed entries of a token at absolute position p: compressed
 // entry j covers tokens [j*r, (j+1)*r) and is visible once p >= (j+1)*r - 1.
 __device__ __forceinline__ int n_vis_of(int pos, int r) { return (pos + 1) / r; }

@@ -83,9 +83,8 @@ struct ScoreSmem {
 
 // ---------------------------------------------------------------- prep ----
 
-__device__ __forceinline__ int tiles_of_token(int B, int N_c, int r, const int32_t *q_seq, const int32_t *q_pos,
-                                              int t) {
-  const int b = q_seq[t], pos = q_pos[t];
+// Key tiles of a token of sequence b at position pos (0 for an invalid token).
+__device__ __forceinline__ int tiles_of(int B, int N_c, int r, int b, int pos) {
   if (b < 0 || b >= B || pos < 0) return 0;
   const int nv = min(n_vis_of(pos, r), N_c);
   return (nv + kTileKeys - 1) / kTileKeys;
@@ -136,6 +135,7 @@ idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq
                  int grid, uint32_t *status) {
   constexpr int P = QFP8 ? 1 : 2;
   constexpr int kHeadsPerWarp = NH / (kPrepThreads / 32);
+  pdl_trigger();
   const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (t == T) {
     __shared__ int warp_sums[32];
@@ -146,11 +146,20 @@ idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq
     __syncthreads();
     for (int base = 0; base < T; base += kPrepThreads * kPlanPer) {
       const int t0 = base + threadIdx.x * kPlanPer;
+      // all loads of the chunk first (no branch depends on a loaded value
+      // before the last load is issued), then the tile counts
+      int sq[kPlanPer], ps[kPlanPer];
+#pragma unroll
+      for (int k = 0; k < kPlanPer; ++k) {
+        const bool in = t0 + k < T;
+        sq[k] = in ? q_seq[t0 + k] : -1;
+        ps[k] = in ? q_pos[t0 + k] : -1;
+      }
       int tl[kPlanPer];
       int sum = 0;
 #pragma unroll
       for (int k = 0; k < kPlanPer; ++k) {
-        tl[k] = (t0 + k < T) ? tiles_of_token(B, N_c, r, q_seq, q_pos, t0 + k) : 0;
+        tl[k] = tiles_of(B, N_c, r, sq[k], ps[k]);
         sum += tl[k];
       }
       const int incl = plan_block_scan(sum, warp_sums);
@@ -186,6 +195,14 @@ idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq
   }
 
   uint8_t *dst = qpack + static_cast<size_t>(t) * P * NH * 128;
+  // every global load first (one round trip): lane i < kHeadsPerWarp holds the
+  // weight and query scale of the warp's head i
+  float w_pre = 0.f, qs_pre = 1.f;
+  if (lane < kHeadsPerWarp) {
+    const int64_t hi = static_cast<int64_t>(t) * NH + warp + (kPrepThreads / 32) * lane;
+    w_pre = w[hi];
+    if (q_scale) qs_pre = q_scale[hi];
+  }
   if (QFP8) {
     uint32_t v[kHeadsPerWarp];
 #pragma unroll
@@ -198,10 +215,8 @@ idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq
     for (int i = 0; i < kHeadsPerWarp; ++i) {
       const int h = warp + (kPrepThreads / 32) * i;
       *reinterpret_cast<uint32_t *>(dst + umma::sw128_offset(h, 4 * lane)) = v[i];
-      if (lane == 0) {
-        const float qsc = q_scale ? q_scale[static_cast<int64_t>(t) * NH + h] : 1.f;
-        wq[static_cast<int64_t>(t) * NH + h] = w[static_cast<int64_t>(t) * NH + h] * qsc;
-      }
+      const float wh = __shfl_sync(0xffffffffu, w_pre, i), qh = __shfl_sync(0xffffffffu, qs_pre, i);
+      if (lane == 0) wq[static_cast<int64_t>(t) * NH + h] = wh * qh;
     }
   } else {
     uint2 raw[kHeadsPerWarp];
@@ -238,10 +253,8 @@ idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq
       }
       *reinterpret_cast<uint32_t *>(dst + umma::sw128_offset(h, 4 * lane)) = w1;
       *reinterpret_cast<uint32_t *>(dst + NH * 128 + umma::sw128_offset(h, 4 * lane)) = w2;
-      if (lane == 0) {
-        const float qsc = q_scale ? q_scale[static_cast<int64_t>(t) * NH + h] : 1.f;
-        wq[static_cast<int64_t>(t) * NH + h] = ldexpf(w[static_cast<int64_t>(t) * NH + h] * qsc, e);
-      }
+      const float wh = __shfl_sync(0xffffffffu, w_pre, i), qh = __shfl_sync(0xffffffffu, qs_pre, i);
+      if (lane == 0) wq[static_cast<int64_t>(t) * NH + h] = ldexpf(wh * qh, e);
     }
   }
   if (write_masked) {
@@ -322,6 +335,7 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
   int *abort_s = reinterpret_cast<int *>(smem + L::misc + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();
 
   // ---- set-up: barriers, tensor memory
   if (tid == 0) {
@@ -350,6 +364,7 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
   tc_fence_after();
   const uint32_t tmem = *tmem_base_s;
 
+  pdl_wait();  // the plan, packed queries and weights come from the prep kernel
   const int total = p.prefix[p.T];
   const int begin = static_cast<int>((static_cast<long long>(total) * blockIdx.x) / gridDim.x);
   const int end = static_cast<int>((static_cast<long long>(total) * (blockIdx.x + 1)) / gridDim.x);
@@ -556,8 +571,9 @@ cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld,
   static bool attr_done[64] = {};
   e = set_smem_once(reinterpret_cast<const void *>(kern), smem, attr_done);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kMainThreads, smem, stream>>>(kmap, sp);
-  return cudaGetLastError();
+  // the prep kernel is short: overlapping this kernel's launch and set-up
+  // with it pays; later edges of the chain gain nothing from early starts
+  return launch_ex(true, kern, dim3(grid), dim3(kMainThreads), smem, stream, 1, kmap, sp);
 }
 
 }  // namespace

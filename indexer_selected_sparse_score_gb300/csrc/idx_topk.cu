@@ -32,6 +32,8 @@ topk_radix_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, 
   __shared__ uint32_t warp_eq[kTopkWarps], warp_take[kTopkWarps];
   __shared__ uint32_t sh_digit, sh_above;
 
+  pdl_trigger();
+  pdl_wait();  // the scores come from the previous kernel
   const int t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   Token tk;
@@ -222,10 +224,12 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
                 int32_t *__restrict__ idx, uint32_t *status) {
   __shared__ uint32_t hist[2048];
   __shared__ uint32_t warp_sums[33];
+  pdl_trigger();
   const int t = blockIdx.x, tid = threadIdx.x;
   Token tk;
   const bool ok = load_token(q_seq, q_pos, t, B, N_c, r, status, tk, tid == 0);
   const int nv = ok ? tk.nv : 0;
+  pdl_wait();  // the scores come from the previous kernel
   int32_t *out = idx + static_cast<int64_t>(t) * K;
   if (nv <= K) {  // every visible position is kept
     for (int i = tid; i < K; i += kTopkThreads) out[i] = i < nv ? i : -1;
@@ -280,19 +284,12 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const sa_index_args &ia
                         int32_t *idx, uint32_t *status, cudaStream_t stream) {
   if (ia.T == 0 || K == 0) return cudaSuccess;
   // a row holds at most N_c visible scores
-  if (ia.N_c <= kRegMax / 4)
-    topk_reg_kernel<kRegE / 4><<<ia.T, kTopkThreads, 0, stream>>>(scores, ld, ia.B, ia.N_c, ia.r, ia.q_seq,
-                                                                   ia.q_pos, K, idx, status);
-  else if (ia.N_c <= kRegMax / 2)
-    topk_reg_kernel<kRegE / 2><<<ia.T, kTopkThreads, 0, stream>>>(scores, ld, ia.B, ia.N_c, ia.r, ia.q_seq,
-                                                                   ia.q_pos, K, idx, status);
-  else if (ia.N_c <= kRegMax)
-    topk_reg_kernel<kRegE><<<ia.T, kTopkThreads, 0, stream>>>(scores, ld, ia.B, ia.N_c, ia.r, ia.q_seq,
-                                                               ia.q_pos, K, idx, status);
-  else
-    topk_radix_kernel<<<ia.T, kTopkThreads, 0, stream>>>(scores, ld, ia.B, ia.N_c, ia.r, ia.q_seq,
-                                                         ia.q_pos, K, idx, status);
-  return cudaGetLastError();
+  auto kern = ia.N_c <= kRegMax / 4   ? topk_reg_kernel<kRegE / 4>
+              : ia.N_c <= kRegMax / 2 ? topk_reg_kernel<kRegE / 2>
+              : ia.N_c <= kRegMax     ? topk_reg_kernel<kRegE>
+                                      : topk_radix_kernel;
+  return launch_ex(false, kern, dim3(ia.T), dim3(kTopkThreads), 0, stream, 1, scores, ld, ia.B, ia.N_c, ia.r, ia.q_seq,
+                    ia.q_pos, K, idx, status);
 }
 
 }  // namespace sa

@@ -381,6 +381,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
   __syncthreads();
   if (split > 1) cluster_sync();  // the partner's barriers are initialised before any remote arrival
   tc_fence_after();
+  pdl_wait();  // the selected indices come from the previous kernel
   const uint32_t tmem = *tmem_base_s;
   auto fail = [&]() {
     raise_flag(p.status, kFlagTimeout);
@@ -940,25 +941,10 @@ cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &
   p.split = attn_split(ia, p.TPT);
   p.PT0 = (p.TPT + 1) / 2;
   const int sms = sm_count();
-  if (p.split == 1) {
-    const int G = ia.T < sms ? ia.T : sms;
-    sparse_mqa_umma_kernel<<<G, kThreads, smem, stream>>>(qmap, kwmap, kcmap, p);
-    return cudaGetLastError();
-  }
-  // one cluster pair per token
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * ia.T);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = 2;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, sparse_mqa_umma_kernel, qmap, kwmap, kcmap, p);
+  // whole tokens (at most one CTA per SM), or one cluster pair per token
+  const int grid = p.split == 1 ? (ia.T < sms ? ia.T : sms) : 2 * ia.T;
+  return launch_ex(false, sparse_mqa_umma_kernel, dim3(grid), dim3(kThreads), smem, stream, p.split, qmap, kwmap, kcmap,
+                    p);
 }
 
 }  // namespace sa
