@@ -82,9 +82,9 @@ def peaks():
         return 6800.0, "fallback"
 
 
-STAGE_SOURCES = {"idx_score": ("idx_score.cu", "idx_score_umma.cu", "umma.cuh"),
-                 "idx_topk": ("idx_topk.cu",),
-                 "sparse_mqa": ("sparse_mqa.cu", "sparse_mqa_umma.cu", "umma.cuh")}
+STAGE_SOURCES = {"idx_score": ("idx_score.cu", "idx_score_umma.cu", "umma.cuh", "common.cuh"),
+                 "idx_topk": ("idx_topk.cu", "common.cuh"),
+                 "sparse_mqa": ("sparse_mqa.cu", "sparse_mqa_umma.cu", "umma.cuh", "common.cuh")}
 
 
 def kernel_source_hash(stage):
