@@ -131,13 +131,18 @@ topk_radix_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, 
 
 // ---------------------------------------------------------------------------
 // Register-resident variant for rows of up to kRegMax scores: each thread
-// holds a contiguous block of E = ceil(n / 1024) keys, the K-th largest key is
-// found by three radix passes of 11, 11 and 10 bits (warp-aggregated
-// shared-memory histograms, one block-wide scan each), and the output offsets
-// come from a single block scan of packed (greater, equal) counts: the number
-// of picks before a thread is greater_before + min(equal_before, needed).
+// holds a contiguous block of E = ceil(n / 1024) keys.  The keys are first
+// reduced to their range (key - min, an order-preserving shift), so the radix
+// digits cover only the L = bit length of (max - min) bits the row actually
+// uses: the first 13-bit pass spreads the row over its bins (plain shared
+// atomics, little contention) and the next pass (two cover a 26-bit range)
+// sees only the keys of the chosen bin.  The output offsets come from a single block scan of packed
+// (greater, equal) counts: the number of picks before a thread is
+// greater_before + min(equal_before, needed).
 
 constexpr int kRegMax = 32768;
+constexpr int kDigitBits = 11;                 // radix digit width
+constexpr int kDigitBins = 1 << kDigitBits;
 constexpr int kRegE = kRegMax / kTopkThreads;  // 32 keys per thread at most
 
 // Block-wide exclusive scan of one uint32 per thread; returns the prefix and
@@ -177,42 +182,44 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_s
 template <int E>
 __device__ __forceinline__ uint32_t radix_pass(const uint32_t (&key)[E], int cnt, uint32_t prefix, uint32_t mask,
                                                int shift, int nbins, uint32_t *hist, uint32_t *warp_sums,
-                                               int &remaining) {
-  const int tid = threadIdx.x, lane = tid & 31;
+                                               int &remaining, uint32_t &in_bin) {
+  constexpr int R = kDigitBins / kTopkThreads;  // ranks (bins) per thread in the scan
+  const int tid = threadIdx.x;
   for (int i = tid; i < nbins; i += kTopkThreads) hist[i] = 0;
   __syncthreads();
 #pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const bool in = e < cnt && (key[e] & mask) == prefix;
-    const uint32_t active = __ballot_sync(0xffffffffu, in);
-    if (in) {
-      const uint32_t bin = (key[e] >> shift) & static_cast<uint32_t>(nbins - 1);
-      const uint32_t peers = __match_any_sync(active, bin);
-      if ((__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], __popc(peers));
-    }
-  }
+  for (int e = 0; e < E; ++e)
+    if (e < cnt && (key[e] & mask) == prefix)
+      atomicAdd(&hist[(key[e] >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
   __syncthreads();
-  // bins in descending order: thread t owns ranks r = 2t, 2t+1 (bin = nbins-1-r)
-  uint32_t c0 = 0, c1 = 0;
-  const int r0 = 2 * tid;
-  if (r0 < nbins) c0 = hist[nbins - 1 - r0];
-  if (r0 + 1 < nbins) c1 = hist[nbins - 2 - r0];
+  // bins in descending order: thread t owns ranks r = R t .. R t + R - 1 (bin = nbins-1-r)
+  uint32_t c[R], sum = 0;
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+    const int rk = R * tid + k;
+    c[k] = rk < nbins ? hist[nbins - 1 - rk] : 0u;
+    sum += c[k];
+  }
   uint32_t total;
-  const uint32_t before = block_excl_scan(c0 + c1, warp_sums, &total);
-  __shared__ uint32_t sel_digit, sel_above;
+  const uint32_t before = block_excl_scan(sum, warp_sums, &total);
+  __shared__ uint32_t sel_digit, sel_above, sel_count;
   const uint32_t rem = static_cast<uint32_t>(remaining);
-  if (before < rem && rem <= before + c0 + c1) {
-    if (rem <= before + c0) {
-      sel_digit = nbins - 1 - r0;
-      sel_above = before;
-    } else {
-      sel_digit = nbins - 2 - r0;
-      sel_above = before + c0;
+  if (before < rem && rem <= before + sum) {
+    uint32_t run = before;
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+      if (run < rem && rem <= run + c[k]) {
+        sel_digit = nbins - 1 - (R * tid + k);
+        sel_above = run;
+        sel_count = c[k];
+      }
+      run += c[k];
     }
   }
   __syncthreads();
   remaining -= static_cast<int>(sel_above);
   const uint32_t d = sel_digit;
+  in_bin = sel_count;
   __syncthreads();
   return d;
 }
@@ -222,7 +229,7 @@ __global__ void __launch_bounds__(kTopkThreads)
 topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, int r,
                 const int32_t *__restrict__ q_seq, const int32_t *__restrict__ q_pos, int K,
                 int32_t *__restrict__ idx, uint32_t *status) {
-  __shared__ uint32_t hist[2048];
+  __shared__ uint32_t hist[kDigitBins];
   __shared__ uint32_t warp_sums[33];
   pdl_trigger();
   const int t = blockIdx.x, tid = threadIdx.x;
@@ -243,13 +250,72 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
 #pragma unroll
   for (int e = 0; e < E; ++e) key[e] = e < cnt ? ordered_key(row[lo + e]) : 0u;
 
+  // the row's key range: keys become key - min (< 2^L)
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    if (e < cnt) {
+      kmin = min(kmin, key[e]);
+      kmax = max(kmax, key[e]);
+    }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  __shared__ uint32_t wmin[kTopkWarps], wmax[kTopkWarps];
+  const int lane = tid & 31, warp = tid >> 5;
+  if (lane == 0) {
+    wmin[warp] = kmin;
+    wmax[warp] = kmax;
+  }
+  __syncthreads();
+  kmin = __reduce_min_sync(0xffffffffu, wmin[lane]);
+  kmax = __reduce_max_sync(0xffffffffu, wmax[lane]);
+#pragma unroll
+  for (int e = 0; e < E; ++e) key[e] = e < cnt ? key[e] - kmin : 0u;
+  const int L = kmax > kmin ? 32 - __clz(kmax - kmin) : 0;
+
+  // radix select over bits [0, L), kDigitBits at a time from the top; once
+  // the chosen bin holds at most 32 keys, one warp ranks them directly
   int remaining = K;
-  const uint32_t d1 = radix_pass<E>(key, cnt, 0u, 0u, 21, 2048, hist, warp_sums, remaining);
-  const uint32_t p1 = d1 << 21, m1 = 0xFFE00000u;
-  const uint32_t d2 = radix_pass<E>(key, cnt, p1, m1, 10, 2048, hist, warp_sums, remaining);
-  const uint32_t p2 = p1 | (d2 << 10), m2 = 0xFFFFFC00u;
-  const uint32_t d3 = radix_pass<E>(key, cnt, p2, m2, 0, 1024, hist, warp_sums, remaining);
-  const uint32_t thr = p2 | d3;
+  uint32_t thr = 0u;
+  __shared__ uint32_t cand[32], ncand, fin_thr, fin_above;
+  for (int hi = L; hi > 0;) {
+    const int nb = hi < kDigitBits ? hi : kDigitBits, shift = hi - nb;
+    const uint32_t mask = hi >= 32 ? 0u : ~((1u << hi) - 1u);  // bits already fixed
+    uint32_t in_bin;
+    const uint32_t d = radix_pass<E>(key, cnt, thr, mask, shift, 1 << nb, hist, warp_sums, remaining, in_bin);
+    thr |= d << shift;
+    hi = shift;
+    if (hi > 0 && in_bin <= 32u) {
+      // gather the bin's keys (those matching every fixed bit)
+      if (tid == 0) ncand = 0;
+      __syncthreads();
+      const uint32_t fixed = ~((1u << hi) - 1u);
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if (e < cnt && (key[e] & fixed) == thr) cand[atomicAdd(&ncand, 1u)] = key[e];
+      __syncthreads();
+      if (warp == 0) {
+        // the remaining-th largest among the candidates: the value v with
+        // #(> v) < remaining <= #(> v) + #(== v)
+        const uint32_t n = ncand, rem = static_cast<uint32_t>(remaining);
+        const uint32_t v = lane < n ? cand[lane] : 0u;
+        uint32_t gt = 0, eq = 0;
+        for (uint32_t j = 0; j < n; ++j) {
+          const uint32_t u = __shfl_sync(0xffffffffu, v, j);
+          gt += u > v;
+          eq += u == v;
+        }
+        if (lane < n && gt < rem && rem <= gt + eq) {  // every lane holding that value agrees
+          fin_thr = v;
+          fin_above = gt;
+        }
+      }
+      __syncthreads();
+      thr = fin_thr;
+      remaining -= static_cast<int>(fin_above);
+      break;
+    }
+  }
   const uint32_t need_eq = static_cast<uint32_t>(remaining);
 
   uint32_t gt = 0, eq = 0;
