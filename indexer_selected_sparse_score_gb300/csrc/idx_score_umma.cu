@@ -58,7 +58,6 @@ constexpr size_t kSmemBudget = kCtasPerSm<NH> == 2 ? 233472 / 2 - 2048 : 232448 
 constexpr int kScaleAhead = 8;                   // key-scale prefetch distance, in tiles
 constexpr int kMainThreads = 192;
 constexpr int kPrepThreads = 256;
-constexpr int kPlanPer = 32;  // tokens per thread per chunk of the plan scan
 constexpr int kPlanSmemTokens = 8192;
 
 template <int NH, int P>
@@ -122,16 +121,17 @@ __device__ __forceinline__ int plan_block_scan(int v, int *warp_sums) {
 // write the folded head weights wq[t, h] = w * q_scale * 2^e, and (optionally)
 // -inf into the masked tail of the score row.
 // Block T: the work plan of the main kernel -- prefix[t] = key tiles of the
-// tokens before t (prefix[T] = all tiles) and start[c] = the token holding the
-// first tile of CTA c of `grid` (each CTA takes tiles [total*c/grid,
-// total*(c+1)/grid)).
+// tokens before t (prefix[T] = all tiles) and, for CTA c of `grid` (which takes
+// tiles [total*c/grid, total*(c+1)/grid)), the 8-int record plan[c] = {begin,
+// end, t, prefix[t], prefix[t+1], sequence of t, n_vis of t, 0} with t the
+// token holding tile `begin`, so the CTA starts from one load.
 template <int NH, bool QFP8>
 __global__ void __launch_bounds__(kPrepThreads)
 idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq,
                  const int32_t *__restrict__ q_pos, const void *__restrict__ q_I,
                  const float *__restrict__ q_scale, const float *__restrict__ w,
                  uint8_t *__restrict__ qpack, float *__restrict__ wq, float *__restrict__ scores,
-                 int64_t ld, int write_masked, int32_t *__restrict__ prefix, int32_t *__restrict__ start,
+                 int64_t ld, int write_masked, int32_t *__restrict__ prefix, int32_t *__restrict__ plan,
                  int grid, uint32_t *status) {
   constexpr int P = QFP8 ? 1 : 2;
   constexpr int kHeadsPerWarp = NH / (kPrepThreads / 32);
@@ -139,43 +139,39 @@ idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq
   const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (t == T) {
     __shared__ int warp_sums[32];
-    __shared__ int carry;
-    __shared__ int pre_s[kPlanSmemTokens + 1];  // prefix kept on chip for the searches below
+    __shared__ int pre_s[kPlanSmemTokens + 1];  // tile counts, then their prefix, kept on chip when they fit
     const bool on_chip = T <= kPlanSmemTokens;
-    if (threadIdx.x == 0) carry = 0;
-    __syncthreads();
-    for (int base = 0; base < T; base += kPrepThreads * kPlanPer) {
-      const int t0 = base + threadIdx.x * kPlanPer;
-      // all loads of the chunk first (no branch depends on a loaded value
-      // before the last load is issued), then the tile counts
-      int sq[kPlanPer], ps[kPlanPer];
+    int *cnt_s = on_chip ? pre_s : prefix;      // generic pointer: shared or global memory
+    // (a) tile count of every token, one token per thread, coalesced, four loads in flight
+    for (int t0 = threadIdx.x; t0 < T; t0 += 4 * kPrepThreads) {
+      int sq[4], ps[4];
 #pragma unroll
-      for (int k = 0; k < kPlanPer; ++k) {
-        const bool in = t0 + k < T;
-        sq[k] = in ? q_seq[t0 + k] : -1;
-        ps[k] = in ? q_pos[t0 + k] : -1;
+      for (int k = 0; k < 4; ++k) {
+        const int tt = min(t0 + k * kPrepThreads, T - 1);
+        sq[k] = q_seq[tt];
+        ps[k] = q_pos[tt];
       }
-      int tl[kPlanPer];
-      int sum = 0;
 #pragma unroll
-      for (int k = 0; k < kPlanPer; ++k) {
-        tl[k] = tiles_of(B, N_c, r, sq[k], ps[k]);
-        sum += tl[k];
-      }
-      const int incl = plan_block_scan(sum, warp_sums);
-      int run = carry + incl - sum;
-#pragma unroll
-      for (int k = 0; k < kPlanPer; ++k) {
-        if (t0 + k < T) {
-          prefix[t0 + k] = run;
-          if (on_chip) pre_s[t0 + k] = run;
-        }
-        run += tl[k];
-      }
-      __syncthreads();
-      if (threadIdx.x == kPrepThreads - 1) carry += incl;
-      __syncthreads();
+      for (int k = 0; k < 4; ++k)
+        if (t0 + k * kPrepThreads < T) cnt_s[t0 + k * kPrepThreads] = tiles_of(B, N_c, r, sq[k], ps[k]);
     }
+    __syncthreads();
+    // (b) exclusive prefix: each thread scans a contiguous chunk
+    const int chunk = (T + kPrepThreads - 1) / kPrepThreads;
+    const int c0 = min(T, static_cast<int>(threadIdx.x) * chunk), c1 = min(T, c0 + chunk);
+    int sum = 0;
+    for (int tt = c0; tt < c1; ++tt) sum += cnt_s[tt];
+    const int incl = plan_block_scan(sum, warp_sums);
+    int run = incl - sum;
+    for (int tt = c0; tt < c1; ++tt) {
+      const int v = cnt_s[tt];
+      cnt_s[tt] = run;
+      if (on_chip) prefix[tt] = run;
+      run += v;
+    }
+    __shared__ int carry;
+    if (threadIdx.x == kPrepThreads - 1) carry = incl;
+    __syncthreads();
     if (threadIdx.x == 0) {
       prefix[T] = carry;
       if (on_chip) pre_s[T] = carry;
@@ -189,7 +185,12 @@ idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq
         const int mid = (lo + hi + 1) >> 1;
         if ((on_chip ? pre_s[mid] : prefix[mid]) <= first) lo = mid; else hi = mid - 1;
       }
-      start[c] = lo;
+      const int b = q_seq[lo], pos = q_pos[lo];
+      const bool ok = b >= 0 && b < B && pos >= 0;
+      int4 *rec = reinterpret_cast<int4 *>(plan + 8 * c);
+      rec[0] = make_int4(static_cast<int>(first), static_cast<int>(total * (c + 1) / grid), lo,
+                         on_chip ? pre_s[lo] : prefix[lo]);
+      rec[1] = make_int4(on_chip ? pre_s[lo + 1] : prefix[lo + 1], ok ? b : 0, ok ? min(n_vis_of(pos, r), N_c) : 0, 0);
     }
     return;
   }
@@ -271,7 +272,7 @@ idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq
 struct ScoreParams {
   int B, T, N_c, r;
   const int32_t *q_seq, *q_pos;
-  const int32_t *prefix, *start;  // work plan written by the prep kernel
+  const int32_t *prefix, *plan;  // work plan written by the prep kernel
   const uint8_t *qpack;
   const float *wq;
   const float *k_scale;
@@ -294,11 +295,12 @@ __device__ __forceinline__ int token_tiles(const ScoreParams &p, int t, int *b_o
 // starts, never per tile.
 struct TileCursor {
   int t, first, next, b, nv;  // token, its first tile, first tile of the next token
-  __device__ void start(const ScoreParams &p, int t0) {
-    t = t0;
-    first = p.prefix[t];
-    next = p.prefix[t + 1];
-    token_tiles(p, t, &b, &nv);
+  __device__ void init(const int4 &a, const int4 &c) {  // from the CTA's plan record
+    t = a.z;
+    first = a.w;
+    next = c.x;
+    b = c.y;
+    nv = c.z;
   }
   // moves to the token holding tile i (i never decreases); true if it changed
   __device__ bool seek(const ScoreParams &p, int i) {
@@ -365,10 +367,9 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
   const uint32_t tmem = *tmem_base_s;
 
   pdl_wait();  // the plan, packed queries and weights come from the prep kernel
-  const int total = p.prefix[p.T];
-  const int begin = static_cast<int>((static_cast<long long>(total) * blockIdx.x) / gridDim.x);
-  const int end = static_cast<int>((static_cast<long long>(total) * (blockIdx.x + 1)) / gridDim.x);
-  const int t_first = p.start[blockIdx.x];  // token holding tile `begin`
+  const int4 plan_a = reinterpret_cast<const int4 *>(p.plan)[2 * blockIdx.x];
+  const int4 plan_b = reinterpret_cast<const int4 *>(p.plan)[2 * blockIdx.x + 1];
+  const int begin = plan_a.x, end = plan_a.y;
   auto fail = [&]() {
     raise_flag(p.status, kFlagTimeout);
     atomicExch(abort_s, 1);
@@ -379,7 +380,7 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
     if (lane == 0 && begin < end) {
       prefetch_tmap(&kmap);
       TileCursor cur;
-      cur.start(p, t_first);
+      cur.init(plan_a, plan_b);
       int prev_t = -1, qn = -1;
       int issued = 0;
       for (int i = begin; i < end && !*(volatile int *)abort_s; ++i) {
@@ -414,7 +415,7 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
       constexpr uint32_t idesc = idesc_e4m3(kTileKeys, NH);
       const bool leader = elect_one();
       TileCursor cur;
-      cur.start(p, t_first);
+      cur.init(plan_a, plan_b);
       int prev_t = -1, qn = -1;
       bool ok = true;
       for (int i = begin; i < end; ++i) {
@@ -463,8 +464,8 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
     const int row = quarter * 32 + lane;
     if (begin < end) {
       TileCursor cur, ahead;  // `ahead` runs kScaleAhead tiles in front for the scale prefetch
-      cur.start(p, t_first);
-      ahead.start(p, t_first);
+      cur.init(plan_a, plan_b);
+      ahead.init(plan_a, plan_b);
       int prev_t = -1, qn = -1;
       auto scale_at = [&](const TileCursor &c, int ii) -> float {
         const int ss = (ii - c.first) * kTileKeys + row;
@@ -541,14 +542,14 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
 
 template <int NH, bool QFP8>
 cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld, bool write_masked,
-                             uint8_t *qpack, float *wq, int32_t *prefix, int32_t *start, uint32_t *status,
+                             uint8_t *qpack, float *wq, int32_t *prefix, int32_t *plan, uint32_t *status,
                              cudaStream_t stream) {
   constexpr int P = QFP8 ? 1 : 2;
   using L = ScoreSmem<NH, P>;
   const int grid = sm_count() * kCtasPerSm<NH>;
   idx_qprep_kernel<NH, QFP8><<<ia.T + 1, kPrepThreads, 0, stream>>>(
       ia.B, ia.T, ia.N_c, ia.r, ia.q_seq, ia.q_pos, ia.q_I, ia.q_scale, ia.w, qpack, wq, scores, ld,
-      write_masked ? 1 : 0, prefix, start, grid, status);
+      write_masked ? 1 : 0, prefix, plan, grid, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -564,7 +565,7 @@ cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
-  ScoreParams sp{ia.B, ia.T, ia.N_c, ia.r, ia.q_seq, ia.q_pos, prefix, start, qpack, wq, ia.k_scale, scores,
+  ScoreParams sp{ia.B, ia.T, ia.N_c, ia.r, ia.q_seq, ia.q_pos, prefix, plan, qpack, wq, ia.k_scale, scores,
                  ld, status};
   auto kern = idx_score_umma_kernel<NH, P>;
   const size_t smem = L::total + 1024;  // + alignment slack for the 1024-byte swizzle atoms
@@ -629,7 +630,7 @@ UmmaScratch umma_scratch_layout(const sa_index_args &ia) {
   L.wq = up(static_cast<size_t>(ia.T) * P * ia.H_I * 128);
   L.prefix = L.wq + up(static_cast<size_t>(ia.T) * ia.H_I * 4);
   L.start = L.prefix + up(static_cast<size_t>(ia.T + 1) * 4);
-  L.total = L.start + up(static_cast<size_t>(2 * sm_count() + 1) * 4);  // up to two CTAs per SM
+  L.total = L.start + up(static_cast<size_t>(2 * sm_count()) * 32);  // 8-int plan record per CTA, up to two per SM
   return L;
 }
 }  // namespace
@@ -644,11 +645,11 @@ cudaError_t launch_idx_score_umma(const sa_index_args &ia, float *scores, int64_
   uint8_t *qpack = base + L.qpack;
   float *wq = reinterpret_cast<float *>(base + L.wq);
   int32_t *prefix = reinterpret_cast<int32_t *>(base + L.prefix);
-  int32_t *start = reinterpret_cast<int32_t *>(base + L.start);
+  int32_t *plan = reinterpret_cast<int32_t *>(base + L.start);
   const bool qf8 = ia.q_dtype == SA_FP8_E4M3;
 #define SA_UMMA_CASE(NH, QF)                                                                              \
   if (ia.H_I == NH && qf8 == QF)                                                                          \
-    return launch_umma_impl<NH, QF>(ia, scores, ld, write_masked, qpack, wq, prefix, start, status, stream);
+    return launch_umma_impl<NH, QF>(ia, scores, ld, write_masked, qpack, wq, prefix, plan, status, stream);
   SA_UMMA_CASE(32, false)
   SA_UMMA_CASE(32, true)
   SA_UMMA_CASE(64, false)
