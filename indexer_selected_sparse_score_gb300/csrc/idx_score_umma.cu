@@ -235,17 +235,27 @@ idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq
       float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      // e such that amax 2^-e is in (224, 448]: for a normal amax = 1.f 2^E,
+      // e = E - 8, plus one when 1.f > 1.75 (so the scaled max is <= 448)
       int e = 0;
+      const uint32_t abits = __float_as_uint(amax), ebits = abits >> 23;
       if (amax > 0.f) {
-        int ex;
-        frexpf(amax, &ex);  // amax = m 2^ex, m in [0.5, 1)
-        e = ex - 9;         // amax 2^-e in [256, 512)
-        if (ldexpf(amax, -e) > 448.f) ++e;
+        if (ebits != 0u && ebits != 0xFFu) {
+          e = static_cast<int>(ebits) - 135 + ((abits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+        } else {
+          int ex;
+          frexpf(amax, &ex);  // amax = m 2^ex, m in [0.5, 1)
+          e = ex - 9;         // amax 2^-e in [256, 512)
+          if (ldexpf(amax, -e) > 448.f) ++e;
+        }
       }
+      // 2^-e as a normal float when it is one (an exact scaling, as ldexpf)
+      const bool pow2_ok = e >= -126 && e <= 126;
+      const float inv2e = __uint_as_float(static_cast<uint32_t>(pow2_ok ? 127 - e : 127) << 23);
       uint32_t w1 = 0, w2 = 0;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float y = ldexpf(x[k], -e);
+        const float y = pow2_ok ? x[k] * inv2e : ldexpf(x[k], -e);
         const __nv_fp8_storage_t p1 = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
         const float rest = y - e4m3_bits_to_float(p1);
         const __nv_fp8_storage_t p2 = __nv_cvt_float_to_fp8(rest, __NV_SATFINITE, __NV_E4M3);
@@ -255,7 +265,11 @@ idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq
       *reinterpret_cast<uint32_t *>(dst + umma::sw128_offset(h, 4 * lane)) = w1;
       *reinterpret_cast<uint32_t *>(dst + NH * 128 + umma::sw128_offset(h, 4 * lane)) = w2;
       const float wh = __shfl_sync(0xffffffffu, w_pre, i), qh = __shfl_sync(0xffffffffu, qs_pre, i);
-      if (lane == 0) wq[static_cast<int64_t>(t) * NH + h] = ldexpf(wh * qh, e);
+      if (lane == 0) {
+        const float f = wh * qh;
+        wq[static_cast<int64_t>(t) * NH + h] =
+            pow2_ok ? f * __uint_as_float(static_cast<uint32_t>(127 + e) << 23) : ldexpf(f, e);
+      }
     }
   }
   if (write_masked) {

@@ -143,6 +143,7 @@ topk_radix_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, 
 constexpr int kRegMax = 32768;
 constexpr int kDigitBits = 11;                 // radix digit width
 constexpr int kDigitBins = 1 << kDigitBits;
+constexpr int kFinish = 256;                   // a bin this small is ranked directly
 constexpr int kRegE = kRegMax / kTopkThreads;  // 32 keys per thread at most
 
 // Block-wide exclusive scan of one uint32 per thread; returns the prefix and
@@ -243,12 +244,29 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
     return;
   }
   const float *row = scores + static_cast<int64_t>(t) * ld;
-  const int per = (nv + kTopkThreads - 1) / kTopkThreads;  // <= E
+  // a multiple of 4 keys per thread (<= E), read as float4 where the row is aligned
+  const int per = ((nv + kTopkThreads - 1) / kTopkThreads + 3) & ~3;
   const int lo = tid * per;
   const int cnt = max(0, min(per, nv - lo));
   uint32_t key[E];
+  if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
 #pragma unroll
-  for (int e = 0; e < E; ++e) key[e] = e < cnt ? ordered_key(row[lo + e]) : 0u;
+    for (int q = 0; q < E / 4; ++q) {
+      if (4 * q + 3 < cnt) {
+        const float4 v = *reinterpret_cast<const float4 *>(row + lo + 4 * q);
+        key[4 * q] = ordered_key(v.x);
+        key[4 * q + 1] = ordered_key(v.y);
+        key[4 * q + 2] = ordered_key(v.z);
+        key[4 * q + 3] = ordered_key(v.w);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) key[4 * q + j] = 4 * q + j < cnt ? ordered_key(row[lo + 4 * q + j]) : 0u;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) key[e] = e < cnt ? ordered_key(row[lo + e]) : 0u;
+  }
 
   // the row's key range: keys become key - min (< 2^L)
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
@@ -274,10 +292,10 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
   const int L = kmax > kmin ? 32 - __clz(kmax - kmin) : 0;
 
   // radix select over bits [0, L), kDigitBits at a time from the top; once
-  // the chosen bin holds at most 32 keys, one warp ranks them directly
+  // the chosen bin holds at most kFinish keys, they are ranked directly
   int remaining = K;
   uint32_t thr = 0u;
-  __shared__ uint32_t cand[32], ncand, fin_thr, fin_above;
+  __shared__ uint32_t cand[kFinish], ncand, fin_thr, fin_above;
   for (int hi = L; hi > 0;) {
     const int nb = hi < kDigitBits ? hi : kDigitBits, shift = hi - nb;
     const uint32_t mask = hi >= 32 ? 0u : ~((1u << hi) - 1u);  // bits already fixed
@@ -285,7 +303,7 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
     const uint32_t d = radix_pass<E>(key, cnt, thr, mask, shift, 1 << nb, hist, warp_sums, remaining, in_bin);
     thr |= d << shift;
     hi = shift;
-    if (hi > 0 && in_bin <= 32u) {
+    if (hi > 0 && in_bin <= static_cast<uint32_t>(kFinish)) {
       // gather the bin's keys (those matching every fixed bit)
       if (tid == 0) ncand = 0;
       __syncthreads();
@@ -294,20 +312,22 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
       for (int e = 0; e < E; ++e)
         if (e < cnt && (key[e] & fixed) == thr) cand[atomicAdd(&ncand, 1u)] = key[e];
       __syncthreads();
-      if (warp == 0) {
+      {
         // the remaining-th largest among the candidates: the value v with
-        // #(> v) < remaining <= #(> v) + #(== v)
+        // #(> v) < remaining <= #(> v) + #(== v); thread i ranks candidate i
         const uint32_t n = ncand, rem = static_cast<uint32_t>(remaining);
-        const uint32_t v = lane < n ? cand[lane] : 0u;
-        uint32_t gt = 0, eq = 0;
-        for (uint32_t j = 0; j < n; ++j) {
-          const uint32_t u = __shfl_sync(0xffffffffu, v, j);
-          gt += u > v;
-          eq += u == v;
-        }
-        if (lane < n && gt < rem && rem <= gt + eq) {  // every lane holding that value agrees
-          fin_thr = v;
-          fin_above = gt;
+        if (static_cast<uint32_t>(tid) < n) {
+          const uint32_t v = cand[tid];
+          uint32_t gt = 0, eq = 0;
+          for (uint32_t j = 0; j < n; ++j) {
+            const uint32_t u = cand[j];
+            gt += u > v;
+            eq += u == v;
+          }
+          if (gt < rem && rem <= gt + eq) {  // every thread holding that value agrees
+            fin_thr = v;
+            fin_above = gt;
+          }
         }
       }
       __syncthreads();
