@@ -735,25 +735,27 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         const float l_all = l + __shfl_xor_sync(0xffffffffu, l, 16);
         const int64_t row = static_cast<int64_t>(t0 + tok) * kH + h;
         if (rank == 1) {
-          // second part of a split token: (m, l, O) go to rank 0's K ring
-          // (O as [64 heads][128] f32, then (m, l) per head) once it is free
+          // second part of a split token: (m, l, O) go to rank 0's K ring once
+          // it is free, laid out by softmax thread (the same thread of rank 0
+          // reads them): O chunk q (4 columns) of thread i at 16 (128 q + i),
+          // so a warp's store covers 512 contiguous bytes; (m, l) at 32 KB + 8 i
           if (!mbar_wait_cluster_warp(xempty, 0)) {
             if (lane == 0) fail();
             break;
           }
-          const uint32_t xo = cluster_map(ks + h * (kD * 4) + 64 * u * 4, 0);
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
+          const uint32_t xo = cluster_map(ks + tid * 16, 0);
+#pragma unroll 1
+          for (int c4 = 0; c4 < 4; ++c4) {  // once per token: a short loop, not unrolled
             uint32_t o[16];
             tmem_ld_16x2_x16(tmem + lane_base + kColO + 16 * c4, o);
             tmem_ld_wait();
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              st_cluster_f4(xo + (16 * c4 + 4 * q) * 4, __uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+              st_cluster_f4(xo + 2048 * (4 * c4 + q), __uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
                             __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
           }
-          if (u == 0) {
-            const uint32_t xml = cluster_map(ks + kH * kD * 4 + h * 8, 0);
+          {
+            const uint32_t xml = cluster_map(ks + 32768 + tid * 8, 0);
             asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(xml), "f"(m_ref), "f"(l_all) : "memory");
           }
           tc_fence_before();
@@ -766,13 +768,13 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
           // whole token, or the first part merged with rank 1's:
           // O = a0 O0 + a1 O1, l = a0 l0 + a1 l1 against M = max(m0, m1)
           float m1 = -INFINITY, l1 = 0.f;
-          const float4 *xo = reinterpret_cast<const float4 *>(ks + h * (kD * 4) + 64 * u * 4);
+          const float4 *xo = reinterpret_cast<const float4 *>(ks) + tid;  // chunk q at xo[128 q]
           if (split > 1) {
             if (!mbar_wait_cluster_warp(xfull, 0)) {
               if (lane == 0) fail();
               break;
             }
-            const float2 ml = *reinterpret_cast<const float2 *>(ks + kH * kD * 4 + h * 8);
+            const float2 ml = *reinterpret_cast<const float2 *>(ks + 32768 + tid * 8);
             m1 = ml.x;
             l1 = ml.y;
           }
@@ -790,15 +792,17 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
           const float inv = Lden > 0.f ? a / Lden : 0.f;
           const float f0 = a0 * inv, f1 = a1 * inv;
           uint4 *dst = reinterpret_cast<uint4 *>(p.out + row * kD + 64 * u);
-          // 16 of the thread's 64 columns at a time (columns 64u + 16c4 ..)
-#pragma unroll
+          // 16 columns at a time (columns 64u + 16c4 ..): merge with the
+          // partner's part, round, store.  Runs once per token, so it is kept
+          // as a short loop (its code runs cold) rather than unrolled.
+#pragma unroll 1
           for (int c4 = 0; c4 < 4; ++c4) {
             uint32_t o[16];
             tmem_ld_16x2_x16(tmem + lane_base + kColO + 16 * c4, o);
             float x[16];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const float4 v4 = split > 1 ? xo[4 * c4 + q] : make_float4(0.f, 0.f, 0.f, 0.f);
+              const float4 v4 = split > 1 ? xo[128 * (4 * c4 + q)] : make_float4(0.f, 0.f, 0.f, 0.f);
               x[4 * q] = v4.x;
               x[4 * q + 1] = v4.y;
               x[4 * q + 2] = v4.z;
@@ -939,7 +943,7 @@ cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(sparse_mqa_umma_kernel), smem, attr_done);
   if (e != cudaSuccess) return e;
   p.split = attn_split(ia, p.TPT);
-  p.PT0 = (p.TPT + 1) / 2;
+  p.PT0 = (p.TPT + 1) / 2;  // rank 0 takes the larger half (window included); rank 1's hand-off costs about its merge
   const int sms = sm_count();
   // whole tokens (at most one CTA per SM), or one cluster pair per token
   const int grid = p.split == 1 ? (ia.T < sms ? ia.T : sms) : 2 * ia.T;
