@@ -58,7 +58,6 @@ constexpr size_t kSmemBudget = kCtasPerSm<NH> == 2 ? 233472 / 2 - 2048 : 232448 
 constexpr int kScaleAhead = 8;                   // key-scale prefetch distance, in tiles
 constexpr int kMainThreads = 192;
 constexpr int kPrepThreads = 256;
-constexpr int kPlanSmemTokens = 8192;
 
 template <int NH, int P>
 struct ScoreSmem {
@@ -66,7 +65,7 @@ struct ScoreSmem {
   // everything but the key ring: two query buffers, two weight vectors, barriers (at most
   // 2 * kMaxStages + 13 of them) and the misc words
   static constexpr size_t kFixed = 2 * static_cast<size_t>(kQBytes) + 2 * NH * sizeof(float) +
-                                   (2 * kMaxStages + 13) * sizeof(uint64_t) + 64 + 8;
+                                   (2 * kMaxStages + 13) * sizeof(uint64_t) + 128 + 8;
   static constexpr int kStages = static_cast<int>(
       (kSmemBudget<NH> - kFixed) / kKeyTileBytes < kMaxStages ? (kSmemBudget<NH> - kFixed) / kKeyTileBytes
                                                                 : kMaxStages);
@@ -76,7 +75,7 @@ struct ScoreSmem {
   static constexpr size_t bars = wq + 2 * NH * sizeof(float);
   static constexpr int kBars = 2 * kStages + 4 + 2 * kAccStages + 1;
   static constexpr size_t misc = bars + kBars * sizeof(uint64_t);
-  static constexpr size_t total = misc + 64;
+  static constexpr size_t total = misc + 128;  // tmem base, abort flag; plan words at misc + 64
   static_assert(total <= kSmemBudget<NH>, "shared memory budget");
 };
 
@@ -120,28 +119,25 @@ __device__ __forceinline__ int plan_block_scan(int v, int *warp_sums) {
 // 128-byte-swizzled layout the MMA reads (piece p, head h at rows p*H_I + h),
 // write the folded head weights wq[t, h] = w * q_scale * 2^e, and (optionally)
 // -inf into the masked tail of the score row.
-// Block T: the work plan of the main kernel -- prefix[t] = key tiles of the
-// tokens before t (prefix[T] = all tiles) and, for CTA c of `grid` (which takes
-// tiles [total*c/grid, total*(c+1)/grid)), the 8-int record plan[c] = {begin,
-// end, t, prefix[t], prefix[t+1], sequence of t, n_vis of t, 0} with t the
-// token holding tile `begin`, so the CTA starts from one load.
+// Block T: prefix[t] = key tiles of the tokens before t (prefix[T] = all
+// tiles), which the main kernel reads when a CTA crosses into a later token
+// (each CTA computes its own starting point from the inputs).
 template <int NH, bool QFP8>
 __global__ void __launch_bounds__(kPrepThreads)
 idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq,
                  const int32_t *__restrict__ q_pos, const void *__restrict__ q_I,
                  const float *__restrict__ q_scale, const float *__restrict__ w,
                  uint8_t *__restrict__ qpack, float *__restrict__ wq, float *__restrict__ scores,
-                 int64_t ld, int write_masked, int32_t *__restrict__ prefix, int32_t *__restrict__ plan,
-                 int grid, uint32_t *status) {
+                 int64_t ld, int write_masked, int32_t *__restrict__ prefix, uint32_t *status) {
   constexpr int P = QFP8 ? 1 : 2;
   constexpr int kHeadsPerWarp = NH / (kPrepThreads / 32);
   pdl_trigger();
   const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (t == T) {
+    // (no large shared array: prep blocks must fit beside the main kernel's
+    // CTAs, which start early and fill the SMs' shared memory)
     __shared__ int warp_sums[32];
-    __shared__ int pre_s[kPlanSmemTokens + 1];  // tile counts, then their prefix, kept on chip when they fit
-    const bool on_chip = T <= kPlanSmemTokens;
-    int *cnt_s = on_chip ? pre_s : prefix;      // generic pointer: shared or global memory
+    int *cnt_s = prefix;  // tile counts, then their prefix, staged in global memory
     // (a) tile count of every token, one token per thread, coalesced, four loads in flight
     for (int t0 = threadIdx.x; t0 < T; t0 += 4 * kPrepThreads) {
       int sq[4], ps[4];
@@ -160,38 +156,31 @@ idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq
     const int chunk = (T + kPrepThreads - 1) / kPrepThreads;
     const int c0 = min(T, static_cast<int>(threadIdx.x) * chunk), c1 = min(T, c0 + chunk);
     int sum = 0;
-    for (int tt = c0; tt < c1; ++tt) sum += cnt_s[tt];
+    for (int base = c0; base < c1; base += 8) {  // eight loads in flight per round
+      int v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = cnt_s[min(base + k, c1 - 1)];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (base + k < c1) sum += v[k];
+    }
     const int incl = plan_block_scan(sum, warp_sums);
     int run = incl - sum;
-    for (int tt = c0; tt < c1; ++tt) {
-      const int v = cnt_s[tt];
-      cnt_s[tt] = run;
-      if (on_chip) prefix[tt] = run;
-      run += v;
+    for (int base = c0; base < c1; base += 8) {
+      int v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = cnt_s[min(base + k, c1 - 1)];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (base + k < c1) {
+          cnt_s[base + k] = run;
+          run += v[k];
+        }
     }
     __shared__ int carry;
     if (threadIdx.x == kPrepThreads - 1) carry = incl;
     __syncthreads();
-    if (threadIdx.x == 0) {
-      prefix[T] = carry;
-      if (on_chip) pre_s[T] = carry;
-    }
-    __syncthreads();
-    const long long total = carry;
-    for (int c = threadIdx.x; c < grid; c += kPrepThreads) {
-      const long long first = total * c / grid;
-      int lo = 0, hi = T - 1;  // largest token whose prefix <= first
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if ((on_chip ? pre_s[mid] : prefix[mid]) <= first) lo = mid; else hi = mid - 1;
-      }
-      const int b = q_seq[lo], pos = q_pos[lo];
-      const bool ok = b >= 0 && b < B && pos >= 0;
-      int4 *rec = reinterpret_cast<int4 *>(plan + 8 * c);
-      rec[0] = make_int4(static_cast<int>(first), static_cast<int>(total * (c + 1) / grid), lo,
-                         on_chip ? pre_s[lo] : prefix[lo]);
-      rec[1] = make_int4(on_chip ? pre_s[lo + 1] : prefix[lo + 1], ok ? b : 0, ok ? min(n_vis_of(pos, r), N_c) : 0, 0);
-    }
+    if (threadIdx.x == 0) prefix[T] = carry;
     return;
   }
 
@@ -286,7 +275,7 @@ idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq
 struct ScoreParams {
   int B, T, N_c, r;
   const int32_t *q_seq, *q_pos;
-  const int32_t *prefix, *plan;  // work plan written by the prep kernel
+  const int32_t *prefix;  // tiles before each token, written by the prep kernel
   const uint8_t *qpack;
   const float *wq;
   const float *k_scale;
@@ -309,7 +298,7 @@ __device__ __forceinline__ int token_tiles(const ScoreParams &p, int t, int *b_o
 // starts, never per tile.
 struct TileCursor {
   int t, first, next, b, nv;  // token, its first tile, first tile of the next token
-  __device__ void init(const int4 &a, const int4 &c) {  // from the CTA's plan record
+  __device__ void init(const int4 &a, const int4 &c) {  // {_, _, t, first}, {next, b, nv, _}
     t = a.z;
     first = a.w;
     next = c.x;
@@ -380,10 +369,74 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
   tc_fence_after();
   const uint32_t tmem = *tmem_base_s;
 
-  pdl_wait();  // the plan, packed queries and weights come from the prep kernel
-  const int4 plan_a = reinterpret_cast<const int4 *>(p.plan)[2 * blockIdx.x];
-  const int4 plan_b = reinterpret_cast<const int4 *>(p.plan)[2 * blockIdx.x + 1];
-  const int begin = plan_a.x, end = plan_a.y;
+  // This CTA's tile range and its first token, from the inputs alone (the
+  // prep kernel's prefix is the same plan; it is read only when a CTA crosses
+  // into a later token), so key tiles can stream before the prep kernel ends.
+  int *plan_s = reinterpret_cast<int *>(smem + L::misc + 64);  // [8]
+  {
+    constexpr int kW = kMainThreads / 32;
+    int *wsum_s = plan_s + 8;  // [kW + 1]
+    const int chunk = (p.T + kMainThreads - 1) / kMainThreads;
+    const int c0 = min(p.T, tid * chunk), c1 = min(p.T, c0 + chunk);
+    int sum = 0;
+    for (int base = c0; base < c1; base += 8) {  // eight loads in flight per round
+      int sq[8], ps[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int tt = min(base + k, c1 - 1);
+        sq[k] = p.q_seq[tt];
+        ps[k] = p.q_pos[tt];
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (base + k < c1) sum += tiles_of(p.B, p.N_c, p.r, sq[k], ps[k]);
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum_s[warp] = incl;
+    __syncthreads();
+    if (tid == 0) {
+      int run = 0;
+      for (int w2 = 0; w2 < kW; ++w2) {
+        const int v = wsum_s[w2];
+        wsum_s[w2] = run;
+        run += v;
+      }
+      wsum_s[kW] = run;
+    }
+    __syncthreads();
+    const int pre = wsum_s[warp] + incl - sum, total = wsum_s[kW];
+    const int begin0 = static_cast<int>(static_cast<long long>(total) * blockIdx.x / gridDim.x);
+    const int end0 = static_cast<int>(static_cast<long long>(total) * (blockIdx.x + 1) / gridDim.x);
+    if (tid == 0) {
+      plan_s[0] = begin0;
+      plan_s[1] = end0;
+    }
+    if (begin0 < end0 && pre <= begin0 && begin0 < pre + sum) {  // this chunk holds tile begin0
+      int run = pre;
+      for (int tt = c0; tt < c1; ++tt) {
+        const int b = p.q_seq[tt], pos = p.q_pos[tt];
+        const int tl = tiles_of(p.B, p.N_c, p.r, b, pos);
+        if (begin0 < run + tl) {
+          plan_s[2] = tt;
+          plan_s[3] = run;
+          plan_s[4] = run + tl;
+          plan_s[5] = b;
+          plan_s[6] = min(n_vis_of(pos, p.r), p.N_c);
+          break;
+        }
+        run += tl;
+      }
+    }
+    __syncthreads();
+  }
+  const int begin = plan_s[0], end = plan_s[1];
+  const int4 plan_a = make_int4(begin, end, plan_s[2], plan_s[3]);
+  const int4 plan_b = make_int4(plan_s[4], plan_s[5], plan_s[6], 0);
   auto fail = [&]() {
     raise_flag(p.status, kFlagTimeout);
     atomicExch(abort_s, 1);
@@ -397,6 +450,15 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
       cur.init(plan_a, plan_b);
       int prev_t = -1, qn = -1;
       int issued = 0;
+      // the key tiles of the first token (up to the ring size) do not depend on
+      // the prep kernel: issue them first, then wait for its packed queries
+      const int n_pre = min(min(end, cur.next) - begin, kStages);
+      for (int n = 0; n < n_pre; ++n) {
+        mbar_expect_tx(&kfull[n], kKeyTileBytes);
+        tma_load_2d(keys + n * kKeyTileBytes, &kmap, &kfull[n], 0, cur.b * p.N_c + (begin + n - cur.first) * kTileKeys);
+        ++issued;
+      }
+      pdl_wait();
       for (int i = begin; i < end && !*(volatile int *)abort_s; ++i) {
         cur.seek(p, i);
         const int t = cur.t, b = cur.b;
@@ -411,6 +473,7 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
         }
         const int j = i - cur.first;
         const int n = i - begin, s = n % kStages;
+        if (n < n_pre) continue;  // issued above
         if (!mbar_wait(&kempty[s], ((n / kStages) & 1) ^ 1)) { fail(); break; }
         mbar_expect_tx(&kfull[s], kKeyTileBytes);
         tma_load_2d(keys + s * kKeyTileBytes, &kmap, &kfull[s], 0, b * p.N_c + j * kTileKeys);
@@ -425,6 +488,7 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
     // ------------------------------------------------------- MMA issuer
     // The whole warp walks the tiles and waits; one elected lane issues the
     // MMAs and commits from operands the warp computed uniformly.
+    pdl_wait();  // token boundaries come from the prep kernel's prefix
     if (begin < end) {
       constexpr uint32_t idesc = idesc_e4m3(kTileKeys, NH);
       const bool leader = elect_one();
@@ -471,6 +535,7 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
     }
   } else {
     // --------------------------------------------------------- epilogue
+    pdl_wait();  // token boundaries come from the prep kernel's prefix
     // The key scales are loaded kScaleAhead tiles ahead into a register
     // queue: under a full memory stream their latency spans several tiles and
     // would otherwise pace the whole pipeline.
@@ -529,11 +594,23 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
         if (lane == 0) mbar_arrive(&aempty[a]);
         const int s = (i - cur.first) * kTileKeys + row;
         if (s < nv) {
-          const float *wv = wqs + (qn & 1) * NH;
-          float acc = 0.f;
+          // sum_h w_h relu(d_h): eight independent partial sums (short chains),
+          // weights read four at a time
+          const float4 *wv4 = reinterpret_cast<const float4 *>(wqs + (qn & 1) * NH);
+          float acc[8];
 #pragma unroll
-          for (int h = 0; h < NH; ++h) acc = fmaf(wv[h], fmaxf(__uint_as_float(v[h]), 0.f), acc);
-          p.scores[static_cast<int64_t>(t) * p.ld + s] = acc * ks;
+          for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+#pragma unroll
+          for (int h4 = 0; h4 < NH / 4; ++h4) {
+            const float4 w4 = wv4[h4];
+            float *a2 = &acc[(h4 & 1) * 4];
+            a2[0] = fmaf(w4.x, fmaxf(__uint_as_float(v[4 * h4]), 0.f), a2[0]);
+            a2[1] = fmaf(w4.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), a2[1]);
+            a2[2] = fmaf(w4.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), a2[2]);
+            a2[3] = fmaf(w4.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), a2[3]);
+          }
+          const float total = ((acc[0] + acc[4]) + (acc[1] + acc[5])) + ((acc[2] + acc[6]) + (acc[3] + acc[7]));
+          p.scores[static_cast<int64_t>(t) * p.ld + s] = total * ks;
         }
       }
       if (qn >= 0) {
@@ -556,14 +633,14 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
 
 template <int NH, bool QFP8>
 cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld, bool write_masked,
-                             uint8_t *qpack, float *wq, int32_t *prefix, int32_t *plan, uint32_t *status,
+                             uint8_t *qpack, float *wq, int32_t *prefix, uint32_t *status,
                              cudaStream_t stream) {
   constexpr int P = QFP8 ? 1 : 2;
   using L = ScoreSmem<NH, P>;
   const int grid = sm_count() * kCtasPerSm<NH>;
   idx_qprep_kernel<NH, QFP8><<<ia.T + 1, kPrepThreads, 0, stream>>>(
       ia.B, ia.T, ia.N_c, ia.r, ia.q_seq, ia.q_pos, ia.q_I, ia.q_scale, ia.w, qpack, wq, scores, ld,
-      write_masked ? 1 : 0, prefix, plan, grid, status);
+      write_masked ? 1 : 0, prefix, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -579,7 +656,7 @@ cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
-  ScoreParams sp{ia.B, ia.T, ia.N_c, ia.r, ia.q_seq, ia.q_pos, prefix, plan, qpack, wq, ia.k_scale, scores,
+  ScoreParams sp{ia.B, ia.T, ia.N_c, ia.r, ia.q_seq, ia.q_pos, prefix, qpack, wq, ia.k_scale, scores,
                  ld, status};
   auto kern = idx_score_umma_kernel<NH, P>;
   const size_t smem = L::total + 1024;  // + alignment slack for the 1024-byte swizzle atoms
@@ -634,7 +711,7 @@ bool idx_score_umma_supported(const sa_index_args &ia) {
 
 namespace {
 struct UmmaScratch {
-  size_t qpack, wq, prefix, start, total;
+  size_t qpack, wq, prefix, total;
 };
 UmmaScratch umma_scratch_layout(const sa_index_args &ia) {
   const int P = ia.q_dtype == SA_FP8_E4M3 ? 1 : 2;
@@ -643,8 +720,7 @@ UmmaScratch umma_scratch_layout(const sa_index_args &ia) {
   L.qpack = 0;
   L.wq = up(static_cast<size_t>(ia.T) * P * ia.H_I * 128);
   L.prefix = L.wq + up(static_cast<size_t>(ia.T) * ia.H_I * 4);
-  L.start = L.prefix + up(static_cast<size_t>(ia.T + 1) * 4);
-  L.total = L.start + up(static_cast<size_t>(2 * sm_count()) * 32);  // 8-int plan record per CTA, up to two per SM
+  L.total = L.prefix + up(static_cast<size_t>(ia.T + 1) * 4);
   return L;
 }
 }  // namespace
@@ -659,11 +735,10 @@ cudaError_t launch_idx_score_umma(const sa_index_args &ia, float *scores, int64_
   uint8_t *qpack = base + L.qpack;
   float *wq = reinterpret_cast<float *>(base + L.wq);
   int32_t *prefix = reinterpret_cast<int32_t *>(base + L.prefix);
-  int32_t *plan = reinterpret_cast<int32_t *>(base + L.start);
   const bool qf8 = ia.q_dtype == SA_FP8_E4M3;
 #define SA_UMMA_CASE(NH, QF)                                                                              \
   if (ia.H_I == NH && qf8 == QF)                                                                          \
-    return launch_umma_impl<NH, QF>(ia, scores, ld, write_masked, qpack, wq, prefix, plan, status, stream);
+    return launch_umma_impl<NH, QF>(ia, scores, ld, write_masked, qpack, wq, prefix, status, stream);
   SA_UMMA_CASE(32, false)
   SA_UMMA_CASE(32, true)
   SA_UMMA_CASE(64, false)
