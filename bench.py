@@ -353,31 +353,82 @@ def run_ours(args):
     if binding.sa_check_device_status(ws) != binding.SA_OK:
         raise RuntimeError("device status not OK after the timed steps")
 
-    # ---- end to end through the C ABI with host buffers
+    # ---- end to end through the C ABI with host buffers: every step copies its
+    # query inputs from one pinned host staging buffer (one H2D copy), runs the
+    # fused call on them, and reads out + idx back (one D2H copy)
     names = ("q_seq", "q_pos", "q_I", "q_scale", "w", "Q")
-    host = {n: getattr(w, n) for n in names if getattr(w, n) is not None}
-    pinned = {n: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
-              for n, a in host.items()}
-    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    idx_h = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
-    d2h = out_h.numel() * out_h.element_size() + idx_h.numel() * idx_h.element_size()
+    host = {n: np.ascontiguousarray(getattr(w, n)) for n in names if getattr(w, n) is not None}
+    offs, off = {}, 0
+    for n, a in host.items():
+        off = (off + 255) & ~255
+        offs[n] = off
+        off += a.nbytes
+    h_in = torch.empty(off, dtype=torch.uint8).pin_memory()
+    h_in_np = h_in.numpy()
+    for n, a in host.items():
+        h_in_np[offs[n]:offs[n] + a.nbytes] = a.reshape(-1).view(np.uint8)
+    h2d = off
+    ob = out.numel() * out.element_size()
+    ib_off = (ob + 255) & ~255
+    # two output buffers (device and pinned host), alternating per step
+    d_outs = [torch.empty(ib_off + idx.numel() * idx.element_size(), dtype=torch.uint8, device="cuda")
+              for _ in range(2)]
+    outs_v = [(d[:ob].view(out.dtype).view(out.shape), d[ib_off:].view(idx.dtype).view(idx.shape)) for d in d_outs]
+    h_outs = [torch.empty(d.numel(), dtype=torch.uint8).pin_memory() for d in d_outs]
+    d2h = d_outs[0].numel()
+    e2e_args = []  # per input copy: device staging buffer and argument structs pointing into it
+    for dp in copies:
+        d_in = torch.empty(off, dtype=torch.uint8, device="cuda")
+        ia = binding.IndexArgs(*[getattr(dp.ia, f_) for f_, _ in binding.IndexArgs._fields_])
+        aa = binding.AttnArgs(*[getattr(dp.aa, f_) for f_, _ in binding.AttnArgs._fields_])
+        base = d_in.data_ptr()
+        for n in host:
+            if n == "Q":
+                aa.Q = base + offs[n]
+            else:
+                setattr(ia, n, base + offs[n])
+        e2e_args.append((d_in, ia, aa))
+    # A serving loop's pipeline: step i's inputs go up on one copy stream while
+    # step i-1 computes, and step i-1's outputs come back on another while step
+    # i computes; events order every reuse of a buffer.
+    up_stream, down_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    nsteps_total = args.steps + 2
+    ev_up = [torch.cuda.Event() for _ in range(nsteps_total)]
+    ev_comp = [torch.cuda.Event() for _ in range(nsteps_total)]
+    ev_down = [torch.cuda.Event() for _ in range(nsteps_total)]
 
-    def e2e_step(i):
-        dp = copies[i % len(copies)]
-        for n, t in pinned.items():
-            dp.tensors[n].copy_(t, non_blocking=True)
-        binding.sa_fused_decode(dp.ia, dp.aa, K, idx, out, ws, stream)
-        out_h.copy_(out, non_blocking=True)
-        idx_h.copy_(idx, non_blocking=True)
+    def e2e_step(i, g):
+        d_in, ia, aa = e2e_args[i % len(e2e_args)]
+        with torch.cuda.stream(up_stream):
+            if g >= len(e2e_args):  # the staging buffer was read by step g - 3
+                up_stream.wait_event(ev_comp[g - len(e2e_args)])
+            d_in.copy_(h_in, non_blocking=True)
+            ev_up[g].record(up_stream)
+        stream.wait_event(ev_up[g])
+        if g >= 2:  # the output buffer was read back by step g - 2
+            stream.wait_event(ev_down[g - 2])
+        out_v, idx_v = outs_v[g % 2]
+        binding.sa_fused_decode(ia, aa, K, idx_v, out_v, ws, stream)
+        ev_comp[g].record(stream)
+        with torch.cuda.stream(down_stream):
+            down_stream.wait_event(ev_comp[g])
+            h_outs[g % 2].copy_(d_outs[g % 2], non_blocking=True)
+            ev_down[g].record(down_stream)
 
     for i in range(2):
-        e2e_step(i)
+        e2e_step(i, i)
     torch.cuda.synchronize()
+    ev_up = [torch.cuda.Event() for _ in range(nsteps_total)]
+    ev_comp = [torch.cuda.Event() for _ in range(nsteps_total)]
+    ev_down = [torch.cuda.Event() for _ in range(nsteps_total)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    up_stream.wait_stream(stream)
+    down_stream.wait_stream(stream)
     for i in range(args.steps):
-        e2e_step(i)
+        e2e_step(i, i)
+    stream.wait_stream(up_stream)
+    stream.wait_stream(down_stream)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
@@ -417,7 +468,9 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": nbytes[dom]},
         "stages": stages,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": "per-step query inputs copied from pinned host memory, index/KV caches resident"},
+                "note": "every step copies its query inputs from pinned host memory (one copy) and reads out + idx "
+                        "back (one copy); the copies run on their own streams, overlapped with the neighbouring "
+                        "steps' compute; index/KV caches resident"},
         "gpu_launches": launches_per_step * args.steps,
         "launch": "CUDA graph replay of one sa_fused_decode call per step",
         "eager": {"ms_per_step": round(eager_ms_per_step, 5),
