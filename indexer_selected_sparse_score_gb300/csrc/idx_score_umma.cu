@@ -282,6 +282,7 @@ struct ScoreParams {
   float *scores;
   int64_t ld;
   uint32_t *status;
+  int evict_first;  // nonzero: key rows are read once per call (at most one token per sequence)
 };
 
 __device__ __forceinline__ int token_tiles(const ScoreParams &p, int t, int *b_out, int *nv_out) {
@@ -342,6 +343,21 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_trigger();
 
+  // The tile plan below starts from every token's sequence and position.
+  // Their loads go out first, so that their latency (the first touch of
+  // these inputs in the step) overlaps the set-up; each thread keeps the
+  // first eight tokens of its chunk in registers.
+  constexpr int kW = kMainThreads / 32;
+  const int chunk = (p.T + kMainThreads - 1) / kMainThreads;
+  const int c0 = min(p.T, tid * chunk), c1 = min(p.T, c0 + chunk);
+  int sq[8], ps[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int tt = min(c0 + k, p.T - 1);
+    sq[k] = p.q_seq[tt];
+    ps[k] = p.q_pos[tt];
+  }
+
   // ---- set-up: barriers, tensor memory
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -374,22 +390,22 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
   // into a later token), so key tiles can stream before the prep kernel ends.
   int *plan_s = reinterpret_cast<int *>(smem + L::misc + 64);  // [8]
   {
-    constexpr int kW = kMainThreads / 32;
     int *wsum_s = plan_s + 8;  // [kW + 1]
-    const int chunk = (p.T + kMainThreads - 1) / kMainThreads;
-    const int c0 = min(p.T, tid * chunk), c1 = min(p.T, c0 + chunk);
     int sum = 0;
-    for (int base = c0; base < c1; base += 8) {  // eight loads in flight per round
-      int sq[8], ps[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (c0 + k < c1) sum += tiles_of(p.B, p.N_c, p.r, sq[k], ps[k]);
+    for (int base = c0 + 8; base < c1; base += 8) {  // longer chunks: eight loads in flight per round
+      int sq2[8], ps2[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const int tt = min(base + k, c1 - 1);
-        sq[k] = p.q_seq[tt];
-        ps[k] = p.q_pos[tt];
+        sq2[k] = p.q_seq[tt];
+        ps2[k] = p.q_pos[tt];
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        if (base + k < c1) sum += tiles_of(p.B, p.N_c, p.r, sq[k], ps[k]);
+        if (base + k < c1) sum += tiles_of(p.B, p.N_c, p.r, sq2[k], ps2[k]);
     }
     int incl = sum;
 #pragma unroll
@@ -417,19 +433,32 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
       plan_s[1] = end0;
     }
     if (begin0 < end0 && pre <= begin0 && begin0 < pre + sum) {  // this chunk holds tile begin0
-      int run = pre;
-      for (int tt = c0; tt < c1; ++tt) {
-        const int b = p.q_seq[tt], pos = p.q_pos[tt];
-        const int tl = tiles_of(p.B, p.N_c, p.r, b, pos);
-        if (begin0 < run + tl) {
-          plan_s[2] = tt;
-          plan_s[3] = run;
-          plan_s[4] = run + tl;
-          plan_s[5] = b;
-          plan_s[6] = min(n_vis_of(pos, p.r), p.N_c);
-          break;
+      int run = pre, tt = c0, b = 0, pos = 0, tl = 0;
+      bool found = false;
+#pragma unroll
+      for (int k = 0; k < 8; ++k)  // the first eight tokens from registers
+        if (!found && c0 + k < c1) {
+          tt = c0 + k;
+          b = sq[k];
+          pos = ps[k];
+          tl = tiles_of(p.B, p.N_c, p.r, b, pos);
+          found = begin0 < run + tl;
+          if (!found) run += tl;
         }
-        run += tl;
+      for (int t2 = c0 + 8; !found && t2 < c1; ++t2) {  // the rest reloaded
+        tt = t2;
+        b = p.q_seq[t2];
+        pos = p.q_pos[t2];
+        tl = tiles_of(p.B, p.N_c, p.r, b, pos);
+        found = begin0 < run + tl;
+        if (!found) run += tl;
+      }
+      if (found) {
+        plan_s[2] = tt;
+        plan_s[3] = run;
+        plan_s[4] = run + tl;
+        plan_s[5] = b;
+        plan_s[6] = min(n_vis_of(pos, p.r), p.N_c);
       }
     }
     __syncthreads();
@@ -446,6 +475,7 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
     // ------------------------------------------------------ TMA producer
     if (lane == 0 && begin < end) {
       prefetch_tmap(&kmap);
+      const uint64_t kpol = l2_policy(p.evict_first != 0);
       TileCursor cur;
       cur.init(plan_a, plan_b);
       int prev_t = -1, qn = -1;
@@ -455,7 +485,8 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
       const int n_pre = min(min(end, cur.next) - begin, kStages);
       for (int n = 0; n < n_pre; ++n) {
         mbar_expect_tx(&kfull[n], kKeyTileBytes);
-        tma_load_2d(keys + n * kKeyTileBytes, &kmap, &kfull[n], 0, cur.b * p.N_c + (begin + n - cur.first) * kTileKeys);
+        tma_load_2d_hint(keys + n * kKeyTileBytes, &kmap, &kfull[n], 0,
+                         cur.b * p.N_c + (begin + n - cur.first) * kTileKeys, kpol);
         ++issued;
       }
       pdl_wait();
@@ -476,7 +507,7 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
         if (n < n_pre) continue;  // issued above
         if (!mbar_wait(&kempty[s], ((n / kStages) & 1) ^ 1)) { fail(); break; }
         mbar_expect_tx(&kfull[s], kKeyTileBytes);
-        tma_load_2d(keys + s * kKeyTileBytes, &kmap, &kfull[s], 0, b * p.N_c + j * kTileKeys);
+        tma_load_2d_hint(keys + s * kKeyTileBytes, &kmap, &kfull[s], 0, b * p.N_c + j * kTileKeys, kpol);
         ++issued;
       }
       // drain: every issued copy must land before the CTA may exit
@@ -546,10 +577,11 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
       cur.init(plan_a, plan_b);
       ahead.init(plan_a, plan_b);
       int prev_t = -1, qn = -1;
+      const uint64_t kpol = l2_policy(p.evict_first != 0);
       auto scale_at = [&](const TileCursor &c, int ii) -> float {
         const int ss = (ii - c.first) * kTileKeys + row;
         if (!p.k_scale || ss >= c.nv) return 1.f;
-        return p.k_scale[static_cast<int64_t>(c.b) * p.N_c + ss];
+        return ld_f32_hint(p.k_scale + static_cast<int64_t>(c.b) * p.N_c + ss, kpol);
       };
       float ksq[kScaleAhead];  // scales of tiles i .. i + kScaleAhead - 1
 #pragma unroll
@@ -657,7 +689,7 @@ cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld,
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
   ScoreParams sp{ia.B, ia.T, ia.N_c, ia.r, ia.q_seq, ia.q_pos, prefix, qpack, wq, ia.k_scale, scores,
-                 ld, status};
+                 ld, status, ia.T <= ia.B ? 1 : 0};
   auto kern = idx_score_umma_kernel<NH, P>;
   const size_t smem = L::total + 1024;  // + alignment slack for the 1024-byte swizzle atoms
   static bool attr_done[64] = {};

@@ -81,6 +81,7 @@ struct AttnUmmaParams {
   int B, T, N_c, r, W, R, K;
   int WT, TPT;                    // window tiles per token, tiles per token
   int split, PT0;                 // CTAs per token (1, or a 2-CTA cluster with one token), tiles of rank 0's part
+  int evict_first;                // nonzero: K/V rows are read once per call (at most one token per sequence)
   const int32_t *q_seq, *q_pos, *idx;
   const __nv_bfloat16 *Vw, *Vc;   // V rows (window ring, compressed), 128 bf16 each
   const float *sink;
@@ -134,9 +135,12 @@ __device__ __forceinline__ void tmem_st_16x2_x8(uint32_t taddr, const uint32_t (
                : "memory");
 }
 
-// 16-byte global -> shared copy (L2 only), tracked by cp_async_mbar_arrive.
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+// 16-byte global -> shared copy (L2 only, eviction policy from l2_policy),
+// tracked by cp_async_mbar_arrive.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "l"(policy)
+               : "memory");
 }
 
 // Arrives on `bar` (without raising its expected count) once every cp.async
@@ -156,11 +160,12 @@ __device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uin
 }
 
 __device__ __forceinline__ void gather4(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y0, int y1,
-                                        int y2, int y3) {
+                                        int y2, int y3, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+      "l"(policy)
       : "memory");
 }
 
@@ -398,6 +403,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
       const int nw = is_k ? kKWarps : kVWarps;
       uint64_t *ring_full = is_k ? kfull : vfull;
       uint64_t *ring_empty = is_k ? kempty : vempty;
+      const uint64_t rpol = l2_policy(p.evict_first != 0);
       uint8_t *ring = is_k ? ks : vs;
       if (count > 0) {
         if (warp == kKWarp0 && lane == 0) {
@@ -522,7 +528,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
             if (mine) {
               const CUtensorMap *map = window ? &kwmap : &kcmap;
               uint8_t *dst = ring + s * 32768 + half * 16384 + 4 * g * 128;
-              gather4(dst, map, &ring_full[s], half * 64, gr[0], gr[1], gr[2], gr[3]);
+              gather4(dst, map, &ring_full[s], half * 64, gr[0], gr[1], gr[2], gr[3], rpol);
             }
           } else {
             // V rows by 16-byte cp.async: a warp instruction copies two rows
@@ -543,7 +549,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
               const int row = hr ? r1 : r0, key = 2 * pr + hr;
               if (row >= 0)
                 cp_async16(slot + key * 128 + (((ch & 7) ^ (key & 7)) << 4),
-                           vbase + static_cast<int64_t>(row) * (kD * 2) + ch * 16);
+                           vbase + static_cast<int64_t>(row) * (kD * 2) + ch * 16, rpol);
             }
             cp_async_mbar_arrive(&ring_full[s]);
           }
@@ -943,6 +949,7 @@ cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(sparse_mqa_umma_kernel), smem, attr_done);
   if (e != cudaSuccess) return e;
   p.split = attn_split(ia, p.TPT);
+  p.evict_first = ia.T <= ia.B ? 1 : 0;
   p.PT0 = (p.TPT + 1) / 2;  // rank 0 takes the larger half (window included); rank 1's hand-off costs about its merge
   const int sms = sm_count();
   // whole tokens (at most one CTA per SM), or one cluster pair per token
