@@ -55,28 +55,51 @@ constexpr int kCtasPerSm = kAccStages * NH <= 256 ? 2 : 1;
 // and the 1 KB alignment slack): 228 KB per SM, 227 KB per CTA.
 template <int NH>
 constexpr size_t kSmemBudget = kCtasPerSm<NH> == 2 ? 233472 / 2 - 2048 : 232448 - 1024;
-constexpr int kScaleAhead = 8;                   // key-scale prefetch distance, in tiles
-constexpr int kMainThreads = 192;
+constexpr int kMainThreads = 224;
 constexpr int kPrepThreads = 256;
+
+// Work split of the main kernel.  The first part of the flattened (token, key
+// tile) list is cut into one contiguous range per CTA; the rest is a pool of
+// kPoolChunk-tile chunks that CTAs claim one at a time from a global counter
+// once their own work runs low, so CTAs on SMs that stream slower than others
+// end up with fewer tiles and all finish together.
+constexpr int kPoolChunk = 4;
+constexpr int kClaimAhead = 4;  // claim when at most this many queued tiles are left to issue
+constexpr int kSegQ = 4;        // segments queued between the scheduler and the producer warp
+__device__ __forceinline__ int static_tiles(int total) {
+  return total - static_cast<int>((3ll * total) / 8);
+}
 
 template <int NH, int P>
 struct ScoreSmem {
   static constexpr int kQBytes = P * NH * 128;
-  // everything but the key ring: two query buffers, two weight vectors, barriers (at most
-  // 2 * kMaxStages + 13 of them) and the misc words
+  static constexpr int kInfoMax = kMaxStages + kAccStages;
+  // everything but the key ring: two query buffers, two weight vectors, the
+  // tile records and their key scales, the segment queue, barriers (at most
+  // 2 * kMaxStages + 13 + 2 * kSegQ of them) and the misc words
   static constexpr size_t kFixed = 2 * static_cast<size_t>(kQBytes) + 2 * NH * sizeof(float) +
-                                   (2 * kMaxStages + 13) * sizeof(uint64_t) + 128 + 8;
+                                   kInfoMax * (kTileKeys * sizeof(float) + 16) + kSegQ * 32 +
+                                   (2 * kMaxStages + 13 + 2 * kSegQ) * sizeof(uint64_t) + 128 + 8;
   static constexpr int kStages = static_cast<int>(
       (kSmemBudget<NH> - kFixed) / kKeyTileBytes < kMaxStages ? (kSmemBudget<NH> - kFixed) / kKeyTileBytes
                                                                 : kMaxStages);
+  // tile records live until the epilogue has read them: the producer reuses
+  // record n % kInfo for tile n only after the MMA of tile n + kAccStages - kInfo
+  // freed its smem stage, and that MMA waited for the epilogue to release tile n - kInfo
+  static constexpr int kInfo = kStages + kAccStages;
   static constexpr size_t keys = 0;
   static constexpr size_t qbuf = keys + static_cast<size_t>(kStages) * kKeyTileBytes;
   static constexpr size_t wq = qbuf + 2 * static_cast<size_t>(kQBytes);
-  static constexpr size_t bars = wq + 2 * NH * sizeof(float);
-  static constexpr int kBars = 2 * kStages + 4 + 2 * kAccStages + 1;
+  static constexpr size_t ksc = wq + 2 * NH * sizeof(float);
+  static constexpr size_t info = ksc + static_cast<size_t>(kInfo) * kTileKeys * sizeof(float);
+  static constexpr size_t seg = info + static_cast<size_t>(kInfo) * 16;
+  static constexpr size_t bars = seg + kSegQ * 32;
+  static constexpr int kBars = 2 * kStages + 4 + 2 * kAccStages + 1 + 2 * kSegQ;
   static constexpr size_t misc = bars + kBars * sizeof(uint64_t);
-  static constexpr size_t total = misc + 128;  // tmem base, abort flag; plan words at misc + 64
+  // tmem base, abort flag, tiles issued; plan words at misc + 64
+  static constexpr size_t total = misc + 128;
   static_assert(total <= kSmemBudget<NH>, "shared memory budget");
+  static_assert(kInfo <= kInfoMax, "tile records");
 };
 
 // ---------------------------------------------------------------- prep ----
@@ -121,14 +144,16 @@ __device__ __forceinline__ int plan_block_scan(int v, int *warp_sums) {
 // -inf into the masked tail of the score row.
 // Block T: prefix[t] = key tiles of the tokens before t (prefix[T] = all
 // tiles), which the main kernel reads when a CTA crosses into a later token
-// (each CTA computes its own starting point from the inputs).
+// (each CTA computes its own starting point from the inputs), and resets the
+// main kernel's pool counter.
 template <int NH, bool QFP8>
 __global__ void __launch_bounds__(kPrepThreads)
 idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq,
                  const int32_t *__restrict__ q_pos, const void *__restrict__ q_I,
                  const float *__restrict__ q_scale, const float *__restrict__ w,
                  uint8_t *__restrict__ qpack, float *__restrict__ wq, float *__restrict__ scores,
-                 int64_t ld, int write_masked, int32_t *__restrict__ prefix, uint32_t *status) {
+                 int64_t ld, int write_masked, int32_t *__restrict__ prefix, int *__restrict__ pool,
+                 uint32_t *status) {
   constexpr int P = QFP8 ? 1 : 2;
   constexpr int kHeadsPerWarp = NH / (kPrepThreads / 32);
   pdl_trigger();
@@ -137,6 +162,7 @@ idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq
     // (no large shared array: prep blocks must fit beside the main kernel's
     // CTAs, which start early and fill the SMs' shared memory)
     __shared__ int warp_sums[32];
+    if (threadIdx.x == 0) *pool = 0;  // no pool chunk handed out yet
     int *cnt_s = prefix;  // tile counts, then their prefix, staged in global memory
     // (a) tile count of every token, one token per thread, coalesced, four loads in flight
     for (int t0 = threadIdx.x; t0 < T; t0 += 4 * kPrepThreads) {
@@ -282,49 +308,17 @@ struct ScoreParams {
   float *scores;
   int64_t ld;
   uint32_t *status;
+  int *pool;        // pool chunks claimed so far (zeroed by the prep kernel)
   int evict_first;  // nonzero: key rows are read once per call (at most one token per sequence)
 };
 
-__device__ __forceinline__ int token_tiles(const ScoreParams &p, int t, int *b_out, int *nv_out) {
-  const int b = p.q_seq[t], pos = p.q_pos[t];
-  if (b < 0 || b >= p.B || pos < 0) return 0;
-  const int nv = min(n_vis_of(pos, p.r), p.N_c);
-  if (b_out) *b_out = b;
-  if (nv_out) *nv_out = nv;
-  return (nv + kTileKeys - 1) / kTileKeys;
-}
-
-// Walks a CTA's tile range token by token; the token boundary and the
-// token's sequence / visible count are read from memory only when a token
-// starts, never per tile.
-struct TileCursor {
-  int t, first, next, b, nv;  // token, its first tile, first tile of the next token
-  __device__ void init(const int4 &a, const int4 &c) {  // {_, _, t, first}, {next, b, nv, _}
-    t = a.z;
-    first = a.w;
-    next = c.x;
-    b = c.y;
-    nv = c.z;
-  }
-  // moves to the token holding tile i (i never decreases); true if it changed
-  __device__ bool seek(const ScoreParams &p, int i) {
-    if (i < next) return false;
-    do {
-      ++t;
-      first = next;
-      next = p.prefix[t + 1];
-    } while (i >= next);
-    token_tiles(p, t, &b, &nv);
-    return true;
-  }
-};
-
 template <int NH, int P>
-__global__ void __launch_bounds__(kMainThreads, 1)
+__global__ void __launch_bounds__(kMainThreads, kCtasPerSm<NH>)
 idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParams p) {
   using L = ScoreSmem<NH, P>;
   constexpr int kQBytes = L::kQBytes;
   constexpr int kStages = L::kStages;
+  constexpr int kInfo = L::kInfo;
   constexpr uint32_t kTmemCols = kAccStages * NH;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the swizzle atoms need 1024-byte alignment: align the base explicitly
@@ -332,13 +326,18 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
   uint8_t *keys = smem + L::keys;
   uint8_t *qbuf = smem + L::qbuf;
   float *wqs = reinterpret_cast<float *>(smem + L::wq);
+  float *ksc = reinterpret_cast<float *>(smem + L::ksc);  // [kInfo][128] key scales of a tile
+  int4 *info = reinterpret_cast<int4 *>(smem + L::info);  // [kInfo] {token (-1: end), first position, n_vis, query buffer}
+  int *segq = reinterpret_cast<int *>(smem + L::seg);     // [kSegQ][8] {tile, end tile, token, first tile, b, n_vis}
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bars);
   uint64_t *kfull = bars, *kempty = bars + kStages;
   uint64_t *qfull = bars + 2 * kStages, *qempty = qfull + 2;
   uint64_t *afull = qempty + 2, *aempty = afull + kAccStages;
   uint64_t *done = aempty + kAccStages;
+  uint64_t *segfull = done + 1, *segempty = segfull + kSegQ;
   uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem + L::misc);
   int *abort_s = reinterpret_cast<int *>(smem + L::misc + 8);
+  int *issued_s = reinterpret_cast<int *>(smem + L::misc + 16);  // key tiles the producer has issued
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_trigger();
@@ -361,7 +360,7 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
   // ---- set-up: barriers, tensor memory
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&kfull[i], 1);
+      mbar_init(&kfull[i], 1 + 32);  // the key tile's copy (with its record) + the 32 key-scale copies
       mbar_init(&kempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -369,11 +368,16 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
       mbar_init(&qempty[i], 1 + 4);  // MMA commit + four epilogue warps
     }
     for (int i = 0; i < kAccStages; ++i) {
-      mbar_init(&afull[i], 1);
+      mbar_init(&afull[i], 2);  // MMA commit + the issuing lane, which passes the tile record on
       mbar_init(&aempty[i], 4);
     }
     mbar_init(done, 1);
+    for (int i = 0; i < kSegQ; ++i) {
+      mbar_init(&segfull[i], 1);
+      mbar_init(&segempty[i], 1);
+    }
     *abort_s = 0;
+    *issued_s = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -385,9 +389,9 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
   tc_fence_after();
   const uint32_t tmem = *tmem_base_s;
 
-  // This CTA's tile range and its first token, from the inputs alone (the
-  // prep kernel's prefix is the same plan; it is read only when a CTA crosses
-  // into a later token), so key tiles can stream before the prep kernel ends.
+  // This CTA's own tile range and its first token, from the inputs alone (the
+  // prep kernel's prefix is the same plan; the scheduler reads it for later
+  // tokens), so key tiles can stream before the prep kernel ends.
   int *plan_s = reinterpret_cast<int *>(smem + L::misc + 64);  // [8]
   {
     int *wsum_s = plan_s + 8;  // [kW + 1]
@@ -426,11 +430,13 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
     }
     __syncthreads();
     const int pre = wsum_s[warp] + incl - sum, total = wsum_s[kW];
-    const int begin0 = static_cast<int>(static_cast<long long>(total) * blockIdx.x / gridDim.x);
-    const int end0 = static_cast<int>(static_cast<long long>(total) * (blockIdx.x + 1) / gridDim.x);
+    const int S = static_tiles(total);
+    const int begin0 = static_cast<int>(static_cast<long long>(S) * blockIdx.x / gridDim.x);
+    const int end0 = static_cast<int>(static_cast<long long>(S) * (blockIdx.x + 1) / gridDim.x);
     if (tid == 0) {
       plan_s[0] = begin0;
       plan_s[1] = end0;
+      plan_s[7] = total;
     }
     if (begin0 < end0 && pre <= begin0 && begin0 < pre + sum) {  // this chunk holds tile begin0
       int run = pre, tt = c0, b = 0, pos = 0, tl = 0;
@@ -463,193 +469,355 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
     }
     __syncthreads();
   }
-  const int begin = plan_s[0], end = plan_s[1];
-  const int4 plan_a = make_int4(begin, end, plan_s[2], plan_s[3]);
-  const int4 plan_b = make_int4(plan_s[4], plan_s[5], plan_s[6], 0);
+  const int begin = plan_s[0], end = plan_s[1], total = plan_s[7];
+  // the first token of the own range (meaningful only when begin < end)
+  const int t0 = plan_s[2], first0 = plan_s[3], next0 = plan_s[4], b0 = plan_s[5], nv0 = plan_s[6];
   auto fail = [&]() {
     raise_flag(p.status, kFlagTimeout);
     atomicExch(abort_s, 1);
   };
+  auto aborted = [&]() { return __any_sync(0xffffffffu, *(volatile int *)abort_s != 0); };
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
-    if (lane == 0 && begin < end) {
-      prefetch_tmap(&kmap);
-      const uint64_t kpol = l2_policy(p.evict_first != 0);
-      TileCursor cur;
-      cur.init(plan_a, plan_b);
-      int prev_t = -1, qn = -1;
-      int issued = 0;
-      // the key tiles of the first token (up to the ring size) do not depend on
-      // the prep kernel: issue them first, then wait for its packed queries
-      const int n_pre = min(min(end, cur.next) - begin, kStages);
-      for (int n = 0; n < n_pre; ++n) {
-        mbar_expect_tx(&kfull[n], kKeyTileBytes);
-        tma_load_2d_hint(keys + n * kKeyTileBytes, &kmap, &kfull[n], 0,
-                         cur.b * p.N_c + (begin + n - cur.first) * kTileKeys, kpol);
-        ++issued;
-      }
-      pdl_wait();
-      for (int i = begin; i < end && !*(volatile int *)abort_s; ++i) {
-        cur.seek(p, i);
-        const int t = cur.t, b = cur.b;
-        if (t != prev_t) {
-          ++qn;
-          const int qb = qn & 1;
-          if (!mbar_wait(&qempty[qb], ((qn >> 1) & 1) ^ 1)) { fail(); break; }
-          mbar_expect_tx(&qfull[qb], kQBytes + NH * 4);
-          bulk_load(qbuf + qb * kQBytes, p.qpack + static_cast<size_t>(t) * kQBytes, kQBytes, &qfull[qb]);
-          bulk_load(wqs + qb * NH, p.wq + static_cast<size_t>(t) * NH, NH * 4, &qfull[qb]);
-          prev_t = t;
-        }
-        const int j = i - cur.first;
-        const int n = i - begin, s = n % kStages;
-        if (n < n_pre) continue;  // issued above
-        if (!mbar_wait(&kempty[s], ((n / kStages) & 1) ^ 1)) { fail(); break; }
+    // The whole warp walks its tiles segment by segment (a run of tiles of
+    // one token): lane 0 writes the tile record and issues the key tile,
+    // every lane copies four of the tile's 128 key scales.
+    if (lane == 0) prefetch_tmap(&kmap);
+    const uint64_t kpol = l2_policy(p.evict_first != 0);
+    int n = 0, qn = -1, prev_t = -1, si = 0;
+    bool ok = true;
+    // current segment: tiles [i, i1) of token t (first tile `first`, sequence b, nv visible)
+    int i = begin, i1 = begin < end ? min(end, next0) : begin;
+    int t = t0, first = first0, b = b0, nv = nv0;
+    auto issue = [&]() {
+      const int s = n % kStages, k = n % kInfo;
+      const int s0 = (i - first) * kTileKeys;
+      if (lane == 0) {
+        info[k] = make_int4(t, s0, nv, qn);
         mbar_expect_tx(&kfull[s], kKeyTileBytes);
-        tma_load_2d_hint(keys + s * kKeyTileBytes, &kmap, &kfull[s], 0, b * p.N_c + j * kTileKeys, kpol);
-        ++issued;
+        tma_load_2d_hint(keys + s * kKeyTileBytes, &kmap, &kfull[s], 0, b * p.N_c + s0, kpol);
       }
-      // drain: every issued copy must land before the CTA may exit
-      for (int n = max(0, issued - kStages); n < issued; ++n)
-        mbar_wait(&kfull[n % kStages], (n / kStages) & 1);
+      if (p.k_scale) {
+        const int pos = s0 + 4 * lane;
+        const float *src = p.k_scale + static_cast<int64_t>(b) * p.N_c + pos;
+        float *dst = ksc + k * kTileKeys + 4 * lane;
+        if (pos + 3 < nv && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+          cp_async16(dst, src, kpol);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (pos + e < nv) cp_async4(dst + e, src + e);
+        }
+      }
+      cp_async_mbar_arrive(&kfull[s]);
+      ++n;
+      ++i;
+    };
+    auto load_q = [&]() -> bool {  // the current token's packed queries and weights
+      ++qn;
+      const int qb = qn & 1;
+      if (!mbar_wait_warp(&qempty[qb], ((qn >> 1) & 1) ^ 1)) return false;
+      if (lane == 0) {
+        mbar_expect_tx(&qfull[qb], kQBytes + NH * 4);
+        bulk_load(qbuf + qb * kQBytes, p.qpack + static_cast<size_t>(t) * kQBytes, kQBytes, &qfull[qb]);
+        bulk_load(wqs + qb * NH, p.wq + static_cast<size_t>(t) * NH, NH * 4, &qfull[qb]);
+      }
+      prev_t = t;
+      return true;
+    };
+    // the first key tiles of the own range (up to the ring size) do not
+    // depend on the prep kernel: issue them first, then wait for its queries
+    const int n_pre = min(i1 - i, kStages);
+    if (n_pre > 0) qn = 0;
+    while (n < n_pre) issue();
+    pdl_wait();
+    if (n_pre > 0) {
+      qn = -1;
+      ok = load_q();
+    }
+    while (ok) {
+      if (aborted()) {
+        ok = false;
+        break;
+      }
+      if (i >= i1) {  // next segment from the scheduler
+        const int q = si % kSegQ;
+        if (!mbar_wait_warp(&segfull[q], (si / kSegQ) & 1)) {
+          ok = false;
+          break;
+        }
+        const int *e = segq + q * 8;
+        i = e[0];
+        i1 = e[1];
+        t = e[2];
+        first = e[3];
+        b = e[4];
+        nv = e[5];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&segempty[q]);
+        ++si;
+        if (i < 0) break;  // no more work
+        continue;
+      }
+      if (t != prev_t && !load_q()) {
+        ok = false;
+        break;
+      }
+      const int s = n % kStages;
+      if (!mbar_wait_warp(&kempty[s], ((n / kStages) & 1) ^ 1)) {
+        ok = false;
+        break;
+      }
+      issue();
+      if (lane == 0) *(volatile int *)issued_s = n;
+    }
+    if (ok) {  // end of work: a record with token -1, passed on by the MMA warp to the epilogue
+      const int s = n % kStages;
+      if (mbar_wait_warp(&kempty[s], ((n / kStages) & 1) ^ 1)) {
+        if (lane == 0) {
+          info[n % kInfo] = make_int4(-1, 0, 0, 0);
+          mbar_arrive(&kfull[s]);
+        }
+        cp_async_mbar_arrive(&kfull[s]);
+        ++n;
+      } else {
+        ok = false;
+      }
+    }
+    if (!ok && lane == 0) fail();
+    // drain: every issued copy lands before the CTA may exit
+    cp_async_wait_all();
+    if (lane == 0) {
+      for (int m = max(0, n - kStages); m < n; ++m) mbar_wait(&kfull[m % kStages], (m / kStages) & 1);
       if (qn >= 0) mbar_wait(&qfull[qn & 1], (qn >> 1) & 1);
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
-    // The whole warp walks the tiles and waits; one elected lane issues the
-    // MMAs and commits from operands the warp computed uniformly.
-    pdl_wait();  // token boundaries come from the prep kernel's prefix
-    if (begin < end) {
-      constexpr uint32_t idesc = idesc_e4m3(kTileKeys, NH);
-      const bool leader = elect_one();
-      TileCursor cur;
-      cur.init(plan_a, plan_b);
-      int prev_t = -1, qn = -1;
-      bool ok = true;
-      for (int i = begin; i < end; ++i) {
-        if (__any_sync(0xffffffffu, *(volatile int *)abort_s != 0)) break;
-        cur.seek(p, i);
-        const int t = cur.t;
-        if (t != prev_t) {
-          if (qn >= 0 && leader) mma_commit(&qempty[qn & 1]);
-          ++qn;
-          if (!mbar_wait_warp(&qfull[qn & 1], (qn >> 1) & 1)) { ok = false; break; }
-          prev_t = t;
-        }
-        const int n = i - begin, s = n % kStages, a = n % kAccStages;
-        if (!mbar_wait_warp(&kfull[s], (n / kStages) & 1) ||
-            !mbar_wait_warp(&aempty[a], ((n / kAccStages) & 1) ^ 1)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t d = tmem + a * NH;
-        const uint32_t a0 = smem_u32(keys + s * kKeyTileBytes);
-        const uint32_t b0 = smem_u32(qbuf + (qn & 1) * kQBytes);
-        if (leader) {
-#pragma unroll
-          for (int pc = 0; pc < P; ++pc)
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_f8f6f4(d, desc_sw128_kmajor(a0 + 32 * k), desc_sw128_kmajor(b0 + pc * NH * 128 + 32 * k),
-                         idesc, (pc | k) != 0);
-          mma_commit(&kempty[s]);
-          mma_commit(&afull[a]);
-        }
-        __syncwarp();
+    // The whole warp walks the tile records and waits; one elected lane
+    // issues the MMAs and commits from operands the warp computed uniformly.
+    constexpr uint32_t idesc = idesc_e4m3(kTileKeys, NH);
+    const bool leader = elect_one();
+    int qn = -1;
+    bool ok = true;
+    for (int n = 0;; ++n) {
+      if (aborted()) break;
+      const int s = n % kStages, a = n % kAccStages;
+      if (!mbar_wait_warp(&kfull[s], (n / kStages) & 1) ||
+          !mbar_wait_warp(&aempty[a], ((n / kAccStages) & 1) ^ 1)) {
+        ok = false;
+        break;
       }
-      if (!ok && lane == 0) fail();
+      const int4 ti = info[n % kInfo];
+      if (ti.x < 0) {  // end of work: pass the record on
+        if (leader) {
+          mbar_arrive(&afull[a]);
+          mbar_arrive(&afull[a]);
+        }
+        break;
+      }
+      if (ti.w != qn) {
+        if (qn >= 0 && leader) mma_commit(&qempty[qn & 1]);
+        qn = ti.w;
+        if (!mbar_wait_warp(&qfull[qn & 1], (qn >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+      }
+      tc_fence_after();
+      const uint32_t d = tmem + a * NH;
+      const uint32_t a0 = smem_u32(keys + s * kKeyTileBytes);
+      const uint32_t b0 = smem_u32(qbuf + (qn & 1) * kQBytes);
       if (leader) {
-        if (qn >= 0) mma_commit(&qempty[qn & 1]);
-        mma_commit(done);
-        if (!mbar_wait(done, 0)) raise_flag(p.status, kFlagTimeout);
+#pragma unroll
+        for (int pc = 0; pc < P; ++pc)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f8f6f4(d, desc_sw128_kmajor(a0 + 32 * k), desc_sw128_kmajor(b0 + pc * NH * 128 + 32 * k),
+                       idesc, (pc | k) != 0);
+        mma_commit(&kempty[s]);
+        mma_commit(&afull[a]);
+        mbar_arrive(&afull[a]);  // releases the tile record and key scales the epilogue reads
       }
       __syncwarp();
     }
-  } else {
+    if (!ok && lane == 0) fail();
+    if (leader) {
+      if (qn >= 0) mma_commit(&qempty[qn & 1]);
+      mma_commit(done);
+      if (!mbar_wait(done, 0)) raise_flag(p.status, kFlagTimeout);
+    }
+    __syncwarp();
+  } else if (warp < 6) {
     // --------------------------------------------------------- epilogue
-    pdl_wait();  // token boundaries come from the prep kernel's prefix
-    // The key scales are loaded kScaleAhead tiles ahead into a register
-    // queue: under a full memory stream their latency spans several tiles and
-    // would otherwise pace the whole pipeline.
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    if (begin < end) {
-      TileCursor cur, ahead;  // `ahead` runs kScaleAhead tiles in front for the scale prefetch
-      cur.init(plan_a, plan_b);
-      ahead.init(plan_a, plan_b);
-      int prev_t = -1, qn = -1;
-      const uint64_t kpol = l2_policy(p.evict_first != 0);
-      auto scale_at = [&](const TileCursor &c, int ii) -> float {
-        const int ss = (ii - c.first) * kTileKeys + row;
-        if (!p.k_scale || ss >= c.nv) return 1.f;
-        return ld_f32_hint(p.k_scale + static_cast<int64_t>(c.b) * p.N_c + ss, kpol);
-      };
-      float ksq[kScaleAhead];  // scales of tiles i .. i + kScaleAhead - 1
-#pragma unroll
-      for (int k = 0; k < kScaleAhead; ++k) {
-        ksq[k] = 1.f;
-        if (begin + k < end) {
-          ahead.seek(p, begin + k);
-          ksq[k] = scale_at(ahead, begin + k);
+    int qn = -1;
+    for (int n = 0;; ++n) {
+      if (aborted()) break;
+      const int a = n % kAccStages, k = n % kInfo;
+      if (!mbar_wait_warp(&afull[a], (n / kAccStages) & 1)) {
+        if (lane == 0) fail();
+        break;
+      }
+      const int4 ti = info[k];
+      if (ti.x < 0) break;
+      if (ti.w != qn) {
+        if (qn >= 0) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&qempty[qn & 1]);
+        }
+        qn = ti.w;
+        if (!mbar_wait_warp(&qfull[qn & 1], (qn >> 1) & 1)) {
+          if (lane == 0) fail();
+          break;
         }
       }
-      for (int i = begin; i < end && !*(volatile int *)abort_s; ++i) {
-        cur.seek(p, i);
-        const int t = cur.t, nv = cur.nv;
-        const float ks = ksq[0];
+      tc_fence_after();
+      uint32_t v[NH];
 #pragma unroll
-        for (int k = 0; k + 1 < kScaleAhead; ++k) ksq[k] = ksq[k + 1];
-        ksq[kScaleAhead - 1] = 1.f;
-        if (i + kScaleAhead < end) {
-          ahead.seek(p, i + kScaleAhead);
-          ksq[kScaleAhead - 1] = scale_at(ahead, i + kScaleAhead);
+      for (int c = 0; c < NH / 32; ++c)
+        tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * NH + 32 * c,
+                           *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
+      // the record and the scale are read before the stage is released (the
+      // producer reuses them once the stage's next MMA has run)
+      const float ks = p.k_scale ? ksc[k * kTileKeys + row] : 1.f;
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&aempty[a]);
+      const int s = ti.y + row;
+      if (s < ti.z) {
+        // sum_h w_h relu(d_h): eight independent partial sums (short chains),
+        // weights read four at a time
+        const float4 *wv4 = reinterpret_cast<const float4 *>(wqs + (qn & 1) * NH);
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+#pragma unroll
+        for (int h4 = 0; h4 < NH / 4; ++h4) {
+          const float4 w4 = wv4[h4];
+          float *a2 = &acc[(h4 & 1) * 4];
+          a2[0] = fmaf(w4.x, fmaxf(__uint_as_float(v[4 * h4]), 0.f), a2[0]);
+          a2[1] = fmaf(w4.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), a2[1]);
+          a2[2] = fmaf(w4.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), a2[2]);
+          a2[3] = fmaf(w4.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), a2[3]);
         }
-        if (t != prev_t) {
-          if (qn >= 0) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&qempty[qn & 1]);
-          }
-          ++qn;
-          if (!mbar_wait_warp(&qfull[qn & 1], (qn >> 1) & 1)) { fail(); break; }
-          prev_t = t;
-        }
-        const int n = i - begin, a = n % kAccStages;
-        if (!mbar_wait_warp(&afull[a], (n / kAccStages) & 1)) { fail(); break; }
-        tc_fence_after();
-        uint32_t v[NH];
-#pragma unroll
-        for (int c = 0; c < NH / 32; ++c)
-          tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * NH + 32 * c,
-                             *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&aempty[a]);
-        const int s = (i - cur.first) * kTileKeys + row;
-        if (s < nv) {
-          // sum_h w_h relu(d_h): eight independent partial sums (short chains),
-          // weights read four at a time
-          const float4 *wv4 = reinterpret_cast<const float4 *>(wqs + (qn & 1) * NH);
-          float acc[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-#pragma unroll
-          for (int h4 = 0; h4 < NH / 4; ++h4) {
-            const float4 w4 = wv4[h4];
-            float *a2 = &acc[(h4 & 1) * 4];
-            a2[0] = fmaf(w4.x, fmaxf(__uint_as_float(v[4 * h4]), 0.f), a2[0]);
-            a2[1] = fmaf(w4.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), a2[1]);
-            a2[2] = fmaf(w4.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), a2[2]);
-            a2[3] = fmaf(w4.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), a2[3]);
-          }
-          const float total = ((acc[0] + acc[4]) + (acc[1] + acc[5])) + ((acc[2] + acc[6]) + (acc[3] + acc[7]));
-          p.scores[static_cast<int64_t>(t) * p.ld + s] = total * ks;
-        }
-      }
-      if (qn >= 0) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&qempty[qn & 1]);
+        const float tot = ((acc[0] + acc[4]) + (acc[1] + acc[5])) + ((acc[2] + acc[6]) + (acc[3] + acc[7]));
+        p.scores[static_cast<int64_t>(ti.x) * p.ld + s] = tot * ks;
       }
     }
+    if (qn >= 0) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&qempty[qn & 1]);
+    }
+  } else {
+    // -------------------------------------------------------- scheduler
+    // Hands the producer its tiles as segments (runs of one token's tiles):
+    // the rest of the own range first, then pool chunks, each claimed only
+    // when the producer has at most kClaimAhead queued tiles left to issue.
+    pdl_wait();  // the token prefix and the pool counter come from the prep kernel
+    const int S = static_tiles(total);
+    // token cursor: token ct holds tiles [cfirst, cnext)
+    int ct = -1, cfirst = 0, cnext = 0, cb = 0, cnv = 0;
+    if (begin < end) {
+      ct = t0;
+      cfirst = first0;
+      cnext = next0;
+      cb = b0;
+      cnv = nv0;
+    }
+    int i = begin < end ? min(end, next0) : begin;
+    int pushed = i - begin, si = 0;
+    bool ok = true;
+    // moves the cursor forward to the token holding tile `tile` (< total):
+    // 32 tokens' boundaries per round, one load each
+    auto seek = [&](int tile) -> bool {
+      if (tile < cnext) return true;
+      for (int base = ct + 1; base < p.T; base += 32) {
+        const int cand = base + lane;
+        const int nx = cand < p.T ? p.prefix[cand + 1] : 0x7FFFFFFF;
+        const uint32_t hit = __ballot_sync(0xffffffffu, nx > tile);
+        if (hit) {
+          const int l = __ffs(hit) - 1;
+          ct = base + l;
+          if (ct >= p.T) return false;
+          cnext = __shfl_sync(0xffffffffu, nx, l);
+          int f = 0, bb = 0, pp = 0;
+          if (lane == 0) {
+            f = p.prefix[ct];
+            bb = p.q_seq[ct];
+            pp = p.q_pos[ct];
+          }
+          cfirst = __shfl_sync(0xffffffffu, f, 0);
+          cb = __shfl_sync(0xffffffffu, bb, 0);
+          cnv = min(n_vis_of(__shfl_sync(0xffffffffu, pp, 0), p.r), p.N_c);
+          return true;
+        }
+      }
+      return false;
+    };
+    auto push = [&](int i0, int i1) -> bool {
+      const int q = si % kSegQ;
+      if (!mbar_wait_warp(&segempty[q], ((si / kSegQ) & 1) ^ 1)) return false;
+      if (lane == 0) {
+        int *e = segq + q * 8;
+        e[0] = i0;
+        e[1] = i1;
+        e[2] = ct;
+        e[3] = cfirst;
+        e[4] = cb;
+        e[5] = cnv;
+        mbar_arrive(&segfull[q]);
+      }
+      __syncwarp();
+      ++si;
+      return true;
+    };
+    // the rest of the own range
+    while (ok && i < end) {
+      const int i1 = seek(i) ? min(end, cnext) : -1;
+      if (i1 < 0 || !push(i, i1)) {
+        ok = false;
+        break;
+      }
+      pushed += i1 - i;
+      i = i1;
+    }
+    // pool chunks
+    while (ok) {
+      const long long w0 = clock64();
+      for (;;) {  // until the producer has at most kClaimAhead queued tiles left
+        int wait = 0;
+        if (lane == 0)
+          wait = pushed - *(volatile int *)issued_s > kClaimAhead && !*(volatile int *)abort_s &&
+                 clock64() - w0 < kWaitBudgetCycles;
+        if (!__shfl_sync(0xffffffffu, wait, 0)) break;
+        __nanosleep(200);
+      }
+      if (aborted() || clock64() - w0 >= kWaitBudgetCycles) {
+        ok = false;
+        break;
+      }
+      int c = 0;
+      if (lane == 0) c = atomicAdd(p.pool, 1);
+      c = __shfl_sync(0xffffffffu, c, 0);
+      int i0 = S + c * kPoolChunk;
+      if (c >= (total - S + kPoolChunk - 1) / kPoolChunk) break;  // pool exhausted
+      const int ie = min(total, i0 + kPoolChunk);
+      while (i0 < ie) {
+        const int i1 = seek(i0) ? min(ie, cnext) : -1;
+        if (i1 < 0 || !push(i0, i1)) {
+          ok = false;
+          break;
+        }
+        pushed += i1 - i0;
+        i0 = i1;
+      }
+    }
+    if (!ok && lane == 0) fail();
+    push(-1, -1);  // end of work
   }
 
   tc_fence_before();
@@ -665,14 +833,14 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
 
 template <int NH, bool QFP8>
 cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld, bool write_masked,
-                             uint8_t *qpack, float *wq, int32_t *prefix, uint32_t *status,
+                             uint8_t *qpack, float *wq, int32_t *prefix, int *pool, uint32_t *status,
                              cudaStream_t stream) {
   constexpr int P = QFP8 ? 1 : 2;
   using L = ScoreSmem<NH, P>;
   const int grid = sm_count() * kCtasPerSm<NH>;
   idx_qprep_kernel<NH, QFP8><<<ia.T + 1, kPrepThreads, 0, stream>>>(
       ia.B, ia.T, ia.N_c, ia.r, ia.q_seq, ia.q_pos, ia.q_I, ia.q_scale, ia.w, qpack, wq, scores, ld,
-      write_masked ? 1 : 0, prefix, status);
+      write_masked ? 1 : 0, prefix, pool, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -688,8 +856,8 @@ cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
-  ScoreParams sp{ia.B, ia.T, ia.N_c, ia.r, ia.q_seq, ia.q_pos, prefix, qpack, wq, ia.k_scale, scores,
-                 ld, status, ia.T <= ia.B ? 1 : 0};
+  ScoreParams sp{ia.B,  ia.T,   ia.N_c, ia.r, ia.q_seq, ia.q_pos, prefix, qpack, wq, ia.k_scale, scores,
+                 ld,    status, pool,   ia.T <= ia.B ? 1 : 0};
   auto kern = idx_score_umma_kernel<NH, P>;
   const size_t smem = L::total + 1024;  // + alignment slack for the 1024-byte swizzle atoms
   static bool attr_done[64] = {};
@@ -743,7 +911,7 @@ bool idx_score_umma_supported(const sa_index_args &ia) {
 
 namespace {
 struct UmmaScratch {
-  size_t qpack, wq, prefix, total;
+  size_t qpack, wq, prefix, pool, total;
 };
 UmmaScratch umma_scratch_layout(const sa_index_args &ia) {
   const int P = ia.q_dtype == SA_FP8_E4M3 ? 1 : 2;
@@ -752,7 +920,8 @@ UmmaScratch umma_scratch_layout(const sa_index_args &ia) {
   L.qpack = 0;
   L.wq = up(static_cast<size_t>(ia.T) * P * ia.H_I * 128);
   L.prefix = L.wq + up(static_cast<size_t>(ia.T) * ia.H_I * 4);
-  L.total = L.prefix + up(static_cast<size_t>(ia.T + 1) * 4);
+  L.pool = L.prefix + up(static_cast<size_t>(ia.T + 1) * 4);
+  L.total = L.pool + 256;
   return L;
 }
 }  // namespace
@@ -767,10 +936,11 @@ cudaError_t launch_idx_score_umma(const sa_index_args &ia, float *scores, int64_
   uint8_t *qpack = base + L.qpack;
   float *wq = reinterpret_cast<float *>(base + L.wq);
   int32_t *prefix = reinterpret_cast<int32_t *>(base + L.prefix);
+  int *pool = reinterpret_cast<int *>(base + L.pool);
   const bool qf8 = ia.q_dtype == SA_FP8_E4M3;
 #define SA_UMMA_CASE(NH, QF)                                                                              \
   if (ia.H_I == NH && qf8 == QF)                                                                          \
-    return launch_umma_impl<NH, QF>(ia, scores, ld, write_masked, qpack, wq, prefix, status, stream);
+    return launch_umma_impl<NH, QF>(ia, scores, ld, write_masked, qpack, wq, prefix, pool, status, stream);
   SA_UMMA_CASE(32, false)
   SA_UMMA_CASE(32, true)
   SA_UMMA_CASE(64, false)

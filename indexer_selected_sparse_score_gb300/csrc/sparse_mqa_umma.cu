@@ -135,20 +135,6 @@ __device__ __forceinline__ void tmem_st_16x2_x8(uint32_t taddr, const uint32_t (
                : "memory");
 }
 
-// 16-byte global -> shared copy (L2 only, eviction policy from l2_policy),
-// tracked by cp_async_mbar_arrive.
-__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint64_t policy) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-               "l"(policy)
-               : "memory");
-}
-
-// Arrives on `bar` (without raising its expected count) once every cp.async
-// this thread issued before has completed.
-__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 // O[tmem] (+)= A[tmem] . B[smem]
 __device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                            uint32_t accumulate) {

@@ -146,6 +146,28 @@ __device__ __forceinline__ float ld_f32_hint(const float *src, uint64_t policy) 
   return v;
 }
 
+// 16-byte global -> shared copy (L2 only, eviction policy from l2_policy),
+// tracked by cp_async_mbar_arrive.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "l"(policy)
+               : "memory");
+}
+
+// 4-byte global -> shared copy (4-byte aligned), tracked by cp_async_mbar_arrive.
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// Arrives on `bar` (without raising its expected count) once every cp.async
+// this thread issued before has completed.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Waits until every cp.async this thread issued has completed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Contiguous bulk copy global -> shared (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
   asm volatile(
