@@ -59,15 +59,28 @@ constexpr int kMainThreads = 224;
 constexpr int kPrepThreads = 256;
 
 // Work split of the main kernel.  The first part of the flattened (token, key
-// tile) list is cut into one contiguous range per CTA; the rest is a pool of
-// kPoolChunk-tile chunks that CTAs claim one at a time from a global counter
-// once their own work runs low, so CTAs on SMs that stream slower than others
-// end up with fewer tiles and all finish together.
+// tile) list is cut into one contiguous range per CTA; the rest is a pool that
+// CTAs claim one chunk at a time from a global counter once their own work
+// runs low, so CTAs on SMs that stream slower than others end up with fewer
+// tiles and all finish together.  The pool goes out in chunks of kPoolChunk
+// tiles (a chunk that starts a token reloads its queries, so smaller chunks
+// cost more than their finer finish saves); the last few tiles go one by one.
 constexpr int kPoolChunk = 4;
 constexpr int kClaimAhead = 4;  // claim when at most this many queued tiles are left to issue
 constexpr int kSegQ = 4;        // segments queued between the scheduler and the producer warp
 __device__ __forceinline__ int static_tiles(int total) {
-  return total - static_cast<int>((3ll * total) / 8);
+  return total - static_cast<int>(total / 4);
+}
+// Tiles [first, end) of pool chunk c (first >= total: the pool is exhausted).
+struct PoolChunk {
+  int first, end;
+};
+__device__ __forceinline__ PoolChunk pool_chunk(int total, int c) {
+  const int S = static_tiles(total), P = total - S;
+  const int n_big = P / kPoolChunk;
+  if (c < n_big) return {S + c * kPoolChunk, S + (c + 1) * kPoolChunk};
+  const int f = S + n_big * kPoolChunk + (c - n_big);
+  return {f, min(total, f + 1)};
 }
 
 template <int NH, int P>
@@ -718,7 +731,6 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
     // the rest of the own range first, then pool chunks, each claimed only
     // when the producer has at most kClaimAhead queued tiles left to issue.
     pdl_wait();  // the token prefix and the pool counter come from the prep kernel
-    const int S = static_tiles(total);
     // token cursor: token ct holds tiles [cfirst, cnext)
     int ct = -1, cfirst = 0, cnext = 0, cb = 0, cnv = 0;
     if (begin < end) {
@@ -803,9 +815,10 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
       int c = 0;
       if (lane == 0) c = atomicAdd(p.pool, 1);
       c = __shfl_sync(0xffffffffu, c, 0);
-      int i0 = S + c * kPoolChunk;
-      if (c >= (total - S + kPoolChunk - 1) / kPoolChunk) break;  // pool exhausted
-      const int ie = min(total, i0 + kPoolChunk);
+      const PoolChunk pc = pool_chunk(total, c);
+      if (pc.first >= total) break;  // pool exhausted
+      int i0 = pc.first;
+      const int ie = pc.end;
       while (i0 < ie) {
         const int i1 = seek(i0) ? min(ie, cnext) : -1;
         if (i1 < 0 || !push(i0, i1)) {

@@ -130,21 +130,24 @@ topk_radix_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, 
 }
 
 // ---------------------------------------------------------------------------
-// Register-resident variant for rows of up to kRegMax scores: each thread
-// holds a contiguous block of E = ceil(n / 1024) keys.  The keys are first
+// Register-resident variant for rows of up to kRegMax scores: thread i holds
+// positions 4096 q + 4 i + j (j < 4) for q < E / 4, so the row's loads depend
+// only on N_c and go out at once (before the token's visible count is known),
+// and any row length spreads evenly over the threads.  The keys are first
 // reduced to their range (key - min, an order-preserving shift), so the radix
 // digits cover only the L = bit length of (max - min) bits the row actually
-// uses: the first 13-bit pass spreads the row over its bins (plain shared
-// atomics, little contention) and the next pass (two cover a 26-bit range)
-// sees only the keys of the chosen bin.  The output offsets come from a single block scan of packed
-// (greater, equal) counts: the number of picks before a thread is
-// greater_before + min(equal_before, needed).
+// uses: the first pass spreads the row over its bins (plain shared atomics,
+// little contention) and a bin of at most kFinish keys is ranked directly.
+// The picks go into two position bitmaps in shared memory (above the k-th key,
+// equal to it); one block scan over 32-position words then writes them in
+// ascending order, the equal ones lowest position first.
 
 constexpr int kRegMax = 32768;
 constexpr int kDigitBits = 11;                 // radix digit width
 constexpr int kDigitBins = 1 << kDigitBits;
 constexpr int kFinish = 256;                   // a bin this small is ranked directly
 constexpr int kRegE = kRegMax / kTopkThreads;  // 32 keys per thread at most
+constexpr int kChunkSpan = 4 * kTopkThreads;   // positions covered by one chunk q of all threads
 
 // Block-wide exclusive scan of one uint32 per thread; returns the prefix and
 // writes the total to *total.
@@ -230,43 +233,54 @@ __global__ void __launch_bounds__(kTopkThreads)
 topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, int r,
                 const int32_t *__restrict__ q_seq, const int32_t *__restrict__ q_pos, int K,
                 int32_t *__restrict__ idx, uint32_t *status) {
+  static_assert(E % 4 == 0 && E * kTopkThreads <= kRegMax, "keys per thread");
   __shared__ uint32_t hist[kDigitBins];
   __shared__ uint32_t warp_sums[33];
+  __shared__ uint32_t sel_gt[kRegMax / 32], sel_eq[kRegMax / 32];  // pick bitmaps by position
   pdl_trigger();
-  const int t = blockIdx.x, tid = threadIdx.x;
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();  // the scores come from the previous kernel
+  // the row's raw scores: chunk q of this thread is positions 4096 q + 4 tid .. + 3
+  const float *row = scores + static_cast<int64_t>(t) * ld;
+  uint32_t key[E];
+  if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
+#pragma unroll
+    for (int q = 0; q < E / 4; ++q) {
+      const int p0 = kChunkSpan * q + 4 * tid;
+      if (p0 + 3 < N_c) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(row + p0);
+        key[4 * q] = u.x;
+        key[4 * q + 1] = u.y;
+        key[4 * q + 2] = u.z;
+        key[4 * q + 3] = u.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) key[4 * q + j] = p0 + j < N_c ? __float_as_uint(row[p0 + j]) : 0u;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int p0 = kChunkSpan * (e >> 2) + 4 * tid + (e & 3);
+      key[e] = p0 < N_c ? __float_as_uint(row[p0]) : 0u;
+    }
+  }
   Token tk;
   const bool ok = load_token(q_seq, q_pos, t, B, N_c, r, status, tk, tid == 0);
   const int nv = ok ? tk.nv : 0;
-  pdl_wait();  // the scores come from the previous kernel
   int32_t *out = idx + static_cast<int64_t>(t) * K;
   if (nv <= K) {  // every visible position is kept
     for (int i = tid; i < K; i += kTopkThreads) out[i] = i < nv ? i : -1;
     return;
   }
-  const float *row = scores + static_cast<int64_t>(t) * ld;
-  // a multiple of 4 keys per thread (<= E), read as float4 where the row is aligned
-  const int per = ((nv + kTopkThreads - 1) / kTopkThreads + 3) & ~3;
-  const int lo = tid * per;
-  const int cnt = max(0, min(per, nv - lo));
-  uint32_t key[E];
-  if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
+  sel_gt[tid] = 0u;
+  sel_eq[tid] = 0u;
+  // the visible keys of a thread are a prefix of its E: positions grow with e
+  const int rem = nv - 4 * tid;
+  const int cnt = rem <= 0 ? 0 : min(E, 4 * (rem / kChunkSpan) + min(4, rem % kChunkSpan));
+  auto pos_of = [&](int e) { return kChunkSpan * (e >> 2) + 4 * tid + (e & 3); };
 #pragma unroll
-    for (int q = 0; q < E / 4; ++q) {
-      if (4 * q + 3 < cnt) {
-        const float4 v = *reinterpret_cast<const float4 *>(row + lo + 4 * q);
-        key[4 * q] = ordered_key(v.x);
-        key[4 * q + 1] = ordered_key(v.y);
-        key[4 * q + 2] = ordered_key(v.z);
-        key[4 * q + 3] = ordered_key(v.w);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) key[4 * q + j] = 4 * q + j < cnt ? ordered_key(row[lo + 4 * q + j]) : 0u;
-      }
-    }
-  } else {
-#pragma unroll
-    for (int e = 0; e < E; ++e) key[e] = e < cnt ? ordered_key(row[lo + e]) : 0u;
-  }
+  for (int e = 0; e < E; ++e) key[e] = e < cnt ? ordered_key(__uint_as_float(key[e])) : 0u;
 
   // the row's key range: keys become key - min (< 2^L)
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
@@ -279,7 +293,6 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
   kmin = __reduce_min_sync(0xffffffffu, kmin);
   kmax = __reduce_max_sync(0xffffffffu, kmax);
   __shared__ uint32_t wmin[kTopkWarps], wmax[kTopkWarps];
-  const int lane = tid & 31, warp = tid >> 5;
   if (lane == 0) {
     wmin[warp] = kmin;
     wmax[warp] = kmax;
@@ -315,7 +328,7 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
       {
         // the remaining-th largest among the candidates: the value v with
         // #(> v) < remaining <= #(> v) + #(== v); thread i ranks candidate i
-        const uint32_t n = ncand, rem = static_cast<uint32_t>(remaining);
+        const uint32_t n = ncand, rem2 = static_cast<uint32_t>(remaining);
         if (static_cast<uint32_t>(tid) < n) {
           const uint32_t v = cand[tid];
           uint32_t gt = 0, eq = 0;
@@ -324,7 +337,7 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
             gt += u > v;
             eq += u == v;
           }
-          if (gt < rem && rem <= gt + eq) {  // every thread holding that value agrees
+          if (gt < rem2 && rem2 <= gt + eq) {  // every thread holding that value agrees
             fin_thr = v;
             fin_above = gt;
           }
@@ -338,29 +351,30 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
   }
   const uint32_t need_eq = static_cast<uint32_t>(remaining);
 
-  uint32_t gt = 0, eq = 0;
+  // picks into the bitmaps (few: K of nv keys)
 #pragma unroll
-  for (int e = 0; e < E; ++e) {
-    if (e < cnt) {
-      gt += key[e] > thr;
-      eq += key[e] == thr;
+  for (int e = 0; e < E; ++e)
+    if (e < cnt && key[e] >= thr) {
+      const int p0 = pos_of(e);
+      atomicOr(key[e] > thr ? &sel_gt[p0 >> 5] : &sel_eq[p0 >> 5], 1u << (p0 & 31));
     }
-  }
+  __syncthreads();
+  // thread i writes the picks among positions 32 i .. 32 i + 31, in order
+  const uint32_t wg = sel_gt[tid], we = sel_eq[tid];
   uint32_t tot;
-  const uint32_t pre = block_excl_scan((gt << 16) | eq, warp_sums, &tot);
+  const uint32_t pre = block_excl_scan((static_cast<uint32_t>(__popc(wg)) << 16) | __popc(we), warp_sums, &tot);
   const uint32_t gt_before = pre >> 16, eq_before = pre & 0xFFFFu;
-  uint32_t pos = gt_before + min(eq_before, need_eq);
-  uint32_t eq_seen = eq_before;
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    if (e < cnt) {
-      bool take = key[e] > thr;
-      if (key[e] == thr) {
-        take = eq_seen < need_eq;
-        ++eq_seen;
-      }
-      if (take && pos < static_cast<uint32_t>(K)) out[pos++] = lo + e;
-    }
+  uint32_t take = wg, x = we;
+  for (uint32_t k = eq_before; x != 0u && k < need_eq; ++k) {  // equal keys, lowest positions first
+    take |= x & (0u - x);
+    x &= x - 1u;
+  }
+  uint32_t o = gt_before + min(eq_before, need_eq);
+  while (take != 0u) {
+    const int bit = __ffs(take) - 1;
+    if (o < static_cast<uint32_t>(K)) out[o] = 32 * tid + bit;
+    ++o;
+    take &= take - 1u;
   }
 }
 
