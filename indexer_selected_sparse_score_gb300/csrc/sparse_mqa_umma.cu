@@ -305,7 +305,8 @@ __device__ __forceinline__ void exp_store64(const uint32_t (&v)[64], const uint3
 
 __global__ void __launch_bounds__(kThreads, 1)
 sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kwmap,
-                       const __grid_constant__ CUtensorMap kcmap, const AttnUmmaParams p) {
+                       const __grid_constant__ CUtensorMap kcmap, const __grid_constant__ CUtensorMap vwmap,
+                       const __grid_constant__ CUtensorMap vcmap, const AttnUmmaParams p) {
   using L = AttnSmem;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -343,7 +344,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&kfull[i], kKWarps);
       mbar_init(&kempty[i], 1);
-      mbar_init(&vfull[i], 32 * kVWarps);  // one cp.async arrival per V-producer thread
+      mbar_init(&vfull[i], kVWarps);
       mbar_init(&vempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -396,12 +397,16 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
           prefetch_tmap(&qmap);
           prefetch_tmap(&kwmap);
           prefetch_tmap(&kcmap);
+          prefetch_tmap(&vwmap);
+          prefetch_tmap(&vcmap);
         }
         if (!is_k) {
-          // V rows of absent keys are never copied but are multiplied by P = 0:
-          // the ring starts zeroed so that they are finite.  (Absent K rows
-          // only reach logits the softmax masks; unused Q rows only reach
-          // accumulator lanes nobody reads.)
+          // V rows of absent keys are multiplied by P = 0 but must be finite:
+          // an absent key of a copied group holds a present key's row, and a
+          // group with no present key is not copied and keeps what the slot
+          // held before, so the ring starts zeroed.  (Absent K rows only reach
+          // logits the softmax masks; unused Q rows only reach accumulator
+          // lanes nobody reads.)
           for (int i = pw * 32 + lane; i < kStages * 32768 / 16; i += 32 * kVWarps)
             reinterpret_cast<uint4 *>(vs)[i] = make_uint4(0, 0, 0, 0);
           fence_proxy_async();
@@ -494,8 +499,8 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
               mbar_arrive(&mfull[n % kMaskSlots]);
             }
           }
-          if (is_k) {
-            // K rows by TMA gather4.  This warp's share of the tile's 64
+          {
+            // K or V rows by TMA gather4.  This warp's share of the tile's 64
             // copies: copy c = (half, group): half = columns 0-63 / 64-127 of
             // the rows, group g = keys 4g..4g+3 (absent keys of a group read a
             // present key's row; a group with none is not copied)
@@ -512,32 +517,10 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
             if (lane == 0) mbar_expect_tx(&ring_full[s], bytes);
             __syncwarp();
             if (mine) {
-              const CUtensorMap *map = window ? &kwmap : &kcmap;
+              const CUtensorMap *map = is_k ? (window ? &kwmap : &kcmap) : (window ? &vwmap : &vcmap);
               uint8_t *dst = ring + s * 32768 + half * 16384 + 4 * g * 128;
               gather4(dst, map, &ring_full[s], half * 64, gr[0], gr[1], gr[2], gr[3], rpol);
             }
-          } else {
-            // V rows by 16-byte cp.async: a warp instruction copies two rows
-            // (keys 2pr, 2pr+1; 16 lanes x 16 B each) into the same swizzled
-            // layout TMA would write (16-byte chunk c of a 128-byte row r at
-            // chunk c ^ (r & 7)); absent keys are not copied.  Each lane's
-            // arrival on the slot's barrier fires once its copies have landed.
-            const uint8_t *vbase = reinterpret_cast<const uint8_t *>(window ? p.Vw : p.Vc);
-            const int hr = lane >> 4, ch = lane & 15;
-            uint8_t *slot = ring + s * 32768 + (ch >> 3) * 16384;
-            for (int pr = pw; pr < kTile / 2; pr += kVWarps) {
-              // keys 2pr, 2pr+1 live in lane pr/2 as entries 2(pr&1), 2(pr&1)+1
-              const bool odd = pr & 1;
-              const int a0 = odd ? (valid[2] ? rows[2] : -1) : (valid[0] ? rows[0] : -1);
-              const int a1 = odd ? (valid[3] ? rows[3] : -1) : (valid[1] ? rows[1] : -1);
-              const int r0 = __shfl_sync(0xffffffffu, a0, pr >> 1);
-              const int r1 = __shfl_sync(0xffffffffu, a1, pr >> 1);
-              const int row = hr ? r1 : r0, key = 2 * pr + hr;
-              if (row >= 0)
-                cp_async16(slot + key * 128 + (((ch & 7) ^ (key & 7)) << 4),
-                           vbase + static_cast<int64_t>(row) * (kD * 2) + ch * 16, rpol);
-            }
-            cp_async_mbar_arrive(&ring_full[s]);
           }
           ++issued;
         }
@@ -601,7 +584,6 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
           if (!mbar_wait_warp(&pfull[b], (n / kSBufs) & 1) || !mbar_wait_warp(&vfull[s], (n / kStages) & 1))
             return false;
           if (first) ++tok_pv;
-          fence_proxy_async();  // V arrived through the generic proxy; the MMA reads it through the async one
           tc_fence_after();
           const uint32_t v0 = smem_u32(vs + s * 32768), pb = tmem + 128 * b;
           if (leader) {
@@ -915,10 +897,12 @@ cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &
   p.Vw = static_cast<const __nv_bfloat16 *>(aa.Vw);
   p.Vc = static_cast<const __nv_bfloat16 *>(aa.Vc);
   p.status = status;
-  CUtensorMap qmap, kwmap, kcmap;
+  CUtensorMap qmap, kwmap, kcmap, vwmap, vcmap;
   if (!encode_rows(&qmap, aa.Q, static_cast<uint64_t>(ia.T) * kH, 16) ||
       !encode_rows(&kwmap, aa.Kw, static_cast<uint64_t>(ia.B) * aa.R, 1) ||
-      !encode_rows(&kcmap, aa.Kc, static_cast<uint64_t>(ia.B) * ia.N_c, 1))
+      !encode_rows(&kcmap, aa.Kc, static_cast<uint64_t>(ia.B) * ia.N_c, 1) ||
+      !encode_rows(&vwmap, aa.Vw, static_cast<uint64_t>(ia.B) * aa.R, 1) ||
+      !encode_rows(&vcmap, aa.Vc, static_cast<uint64_t>(ia.B) * ia.N_c, 1))
     return cudaErrorInvalidValue;
   const size_t smem = attn_smem_bytes();
   // the register split above assumes the kernel launches with kLaunchRegs
@@ -941,7 +925,7 @@ cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &
   // whole tokens (at most one CTA per SM), or one cluster pair per token
   const int grid = p.split == 1 ? (ia.T < sms ? ia.T : sms) : 2 * ia.T;
   return launch_ex(false, sparse_mqa_umma_kernel, dim3(grid), dim3(kThreads), smem, stream, p.split, qmap, kwmap, kcmap,
-                    p);
+                    vwmap, vcmap, p);
 }
 
 }  // namespace sa
