@@ -924,7 +924,10 @@ cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &
   const int sms = sm_count();
   // whole tokens (at most one CTA per SM), or one cluster pair per token
   const int grid = p.split == 1 ? (ia.T < sms ? ia.T : sms) : 2 * ia.T;
-  return launch_ex(false, sparse_mqa_umma_kernel, dim3(grid), dim3(kThreads), smem, stream, p.split, qmap, kwmap, kcmap,
+  // a programmatic dependent launch: CTAs that find a free SM set up (barriers,
+  // tensor memory) while the top-k kernel finishes, and wait for it before
+  // reading the indices
+  return launch_ex(true, sparse_mqa_umma_kernel, dim3(grid), dim3(kThreads), smem, stream, p.split, qmap, kwmap, kcmap,
                     vwmap, vcmap, p);
 }
 
