@@ -41,6 +41,10 @@ SMALL = {
     # tensor-core path with tokens that see no compressed row between long ones
     "umma_early": wl.small("umma_early", B=6, T=6, H_I=64, D_I=128, r=4, N_c=700, K=100, H=64,
                            W=32, R=32, w_div=64.0),
+    # many short decode tokens on the tensor-core index path: 0-3 key tiles each, so a
+    # work-pool chunk spans several tokens and each plan thread takes two tokens
+    "umma_many": wl.small("umma_many", B=300, T=300, H_I=64, D_I=128, r=4, N_c=300, K=64, H=64,
+                          pos_lo=0, pos_hi=1199, w_div=64.0),
     # prefill chunk: 96 causal tokens of one sequence, ring of T + W - 1 slots
     "prefill": wl.small("prefill", B=1, T=96, r=4, N_c=160, H_I=64, D_I=128, K=48, H=64, W=16,
                         R=112, q_dtype=wl.FP8_E4M3, q_scale=True, pos_mode="prefill",
@@ -165,6 +169,30 @@ def test_bad_device_indices_are_skipped_and_flagged():
     clean[0, 3] = -1
     clean[1, 0] = -1
     check_attn(g, oracle.sparse_attn(problem(w), clean))
+
+
+def test_bad_sequence_id_tensor_core_path():
+    """A token with an out-of-range sequence id among valid ones on the
+    tensor-core index path: flagged, its row fully masked, every other row
+    as the oracle computes it."""
+    w = wl.generate(wl.small("badseq_umma", B=8, T=8, H_I=64, D_I=128, r=4, N_c=700, K=100, H=64,
+                             pos_lo=900, pos_hi=2799, w_div=64.0), seed=12)
+    bad = 3
+    ref_w = wl.generate(wl.small("badseq_umma", B=8, T=8, H_I=64, D_I=128, r=4, N_c=700, K=100, H=64,
+                                 pos_lo=900, pos_hi=2799, w_div=64.0), seed=12)
+    S, A = oracle.index_scores(problem(ref_w), with_magnitude=True)
+    w.q_seq = w.q_seq.copy()
+    w.q_seq[bad] = 99
+    dp = binding.upload(w)
+    ws = binding.new_workspace(dp)
+    import torch
+    scores = torch.empty((w.T, w.N_c), dtype=torch.float32, device="cuda")
+    binding.sa_indexer_scores(dp.ia, scores, ws)
+    assert binding.sa_check_device_status(ws) == binding.SA_ERR_DEVICE_DATA
+    g = scores.cpu().numpy()
+    assert np.all(np.isneginf(g[bad]))
+    keep = [t for t in range(w.T) if t != bad]
+    check_scores(g[keep], S[keep], A[keep])
 
 
 def test_bad_sequence_id_is_flagged():
