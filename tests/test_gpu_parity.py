@@ -45,6 +45,12 @@ SMALL = {
     # work-pool chunk spans several tokens and each plan thread takes two tokens
     "umma_many": wl.small("umma_many", B=300, T=300, H_I=64, D_I=128, r=4, N_c=300, K=64, H=64,
                           pos_lo=0, pos_hi=1199, w_div=64.0),
+    # tensor-core attention with 9 tiles per token: 64 tokens (cluster pairs, each
+    # merging two parts of 5 and 4 tiles) and 128 tokens with a sink (whole tokens)
+    "pairs_9tiles": wl.small("pairs_9tiles", B=64, T=64, H_I=64, D_I=128, r=4, N_c=1200, K=1024, H=64,
+                             W=128, R=128, pos_lo=4100, pos_hi=4799, w_div=64.0),
+    "whole_9tiles_sink": wl.small("whole_9tiles_sink", B=128, T=128, H_I=64, D_I=128, r=4, N_c=1200, K=1024,
+                                  H=64, W=128, R=128, sink=True, pos_lo=4100, pos_hi=4799, w_div=64.0),
     # prefill chunk: 96 causal tokens of one sequence, ring of T + W - 1 slots
     "prefill": wl.small("prefill", B=1, T=96, r=4, N_c=160, H_I=64, D_I=128, K=48, H=64, W=16,
                         R=112, q_dtype=wl.FP8_E4M3, q_scale=True, pos_mode="prefill",
