@@ -146,8 +146,17 @@ constexpr int kRegMax = 32768;
 constexpr int kDigitBits = 11;                 // radix digit width
 constexpr int kDigitBins = 1 << kDigitBits;
 constexpr int kFinish = 256;                   // a bin this small is ranked directly
-constexpr int kRegE = kRegMax / kTopkThreads;  // 32 keys per thread at most
-constexpr int kChunkSpan = 4 * kTopkThreads;   // positions covered by one chunk q of all threads
+// The register top-k runs with NT threads: 1024 when each SM holds about one
+// row (one row's latency is the step's), 512 when rows outnumber the SMs (two
+// CTAs per SM keep more rows in flight).  Per NT: keys per thread at most,
+// positions one chunk q of all threads covers, bitmap words per thread.
+template <int NT>
+struct RegShape {
+  static constexpr int kWarps = NT / 32;
+  static constexpr int kE = kRegMax / NT;
+  static constexpr int kChunkSpan = 4 * NT;
+  static constexpr int kSelWords = kRegMax / 32 / NT;
+};
 
 // Block-wide exclusive scan of one uint32 per thread; returns the prefix and
 // writes the total to *total.
@@ -162,7 +171,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_s
   if (lane == 31) warp_sums[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    uint32_t w = warp_sums[lane];
+    uint32_t w = lane < static_cast<int>(blockDim.x >> 5) ? warp_sums[lane] : 0u;
     uint32_t wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -183,13 +192,13 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_s
 // that match `prefix` under `mask`, then locate the bin holding the
 // `remaining`-th largest.  Returns the digit; `remaining` becomes the rank
 // within that bin.
-template <int E>
+template <int E, int NT>
 __device__ __forceinline__ uint32_t radix_pass(const uint32_t (&key)[E], int cnt, uint32_t prefix, uint32_t mask,
                                                int shift, int nbins, uint32_t *hist, uint32_t *warp_sums,
                                                int &remaining, uint32_t &in_bin) {
-  constexpr int R = kDigitBins / kTopkThreads;  // ranks (bins) per thread in the scan
+  constexpr int R = kDigitBins / NT;  // ranks (bins) per thread in the scan
   const int tid = threadIdx.x;
-  for (int i = tid; i < nbins; i += kTopkThreads) hist[i] = 0;
+  for (int i = tid; i < nbins; i += NT) hist[i] = 0;
   __syncthreads();
 #pragma unroll
   for (int e = 0; e < E; ++e)
@@ -228,12 +237,14 @@ __device__ __forceinline__ uint32_t radix_pass(const uint32_t (&key)[E], int cnt
   return d;
 }
 
-template <int E>
-__global__ void __launch_bounds__(kTopkThreads)
+template <int E, int NT>
+__global__ void __launch_bounds__(NT)
 topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, int r,
                 const int32_t *__restrict__ q_seq, const int32_t *__restrict__ q_pos, int K,
                 int32_t *__restrict__ idx, uint32_t *status) {
-  static_assert(E % 4 == 0 && E * kTopkThreads <= kRegMax, "keys per thread");
+  static_assert(E % 4 == 0 && E * NT <= kRegMax, "keys per thread");
+  using S = RegShape<NT>;
+  constexpr int kChunkSpan = S::kChunkSpan, kSelWords = S::kSelWords, kRegWarps = S::kWarps;
   __shared__ uint32_t hist[kDigitBins];
   __shared__ uint32_t warp_sums[33];
   __shared__ uint32_t sel_gt[kRegMax / 32], sel_eq[kRegMax / 32];  // pick bitmaps by position
@@ -270,11 +281,14 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
   const int nv = ok ? tk.nv : 0;
   int32_t *out = idx + static_cast<int64_t>(t) * K;
   if (nv <= K) {  // every visible position is kept
-    for (int i = tid; i < K; i += kTopkThreads) out[i] = i < nv ? i : -1;
+    for (int i = tid; i < K; i += NT) out[i] = i < nv ? i : -1;
     return;
   }
-  sel_gt[tid] = 0u;
-  sel_eq[tid] = 0u;
+#pragma unroll
+  for (int w = 0; w < kSelWords; ++w) {
+    sel_gt[kSelWords * tid + w] = 0u;
+    sel_eq[kSelWords * tid + w] = 0u;
+  }
   // the visible keys of a thread are a prefix of its E: positions grow with e
   const int rem = nv - 4 * tid;
   const int cnt = rem <= 0 ? 0 : min(E, 4 * (rem / kChunkSpan) + min(4, rem % kChunkSpan));
@@ -292,14 +306,14 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
     }
   kmin = __reduce_min_sync(0xffffffffu, kmin);
   kmax = __reduce_max_sync(0xffffffffu, kmax);
-  __shared__ uint32_t wmin[kTopkWarps], wmax[kTopkWarps];
+  __shared__ uint32_t wmin[kRegWarps], wmax[kRegWarps];
   if (lane == 0) {
     wmin[warp] = kmin;
     wmax[warp] = kmax;
   }
   __syncthreads();
-  kmin = __reduce_min_sync(0xffffffffu, wmin[lane]);
-  kmax = __reduce_max_sync(0xffffffffu, wmax[lane]);
+  kmin = __reduce_min_sync(0xffffffffu, lane < kRegWarps ? wmin[lane] : 0xFFFFFFFFu);
+  kmax = __reduce_max_sync(0xffffffffu, lane < kRegWarps ? wmax[lane] : 0u);
 #pragma unroll
   for (int e = 0; e < E; ++e) key[e] = e < cnt ? key[e] - kmin : 0u;
   const int L = kmax > kmin ? 32 - __clz(kmax - kmin) : 0;
@@ -313,7 +327,7 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
     const int nb = hi < kDigitBits ? hi : kDigitBits, shift = hi - nb;
     const uint32_t mask = hi >= 32 ? 0u : ~((1u << hi) - 1u);  // bits already fixed
     uint32_t in_bin;
-    const uint32_t d = radix_pass<E>(key, cnt, thr, mask, shift, 1 << nb, hist, warp_sums, remaining, in_bin);
+    const uint32_t d = radix_pass<E, NT>(key, cnt, thr, mask, shift, 1 << nb, hist, warp_sums, remaining, in_bin);
     thr |= d << shift;
     hi = shift;
     if (hi > 0 && in_bin <= static_cast<uint32_t>(kFinish)) {
@@ -359,22 +373,31 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
       atomicOr(key[e] > thr ? &sel_gt[p0 >> 5] : &sel_eq[p0 >> 5], 1u << (p0 & 31));
     }
   __syncthreads();
-  // thread i writes the picks among positions 32 i .. 32 i + 31, in order
-  const uint32_t wg = sel_gt[tid], we = sel_eq[tid];
-  uint32_t tot;
-  const uint32_t pre = block_excl_scan((static_cast<uint32_t>(__popc(wg)) << 16) | __popc(we), warp_sums, &tot);
-  const uint32_t gt_before = pre >> 16, eq_before = pre & 0xFFFFu;
-  uint32_t take = wg, x = we;
-  for (uint32_t k = eq_before; x != 0u && k < need_eq; ++k) {  // equal keys, lowest positions first
-    take |= x & (0u - x);
-    x &= x - 1u;
+  // thread i writes the picks among its kSelWords words of 32 positions, in order
+  uint32_t ng = 0, ne = 0;
+#pragma unroll
+  for (int w = 0; w < kSelWords; ++w) {
+    ng += __popc(sel_gt[kSelWords * tid + w]);
+    ne += __popc(sel_eq[kSelWords * tid + w]);
   }
-  uint32_t o = gt_before + min(eq_before, need_eq);
-  while (take != 0u) {
-    const int bit = __ffs(take) - 1;
-    if (o < static_cast<uint32_t>(K)) out[o] = 32 * tid + bit;
-    ++o;
-    take &= take - 1u;
+  uint32_t tot;
+  const uint32_t pre = block_excl_scan((ng << 16) | ne, warp_sums, &tot);
+  uint32_t eq_seen = pre & 0xFFFFu;  // equal keys at lower positions
+  uint32_t o = (pre >> 16) + min(eq_seen, need_eq);
+#pragma unroll
+  for (int w = 0; w < kSelWords; ++w) {
+    uint32_t take = sel_gt[kSelWords * tid + w], x = sel_eq[kSelWords * tid + w];
+    for (; x != 0u && eq_seen < need_eq; ++eq_seen) {  // equal keys, lowest positions first
+      take |= x & (0u - x);
+      x &= x - 1u;
+    }
+    eq_seen += __popc(x);  // equal keys past the quota
+    while (take != 0u) {
+      const int bit = __ffs(take) - 1;
+      if (o < static_cast<uint32_t>(K)) out[o] = 32 * (kSelWords * tid + w) + bit;
+      ++o;
+      take &= take - 1u;
+    }
   }
 }
 
@@ -384,12 +407,24 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const sa_index_args &ia
                         int32_t *idx, uint32_t *status, cudaStream_t stream) {
   if (ia.T == 0 || K == 0) return cudaSuccess;
   // a row holds at most N_c visible scores
-  auto kern = ia.N_c <= kRegMax / 4   ? topk_reg_kernel<kRegE / 4>
-              : ia.N_c <= kRegMax / 2 ? topk_reg_kernel<kRegE / 2>
-              : ia.N_c <= kRegMax     ? topk_reg_kernel<kRegE>
-                                      : topk_radix_kernel;
-  return launch_ex(false, kern, dim3(ia.T), dim3(kTopkThreads), 0, stream, 1, scores, ld, ia.B, ia.N_c, ia.r, ia.q_seq,
-                    ia.q_pos, K, idx, status);
+  if (ia.N_c > kRegMax)
+    return launch_ex(false, topk_radix_kernel, dim3(ia.T), dim3(kTopkThreads), 0, stream, 1, scores, ld, ia.B, ia.N_c,
+                     ia.r, ia.q_seq, ia.q_pos, K, idx, status);
+  const bool many_rows = ia.T > 2 * sm_count();
+  constexpr int kE = RegShape<1024>::kE;  // 32 keys per thread at most with 1024 threads
+  using Kern = void (*)(const float *, int64_t, int, int, int, const int32_t *, const int32_t *, int, int32_t *,
+                        uint32_t *);
+  Kern kern;
+  if (many_rows)
+    kern = ia.N_c <= kRegMax / 4 ? topk_reg_kernel<kE / 2, 512>
+         : ia.N_c <= kRegMax / 2 ? topk_reg_kernel<kE, 512>
+                                 : topk_reg_kernel<2 * kE, 512>;
+  else
+    kern = ia.N_c <= kRegMax / 4 ? topk_reg_kernel<kE / 4, 1024>
+         : ia.N_c <= kRegMax / 2 ? topk_reg_kernel<kE / 2, 1024>
+                                 : topk_reg_kernel<kE, 1024>;
+  return launch_ex(false, kern, dim3(ia.T), dim3(many_rows ? 512 : 1024), 0, stream, 1, scores, ld, ia.B, ia.N_c, ia.r,
+                   ia.q_seq, ia.q_pos, K, idx, status);
 }
 
 }  // namespace sa
