@@ -86,6 +86,8 @@ def _lib(mutant: int = 0, path: Optional[str] = None):
         lib.orc_index_scores.restype = i32
         lib.orc_topk_row.argtypes = [vp, i32, i32, vp]
         lib.orc_topk_row.restype = i32
+        lib.orc_candidate_blocks.argtypes = [vp, i32, i32, i32, i32, vp]
+        lib.orc_candidate_blocks.restype = i32
         lib.orc_sparse_attn.argtypes = [P, vp, i32, vp, i32, vp]
         lib.orc_sparse_attn.restype = i32
         lib.orc_fused.argtypes = [P, i32, vp, i32, vp, vp]
@@ -206,6 +208,31 @@ def topk(p: Problem, scores: np.ndarray, K: int, rows=None, mutant: int = 0) -> 
     for i, t in enumerate(rr):
         out[i] = topk_row(scores[i], n_vis(int(p.q_pos[t]), p.r, mutant), K, mutant)
     return out
+
+
+def candidate_blocks_row(scores: np.ndarray, nv: int, block_size: int, topk_blocks: int,
+                         mutant: int = 0) -> np.ndarray:
+    """Level one of the two-level top-k ("DeepSeek-V4.1-Flash-NVFP4
+    inference/model.py", select_candidate_blocks) on one score row of N_c
+    positions: a bool per block of ``block_size`` positions, True if kept."""
+    s = np.ascontiguousarray(scores, dtype=np.float64)
+    nb = (s.size + block_size - 1) // block_size
+    keep = np.zeros(max(nb, 1), dtype=np.uint8)
+    if _lib(mutant).orc_candidate_blocks(s.ctypes.data, nv, s.size, block_size, topk_blocks, keep.ctypes.data) < 0:
+        raise ValueError("oracle: invalid candidate-block arguments")
+    return keep[:nb].astype(bool)
+
+
+def candidate_topk_row(scores: np.ndarray, nv: int, K: int, keep: np.ndarray, block_size: int,
+                       mutant: int = 0) -> np.ndarray:
+    """Level two ("DeepSeek-V4.1-Flash-NVFP4 inference/model.py",
+    Indexer.forward in a layer that uses candidates): the row's positions
+    outside the kept blocks are set to -inf, then the same top-k as topk_row
+    (K_eff = min(K, n_vis), ties to the lower position, ascending, -1 padded)."""
+    s = np.array(scores, dtype=np.float64)
+    blocks = np.arange(s.size) // block_size
+    s[~keep[blocks]] = -np.inf
+    return topk_row(s, nv, K, mutant)
 
 
 def sparse_attn(p: Problem, idx: np.ndarray, rows=None, mutant: int = 0) -> np.ndarray:

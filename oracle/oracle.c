@@ -241,6 +241,43 @@ int32_t orc_topk_row(const double *S, int32_t n_vis, int32_t K, int32_t *idx) {
   return k_eff;
 }
 
+/* ---- two-level top-k, level one ------------------------------------------ */
+
+/* "DeepSeek-V4.1-Flash-NVFP4 inference/model.py", select_candidate_blocks (and
+ * Indexer.forward, which calls it in the candidate source layer): positions
+ * [0, N_c) of a score row are cut into blocks of bs, the last one short; a
+ * block's score is the best score of its positions, where positions at or
+ * past n_vis count as -inf (not reachable yet); the block holding the newest
+ * visible position, (n_vis - 1) / bs, is pinned to +inf; the min(topk_blocks,
+ * number of blocks) highest-scoring blocks are taken (ties: the lower block)
+ * and those whose score is -inf are dropped.  keep[b] = 1 for a kept block.
+ * Returns the number of blocks kept, or -1 on bad arguments. */
+int32_t orc_candidate_blocks(const double *S, int32_t n_vis, int32_t N_c, int32_t bs, int32_t topk_blocks,
+                             uint8_t *keep) {
+  if (n_vis < 0 || N_c < 0 || n_vis > N_c || bs < 1 || topk_blocks < 0) return -1;
+  const int32_t nb = (N_c + bs - 1) / bs;
+  scored_pos *blk = (scored_pos *)malloc(sizeof(scored_pos) * (size_t)(nb > 0 ? nb : 1));
+  for (int32_t b = 0; b < nb; ++b) {
+    double m = -INFINITY;
+    for (int32_t s = b * bs; s < (b + 1) * bs && s < N_c; ++s)
+      if (s < n_vis && S[s] > m) m = S[s];
+    blk[b].score = m;
+    blk[b].pos = b;
+    keep[b] = 0;
+  }
+  if (n_vis >= 1) blk[(n_vis - 1) / bs].score = INFINITY;
+  qsort(blk, (size_t)nb, sizeof(scored_pos), by_score_then_pos);
+  const int32_t n = topk_blocks < nb ? topk_blocks : nb;
+  int32_t kept = 0;
+  for (int32_t i = 0; i < n; ++i)
+    if (blk[i].score > -INFINITY) {
+      keep[blk[i].pos] = 1;
+      ++kept;
+    }
+  free(blk);
+  return kept;
+}
+
 /* ---- sparse attention ---------------------------------------------------- */
 
 /* For query token t (sequence b, position p) the key set J is the window rows
