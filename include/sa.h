@@ -139,6 +139,43 @@ SA_API sa_status sa_indexer_scores(const sa_index_args *ia, float *scores, void 
 SA_API sa_status sa_topk(const float *scores, const sa_index_args *ia, int32_t K, int32_t *idx, void *ws,
                   size_t ws_bytes, sa_stream_t stream);
 
+/* Two-level top-k, level one ("DeepSeek-V4.1-Flash-NVFP4 inference/model.py",
+ * select_candidate_blocks, called by Indexer.forward in the layer that is the
+ * candidate source).  Positions [0, N_c) are cut into
+ * nb = ceil(N_c / block_size) blocks, the last one short.  For token t, block
+ * b scores max{ scores[t, s] : s in block b, s < n_vis(t) }, or -inf when it
+ * holds no visible position; the block holding the newest visible position,
+ * (n_vis(t) - 1) / block_size, scores +inf instead.  The min(topk_blocks, nb)
+ * highest-scoring blocks are taken (ties: the lower block wins) and those
+ * scoring -inf are dropped.  A kept block b sets bit b % 32 of cand[t, b / 32];
+ * every other bit of the row, those past nb included, is 0.
+ * scores: [T, N_c] fp32 (only s < n_vis(t) is read; NaN scores give
+ * unspecified picks); cand: [T, sa_candidate_words(N_c, block_size)] uint32,
+ * written in full.  block_size >= 1, topk_blocks >= 0; nb > 32768 returns
+ * SA_ERR_UNSUPPORTED.  The selection is exact on the fp32 values.  The
+ * workspace needs only its 256-byte header (the status word). */
+SA_API sa_status sa_candidate_blocks(const float *scores, const sa_index_args *ia, int32_t block_size,
+                                     int32_t topk_blocks, uint32_t *cand, void *ws, size_t ws_bytes,
+                                     sa_stream_t stream);
+
+/* uint32 words per token row of a candidate block mask:
+ * ceil(ceil(N_c / block_size) / 32); 0 when N_c < 1 or block_size < 1. */
+SA_API int32_t sa_candidate_words(int32_t N_c, int32_t block_size);
+
+/* Two-level top-k, level two (Indexer.forward in a layer that uses the
+ * candidates: its own scores masked to -inf outside the candidate blocks, then
+ * the top-k of sa_topk).  Equals sa_topk on scores with scores[t, s] replaced
+ * by -inf wherever bit (s / block_size) of cand[t] is clear: the K_eff =
+ * min(K, n_vis(t)) picks are the positions of kept blocks by score and, when
+ * fewer than K_eff visible positions lie in kept blocks, then the lowest
+ * visible positions outside them (-inf ties go to the lower position).
+ * cand: [T, sa_candidate_words(N_c, block_size)] uint32, e.g. from
+ * sa_candidate_blocks (of this or another layer's scores).  Other arguments
+ * and the output as for sa_topk. */
+SA_API sa_status sa_topk_candidates(const float *scores, const sa_index_args *ia, int32_t K,
+                                    const uint32_t *cand, int32_t block_size, int32_t *idx, void *ws,
+                                    size_t ws_bytes, sa_stream_t stream);
+
 /* Sparse MQA over the window and the selected compressed rows
  * ("DeepSeek-V4.1-Flash-NVFP4 inference/model.py", Attention.forward and
  * sparse_attn): for token t and head h the keys are the window rows then the

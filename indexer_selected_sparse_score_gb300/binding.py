@@ -58,6 +58,7 @@ class AttnArgs(ctypes.Structure):
 
 
 EXPORTED = ("sa_workspace_size", "sa_workspace_init", "sa_indexer_scores", "sa_topk",
+            "sa_candidate_blocks", "sa_candidate_words", "sa_topk_candidates",
             "sa_sparse_attn", "sa_fused_decode", "sa_fused_decode_staged",
             "sa_fused_decode_launch_count", "sa_check_device_status", "sa_status_string",
             "sa_last_error_detail")
@@ -81,6 +82,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.sa_workspace_init.argtypes = [vp, sz, vp]
     lib.sa_indexer_scores.argtypes = [IA, vp, vp, sz, vp]
     lib.sa_topk.argtypes = [vp, IA, i32, vp, vp, sz, vp]
+    lib.sa_candidate_blocks.argtypes = [vp, IA, i32, i32, vp, vp, sz, vp]
+    lib.sa_candidate_words.argtypes = [i32, i32]
+    lib.sa_candidate_words.restype = i32
+    lib.sa_topk_candidates.argtypes = [vp, IA, i32, vp, i32, vp, vp, sz, vp]
     lib.sa_sparse_attn.argtypes = [IA, AA, vp, i32, vp, vp, sz, vp]
     lib.sa_fused_decode.argtypes = [IA, AA, i32, vp, vp, vp, sz, vp]
     lib.sa_fused_decode_staged.argtypes = [IA, AA, i32, vp, vp, vp, sz, vp, ctypes.POINTER(vp)]
@@ -92,7 +97,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.sa_status_string.argtypes = [i32]
     lib.sa_status_string.restype = ctypes.c_char_p
     lib.sa_last_error_detail.restype = ctypes.c_char_p
-    for name in ("sa_workspace_init", "sa_indexer_scores", "sa_topk", "sa_sparse_attn",
+    for name in ("sa_workspace_init", "sa_indexer_scores", "sa_topk", "sa_candidate_blocks",
+                 "sa_topk_candidates", "sa_sparse_attn",
                  "sa_fused_decode", "sa_fused_decode_staged", "sa_check_device_status"):
         getattr(lib, name).restype = i32
     if path == LIB:
@@ -144,6 +150,26 @@ def sa_indexer_scores(ia: IndexArgs, scores, ws, stream=None) -> None:
 def sa_topk(scores, ia: IndexArgs, K: int, idx, ws, stream=None) -> None:
     p, n = _ws(ws)
     _check(load().sa_topk(_p(scores), ctypes.byref(ia), K, _p(idx), p, n, _s(stream)))
+
+
+def sa_candidate_words(N_c: int, block_size: int) -> int:
+    return int(load().sa_candidate_words(N_c, block_size))
+
+
+def sa_candidate_blocks(scores, ia: IndexArgs, block_size: int, topk_blocks: int, cand, ws,
+                        stream=None) -> None:
+    """Level one of the two-level top-k: ``cand`` ([T, sa_candidate_words] int32
+    or uint32) receives one bit per kept block."""
+    p, n = _ws(ws)
+    _check(load().sa_candidate_blocks(_p(scores), ctypes.byref(ia), block_size, topk_blocks, _p(cand), p, n,
+                                      _s(stream)))
+
+
+def sa_topk_candidates(scores, ia: IndexArgs, K: int, cand, block_size: int, idx, ws, stream=None) -> None:
+    """Level two: sa_topk with the scores outside the kept blocks of ``cand`` at -inf."""
+    p, n = _ws(ws)
+    _check(load().sa_topk_candidates(_p(scores), ctypes.byref(ia), K, _p(cand), block_size, _p(idx), p, n,
+                                     _s(stream)))
 
 
 def sa_sparse_attn(ia: IndexArgs, aa: AttnArgs, idx, K: int, out, ws, stream=None) -> None:

@@ -9,6 +9,11 @@
 // lower position and the output comes out ascending.  Rows of up to 32768
 // scores are held in registers (topk_reg_kernel); longer rows stream from
 // global memory in four 8-bit passes (topk_radix_kernel).
+//
+// Level two of the two-level top-k ("DeepSeek-V4.1-Flash-NVFP4
+// inference/model.py", Indexer.forward in a layer that uses candidates) is the
+// same selection on scores masked to -inf outside the kept candidate blocks:
+// given a block mask, both kernels apply it as they read the row.
 #include "common.cuh"
 #include "internal.h"
 
@@ -24,10 +29,20 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
+// Whether position s lies in a kept block of a candidate mask row (bit b of
+// word b / 32 for block b = s / bs).
+__device__ __forceinline__ bool cand_kept(const uint32_t *crow, int s, int bs) {
+  const int b = s / bs;
+  return (crow[b >> 5] >> (b & 31)) & 1u;
+}
+
+constexpr uint32_t kNegInfBits = 0xFF800000u;  // fp32 -inf
+
 __global__ void __launch_bounds__(kTopkThreads)
 topk_radix_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, int r,
                   const int32_t *__restrict__ q_seq, const int32_t *__restrict__ q_pos, int K,
-                  int32_t *__restrict__ idx, uint32_t *status) {
+                  int32_t *__restrict__ idx, uint32_t *status, const uint32_t *__restrict__ cmask,
+                  int cand_words, int bs) {
   __shared__ uint32_t hist[256];
   __shared__ uint32_t warp_eq[kTopkWarps], warp_take[kTopkWarps];
   __shared__ uint32_t sh_digit, sh_above;
@@ -47,13 +62,17 @@ topk_radix_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, 
   }
 
   const float *row = scores + static_cast<int64_t>(t) * ld;
+  const uint32_t *crow = cmask ? cmask + static_cast<int64_t>(t) * cand_words : nullptr;
+  auto key_at = [&](int s) {
+    return crow && !cand_kept(crow, s, bs) ? ordered_key(__uint_as_float(kNegInfBits)) : ordered_key(row[s]);
+  };
   uint32_t prefix = 0, mask = 0;
   int remaining = K;  // picks still to make among keys matching `prefix`
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
     for (int s = tid; s < nv; s += kTopkThreads) {
-      const uint32_t u = ordered_key(row[s]);
+      const uint32_t u = key_at(s);
       if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
     }
     __syncthreads();
@@ -98,7 +117,7 @@ topk_radix_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, 
   uint32_t sel_base = 0, eq_base = 0;
   for (int base = 0; base < nv; base += kTopkThreads) {
     const int s = base + tid;
-    const uint32_t u = s < nv ? ordered_key(row[s]) : 0u;
+    const uint32_t u = s < nv ? key_at(s) : 0u;
     const bool gt = s < nv && u > thr;
     const bool eq = s < nv && u == thr;
     const uint32_t bal_eq = __ballot_sync(0xffffffffu, eq);
@@ -237,11 +256,12 @@ __device__ __forceinline__ uint32_t radix_pass(const uint32_t (&key)[E], int cnt
   return d;
 }
 
-template <int E, int NT>
+template <int E, int NT, bool kCand>
 __global__ void __launch_bounds__(NT)
 topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, int r,
                 const int32_t *__restrict__ q_seq, const int32_t *__restrict__ q_pos, int K,
-                int32_t *__restrict__ idx, uint32_t *status) {
+                int32_t *__restrict__ idx, uint32_t *status, const uint32_t *__restrict__ cmask,
+                int cand_words, int bs) {
   static_assert(E % 4 == 0 && E * NT <= kRegMax, "keys per thread");
   using S = RegShape<NT>;
   constexpr int kChunkSpan = S::kChunkSpan, kSelWords = S::kSelWords, kRegWarps = S::kWarps;
@@ -274,6 +294,27 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
     for (int e = 0; e < E; ++e) {
       const int p0 = kChunkSpan * (e >> 2) + 4 * tid + (e & 3);
       key[e] = p0 < N_c ? __float_as_uint(row[p0]) : 0u;
+    }
+  }
+  if constexpr (kCand) {
+    // positions outside the kept blocks score -inf; a chunk of four
+    // positions inside one block needs one look-up
+    const uint32_t *crow = cmask + static_cast<int64_t>(t) * cand_words;
+#pragma unroll
+    for (int q = 0; q < E / 4; ++q) {
+      const int p0 = kChunkSpan * q + 4 * tid;
+      if (p0 < N_c) {
+        if (p0 + 3 < N_c && p0 / bs == (p0 + 3) / bs) {
+          if (!cand_kept(crow, p0, bs)) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) key[4 * q + j] = kNegInfBits;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (p0 + j < N_c && !cand_kept(crow, p0 + j, bs)) key[4 * q + j] = kNegInfBits;
+        }
+      }
     }
   }
   Token tk;
@@ -401,30 +442,35 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
   }
 }
 
+using RegKern = void (*)(const float *, int64_t, int, int, int, const int32_t *, const int32_t *, int, int32_t *,
+                         uint32_t *, const uint32_t *, int, int);
+
+template <bool kCand>
+RegKern pick_reg_kernel(int N_c, bool many_rows) {
+  constexpr int kE = RegShape<1024>::kE;  // 32 keys per thread at most with 1024 threads
+  if (many_rows)
+    return N_c <= kRegMax / 4 ? topk_reg_kernel<kE / 2, 512, kCand>
+         : N_c <= kRegMax / 2 ? topk_reg_kernel<kE, 512, kCand>
+                              : topk_reg_kernel<2 * kE, 512, kCand>;
+  return N_c <= kRegMax / 4 ? topk_reg_kernel<kE / 4, 1024, kCand>
+       : N_c <= kRegMax / 2 ? topk_reg_kernel<kE / 2, 1024, kCand>
+                            : topk_reg_kernel<kE, 1024, kCand>;
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const float *scores, int64_t ld, const sa_index_args &ia, int K,
-                        int32_t *idx, uint32_t *status, cudaStream_t stream) {
+                        int32_t *idx, uint32_t *status, cudaStream_t stream, const uint32_t *cand,
+                        int cand_words, int block_size) {
   if (ia.T == 0 || K == 0) return cudaSuccess;
   // a row holds at most N_c visible scores
   if (ia.N_c > kRegMax)
     return launch_ex(false, topk_radix_kernel, dim3(ia.T), dim3(kTopkThreads), 0, stream, 1, scores, ld, ia.B, ia.N_c,
-                     ia.r, ia.q_seq, ia.q_pos, K, idx, status);
+                     ia.r, ia.q_seq, ia.q_pos, K, idx, status, cand, cand_words, block_size);
   const bool many_rows = ia.T > 2 * sm_count();
-  constexpr int kE = RegShape<1024>::kE;  // 32 keys per thread at most with 1024 threads
-  using Kern = void (*)(const float *, int64_t, int, int, int, const int32_t *, const int32_t *, int, int32_t *,
-                        uint32_t *);
-  Kern kern;
-  if (many_rows)
-    kern = ia.N_c <= kRegMax / 4 ? topk_reg_kernel<kE / 2, 512>
-         : ia.N_c <= kRegMax / 2 ? topk_reg_kernel<kE, 512>
-                                 : topk_reg_kernel<2 * kE, 512>;
-  else
-    kern = ia.N_c <= kRegMax / 4 ? topk_reg_kernel<kE / 4, 1024>
-         : ia.N_c <= kRegMax / 2 ? topk_reg_kernel<kE / 2, 1024>
-                                 : topk_reg_kernel<kE, 1024>;
+  const RegKern kern = cand ? pick_reg_kernel<true>(ia.N_c, many_rows) : pick_reg_kernel<false>(ia.N_c, many_rows);
   return launch_ex(false, kern, dim3(ia.T), dim3(many_rows ? 512 : 1024), 0, stream, 1, scores, ld, ia.B, ia.N_c, ia.r,
-                   ia.q_seq, ia.q_pos, K, idx, status);
+                   ia.q_seq, ia.q_pos, K, idx, status, cand, cand_words, block_size);
 }
 
 }  // namespace sa

@@ -46,8 +46,18 @@ cudaError_t launch_idx_score_umma(const sa_index_args &ia, float *scores, int64_
                                   bool write_masked, void *scratch, uint32_t *status,
                                   cudaStream_t stream);
 
+// Per-query top-k.  With `cand` ([T, cand_words] block mask, blocks of
+// block_size positions) the positions outside kept blocks count as -inf.
 cudaError_t launch_topk(const float *scores, int64_t ld, const sa_index_args &ia, int K,
-                        int32_t *idx, uint32_t *status, cudaStream_t stream);
+                        int32_t *idx, uint32_t *status, cudaStream_t stream,
+                        const uint32_t *cand = nullptr, int cand_words = 0, int block_size = 1);
+
+// Level one of the two-level top-k: per token, the block mask of the kept
+// candidate blocks ([T, candidate_words(N_c, block_size)] uint32).
+int candidate_words(int N_c, int block_size);
+constexpr int kMaxCandidateBlocks = 32768;
+cudaError_t launch_candidate_blocks(const float *scores, int64_t ld, const sa_index_args &ia, int block_size,
+                                   int topk_blocks, uint32_t *cand, uint32_t *status, cudaStream_t stream);
 
 // Attention + combine.  The tensor-core kernel (64 heads of dim 128) uses
 // `attn_scratch` (attn_umma_scratch bytes); the CUDA-core kernel uses the

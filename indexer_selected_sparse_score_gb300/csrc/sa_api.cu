@@ -201,6 +201,47 @@ sa_status sa_topk(const float *scores, const sa_index_args *ia, int32_t K, int32
   return e == cudaSuccess ? SA_OK : cuda_fail(e, "top-k launch");
 }
 
+int32_t sa_candidate_words(int32_t N_c, int32_t block_size) {
+  if (N_c < 1 || block_size < 1) return 0;
+  return sa::candidate_words(N_c, block_size);
+}
+
+sa_status sa_candidate_blocks(const float *scores, const sa_index_args *ia, int32_t block_size,
+                              int32_t topk_blocks, uint32_t *cand, void *ws, size_t ws_bytes, sa_stream_t stream) {
+  if (sa_status s = check_index(ia, false)) return s;
+  if (block_size < 1 || topk_blocks < 0)
+    return fail(SA_ERR_INVALID_ARG, "need block_size >= 1 and topk_blocks >= 0 (got %d, %d)", block_size,
+                topk_blocks);
+  const int64_t nb = (static_cast<int64_t>(ia->N_c) + block_size - 1) / block_size;
+  if (nb > sa::kMaxCandidateBlocks)
+    return fail(SA_ERR_UNSUPPORTED, "%lld candidate blocks per row (at most %d)", static_cast<long long>(nb),
+                sa::kMaxCandidateBlocks);
+  if (ia->T > 0 && (!scores || !cand))
+    return fail(SA_ERR_INVALID_ARG, "scores and cand must be device pointers");
+  if (!aligned4(scores) || !aligned4(cand))
+    return fail(SA_ERR_INVALID_ARG, "scores and cand must be 4-byte aligned");
+  if (sa_status s = check_ws(ws, ws_bytes, 256)) return s;
+  cudaError_t e = sa::launch_candidate_blocks(scores, ia->N_c, *ia, block_size, topk_blocks, cand,
+                                              at<uint32_t>(ws, 0), reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SA_OK : cuda_fail(e, "candidate block launch");
+}
+
+sa_status sa_topk_candidates(const float *scores, const sa_index_args *ia, int32_t K, const uint32_t *cand,
+                             int32_t block_size, int32_t *idx, void *ws, size_t ws_bytes, sa_stream_t stream) {
+  if (sa_status s = check_index(ia, false)) return s;
+  if (K < 0) return fail(SA_ERR_INVALID_ARG, "K must be >= 0 (got %d)", K);
+  if (block_size < 1) return fail(SA_ERR_INVALID_ARG, "block_size must be >= 1 (got %d)", block_size);
+  if (ia->T > 0 && K > 0 && (!scores || !idx || !cand))
+    return fail(SA_ERR_INVALID_ARG, "scores, cand and idx must be device pointers");
+  if (!aligned4(scores) || !aligned4(idx) || !aligned4(cand))
+    return fail(SA_ERR_INVALID_ARG, "scores, cand and idx must be 4-byte aligned");
+  if (sa_status s = check_ws(ws, ws_bytes, 256)) return s;
+  cudaError_t e = sa::launch_topk(scores, ia->N_c, *ia, K, idx, at<uint32_t>(ws, 0),
+                                  reinterpret_cast<cudaStream_t>(stream), cand,
+                                  sa::candidate_words(ia->N_c, block_size), block_size);
+  return e == cudaSuccess ? SA_OK : cuda_fail(e, "top-k launch");
+}
+
 sa_status sa_sparse_attn(const sa_index_args *ia, const sa_attn_args *aa, const int32_t *idx,
                          int32_t K, void *out, void *ws, size_t ws_bytes, sa_stream_t stream) {
   if (sa_status s = check_index(ia, false)) return s;

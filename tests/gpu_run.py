@@ -67,3 +67,66 @@ def run_fused(w, K=None, with_idx=True, dp=None):
 @functools.lru_cache(maxsize=2)
 def config_workload(name: str):
     return wl.generate(wl.CONFIGS[name])
+
+
+def _token_args(B: int, N_c: int, r: int, q_seq: np.ndarray, q_pos: np.ndarray):
+    """IndexArgs carrying only the token arrays (all the top-k entry points
+    read), plus the device tensors that must outlive the call."""
+    d_seq = torch.from_numpy(np.ascontiguousarray(q_seq, dtype=np.int32)).cuda()
+    d_pos = torch.from_numpy(np.ascontiguousarray(q_pos, dtype=np.int32)).cuda()
+    ia = binding.IndexArgs(B, len(q_seq), 16, 64, N_c, r, d_seq.data_ptr(), d_pos.data_ptr(), None, 0, None,
+                           None, None, 0, None)
+    return ia, (d_seq, d_pos)
+
+
+def _small_ws() -> torch.Tensor:
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    binding.sa_workspace_init(ws)
+    return ws
+
+
+def run_candidates(scores: np.ndarray, q_seq, q_pos, B: int, r: int, block_size: int, topk_blocks: int):
+    """Level one on the GPU: the [T, words] uint32 block mask."""
+    ensure_built()
+    T, N_c = scores.shape
+    ia, keep = _token_args(B, N_c, r, q_seq, q_pos)
+    ws = _small_ws()
+    s = torch.from_numpy(np.ascontiguousarray(scores, dtype=np.float32)).cuda()
+    words = binding.sa_candidate_words(N_c, block_size)
+    cand = torch.full((T, words), -1, dtype=torch.int32, device="cuda")  # every bit set beforehand
+    binding.sa_candidate_blocks(s, ia, block_size, topk_blocks, cand, ws)
+    assert binding.sa_check_device_status(ws) == binding.SA_OK
+    del keep
+    return cand.cpu().numpy().view(np.uint32)
+
+
+def run_topk_candidates(scores: np.ndarray, q_seq, q_pos, B: int, r: int, K: int, cand: np.ndarray,
+                        block_size: int):
+    """Level two on the GPU: [T, K] indices."""
+    ensure_built()
+    T, N_c = scores.shape
+    ia, keep = _token_args(B, N_c, r, q_seq, q_pos)
+    ws = _small_ws()
+    s = torch.from_numpy(np.ascontiguousarray(scores, dtype=np.float32)).cuda()
+    c = torch.from_numpy(np.ascontiguousarray(cand).view(np.int32)).cuda()
+    idx = torch.full((T, max(K, 1)), -7, dtype=torch.int32, device="cuda")
+    binding.sa_topk_candidates(s, ia, K, c, block_size, idx, ws)
+    assert binding.sa_check_device_status(ws) == binding.SA_OK
+    del keep
+    return idx[:, :K].cpu().numpy()
+
+
+def unpack_blocks(cand: np.ndarray, nb: int) -> np.ndarray:
+    """[T, words] uint32 block masks -> [T, nb] bool; bits past nb must be 0."""
+    bits = np.unpackbits(np.ascontiguousarray(cand).view(np.uint8), axis=1, bitorder="little")
+    assert not bits[:, nb:].any(), "bits past the last block are set"
+    return bits[:, :nb].astype(bool)
+
+
+def pack_blocks(keep: np.ndarray) -> np.ndarray:
+    """[T, nb] bool -> [T, ceil(nb / 32)] uint32 (bit b % 32 of word b / 32)."""
+    T, nb = keep.shape
+    words = (nb + 31) // 32
+    padded = np.zeros((T, words * 32), dtype=np.uint8)
+    padded[:, :nb] = keep
+    return np.packbits(padded, axis=1, bitorder="little").view(np.uint32)

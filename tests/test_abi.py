@@ -101,3 +101,55 @@ def test_product_package_never_reaches_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
                 assert "oracle.h" not in text and "liboracle" not in text, f
+
+
+def test_candidate_words(lib):
+    assert lib.sa_candidate_words(32768, 8) == 128
+    assert lib.sa_candidate_words(20, 4) == 1
+    assert lib.sa_candidate_words(257, 8) == 2       # 33 blocks
+    assert lib.sa_candidate_words(100, 1000) == 1    # one short block
+    assert lib.sa_candidate_words(0, 8) == 0
+    assert lib.sa_candidate_words(100, 0) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(block_size=0), binding.SA_ERR_INVALID_ARG),
+    (dict(topk_blocks=-1), binding.SA_ERR_INVALID_ARG),
+    (dict(ia=_ia(N_c=32768 * 8 + 1)), binding.SA_ERR_UNSUPPORTED),   # 32769 blocks
+    (dict(scores=None), binding.SA_ERR_INVALID_ARG),
+    (dict(cand=None), binding.SA_ERR_INVALID_ARG),
+    (dict(cand=258), binding.SA_ERR_INVALID_ARG),                     # misaligned
+    (dict(ws=None), binding.SA_ERR_WORKSPACE),
+    (dict(ws_bytes=64), binding.SA_ERR_WORKSPACE),
+    (dict(ia=_ia(r=0)), binding.SA_ERR_INVALID_ARG),
+])
+def test_candidate_blocks_rejects_bad_arguments(lib, kw, status):
+    a = dict(scores=256, ia=_ia(), block_size=8, topk_blocks=4, cand=256, ws=256, ws_bytes=256)
+    a.update(kw)
+    st = lib.sa_candidate_blocks(a["scores"], ctypes.byref(a["ia"]), a["block_size"], a["topk_blocks"],
+                                 a["cand"], a["ws"], a["ws_bytes"], None)
+    assert st == status
+    assert lib.sa_last_error_detail()
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(block_size=0), binding.SA_ERR_INVALID_ARG),
+    (dict(K=-1), binding.SA_ERR_INVALID_ARG),
+    (dict(cand=None), binding.SA_ERR_INVALID_ARG),
+    (dict(idx=None), binding.SA_ERR_INVALID_ARG),
+    (dict(cand=258), binding.SA_ERR_INVALID_ARG),
+    (dict(ws=None), binding.SA_ERR_WORKSPACE),
+])
+def test_topk_candidates_rejects_bad_arguments(lib, kw, status):
+    a = dict(scores=256, ia=_ia(), K=8, cand=256, block_size=8, idx=256, ws=256, ws_bytes=256)
+    a.update(kw)
+    st = lib.sa_topk_candidates(a["scores"], ctypes.byref(a["ia"]), a["K"], a["cand"], a["block_size"],
+                                a["idx"], a["ws"], a["ws_bytes"], None)
+    assert st == status
+
+
+def test_candidate_calls_with_no_tokens_enqueue_nothing(lib):
+    # T = 0: valid arguments and nothing to do (no device is touched)
+    ia = _ia(T=0, q_seq=None, q_pos=None)
+    assert lib.sa_candidate_blocks(None, ctypes.byref(ia), 8, 4, None, 256, 256, None) == binding.SA_OK
+    assert lib.sa_topk_candidates(None, ctypes.byref(ia), 8, None, 8, None, 256, 256, None) == binding.SA_OK

@@ -85,3 +85,26 @@ def test_config_attn_on_oracle_indices(cfg):
     assert binding.sa_check_device_status(ws) == binding.SA_OK
     g = out.float().cpu().numpy().astype(np.float64)
     check_attn(g[rows], oracle.sparse_attn(problem(w), full, rows=rows))
+
+
+@pytest.mark.parametrize("topk_blocks", [2048, 256])
+def test_config_two_level_topk(cfg, topk_blocks):
+    """Two-level top-k at full size on the indexer's own scores: level one
+    (blocks of 8, as the pages' configuration) exact on every token, level two
+    exact on the sampled tokens.  With 256 blocks the selection is active on
+    every config; with 2048 it is on c4's longer rows."""
+    from gpu_run import run_candidates, run_topk_candidates, unpack_blocks
+    name, w, rows, S, A = cfg
+    g = run_scores(w)
+    bs = 8
+    nb = (w.N_c + bs - 1) // bs
+    cand = run_candidates(g, w.q_seq, w.q_pos, w.B, w.r, bs, topk_blocks)
+    got = unpack_blocks(cand, nb)
+    idx = run_topk_candidates(g, w.q_seq, w.q_pos, w.B, w.r, w.K, cand, bs)
+    for t in range(w.T):
+        nv = n_vis(int(w.q_pos[t]), w.r)
+        keep = oracle.candidate_blocks_row(g[t].astype(np.float64), nv, bs, topk_blocks)
+        assert np.array_equal(got[t], keep), (name, t)
+        if t in rows:
+            ref = oracle.candidate_topk_row(g[t].astype(np.float64), nv, w.K, keep, bs)
+            assert idx[t].tolist() == ref.tolist(), (name, t)
