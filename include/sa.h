@@ -151,8 +151,8 @@ SA_API sa_status sa_topk(const float *scores, const sa_index_args *ia, int32_t K
  * every other bit of the row, those past nb included, is 0.
  * scores: [T, N_c] fp32 (only s < n_vis(t) is read; NaN scores give
  * unspecified picks); cand: [T, sa_candidate_words(N_c, block_size)] uint32,
- * written in full.  block_size >= 1, topk_blocks >= 0; nb > 32768 returns
- * SA_ERR_UNSUPPORTED.  The selection is exact on the fp32 values.  The
+ * written in full.  block_size >= 1, topk_blocks >= 0; nb > 32768 or
+ * N_c > 2^30 returns SA_ERR_UNSUPPORTED.  The selection is exact on the fp32 values.  The
  * workspace needs only its 256-byte header (the status word). */
 SA_API sa_status sa_candidate_blocks(const float *scores, const sa_index_args *ia, int32_t block_size,
                                      int32_t topk_blocks, uint32_t *cand, void *ws, size_t ws_bytes,
@@ -170,8 +170,9 @@ SA_API int32_t sa_candidate_words(int32_t N_c, int32_t block_size);
  * fewer than K_eff visible positions lie in kept blocks, then the lowest
  * visible positions outside them (-inf ties go to the lower position).
  * cand: [T, sa_candidate_words(N_c, block_size)] uint32, e.g. from
- * sa_candidate_blocks (of this or another layer's scores).  Other arguments
- * and the output as for sa_topk. */
+ * sa_candidate_blocks (of this or another layer's scores).  N_c > 2^30
+ * returns SA_ERR_UNSUPPORTED.  Other arguments and the output as for
+ * sa_topk. */
 SA_API sa_status sa_topk_candidates(const float *scores, const sa_index_args *ia, int32_t K,
                                     const uint32_t *cand, int32_t block_size, int32_t *idx, void *ws,
                                     size_t ws_bytes, sa_stream_t stream);

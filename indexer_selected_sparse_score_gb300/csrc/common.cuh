@@ -83,4 +83,25 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Division by a runtime divisor d >= 1 with one 64-bit multiply: with
+// l = ceil(log2 d) and m = ceil(2^(32+l) / d) (at most 2^33), floor(n / d) =
+// (n m) >> (32 + l) for 0 <= n < 2^32 (the round-up multiplier of Granlund and
+// Montgomery, "Division by Invariant Integers using Multiplication", 1994:
+// m d - 2^(32+l) < d <= 2^l bounds the error below one).  fast_div takes
+// n < 2^31, where n m fits in 64 bits.
+struct FastDiv {
+  uint64_t m;
+  int s;
+};
+
+__host__ __device__ inline FastDiv make_fastdiv(uint32_t d) {
+  int l = 0;
+  while ((uint64_t{1} << l) < d) ++l;
+  return FastDiv{((uint64_t{1} << (32 + l)) + d - 1) / d, 32 + l};
+}
+
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, FastDiv f) {
+  return static_cast<uint32_t>((static_cast<uint64_t>(n) * f.m) >> f.s);
+}
+
 }  // namespace sa

@@ -24,10 +24,9 @@
 namespace sa {
 namespace {
 
-constexpr int kCandThreads = 512;
-constexpr int kCandWarps = kCandThreads / 32;
 constexpr uint32_t kKeyNegInf = 0x007FFFFFu;  // ordered_key(-inf)
 constexpr uint32_t kKeyPosInf = 0xFF800000u;  // ordered_key(+inf)
+constexpr int kLoadBatch = 8;                 // float4 loads each thread has in flight
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t m;
@@ -35,62 +34,81 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
-__global__ void __launch_bounds__(kCandThreads)
-candidate_blocks_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, int r,
-                        const int32_t *__restrict__ q_seq, const int32_t *__restrict__ q_pos, int bs,
-                        int topk_blocks, int words, uint32_t *__restrict__ cand, uint32_t *status) {
-  extern __shared__ uint32_t bkey[];  // [32 * words] block keys; 0 is never taken
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t warp_sums[kCandWarps];
-  __shared__ uint32_t sh_digit, sh_above;
-  pdl_trigger();
-  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nb = static_cast<int>((static_cast<int64_t>(N_c) + bs - 1) / bs);
-  for (int i = tid; i < 32 * words; i += kCandThreads) bkey[i] = 0u;
-  pdl_wait();  // the scores come from the previous kernel
-  Token tk;
-  const bool ok = load_token(q_seq, q_pos, t, B, N_c, r, status, tk, tid == 0);
-  const int nv = ok ? tk.nv : 0;
-  __syncthreads();
-
-  // block maxima over the visible positions
-  const float *row = scores + static_cast<int64_t>(t) * ld;
+// Block keys into shared memory: bkey[b] = the largest key of a visible
+// position of block b above ordered_key(-inf), else 0; the newest block gets
+// ordered_key(+inf).
+template <int NT>
+__device__ __forceinline__ void block_maxima(const float *__restrict__ row, int nv, FastDiv dbs, int bs,
+                                             uint32_t *bkey) {
+  const int tid = threadIdx.x;
   const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
-  for (int p0 = 4 * tid; p0 < nv; p0 += 4 * kCandThreads) {
-    uint32_t k[4];
-    if (vec && p0 + 3 < nv) {
-      const float4 f = *reinterpret_cast<const float4 *>(row + p0);
-      k[0] = ordered_key(f.x);
-      k[1] = ordered_key(f.y);
-      k[2] = ordered_key(f.z);
-      k[3] = ordered_key(f.w);
-    } else {
+  const float ninf = __uint_as_float(0xFF800000u);
+  for (int base = 0; base < nv; base += 4 * NT * kLoadBatch) {
+    float4 f[kLoadBatch];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) k[j] = p0 + j < nv ? ordered_key(row[p0 + j]) : 0u;
+    for (int i = 0; i < kLoadBatch; ++i) {  // every load of the batch goes out before any is used
+      const int p0 = base + 4 * (NT * i + tid);
+      if (vec && p0 + 3 < nv) {
+        f[i] = *reinterpret_cast<const float4 *>(row + p0);
+      } else {
+        f[i].x = p0 < nv ? row[p0] : ninf;
+        f[i].y = p0 + 1 < nv ? row[p0 + 1] : ninf;
+        f[i].z = p0 + 2 < nv ? row[p0 + 2] : ninf;
+        f[i].w = p0 + 3 < nv ? row[p0 + 3] : ninf;
+      }
     }
-    const int b0 = p0 / bs;
-    if ((p0 + 3) / bs == b0) {
-      const uint32_t m = max(max(k[0], k[1]), max(k[2], k[3]));
-      if (m > kKeyNegInf) atomicMax(&bkey[b0], m);
-    } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (k[j] > kKeyNegInf) atomicMax(&bkey[(p0 + j) / bs], k[j]);
+    for (int i = 0; i < kLoadBatch; ++i) {
+      const int p0 = base + 4 * (NT * i + tid);
+      if (p0 < nv) {
+        const uint32_t k[4] = {ordered_key(f[i].x), ordered_key(f[i].y), ordered_key(f[i].z), ordered_key(f[i].w)};
+        const uint32_t b0 = fast_div(p0, dbs);
+        if (fast_div(p0 + 3, dbs) == b0) {  // the four positions share a block
+          const uint32_t m = max(max(k[0], k[1]), max(k[2], k[3]));
+          if (m > kKeyNegInf) atomicMax(&bkey[b0], m);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (k[j] > kKeyNegInf) atomicMax(&bkey[fast_div(p0 + j, dbs)], k[j]);
+        }
+      }
     }
   }
   __syncthreads();
   if (tid == 0 && nv >= 1) bkey[(nv - 1) / bs] = kKeyPosInf;  // the newest block is pinned
   __syncthreads();
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT)
+candidate_blocks_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, int r,
+                        const int32_t *__restrict__ q_seq, const int32_t *__restrict__ q_pos, int bs, FastDiv dbs,
+                        int topk_blocks, int words, uint32_t *__restrict__ cand, uint32_t *status) {
+  constexpr int kWarps = NT / 32;
+  extern __shared__ uint32_t bkey[];  // [32 * words] block keys; 0 is never taken
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t warp_sums[kWarps];
+  __shared__ uint32_t sh_digit, sh_above;
+  pdl_trigger();
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nb = static_cast<int>((static_cast<int64_t>(N_c) + bs - 1) / bs);
+  for (int i = tid; i < 32 * words; i += NT) bkey[i] = 0u;
+  pdl_wait();  // the scores come from the previous kernel
+  Token tk;
+  const bool ok = load_token(q_seq, q_pos, t, B, N_c, r, status, tk, tid == 0);
+  const int nv = ok ? tk.nv : 0;
+  __syncthreads();
+  block_maxima<NT>(scores + static_cast<int64_t>(t) * ld, nv, dbs, bs, bkey);
 
   // reachable blocks (key > 0)
   uint32_t c = 0;
-  for (int b = tid; b < nb; b += kCandThreads) c += bkey[b] != 0u;
+  for (int b = tid; b < nb; b += NT) c += bkey[b] != 0u;
   c = __reduce_add_sync(0xffffffffu, c);
   if (lane == 0) warp_sums[warp] = c;
   __syncthreads();
   uint32_t reach = 0;
 #pragma unroll
-  for (int i = 0; i < kCandWarps; ++i) reach += warp_sums[i];
+  for (int i = 0; i < kWarps; ++i) reach += warp_sums[i];
   __syncthreads();
 
   // keep = key > thr, or key == thr among the first need_eq such blocks
@@ -101,11 +119,16 @@ candidate_blocks_kernel(const float *__restrict__ scores, int64_t ld, int B, int
   } else if (reach > n) {
     uint32_t prefix = 0u, mask = 0u, remaining = n;
     for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += kCandThreads) hist[i] = 0u;
+      for (int i = tid; i < 256; i += NT) hist[i] = 0u;
       __syncthreads();
-      for (int b = tid; b < nb; b += kCandThreads) {
-        const uint32_t u = bkey[b];
-        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+      // block maxima crowd into few bins: lanes with the same bin add once
+      for (int base = 0; base < nb; base += NT) {
+        const int b = base + tid;
+        const uint32_t u = b < nb ? bkey[b] : 0u;
+        const bool act = b < nb && (u & mask) == prefix;
+        const uint32_t bin = act ? (u >> shift) & 255u : 256u;
+        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+        if (act && __ffs(peers) - 1 == lane) atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(peers)));
       }
       __syncthreads();
       if (warp == 0) {
@@ -148,7 +171,7 @@ candidate_blocks_kernel(const float *__restrict__ scores, int64_t ld, int B, int
   }
 
   // warp w writes words [w * per, (w + 1) * per) in order
-  const int per = (words + kCandWarps - 1) / kCandWarps;
+  const int per = (words + kWarps - 1) / kWarps;
   const int w_begin = min(words, warp * per), w_end = min(words, w_begin + per);
   uint32_t eq_cnt = 0;
   for (int w = w_begin; w < w_end; ++w) eq_cnt += __popc(__ballot_sync(0xffffffffu, bkey[32 * w + lane] == thr));
@@ -178,14 +201,17 @@ int candidate_words(int N_c, int block_size) {
 cudaError_t launch_candidate_blocks(const float *scores, int64_t ld, const sa_index_args &ia, int block_size,
                                    int topk_blocks, uint32_t *cand, uint32_t *status, cudaStream_t stream) {
   if (ia.T == 0) return cudaSuccess;
-  static bool attr_done[64] = {};
-  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(candidate_blocks_kernel),
-                                sizeof(uint32_t) * kMaxCandidateBlocks, attr_done);
+  // 1024 threads while each SM holds about one row, 512 when rows outnumber the SMs
+  const bool many_rows = ia.T > 2 * sm_count();
+  const auto kern = many_rows ? candidate_blocks_kernel<512> : candidate_blocks_kernel<1024>;
+  static bool attr_done[2][64] = {};
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), sizeof(uint32_t) * kMaxCandidateBlocks,
+                                attr_done[many_rows ? 0 : 1]);
   if (e != cudaSuccess) return e;
   const int words = candidate_words(ia.N_c, block_size);
-  return launch_ex(false, candidate_blocks_kernel, dim3(ia.T), dim3(kCandThreads), sizeof(uint32_t) * 32 * words,
-                   stream, 1, scores, ld, ia.B, ia.N_c, ia.r, ia.q_seq, ia.q_pos, block_size, topk_blocks, words,
-                   cand, status);
+  return launch_ex(false, kern, dim3(ia.T), dim3(many_rows ? 512 : 1024), sizeof(uint32_t) * 32 * words, stream, 1,
+                   scores, ld, ia.B, ia.N_c, ia.r, ia.q_seq, ia.q_pos, block_size,
+                   make_fastdiv(static_cast<uint32_t>(block_size)), topk_blocks, words, cand, status);
 }
 
 }  // namespace sa

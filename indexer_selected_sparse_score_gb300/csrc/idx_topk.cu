@@ -29,10 +29,10 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
-// Whether position s lies in a kept block of a candidate mask row (bit b of
-// word b / 32 for block b = s / bs).
-__device__ __forceinline__ bool cand_kept(const uint32_t *crow, int s, int bs) {
-  const int b = s / bs;
+// Whether position s lies in a kept block of a candidate mask row (bit b % 32
+// of word b / 32 for block b = s / block_size).
+__device__ __forceinline__ bool cand_kept(const uint32_t *crow, int s, FastDiv dbs) {
+  const uint32_t b = fast_div(static_cast<uint32_t>(s), dbs);
   return (crow[b >> 5] >> (b & 31)) & 1u;
 }
 
@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(kTopkThreads)
 topk_radix_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, int r,
                   const int32_t *__restrict__ q_seq, const int32_t *__restrict__ q_pos, int K,
                   int32_t *__restrict__ idx, uint32_t *status, const uint32_t *__restrict__ cmask,
-                  int cand_words, int bs) {
+                  int cand_words, FastDiv dbs) {
   __shared__ uint32_t hist[256];
   __shared__ uint32_t warp_eq[kTopkWarps], warp_take[kTopkWarps];
   __shared__ uint32_t sh_digit, sh_above;
@@ -64,7 +64,7 @@ topk_radix_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, 
   const float *row = scores + static_cast<int64_t>(t) * ld;
   const uint32_t *crow = cmask ? cmask + static_cast<int64_t>(t) * cand_words : nullptr;
   auto key_at = [&](int s) {
-    return crow && !cand_kept(crow, s, bs) ? ordered_key(__uint_as_float(kNegInfBits)) : ordered_key(row[s]);
+    return crow && !cand_kept(crow, s, dbs) ? ordered_key(__uint_as_float(kNegInfBits)) : ordered_key(row[s]);
   };
   uint32_t prefix = 0, mask = 0;
   int remaining = K;  // picks still to make among keys matching `prefix`
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(NT)
 topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, int r,
                 const int32_t *__restrict__ q_seq, const int32_t *__restrict__ q_pos, int K,
                 int32_t *__restrict__ idx, uint32_t *status, const uint32_t *__restrict__ cmask,
-                int cand_words, int bs) {
+                int cand_words, FastDiv dbs) {
   static_assert(E % 4 == 0 && E * NT <= kRegMax, "keys per thread");
   using S = RegShape<NT>;
   constexpr int kChunkSpan = S::kChunkSpan, kSelWords = S::kSelWords, kRegWarps = S::kWarps;
@@ -304,15 +304,15 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
     for (int q = 0; q < E / 4; ++q) {
       const int p0 = kChunkSpan * q + 4 * tid;
       if (p0 < N_c) {
-        if (p0 + 3 < N_c && p0 / bs == (p0 + 3) / bs) {
-          if (!cand_kept(crow, p0, bs)) {
+        if (p0 + 3 < N_c && fast_div(p0, dbs) == fast_div(p0 + 3, dbs)) {
+          if (!cand_kept(crow, p0, dbs)) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) key[4 * q + j] = kNegInfBits;
           }
         } else {
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            if (p0 + j < N_c && !cand_kept(crow, p0 + j, bs)) key[4 * q + j] = kNegInfBits;
+            if (p0 + j < N_c && !cand_kept(crow, p0 + j, dbs)) key[4 * q + j] = kNegInfBits;
         }
       }
     }
@@ -443,7 +443,7 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
 }
 
 using RegKern = void (*)(const float *, int64_t, int, int, int, const int32_t *, const int32_t *, int, int32_t *,
-                         uint32_t *, const uint32_t *, int, int);
+                         uint32_t *, const uint32_t *, int, FastDiv);
 
 template <bool kCand>
 RegKern pick_reg_kernel(int N_c, bool many_rows) {
@@ -463,14 +463,15 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const sa_index_args &ia
                         int32_t *idx, uint32_t *status, cudaStream_t stream, const uint32_t *cand,
                         int cand_words, int block_size) {
   if (ia.T == 0 || K == 0) return cudaSuccess;
+  const FastDiv dbs = make_fastdiv(static_cast<uint32_t>(block_size));
   // a row holds at most N_c visible scores
   if (ia.N_c > kRegMax)
     return launch_ex(false, topk_radix_kernel, dim3(ia.T), dim3(kTopkThreads), 0, stream, 1, scores, ld, ia.B, ia.N_c,
-                     ia.r, ia.q_seq, ia.q_pos, K, idx, status, cand, cand_words, block_size);
+                     ia.r, ia.q_seq, ia.q_pos, K, idx, status, cand, cand_words, dbs);
   const bool many_rows = ia.T > 2 * sm_count();
   const RegKern kern = cand ? pick_reg_kernel<true>(ia.N_c, many_rows) : pick_reg_kernel<false>(ia.N_c, many_rows);
   return launch_ex(false, kern, dim3(ia.T), dim3(many_rows ? 512 : 1024), 0, stream, 1, scores, ld, ia.B, ia.N_c, ia.r,
-                   ia.q_seq, ia.q_pos, K, idx, status, cand, cand_words, block_size);
+                   ia.q_seq, ia.q_pos, K, idx, status, cand, cand_words, dbs);
 }
 
 }  // namespace sa

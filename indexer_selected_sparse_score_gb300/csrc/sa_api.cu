@@ -212,6 +212,7 @@ sa_status sa_candidate_blocks(const float *scores, const sa_index_args *ia, int3
   if (block_size < 1 || topk_blocks < 0)
     return fail(SA_ERR_INVALID_ARG, "need block_size >= 1 and topk_blocks >= 0 (got %d, %d)", block_size,
                 topk_blocks);
+  if (ia->N_c > (1 << 30)) return fail(SA_ERR_UNSUPPORTED, "N_c %d above 2^30", ia->N_c);
   const int64_t nb = (static_cast<int64_t>(ia->N_c) + block_size - 1) / block_size;
   if (nb > sa::kMaxCandidateBlocks)
     return fail(SA_ERR_UNSUPPORTED, "%lld candidate blocks per row (at most %d)", static_cast<long long>(nb),
@@ -231,6 +232,7 @@ sa_status sa_topk_candidates(const float *scores, const sa_index_args *ia, int32
   if (sa_status s = check_index(ia, false)) return s;
   if (K < 0) return fail(SA_ERR_INVALID_ARG, "K must be >= 0 (got %d)", K);
   if (block_size < 1) return fail(SA_ERR_INVALID_ARG, "block_size must be >= 1 (got %d)", block_size);
+  if (ia->N_c > (1 << 30)) return fail(SA_ERR_UNSUPPORTED, "N_c %d above 2^30", ia->N_c);
   if (ia->T > 0 && K > 0 && (!scores || !idx || !cand))
     return fail(SA_ERR_INVALID_ARG, "scores, cand and idx must be device pointers");
   if (!aligned4(scores) || !aligned4(idx) || !aligned4(cand))

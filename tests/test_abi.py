@@ -116,6 +116,7 @@ def test_candidate_words(lib):
     (dict(block_size=0), binding.SA_ERR_INVALID_ARG),
     (dict(topk_blocks=-1), binding.SA_ERR_INVALID_ARG),
     (dict(ia=_ia(N_c=32768 * 8 + 1)), binding.SA_ERR_UNSUPPORTED),   # 32769 blocks
+    (dict(ia=_ia(N_c=(1 << 30) + 1), block_size=1 << 20), binding.SA_ERR_UNSUPPORTED),  # row too long
     (dict(scores=None), binding.SA_ERR_INVALID_ARG),
     (dict(cand=None), binding.SA_ERR_INVALID_ARG),
     (dict(cand=258), binding.SA_ERR_INVALID_ARG),                     # misaligned
@@ -139,6 +140,7 @@ def test_candidate_blocks_rejects_bad_arguments(lib, kw, status):
     (dict(idx=None), binding.SA_ERR_INVALID_ARG),
     (dict(cand=258), binding.SA_ERR_INVALID_ARG),
     (dict(ws=None), binding.SA_ERR_WORKSPACE),
+    (dict(ia=_ia(N_c=(1 << 30) + 1)), binding.SA_ERR_UNSUPPORTED),
 ])
 def test_topk_candidates_rejects_bad_arguments(lib, kw, status):
     a = dict(scores=256, ia=_ia(), K=8, cand=256, block_size=8, idx=256, ws=256, ws_bytes=256)
