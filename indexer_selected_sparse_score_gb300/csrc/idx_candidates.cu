@@ -27,6 +27,9 @@ namespace {
 constexpr uint32_t kKeyNegInf = 0x007FFFFFu;  // ordered_key(-inf)
 constexpr uint32_t kKeyPosInf = 0xFF800000u;  // ordered_key(+inf)
 constexpr int kLoadBatch = 8;                 // float4 loads each thread has in flight
+constexpr int kDigitBits = 11;                // radix digit over the finite keys' range
+constexpr int kBins = 1 << kDigitBits;
+constexpr int kFinish = 256;                  // a bin this small is ranked directly
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t m;
@@ -35,14 +38,16 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 }
 
 // Block keys into shared memory: bkey[b] = the largest key of a visible
-// position of block b above ordered_key(-inf), else 0; the newest block gets
-// ordered_key(+inf).
+// position of block b above ordered_key(-inf), else 0.  Returns how many
+// blocks this thread turned from 0 to a positive key (each reachable block
+// is counted once, by the atomic that saw 0).
 template <int NT>
-__device__ __forceinline__ void block_maxima(const float *__restrict__ row, int nv, FastDiv dbs, int bs,
-                                             uint32_t *bkey) {
+__device__ __forceinline__ uint32_t block_maxima(const float *__restrict__ row, int nv, FastDiv dbs,
+                                                 uint32_t *bkey) {
   const int tid = threadIdx.x;
   const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
   const float ninf = __uint_as_float(0xFF800000u);
+  uint32_t first = 0;
   for (int base = 0; base < nv; base += 4 * NT * kLoadBatch) {
     float4 f[kLoadBatch];
 #pragma unroll
@@ -65,18 +70,196 @@ __device__ __forceinline__ void block_maxima(const float *__restrict__ row, int 
         const uint32_t b0 = fast_div(p0, dbs);
         if (fast_div(p0 + 3, dbs) == b0) {  // the four positions share a block
           const uint32_t m = max(max(k[0], k[1]), max(k[2], k[3]));
-          if (m > kKeyNegInf) atomicMax(&bkey[b0], m);
+          if (m > kKeyNegInf) first += atomicMax(&bkey[b0], m) == 0u;
         } else {
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            if (k[j] > kKeyNegInf) atomicMax(&bkey[fast_div(p0 + j, dbs)], k[j]);
+            if (k[j] > kKeyNegInf) first += atomicMax(&bkey[fast_div(p0 + j, dbs)], k[j]) == 0u;
         }
       }
     }
   }
+  return first;
+}
+
+// Block-wide exclusive scan of one value per thread (warp_sums: kWarps + 1
+// words); returns the prefix and the total.
+template <int NT>
+__device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t *warp_sums, uint32_t &total) {
+  constexpr int kWarps = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
   __syncthreads();
-  if (tid == 0 && nv >= 1) bkey[(nv - 1) / bs] = kKeyPosInf;  // the newest block is pinned
+  if (warp == 0) {
+    const uint32_t w = lane < kWarps ? warp_sums[lane] : 0u;
+    uint32_t wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    if (lane < kWarps) warp_sums[lane] = wi - w;
+    if (lane == 31) warp_sums[kWarps] = wi;
+  }
   __syncthreads();
+  const uint32_t r = warp_sums[warp] + incl - v;
+  total = warp_sums[kWarps];
+  __syncthreads();
+  return r;
+}
+
+struct SelectSmem {
+  uint32_t hist[kBins];
+  uint32_t warp_sums[33];
+  uint32_t red[3][32];
+  uint32_t fin[kFinish];
+  uint32_t nfin, digit, above, in_bin, fin_v, fin_gt, fin_eq;
+};
+
+// The n-th largest key among bkey[0, nb) -- ties to the lower block -- as
+// (thr, need_eq): a block is taken if its key is above thr, or equal to it
+// and among the first need_eq such blocks.  Needs n >= 1 and more than n
+// positive keys.  The keys at or above ordered_key(+inf) (the pinned block)
+// are set aside, and the rest are selected on their own range.
+template <int NT>
+__device__ void select_threshold(const uint32_t *bkey, int nb, uint32_t n, SelectSmem &sm, uint32_t &thr,
+                                 uint32_t &need_eq) {
+  constexpr int kWarps = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // keys at or above +inf, and the range of the finite positive keys
+  uint32_t ctop = 0, kmin = 0xFFFFFFFFu, kmax = 0u, cfin = 0;
+  for (int b = tid; b < nb; b += NT) {
+    const uint32_t u = bkey[b];
+    if (u >= kKeyPosInf) {
+      ++ctop;
+    } else if (u != 0u) {
+      ++cfin;
+      kmin = min(kmin, u);
+      kmax = max(kmax, u);
+    }
+  }
+  ctop = __reduce_add_sync(0xffffffffu, ctop);
+  cfin = __reduce_add_sync(0xffffffffu, cfin);
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0) {
+    sm.red[0][warp] = ctop;
+    sm.red[1][warp] = kmin;
+    sm.red[2][warp] = kmax;
+    sm.warp_sums[warp] = cfin;
+  }
+  __syncthreads();
+  ctop = 0;
+  cfin = 0;
+  kmin = 0xFFFFFFFFu;
+  kmax = 0u;
+#pragma unroll
+  for (int i = 0; i < kWarps; ++i) {
+    ctop += sm.red[0][i];
+    cfin += sm.warp_sums[i];
+    kmin = min(kmin, sm.red[1][i]);
+    kmax = max(kmax, sm.red[2][i]);
+  }
+  __syncthreads();
+
+  if (ctop >= n) {
+    // at least n blocks at +inf (the pinned block ties with +inf scores): take
+    // the lowest-numbered n of them
+    thr = kKeyPosInf;
+    need_eq = n;
+    return;
+  }
+  uint32_t remaining = n - ctop;  // picks among the cfin finite keys (cfin > remaining)
+  const int L = kmax > kmin ? 32 - __clz(kmax - kmin) : 0;
+  uint32_t rel = 0u, eq_total = cfin;  // keys equal to the threshold, when known
+  for (int hi = L; hi > 0;) {
+    const int nbits = hi < kDigitBits ? hi : kDigitBits, shift = hi - nbits;
+    const uint32_t nbins = 1u << nbits;
+    const uint32_t fixed = hi >= 32 ? 0u : ~((1u << hi) - 1u);  // bits already chosen
+    for (int i = tid; i < kBins; i += NT) sm.hist[i] = 0u;
+    __syncthreads();
+    for (int base = 0; base < nb; base += NT) {
+      const int b = base + tid;
+      const uint32_t u = b < nb ? bkey[b] : 0u;
+      const bool act = u != 0u && u < kKeyPosInf && ((u - kmin) & fixed) == rel;
+      const uint32_t bin = act ? ((u - kmin) >> shift) & (nbins - 1u) : 0xFFFFFFFFu;
+      const uint32_t peers = __match_any_sync(0xffffffffu, bin);  // equal bins add once
+      if (act && __ffs(peers) - 1 == lane) atomicAdd(&sm.hist[bin], static_cast<uint32_t>(__popc(peers)));
+    }
+    __syncthreads();
+    // bins in descending order: thread t owns ranks R t .. R t + R - 1 (bin nbins - 1 - rank)
+    constexpr int R = (kBins + NT - 1) / NT;
+    uint32_t c[R], sum = 0;
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+      const int rk = R * tid + k;
+      c[k] = rk < static_cast<int>(nbins) ? sm.hist[nbins - 1 - rk] : 0u;
+      sum += c[k];
+    }
+    uint32_t total;
+    const uint32_t before = block_scan<NT>(sum, sm.warp_sums, total);
+    if (before < remaining && remaining <= before + sum) {
+      uint32_t run = before;
+#pragma unroll
+      for (int k = 0; k < R; ++k) {
+        if (run < remaining && remaining <= run + c[k]) {
+          sm.digit = nbins - 1 - (R * tid + k);
+          sm.above = run;
+          sm.in_bin = c[k];
+        }
+        run += c[k];
+      }
+    }
+    __syncthreads();
+    remaining -= sm.above;
+    rel |= sm.digit << shift;
+    eq_total = sm.in_bin;
+    hi = shift;
+    __syncthreads();
+    if (hi > 0 && eq_total <= static_cast<uint32_t>(kFinish)) {
+      // rank the bin's keys directly: the value v with #(> v) < remaining <= #(>= v)
+      if (tid == 0) sm.nfin = 0;
+      __syncthreads();
+      const uint32_t fx = ~((1u << hi) - 1u);
+      for (int b = tid; b < nb; b += NT) {
+        const uint32_t u = bkey[b];
+        if (u != 0u && u < kKeyPosInf && ((u - kmin) & fx) == rel) sm.fin[atomicAdd(&sm.nfin, 1u)] = u - kmin;
+      }
+      __syncthreads();
+      const uint32_t m = sm.nfin;
+      if (static_cast<uint32_t>(tid) < m) {
+        const uint32_t v = sm.fin[tid];
+        uint32_t gt = 0, eq = 0;
+        for (uint32_t j = 0; j < m; ++j) {
+          gt += sm.fin[j] > v;
+          eq += sm.fin[j] == v;
+        }
+        if (gt < remaining && remaining <= gt + eq) {  // every thread holding v agrees
+          sm.fin_v = v;
+          sm.fin_gt = gt;
+          sm.fin_eq = eq;
+        }
+      }
+      __syncthreads();
+      rel = sm.fin_v;
+      remaining -= sm.fin_gt;
+      eq_total = sm.fin_eq;
+      __syncthreads();
+      break;
+    }
+  }
+  thr = kmin + rel;
+  need_eq = remaining;
+  if (need_eq == eq_total) {  // every key equal to thr is taken: keep = key >= thr
+    thr -= 1u;                // thr >= kmin > 0
+    need_eq = 0u;
+  }
 }
 
 template <int NT>
@@ -86,9 +269,8 @@ candidate_blocks_kernel(const float *__restrict__ scores, int64_t ld, int B, int
                         int topk_blocks, int words, uint32_t *__restrict__ cand, uint32_t *status) {
   constexpr int kWarps = NT / 32;
   extern __shared__ uint32_t bkey[];  // [32 * words] block keys; 0 is never taken
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t warp_sums[kWarps];
-  __shared__ uint32_t sh_digit, sh_above;
+  __shared__ SelectSmem sm;
+  __shared__ uint32_t pin_new;
   pdl_trigger();
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nb = static_cast<int>((static_cast<int64_t>(N_c) + bs - 1) / bs);
@@ -98,87 +280,45 @@ candidate_blocks_kernel(const float *__restrict__ scores, int64_t ld, int B, int
   const bool ok = load_token(q_seq, q_pos, t, B, N_c, r, status, tk, tid == 0);
   const int nv = ok ? tk.nv : 0;
   __syncthreads();
-  block_maxima<NT>(scores + static_cast<int64_t>(t) * ld, nv, dbs, bs, bkey);
 
-  // reachable blocks (key > 0)
-  uint32_t c = 0;
-  for (int b = tid; b < nb; b += NT) c += bkey[b] != 0u;
-  c = __reduce_add_sync(0xffffffffu, c);
-  if (lane == 0) warp_sums[warp] = c;
+  // block maxima and the reachable count
+  uint32_t first = block_maxima<NT>(scores + static_cast<int64_t>(t) * ld, nv, dbs, bkey);
+  first = __reduce_add_sync(0xffffffffu, first);
+  if (lane == 0) sm.warp_sums[warp] = first;
   __syncthreads();
-  uint32_t reach = 0;
+  if (tid == 0) {
+    pin_new = 0u;
+    if (nv >= 1) {  // the newest block is pinned
+      const int b = (nv - 1) / bs;
+      pin_new = bkey[b] == 0u;
+      bkey[b] = kKeyPosInf;
+    }
+  }
+  __syncthreads();
+  uint32_t reach = pin_new;
 #pragma unroll
-  for (int i = 0; i < kWarps; ++i) reach += warp_sums[i];
+  for (int i = 0; i < kWarps; ++i) reach += sm.warp_sums[i];
   __syncthreads();
 
   // keep = key > thr, or key == thr among the first need_eq such blocks
   const uint32_t n = static_cast<uint32_t>(min(topk_blocks, nb));
   uint32_t thr = 0u, need_eq = 0u;  // every reachable block
-  if (n == 0u) {
+  if (n == 0u)
     thr = 0xFFFFFFFFu;  // no block
-  } else if (reach > n) {
-    uint32_t prefix = 0u, mask = 0u, remaining = n;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += NT) hist[i] = 0u;
-      __syncthreads();
-      // block maxima crowd into few bins: lanes with the same bin add once
-      for (int base = 0; base < nb; base += NT) {
-        const int b = base + tid;
-        const uint32_t u = b < nb ? bkey[b] : 0u;
-        const bool act = b < nb && (u & mask) == prefix;
-        const uint32_t bin = act ? (u >> shift) & 255u : 256u;
-        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-        if (act && __ffs(peers) - 1 == lane) atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(peers)));
-      }
-      __syncthreads();
-      if (warp == 0) {
-        // lane l owns bins 8l .. 8l+7: find the bin where the count of keys
-        // at or above it first reaches `remaining`, from the top bin down
-        uint32_t cb[8], local = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          cb[j] = hist[8 * lane + j];
-          local += cb[j];
-        }
-        uint32_t sfx = local;  // keys in this lane's bins and above
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t v = __shfl_down_sync(0xffffffffu, sfx, o);
-          if (lane + o < 32) sfx += v;
-        }
-        const uint32_t above = sfx - local;
-        if (above < remaining && remaining <= sfx) {
-          uint32_t acc = above;
-#pragma unroll
-          for (int j = 7; j >= 0; --j) {
-            if (acc + cb[j] >= remaining) {
-              sh_digit = 8 * lane + j;
-              sh_above = acc;
-              break;
-            }
-            acc += cb[j];
-          }
-        }
-      }
-      __syncthreads();
-      remaining -= sh_above;
-      prefix |= sh_digit << shift;
-      mask |= 255u << shift;
-      __syncthreads();
-    }
-    thr = prefix;
-    need_eq = remaining;
-  }
+  else if (reach > n)
+    select_threshold<NT>(bkey, nb, n, sm, thr, need_eq);
 
   // warp w writes words [w * per, (w + 1) * per) in order
   const int per = (words + kWarps - 1) / kWarps;
   const int w_begin = min(words, warp * per), w_end = min(words, w_begin + per);
-  uint32_t eq_cnt = 0;
-  for (int w = w_begin; w < w_end; ++w) eq_cnt += __popc(__ballot_sync(0xffffffffu, bkey[32 * w + lane] == thr));
-  if (lane == 0) warp_sums[warp] = eq_cnt;
-  __syncthreads();
   uint32_t eq_seen = 0;  // blocks equal to thr in lower words
-  for (int i = 0; i < warp; ++i) eq_seen += warp_sums[i];
+  if (need_eq > 0u) {
+    uint32_t eq_cnt = 0;
+    for (int w = w_begin; w < w_end; ++w) eq_cnt += __popc(__ballot_sync(0xffffffffu, bkey[32 * w + lane] == thr));
+    if (lane == 0) sm.warp_sums[warp] = eq_cnt;
+    __syncthreads();
+    for (int i = 0; i < warp; ++i) eq_seen += sm.warp_sums[i];
+  }
   uint32_t *out = cand + static_cast<int64_t>(t) * words;
   for (int w = w_begin; w < w_end; ++w) {
     const uint32_t u = bkey[32 * w + lane];
