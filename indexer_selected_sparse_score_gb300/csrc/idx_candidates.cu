@@ -11,13 +11,16 @@
 // block (bit b % 32 of word b / 32).
 //
 // One CTA per token.  The block maxima are built in shared memory as
-// order-preserving keys by shared atomicMax over the visible positions only (a
-// chunk of four positions inside one block folds to one atomic); a block that
-// is -inf or unreachable keeps key 0, which is never taken.  When more blocks
-// are reachable than are taken, an exact radix select (four 8-bit passes over
-// the block keys) finds the key of the last block taken; each warp then writes
-// its run of 32-block words in order, taking the blocks equal to that key
-// lowest-numbered first until the quota is met.
+// order-preserving keys by shared atomicMax over the visible positions only
+// (the row's loads go out in batches before any is used; a chunk of four
+// positions inside one block folds to one atomic, and the atomic that finds a
+// block at 0 counts it as reachable).  A block that is -inf or unreachable
+// keeps key 0, which is never taken.  When more blocks are reachable than are
+// taken, an exact radix select over the positive keys (11-bit digits from the
+// top, then a direct ranking of a bin of at most 256 keys) finds the key of
+// the last block taken; each warp then writes its run of 32-block words in
+// order, taking the blocks equal to that key lowest-numbered first until the
+// quota is met.
 #include "common.cuh"
 #include "internal.h"
 
@@ -117,80 +120,37 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t *warp_sums, 
 struct SelectSmem {
   uint32_t hist[kBins];
   uint32_t warp_sums[33];
-  uint32_t red[3][32];
   uint32_t fin[kFinish];
   uint32_t nfin, digit, above, in_bin, fin_v, fin_gt, fin_eq;
 };
 
-// The n-th largest key among bkey[0, nb) -- ties to the lower block -- as
-// (thr, need_eq): a block is taken if its key is above thr, or equal to it
-// and among the first need_eq such blocks.  Needs n >= 1 and more than n
-// positive keys.  The keys at or above ordered_key(+inf) (the pinned block)
-// are set aside, and the rest are selected on their own range.
+// Sum over the warps of one value per warp held in part[0, kWarps): each warp
+// reads all of them with one lane-parallel load (count = the first `count`).
+template <int NT>
+__device__ __forceinline__ uint32_t sum_parts(const uint32_t *part, int count) {
+  const int lane = threadIdx.x & 31;
+  return __reduce_add_sync(0xffffffffu, lane < count ? part[lane] : 0u);
+}
+
+// The n-th largest positive key among bkey[0, nb) -- ties to the lower block
+// -- as (thr, need_eq): a block is taken if its key is above thr, or equal to
+// it and among the first need_eq such blocks.  Needs n >= 1 and more than n
+// positive keys.  Radix select from the top, 11 bits at a time; once the
+// chosen bin holds at most kFinish keys they are ranked directly.
 template <int NT>
 __device__ void select_threshold(const uint32_t *bkey, int nb, uint32_t n, SelectSmem &sm, uint32_t &thr,
                                  uint32_t &need_eq) {
-  constexpr int kWarps = NT / 32;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // keys at or above +inf, and the range of the finite positive keys
-  uint32_t ctop = 0, kmin = 0xFFFFFFFFu, kmax = 0u, cfin = 0;
-  for (int b = tid; b < nb; b += NT) {
-    const uint32_t u = bkey[b];
-    if (u >= kKeyPosInf) {
-      ++ctop;
-    } else if (u != 0u) {
-      ++cfin;
-      kmin = min(kmin, u);
-      kmax = max(kmax, u);
-    }
-  }
-  ctop = __reduce_add_sync(0xffffffffu, ctop);
-  cfin = __reduce_add_sync(0xffffffffu, cfin);
-  kmin = __reduce_min_sync(0xffffffffu, kmin);
-  kmax = __reduce_max_sync(0xffffffffu, kmax);
-  if (lane == 0) {
-    sm.red[0][warp] = ctop;
-    sm.red[1][warp] = kmin;
-    sm.red[2][warp] = kmax;
-    sm.warp_sums[warp] = cfin;
-  }
-  __syncthreads();
-  ctop = 0;
-  cfin = 0;
-  kmin = 0xFFFFFFFFu;
-  kmax = 0u;
-#pragma unroll
-  for (int i = 0; i < kWarps; ++i) {
-    ctop += sm.red[0][i];
-    cfin += sm.warp_sums[i];
-    kmin = min(kmin, sm.red[1][i]);
-    kmax = max(kmax, sm.red[2][i]);
-  }
-  __syncthreads();
-
-  if (ctop >= n) {
-    // at least n blocks at +inf (the pinned block ties with +inf scores): take
-    // the lowest-numbered n of them
-    thr = kKeyPosInf;
-    need_eq = n;
-    return;
-  }
-  uint32_t remaining = n - ctop;  // picks among the cfin finite keys (cfin > remaining)
-  const int L = kmax > kmin ? 32 - __clz(kmax - kmin) : 0;
-  uint32_t rel = 0u, eq_total = cfin;  // keys equal to the threshold, when known
-  for (int hi = L; hi > 0;) {
+  const int tid = threadIdx.x;
+  uint32_t remaining = n, prefix = 0u, eq_total = 0u;
+  for (int hi = 32; hi > 0;) {
     const int nbits = hi < kDigitBits ? hi : kDigitBits, shift = hi - nbits;
     const uint32_t nbins = 1u << nbits;
     const uint32_t fixed = hi >= 32 ? 0u : ~((1u << hi) - 1u);  // bits already chosen
     for (int i = tid; i < kBins; i += NT) sm.hist[i] = 0u;
     __syncthreads();
-    for (int base = 0; base < nb; base += NT) {
-      const int b = base + tid;
-      const uint32_t u = b < nb ? bkey[b] : 0u;
-      const bool act = u != 0u && u < kKeyPosInf && ((u - kmin) & fixed) == rel;
-      const uint32_t bin = act ? ((u - kmin) >> shift) & (nbins - 1u) : 0xFFFFFFFFu;
-      const uint32_t peers = __match_any_sync(0xffffffffu, bin);  // equal bins add once
-      if (act && __ffs(peers) - 1 == lane) atomicAdd(&sm.hist[bin], static_cast<uint32_t>(__popc(peers)));
+    for (int b = tid; b < nb; b += NT) {
+      const uint32_t u = bkey[b];
+      if (u != 0u && (u & fixed) == prefix) atomicAdd(&sm.hist[(u >> shift) & (nbins - 1u)], 1u);
     }
     __syncthreads();
     // bins in descending order: thread t owns ranks R t .. R t + R - 1 (bin nbins - 1 - rank)
@@ -218,7 +178,7 @@ __device__ void select_threshold(const uint32_t *bkey, int nb, uint32_t n, Selec
     }
     __syncthreads();
     remaining -= sm.above;
-    rel |= sm.digit << shift;
+    prefix |= sm.digit << shift;
     eq_total = sm.in_bin;
     hi = shift;
     __syncthreads();
@@ -229,7 +189,7 @@ __device__ void select_threshold(const uint32_t *bkey, int nb, uint32_t n, Selec
       const uint32_t fx = ~((1u << hi) - 1u);
       for (int b = tid; b < nb; b += NT) {
         const uint32_t u = bkey[b];
-        if (u != 0u && u < kKeyPosInf && ((u - kmin) & fx) == rel) sm.fin[atomicAdd(&sm.nfin, 1u)] = u - kmin;
+        if (u != 0u && (u & fx) == prefix) sm.fin[atomicAdd(&sm.nfin, 1u)] = u;
       }
       __syncthreads();
       const uint32_t m = sm.nfin;
@@ -247,17 +207,17 @@ __device__ void select_threshold(const uint32_t *bkey, int nb, uint32_t n, Selec
         }
       }
       __syncthreads();
-      rel = sm.fin_v;
+      prefix = sm.fin_v;
       remaining -= sm.fin_gt;
       eq_total = sm.fin_eq;
       __syncthreads();
       break;
     }
   }
-  thr = kmin + rel;
+  thr = prefix;
   need_eq = remaining;
   if (need_eq == eq_total) {  // every key equal to thr is taken: keep = key >= thr
-    thr -= 1u;                // thr >= kmin > 0
+    thr -= 1u;                // thr >= 1: a positive key
     need_eq = 0u;
   }
 }
@@ -295,9 +255,7 @@ candidate_blocks_kernel(const float *__restrict__ scores, int64_t ld, int B, int
     }
   }
   __syncthreads();
-  uint32_t reach = pin_new;
-#pragma unroll
-  for (int i = 0; i < kWarps; ++i) reach += sm.warp_sums[i];
+  const uint32_t reach = pin_new + sum_parts<NT>(sm.warp_sums, kWarps);
   __syncthreads();
 
   // keep = key > thr, or key == thr among the first need_eq such blocks
@@ -317,7 +275,7 @@ candidate_blocks_kernel(const float *__restrict__ scores, int64_t ld, int B, int
     for (int w = w_begin; w < w_end; ++w) eq_cnt += __popc(__ballot_sync(0xffffffffu, bkey[32 * w + lane] == thr));
     if (lane == 0) sm.warp_sums[warp] = eq_cnt;
     __syncthreads();
-    for (int i = 0; i < warp; ++i) eq_seen += sm.warp_sums[i];
+    eq_seen = sum_parts<NT>(sm.warp_sums, warp);
   }
   uint32_t *out = cand + static_cast<int64_t>(t) * words;
   for (int w = w_begin; w < w_end; ++w) {
