@@ -212,7 +212,8 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_s
 // `remaining`-th largest.  Returns the digit; `remaining` becomes the rank
 // within that bin.
 template <int E, int NT>
-__device__ __forceinline__ uint32_t radix_pass(const uint32_t (&key)[E], int cnt, uint32_t prefix, uint32_t mask,
+__device__ __forceinline__ uint32_t radix_pass(const uint32_t (&key)[E], int cnt, uint64_t skip, uint32_t prefix,
+                                               uint32_t mask,
                                                int shift, int nbins, uint32_t *hist, uint32_t *warp_sums,
                                                int &remaining, uint32_t &in_bin) {
   constexpr int R = kDigitBins / NT;  // ranks (bins) per thread in the scan
@@ -221,7 +222,7 @@ __device__ __forceinline__ uint32_t radix_pass(const uint32_t (&key)[E], int cnt
   __syncthreads();
 #pragma unroll
   for (int e = 0; e < E; ++e)
-    if (e < cnt && (key[e] & mask) == prefix)
+    if (e < cnt && !((skip >> e) & 1u) && (key[e] & mask) == prefix)
       atomicAdd(&hist[(key[e] >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
   __syncthreads();
   // bins in descending order: thread t owns ranks r = R t .. R t + R - 1 (bin = nbins-1-r)
@@ -296,26 +297,29 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
       key[e] = p0 < N_c ? __float_as_uint(row[p0]) : 0u;
     }
   }
+  // bit e set: key e scores -inf (it lies outside the kept candidate blocks,
+  // or its score is -inf)
+  uint64_t masked = 0u;
   if constexpr (kCand) {
-    // positions outside the kept blocks score -inf; a chunk of four
-    // positions inside one block needs one look-up
+    static_assert(E <= 64, "one mask bit per key");
+    // a chunk of four positions inside one block needs one look-up
     const uint32_t *crow = cmask + static_cast<int64_t>(t) * cand_words;
 #pragma unroll
     for (int q = 0; q < E / 4; ++q) {
       const int p0 = kChunkSpan * q + 4 * tid;
       if (p0 < N_c) {
         if (p0 + 3 < N_c && fast_div(p0, dbs) == fast_div(p0 + 3, dbs)) {
-          if (!cand_kept(crow, p0, dbs)) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) key[4 * q + j] = kNegInfBits;
-          }
+          if (!cand_kept(crow, p0, dbs)) masked |= uint64_t{15} << (4 * q);
         } else {
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            if (p0 + j < N_c && !cand_kept(crow, p0 + j, dbs)) key[4 * q + j] = kNegInfBits;
+            if (p0 + j < N_c && !cand_kept(crow, p0 + j, dbs)) masked |= uint64_t{1} << (4 * q + j);
         }
       }
     }
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if (key[e] == kNegInfBits) masked |= uint64_t{1} << e;
   }
   Token tk;
   const bool ok = load_token(q_seq, q_pos, t, B, N_c, r, status, tk, tid == 0);
@@ -334,6 +338,37 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
   const int rem = nv - 4 * tid;
   const int cnt = rem <= 0 ? 0 : min(E, 4 * (rem / kChunkSpan) + min(4, rem % kChunkSpan));
   auto pos_of = [&](int e) { return kChunkSpan * (e >> 2) + 4 * tid + (e & 3); };
+  // keys that take part in the selection: visible and above -inf
+  auto live = [&](int e) { return e < cnt && !((masked >> e) & 1u); };
+
+  // Level two: when the visible positions that score above -inf (in kept
+  // blocks) number at most K, the picks are all of them and then the lowest
+  // visible positions at -inf (the ties); otherwise no position at -inf can
+  // be picked, and they are left out of the selection.
+  bool direct = false;
+  uint32_t direct_eq = 0u;
+  if constexpr (kCand) {
+    uint32_t nl = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) nl += live(e);
+    nl = __reduce_add_sync(0xffffffffu, nl);
+    __shared__ uint32_t wlive[kRegWarps];
+    if (lane == 0) wlive[warp] = nl;
+    __syncthreads();  // also orders the bitmap zeroing before the picks below
+    nl = __reduce_add_sync(0xffffffffu, lane < kRegWarps ? wlive[lane] : 0u);
+    if (nl <= static_cast<uint32_t>(K)) {
+      direct = true;
+      direct_eq = static_cast<uint32_t>(K) - nl;
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if (e < cnt) {
+          const int p0 = pos_of(e);
+          atomicOr(((masked >> e) & 1u) ? &sel_eq[p0 >> 5] : &sel_gt[p0 >> 5], 1u << (p0 & 31));
+        }
+    }
+  }
+  int remaining = K;
+  if (!direct) {
 #pragma unroll
   for (int e = 0; e < E; ++e) key[e] = e < cnt ? ordered_key(__uint_as_float(key[e])) : 0u;
 
@@ -341,7 +376,7 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
 #pragma unroll
   for (int e = 0; e < E; ++e)
-    if (e < cnt) {
+    if (live(e)) {
       kmin = min(kmin, key[e]);
       kmax = max(kmax, key[e]);
     }
@@ -356,19 +391,19 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
   kmin = __reduce_min_sync(0xffffffffu, lane < kRegWarps ? wmin[lane] : 0xFFFFFFFFu);
   kmax = __reduce_max_sync(0xffffffffu, lane < kRegWarps ? wmax[lane] : 0u);
 #pragma unroll
-  for (int e = 0; e < E; ++e) key[e] = e < cnt ? key[e] - kmin : 0u;
+  for (int e = 0; e < E; ++e) key[e] = live(e) ? key[e] - kmin : 0u;
   const int L = kmax > kmin ? 32 - __clz(kmax - kmin) : 0;
 
   // radix select over bits [0, L), kDigitBits at a time from the top; once
   // the chosen bin holds at most kFinish keys, they are ranked directly
-  int remaining = K;
   uint32_t thr = 0u;
   __shared__ uint32_t cand[kFinish], ncand, fin_thr, fin_above;
   for (int hi = L; hi > 0;) {
     const int nb = hi < kDigitBits ? hi : kDigitBits, shift = hi - nb;
     const uint32_t mask = hi >= 32 ? 0u : ~((1u << hi) - 1u);  // bits already fixed
     uint32_t in_bin;
-    const uint32_t d = radix_pass<E, NT>(key, cnt, thr, mask, shift, 1 << nb, hist, warp_sums, remaining, in_bin);
+    const uint32_t d =
+        radix_pass<E, NT>(key, cnt, masked, thr, mask, shift, 1 << nb, hist, warp_sums, remaining, in_bin);
     thr |= d << shift;
     hi = shift;
     if (hi > 0 && in_bin <= static_cast<uint32_t>(kFinish)) {
@@ -378,7 +413,7 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
       const uint32_t fixed = ~((1u << hi) - 1u);
 #pragma unroll
       for (int e = 0; e < E; ++e)
-        if (e < cnt && (key[e] & fixed) == thr) cand[atomicAdd(&ncand, 1u)] = key[e];
+        if (live(e) && (key[e] & fixed) == thr) cand[atomicAdd(&ncand, 1u)] = key[e];
       __syncthreads();
       {
         // the remaining-th largest among the candidates: the value v with
@@ -404,15 +439,16 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
       break;
     }
   }
-  const uint32_t need_eq = static_cast<uint32_t>(remaining);
 
   // picks into the bitmaps (few: K of nv keys)
 #pragma unroll
   for (int e = 0; e < E; ++e)
-    if (e < cnt && key[e] >= thr) {
+    if (live(e) && key[e] >= thr) {
       const int p0 = pos_of(e);
       atomicOr(key[e] > thr ? &sel_gt[p0 >> 5] : &sel_eq[p0 >> 5], 1u << (p0 & 31));
     }
+  }
+  const uint32_t need_eq = direct ? direct_eq : static_cast<uint32_t>(remaining);
   __syncthreads();
   // thread i writes the picks among its kSelWords words of 32 positions, in order
   uint32_t ng = 0, ne = 0;
