@@ -297,29 +297,12 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
       key[e] = p0 < N_c ? __float_as_uint(row[p0]) : 0u;
     }
   }
-  // bit e set: key e scores -inf (it lies outside the kept candidate blocks,
-  // or its score is -inf)
-  uint64_t masked = 0u;
+  // the row's candidate mask (kCand) goes to shared memory with one load per
+  // thread, issued beside the score loads
+  __shared__ uint32_t cwords[kCand ? kRegMax / 32 : 1];
   if constexpr (kCand) {
-    static_assert(E <= 64, "one mask bit per key");
-    // a chunk of four positions inside one block needs one look-up
     const uint32_t *crow = cmask + static_cast<int64_t>(t) * cand_words;
-#pragma unroll
-    for (int q = 0; q < E / 4; ++q) {
-      const int p0 = kChunkSpan * q + 4 * tid;
-      if (p0 < N_c) {
-        if (p0 + 3 < N_c && fast_div(p0, dbs) == fast_div(p0 + 3, dbs)) {
-          if (!cand_kept(crow, p0, dbs)) masked |= uint64_t{15} << (4 * q);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (p0 + j < N_c && !cand_kept(crow, p0 + j, dbs)) masked |= uint64_t{1} << (4 * q + j);
-        }
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < E; ++e)
-      if (key[e] == kNegInfBits) masked |= uint64_t{1} << e;
+    for (int i = tid; i < cand_words; i += NT) cwords[i] = crow[i];
   }
   Token tk;
   const bool ok = load_token(q_seq, q_pos, t, B, N_c, r, status, tk, tid == 0);
@@ -333,6 +316,30 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
   for (int w = 0; w < kSelWords; ++w) {
     sel_gt[kSelWords * tid + w] = 0u;
     sel_eq[kSelWords * tid + w] = 0u;
+  }
+  // bit e set: key e scores -inf (it lies outside the kept candidate blocks,
+  // or its score is -inf)
+  uint64_t masked = 0u;
+  if constexpr (kCand) {
+    static_assert(E <= 64, "one mask bit per key");
+    __syncthreads();  // the mask words are in shared memory
+    // a chunk of four positions inside one block needs one look-up
+#pragma unroll
+    for (int q = 0; q < E / 4; ++q) {
+      const int p0 = kChunkSpan * q + 4 * tid;
+      if (p0 < N_c) {
+        if (p0 + 3 < N_c && fast_div(p0, dbs) == fast_div(p0 + 3, dbs)) {
+          if (!cand_kept(cwords, p0, dbs)) masked |= uint64_t{15} << (4 * q);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (p0 + j < N_c && !cand_kept(cwords, p0 + j, dbs)) masked |= uint64_t{1} << (4 * q + j);
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if (key[e] == kNegInfBits) masked |= uint64_t{1} << e;
   }
   // the visible keys of a thread are a prefix of its E: positions grow with e
   const int rem = nv - 4 * tid;
