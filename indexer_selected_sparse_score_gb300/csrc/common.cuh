@@ -92,12 +92,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct FastDiv {
   uint64_t m;
   int s;
+  uint32_t d;  // the divisor
 };
 
 __host__ __device__ inline FastDiv make_fastdiv(uint32_t d) {
   int l = 0;
   while ((uint64_t{1} << l) < d) ++l;
-  return FastDiv{((uint64_t{1} << (32 + l)) + d - 1) / d, 32 + l};
+  return FastDiv{((uint64_t{1} << (32 + l)) + d - 1) / d, 32 + l, d};
 }
 
 __device__ __forceinline__ uint32_t fast_div(uint32_t n, FastDiv f) {
