@@ -37,7 +37,6 @@ __device__ __forceinline__ bool cand_kept(const uint32_t *crow, int s, FastDiv d
 }
 
 constexpr uint32_t kNegInfBits = 0xFF800000u;  // fp32 -inf
-constexpr uint32_t kKeyNegInf = 0x007FFFFFu;   // ordered_key(-inf)
 
 __global__ void __launch_bounds__(kTopkThreads)
 topk_radix_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, int r,
@@ -212,7 +211,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_s
 // that match `prefix` under `mask`, then locate the bin holding the
 // `remaining`-th largest.  Returns the digit; `remaining` becomes the rank
 // within that bin.
-template <int E, int NT, bool kSkipZero>
+template <int E, int NT>
 __device__ __forceinline__ uint32_t radix_pass(const uint32_t (&key)[E], int cnt, uint32_t prefix, uint32_t mask,
                                                int shift, int nbins, uint32_t *hist, uint32_t *warp_sums,
                                                int &remaining, uint32_t &in_bin) {
@@ -222,7 +221,7 @@ __device__ __forceinline__ uint32_t radix_pass(const uint32_t (&key)[E], int cnt
   __syncthreads();
 #pragma unroll
   for (int e = 0; e < E; ++e)
-    if (e < cnt && (!kSkipZero || key[e] != 0u) && (key[e] & mask) == prefix)
+    if (e < cnt && (key[e] & mask) == prefix)
       atomicAdd(&hist[(key[e] >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
   __syncthreads();
   // bins in descending order: thread t owns ranks r = R t .. R t + R - 1 (bin = nbins-1-r)
@@ -317,74 +316,39 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
     sel_gt[kSelWords * tid + w] = 0u;
     sel_eq[kSelWords * tid + w] = 0u;
   }
+  if constexpr (kCand) {
+    // positions outside the kept candidate blocks score -inf; a chunk of four
+    // positions inside one block needs one look-up
+    __syncthreads();  // the mask words are in shared memory
+#pragma unroll
+    for (int q = 0; q < E / 4; ++q) {
+      const int p0 = kChunkSpan * q + 4 * tid;
+      if (p0 < nv) {
+        if (dbs.d % 4u == 0u || fast_div(p0, dbs) == fast_div(p0 + 3, dbs)) {
+          if (!cand_kept(cwords, p0, dbs)) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) key[4 * q + j] = kNegInfBits;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (p0 + j < nv && !cand_kept(cwords, p0 + j, dbs)) key[4 * q + j] = kNegInfBits;
+        }
+      }
+    }
+  }
   // the visible keys of a thread are a prefix of its E: positions grow with e
   const int rem = nv - 4 * tid;
   const int cnt = rem <= 0 ? 0 : min(E, 4 * (rem / kChunkSpan) + min(4, rem % kChunkSpan));
   auto pos_of = [&](int e) { return kChunkSpan * (e >> 2) + 4 * tid + (e & 3); };
+#pragma unroll
+  for (int e = 0; e < E; ++e) key[e] = e < cnt ? ordered_key(__uint_as_float(key[e])) : 0u;
 
-  // Level two (kCand): the positions at -inf -- outside the kept candidate
-  // blocks, or scoring -inf -- get key 0, and the other visible keys become
-  // key - min + 1 below, so key 0 marks them.  When the visible positions
-  // above -inf number at most K, the picks are all of them and then the lowest
-  // visible positions at -inf (the ties); otherwise no position at -inf can be
-  // picked and key 0 stays out of the selection.
-  bool direct = false;
-  uint32_t direct_eq = 0u;
-  if constexpr (kCand) {
-    __syncthreads();  // the mask words are in shared memory
-    uint32_t nl = 0;
-#pragma unroll
-    for (int q = 0; q < E / 4; ++q) {
-      const int p0 = kChunkSpan * q + 4 * tid;
-      if (4 * q < cnt) {
-        // a chunk of four positions inside one block needs one look-up
-        const bool one_block = dbs.d % 4u == 0u || fast_div(p0, dbs) == fast_div(p0 + 3, dbs);
-        const bool kept0 = cand_kept(cwords, p0, dbs);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int e = 4 * q + j;
-          uint32_t k = 0u;
-          if (e < cnt && (one_block ? kept0 : cand_kept(cwords, p0 + j, dbs))) {
-            k = ordered_key(__uint_as_float(key[e]));
-            if (k <= kKeyNegInf) k = 0u;
-          }
-          key[e] = k;
-          nl += k != 0u;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) key[4 * q + j] = 0u;
-      }
-    }
-    nl = __reduce_add_sync(0xffffffffu, nl);
-    __shared__ uint32_t wlive[kRegWarps];
-    if (lane == 0) wlive[warp] = nl;
-    __syncthreads();  // also orders the bitmap zeroing before the picks below
-    nl = __reduce_add_sync(0xffffffffu, lane < kRegWarps ? wlive[lane] : 0u);
-    if (nl <= static_cast<uint32_t>(K)) {
-      direct = true;
-      direct_eq = static_cast<uint32_t>(K) - nl;
-#pragma unroll
-      for (int e = 0; e < E; ++e)
-        if (e < cnt) {
-          const int p0 = pos_of(e);
-          atomicOr(key[e] == 0u ? &sel_eq[p0 >> 5] : &sel_gt[p0 >> 5], 1u << (p0 & 31));
-        }
-    }
-  }
-  int remaining = K;
-  if (!direct) {
-  if constexpr (!kCand) {
-#pragma unroll
-    for (int e = 0; e < E; ++e) key[e] = e < cnt ? ordered_key(__uint_as_float(key[e])) : 0u;
-  }
-
-  // the row's key range: keys become key - min (< 2^L); with kCand, key -
-  // min + 1 for the keys above 0
+  // the row's key range: keys become key - min (< 2^L)
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
 #pragma unroll
   for (int e = 0; e < E; ++e)
-    if (kCand ? key[e] != 0u : e < cnt) {
+    if (e < cnt) {
       kmin = min(kmin, key[e]);
       kmax = max(kmax, key[e]);
     }
@@ -398,27 +362,20 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
   __syncthreads();
   kmin = __reduce_min_sync(0xffffffffu, lane < kRegWarps ? wmin[lane] : 0xFFFFFFFFu);
   kmax = __reduce_max_sync(0xffffffffu, lane < kRegWarps ? wmax[lane] : 0u);
-  if constexpr (kCand) {
 #pragma unroll
-    for (int e = 0; e < E; ++e) key[e] = key[e] != 0u ? key[e] - kmin + 1u : 0u;
-    kmax = kmax - kmin + 1u;  // the range is now [1, kmax]
-    kmin = 0u;
-  } else {
-#pragma unroll
-    for (int e = 0; e < E; ++e) key[e] = e < cnt ? key[e] - kmin : 0u;
-  }
+  for (int e = 0; e < E; ++e) key[e] = e < cnt ? key[e] - kmin : 0u;
   const int L = kmax > kmin ? 32 - __clz(kmax - kmin) : 0;
 
   // radix select over bits [0, L), kDigitBits at a time from the top; once
   // the chosen bin holds at most kFinish keys, they are ranked directly
+  int remaining = K;
   uint32_t thr = 0u;
   __shared__ uint32_t cand[kFinish], ncand, fin_thr, fin_above;
   for (int hi = L; hi > 0;) {
     const int nb = hi < kDigitBits ? hi : kDigitBits, shift = hi - nb;
     const uint32_t mask = hi >= 32 ? 0u : ~((1u << hi) - 1u);  // bits already fixed
     uint32_t in_bin;
-    const uint32_t d =
-        radix_pass<E, NT, kCand>(key, cnt, thr, mask, shift, 1 << nb, hist, warp_sums, remaining, in_bin);
+    const uint32_t d = radix_pass<E, NT>(key, cnt, thr, mask, shift, 1 << nb, hist, warp_sums, remaining, in_bin);
     thr |= d << shift;
     hi = shift;
     if (hi > 0 && in_bin <= static_cast<uint32_t>(kFinish)) {
@@ -428,7 +385,7 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
       const uint32_t fixed = ~((1u << hi) - 1u);
 #pragma unroll
       for (int e = 0; e < E; ++e)
-        if (e < cnt && (!kCand || key[e] != 0u) && (key[e] & fixed) == thr) cand[atomicAdd(&ncand, 1u)] = key[e];
+        if (e < cnt && (key[e] & fixed) == thr) cand[atomicAdd(&ncand, 1u)] = key[e];
       __syncthreads();
       {
         // the remaining-th largest among the candidates: the value v with
@@ -454,16 +411,15 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
       break;
     }
   }
+  const uint32_t need_eq = static_cast<uint32_t>(remaining);
 
   // picks into the bitmaps (few: K of nv keys)
 #pragma unroll
   for (int e = 0; e < E; ++e)
-    if (e < cnt && key[e] >= thr) {  // with kCand, thr >= 1
+    if (e < cnt && key[e] >= thr) {
       const int p0 = pos_of(e);
       atomicOr(key[e] > thr ? &sel_gt[p0 >> 5] : &sel_eq[p0 >> 5], 1u << (p0 & 31));
     }
-  }
-  const uint32_t need_eq = direct ? direct_eq : static_cast<uint32_t>(remaining);
   __syncthreads();
   // thread i writes the picks among its kSelWords words of 32 positions, in order
   uint32_t ng = 0, ne = 0;
