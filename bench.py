@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--soak-seconds", type=float, default=1.5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-two-level", action="store_true", help="skip the two-level top-k measurement")
     return ap.parse_args()
 
 
@@ -84,6 +85,8 @@ def peaks():
 
 STAGE_SOURCES = {"idx_score": ("idx_score.cu", "idx_score_umma.cu", "umma.cuh", "common.cuh"),
                  "idx_topk": ("idx_topk.cu", "common.cuh"),
+                 "level_one": ("idx_candidates.cu", "common.cuh"),
+                 "level_two": ("idx_topk.cu", "common.cuh"),
                  "sparse_mqa": ("sparse_mqa.cu", "sparse_mqa_umma.cu", "umma.cuh", "common.cuh")}
 
 
@@ -300,7 +303,8 @@ def two_level_topk(binding, torch, wl, steps, peak):
     for name, v in ms.items():
         gbs = alg[name] / (v / 1000.0) / 1e9
         res[name] = {"us": round(v * 1000.0, 2), "algorithmic_bytes": alg[name], "GB_s": round(gbs, 1),
-                     "frac_of_hbm_peak": round(gbs / peak, 4)}
+                     "frac_of_hbm_peak": round(gbs / peak, 4),
+                     "traffic": recorded_traffic(name if name != "one_level_topk" else "idx_topk", "c4_two_level")}
     return res
 
 
@@ -522,7 +526,7 @@ def run_ours(args):
     step_frac = nbytes["step"] / (ms_per_step / 1000.0) / 1e9 / peak
 
     clocks = sampler.summary(t_soak, t_end)
-    two_level = two_level_topk(binding, torch, wl, args.steps, peak)
+    two_level = None if args.no_two_level else two_level_topk(binding, torch, wl, args.steps, peak)
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
