@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-two-level", action="store_true", help="skip the two-level top-k measurement")
+    ap.add_argument("--no-v41", action="store_true", help="skip the V4.1-shape measurement")
     return ap.parse_args()
 
 
@@ -308,6 +309,95 @@ def two_level_topk(binding, torch, wl, steps, peak):
     return res
 
 
+def v41_decode(binding, torch, steps, peak):
+    """The fused step on the released V4.1 attention shape: decode batch 64 at
+    positions U[32768, 65535], r 2 (N_c 32768), index 32 x 128 with bf16 queries and
+    fp8 keys + per-position scale U(0.5, 2), w U(0,1)/32, top-k 512, window 128,
+    64 query heads of dim 512 over one kv tensor used as K and V, a per-head sink,
+    scale 512^-0.5.  Inputs are drawn on the device (seeded N(0,1)), three copies
+    rotate between steps; CUDA-graph replay of sa_fused_decode, plus the stage
+    times from sa_fused_decode_staged."""
+    B = T = 64
+    r, N_c, H_I, D_I, K, W, R, H, D = 2, 32768, 32, 128, 512, 128, 128, 64, 512
+    q_pos = np.random.default_rng(41).integers(32768, 65535, size=T, endpoint=True).astype(np.int32)
+    q_seq = np.arange(T, dtype=np.int32)
+    gen = torch.Generator(device="cuda").manual_seed(41)
+    bf = torch.bfloat16
+
+    def normal(shape, dtype=bf):
+        return torch.empty(shape, dtype=dtype, device="cuda").normal_(generator=gen)
+
+    copies = []
+    for _ in range(3):
+        d = {"q_seq": torch.from_numpy(q_seq).cuda(), "q_pos": torch.from_numpy(q_pos).cuda(),
+             "q_I": normal((T, H_I, D_I)), "w": torch.rand((T, H_I), device="cuda", generator=gen) / 32,
+             "k_I": normal((B, N_c, D_I)).to(torch.float8_e4m3fn),
+             "k_scale": torch.rand((B, N_c), device="cuda", generator=gen) * 1.5 + 0.5,
+             "Q": normal((T, H, D)), "KVw": normal((B, R, D)), "KVc": normal((B, N_c, D)),
+             "sink": normal((H,), torch.float32)}
+        ia = binding.IndexArgs(B, T, H_I, D_I, N_c, r, d["q_seq"].data_ptr(), d["q_pos"].data_ptr(),
+                               d["q_I"].data_ptr(), 0, None, d["w"].data_ptr(), d["k_I"].data_ptr(), 1,
+                               d["k_scale"].data_ptr())
+        aa = binding.AttnArgs(H, D, W, R, d["Q"].data_ptr(), d["KVw"].data_ptr(), d["KVw"].data_ptr(),
+                              d["KVc"].data_ptr(), d["KVc"].data_ptr(), d["sink"].data_ptr(), float(D) ** -0.5)
+        copies.append((d, ia, aa))
+    n = binding.sa_workspace_size(copies[0][1], copies[0][2], K)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    binding.sa_workspace_init(ws)
+    out = torch.empty((T, H, D), dtype=bf, device="cuda")
+    idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    for _, ia, aa in copies:
+        binding.sa_fused_decode(ia, aa, K, idx, out, ws)
+    torch.cuda.synchronize()
+    graphs = []
+    for _, ia, aa in copies:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            binding.sa_fused_decode(ia, aa, K, idx, out, ws)
+        graphs.append(g)
+    for i in range(6):
+        graphs[i % 3].replay()
+    torch.cuda.synchronize()
+    n_steps = max(10, steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(n_steps):
+        graphs[i % 3].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n_steps
+    # stage times: eager staged calls, each after the previous copy's step
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    sums = [0.0, 0.0, 0.0]
+    for i in range(n_steps):
+        _, ia0, aa0 = copies[(i - 1) % 3]
+        binding.sa_fused_decode(ia0, aa0, K, idx, out, ws)
+        _, ia, aa = copies[i % 3]
+        binding.sa_fused_decode_staged(ia, aa, K, idx, out, ws, [e.cuda_event for e in evs])
+        torch.cuda.synchronize()
+        for j in range(3):
+            sums[j] += evs[j].elapsed_time(evs[j + 1])
+    if binding.sa_check_device_status(ws) != binding.SA_OK:
+        raise RuntimeError("device status not OK after the V4.1-shape steps")
+    nv = np.minimum((q_pos.astype(np.int64) + 1) // r, N_c)
+    n_w = np.minimum(W, q_pos.astype(np.int64) + 1)
+    idx_bytes = int(np.sum(nv) * (D_I + 4))
+    attn_bytes = int(np.sum(n_w + np.minimum(K, nv)) * D * 2)  # one kv row serves as K and V
+    step_bytes = idx_bytes + attn_bytes
+    st = dict(zip(("idx_score", "idx_topk", "sparse_mqa"), (v / n_steps for v in sums)))
+    attn_flop = float(np.sum(n_w + np.minimum(K, nv))) * H * D * 4  # Q.K and P.V
+    return {"workload": "V4.1 released attention shape: decode batch 64, positions U[32768,65535], r 2, "
+                        "index 32x128 fp8 keys + scale, topk 512, window 128, 64 heads x dim 512, one kv "
+                        "tensor as K and V, sink; device-drawn N(0,1) inputs, 3 rotating copies",
+            "ms_per_step": round(ms, 5), "value": round(T / (ms / 1000.0), 1), "unit": "query-tokens/s",
+            "step_bytes": step_bytes, "frac_of_hbm_peak": round(step_bytes / (ms / 1000.0) / 1e9 / peak, 4),
+            "stages_ms": {k: round(v, 5) for k, v in st.items()},
+            "idx_score_GB_s": round(idx_bytes / (st["idx_score"] / 1000.0) / 1e9, 1),
+            "sparse_mqa_GB_s": round(attn_bytes / (st["sparse_mqa"] / 1000.0) / 1e9, 1),
+            "sparse_mqa_TFLOP_s": round(attn_flop / (st["sparse_mqa"] / 1000.0) / 1e12, 2),
+            "note": "attention at head dim 512 runs on the CUDA-core kernel (fp32 FMA)"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -527,6 +617,7 @@ def run_ours(args):
 
     clocks = sampler.summary(t_soak, t_end)
     two_level = None if args.no_two_level else two_level_topk(binding, torch, wl, args.steps, peak)
+    v41 = None if args.no_v41 else v41_decode(binding, torch, args.steps, peak)
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -555,6 +646,7 @@ def run_ours(args):
                   "note": "the same steps launched through the C ABI without a graph"},
         "clocks": clocks,
         "two_level_topk": two_level,
+        "v41_decode": v41,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)

@@ -94,7 +94,8 @@ typedef struct {
  * sparse_attn(q, kv, attn_sink, topk_idxs, softmax_scale) over the window KV
  * concatenated with the compressed KV). */
 typedef struct {
-  int32_t H, D;        /* query heads (H*D a multiple of 256, H <= 128), head dim (128) */
+  int32_t H, D;        /* query heads and head dim: D 128 with H 16/32/64/128, or D 512
+                          (the released V4.1 shape) with H 16/32/64 */
   int32_t W;           /* window length (>= 1) */
   int32_t R;           /* raw ring slots per sequence (>= W; a prefill chunk of n
                           tokens needs R >= n + W - 1) */
@@ -102,7 +103,8 @@ typedef struct {
   const void *Kw;      /* [B, R, D] bf16 raw window keys, slot = position mod R */
   const void *Vw;      /* [B, R, D] bf16 raw window values (may equal Kw) */
   const void *Kc;      /* [B, N_c, D] bf16 compressed keys */
-  const void *Vc;      /* [B, N_c, D] bf16 compressed values (may equal Kc) */
+  const void *Vc;      /* [B, N_c, D] bf16 compressed values (may equal Kc; when Vw == Kw
+                          and Vc == Kc -- V4.1's single kv -- each row is read once) */
   const float *sink;   /* [H] per-head attention sink logit, or NULL for none */
   float scale;         /* softmax scale applied to Q.K (e.g. D^-0.5) */
 } sa_attn_args;

@@ -61,7 +61,8 @@ sa_status check_index(const sa_index_args *ia, bool need_index_inputs) {
 sa_status check_attn(const sa_attn_args *aa, int T) {
   if (!aa) return fail(SA_ERR_INVALID_ARG, "attention args pointer is NULL");
   if (!sa::attn_shape_supported(aa->H, aa->D))
-    return fail(SA_ERR_UNSUPPORTED, "attention %d heads x dim %d: need dim 128 and 16/32/64/128 heads",
+    return fail(SA_ERR_UNSUPPORTED,
+                "attention %d heads x dim %d: need dim 128 with 16/32/64/128 heads or dim 512 with 16/32/64",
                 aa->H, aa->D);
   if (aa->W < 1 || aa->R < aa->W)
     return fail(SA_ERR_INVALID_ARG, "need W >= 1 and R >= W (got W=%d R=%d)", aa->W, aa->R);

@@ -4,10 +4,12 @@
 // cat(window_idxs, compress_idxs + offset), sparse_attn(q, kv, attn_sink,
 // topk_idxs, softmax_scale); one shared KV head serves every query head).
 //
-// CUDA-core kernel (head counts other than 64; the tensor-core kernel for 64
-// heads is in sparse_mqa_umma.cu): one CTA per (token, split).  The token's key list is its
-// window rows (oldest first) followed by its K index slots; a split takes a
-// contiguous chunk of that list.  Rows are gathered 16 bytes per thread,
+// CUDA-core kernel (head dim 128 with head counts other than 64, and head dim
+// 512 -- the released V4.1 shape; the tensor-core kernel for 64 heads of dim
+// 128 is in sparse_mqa_umma.cu): one CTA per (token, split).  The token's key
+// list is its window rows (oldest first) followed by its K index slots; a
+// split takes a contiguous chunk of that list.  When K and V are one tensor
+// (V4.1's single kv), each row is loaded once and serves as both tiles.  Rows are gathered 16 bytes per thread,
 // logits and the online softmax run in fp32 in the log2 domain (logits are
 // pre-multiplied by scale * log2(e)), and each split leaves (m, l, o) partials
 // that the combine kernel merges.  A single split writes the output directly.
@@ -17,8 +19,14 @@
 namespace sa {
 namespace {
 
-constexpr int kAttnThreads = 256;
-constexpr int kKeyTile = 32;
+constexpr int kKeyTile = 32;  // keys per tile (16 for dim 512 with separate K and V)
+
+// Launch shape per head dim: threads per CTA and keys per tile.
+template <int D, bool kSameKV>
+struct AttnShape {
+  static constexpr int kThreads = D == 512 ? 512 : 256;
+  static constexpr int kTile = (D == 512 && !kSameKV) ? 16 : kKeyTile;
+};
 
 struct AttnParams {
   int B, T, N_c, r;
@@ -35,24 +43,28 @@ struct AttnParams {
   uint32_t *status;
 };
 
-template <int H, int D>
+template <int H, int D, bool kSameKV>
 constexpr size_t attn_smem_bytes() {
-  return sizeof(float) * (static_cast<size_t>(H) * (D + 1) + kKeyTile * (D + 1) + kKeyTile * D +
-                          H * (kKeyTile + 1) + 3 * H) +
-         sizeof(int) * 2 * kKeyTile;
+  constexpr int KT = AttnShape<D, kSameKV>::kTile;
+  return sizeof(float) * (static_cast<size_t>(H) * (D + 1) + KT * (D + 1) + (kSameKV ? 0 : KT * D) +
+                          H * (KT + 1) + 3 * H) +
+         sizeof(int) * 2 * KT;
 }
 
-template <int H, int D>
-__global__ void __launch_bounds__(kAttnThreads) sparse_mqa_simt_kernel(AttnParams p) {
+template <int H, int D, bool kSameKV>
+__global__ void __launch_bounds__(AttnShape<D, kSameKV>::kThreads) sparse_mqa_simt_kernel(AttnParams p) {
+  constexpr int kAttnThreads = AttnShape<D, kSameKV>::kThreads;
+  constexpr int kKeyTile = AttnShape<D, kSameKV>::kTile;
   constexpr int NPT = H * D / kAttnThreads;
   constexpr int DP = D + 1;
   constexpr int PP = kKeyTile + 1;
+  constexpr int VS = kSameKV ? DP : D;  // row stride of the V tile
   static_assert(NPT * kAttnThreads == H * D, "H*D must be a multiple of the CTA size");
   extern __shared__ float4 smem4[];
-  float *Qs = reinterpret_cast<float *>(smem4);  // [H][DP]
-  float *Ks = Qs + H * DP;                       // [kKeyTile][DP]
-  float *Vs = Ks + kKeyTile * DP;                // [kKeyTile][D]
-  float *Ps = Vs + kKeyTile * D;                 // [H][PP]
+  float *Qs = reinterpret_cast<float *>(smem4);     // [H][DP]
+  float *Ks = Qs + H * DP;                          // [kKeyTile][DP]
+  float *Vs = kSameKV ? Ks : Ks + kKeyTile * DP;    // [kKeyTile][VS]
+  float *Ps = Ks + kKeyTile * DP + (kSameKV ? 0 : kKeyTile * D);  // [H][PP]
   float *m_s = Ps + H * PP;
   float *l_s = m_s + H;
   float *c_s = l_s + H;
@@ -109,9 +121,11 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_mqa_simt_kernel(AttnParam
       uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
       if (row >= 0) {
         const uint16_t *kb = src_of[j] ? p.Kc : p.Kw;
-        const uint16_t *vb = src_of[j] ? p.Vc : p.Vw;
         kv = __ldg(reinterpret_cast<const uint4 *>(kb + static_cast<int64_t>(row) * D) + c);
-        vv = __ldg(reinterpret_cast<const uint4 *>(vb + static_cast<int64_t>(row) * D) + c);
+        if constexpr (!kSameKV) {
+          const uint16_t *vb = src_of[j] ? p.Vc : p.Vw;
+          vv = __ldg(reinterpret_cast<const uint4 *>(vb + static_cast<int64_t>(row) * D) + c);
+        }
       }
       const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
       const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
@@ -119,8 +133,10 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_mqa_simt_kernel(AttnParam
       for (int e = 0; e < 4; ++e) {
         Ks[j * DP + 8 * c + 2 * e] = __uint_as_float(kw[e] << 16);
         Ks[j * DP + 8 * c + 2 * e + 1] = __uint_as_float(kw[e] & 0xFFFF0000u);
-        Vs[j * D + 8 * c + 2 * e] = __uint_as_float(vw[e] << 16);
-        Vs[j * D + 8 * c + 2 * e + 1] = __uint_as_float(vw[e] & 0xFFFF0000u);
+        if constexpr (!kSameKV) {
+          Vs[j * D + 8 * c + 2 * e] = __uint_as_float(vw[e] << 16);
+          Vs[j * D + 8 * c + 2 * e + 1] = __uint_as_float(vw[e] & 0xFFFF0000u);
+        }
       }
     }
     __syncthreads();
@@ -165,7 +181,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_mqa_simt_kernel(AttnParam
       const int h = el / D, d = el % D;
       float a = acc[e] * c_s[h];
 #pragma unroll 8
-      for (int j = 0; j < kKeyTile; ++j) a = fmaf(Ps[h * PP + j], Vs[j * D + d], a);
+      for (int j = 0; j < kKeyTile; ++j) a = fmaf(Ps[h * PP + j], Vs[j * VS + d], a);
       acc[e] = a;
     }
     __syncthreads();
@@ -232,15 +248,16 @@ __global__ void __launch_bounds__(D) combine_kernel(int H, int S, const float *_
   out[static_cast<int64_t>(th) * D + d] = __float2bfloat16_rn(o);
 }
 
-template <int H, int D>
+template <int H, int D, bool kSameKV>
 cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
-  auto kern = sparse_mqa_simt_kernel<H, D>;
-  constexpr size_t smem = attn_smem_bytes<H, D>();
+  auto kern = sparse_mqa_simt_kernel<H, D, kSameKV>;
+  constexpr size_t smem = attn_smem_bytes<H, D, kSameKV>();
+  static_assert(smem <= 227 * 1024, "shared memory of one CTA");
   static bool attr_done[64] = {};
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), smem, attr_done);
   if (e != cudaSuccess) return e;
   dim3 grid(p.splits, p.T);
-  kern<<<grid, kAttnThreads, smem, stream>>>(p);
+  kern<<<grid, AttnShape<D, kSameKV>::kThreads, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.splits == 1) return e;
   combine_kernel<D><<<p.T * H, D, 0, stream>>>(H, p.splits, p.part_m, p.part_l, p.part_o, p.sink,
@@ -251,7 +268,8 @@ cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
 }  // namespace
 
 bool attn_shape_supported(int H, int D) {
-  return D == 128 && (H == 16 || H == 32 || H == 64 || H == 128);
+  return (D == 128 && (H == 16 || H == 32 || H == 64 || H == 128)) ||
+         (D == 512 && (H == 16 || H == 32 || H == 64));
 }
 
 int fused_launch_count(const sa_index_args &ia, const sa_attn_args &aa, int K,
@@ -306,11 +324,21 @@ cudaError_t launch_sparse_mqa(const sa_index_args &ia, const sa_attn_args &aa, c
   p.part_o = part_o;
   p.out = static_cast<__nv_bfloat16 *>(out);
   p.status = status;
+  // one tensor for K and V (the window ring and the compressed cache alike)
+  const bool same = aa.Kw == aa.Vw && aa.Kc == aa.Vc;
+  if (aa.D == 512) {
+    switch (aa.H) {
+      case 16: return same ? launch_attn<16, 512, true>(p, stream) : launch_attn<16, 512, false>(p, stream);
+      case 32: return same ? launch_attn<32, 512, true>(p, stream) : launch_attn<32, 512, false>(p, stream);
+      case 64: return same ? launch_attn<64, 512, true>(p, stream) : launch_attn<64, 512, false>(p, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (aa.H) {
-    case 16: return launch_attn<16, 128>(p, stream);
-    case 32: return launch_attn<32, 128>(p, stream);
-    case 64: return launch_attn<64, 128>(p, stream);
-    case 128: return launch_attn<128, 128>(p, stream);
+    case 16: return same ? launch_attn<16, 128, true>(p, stream) : launch_attn<16, 128, false>(p, stream);
+    case 32: return same ? launch_attn<32, 128, true>(p, stream) : launch_attn<32, 128, false>(p, stream);
+    case 64: return same ? launch_attn<64, 128, true>(p, stream) : launch_attn<64, 128, false>(p, stream);
+    case 128: return same ? launch_attn<128, 128, true>(p, stream) : launch_attn<128, 128, false>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -155,3 +155,11 @@ def test_candidate_calls_with_no_tokens_enqueue_nothing(lib):
     ia = _ia(T=0, q_seq=None, q_pos=None)
     assert lib.sa_candidate_blocks(None, ctypes.byref(ia), 8, 4, None, 256, 256, None) == binding.SA_OK
     assert lib.sa_topk_candidates(None, ctypes.byref(ia), 8, None, 8, None, 256, 256, None) == binding.SA_OK
+
+
+def test_attention_head_dims(lib):
+    # dim 512 (the released V4.1 shape) with up to 64 heads; 128 heads of dim 512 do not fit
+    assert lib.sa_workspace_size(ctypes.byref(_ia()), ctypes.byref(_aa(H=64, D=512)), 8) > 0
+    assert lib.sa_workspace_size(ctypes.byref(_ia()), ctypes.byref(_aa(H=16, D=512)), 8) > 0
+    assert _call_fused(lib, _ia(), _aa(H=128, D=512)) == binding.SA_ERR_UNSUPPORTED
+    assert _call_fused(lib, _ia(), _aa(H=64, D=256)) == binding.SA_ERR_UNSUPPORTED
