@@ -368,6 +368,8 @@ def v41_decode(binding, torch, steps, peak):
     ms = e0.elapsed_time(e1) / n_steps
     # stage times: eager staged calls, each after the previous copy's step
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for e in evs:
+        e.record()  # materialise the CUDA event handles
     sums = [0.0, 0.0, 0.0]
     for i in range(n_steps):
         _, ia0, aa0 = copies[(i - 1) % 3]
