@@ -366,19 +366,27 @@ def v41_decode(binding, torch, steps, peak):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / n_steps
-    # stage times: eager staged calls, each after the previous copy's step
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-    for e in evs:
-        e.record()  # materialise the CUDA event handles
+    # stage times: one staged graph per copy (events between the stages), each
+    # replayed right after the previous copy's step
+    stage_events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in copies]
+    for row in stage_events:
+        for e in row:
+            e.record()  # materialise the CUDA event handles
+    torch.cuda.synchronize()
+    staged = []
+    for (_, ia, aa), evs in zip(copies, stage_events):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            binding.sa_fused_decode_staged(ia, aa, K, idx, out, ws, [e.cuda_event for e in evs])
+        staged.append(g)
     sums = [0.0, 0.0, 0.0]
     for i in range(n_steps):
-        _, ia0, aa0 = copies[(i - 1) % 3]
-        binding.sa_fused_decode(ia0, aa0, K, idx, out, ws)
-        _, ia, aa = copies[i % 3]
-        binding.sa_fused_decode_staged(ia, aa, K, idx, out, ws, [e.cuda_event for e in evs])
+        k = i % 3
+        staged[(k - 1) % 3].replay()
+        staged[k].replay()
         torch.cuda.synchronize()
         for j in range(3):
-            sums[j] += evs[j].elapsed_time(evs[j + 1])
+            sums[j] += stage_events[k][j].elapsed_time(stage_events[k][j + 1])
     if binding.sa_check_device_status(ws) != binding.SA_OK:
         raise RuntimeError("device status not OK after the V4.1-shape steps")
     nv = np.minimum((q_pos.astype(np.int64) + 1) // r, N_c)
