@@ -43,11 +43,14 @@ struct AttnParams {
   uint32_t *status;
 };
 
+// Shared-memory rows of Q and K are D + 4 floats apart (16-byte aligned rows
+// whose 16-byte chunks fall in distinct banks across 8 consecutive rows), P
+// rows KT + 4.
 template <int H, int D, bool kSameKV>
 constexpr size_t attn_smem_bytes() {
   constexpr int KT = AttnShape<D, kSameKV>::kTile;
-  return sizeof(float) * (static_cast<size_t>(H) * (D + 1) + KT * (D + 1) + (kSameKV ? 0 : KT * D) +
-                          H * (KT + 1) + 3 * H) +
+  return sizeof(float) * (static_cast<size_t>(H) * (D + 4) + KT * (D + 4) + (kSameKV ? 0 : KT * D) +
+                          H * (KT + 4) + 3 * H) +
          sizeof(int) * 2 * KT;
 }
 
@@ -56,10 +59,15 @@ __global__ void __launch_bounds__(AttnShape<D, kSameKV>::kThreads) sparse_mqa_si
   constexpr int kAttnThreads = AttnShape<D, kSameKV>::kThreads;
   constexpr int kKeyTile = AttnShape<D, kSameKV>::kTile;
   constexpr int NPT = H * D / kAttnThreads;
-  constexpr int DP = D + 1;
-  constexpr int PP = kKeyTile + 1;
+  constexpr int DP = D + 4;
+  constexpr int PP = kKeyTile + 4;
   constexpr int VS = kSameKV ? DP : D;  // row stride of the V tile
+  // logits: thread = (key j, heads h0 + m * HSTEP); P.V: thread = (column d, heads d0 + e * DSTEP)
+  constexpr int HSTEP = kAttnThreads / kKeyTile < H ? kAttnThreads / kKeyTile : H, HPT = H / HSTEP;
+  constexpr int DSTEP = kAttnThreads / D;
   static_assert(NPT * kAttnThreads == H * D, "H*D must be a multiple of the CTA size");
+  static_assert(HPT * HSTEP == H && kAttnThreads % kKeyTile == 0, "logit blocking");
+  static_assert(kAttnThreads % D == 0 && kKeyTile % 4 == 0, "P.V blocking");
   extern __shared__ float4 smem4[];
   float *Qs = reinterpret_cast<float *>(smem4);     // [H][DP]
   float *Ks = Qs + H * DP;                          // [kKeyTile][DP]
@@ -140,18 +148,31 @@ __global__ void __launch_bounds__(AttnShape<D, kSameKV>::kThreads) sparse_mqa_si
       }
     }
     __syncthreads();
-    for (int i = tid; i < H * kKeyTile; i += kAttnThreads) {
-      const int h = i / kKeyTile, j = i % kKeyTile;
-      float v = -INFINITY;
-      if (row_of[j] >= 0) {
-        float dot = 0.f;
-        const float *qh = Qs + h * DP;
-        const float *kj = Ks + j * DP;
-#pragma unroll 16
-        for (int d = 0; d < D; ++d) dot = fmaf(qh[d], kj[d], dot);
-        v = dot;
+    if (tid / kKeyTile < HSTEP) {
+      // each 16-byte chunk of key j's row serves HPT heads (threads past HSTEP
+      // rows of keys have no heads left and skip this)
+      const int j = tid % kKeyTile, h0 = tid / kKeyTile;
+      float dot[HPT];
+#pragma unroll
+      for (int m = 0; m < HPT; ++m) dot[m] = 0.f;
+      const float *kj = Ks + j * DP;
+#pragma unroll 4
+      for (int d = 0; d < D; d += 4) {
+        const float4 kv = *reinterpret_cast<const float4 *>(kj + d);
+#pragma unroll
+        for (int m = 0; m < HPT; ++m) {
+          const float4 qv = *reinterpret_cast<const float4 *>(Qs + (h0 + m * HSTEP) * DP + d);
+          float a = dot[m];
+          a = fmaf(qv.x, kv.x, a);
+          a = fmaf(qv.y, kv.y, a);
+          a = fmaf(qv.z, kv.z, a);
+          a = fmaf(qv.w, kv.w, a);
+          dot[m] = a;
+        }
       }
-      Ps[h * PP + j] = v;
+      const bool live = row_of[j] >= 0;
+#pragma unroll
+      for (int m = 0; m < HPT; ++m) Ps[(h0 + m * HSTEP) * PP + j] = live ? dot[m] : -INFINITY;
     }
     __syncthreads();
     for (int h = tid; h < H; h += kAttnThreads) {
@@ -175,14 +196,26 @@ __global__ void __launch_bounds__(AttnShape<D, kSameKV>::kThreads) sparse_mqa_si
       c_s[h] = corr;
     }
     __syncthreads();
+    {
+      // each V element serves the thread's NPT heads; P comes four keys at a time
+      const int d = tid % D, hb = tid / D;
 #pragma unroll
-    for (int e = 0; e < NPT; ++e) {
-      const int el = tid + e * kAttnThreads;
-      const int h = el / D, d = el % D;
-      float a = acc[e] * c_s[h];
-#pragma unroll 8
-      for (int j = 0; j < kKeyTile; ++j) a = fmaf(Ps[h * PP + j], Vs[j * VS + d], a);
-      acc[e] = a;
+      for (int e = 0; e < NPT; ++e) acc[e] *= c_s[hb + e * DSTEP];
+#pragma unroll 1
+      for (int j = 0; j < kKeyTile; j += 4) {
+        const float v0 = Vs[j * VS + d], v1 = Vs[(j + 1) * VS + d];
+        const float v2 = Vs[(j + 2) * VS + d], v3 = Vs[(j + 3) * VS + d];
+#pragma unroll
+        for (int e = 0; e < NPT; ++e) {
+          const float4 pp = *reinterpret_cast<const float4 *>(Ps + (hb + e * DSTEP) * PP + j);
+          float a = acc[e];
+          a = fmaf(pp.x, v0, a);
+          a = fmaf(pp.y, v1, a);
+          a = fmaf(pp.z, v2, a);
+          a = fmaf(pp.w, v3, a);
+          acc[e] = a;
+        }
+      }
     }
     __syncthreads();
   }
