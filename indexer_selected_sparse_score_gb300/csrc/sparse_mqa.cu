@@ -298,6 +298,275 @@ cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Head dim 512 (the released V4.1 shape) on the warp-level bf16 tensor-core MMA
+// (mma.sync m16n8k16, fp32 accumulate).  One CTA of 16 warps per (token,
+// split), 32 keys per tile:
+//  - Q (bf16, unscaled) stays in shared memory; each tile's K rows (and V rows,
+//    unless K and V are one tensor) are gathered into shared memory as bf16;
+//  - S = Q K^T: warp w owns the 16 x 8 block of heads 16 (w / 4).. and keys
+//    8 (w % 4).. (fewer than 64 heads leave warps idle here), 32 MMAs over the
+//    512 dims; the logits, scaled into the log2 domain, go to shared memory;
+//  - the online softmax (one thread per head) writes P as two bf16 parts,
+//    P = hi + lo with |P - hi - lo| < 2^-16 P, so P.V keeps fp32-level accuracy;
+//  - O += P V: warp w owns the heads of one 16-row block and a run of 8-column
+//    blocks of the 512 dims; its accumulators stay in registers across tiles,
+//    rescaled by the softmax correction; V fragments come by ldmatrix.trans.
+constexpr int kMmaThreads = 512;
+constexpr int kMmaD = 512;
+constexpr int kMmaKT = 32;
+constexpr int kQS = kMmaD + 8;   // bf16 row stride of the Q, K and V tiles (1040 bytes)
+constexpr int kSS = kMmaKT + 4;  // fp32 row stride of S
+constexpr int kPS = kMmaKT + 8;  // bf16 row stride of P hi and lo (80 bytes)
+
+template <int H, bool kSameKV>
+struct Mma512Layout {
+  static constexpr size_t q = 0;
+  static constexpr size_t k = q + sizeof(uint16_t) * H * kQS;
+  static constexpr size_t v = k + sizeof(uint16_t) * kMmaKT * kQS;
+  static constexpr size_t s = v + (kSameKV ? 0 : sizeof(uint16_t) * kMmaKT * kQS);
+  static constexpr size_t phi = s + sizeof(float) * H * kSS;
+  static constexpr size_t plo = phi + sizeof(uint16_t) * H * kPS;
+  static constexpr size_t ms = plo + sizeof(uint16_t) * H * kPS;
+  static constexpr size_t rows = ms + sizeof(float) * 3 * H;
+  static constexpr size_t total = rows + sizeof(int) * 2 * kMmaKT;
+};
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldmatrix_x2_trans(uint32_t &r0, uint32_t &r1, const void *smem_row) {
+  const uint32_t addr = static_cast<uint32_t>(__cvta_generic_to_shared(smem_row));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t ld_u32(const uint16_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
+
+template <int H, bool kSameKV>
+__global__ void __launch_bounds__(kMmaThreads) sparse_mqa_mma512_kernel(AttnParams p) {
+  using Lay = Mma512Layout<H, kSameKV>;
+  constexpr int D = kMmaD, KT = kMmaKT;
+  constexpr int MT = H / 16;          // 16-row blocks of heads
+  constexpr int WPM = 16 / MT;        // warps per head block in P.V
+  constexpr int NTW = (D / 8) / WPM;  // 8-column blocks per warp in P.V
+  static_assert(MT * 16 == H && WPM * MT == 16 && NTW * WPM * 8 == D, "warp split");
+  extern __shared__ float4 smem4[];
+  char *sm = reinterpret_cast<char *>(smem4);
+  uint16_t *Qb = reinterpret_cast<uint16_t *>(sm + Lay::q);
+  uint16_t *Kb = reinterpret_cast<uint16_t *>(sm + Lay::k);
+  uint16_t *Vb = kSameKV ? Kb : reinterpret_cast<uint16_t *>(sm + Lay::v);
+  float *Sf = reinterpret_cast<float *>(sm + Lay::s);
+  uint16_t *Phi = reinterpret_cast<uint16_t *>(sm + Lay::phi);
+  uint16_t *Plo = reinterpret_cast<uint16_t *>(sm + Lay::plo);
+  float *m_s = reinterpret_cast<float *>(sm + Lay::ms);
+  float *l_s = m_s + H;
+  float *c_s = l_s + H;
+  int *row_of = reinterpret_cast<int *>(sm + Lay::rows);
+  int *src_of = row_of + KT;
+
+  const int t = blockIdx.y, split = blockIdx.x, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, q4 = lane & 3;
+  Token tk;
+  const bool ok = load_token(p.q_seq, p.q_pos, t, p.B, p.N_c, p.r, p.status, tk, split == 0 && tid == 0);
+  const int n_w = ok ? min(p.W, tk.pos + 1) : 0;
+  const int n_keys = ok ? n_w + p.K : 0;
+  const int k_begin = split * p.split_keys;
+  const int k_end = min(k_begin + p.split_keys, n_keys);
+
+  const int64_t qbase = static_cast<int64_t>(t) * H * D;
+  for (int i = tid; i < H * (D / 8); i += kMmaThreads) {  // 16-byte chunks of Q
+    const int h = i / (D / 8), c = i % (D / 8);
+    *reinterpret_cast<uint4 *>(Qb + h * kQS + 8 * c) =
+        __ldg(reinterpret_cast<const uint4 *>(p.Q + qbase + static_cast<int64_t>(h) * D) + c);
+  }
+  for (int h = tid; h < H; h += kMmaThreads) {
+    m_s[h] = -INFINITY;
+    l_s[h] = 0.f;
+  }
+  // P.V ownership: head block pm, column blocks pn0 .. pn0 + NTW - 1
+  const int pm = warp / WPM, pn0 = (warp % WPM) * NTW;
+  float acc[NTW][4];
+#pragma unroll
+  for (int i = 0; i < NTW; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
+  __syncthreads();
+
+  for (int tile = k_begin; tile < k_end; tile += KT) {
+    if (tid < KT) {
+      const int kk = tile + tid;
+      int row = -1, src = 0;
+      if (kk < k_end) {
+        if (kk < n_w) {
+          const int pos = tk.pos - n_w + 1 + kk;
+          row = tk.b * p.R + pos % p.R;
+        } else {
+          const int c = p.idx[static_cast<int64_t>(t) * p.K + (kk - n_w)];
+          if (c >= 0 && c < tk.nv) {
+            row = tk.b * p.N_c + c;
+            src = 1;
+          } else if (c != -1) {
+            raise_flag(p.status, kFlagBadIndex);
+          }
+        }
+      }
+      row_of[tid] = row;
+      src_of[tid] = src;
+    }
+    __syncthreads();
+    for (int i = tid; i < KT * (D / 8); i += kMmaThreads) {  // gather the tile's rows, 16 bytes at a time
+      const int j = i / (D / 8), c = i % (D / 8);
+      const int row = row_of[j];
+      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+      if (row >= 0) {
+        const uint16_t *kb = src_of[j] ? p.Kc : p.Kw;
+        kv = __ldg(reinterpret_cast<const uint4 *>(kb + static_cast<int64_t>(row) * D) + c);
+        if constexpr (!kSameKV) {
+          const uint16_t *vb = src_of[j] ? p.Vc : p.Vw;
+          vv = __ldg(reinterpret_cast<const uint4 *>(vb + static_cast<int64_t>(row) * D) + c);
+        }
+      }
+      *reinterpret_cast<uint4 *>(Kb + j * kQS + 8 * c) = kv;
+      if constexpr (!kSameKV) *reinterpret_cast<uint4 *>(Vb + j * kQS + 8 * c) = vv;
+    }
+    __syncthreads();
+    if (warp < MT * (KT / 8)) {  // S block: heads 16 smt .., keys 8 snt ..
+      const int smt = warp / (KT / 8), snt = warp % (KT / 8);
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint16_t *qa = Qb + (16 * smt + g) * kQS + 2 * q4;
+      const uint16_t *kbp = Kb + (8 * snt + g) * kQS + 2 * q4;
+#pragma unroll 8
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t a[4] = {ld_u32(qa + 16 * ks), ld_u32(qa + 8 * kQS + 16 * ks), ld_u32(qa + 16 * ks + 8),
+                               ld_u32(qa + 8 * kQS + 16 * ks + 8)};
+        mma_bf16_16816(c, a, ld_u32(kbp + 16 * ks), ld_u32(kbp + 16 * ks + 8));
+      }
+      const int h0 = 16 * smt + g, j0 = 8 * snt + 2 * q4;
+      const bool v0 = row_of[j0] >= 0, v1 = row_of[j0 + 1] >= 0;
+      Sf[h0 * kSS + j0] = v0 ? c[0] * p.qk_scale : -INFINITY;
+      Sf[h0 * kSS + j0 + 1] = v1 ? c[1] * p.qk_scale : -INFINITY;
+      Sf[(h0 + 8) * kSS + j0] = v0 ? c[2] * p.qk_scale : -INFINITY;
+      Sf[(h0 + 8) * kSS + j0 + 1] = v1 ? c[3] * p.qk_scale : -INFINITY;
+    }
+    __syncthreads();
+    for (int h = tid; h < H; h += kMmaThreads) {  // online softmax, P split into bf16 hi + lo
+      float mx = -INFINITY;
+      for (int j = 0; j < KT; ++j) mx = fmaxf(mx, Sf[h * kSS + j]);
+      const float m_old = m_s[h];
+      const float m_new = fmaxf(m_old, mx);
+      float corr = 1.f, sum = 0.f;
+      for (int j = 0; j < KT; ++j) {
+        const float pj = m_new != -INFINITY ? exp2f(Sf[h * kSS + j] - m_new) : 0.f;
+        sum += pj;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(pj);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(pj - __bfloat162float(hi));
+        Phi[h * kPS + j] = __bfloat16_as_ushort(hi);
+        Plo[h * kPS + j] = __bfloat16_as_ushort(lo);
+      }
+      if (m_new != -INFINITY) corr = exp2f(m_old - m_new);
+      l_s[h] = l_s[h] * corr + sum;
+      m_s[h] = m_new;
+      c_s[h] = corr;
+    }
+    __syncthreads();
+    {
+      const int r0 = 16 * pm + g;
+      const float cr0 = c_s[r0], cr1 = c_s[r0 + 8];
+#pragma unroll
+      for (int i = 0; i < NTW; ++i) {
+        acc[i][0] *= cr0;
+        acc[i][1] *= cr0;
+        acc[i][2] *= cr1;
+        acc[i][3] *= cr1;
+      }
+#pragma unroll
+      for (int ks = 0; ks < KT / 16; ++ks) {
+        const uint16_t *ph = Phi + r0 * kPS + 16 * ks + 2 * q4;
+        const uint16_t *pl = Plo + r0 * kPS + 16 * ks + 2 * q4;
+        const uint32_t ahi[4] = {ld_u32(ph), ld_u32(ph + 8 * kPS), ld_u32(ph + 8), ld_u32(ph + 8 * kPS + 8)};
+        const uint32_t alo[4] = {ld_u32(pl), ld_u32(pl + 8 * kPS), ld_u32(pl + 8), ld_u32(pl + 8 * kPS + 8)};
+        // lanes 0-15 address rows 16 ks + (lane & 15) of V (lanes 16-31 repeat them)
+        const uint16_t *vrow = Vb + (16 * ks + (lane & 15)) * kQS;
+#pragma unroll
+        for (int i = 0; i < NTW; ++i) {
+          uint32_t b0, b1;
+          ldmatrix_x2_trans(b0, b1, vrow + 8 * (pn0 + i));
+          mma_bf16_16816(acc[i], ahi, b0, b1);
+          mma_bf16_16816(acc[i], alo, b0, b1);
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  const int r0 = 16 * pm + g;
+  if (p.splits == 1) {
+    float sc[2];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int h = r0 + 8 * half;
+      const float m = m_s[h];
+      const float s2 = p.sink ? p.sink[h] * kLog2e : -INFINITY;
+      const float M = fmaxf(m, s2);
+      sc[half] = 0.f;
+      if (M != -INFINITY) {
+        const float a = exp2f(m - M);
+        const float L = l_s[h] * a + (p.sink ? exp2f(s2 - M) : 0.f);
+        sc[half] = a / L;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NTW; ++i) {
+      const int d = 8 * (pn0 + i) + 2 * q4;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int64_t o = qbase + static_cast<int64_t>(r0 + 8 * half) * D + d;
+        p.out[o] = __float2bfloat16_rn(acc[i][2 * half] * sc[half]);
+        p.out[o + 1] = __float2bfloat16_rn(acc[i][2 * half + 1] * sc[half]);
+      }
+    }
+  } else {
+    for (int h = tid; h < H; h += kMmaThreads) {
+      const int64_t pi = (static_cast<int64_t>(t) * H + h) * p.splits + split;
+      p.part_m[pi] = m_s[h];
+      p.part_l[pi] = l_s[h];
+    }
+#pragma unroll
+    for (int i = 0; i < NTW; ++i) {
+      const int d = 8 * (pn0 + i) + 2 * q4;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int64_t pi = (static_cast<int64_t>(t) * H + r0 + 8 * half) * p.splits + split;
+        p.part_o[pi * D + d] = acc[i][2 * half];
+        p.part_o[pi * D + d + 1] = acc[i][2 * half + 1];
+      }
+    }
+  }
+}
+
+template <int H, bool kSameKV>
+cudaError_t launch_attn_mma512(const AttnParams &p, cudaStream_t stream) {
+  auto kern = sparse_mqa_mma512_kernel<H, kSameKV>;
+  constexpr size_t smem = Mma512Layout<H, kSameKV>::total;
+  static_assert(smem <= 227 * 1024, "shared memory of one CTA");
+  static bool attr_done[64] = {};
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), smem, attr_done);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.splits, p.T);
+  kern<<<grid, kMmaThreads, smem, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.splits == 1) return e;
+  combine_kernel<kMmaD><<<p.T * H, kMmaD, 0, stream>>>(H, p.splits, p.part_m, p.part_l, p.part_o, p.sink, p.out);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 bool attn_shape_supported(int H, int D) {
@@ -359,11 +628,11 @@ cudaError_t launch_sparse_mqa(const sa_index_args &ia, const sa_attn_args &aa, c
   p.status = status;
   // one tensor for K and V (the window ring and the compressed cache alike)
   const bool same = aa.Kw == aa.Vw && aa.Kc == aa.Vc;
-  if (aa.D == 512) {
+  if (aa.D == 512) {  // warp-level bf16 MMA
     switch (aa.H) {
-      case 16: return same ? launch_attn<16, 512, true>(p, stream) : launch_attn<16, 512, false>(p, stream);
-      case 32: return same ? launch_attn<32, 512, true>(p, stream) : launch_attn<32, 512, false>(p, stream);
-      case 64: return same ? launch_attn<64, 512, true>(p, stream) : launch_attn<64, 512, false>(p, stream);
+      case 16: return same ? launch_attn_mma512<16, true>(p, stream) : launch_attn_mma512<16, false>(p, stream);
+      case 32: return same ? launch_attn_mma512<32, true>(p, stream) : launch_attn_mma512<32, false>(p, stream);
+      case 64: return same ? launch_attn_mma512<64, true>(p, stream) : launch_attn_mma512<64, false>(p, stream);
       default: return cudaErrorInvalidValue;
     }
   }
