@@ -303,11 +303,12 @@ cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
 // (mma.sync m16n8k16, fp32 accumulate).  One CTA of 16 warps per (token,
 // split), 32 keys per tile:
 //  - Q (bf16, unscaled) stays in shared memory; each tile's K rows (and V rows,
-//    unless K and V are one tensor) are gathered into shared memory as bf16;
+//    unless K and V are one tensor) are gathered into shared memory as bf16 by
+//    cp.async, into one of two buffers while the other tile is computed;
 //  - S = Q K^T: warp w owns the 16 x 8 block of heads 16 (w / 4).. and keys
 //    8 (w % 4).. (fewer than 64 heads leave warps idle here), 32 MMAs over the
 //    512 dims; the logits, scaled into the log2 domain, go to shared memory;
-//  - the online softmax (one thread per head) writes P as two bf16 parts,
+//  - the online softmax (one warp per head, a lane per key) writes P as two bf16 parts,
 //    P = hi + lo with |P - hi - lo| < 2^-16 P, so P.V keeps fp32-level accuracy;
 //  - O += P V: warp w owns the heads of one 16-row block and a run of 8-column
 //    blocks of the 512 dims; its accumulators stay in registers across tiles,
@@ -321,16 +322,30 @@ constexpr int kPS = kMmaKT + 8;  // bf16 row stride of P hi and lo (80 bytes)
 
 template <int H, bool kSameKV>
 struct Mma512Layout {
+  static constexpr size_t tile = sizeof(uint16_t) * kMmaKT * kQS;  // one K (or V) tile
   static constexpr size_t q = 0;
-  static constexpr size_t k = q + sizeof(uint16_t) * H * kQS;
-  static constexpr size_t v = k + sizeof(uint16_t) * kMmaKT * kQS;
-  static constexpr size_t s = v + (kSameKV ? 0 : sizeof(uint16_t) * kMmaKT * kQS);
+  static constexpr size_t k = q + sizeof(uint16_t) * H * kQS;       // two K buffers
+  static constexpr size_t v = k + 2 * tile;                         // two V buffers (separate V)
+  static constexpr size_t s = v + (kSameKV ? 0 : 2 * tile);
   static constexpr size_t phi = s + sizeof(float) * H * kSS;
   static constexpr size_t plo = phi + sizeof(uint16_t) * H * kPS;
   static constexpr size_t ms = plo + sizeof(uint16_t) * H * kPS;
   static constexpr size_t rows = ms + sizeof(float) * 3 * H;
-  static constexpr size_t total = rows + sizeof(int) * 2 * kMmaKT;
+  static constexpr size_t total = rows + sizeof(int) * 4 * kMmaKT;  // row ids per buffer
 };
+
+// 16-byte global -> shared copy; with valid false it writes 16 zero bytes and
+// reads nothing (src must still be a mapped address).
+__device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, bool valid) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -360,16 +375,16 @@ __global__ void __launch_bounds__(kMmaThreads) sparse_mqa_mma512_kernel(AttnPara
   extern __shared__ float4 smem4[];
   char *sm = reinterpret_cast<char *>(smem4);
   uint16_t *Qb = reinterpret_cast<uint16_t *>(sm + Lay::q);
-  uint16_t *Kb = reinterpret_cast<uint16_t *>(sm + Lay::k);
-  uint16_t *Vb = kSameKV ? Kb : reinterpret_cast<uint16_t *>(sm + Lay::v);
+  uint16_t *Kbuf = reinterpret_cast<uint16_t *>(sm + Lay::k);                        // [2][KT][kQS]
+  uint16_t *Vbuf = kSameKV ? Kbuf : reinterpret_cast<uint16_t *>(sm + Lay::v);     // [2][KT][kQS]
   float *Sf = reinterpret_cast<float *>(sm + Lay::s);
   uint16_t *Phi = reinterpret_cast<uint16_t *>(sm + Lay::phi);
   uint16_t *Plo = reinterpret_cast<uint16_t *>(sm + Lay::plo);
   float *m_s = reinterpret_cast<float *>(sm + Lay::ms);
   float *l_s = m_s + H;
   float *c_s = l_s + H;
-  int *row_of = reinterpret_cast<int *>(sm + Lay::rows);
-  int *src_of = row_of + KT;
+  int *rows_buf = reinterpret_cast<int *>(sm + Lay::rows);  // [2][KT] row ids, then [2][KT] sources
+  int *srcs_buf = rows_buf + 2 * KT;
 
   const int t = blockIdx.y, split = blockIdx.x, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, q4 = lane & 3;
@@ -399,44 +414,59 @@ __global__ void __launch_bounds__(kMmaThreads) sparse_mqa_mma512_kernel(AttnPara
     for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
   __syncthreads();
 
-  for (int tile = k_begin; tile < k_end; tile += KT) {
-    if (tid < KT) {
-      const int kk = tile + tid;
-      int row = -1, src = 0;
-      if (kk < k_end) {
-        if (kk < n_w) {
-          const int pos = tk.pos - n_w + 1 + kk;
-          row = tk.b * p.R + pos % p.R;
-        } else {
-          const int c = p.idx[static_cast<int64_t>(t) * p.K + (kk - n_w)];
-          if (c >= 0 && c < tk.nv) {
-            row = tk.b * p.N_c + c;
-            src = 1;
-          } else if (c != -1) {
-            raise_flag(p.status, kFlagBadIndex);
-          }
+  // row ids of a tile (threads below KT), then its rows copied into buffer b
+  auto tile_rows = [&](int tile, int b) {
+    const int kk = tile + tid;
+    int row = -1, src = 0;
+    if (kk < k_end) {
+      if (kk < n_w) {
+        const int pos = tk.pos - n_w + 1 + kk;
+        row = tk.b * p.R + pos % p.R;
+      } else {
+        const int c = p.idx[static_cast<int64_t>(t) * p.K + (kk - n_w)];
+        if (c >= 0 && c < tk.nv) {
+          row = tk.b * p.N_c + c;
+          src = 1;
+        } else if (c != -1) {
+          raise_flag(p.status, kFlagBadIndex);
         }
       }
-      row_of[tid] = row;
-      src_of[tid] = src;
     }
-    __syncthreads();
-    for (int i = tid; i < KT * (D / 8); i += kMmaThreads) {  // gather the tile's rows, 16 bytes at a time
+    rows_buf[b * KT + tid] = row;
+    srcs_buf[b * KT + tid] = src;
+  };
+  auto tile_copy = [&](int b) {
+    for (int i = tid; i < KT * (D / 8); i += kMmaThreads) {  // 16 bytes at a time; empty slots read as 0
       const int j = i / (D / 8), c = i % (D / 8);
-      const int row = row_of[j];
-      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-      if (row >= 0) {
-        const uint16_t *kb = src_of[j] ? p.Kc : p.Kw;
-        kv = __ldg(reinterpret_cast<const uint4 *>(kb + static_cast<int64_t>(row) * D) + c);
-        if constexpr (!kSameKV) {
-          const uint16_t *vb = src_of[j] ? p.Vc : p.Vw;
-          vv = __ldg(reinterpret_cast<const uint4 *>(vb + static_cast<int64_t>(row) * D) + c);
-        }
-      }
-      *reinterpret_cast<uint4 *>(Kb + j * kQS + 8 * c) = kv;
-      if constexpr (!kSameKV) *reinterpret_cast<uint4 *>(Vb + j * kQS + 8 * c) = vv;
+      const int row = rows_buf[b * KT + j];
+      const bool valid = row >= 0;
+      const int64_t off = static_cast<int64_t>(valid ? row : 0) * D + 8 * c;
+      const bool comp = srcs_buf[b * KT + j] != 0;
+      cp_async16_zfill(Kbuf + (b * KT + j) * kQS + 8 * c, (comp ? p.Kc : p.Kw) + off, valid);
+      if constexpr (!kSameKV) cp_async16_zfill(Vbuf + (b * KT + j) * kQS + 8 * c, (comp ? p.Vc : p.Vw) + off, valid);
     }
+    cp_async_commit();
+  };
+  if (k_begin < k_end) {
+    if (tid < KT) tile_rows(k_begin, 0);
     __syncthreads();
+    tile_copy(0);
+  }
+
+  for (int tile = k_begin, it = 0; tile < k_end; tile += KT, ++it) {
+    const int b = it & 1;
+    if (tile + KT < k_end) {  // the next tile's copies go out before this one is computed
+      if (tid < KT) tile_rows(tile + KT, b ^ 1);
+      __syncthreads();
+      tile_copy(b ^ 1);
+      cp_async_wait_group<1>();
+    } else {
+      cp_async_wait_group<0>();
+    }
+    __syncthreads();  // every thread's copies of this tile are in
+    const uint16_t *Kb = Kbuf + b * KT * kQS;
+    const uint16_t *Vb = Vbuf + b * KT * kQS;
+    const int *row_of = rows_buf + b * KT;
     if (warp < MT * (KT / 8)) {  // S block: heads 16 smt .., keys 8 snt ..
       const int smt = warp / (KT / 8), snt = warp % (KT / 8);
       float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -456,24 +486,27 @@ __global__ void __launch_bounds__(kMmaThreads) sparse_mqa_mma512_kernel(AttnPara
       Sf[(h0 + 8) * kSS + j0 + 1] = v1 ? c[3] * p.qk_scale : -INFINITY;
     }
     __syncthreads();
-    for (int h = tid; h < H; h += kMmaThreads) {  // online softmax, P split into bf16 hi + lo
-      float mx = -INFINITY;
-      for (int j = 0; j < KT; ++j) mx = fmaxf(mx, Sf[h * kSS + j]);
+    for (int h = warp; h < H; h += kMmaThreads / 32) {  // online softmax: a warp per head, a lane per key
+      const float sv = Sf[h * kSS + lane];
+      float mx = sv;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       const float m_old = m_s[h];
       const float m_new = fmaxf(m_old, mx);
-      float corr = 1.f, sum = 0.f;
-      for (int j = 0; j < KT; ++j) {
-        const float pj = m_new != -INFINITY ? exp2f(Sf[h * kSS + j] - m_new) : 0.f;
-        sum += pj;
-        const __nv_bfloat16 hi = __float2bfloat16_rn(pj);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(pj - __bfloat162float(hi));
-        Phi[h * kPS + j] = __bfloat16_as_ushort(hi);
-        Plo[h * kPS + j] = __bfloat16_as_ushort(lo);
+      const float pj = m_new != -INFINITY ? exp2f(sv - m_new) : 0.f;
+      float sum = pj;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      const __nv_bfloat16 hi = __float2bfloat16_rn(pj);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(pj - __bfloat162float(hi));
+      Phi[h * kPS + lane] = __bfloat16_as_ushort(hi);
+      Plo[h * kPS + lane] = __bfloat16_as_ushort(lo);
+      if (lane == 0) {
+        const float corr = m_new != -INFINITY ? exp2f(m_old - m_new) : 1.f;
+        l_s[h] = l_s[h] * corr + sum;
+        m_s[h] = m_new;
+        c_s[h] = corr;
       }
-      if (m_new != -INFINITY) corr = exp2f(m_old - m_new);
-      l_s[h] = l_s[h] * corr + sum;
-      m_s[h] = m_new;
-      c_s[h] = corr;
     }
     __syncthreads();
     {
