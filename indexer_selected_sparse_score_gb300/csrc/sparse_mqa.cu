@@ -469,15 +469,23 @@ __global__ void __launch_bounds__(kMmaThreads) sparse_mqa_mma512_kernel(AttnPara
     const int *row_of = rows_buf + b * KT;
     if (warp < MT * (KT / 8)) {  // S block: heads 16 smt .., keys 8 snt ..
       const int smt = warp / (KT / 8), snt = warp % (KT / 8);
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      // four accumulators over interleaved 16-dim steps: four short MMA chains, summed at the end
+      float cc[4][4] = {};
       const uint16_t *qa = Qb + (16 * smt + g) * kQS + 2 * q4;
       const uint16_t *kbp = Kb + (8 * snt + g) * kQS + 2 * q4;
-#pragma unroll 8
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const uint32_t a[4] = {ld_u32(qa + 16 * ks), ld_u32(qa + 8 * kQS + 16 * ks), ld_u32(qa + 16 * ks + 8),
-                               ld_u32(qa + 8 * kQS + 16 * ks + 8)};
-        mma_bf16_16816(c, a, ld_u32(kbp + 16 * ks), ld_u32(kbp + 16 * ks + 8));
+#pragma unroll 2
+      for (int k0 = 0; k0 < D / 16; k0 += 4) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int ks = k0 + u;
+          const uint32_t a[4] = {ld_u32(qa + 16 * ks), ld_u32(qa + 8 * kQS + 16 * ks), ld_u32(qa + 16 * ks + 8),
+                                 ld_u32(qa + 8 * kQS + 16 * ks + 8)};
+          mma_bf16_16816(cc[u], a, ld_u32(kbp + 16 * ks), ld_u32(kbp + 16 * ks + 8));
+        }
       }
+      float c[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) c[e] = (cc[0][e] + cc[1][e]) + (cc[2][e] + cc[3][e]);
       const int h0 = 16 * smt + g, j0 = 8 * snt + 2 * q4;
       const bool v0 = row_of[j0] >= 0, v1 = row_of[j0 + 1] >= 0;
       Sf[h0 * kSS + j0] = v0 ? c[0] * p.qk_scale : -INFINITY;
