@@ -87,6 +87,12 @@ def _lib(mutant: int = 0, path: Optional[str] = None):
         lib.orc_topk_row.argtypes = [vp, i32, i32, vp]
         lib.orc_topk_row.restype = i32
         lib.orc_candidate_blocks.argtypes = [vp, i32, i32, i32, i32, vp]
+        lib.orc_hadamard_bf16.argtypes = [vp, i32, vp]
+        lib.orc_hadamard_bf16.restype = i32
+        lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.orc_e4m3_encode.restype = ctypes.c_uint8
+        lib.orc_act_quant_row.argtypes = [vp, i32, vp, vp]
+        lib.orc_act_quant_row.restype = i32
         lib.orc_candidate_blocks.restype = i32
         lib.orc_sparse_attn.argtypes = [P, vp, i32, vp, i32, vp]
         lib.orc_sparse_attn.restype = i32
@@ -233,6 +239,43 @@ def candidate_topk_row(scores: np.ndarray, nv: int, K: int, keep: np.ndarray, bl
     blocks = np.arange(s.size) // block_size
     s[~keep[blocks]] = -np.inf
     return topk_row(s, nv, K, mutant)
+
+
+def hadamard_bf16(x_bits: np.ndarray, mutant: int = 0) -> np.ndarray:
+    """V3.2 rotate_activation ("DeepSeek-V3.2-Exp inference/model.py"): each row
+    of bf16 bits times the Sylvester-Hadamard matrix, scaled by n^-1/2, in bf16."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    rows = x.reshape(-1, x.shape[-1])
+    out = np.empty_like(rows)
+    for i in range(rows.shape[0]):
+        if _lib(mutant).orc_hadamard_bf16(rows[i].ctypes.data, rows.shape[1], out[i].ctypes.data) != 0:
+            raise ValueError("oracle: row length is not a power of two")
+    return out.reshape(x.shape)
+
+
+def e4m3_encode(v: np.ndarray, mutant: int = 0) -> np.ndarray:
+    """Nearest float8 e4m3fn codes (ties to even, saturating at +-448)."""
+    f = np.ascontiguousarray(v, dtype=np.float32).reshape(-1)
+    lib = _lib(mutant)
+    return np.array([lib.orc_e4m3_encode(float(x)) for x in f], dtype=np.uint8).reshape(np.shape(v))
+
+
+def act_quant_rows(y_bits: np.ndarray, mutant: int = 0):
+    """act_quant with one block per row (V3.2 Indexer.forward): (codes uint8, scales float32)."""
+    y = np.ascontiguousarray(y_bits, dtype=np.uint16)
+    rows = y.reshape(-1, y.shape[-1])
+    codes = np.empty(rows.shape, dtype=np.uint8)
+    scales = np.empty(rows.shape[0], dtype=np.float32)
+    for i in range(rows.shape[0]):
+        if _lib(mutant).orc_act_quant_row(rows[i].ctypes.data, rows.shape[1], codes[i].ctypes.data,
+                                          scales[i:i + 1].ctypes.data) != 0:
+            raise ValueError("oracle: empty row")
+    return codes.reshape(y.shape), scales.reshape(y.shape[:-1])
+
+
+def rotate_quant_rows(x_bits: np.ndarray, mutant: int = 0):
+    """The V3.2 index producer on rows of bf16 bits: rotation, then act_quant."""
+    return act_quant_rows(hadamard_bf16(x_bits, mutant), mutant)
 
 
 def sparse_attn(p: Problem, idx: np.ndarray, rows=None, mutant: int = 0) -> np.ndarray:

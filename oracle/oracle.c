@@ -278,6 +278,93 @@ int32_t orc_candidate_blocks(const double *S, int32_t n_vis, int32_t N_c, int32_
   return kept;
 }
 
+/* ---- V3.2 index producer: Hadamard rotation and fp8 quantisation -------- */
+
+/* Nearest bfloat16 (ties to even) of a finite float, as bits. */
+static uint16_t bf16_nearest(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof(u));
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+/* "DeepSeek-V3.2-Exp inference/model.py", rotate_activation: a bf16 row of n
+ * (a power of two) times the Sylvester-Hadamard matrix of order n
+ * (H[i][j] = (-1)^popcount(i & j)), scaled by n^-1/2, returned in bf16.
+ * Computed in fp32 (reading: the precision of the library the page calls) by
+ * the butterfly stages h = 1, 2, 4, ..., n/2, each mapping the pair at
+ * positions (i, i + h), i & h == 0, from (a, b) to (a + b, a - b); then each
+ * value times the fp32 constant (float)(1 / sqrt(n)), rounded to bf16.  The
+ * stage order is fixed so that the fp8 codes derived from the result are
+ * reproducible bit for bit. */
+int32_t orc_hadamard_bf16(const uint16_t *x, int32_t n, uint16_t *y) {
+  if (n < 1 || (n & (n - 1))) return -1;
+  float *v = (float *)malloc(sizeof(float) * (size_t)n);
+  for (int32_t i = 0; i < n; ++i) v[i] = (float)orc_bf16_value(x[i]);
+  for (int32_t h = 1; h < n; h <<= 1)
+    for (int32_t i = 0; i < n; ++i)
+      if (!(i & h)) {
+        const float a = v[i], b = v[i + h];
+        v[i] = a + b;
+#if ORC_MUTANT == 12
+        v[i + h] = b - a;
+#else
+        v[i + h] = a - b;
+#endif
+      }
+  const float sc = (float)(1.0 / sqrt((double)n));
+  for (int32_t i = 0; i < n; ++i) y[i] = bf16_nearest(v[i] * sc);
+  free(v);
+  return 0;
+}
+
+/* The float8 e4m3fn code nearest to v (ties to the even code), saturating at
+ * +-448, the largest finite value: from the format's definition (subnormals
+ * are multiples of 2^-9 below 2^-6; a normal 1.m * 2^E has 3 mantissa bits). */
+uint8_t orc_e4m3_encode(float v) {
+  const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+  const double a = fabs((double)v);
+  if (!(a < 448.0)) return sign | 0x7E;
+#if ORC_MUTANT == 13
+#define ORC_RINT round /* ties away from zero */
+#else
+#define ORC_RINT rint
+#endif
+  if (a < 0x1p-6) return sign | (uint8_t)ORC_RINT(a * 512.0); /* 8 is the smallest normal's code */
+  int e;
+  const double fr = frexp(a, &e); /* a = fr * 2^e, fr in [0.5, 1) */
+  int E = e - 1;
+  double m = ORC_RINT((2.0 * fr - 1.0) * 8.0);
+  if (m == 8.0) {
+    m = 0.0;
+    E += 1;
+  }
+  int code = ((E + 7) << 3) | (int)m;
+  if (code > 0x7E) code = 0x7E;
+  return sign | (uint8_t)code;
+}
+
+/* act_quant over one block of n values (V3.2 Indexer.forward quantises each
+ * head_dim = 128 row as one block; reading: the scale is amax / 448 in fp32,
+ * the codes are e4m3(y / scale) with an fp32 division, and an all-zero block
+ * gets scale 1).  y: bf16 bits. */
+int32_t orc_act_quant_row(const uint16_t *y, int32_t n, uint8_t *codes, float *scale) {
+  if (n < 1) return -1;
+  float amax = 0.f;
+  for (int32_t i = 0; i < n; ++i) {
+    const float a = (float)fabs(orc_bf16_value(y[i]));
+    if (a > amax) amax = a;
+  }
+#if ORC_MUTANT == 14
+  const float s = amax > 0.f ? amax / 240.0f : 1.0f;
+#else
+  const float s = amax > 0.f ? amax / 448.0f : 1.0f;
+#endif
+  for (int32_t i = 0; i < n; ++i) codes[i] = orc_e4m3_encode((float)orc_bf16_value(y[i]) / s);
+  *scale = s;
+  return 0;
+}
+
 /* ---- sparse attention ---------------------------------------------------- */
 
 /* For query token t (sequence b, position p) the key set J is the window rows

@@ -54,6 +54,11 @@ int32_t orc_window_slots(int32_t pos, int32_t W, int32_t R, int32_t *slots);
 int32_t orc_index_scores(const orc_problem *P, const int32_t *rows, int32_t n_rows,
                          double *S /*[n_rows,N_c]*/, double *A /*[n_rows,N_c] or NULL*/);
 int32_t orc_topk_row(const double *S, int32_t n_vis, int32_t K, int32_t *idx /*[K]*/);
+int32_t orc_candidate_blocks(const double *S, int32_t n_vis, int32_t N_c, int32_t bs, int32_t topk_blocks,
+                             uint8_t *keep /*[ceil(N_c / bs)]*/);
+int32_t orc_hadamard_bf16(const uint16_t *x, int32_t n, uint16_t *y);
+uint8_t orc_e4m3_encode(float v);
+int32_t orc_act_quant_row(const uint16_t *y, int32_t n, uint8_t *codes, float *scale);
 int32_t orc_sparse_attn(const orc_problem *P, const int32_t *idx /*[T,K]*/, int32_t K,
                         const int32_t *rows, int32_t n_rows, double *O /*[n_rows,H,D]*/);
 int32_t orc_fused(const orc_problem *P, int32_t K, const int32_t *rows, int32_t n_rows,
