@@ -89,6 +89,7 @@ STAGE_SOURCES = {"idx_score": ("idx_score.cu", "idx_score_umma.cu", "umma.cuh", 
                  "idx_topk": ("idx_topk.cu", "common.cuh"),
                  "level_one": ("idx_candidates.cu", "common.cuh"),
                  "level_two": ("idx_topk.cu", "common.cuh"),
+                 "index_producer": ("idx_producer.cu", "common.cuh"),
                  "sparse_mqa": ("sparse_mqa.cu", "sparse_mqa_umma.cu", "umma.cuh", "common.cuh")}
 
 
@@ -410,6 +411,41 @@ def v41_decode(binding, torch, steps, peak):
             "note": "attention at head dim 512 runs on the warp-level bf16 MMA (mma.sync) kernel"}
 
 
+def index_producer(binding, torch, steps, peak):
+    """Device time of sa_rotate_quant (the V3.2 index producer: Hadamard
+    rotation and e4m3 block quantisation) on the rows of a 4096-token prefill
+    chunk: 64 query heads + 1 key per token = 266,240 rows of 128 bf16 values
+    (device-drawn N(0,1)); L2 flushed before each launch."""
+    rows = 4096 * 65
+    gen = torch.Generator(device="cuda").manual_seed(32)
+    x = torch.empty((rows, 128), dtype=torch.bfloat16, device="cuda").normal_(generator=gen)
+    codes = torch.empty((rows, 128), dtype=torch.uint8, device="cuda")
+    scales = torch.empty(rows, dtype=torch.float32, device="cuda")
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    binding.sa_workspace_init(ws)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        binding.sa_rotate_quant(x, rows, codes, scales, ws)
+    n, tot = max(5, steps), 0.0
+    for _ in range(n):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        binding.sa_rotate_quant(x, rows, codes, scales, ws)
+        e1.record()
+        torch.cuda.synchronize()
+        tot += e0.elapsed_time(e1)
+    if binding.sa_check_device_status(ws) != binding.SA_OK:
+        raise RuntimeError("device status not OK after the index producer")
+    us = tot / n * 1000.0
+    alg = rows * (128 * 2 + 128 + 4)
+    gbs = alg / (us / 1e6) / 1e9
+    return {"workload": "rows of a 4096-token prefill chunk: 64 query heads + 1 key, 128 bf16 each "
+                        "(266,240 rows); L2 flushed per launch",
+            "us": round(us, 2), "algorithmic_bytes": alg, "GB_s": round(gbs, 1),
+            "frac_of_hbm_peak": round(gbs / peak, 4), "traffic": recorded_traffic("index_producer", "prefill")}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -634,6 +670,7 @@ def run_ours(args):
     clocks = sampler.summary(t_soak, t_end)
     two_level = None if args.no_two_level else two_level_topk(binding, torch, wl, args.steps, peak)
     v41 = None if args.no_v41 else v41_decode(binding, torch, args.steps, peak)
+    producer = index_producer(binding, torch, args.steps, peak)
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -663,6 +700,7 @@ def run_ours(args):
         "clocks": clocks,
         "two_level_topk": two_level,
         "v41_decode": v41,
+        "index_producer": producer,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)

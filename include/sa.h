@@ -179,6 +179,24 @@ SA_API sa_status sa_topk_candidates(const float *scores, const sa_index_args *ia
                                     const uint32_t *cand, int32_t block_size, int32_t *idx, void *ws,
                                     size_t ws_bytes, sa_stream_t stream);
 
+/* Index producer of the uncompressed indexer ("DeepSeek-V3.2-Exp
+ * inference/model.py", Indexer.forward: rotate_activation, act_quant of q and
+ * k, the k_cache / k_scale_cache write).  For each row r of x ([rows, dim]
+ * bf16, dim 128): y = bf16(H x_r * 128^-1/2), H the Sylvester-Hadamard matrix
+ * (H[i][j] = (-1)^popcount(i & j)), computed in fp32 by the butterfly stages
+ * h = 1, 2, ..., 64 in that order; then scale = amax|y| / 448 (fp32; 1 for an
+ * all-zero row) and codes = float8 e4m3fn of y / scale (nearest, ties to
+ * even, saturating at +-448).  The codes and the scale go to row d of codes
+ * ([*, 128] uint8) and scales ([*] fp32), with d = r when dst is NULL and
+ * d = dst[r] otherwise (e.g. b * N_c + position for the index key cache of r =
+ * 1); a d outside [0, dst_rows) is skipped and flagged (sa_check_device_status
+ * reports SA_ERR_DEVICE_DATA).  x 16-byte aligned; codes, scales and dst 4-byte
+ * aligned; dim other than 128 returns SA_ERR_UNSUPPORTED.  The workspace needs
+ * only its 256-byte header.  Feeding the codes and scales to sa_indexer_scores
+ * (fp8 queries with q_scale, fp8 keys with k_scale) gives the V3.2 index score. */
+SA_API sa_status sa_rotate_quant(const void *x, int32_t rows, int32_t dim, const int32_t *dst, int64_t dst_rows,
+                                 uint8_t *codes, float *scales, void *ws, size_t ws_bytes, sa_stream_t stream);
+
 /* Sparse MQA over the window and the selected compressed rows
  * ("DeepSeek-V4.1-Flash-NVFP4 inference/model.py", Attention.forward and
  * sparse_attn): for token t and head h the keys are the window rows then the

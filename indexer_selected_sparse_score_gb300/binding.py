@@ -58,7 +58,7 @@ class AttnArgs(ctypes.Structure):
 
 
 EXPORTED = ("sa_workspace_size", "sa_workspace_init", "sa_indexer_scores", "sa_topk",
-            "sa_candidate_blocks", "sa_candidate_words", "sa_topk_candidates",
+            "sa_candidate_blocks", "sa_candidate_words", "sa_topk_candidates", "sa_rotate_quant",
             "sa_sparse_attn", "sa_fused_decode", "sa_fused_decode_staged",
             "sa_fused_decode_launch_count", "sa_check_device_status", "sa_status_string",
             "sa_last_error_detail")
@@ -86,6 +86,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.sa_candidate_words.argtypes = [i32, i32]
     lib.sa_candidate_words.restype = i32
     lib.sa_topk_candidates.argtypes = [vp, IA, i32, vp, i32, vp, vp, sz, vp]
+    lib.sa_rotate_quant.argtypes = [vp, i32, i32, vp, ctypes.c_int64, vp, vp, vp, sz, vp]
     lib.sa_sparse_attn.argtypes = [IA, AA, vp, i32, vp, vp, sz, vp]
     lib.sa_fused_decode.argtypes = [IA, AA, i32, vp, vp, vp, sz, vp]
     lib.sa_fused_decode_staged.argtypes = [IA, AA, i32, vp, vp, vp, sz, vp, ctypes.POINTER(vp)]
@@ -98,7 +99,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.sa_status_string.restype = ctypes.c_char_p
     lib.sa_last_error_detail.restype = ctypes.c_char_p
     for name in ("sa_workspace_init", "sa_indexer_scores", "sa_topk", "sa_candidate_blocks",
-                 "sa_topk_candidates", "sa_sparse_attn",
+                 "sa_topk_candidates", "sa_rotate_quant", "sa_sparse_attn",
                  "sa_fused_decode", "sa_fused_decode_staged", "sa_check_device_status"):
         getattr(lib, name).restype = i32
     if path == LIB:
@@ -170,6 +171,14 @@ def sa_topk_candidates(scores, ia: IndexArgs, K: int, cand, block_size: int, idx
     p, n = _ws(ws)
     _check(load().sa_topk_candidates(_p(scores), ctypes.byref(ia), K, _p(cand), block_size, _p(idx), p, n,
                                      _s(stream)))
+
+
+def sa_rotate_quant(x, rows: int, codes, scales, ws, dst=None, dst_rows: int = 0, dim: int = 128,
+                    stream=None) -> None:
+    """V3.2 index producer: Hadamard rotation and e4m3 block quantisation of
+    ``rows`` rows of 128 bf16 values; row r lands at row ``dst[r]`` when given."""
+    p, n = _ws(ws)
+    _check(load().sa_rotate_quant(_p(x), rows, dim, _p(dst), dst_rows, _p(codes), _p(scales), p, n, _s(stream)))
 
 
 def sa_sparse_attn(ia: IndexArgs, aa: AttnArgs, idx, K: int, out, ws, stream=None) -> None:

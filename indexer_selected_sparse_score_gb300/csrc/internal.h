@@ -56,6 +56,11 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const sa_index_args &ia
 // candidate blocks ([T, candidate_words(N_c, block_size)] uint32).
 int candidate_words(int N_c, int block_size);
 constexpr int kMaxCandidateBlocks = 32768;
+// Index producer of the uncompressed indexer: Hadamard rotation and e4m3
+// block quantisation of rows of 128 bf16 values, optionally scattered to
+// rows dst[r] of the destination.
+cudaError_t launch_rotate_quant(const void *x, int rows, const int32_t *dst, int64_t dst_rows, uint8_t *codes,
+                                float *scales, uint32_t *status, cudaStream_t stream);
 cudaError_t launch_candidate_blocks(const float *scores, int64_t ld, const sa_index_args &ia, int block_size,
                                    int topk_blocks, uint32_t *cand, uint32_t *status, cudaStream_t stream);
 

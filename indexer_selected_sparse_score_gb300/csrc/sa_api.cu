@@ -202,6 +202,21 @@ sa_status sa_topk(const float *scores, const sa_index_args *ia, int32_t K, int32
   return e == cudaSuccess ? SA_OK : cuda_fail(e, "top-k launch");
 }
 
+sa_status sa_rotate_quant(const void *x, int32_t rows, int32_t dim, const int32_t *dst, int64_t dst_rows,
+                          uint8_t *codes, float *scales, void *ws, size_t ws_bytes, sa_stream_t stream) {
+  if (rows < 0) return fail(SA_ERR_INVALID_ARG, "rows must be >= 0 (got %d)", rows);
+  if (dim != 128) return fail(SA_ERR_UNSUPPORTED, "row length %d: the producer takes rows of 128", dim);
+  if (dst && dst_rows < 0) return fail(SA_ERR_INVALID_ARG, "dst_rows must be >= 0");
+  if (rows > 0 && (!x || !codes || !scales))
+    return fail(SA_ERR_INVALID_ARG, "x, codes and scales must be device pointers");
+  if (!aligned16(x) || !aligned4(codes) || !aligned4(scales) || !aligned4(dst))
+    return fail(SA_ERR_INVALID_ARG, "x must be 16-byte aligned; codes, scales and dst 4-byte aligned");
+  if (sa_status s = check_ws(ws, ws_bytes, 256)) return s;
+  cudaError_t e = sa::launch_rotate_quant(x, rows, dst, dst_rows, codes, scales, at<uint32_t>(ws, 0),
+                                          reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SA_OK : cuda_fail(e, "rotate-quant launch");
+}
+
 int32_t sa_candidate_words(int32_t N_c, int32_t block_size) {
   if (N_c < 1 || block_size < 1) return 0;
   return sa::candidate_words(N_c, block_size);

@@ -163,3 +163,24 @@ def test_attention_head_dims(lib):
     assert lib.sa_workspace_size(ctypes.byref(_ia()), ctypes.byref(_aa(H=16, D=512)), 8) > 0
     assert _call_fused(lib, _ia(), _aa(H=128, D=512)) == binding.SA_ERR_UNSUPPORTED
     assert _call_fused(lib, _ia(), _aa(H=64, D=256)) == binding.SA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(rows=-1), binding.SA_ERR_INVALID_ARG),
+    (dict(dim=64), binding.SA_ERR_UNSUPPORTED),
+    (dict(x=None), binding.SA_ERR_INVALID_ARG),
+    (dict(x=264), binding.SA_ERR_INVALID_ARG),          # not 16-byte aligned
+    (dict(codes=258), binding.SA_ERR_INVALID_ARG),
+    (dict(dst=256, dst_rows=-1), binding.SA_ERR_INVALID_ARG),
+    (dict(ws=None), binding.SA_ERR_WORKSPACE),
+])
+def test_rotate_quant_rejects_bad_arguments(lib, kw, status):
+    a = dict(x=256, rows=4, dim=128, dst=None, dst_rows=0, codes=256, scales=256, ws=256, ws_bytes=256)
+    a.update(kw)
+    st = lib.sa_rotate_quant(a["x"], a["rows"], a["dim"], a["dst"], a["dst_rows"], a["codes"], a["scales"],
+                             a["ws"], a["ws_bytes"], None)
+    assert st == status
+
+
+def test_rotate_quant_with_no_rows_enqueues_nothing(lib):
+    assert lib.sa_rotate_quant(None, 0, 128, None, 0, None, None, 256, 256, None) == binding.SA_OK
