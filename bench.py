@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--no-two-level", action="store_true", help="skip the two-level top-k measurement")
     ap.add_argument("--no-v41", action="store_true", help="skip the V4.1-shape measurement")
     ap.add_argument("--v41-only", action="store_true", help="print only the V4.1-shape measurement")
+    ap.add_argument("--producer-only", action="store_true", help="print only the index-producer measurement")
     return ap.parse_args()
 
 
@@ -463,6 +464,10 @@ def run_ours(args):
         dist.barrier()
     binding.load()
 
+    if args.producer_only:
+        if rank == 0:
+            print(json.dumps({"index_producer": index_producer(binding, torch, args.steps, peaks()[0])}), flush=True)
+        return
     if args.v41_only:
         if rank == 0:
             print(json.dumps({"v41_decode": v41_decode(binding, torch, args.steps, peaks()[0])}), flush=True)
