@@ -93,6 +93,10 @@ def _lib(mutant: int = 0, path: Optional[str] = None):
         lib.orc_e4m3_encode.restype = ctypes.c_uint8
         lib.orc_act_quant_row.argtypes = [vp, i32, vp, vp]
         lib.orc_act_quant_row.restype = i32
+        lib.orc_compress_prefill.argtypes = [vp, vp, i32, i32, i32, vp, ctypes.c_double, vp, vp, vp]
+        lib.orc_compress_prefill.restype = i32
+        lib.orc_compress_decode.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, ctypes.c_double, vp]
+        lib.orc_compress_decode.restype = i32
         lib.orc_candidate_blocks.restype = i32
         lib.orc_sparse_attn.argtypes = [P, vp, i32, vp, i32, vp]
         lib.orc_sparse_attn.restype = i32
@@ -276,6 +280,50 @@ def act_quant_rows(y_bits: np.ndarray, mutant: int = 0):
 def rotate_quant_rows(x_bits: np.ndarray, mutant: int = 0):
     """The V3.2 index producer on rows of bf16 bits: rotation, then act_quant."""
     return act_quant_rows(hadamard_bf16(x_bits, mutant), mutant)
+
+
+class CompressorState:
+    """The partial group a compressor carries across decode steps (kv_state,
+    score_state of "DeepSeek-V4.1-Flash-NVFP4 inference/model.py", Compressor)."""
+
+    def __init__(self, r: int, D: int):
+        self.kv = np.zeros((r, D), dtype=np.float32)
+        self.score = np.full((r, D), -np.inf, dtype=np.float32)
+
+
+def compress_prefill(kv: np.ndarray, score: np.ndarray, r: int, weight: np.ndarray, eps: float,
+                     state: Optional[CompressorState] = None, mutant: int = 0) -> np.ndarray:
+    """Compressor.forward from position 0 on one sequence: kv, score [S, D] fp32;
+    returns the S // r pooled, normalised rows [S // r, D] (float64, before the
+    cast); the trailing S % r tokens go to ``state``."""
+    kv = np.ascontiguousarray(kv, dtype=np.float32)
+    score = np.ascontiguousarray(score, dtype=np.float32)
+    w = np.ascontiguousarray(weight, dtype=np.float32)
+    S, D = kv.shape
+    out = np.empty((max(S // r, 1), D), dtype=np.float64)
+    ks = state.kv.ctypes.data if state is not None else None
+    ss = state.score.ctypes.data if state is not None else None
+    g = _lib(mutant).orc_compress_prefill(kv.ctypes.data, score.ctypes.data, S, D, r, w.ctypes.data, eps,
+                                          out.ctypes.data, ks, ss)
+    if g < 0:
+        raise ValueError("oracle: invalid compressor arguments")
+    return out[:g]
+
+
+def compress_decode(kv_tok: np.ndarray, score_tok: np.ndarray, pos: int, r: int, weight: np.ndarray, eps: float,
+                    state: CompressorState, mutant: int = 0) -> Optional[np.ndarray]:
+    """One Compressor.forward decode step at position ``pos``: the pooled row [D]
+    when the group completes, else None."""
+    kv_tok = np.ascontiguousarray(kv_tok, dtype=np.float32)
+    score_tok = np.ascontiguousarray(score_tok, dtype=np.float32)
+    w = np.ascontiguousarray(weight, dtype=np.float32)
+    D = kv_tok.shape[0]
+    out = np.empty(D, dtype=np.float64)
+    rc = _lib(mutant).orc_compress_decode(kv_tok.ctypes.data, score_tok.ctypes.data, pos, D, r, state.kv.ctypes.data,
+                                          state.score.ctypes.data, w.ctypes.data, eps, out.ctypes.data)
+    if rc < 0:
+        raise ValueError("oracle: invalid compressor arguments")
+    return out if rc == 1 else None
 
 
 def sparse_attn(p: Problem, idx: np.ndarray, rows=None, mutant: int = 0) -> np.ndarray:

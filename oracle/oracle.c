@@ -365,6 +365,94 @@ int32_t orc_act_quant_row(const uint16_t *y, int32_t n, uint8_t *codes, float *s
   return 0;
 }
 
+/* ---- V4.1 compressor: gated pooling of r tokens, then RMSNorm ------------- */
+
+/* "DeepSeek-V4.1-Flash-NVFP4 inference/model.py", RMSNorm.forward: c times
+ * (mean over the D channels of c^2 + eps)^-1/2, times weight. */
+static void rms_norm(double *c, int32_t D, const float *weight, double eps) {
+  double ss = 0.0;
+  for (int32_t d = 0; d < D; ++d) ss += c[d] * c[d];
+#if ORC_MUTANT == 16
+  const double inv = 1.0 / sqrt(ss + eps); /* sum instead of mean */
+#else
+  const double inv = 1.0 / sqrt(ss / (double)D + eps);
+#endif
+  for (int32_t d = 0; d < D; ++d) c[d] = c[d] * inv * (double)weight[d];
+}
+
+/* One group (same page, Compressor.forward): for every channel d, the r
+ * tokens' kv values weighted by the softmax over the r tokens of their gate
+ * scores, summed; rounded to bf16 (the cast to the activation dtype); then
+ * rms_norm.  kv, score: [r, D] with row stride ld. */
+static void pool_group(const float *kv, const float *score, int64_t ld, int32_t D, int32_t r, const float *weight,
+                       double eps, double *out) {
+#if ORC_MUTANT == 15
+  /* softmax over the channels of each token instead of over the tokens */
+  for (int32_t d = 0; d < D; ++d) out[d] = 0.0;
+  for (int32_t j = 0; j < r; ++j) {
+    double m = -INFINITY, z = 0.0;
+    for (int32_t d = 0; d < D; ++d) m = fmax(m, (double)score[j * ld + d]);
+    for (int32_t d = 0; d < D; ++d) z += exp((double)score[j * ld + d] - m);
+    for (int32_t d = 0; d < D; ++d) out[d] += (double)kv[j * ld + d] * exp((double)score[j * ld + d] - m) / z;
+  }
+#else
+  for (int32_t d = 0; d < D; ++d) {
+    double m = -INFINITY, z = 0.0, acc = 0.0;
+    for (int32_t j = 0; j < r; ++j) m = fmax(m, (double)score[j * ld + d]);
+    for (int32_t j = 0; j < r; ++j) {
+      const double e = exp((double)score[j * ld + d] - m);
+      z += e;
+      acc += e * (double)kv[j * ld + d];
+    }
+    out[d] = acc / z;
+  }
+#endif
+  /* the pooled row is cast to the activation dtype (bf16) before the norm:
+   * Compressor.forward returns norm(kv.to(dtype)) */
+  for (int32_t d = 0; d < D; ++d) out[d] = orc_bf16_value(bf16_nearest((float)out[d]));
+  rms_norm(out, D, weight, eps);
+}
+
+/* Prefill of one sequence from position 0 (Compressor.forward, start_pos == 0):
+ * kv and score [S, D] (the fp32 projections wkv(x), wgate(x)); ratio r >= 2.
+ * Writes the S / r complete groups to out [S / r, D] (before the cast to the
+ * activation dtype) and the trailing S % r tokens to slots 0 .. S % r - 1 of
+ * the state [r, D] (kv_state, score_state; may be NULL).  Returns S / r. */
+int32_t orc_compress_prefill(const float *kv, const float *score, int32_t S, int32_t D, int32_t r,
+                             const float *weight, double eps, double *out, float *kv_state, float *score_state) {
+  if (S < 0 || D < 1 || r < 2) return -1;
+  const int32_t G = S / r;
+  for (int32_t g = 0; g < G; ++g)
+    pool_group(kv + (int64_t)g * r * D, score + (int64_t)g * r * D, D, D, r, weight, eps, out + (int64_t)g * D);
+  if (kv_state && score_state)
+    for (int32_t j = 0; j < S - G * r; ++j)
+      for (int32_t d = 0; d < D; ++d) {
+        kv_state[(int64_t)j * D + d] = kv[((int64_t)G * r + j) * D + d];
+        score_state[(int64_t)j * D + d] = score[((int64_t)G * r + j) * D + d];
+      }
+  return G;
+}
+
+/* One decode step at absolute position pos (start_pos > 0): the token goes to
+ * slot pos % r of the state; when the group just completed ((pos + 1) % r ==
+ * 0) the state's r slots are pooled into out [D] and 1 is returned, else 0. */
+int32_t orc_compress_decode(const float *kv_tok, const float *score_tok, int32_t pos, int32_t D, int32_t r,
+                            float *kv_state, float *score_state, const float *weight, double eps, double *out) {
+  if (pos < 0 || D < 1 || r < 2) return -1;
+#if ORC_MUTANT == 17
+  const int32_t slot = (pos + 1) % r;
+#else
+  const int32_t slot = pos % r;
+#endif
+  for (int32_t d = 0; d < D; ++d) {
+    kv_state[(int64_t)slot * D + d] = kv_tok[d];
+    score_state[(int64_t)slot * D + d] = score_tok[d];
+  }
+  if ((pos + 1) % r != 0) return 0;
+  pool_group(kv_state, score_state, D, D, r, weight, eps, out);
+  return 1;
+}
+
 /* ---- sparse attention ---------------------------------------------------- */
 
 /* For query token t (sequence b, position p) the key set J is the window rows

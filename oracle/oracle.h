@@ -59,6 +59,10 @@ int32_t orc_candidate_blocks(const double *S, int32_t n_vis, int32_t N_c, int32_
 int32_t orc_hadamard_bf16(const uint16_t *x, int32_t n, uint16_t *y);
 uint8_t orc_e4m3_encode(float v);
 int32_t orc_act_quant_row(const uint16_t *y, int32_t n, uint8_t *codes, float *scale);
+int32_t orc_compress_prefill(const float *kv, const float *score, int32_t S, int32_t D, int32_t r,
+                             const float *weight, double eps, double *out, float *kv_state, float *score_state);
+int32_t orc_compress_decode(const float *kv_tok, const float *score_tok, int32_t pos, int32_t D, int32_t r,
+                            float *kv_state, float *score_state, const float *weight, double eps, double *out);
 int32_t orc_sparse_attn(const orc_problem *P, const int32_t *idx /*[T,K]*/, int32_t K,
                         const int32_t *rows, int32_t n_rows, double *O /*[n_rows,H,D]*/);
 int32_t orc_fused(const orc_problem *P, int32_t K, const int32_t *rows, int32_t n_rows,
