@@ -197,6 +197,18 @@ SA_API sa_status sa_topk_candidates(const float *scores, const sa_index_args *ia
 SA_API sa_status sa_rotate_quant(const void *x, int32_t rows, int32_t dim, const int32_t *dst, int64_t dst_rows,
                                  uint8_t *codes, float *scales, void *ws, size_t ws_bytes, sa_stream_t stream);
 
+/* Compressor from position 0 ("DeepSeek-V4.1-Flash-NVFP4 inference/model.py",
+ * Compressor.forward with start_pos 0, and RMSNorm.forward).  kv and score:
+ * [B, S, D] fp32 (the projections wkv(x) and wgate(x)); for sequence b and
+ * group g < S / r (tokens g*r .. g*r + r - 1):
+ *   c[d] = bf16( sum_j softmax_j(score[b, g*r + j, d]) kv[b, g*r + j, d] )
+ *   out[b, g, d] = bf16( weight[d] * c[d] / sqrt(mean_d c[d]^2 + eps) )
+ * in fp32.  out: [B, S / r, D] bf16.  The trailing S % r tokens are not read:
+ * the caller keeps them as the partial group that decode steps complete.
+ * r >= 2; D a multiple of 32 in [32, 1024]; B <= 65535; eps >= 0. */
+SA_API sa_status sa_compress_prefill(const float *kv, const float *score, int32_t B, int32_t S, int32_t D, int32_t r,
+                                     const float *weight, float eps, void *out, sa_stream_t stream);
+
 /* Sparse MQA over the window and the selected compressed rows
  * ("DeepSeek-V4.1-Flash-NVFP4 inference/model.py", Attention.forward and
  * sparse_attn): for token t and head h the keys are the window rows then the

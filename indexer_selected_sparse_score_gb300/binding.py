@@ -59,6 +59,7 @@ class AttnArgs(ctypes.Structure):
 
 EXPORTED = ("sa_workspace_size", "sa_workspace_init", "sa_indexer_scores", "sa_topk",
             "sa_candidate_blocks", "sa_candidate_words", "sa_topk_candidates", "sa_rotate_quant",
+            "sa_compress_prefill",
             "sa_sparse_attn", "sa_fused_decode", "sa_fused_decode_staged",
             "sa_fused_decode_launch_count", "sa_check_device_status", "sa_status_string",
             "sa_last_error_detail")
@@ -87,6 +88,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.sa_candidate_words.restype = i32
     lib.sa_topk_candidates.argtypes = [vp, IA, i32, vp, i32, vp, vp, sz, vp]
     lib.sa_rotate_quant.argtypes = [vp, i32, i32, vp, ctypes.c_int64, vp, vp, vp, sz, vp]
+    lib.sa_compress_prefill.argtypes = [vp, vp, i32, i32, i32, i32, vp, ctypes.c_float, vp, vp]
     lib.sa_sparse_attn.argtypes = [IA, AA, vp, i32, vp, vp, sz, vp]
     lib.sa_fused_decode.argtypes = [IA, AA, i32, vp, vp, vp, sz, vp]
     lib.sa_fused_decode_staged.argtypes = [IA, AA, i32, vp, vp, vp, sz, vp, ctypes.POINTER(vp)]
@@ -99,7 +101,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.sa_status_string.restype = ctypes.c_char_p
     lib.sa_last_error_detail.restype = ctypes.c_char_p
     for name in ("sa_workspace_init", "sa_indexer_scores", "sa_topk", "sa_candidate_blocks",
-                 "sa_topk_candidates", "sa_rotate_quant", "sa_sparse_attn",
+                 "sa_topk_candidates", "sa_rotate_quant", "sa_compress_prefill", "sa_sparse_attn",
                  "sa_fused_decode", "sa_fused_decode_staged", "sa_check_device_status"):
         getattr(lib, name).restype = i32
     if path == LIB:
@@ -179,6 +181,11 @@ def sa_rotate_quant(x, rows: int, codes, scales, ws, dst=None, dst_rows: int = 0
     ``rows`` rows of 128 bf16 values; row r lands at row ``dst[r]`` when given."""
     p, n = _ws(ws)
     _check(load().sa_rotate_quant(_p(x), rows, dim, _p(dst), dst_rows, _p(codes), _p(scales), p, n, _s(stream)))
+
+
+def sa_compress_prefill(kv, score, B: int, S: int, D: int, r: int, weight, eps: float, out, stream=None) -> None:
+    """V4.1 compressor from position 0: [B, S // r, D] bf16 pooled, normalised rows."""
+    _check(load().sa_compress_prefill(_p(kv), _p(score), B, S, D, r, _p(weight), eps, _p(out), _s(stream)))
 
 
 def sa_sparse_attn(ia: IndexArgs, aa: AttnArgs, idx, K: int, out, ws, stream=None) -> None:

@@ -61,6 +61,9 @@ constexpr int kMaxCandidateBlocks = 32768;
 // rows dst[r] of the destination.
 cudaError_t launch_rotate_quant(const void *x, int rows, const int32_t *dst, int64_t dst_rows, uint8_t *codes,
                                 float *scales, uint32_t *status, cudaStream_t stream);
+// V4.1 compressor from position 0: S / r pooled, normalised bf16 rows per sequence.
+cudaError_t launch_compress_prefill(const float *kv, const float *score, int B, int S, int D, int r,
+                                    const float *weight, float eps, void *out, cudaStream_t stream);
 cudaError_t launch_candidate_blocks(const float *scores, int64_t ld, const sa_index_args &ia, int block_size,
                                    int topk_blocks, uint32_t *cand, uint32_t *status, cudaStream_t stream);
 

@@ -202,6 +202,21 @@ sa_status sa_topk(const float *scores, const sa_index_args *ia, int32_t K, int32
   return e == cudaSuccess ? SA_OK : cuda_fail(e, "top-k launch");
 }
 
+sa_status sa_compress_prefill(const float *kv, const float *score, int32_t B, int32_t S, int32_t D, int32_t r,
+                              const float *weight, float eps, void *out, sa_stream_t stream) {
+  if (B < 0 || S < 0 || B > 65535) return fail(SA_ERR_INVALID_ARG, "need 0 <= B <= 65535 and S >= 0");
+  if (r < 2) return fail(SA_ERR_INVALID_ARG, "compression ratio must be >= 2 (got %d)", r);
+  if (D < 32 || D > 1024 || D % 32) return fail(SA_ERR_UNSUPPORTED, "head dim %d: need a multiple of 32 in [32, 1024]", D);
+  if (!std::isfinite(eps) || eps < 0.f) return fail(SA_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (B > 0 && S >= r && (!kv || !score || !weight || !out))
+    return fail(SA_ERR_INVALID_ARG, "kv, score, weight and out must be device pointers");
+  if (!aligned4(kv) || !aligned4(score) || !aligned4(weight) || !aligned4(out))
+    return fail(SA_ERR_INVALID_ARG, "kv, score, weight and out must be 4-byte aligned");
+  cudaError_t e = sa::launch_compress_prefill(kv, score, B, S, D, r, weight, eps, out,
+                                              reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SA_OK : cuda_fail(e, "compressor launch");
+}
+
 sa_status sa_rotate_quant(const void *x, int32_t rows, int32_t dim, const int32_t *dst, int64_t dst_rows,
                           uint8_t *codes, float *scales, void *ws, size_t ws_bytes, sa_stream_t stream) {
   if (rows < 0) return fail(SA_ERR_INVALID_ARG, "rows must be >= 0 (got %d)", rows);

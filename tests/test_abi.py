@@ -184,3 +184,24 @@ def test_rotate_quant_rejects_bad_arguments(lib, kw, status):
 
 def test_rotate_quant_with_no_rows_enqueues_nothing(lib):
     assert lib.sa_rotate_quant(None, 0, 128, None, 0, None, None, 256, 256, None) == binding.SA_OK
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(r=1), binding.SA_ERR_INVALID_ARG),
+    (dict(D=48), binding.SA_ERR_UNSUPPORTED),
+    (dict(D=2048), binding.SA_ERR_UNSUPPORTED),
+    (dict(B=70000), binding.SA_ERR_INVALID_ARG),
+    (dict(eps=float("nan")), binding.SA_ERR_INVALID_ARG),
+    (dict(kv=None), binding.SA_ERR_INVALID_ARG),
+    (dict(out=258), binding.SA_ERR_INVALID_ARG),
+])
+def test_compress_prefill_rejects_bad_arguments(lib, kw, status):
+    a = dict(kv=256, score=256, B=2, S=8, D=64, r=4, weight=256, eps=1e-6, out=256)
+    a.update(kw)
+    st = lib.sa_compress_prefill(a["kv"], a["score"], a["B"], a["S"], a["D"], a["r"], a["weight"], a["eps"], a["out"],
+                                 None)
+    assert st == status
+
+
+def test_compress_prefill_with_no_group_enqueues_nothing(lib):
+    assert lib.sa_compress_prefill(None, None, 2, 3, 64, 4, None, 1e-6, None, None) == binding.SA_OK
