@@ -53,6 +53,18 @@ def parse():
     return ap.parse_args()
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest of every rank's value (a job's time is its slowest rank's);
+    the value itself without an initialised process group of several ranks."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
@@ -541,11 +553,7 @@ def run_ours(args):
         dist.barrier()
     t_end = time.time()
     sampler.stop()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        tt = torch.tensor([ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), "cuda")
     ms_per_step = ms / args.steps
     value = w.T * world * args.steps / (ms / 1000.0)
 
@@ -654,11 +662,7 @@ def run_ours(args):
     stream.wait_stream(down_stream)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), "cuda")
     e2e_value = w.T * world * args.steps / (e2e_ms / 1000.0)
 
     # ---- roofline of the dominant kernel

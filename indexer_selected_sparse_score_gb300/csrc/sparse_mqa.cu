@@ -4,12 +4,14 @@
 // cat(window_idxs, compress_idxs + offset), sparse_attn(q, kv, attn_sink,
 // topk_idxs, softmax_scale); one shared KV head serves every query head).
 //
-// CUDA-core kernel (head dim 128 with head counts other than 64, and head dim
-// 512 -- the released V4.1 shape; the tensor-core kernel for 64 heads of dim
-// 128 is in sparse_mqa_umma.cu): one CTA per (token, split).  The token's key
-// list is its window rows (oldest first) followed by its K index slots; a
-// split takes a contiguous chunk of that list.  When K and V are one tensor
-// (V4.1's single kv), each row is loaded once and serves as both tiles.  Rows are gathered 16 bytes per thread,
+// Two kernels here: the CUDA-core kernel (head dim 128 with head counts other
+// than 64; the tcgen05 kernel for 64 heads of dim 128 is in
+// sparse_mqa_umma.cu) and, further down, the warp-level MMA kernel for head
+// dim 512 (the released V4.1 shape).  Both run one CTA per (token, split).
+// The token's key list is its window rows (oldest first) followed by its K
+// index slots; a split takes a contiguous chunk of that list.  When K and V
+// are one tensor (V4.1's single kv), each row is loaded once and serves as
+// both tiles.  Rows are gathered 16 bytes per thread,
 // logits and the online softmax run in fp32 in the log2 domain (logits are
 // pre-multiplied by scale * log2(e)), and each split leaves (m, l, o) partials
 // that the combine kernel merges.  A single split writes the output directly.
@@ -19,9 +21,11 @@
 namespace sa {
 namespace {
 
-constexpr int kKeyTile = 32;  // keys per tile (16 for dim 512 with separate K and V)
+constexpr int kKeyTile = 32;  // keys per tile
 
-// Launch shape per head dim: threads per CTA and keys per tile.
+// Launch shape of the CUDA-core kernel per head dim: threads per CTA and keys
+// per tile (a dim-512 form, 512 threads with 16-key tiles when K and V are
+// separate, fits the shared memory; dim 512 is served by the MMA kernel).
 template <int D, bool kSameKV>
 struct AttnShape {
   static constexpr int kThreads = D == 512 ? 512 : 256;
