@@ -7,8 +7,9 @@ IEEE double); this file compiles it with gcc and marshals numpy arrays.
 
 Pages followed (title, section): "DeepSeek-V4.1-Flash-NVFP4 inference/model.py"
 (Indexer.forward, get_window_topk_idxs, Attention._window_kv,
-Attention.forward) and "DeepSeek-V3.2-Exp inference/model.py"
-(Indexer.forward with fp8 keys and per-position scales).
+Attention.forward, select_candidate_blocks, Compressor.forward, RMSNorm.forward)
+and "DeepSeek-V3.2-Exp inference/model.py" (Indexer.forward with fp8 keys and
+per-position scales; rotate_activation and act_quant).
 """
 from __future__ import annotations
 

@@ -19,7 +19,11 @@
  *    rows concatenated with the selected compressed rows.
  *  - "DeepSeek-V3.2-Exp inference/model.py", Indexer.forward: fp8-e4m3 index
  *    keys with one fp32 scale per position (head_dim 128 = one block), and
- *    fp8 queries with a per-(token, head) scale folded into the weights.
+ *    fp8 queries with a per-(token, head) scale folded into the weights;
+ *    rotate_activation and act_quant, the producer of those codes and scales.
+ *  - "DeepSeek-V4.1-Flash-NVFP4 inference/model.py", select_candidate_blocks
+ *    (level one of the two-level top-k) and its use in Indexer.forward;
+ *    Compressor.forward with RMSNorm.forward (gated pooling of r tokens).
  *
  * Readings where the pages are silent (each listed in the design notes):
  *  - scales are dequantisation multipliers: q_hat = q * q_scale[t,h],
@@ -28,7 +32,10 @@
  *  - ties in the top-k go to the lower position;
  *  - the optional attention sink adds exp(sink_h - m) to the softmax
  *    denominator only (parity unpinned: the formula is not on the pages);
- *  - window rows and compressed rows are concatenated, never de-duplicated.
+ *  - window rows and compressed rows are concatenated, never de-duplicated;
+ *  - where floating point decides an integer (the fp8 codes of the producer),
+ *    the oracle takes that step in the precision the kernel takes it (fp32,
+ *    in a fixed butterfly order) so that the codes compare exactly.
  *
  * Compile-time ORC_MUTANT=n builds deliberately wrong variants; the pin tests
  * build them to show that each plausible mistake fails at least one pin.  The
