@@ -15,7 +15,7 @@ What the pins rest on:
     permutation invariance;
   * top-k: brute force by Python sorting, with planted ties;
   * attention: a second, dense-masked formulation (the V3.2 page's
-    index_mask form) in numpy, the benchmark spec's identity that keeping every
+    index_mask form) in numpy, the identity that keeping every
     visible position equals dense attention over window + all visible
     compressed rows, V = 1 giving 1 (weights sum to one), W=1/K=0 giving the
     query's own V row, Q = 0 giving the plain mean of V.
@@ -96,7 +96,7 @@ def pin_window_golden(mutant=0):
 
 def pin_visibility_forms(mutant=0):
     """Both forms the V4.1 page gives for the visible compressed count, and the
-    the benchmark spec form (j+1)*r <= t+1, for every t < 64 and r in 1..8."""
+    per-entry form (j+1)*r <= t+1, for every t < 64 and r in 1..8."""
     for r in range(1, 9):
         seqlen = 64
         # prefill form: query i sees positions j < (i+1)//r among seqlen//r
@@ -280,7 +280,7 @@ def pin_attn_sink_dense(mutant=0):
 
 
 def pin_attn_all_visible_identity(mutant=0):
-    """The benchmark spec check 2: with K >= n_vis the selected set is every visible
+    """With K >= n_vis the selected set is every visible
     position, so the step equals dense attention over the window plus all
     visible compressed rows."""
     w = _tiny_attn(41, r=2, W=4, N_c=8, pos_lo=3)
@@ -295,7 +295,7 @@ def pin_attn_all_visible_identity(mutant=0):
 
 
 def pin_attn_weights_sum_to_one(mutant=0):
-    """The benchmark spec check 3: with every V row equal to 1 the output is exactly the
+    """With every V row equal to 1 the output is exactly the
     sum of the softmax weights, which must be 1."""
     w = _tiny_attn(51)
     one = wl.to_bf16_bits(np.ones(1, dtype=np.float32))[0]
