@@ -98,6 +98,11 @@ def _lib(mutant: int = 0, path: Optional[str] = None):
         lib.orc_compress_prefill.restype = i32
         lib.orc_compress_decode.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, ctypes.c_double, vp]
         lib.orc_compress_decode.restype = i32
+        lib.orc_rope_angle.argtypes = [i32, i32, ctypes.c_int64, ctypes.c_double, ctypes.c_double, i32,
+                                       ctypes.c_double, ctypes.c_double]
+        lib.orc_rope_angle.restype = ctypes.c_double
+        lib.orc_apply_rope.argtypes = [vp, i32, ctypes.c_int64, ctypes.c_double, ctypes.c_double, i32,
+                                       ctypes.c_double, ctypes.c_double, i32]
         lib.orc_candidate_blocks.restype = i32
         lib.orc_sparse_attn.argtypes = [P, vp, i32, vp, i32, vp]
         lib.orc_sparse_attn.restype = i32
@@ -281,6 +286,35 @@ def act_quant_rows(y_bits: np.ndarray, mutant: int = 0):
 def rotate_quant_rows(x_bits: np.ndarray, mutant: int = 0):
     """The V3.2 index producer on rows of bf16 bits: rotation, then act_quant."""
     return act_quant_rows(hadamard_bf16(x_bits, mutant), mutant)
+
+
+@dataclass
+class Rope:
+    """Rotary parameters of "DeepSeek-V4.1-Flash-NVFP4 inference/model.py"
+    (precompute_freqs_cis); the defaults are the released config's index and
+    compressor settings on the atlas page (rope_head_dim 64, compress_rope_theta
+    160000, rope_factor 16, original_seq_len 65536, beta_fast 32, beta_slow 1)."""
+    dim: int = 64
+    base: float = 160000.0
+    factor: float = 16.0
+    original_seq_len: int = 65536
+    beta_fast: float = 32.0
+    beta_slow: float = 1.0
+
+
+def rope_angles(rope: Rope, pos: int, mutant: int = 0) -> np.ndarray:
+    lib = _lib(mutant)
+    return np.array([lib.orc_rope_angle(rope.dim, i, pos, rope.base, rope.factor, rope.original_seq_len,
+                                        rope.beta_fast, rope.beta_slow) for i in range(rope.dim // 2)])
+
+
+def apply_rope(x: np.ndarray, rope: Rope, pos: int, inverse: bool = False, mutant: int = 0) -> np.ndarray:
+    """apply_rotary_emb on one row of rope.dim values (float64, a new array)."""
+    v = np.array(x, dtype=np.float64).reshape(-1).copy()
+    assert v.size == rope.dim
+    _lib(mutant).orc_apply_rope(v.ctypes.data, rope.dim, pos, rope.base, rope.factor, rope.original_seq_len,
+                                rope.beta_fast, rope.beta_slow, int(inverse))
+    return v
 
 
 class CompressorState:

@@ -41,6 +41,7 @@
  * build them to show that each plausible mistake fails at least one pin.  The
  * default build (ORC_MUTANT undefined) is the oracle.
  */
+#define _DEFAULT_SOURCE
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -458,6 +459,50 @@ int32_t orc_compress_decode(const float *kv_tok, const float *score_tok, int32_t
   if ((pos + 1) % r != 0) return 0;
   pool_group(kv_state, score_state, D, D, r, weight, eps, out);
   return 1;
+}
+
+/* ---- V4.1 rotary embedding (YaRN) ------------------------------------------ */
+
+/* "DeepSeek-V4.1-Flash-NVFP4 inference/model.py", precompute_freqs_cis: the
+ * angle of pair i (i < dim / 2) at position pos.  The base frequency is
+ * base^(-2i / dim); with original_seq_len > 0 (YaRN) the pairs below the
+ * corrected dimension of beta_fast keep it, those above that of beta_slow are
+ * divided by factor, and a linear ramp fades between them (low, high: floor
+ * and ceil of the corrected dimensions, clamped to [0, dim - 1]; the ramp's
+ * span is at least 1e-3).  The page computes the frequencies in fp32; the
+ * oracle takes them in double.  angle = pos * freq. */
+double orc_rope_angle(int32_t dim, int32_t i, int64_t pos, double base, double factor, int32_t original_seq_len,
+                      double beta_fast, double beta_slow) {
+  double freq = 1.0 / pow(base, (double)(2 * i) / (double)dim);
+  if (original_seq_len > 0) {
+    const double lo_d = dim * log(original_seq_len / (beta_fast * 2.0 * M_PI)) / (2.0 * log(base));
+    const double hi_d = dim * log(original_seq_len / (beta_slow * 2.0 * M_PI)) / (2.0 * log(base));
+    const double low = fmax(floor(lo_d), 0.0);
+    const double high = fmin(ceil(hi_d), (double)(dim - 1));
+    double ramp = ((double)i - low) / fmax(high - low, 1e-3);
+    ramp = fmin(fmax(ramp, 0.0), 1.0);
+    const double smooth = 1.0 - ramp;
+#if ORC_MUTANT == 18
+    freq = freq / factor * smooth + freq * (1.0 - smooth); /* ramp reversed */
+#else
+    freq = freq / factor * (1.0 - smooth) + freq * smooth;
+#endif
+  }
+  return (double)pos * freq;
+}
+
+/* Same page, apply_rotary_emb: adjacent pairs (x[2i], x[2i+1]) of a row of
+ * dim values taken as complex numbers and multiplied by e^(i angle_i) (its
+ * conjugate when inverse is set), in place, in double. */
+void orc_apply_rope(double *x, int32_t dim, int64_t pos, double base, double factor, int32_t original_seq_len,
+                    double beta_fast, double beta_slow, int32_t inverse) {
+  for (int32_t i = 0; i < dim / 2; ++i) {
+    const double a = orc_rope_angle(dim, i, pos, base, factor, original_seq_len, beta_fast, beta_slow);
+    const double c = cos(a), s = inverse ? -sin(a) : sin(a);
+    const double re = x[2 * i], im = x[2 * i + 1];
+    x[2 * i] = re * c - im * s;
+    x[2 * i + 1] = re * s + im * c;
+  }
 }
 
 /* ---- sparse attention ---------------------------------------------------- */

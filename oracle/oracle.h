@@ -61,6 +61,10 @@ uint8_t orc_e4m3_encode(float v);
 int32_t orc_act_quant_row(const uint16_t *y, int32_t n, uint8_t *codes, float *scale);
 int32_t orc_compress_prefill(const float *kv, const float *score, int32_t S, int32_t D, int32_t r,
                              const float *weight, double eps, double *out, float *kv_state, float *score_state);
+double orc_rope_angle(int32_t dim, int32_t i, int64_t pos, double base, double factor, int32_t original_seq_len,
+                      double beta_fast, double beta_slow);
+void orc_apply_rope(double *x, int32_t dim, int64_t pos, double base, double factor, int32_t original_seq_len,
+                    double beta_fast, double beta_slow, int32_t inverse);
 int32_t orc_compress_decode(const float *kv_tok, const float *score_tok, int32_t pos, int32_t D, int32_t r,
                             float *kv_state, float *score_state, const float *weight, double eps, double *out);
 int32_t orc_sparse_attn(const orc_problem *P, const int32_t *idx /*[T,K]*/, int32_t K,
