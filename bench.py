@@ -2,12 +2,15 @@
 """Throughput of the fused sparse attention step (index scores -> top-k ->
 windowed + sparse MQA) on GB300, as one JSON line.
 
-Default workload: decode, batch 64, positions U[32768, 65535], r=4, index
-64x128 fp8 keys + per-position scale, topk 2048, attention 64x128, window
-128 (the first workload with an HBM-roofline target); ``--workload`` picks
-another.  One step = one sa_fused_decode call over the whole batch with its
-inputs resident in HBM.  Three copies of every input rotate between steps, so
-each step reads data evicted from L2 by the two before it.
+Default workload: ragged long-context decode, batch 128, lengths
+U[8192, 131072] (query at L-1), r=4, index 64x128 fp8 keys + per-position
+scale, topk 2048, attention 64x128, window 128 -- the largest decode workload
+with an HBM-roofline target; ``--workload`` picks another.  One step = one
+sa_fused_decode call over the whole batch with its inputs resident in HBM.
+Three copies of every input rotate between steps, so each step reads data
+evicted from L2 by the two before it.  The line also carries the decode
+batch-64 workload and the 4096-token prefill chunk as extra fields
+(``workloads``), timed the same way.
 
 ``--impl reference`` times the float64 CPU oracle on the host cores instead
 (the baseline arm); it never touches the GPU.
@@ -41,7 +44,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="c2", choices=("c0", "c1", "c2", "c3", "c4"))
+    ap.add_argument("--workload", default="c4", choices=("c0", "c1", "c2", "c3", "c4"))
+    ap.add_argument("--extra", default="c2,c3",
+                    help="other workloads timed the same way and reported as extra fields ('' for none)")
     ap.add_argument("--copies", type=int, default=3)
     ap.add_argument("--soak-seconds", type=float, default=1.5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -459,6 +464,126 @@ def index_producer(binding, torch, steps, peak):
             "frac_of_hbm_peak": round(gbs / peak, 4), "traffic": recorded_traffic("index_producer", "prefill")}
 
 
+def time_workload(binding, torch, w, n_copies, steps, warmup, before_timed=None, after_timed=None):
+    """Device time of the fused step on workload ``w``: ``n_copies`` device
+    copies of the inputs rotate between steps; one CUDA graph per copy holds
+    one sa_fused_decode call.  Returns the time of exactly ``steps`` graph
+    replays between CUDA events on the launching stream (after ``warmup``
+    untimed replays), the same steps launched eagerly, and per-stage times from
+    staged graphs (events between the stages), each measured step replayed
+    right after the previous copy's step so that it starts on a busy GPU, as in
+    the timed loop."""
+    copies = [binding.upload(w, device="cuda") for _ in range(max(1, n_copies))]
+    K = w.K
+    ws = binding.new_workspace(copies[0])
+    out = torch.empty((w.T, w.H, w.D), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((w.T, max(K, 1)), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    launches_per_step = binding.sa_fused_decode_launch_count(copies[0].ia, copies[0].aa, K)
+
+    def eager_step(i):
+        dp = copies[i % len(copies)]
+        binding.sa_fused_decode(dp.ia, dp.aa, K, idx, out, ws, stream)
+
+    for i in range(warmup):
+        eager_step(i)
+    torch.cuda.synchronize()
+    if binding.sa_check_device_status(ws) != binding.SA_OK:
+        raise RuntimeError("device status not OK after warm-up")
+    graphs = []
+    for dp in copies:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            binding.sa_fused_decode(dp.ia, dp.aa, K, idx, out, ws)
+        graphs.append(g)
+    stage_events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in copies]
+    for row in stage_events:
+        for e in row:
+            e.record(stream)  # materialise the CUDA event handles
+    torch.cuda.synchronize()
+    staged_graphs = []
+    for dp, evs in zip(copies, stage_events):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            binding.sa_fused_decode_staged(dp.ia, dp.aa, K, idx, out, ws, [e.cuda_event for e in evs])
+        staged_graphs.append(g)
+    for i in range(max(3, warmup)):
+        graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+
+    def step(i):
+        graphs[i % len(graphs)].replay()
+
+    if before_timed:
+        before_timed(step)
+    # ---- timed region: exactly `steps` graph replays
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if after_timed:
+        after_timed()
+    ms_total = ev0.elapsed_time(ev1)
+    # ---- the same steps launched eagerly through the C ABI (no graph)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        eager_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    eager_ms_per_step = e0.elapsed_time(e1) / steps
+    # ---- per-stage device time from the staged graphs
+    sums = {s_: 0.0 for s_ in STAGES}
+    for i in range(steps):
+        k = i % len(staged_graphs)
+        staged_graphs[(k - 1) % len(staged_graphs)].replay()
+        staged_graphs[k].replay()
+        torch.cuda.synchronize()
+        evs = stage_events[k]
+        for j, s_ in enumerate(STAGES):
+            sums[s_] += evs[j].elapsed_time(evs[j + 1])
+    stage_ms = {s_: sums[s_] / steps for s_ in STAGES}
+    if binding.sa_check_device_status(ws) != binding.SA_OK:
+        raise RuntimeError("device status not OK after the timed steps")
+    return {"copies": copies, "ws": ws, "out": out, "idx": idx, "stream": stream,
+            "launches_per_step": launches_per_step, "ms_total": ms_total,
+            "eager_ms_per_step": eager_ms_per_step, "stage_ms": stage_ms}
+
+
+def workload_field(binding, torch, wl, name, steps, warmup, n_copies, peak):
+    """One extra workload, timed like the headline line: query-tokens/s, the
+    step's HBM-roofline fraction, and per-stage times, bytes and traffic."""
+    spec = wl.CONFIGS[name]
+    w = wl.generate(spec)
+    tw = time_workload(binding, torch, w, n_copies, steps, warmup)
+    ms = tw["ms_total"] / steps
+    nbytes = algorithmic_bytes(w)
+    res = {"workload": f"{spec.name}: {spec.description}", "ms_per_step": round(ms, 5),
+           "value": round(w.T / (ms / 1000.0), 1), "unit": UNIT, "step_bytes": nbytes["step"],
+           "frac_of_hbm_peak": round(nbytes["step"] / (ms / 1000.0) / 1e9 / peak, 4),
+           "frac_of_8TBps": round(nbytes["step"] / (ms / 1000.0) / 8e12, 4),
+           "eager_ms_per_step": round(tw["eager_ms_per_step"], 5),
+           "stages": {s: {"ms": round(tw["stage_ms"][s], 5), "algorithmic_bytes": nbytes[s],
+                          "GB_s": round(nbytes[s] / (tw["stage_ms"][s] / 1000.0) / 1e9, 1),
+                          "traffic": recorded_traffic(s, name)} for s in STAGES}}
+    if name == "c3":
+        res["note"] = ("prefill: 4096 queries share one sequence's keys, so the per-query bytes of the metric "
+                       "are mostly L2 hits; the stage is tensor-bound (index ~0.52 TFLOP fp8, attention "
+                       "~0.29 TFLOP bf16)")
+        res["tensor_tflops"] = {
+            "idx_score": round(2.0 * float(np.sum(np.minimum((w.q_pos.astype(np.int64) + 1) // w.r, w.N_c)))
+                               * w.H_I * w.D_I / (tw["stage_ms"]["idx_score"] / 1000.0) / 1e12, 1),
+            "sparse_mqa": round(4.0 * float(np.sum(np.minimum(w.W, w.q_pos.astype(np.int64) + 1)
+                                                   + np.minimum(w.K, (w.q_pos.astype(np.int64) + 1) // w.r)))
+                                * w.H * w.D / (tw["stage_ms"]["sparse_mqa"] / 1000.0) / 1e12, 1)}
+    del tw
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -486,103 +611,36 @@ def run_ours(args):
         return
     spec = wl.CONFIGS[args.workload]
     w = wl.generate(spec, seed=wl.SEEDS[spec.name] + 1000 * rank)
-    copies = [binding.upload(w, device="cuda") for _ in range(max(1, args.copies))]
-    K = w.K
-    ws = binding.new_workspace(copies[0])
-    out = torch.empty((w.T, w.H, w.D), dtype=torch.bfloat16, device="cuda")
-    idx = torch.empty((w.T, max(K, 1)), dtype=torch.int32, device="cuda")
-    stream = torch.cuda.current_stream()
-    launches_per_step = binding.sa_fused_decode_launch_count(copies[0].ia, copies[0].aa, K)
-
-    def eager_step(i):
-        dp = copies[i % len(copies)]
-        binding.sa_fused_decode(dp.ia, dp.aa, K, idx, out, ws, stream)
-
-    for i in range(args.warmup):
-        eager_step(i)
-    torch.cuda.synchronize()
-    if binding.sa_check_device_status(ws) != binding.SA_OK:
-        raise RuntimeError("device status not OK after warm-up")
-
-    # One CUDA graph per input copy: the step as a decode loop would replay it.
-    graphs = []
-    for dp in copies:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            binding.sa_fused_decode(dp.ia, dp.aa, K, idx, out, ws)
-        graphs.append(g)
-    # and one per copy with CUDA events between the stages (per-kernel timing)
-    stage_events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in copies]
-    for row in stage_events:
-        for e in row:
-            e.record(stream)  # materialise the CUDA event handles
-    torch.cuda.synchronize()
-    staged_graphs = []
-    for dp, evs in zip(copies, stage_events):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            binding.sa_fused_decode_staged(dp.ia, dp.aa, K, idx, out, ws, [e.cuda_event for e in evs])
-        staged_graphs.append(g)
-    for i in range(max(3, args.warmup)):
-        graphs[i % len(graphs)].replay()
-    torch.cuda.synchronize()
-
-    def step(i):
-        graphs[i % len(graphs)].replay()
-
     sampler = ClockSampler(local_rank)
-    sampler.start()
-    t_soak = time.time()
-    i = 0
-    while time.time() - t_soak < args.soak_seconds:  # same steps, untimed, to read clocks under load
-        step(i)
-        i += 1
-        if i % 64 == 0:
-            torch.cuda.synchronize()
-    # ---- timed region: exactly K steps (graph replays)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    t_end = time.time()
-    sampler.stop()
-    ms = max_over_ranks(ev0.elapsed_time(ev1), "cuda")
+    soak = {}
+
+    def clock_soak(step):
+        sampler.start()
+        soak["t0"] = time.time()
+        i = 0
+        while time.time() - soak["t0"] < args.soak_seconds:  # same steps, untimed, to read clocks under load
+            step(i)
+            i += 1
+            if i % 64 == 0:
+                torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+
+    def after_timed():
+        if world > 1:
+            dist.barrier()
+        soak["t1"] = time.time()
+        sampler.stop()
+
+    tw = time_workload(binding, torch, w, args.copies, args.steps, args.warmup,
+                       before_timed=clock_soak, after_timed=after_timed)
+    copies, ws, out, idx, K, stream = tw["copies"], tw["ws"], tw["out"], tw["idx"], w.K, tw["stream"]
+    launches_per_step = tw["launches_per_step"]
+    ms = max_over_ranks(tw["ms_total"], "cuda")
     ms_per_step = ms / args.steps
     value = w.T * world * args.steps / (ms / 1000.0)
-
-    # ---- the same K steps launched eagerly through the C ABI (no graph)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        eager_step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    eager_ms_per_step = e0.elapsed_time(e1) / args.steps
-
-    # ---- per-stage device time: staged graphs, events between the stages.  Each
-    # measured step follows the previous copy's step back to back, as in the
-    # timed loop (that step's own events are not read), so its first stage does
-    # not start from an idle GPU.
-    sums = {s_: 0.0 for s_ in STAGES}
-    for i in range(args.steps):
-        k = i % len(staged_graphs)
-        staged_graphs[(k - 1) % len(staged_graphs)].replay()
-        staged_graphs[k].replay()
-        torch.cuda.synchronize()
-        evs = stage_events[k]
-        for j, s_ in enumerate(STAGES):
-            sums[s_] += evs[j].elapsed_time(evs[j + 1])
-    stage_ms = {s_: sums[s_] / args.steps for s_ in STAGES}
-    if binding.sa_check_device_status(ws) != binding.SA_OK:
-        raise RuntimeError("device status not OK after the timed steps")
+    eager_ms_per_step = tw["eager_ms_per_step"]
+    stage_ms = tw["stage_ms"]
 
     # ---- end to end through the C ABI with host buffers: every step copies its
     # query inputs from one pinned host staging buffer (one H2D copy), runs the
@@ -676,10 +734,13 @@ def run_ours(args):
               for s in STAGES}
     step_frac = nbytes["step"] / (ms_per_step / 1000.0) / 1e9 / peak
 
-    clocks = sampler.summary(t_soak, t_end)
+    clocks = sampler.summary(soak["t0"], soak["t1"])
     two_level = None if args.no_two_level else two_level_topk(binding, torch, wl, args.steps, peak)
     v41 = None if args.no_v41 else v41_decode(binding, torch, args.steps, peak)
     producer = index_producer(binding, torch, args.steps, peak)
+    extra = {}
+    for name in [x for x in args.extra.split(",") if x and x != spec.name]:
+        extra[name] = workload_field(binding, torch, wl, name, args.steps, args.warmup, args.copies, peak)
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -710,6 +771,7 @@ def run_ours(args):
         "two_level_topk": two_level,
         "v41_decode": v41,
         "index_producer": producer,
+        "workloads": extra,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)

@@ -246,6 +246,10 @@ SA_API int32_t sa_fused_decode_launch_count(const sa_index_args *ia, const sa_at
 /* Bytes of the fixed device scratch array behind sa_fused_decode_noalloc. */
 #define SA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 
+/* SA_NOALLOC_SCRATCH_BYTES as compiled into the library (for bindings that
+ * cannot read this header). */
+SA_API size_t sa_noalloc_scratch_bytes(void);
+
 /* sa_fused_decode for callers that cannot allocate device memory.  (The model
  * pages have no counterpart: this is a deployment variant of the fused step.)
  *
@@ -264,9 +268,11 @@ SA_API int32_t sa_fused_decode_launch_count(const sa_index_args *ia, const sa_at
  * - Size limit: a problem whose scratch (sa_workspace_size for the same
  *   arguments) exceeds SA_NOALLOC_SCRATCH_BYTES is rejected with
  *   SA_ERR_UNSUPPORTED and enqueues nothing.
- * - Set-up: the first call on each device (with that device current) looks
- *   up the array's device address once (cudaGetSymbolAddress); make that
- *   first call before any stream capture.
+ * - Set-up: the first call in each CUDA context (a device's primary context,
+ *   with that device current, in the usual case) looks up the array's device
+ *   address once (cudaGetSymbolAddress); make that first call before any
+ *   stream capture.  After cudaDeviceReset, or in another context, the array
+ *   may sit elsewhere; the address is looked up again there.
  * - Sharing: every call on a device uses the same array, which keeps the last
  *   call's contents (no part of it needs to start at zero).  Calls whose work
  *   overlaps on the GPU -- on different streams, or from different host

@@ -62,7 +62,7 @@ EXPORTED = ("sa_workspace_size", "sa_workspace_init", "sa_indexer_scores", "sa_t
             "sa_compress_prefill",
             "sa_sparse_attn", "sa_fused_decode", "sa_fused_decode_staged",
             "sa_fused_decode_launch_count", "sa_check_device_status", "sa_status_string",
-            "sa_last_error_detail")
+            "sa_last_error_detail", "sa_fused_decode_noalloc", "sa_noalloc_scratch_bytes")
 
 _LIB = None
 
@@ -96,6 +96,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.sa_fused_decode_launch_count.restype = i32
     lib.sa_fused_decode_noalloc.argtypes = [IA, AA, i32, vp, vp, vp, vp]
     lib.sa_fused_decode_noalloc.restype = i32
+    lib.sa_noalloc_scratch_bytes.argtypes = []
+    lib.sa_noalloc_scratch_bytes.restype = sz
     lib.sa_check_device_status.argtypes = [vp, vp]
     lib.sa_status_string.argtypes = [i32]
     lib.sa_status_string.restype = ctypes.c_char_p
@@ -218,6 +220,11 @@ def sa_fused_decode_noalloc(ia: IndexArgs, aa: AttnArgs, K: int, idx_out, out, d
     allocation); see include/sa.h for its size limit and sharing rules."""
     _check(load().sa_fused_decode_noalloc(ctypes.byref(ia), ctypes.byref(aa), K, _p(idx_out), _p(out),
                                           _p(device_status), _s(stream)))
+
+
+def sa_noalloc_scratch_bytes() -> int:
+    """Bytes of the fixed scratch behind sa_fused_decode_noalloc."""
+    return int(load().sa_noalloc_scratch_bytes())
 
 
 def sa_check_device_status(ws, stream=None) -> int:

@@ -2,19 +2,45 @@
 // inference/model.py", Indexer.forward: rotate_activation, then act_quant of
 // q and k, and the write of k into the index key cache).
 //
-// Each row of 128 bf16 values is multiplied by the Sylvester-Hadamard matrix
-// and scaled by 128^-1/2: fp32 butterflies in the fixed stage order h = 1, 2,
-// ..., 64, each taking the pair (i, i + h) from (a, b) to (a + b, a - b), then
-// the product with the fp32 constant 128^-1/2 rounded to bf16.  The row is
-// then quantised as one block: scale = amax / 448 and codes = e4m3(y / scale)
-// (nearest, ties to even, saturating at 448), both divisions in fp32; an
-// all-zero row gets scale 1.  Every rounding is an explicit _rn operation, so
-// the codes are reproducible bit for bit.
+// Each row x of 128 bf16 values becomes y = bf16(H x * 128^-1/2), H the
+// Sylvester-Hadamard matrix, with y the exact value rounded once (nearest,
+// ties to even; an exact zero is +0).  The row is then quantised as one block:
+// scale = amax|y| / 448 and codes = e4m3(y / scale) (nearest, ties to even,
+// saturating at 448), both quotients correctly rounded fp32; an all-zero row
+// gets scale 1.
 //
-// One warp per row: lane l holds elements 4l .. 4l+3, so stages 1 and 2 run in
-// registers and stage h >= 4 pairs lane l with lane l ^ (h / 4).  A row may land
-// at another row of the destination (dst[r]: e.g. row b * N_c + position of the
-// k cache); a destination outside [0, dst_rows) is skipped and flagged.
+// Four lanes per row: lane 4r + h holds elements 32h .. 32h + 31 of row r.  A
+// warp takes 8 consecutive rows at a time; they arrive by cp.async into a
+// shared-memory tile of 64-byte quarter rows whose 16-byte chunks are XOR
+// swizzled, so that each lane reads its quarter without bank conflicts (two
+// tiles per warp: the next one is in flight while the current one computes).
+//
+// Exact sums.  With e the exponent of the row's largest |x|, every x_j is
+// taken as the integer X_j = round(x_j 2^(20 - e)) (|X_j| < 2^21), which is
+// x_j exactly unless |x_j| < 2^(e - 13) ("tiny"); the butterflies run on
+// 32-bit integers (stages 1 .. 16 in registers, 32 and 64 across the lanes
+// of the row), so S = H X is exact.  y = S 2^(e - 20) 128^-1/2 is formed in fp32 as p
+// with |p - y| < 1.16 * 2^-23 |p| (the conversion of S, the fp32 constant,
+// the product), and the tiny elements' rounding adds at most
+// n_tiny * 2^(e - 21) * 2^-3.5.  p rounds like y unless a bf16 rounding
+// midpoint lies within that bound of p (about one element in 2 * 10^4); such
+// an element is redone in double from the exact S and the tiny elements'
+// exact residuals, then rounded.  Rows whose largest exponent lies outside
+// [-100, 100], or that hold more tiny elements than the residual list keeps,
+// are computed element by element from the row in 64-bit integers and double.
+//
+// Quotients.  inv = 1/scale correctly rounded (__frcp_rn), q = y * inv and the
+// correction q + inv (y - q scale) with fused multiply-adds give the correctly
+// rounded y / scale (Markstein, "Computation of elementary functions on the
+// IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990: a correctly
+// rounded reciprocal and a quotient within one ulp make the FMA-corrected
+// quotient correctly rounded when nothing underflows).  A row whose scale is
+// below 2^-100 divides y 2^100 by scale 2^100, the same quotient.
+//
+// Codes leave through a swizzled shared-memory staging tile so that each
+// 128-byte code row is written by 8 lanes together.  A row may land at another
+// row of the destination (dst[r]: e.g. row b * N_c + position of the k cache);
+// a destination outside [0, dst_rows) is skipped and flagged.
 #include <cmath>
 
 #include "common.cuh"
@@ -23,71 +49,345 @@
 namespace sa {
 namespace {
 
-constexpr int kProdDim = 128;
-constexpr int kProdWarps = 8;
+constexpr int kDim = 128;
+constexpr int kQ = 32;                           // elements per lane (a quarter row)
+constexpr int kWarps = 4;                        // warps per CTA
+constexpr int kTileRows = 8;                     // rows per warp tile: four lanes per row
+constexpr int kTileBytes = kTileRows * kDim * 2; // 2 KB of bf16 input
+constexpr int kCodeBytes = kTileRows * kDim;     // 1 KB of codes
+constexpr int kTinyCap = 4;                      // tiny residuals kept per lane
+constexpr int kTinyBytes = 32 * kTinyCap * 8;    // (index, residual) pairs
+constexpr int kYBytes = kTileRows * kDim * 2;    // y of rows on the element-wise path
+constexpr int kWarpSmem = 2 * kTileBytes + kCodeBytes + kTinyBytes + kYBytes;
+constexpr int kSmem = kWarps * kWarpSmem;        // 32 KB per CTA
+constexpr int kCtasPerSm = 5;
+constexpr uint32_t kMagicBits = 0x4B400000u;     // bits of 1.5 * 2^23
+constexpr float kMagic = 12582912.0f;            // 1.5 * 2^23
+// 128^-1/2 = 2^-3.5: nearest fp32 (relative error 2^-25.8) and nearest double
+constexpr float kRootF = 0.0883883461356163f;
+constexpr double kRootD = 0.08838834764831844;
 
-__global__ void __launch_bounds__(32 * kProdWarps)
-rotate_quant_kernel(const uint16_t *__restrict__ x, int rows, float inv_sqrt_n, const int32_t *__restrict__ dst,
-                    int64_t dst_rows, uint8_t *__restrict__ codes, float *__restrict__ scales, uint32_t *status) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kProdWarps + (threadIdx.x >> 5);
-  if (row >= rows) return;
-  const uint2 raw = *reinterpret_cast<const uint2 *>(x + row * kProdDim + 4 * lane);
-  float v[4] = {bf16_bits_to_float(static_cast<uint16_t>(raw.x & 0xFFFFu)),
-                bf16_bits_to_float(static_cast<uint16_t>(raw.x >> 16)),
-                bf16_bits_to_float(static_cast<uint16_t>(raw.y & 0xFFFFu)),
-                bf16_bits_to_float(static_cast<uint16_t>(raw.y >> 16))};
-  // stages h = 1 and 2 inside the lane
-  {
-    const float a = v[0], b = v[1], c = v[2], d = v[3];
-    v[0] = __fadd_rn(a, b);
-    v[1] = __fsub_rn(a, b);
-    v[2] = __fadd_rn(c, d);
-    v[3] = __fsub_rn(c, d);
-  }
-  {
-    const float a = v[0], b = v[1], c = v[2], d = v[3];
-    v[0] = __fadd_rn(a, c);
-    v[2] = __fsub_rn(a, c);
-    v[1] = __fadd_rn(b, d);
-    v[3] = __fsub_rn(b, d);
-  }
-  // stages h = 4 .. 64 across lanes: the lower element of a pair keeps a + b,
-  // the upper one a - b (a the lower element's value)
-#pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
-    const bool upper = (lane & m) != 0;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float o = __shfl_xor_sync(0xffffffffu, v[k], m);
-      v[k] = upper ? __fsub_rn(o, v[k]) : __fadd_rn(v[k], o);
-    }
-  }
-  float y[4];
-  uint32_t amax_bits = 0u;  // |y| as bits: non-negative floats order like their bits
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void sts16(uint32_t a, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"(v) : "memory");
+}
+
+// Input tile: quarter row q = 4r + h (32 bf16 = 64 B), 16-byte chunk c of 4,
+// XOR swizzled by q / 2; code tile: quarter row q (32 codes), chunk c of 2,
+// swizzled by q / 4.  Eight consecutive lanes touching chunk c of their own
+// quarter rows, or eight chunks of one row, hit distinct bank groups.
+__device__ __forceinline__ uint32_t in_off(int q, int c) {
+  return static_cast<uint32_t>(q * 64 + ((c ^ ((q >> 1) & 3)) << 4));
+}
+__device__ __forceinline__ uint32_t code_off(int q, int c) {
+  return static_cast<uint32_t>(q * 32 + ((c ^ ((q >> 2) & 1)) << 4));
+}
+
+// Issues the copies of tile t (rows 8t .. 8t + 7) into `tile`; rows past
+// `rows` are zero-filled.
+__device__ __forceinline__ void load_tile(const uint16_t *__restrict__ x, int rows, int t, uint32_t tile,
+                                          int lane) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    y[k] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(v[k], inv_sqrt_n)));
-    amax_bits = max(amax_bits, __float_as_uint(fabsf(y[k])));
+    const int g = k * 32 + lane;  // 16-byte chunk g of the tile: quarter row g / 4, chunk g % 4
+    const int q = g >> 2, c = g & 3;
+    const int64_t row = static_cast<int64_t>(t) * kTileRows + (q >> 2);
+    const bool ok = row < rows;
+    cp_async16(tile + in_off(q, c), x + (ok ? row : 0) * kDim + (q & 3) * kQ + c * 8, ok ? 16u : 0u);
   }
-  const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, amax_bits));
-  const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-  uint32_t packed = 0u;
+}
+
+// y_m of row r of `tile`, exactly: the sum in 64-bit integers with quantum
+// 2^(eref - 45) (exact for every element above 2^(eref - 38); the rest are
+// truncated, an error below 2^(eref - 38) in all), times 128^-1/2 in double,
+// rounded once to bf16.
+__device__ __noinline__ uint32_t exact_element(uint32_t tile, int r, int m, int eref) {
+  long long acc = 0;
+  for (int g = 0; g < 16; ++g) {
+    const uint4 v = lds128(tile + in_off(4 * r + (g >> 2), g & 3));
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(__fdiv_rn(y[k], s), __NV_SATFINITE, __NV_E4M3);
-    packed |= static_cast<uint32_t>(c) << (8 * k);
-  }
-  int64_t d = row;
-  if (dst) {
-    d = dst[row];
-    if (d < 0 || d >= dst_rows) {
-      if (lane == 0) raise_flag(status, kFlagBadIndex);
-      return;
+    for (int k = 0; k < 8; ++k) {
+      const int j = g * 8 + k;
+      const uint32_t b = (wv[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
+      if ((b & 0x7FFFu) == 0) continue;
+      const int ex = (b >> 7) & 0xFF;
+      const long long mant = ex ? (128 | (b & 0x7F)) : (b & 0x7F);
+      const int e = ex ? ex - 134 : -133;  // |x_j| = mant * 2^e
+      const int sh = e - (eref - 45);
+      long long term = sh >= 0 ? (mant << sh) : (sh > -62 ? (mant >> -sh) : 0);
+      if ((b & 0x8000u) != ((__popc(m & j) & 1) ? 0x8000u : 0u)) term = -term;
+      acc += term;
     }
   }
-  *reinterpret_cast<uint32_t *>(codes + d * kProdDim + 4 * lane) = packed;
-  if (lane == 0) scales[d] = s;
+  const double yd = static_cast<double>(acc) * ldexp(kRootD, eref - 45);
+  return __bfloat16_as_ushort(__double2bfloat16(yd));
+}
+
+// y_m from the exact integer sum S (quantum `lsb`) and the tiny elements'
+// residuals (x_j - X_j lsb, exact in fp32) listed by the four lanes of the
+// row: (S lsb + sum_j sign_mj res_j) 128^-1/2 in double, rounded once to bf16.
+__device__ __noinline__ uint32_t fixed_element(uint32_t S, int m, double lsb, uint32_t row_lists, uint32_t counts) {
+  double acc = static_cast<double>(static_cast<int32_t>(S)) * lsb;
+  for (int l = 0; l < 4; ++l) {
+    const int n = (counts >> (8 * l)) & 0xFF;
+    for (int i = 0; i < n; ++i) {
+      const uint32_t a = row_lists + l * (kTinyCap * 8) + 8 * i;
+      const int j = static_cast<int>(lds32(a));
+      const double res = static_cast<double>(__uint_as_float(lds32(a + 4)));
+      acc += (__popc(m & j) & 1) ? -res : res;
+    }
+  }
+  return __bfloat16_as_ushort(__double2bfloat16(acc * kRootD));
+}
+
+__global__ void __launch_bounds__(32 * kWarps, kCtasPerSm)
+rotate_quant_kernel(const uint16_t *__restrict__ x, int rows, const int32_t *__restrict__ dst, int64_t dst_rows,
+                    uint8_t *__restrict__ codes, float *__restrict__ scales, uint32_t *status) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int h = lane & 3, r = lane >> 2;  // quarter, row within the tile
+  const uint32_t base = smem_addr(smem) + warp * kWarpSmem;
+  const uint32_t code_tile = base + 2 * kTileBytes;
+  const uint32_t lists = code_tile + kCodeBytes;
+  const uint32_t own_list = lists + lane * (kTinyCap * 8);
+  const uint32_t row_lists = lists + (lane & ~3) * (kTinyCap * 8);
+  const uint32_t yscr = lists + kTinyBytes + lane * (kQ * 2);
+  const int n_tiles = (rows + kTileRows - 1) / kTileRows;
+  const int nw = gridDim.x * kWarps;
+  int t = blockIdx.x * kWarps + warp;
+  if (t < n_tiles) load_tile(x, rows, t, base, lane);
+  cp_async_commit();
+  for (int buf = 0; t < n_tiles; t += nw, buf ^= 1) {
+    if (t + nw < n_tiles) load_tile(x, rows, t + nw, base + (buf ^ 1) * kTileBytes, lane);
+    cp_async_commit();
+    cp_async_wait_one();
+    __syncwarp();
+    const uint32_t tile = base + buf * kTileBytes;
+    const int64_t row = static_cast<int64_t>(t) * kTileRows + r;
+
+    // ---- this lane's 32 elements as 16 words of two bf16 (element 2i low)
+    uint32_t w[16];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 v = lds128(tile + in_off(lane, c));
+      w[4 * c] = v.x, w[4 * c + 1] = v.y, w[4 * c + 2] = v.z, w[4 * c + 3] = v.w;
+    }
+    float amax_x = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      amax_x = fmaxf(amax_x, fabsf(__uint_as_float(w[i] << 16)));
+      amax_x = fmaxf(amax_x, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+    }
+    amax_x = fmaxf(amax_x, __shfl_xor_sync(0xffffffffu, amax_x, 1));
+    amax_x = fmaxf(amax_x, __shfl_xor_sync(0xffffffffu, amax_x, 2));
+    const int emax = static_cast<int>((__float_as_uint(amax_x) >> 23) & 0xFF) - 127;
+    // tiny elements (0 < |x| < 2^(emax - 13)): per half of a word, bit 15 of
+    // (|x| | 0x8000) - 1 says |x| > 0, that of (|x| | 0x8000) - limit says
+    // |x| >= limit; the flags add up per half
+    const uint32_t lim = static_cast<uint32_t>(max(emax - 13 + 127, 0)) << 7;
+    const uint32_t lim2 = lim | (lim << 16);
+    uint32_t tiny_cnt = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t u = w[i] | 0x80008000u;
+      tiny_cnt += (((u - 0x00010001u) & ~(u - lim2)) & 0x80008000u) >> 15;
+    }
+    const uint32_t n_own = (tiny_cnt & 0xFFFFu) + (tiny_cnt >> 16);
+    // the four lanes' counts, one byte each (lane 4r + l in byte l)
+    uint32_t counts = min(n_own, 127u) << (8 * h);
+    counts |= __shfl_xor_sync(0xffffffffu, counts, 1);
+    counts |= __shfl_xor_sync(0xffffffffu, counts, 2);
+    const bool over = ((counts + 0x7B7B7B7Bu) & 0x80808080u) != 0;  // some byte above kTinyCap (no carries: <= 127)
+    const bool fast = emax >= -100 && emax <= 100 && !over;
+    const bool has_tiny = counts != 0;
+    const float sc = __uint_as_float(static_cast<uint32_t>(127 + 20 - (fast ? emax : 0)) << 23);
+    const float lsb = __uint_as_float(static_cast<uint32_t>(127 - 20 + (fast ? emax : 0)) << 23);
+    // this lane's tiny elements and their exact residuals x - X lsb, for the
+    // fix-ups (a rolled loop over the tile, run only by lanes that have some)
+    if (n_own > 0 && fast) {
+      const float limf = __uint_as_float(lim << 16);
+      int k = 0;
+      for (int i = 0; i < kQ; ++i) {
+        const float xv = __uint_as_float(lds16(tile + in_off(lane, i >> 3) + 2 * (i & 7)) << 16);
+        if (xv != 0.f && fabsf(xv) < limf) {
+          const float X = __fsub_rn(__fmaf_rn(xv, sc, kMagic), kMagic);
+          sts32(own_list + 8 * k, static_cast<uint32_t>(kQ * h + i));
+          sts32(own_list + 8 * k + 4, __float_as_uint(__fmaf_rn(-X, lsb, xv)));
+          ++k;
+        }
+      }
+    }
+    __syncwarp();
+
+    // ---- integers with the offset of the conversion trick kept (wrap-around
+    // arithmetic; the butterflies carry the offset into output 0 only)
+    uint32_t v[kQ];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      v[2 * i] = __float_as_uint(__fmaf_rn(__uint_as_float(w[i] << 16), sc, kMagic));
+      v[2 * i + 1] = __float_as_uint(__fmaf_rn(__uint_as_float(w[i] & 0xFFFF0000u), sc, kMagic));
+    }
+#pragma unroll
+    for (int s = 1; s < kQ; s <<= 1) {
+#pragma unroll
+      for (int i = 0; i < kQ; ++i) {
+        if (i & s) continue;
+        const uint32_t a = v[i], b = v[i + s];
+        v[i] = a + b;
+        v[i + s] = a - b;
+      }
+    }
+    // stages 32 and 64 across the row's lanes: the lower element of a pair
+    // keeps a + b, the upper one a - b
+#pragma unroll
+    for (int m = 1; m <= 2; m <<= 1) {
+      const uint32_t sgn = (h & m) ? 0xFFFFFFFFu : 1u;
+#pragma unroll
+      for (int i = 0; i < kQ; ++i) {
+        const uint32_t o = __shfl_xor_sync(0xffffffffu, v[i], m);
+        v[i] = o + sgn * v[i];
+      }
+    }
+    if (h == 0) v[0] -= kMagicBits * 128u;
+
+    // ---- p = S lsb 128^-1/2 and its bf16 rounding; where p cannot decide
+    // the rounding (a midpoint within the error bound of p), the element is
+    // fixed from S and the tiny residuals in double.  Without tiny elements
+    // in the warp the bound is 1.16 * 2^-23 |p| < 2.4 ulp(p), checked on the
+    // low 16 bits of p (a bf16 midpoint has them at 0x8000); otherwise it is
+    // 1.25 * 2^-23 |p| + t_abs, and an element with t_abs >= 2^-11 |p| (where
+    // the midpoint below p's binade may be the nearer one) is always fixed.
+    const float root = kRootF * lsb;
+    const uint32_t n_row = (counts & 0xFF) + ((counts >> 8) & 0xFF) + ((counts >> 16) & 0xFF) + (counts >> 24);
+    const float t_abs = static_cast<float>(n_row) * 0.5f * lsb * 0.0884f;  // n_tiny * lsb / 2 * 128^-1/2, rounded up
+    const float p_small = t_abs * 2048.0f;
+    const bool warp_tiny = __any_sync(0xffffffffu, has_tiny);
+    uint32_t yb[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float p0 = __fmul_rn(__int2float_rn(static_cast<int32_t>(v[2 * i])), root);
+      const float p1 = __fmul_rn(__int2float_rn(static_cast<int32_t>(v[2 * i + 1])), root);
+      __nv_bfloat162 pr = __floats2bfloat162_rn(p0, p1);
+      uint32_t word = *reinterpret_cast<uint32_t *>(&pr);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float p = k ? p1 : p0;
+        bool amb;
+        if (warp_tiny) {
+          const float mid = __uint_as_float((__float_as_uint(p) & 0xFFFF0000u) | 0x8000u);
+          amb = fabsf(__fsub_rn(p, mid)) <= __fmaf_rn(fabsf(p), 1.25f * 0x1p-23f, t_abs) || fabsf(p) <= p_small;
+        } else {
+          amb = ((__float_as_uint(p) - 0x7FFDu) & 0xFFFFu) <= 6u;
+        }
+        if (amb && fast) {
+          const uint32_t e = fixed_element(v[2 * i + k], kQ * h + 2 * i + k, static_cast<double>(lsb), row_lists,
+                                           counts);
+          word = k ? ((word & 0xFFFFu) | (e << 16)) : ((word & 0xFFFF0000u) | e);
+        }
+      }
+      yb[i] = word;
+    }
+    // rows outside the fast path: element by element from the row
+    if (__any_sync(0xffffffffu, !fast)) {
+      if (!fast)
+        for (int i = 0; i < kQ; ++i)
+          sts16(yscr + 2 * i, static_cast<uint16_t>(exact_element(tile, r, kQ * h + i, emax)));
+      __syncwarp();
+      if (!fast) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) yb[i] = lds32(yscr + 4 * i);
+      }
+    }
+
+    // ---- act_quant of the row: scale = amax / 448, codes = e4m3(y / scale)
+    float yf[kQ];
+    float amax_y = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      yf[2 * i] = __uint_as_float(yb[i] << 16);
+      yf[2 * i + 1] = __uint_as_float(yb[i] & 0xFFFF0000u);
+      amax_y = fmaxf(amax_y, fmaxf(fabsf(yf[2 * i]), fabsf(yf[2 * i + 1])));
+    }
+    amax_y = fmaxf(amax_y, __shfl_xor_sync(0xffffffffu, amax_y, 1));
+    amax_y = fmaxf(amax_y, __shfl_xor_sync(0xffffffffu, amax_y, 2));
+    const float s = amax_y > 0.f ? __fdiv_rn(amax_y, 448.0f) : 1.0f;
+    const bool small = s < 0x1p-100f;
+    const float s2 = small ? s * 0x1p100f : s;  // exact power-of-two scalings
+    const float inv = __frcp_rn(s2);
+    if (__any_sync(0xffffffffu, small)) {
+      const float ysc = small ? 0x1p100f : 1.0f;
+#pragma unroll
+      for (int i = 0; i < kQ; ++i) yf[i] = __fmul_rn(yf[i], ysc);
+    }
+    uint32_t cw[8];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float q[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float yv = yf[2 * i + k];
+        const float q0 = __fmul_rn(yv, inv);
+        const float rem = __fmaf_rn(-q0, s2, yv);
+        q[k] = __fmaf_rn(rem, inv, q0);
+      }
+      const uint32_t pair = __nv_cvt_float2_to_fp8x2(make_float2(q[0], q[1]), __NV_SATFINITE, __NV_E4M3);
+      cw[i >> 1] = (i & 1) ? (cw[i >> 1] | (pair << 16)) : pair;
+    }
+
+    // ---- destination row, then the codes through the staging tile
+    int64_t d = row;
+    bool ok = row < rows;
+    if (ok && dst) {
+      d = dst[row];
+      if (d < 0 || d >= dst_rows) {
+        if (h == 0) raise_flag(status, kFlagBadIndex);
+        ok = false;
+      }
+    }
+    sts128(code_tile + code_off(lane, 0), make_uint4(cw[0], cw[1], cw[2], cw[3]));
+    sts128(code_tile + code_off(lane, 1), make_uint4(cw[4], cw[5], cw[6], cw[7]));
+    if (ok && h == 0) scales[d] = s;
+    const long long dlane = ok ? d : -1;
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int rr = 4 * k + (lane >> 3), c8 = lane & 7;  // row of the tile, 16-byte chunk of its 128 codes
+      const long long dr = __shfl_sync(0xffffffffu, dlane, 4 * rr);
+      const uint4 v4 = lds128(code_tile + code_off(4 * rr + (c8 >> 1), c8 & 1));
+      if (dr >= 0) *reinterpret_cast<uint4 *>(codes + dr * kDim + c8 * 16) = v4;
+    }
+    __syncwarp();
+  }
 }
 
 }  // namespace
@@ -95,10 +395,13 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int rows, float inv_sqrt_n, 
 cudaError_t launch_rotate_quant(const void *x, int rows, const int32_t *dst, int64_t dst_rows, uint8_t *codes,
                                 float *scales, uint32_t *status, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
-  const float inv_sqrt_n = static_cast<float>(1.0 / std::sqrt(static_cast<double>(kProdDim)));
-  const int blocks = (rows + kProdWarps - 1) / kProdWarps;
-  return launch_ex(false, rotate_quant_kernel, dim3(blocks), dim3(32 * kProdWarps), 0, stream, 1,
-                   static_cast<const uint16_t *>(x), rows, inv_sqrt_n, dst, dst_rows, codes, scales, status);
+  static bool smem_set[64] = {};
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(rotate_quant_kernel), kSmem, smem_set);
+  if (e != cudaSuccess) return e;
+  const int tiles = (rows + kTileRows - 1) / kTileRows;
+  const int blocks = std::min((tiles + kWarps - 1) / kWarps, sm_count() * kCtasPerSm);
+  return launch_ex(false, rotate_quant_kernel, dim3(blocks), dim3(32 * kWarps), kSmem, stream, 1,
+                   static_cast<const uint16_t *>(x), rows, dst, dst_rows, codes, scales, status);
 }
 
 }  // namespace sa

@@ -17,30 +17,67 @@ constexpr size_t kNoAllocScratchBytes = SA_NOALLOC_SCRATCH_BYTES;
 // process exits; every call of sa_fused_decode_noalloc on a device shares it.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
+// Device addresses of g_noalloc_scratch, one per CUDA context that has
+// called in (a device's primary context in the usual case).  In host code the
+// symbol's name is only a host-side handle; the device address comes from
+// cudaGetSymbolAddress, looked up once per context with that context current.
+// Keying on the context rather than the device ordinal keeps the address
+// right after cudaDeviceReset or in a context other than the primary one,
+// where the module is loaded anew and the array may move.
+constexpr int kMaxContexts = 64;
 std::mutex g_setup_mutex;
-void *g_scratch_addr[kMaxDevices] = {};
+CUcontext g_ctx[kMaxContexts] = {};
+void *g_scratch_addr[kMaxContexts] = {};
+int g_n_ctx = 0;
 
-// Device address of g_noalloc_scratch on the current device.  In host code
-// the symbol's name is only a host-side handle; the device address comes from
-// cudaGetSymbolAddress, looked up once per device with that device current.
-cudaError_t scratch_address(void **ptr) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_addr[dev]) {
+using CtxGetCurrent = CUresult (*)(CUcontext *);
+
+CtxGetCurrent ctx_get_current() {
+  static CtxGetCurrent fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrent>(p);
+  });
+  return fn;
+}
+
+cudaError_t scratch_address(void **ptr) {
+  CtxGetCurrent get = ctx_get_current();
+  if (!get) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  if (!ctx) {  // no context current on this thread yet: the runtime makes the device's primary one current
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaSetDevice(dev);
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
+    if (get(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorDeviceUninitialized;
   }
-  *ptr = g_scratch_addr[dev];
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  for (int i = 0; i < g_n_ctx; ++i)
+    if (g_ctx[i] == ctx) {
+      *ptr = g_scratch_addr[i];
+      return cudaSuccess;
+    }
+  void *p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) return e;
+  if (g_n_ctx < kMaxContexts) {
+    g_ctx[g_n_ctx] = ctx;
+    g_scratch_addr[g_n_ctx] = p;
+    ++g_n_ctx;
+  }
+  *ptr = p;
   return cudaSuccess;
 }
 
 }  // namespace
+
+extern "C" size_t sa_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
 extern "C" sa_status sa_fused_decode_noalloc(const sa_index_args *ia, const sa_attn_args *aa,
                                              int32_t K, int32_t *idx_out, void *out,

@@ -90,6 +90,8 @@ def _lib(mutant: int = 0, path: Optional[str] = None):
         lib.orc_candidate_blocks.argtypes = [vp, i32, i32, i32, i32, vp]
         lib.orc_hadamard_bf16.argtypes = [vp, i32, vp]
         lib.orc_hadamard_bf16.restype = i32
+        lib.orc_hadamard_f64.argtypes = [vp, i32, vp]
+        lib.orc_hadamard_f64.restype = i32
         lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
         lib.orc_e4m3_encode.restype = ctypes.c_uint8
         lib.orc_act_quant_row.argtypes = [vp, i32, vp, vp]
@@ -253,12 +255,27 @@ def candidate_topk_row(scores: np.ndarray, nv: int, K: int, keep: np.ndarray, bl
 
 def hadamard_bf16(x_bits: np.ndarray, mutant: int = 0) -> np.ndarray:
     """V3.2 rotate_activation ("DeepSeek-V3.2-Exp inference/model.py"): each row
-    of bf16 bits times the Sylvester-Hadamard matrix, scaled by n^-1/2, in bf16."""
+    of bf16 bits times the Sylvester-Hadamard matrix, scaled by n^-1/2, the
+    exact value rounded once to bf16 (nearest, ties to even)."""
     x = np.ascontiguousarray(x_bits, dtype=np.uint16)
     rows = x.reshape(-1, x.shape[-1])
     out = np.empty_like(rows)
     for i in range(rows.shape[0]):
-        if _lib(mutant).orc_hadamard_bf16(rows[i].ctypes.data, rows.shape[1], out[i].ctypes.data) != 0:
+        rc = _lib(mutant).orc_hadamard_bf16(rows[i].ctypes.data, rows.shape[1], out[i].ctypes.data)
+        if rc == -1:
+            raise ValueError("oracle: row length is not a power of two")
+        if rc != 0:
+            raise ValueError("oracle: the row's dynamic range is beyond the exact evaluation (2^46)")
+    return out.reshape(x.shape)
+
+
+def hadamard_f64(x_bits: np.ndarray) -> np.ndarray:
+    """The same rotation before its rounding to bf16 (float64)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    rows = x.reshape(-1, x.shape[-1])
+    out = np.empty(rows.shape, dtype=np.float64)
+    for i in range(rows.shape[0]):
+        if _lib().orc_hadamard_f64(rows[i].ctypes.data, rows.shape[1], out[i].ctypes.data) != 0:
             raise ValueError("oracle: row length is not a power of two")
     return out.reshape(x.shape)
 

@@ -33,9 +33,9 @@
  *  - the optional attention sink adds exp(sink_h - m) to the softmax
  *    denominator only (parity unpinned: the formula is not on the pages);
  *  - window rows and compressed rows are concatenated, never de-duplicated;
- *  - where floating point decides an integer (the fp8 codes of the producer),
- *    the oracle takes that step in the precision the kernel takes it (fp32,
- *    in a fixed butterfly order) so that the codes compare exactly.
+ *  - the Hadamard rotation of the producer is the exact value rounded once to
+ *    bf16; the producer's act_quant (scale and codes) is taken in fp32, the
+ *    precision of the page's quantiser.
  *
  * Compile-time ORC_MUTANT=n builds deliberately wrong variants; the pin tests
  * build them to show that each plausible mistake fails at least one pin.  The
@@ -296,33 +296,145 @@ static uint16_t bf16_nearest(float f) {
   return (uint16_t)(u >> 16);
 }
 
-/* "DeepSeek-V3.2-Exp inference/model.py", rotate_activation: a bf16 row of n
- * (a power of two) times the Sylvester-Hadamard matrix of order n
- * (H[i][j] = (-1)^popcount(i & j)), scaled by n^-1/2, returned in bf16.
- * Computed in fp32 (reading: the precision of the library the page calls) by
- * the butterfly stages h = 1, 2, 4, ..., n/2, each mapping the pair at
- * positions (i, i + h), i & h == 0, from (a, b) to (a + b, a - b); then each
- * value times the fp32 constant (float)(1 / sqrt(n)), rounded to bf16.  The
- * stage order is fixed so that the fp8 codes derived from the result are
- * reproducible bit for bit. */
+/* bfloat16 bits of sign * c * 2^q (c < 512 a count of quanta 2^q, already
+ * rounded): renormalises a carry into the next binade and saturates to inf. */
+static uint16_t bf16_encode(int sign, uint64_t c, int q) {
+  if (c == 0) return sign ? 0x8000u : 0u;
+  while (c >= 256) { /* only an exact power of two after a carry */
+    c >>= 1;
+    q += 1;
+  }
+  uint16_t bits;
+  if (c < 128) {
+    bits = (uint16_t)c; /* subnormal: q == -133 */
+  } else {
+    const int bexp = q + 7 + 127;
+    bits = bexp >= 255 ? 0x7F80u : (uint16_t)((bexp << 7) | (int)(c - 128));
+  }
+  return sign ? (uint16_t)(bits | 0x8000u) : bits;
+}
+
+static int bitlen_u128(unsigned __int128 a) {
+  int n = 0;
+  while (a) {
+    a >>= 1;
+    ++n;
+  }
+  return n;
+}
+
+/* floor(sqrt(a)) of a 128-bit integer, bit by bit. */
+static unsigned __int128 isqrt_u128(unsigned __int128 a) {
+  unsigned __int128 r = 0;
+  for (int b = 63; b >= 0; --b) {
+    const unsigned __int128 t = r | ((unsigned __int128)1 << b);
+    if (t * t <= a) r = t;
+  }
+  return r;
+}
+
+/* The bfloat16 nearest (ties to even) to v = A * 2^E, times sqrt(2) when
+ * `root2` is set, decided exactly in integer arithmetic.  A < 2^62.  A product
+ * with sqrt(2) is irrational, so it never ties. */
+static uint16_t bf16_round_exact(int sign, uint64_t A, int E, int root2) {
+  if (A == 0) return 0; /* an exact zero is +0 */
+  const unsigned __int128 A2 = (unsigned __int128)A * A;
+  const int L = bitlen_u128(A);
+  int f = L - 1 + E; /* floor(log2 v) */
+  if (root2 && A2 >= ((unsigned __int128)1 << (2 * L - 1))) f += 1;
+  int q = f - 7; /* 8 significant bits */
+  if (q < -133) q = -133;
+  const int s = E - q; /* v / 2^q = A * 2^s (* sqrt 2) */
+  uint64_t c;
+  if (!root2) {
+    if (s >= 0) return bf16_encode(sign, A << s, q);
+    if (-s >= 64) return bf16_encode(sign, 0, q); /* far below half a quantum */
+    const uint64_t fl = A >> -s, rem = A & ((1ull << -s) - 1), half = 1ull << (-s - 1);
+    c = fl + ((rem > half || (rem == half && (fl & 1))) ? 1 : 0);
+    return bf16_encode(sign, c, q);
+  }
+  /* c0 = floor(A sqrt2 2^s) = isqrt(floor(2 A^2 2^(2s))); round up iff
+   * A sqrt2 2^s > c0 + 1/2, i.e. 8 A^2 2^(2s) > (2 c0 + 1)^2 */
+  unsigned __int128 z;
+  if (s >= 0)
+    z = (2 * A2) << (2 * s);
+  else
+    z = (-2 * s >= 127) ? 0 : (2 * A2) >> (-2 * s);
+  const uint64_t c0 = (uint64_t)isqrt_u128(z);
+  const unsigned __int128 odd2 = (unsigned __int128)(2 * c0 + 1) * (2 * c0 + 1);
+  int up;
+  if (s >= 0)
+    up = (8 * A2) << (2 * s) > odd2;
+  else
+    up = (-2 * s >= 120) ? 0 : (8 * A2 > (odd2 << (-2 * s)));
+  c = c0 + (up ? 1 : 0);
+  return bf16_encode(sign, c, q);
+}
+
+/* "DeepSeek-V3.2-Exp inference/model.py", rotate_activation: a bf16 row x of n
+ * values (n a power of two) maps to y = H x * n^-1/2, H the Sylvester-Hadamard
+ * matrix of order n (H[i][j] = (-1)^popcount(i & j)), returned in bf16.
+ * Reading: y is the exact value rounded once to the nearest bfloat16 (ties to
+ * even); the page calls a library whose internal precision and order it does
+ * not show.  Each sum is formed exactly in integers (every bf16 value is an
+ * integer multiple of the row's smallest quantum), then scaled by
+ * n^-1/2 = 2^(-k/2) for n = 2^k (times sqrt 2 when k is odd) and rounded by an
+ * exact comparison.  Returns -1 for a bad n, -2 when the row's exact sums do
+ * not fit in 62 bits (a dynamic range beyond about 2^46 within one row). */
 int32_t orc_hadamard_bf16(const uint16_t *x, int32_t n, uint16_t *y) {
   if (n < 1 || (n & (n - 1))) return -1;
-  float *v = (float *)malloc(sizeof(float) * (size_t)n);
-  for (int32_t i = 0; i < n; ++i) v[i] = (float)orc_bf16_value(x[i]);
-  for (int32_t h = 1; h < n; h <<= 1)
-    for (int32_t i = 0; i < n; ++i)
-      if (!(i & h)) {
-        const float a = v[i], b = v[i + h];
-        v[i] = a + b;
+  int k = 0;
+  while ((1 << k) < n) ++k;
+  /* x_j = m_j * 2^e_j with m_j an integer of at most 8 bits */
+  int64_t *m = (int64_t *)malloc(sizeof(int64_t) * (size_t)n);
+  int *e = (int *)malloc(sizeof(int) * (size_t)n);
+  int emin = 1 << 30, emax = -(1 << 30);
+  for (int32_t j = 0; j < n; ++j) {
+    const int ex = (x[j] >> 7) & 0xFF, man = x[j] & 0x7F;
+    m[j] = ex ? 128 + man : man;
+    e[j] = ex ? ex - 127 - 7 : -133;
+    if (x[j] & 0x8000) m[j] = -m[j];
+    if (m[j] != 0) {
+      if (e[j] < emin) emin = e[j];
+      if (e[j] > emax) emax = e[j];
+    }
+  }
+  int32_t rc = 0;
+  if (emax >= emin && emax - emin + 8 + k > 61) rc = -2;
+  for (int32_t i = 0; i < n && rc == 0; ++i) {
+    int64_t N = 0;
+    for (int32_t j = 0; j < n; ++j) {
+      if (m[j] == 0) continue;
 #if ORC_MUTANT == 12
-        v[i + h] = b - a;
+      const int neg = __builtin_popcount((unsigned)(i ^ j)) & 1; /* wrong sign rule */
 #else
-        v[i + h] = a - b;
+      const int neg = __builtin_popcount((unsigned)(i & j)) & 1;
 #endif
-      }
-  const float sc = (float)(1.0 / sqrt((double)n));
-  for (int32_t i = 0; i < n; ++i) y[i] = bf16_nearest(v[i] * sc);
-  free(v);
+      const int64_t term = m[j] * ((int64_t)1 << (e[j] - emin));
+      N += neg ? -term : term;
+    }
+    const int sign = N < 0;
+    const uint64_t A = (uint64_t)(N < 0 ? -N : N);
+    /* n^-1/2 = 2^(-k/2) for even k, 2^(-(k+1)/2) sqrt 2 for odd k */
+    y[i] = bf16_round_exact(sign, A, emin - (k + 1) / 2, k & 1);
+  }
+  free(e);
+  free(m);
+  return rc;
+}
+
+/* The same rotation without the final rounding, in double (each exact sum
+ * times n^-1/2, one rounding to double): what the bf16 result rounds. */
+int32_t orc_hadamard_f64(const uint16_t *x, int32_t n, double *y) {
+  if (n < 1 || (n & (n - 1))) return -1;
+  for (int32_t i = 0; i < n; ++i) {
+    long double acc = 0.0L; /* the row's sums are exact in 64 bits for the rows tests use */
+    for (int32_t j = 0; j < n; ++j) {
+      const double v = orc_bf16_value(x[j]);
+      acc += (__builtin_popcount((unsigned)(i & j)) & 1) ? -(long double)v : (long double)v;
+    }
+    y[i] = (double)(acc / sqrtl((long double)n));
+  }
   return 0;
 }
 
@@ -548,12 +660,24 @@ static void attn_token(const orc_problem *P, int32_t t, const int32_t *idx_row, 
 #endif
       if (logit[j] > m) m = logit[j];
     }
-    if (P->sink && (double)P->sink[h] > m) m = (double)P->sink[h];
+#if ORC_MUTANT == 21
+    const double sink = P->sink ? (double)P->scale * (double)P->sink[h] : 0.0; /* sink taken as a dot product */
+#else
+    const double sink = P->sink ? (double)P->sink[h] : 0.0;
+#endif
+    if (P->sink && sink > m) m = sink;
     double Z = 0.0;
     for (int32_t j = 0; j < n; ++j) Z += exp(logit[j] - m);
-    if (P->sink) Z += exp((double)P->sink[h] - m);
+#if ORC_MUTANT != 20 /* mutant 20: the sink left out of the denominator */
+    if (P->sink) Z += exp(sink - m);
+#endif
     double *o = O + h * D;
     for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+#if ORC_MUTANT == 19
+    /* the sink taken as a key whose value row is all ones (it joins the numerator too) */
+    if (P->sink)
+      for (int64_t d = 0; d < D; ++d) o[d] += exp(sink - m) / Z;
+#endif
     for (int32_t j = 0; j < n; ++j) {
       const double a = exp(logit[j] - m) / Z;
 #if ORC_MUTANT == 8

@@ -57,6 +57,7 @@ int32_t orc_topk_row(const double *S, int32_t n_vis, int32_t K, int32_t *idx /*[
 int32_t orc_candidate_blocks(const double *S, int32_t n_vis, int32_t N_c, int32_t bs, int32_t topk_blocks,
                              uint8_t *keep /*[ceil(N_c / bs)]*/);
 int32_t orc_hadamard_bf16(const uint16_t *x, int32_t n, uint16_t *y);
+int32_t orc_hadamard_f64(const uint16_t *x, int32_t n, double *y);
 uint8_t orc_e4m3_encode(float v);
 int32_t orc_act_quant_row(const uint16_t *y, int32_t n, uint8_t *codes, float *scale);
 int32_t orc_compress_prefill(const float *kv, const float *score, int32_t S, int32_t D, int32_t r,

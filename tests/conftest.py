@@ -28,3 +28,22 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Prints the worst parity error of each checked quantity (tests/margins.py)."""
+    import margins
+    worst = margins.worst_by_quantity()
+    if not worst:
+        return
+    tr = terminalreporter
+    tr.section("parity margins (worst observed error per quantity)")
+    for q in sorted(worst):
+        v, b, t = worst[q]
+        bound = f"bound {b:.3g}  margin x{b / v:.3g}" if (b is not None and v > 0) else (
+            f"bound {b:.3g}" if b is not None else "reported")
+        tr.write_line(f"{q:44s} {v:11.4g}   {bound:28s} {t}")
+    if config.getoption("verbose") > 0:
+        tr.section("parity margins per test")
+        for t, q, v, b in margins.rows():
+            tr.write_line(f"{t}  {q}: {v:.4g}" + (f" (bound {b:.3g})" if b is not None else ""))

@@ -279,6 +279,43 @@ def pin_attn_sink_dense(mutant=0):
     assert np.allclose(got, _dense_masked(w, idx), rtol=0, atol=1e-12)
 
 
+def pin_attn_sink_limits(mutant=0):
+    """The sink joins the softmax denominator only, so for any sink value s a
+    head's output is the sink-free output times Z / (Z + e^s), with Z the sum of
+    e^l over the attended logits: O_s * (1 + e^(s - LSE)) = O_none (LSE =
+    log Z).  Three limits follow: s -> -inf gives O_none exactly, s = LSE
+    halves it, s -> +inf sends it to 0.  Z is taken here from the logits
+    written out directly (numpy, one dot product per key)."""
+    rng = np.random.default_rng(7)
+    w = _tiny_attn(33, sink=True)
+    idx = _random_unique_idx(w, 5, rng)
+    none = _tiny_attn(33, sink=False)
+    O0 = oracle.sparse_attn(problem(none), idx, mutant=mutant)
+    Q, Kw, Kc = bf16_to_f64(w.Q), bf16_to_f64(w.Kw), bf16_to_f64(w.Kc)
+    lse = np.zeros((w.T, w.H))
+    for t in range(w.T):
+        b, p = int(w.q_seq[t]), int(w.q_pos[t])
+        keys = [Kw[b, pp % w.R] for pp in range(max(0, p - w.W + 1), p + 1)]
+        keys += [Kc[b, c] for c in idx[t] if c >= 0]
+        lg = (Q[t] @ np.array(keys).T) * float(w.scale)          # [H, n]
+        mx = lg.max(axis=1)
+        lse[t] = mx + np.log(np.exp(lg - mx[:, None]).sum(axis=1))
+    # s -> -inf: the sink-free output, exactly
+    w.sink = np.full(w.H, -1e30, dtype=np.float32)
+    assert np.array_equal(oracle.sparse_attn(problem(w), idx, mutant=mutant), O0)
+    # s -> +inf: nothing left of the output
+    w.sink = np.full(w.H, 1e30, dtype=np.float32)
+    assert np.array_equal(oracle.sparse_attn(problem(w), idx, mutant=mutant), np.zeros_like(O0))
+    # s = LSE (one token's values, rounded to the sink's fp32): O_none / (1 + e^(s - LSE))
+    for t in range(w.T):
+        w.sink = lse[t].astype(np.float32)
+        s = w.sink.astype(np.float64)
+        Os = oracle.sparse_attn(problem(w), idx, rows=[t], mutant=mutant)[0]
+        want = O0[t] / (1.0 + np.exp(s - lse[t]))[:, None]
+        assert np.allclose(Os, want, rtol=1e-12, atol=1e-14), (t, np.abs(Os - want).max())
+        assert np.allclose(Os, O0[t] / 2, rtol=1e-6, atol=1e-14)
+
+
 def pin_attn_all_visible_identity(mutant=0):
     """With K >= n_vis the selected set is every visible
     position, so the step equals dense attention over the window plus all
@@ -332,5 +369,5 @@ def pin_attn_special_cases(mutant=0):
 ALL_PINS = [pin_bf16_exhaustive, pin_e4m3_exhaustive, pin_format_golden, pin_window_golden,
             pin_visibility_forms, pin_window_rule, pin_scores_exact, pin_scores_closed_form,
             pin_scores_head_permutation, pin_topk_bruteforce, pin_attn_dense_masked,
-            pin_attn_sink_dense, pin_attn_all_visible_identity, pin_attn_weights_sum_to_one,
+            pin_attn_sink_dense, pin_attn_sink_limits, pin_attn_all_visible_identity, pin_attn_weights_sum_to_one,
             pin_attn_special_cases]

@@ -1,11 +1,16 @@
 """The V3.2 index producer on the GPU (Hadamard rotation and e4m3 block
 quantisation, "DeepSeek-V3.2-Exp inference/model.py", Indexer.forward): codes
-and scales equal the oracle's bit for bit, rows scatter to their cache rows,
+and scales equal the oracle's bit for bit -- the oracle rounds the exact
+rotation once to bf16 -- except on rows where the exact rotation lies within
+2^-40 of its own size of a bf16 rounding midpoint, where the kernel's exact
+fallback (64-bit integer sums, one double product) may round either way;
+such rows are counted and must be rare.  Rows scatter to their cache rows,
 and bad destinations are skipped and flagged (GPU only)."""
 import numpy as np
 import pytest
 import torch
 
+import margins
 import oracle
 from gpu_run import ensure_built
 from indexer_selected_sparse_score_gb300 import binding
@@ -38,23 +43,52 @@ def run(x_bits, dst=None, dst_rows=0, fill=0x55):
 
 
 def special_rows():
+    rng = np.random.default_rng(99)
+    tiny = rng.normal(size=128)
+    tiny[::9] *= 2.0 ** -30          # elements far below the row's largest
     rows = [np.zeros(128), np.full(128, -0.0), np.eye(128)[5], np.full(128, 0.75), -np.eye(128)[127] * 3e4,
-            np.linspace(-1e-20, 1e-20, 128), np.where(np.arange(128) % 2, 1e30, -1e30)]
+            np.linspace(-1e-20, 1e-20, 128), np.where(np.arange(128) % 2, 1e30, -1e30),
+            rng.normal(size=128) * 1e33, rng.normal(size=128) * 1e-33, tiny,
+            np.round(rng.normal(size=128) * 8) / 8]
     return bf16_bits(np.stack(rows))
 
 
-@pytest.mark.parametrize("rows", [1, 7, 8, 1000, 4103])
+N_SPECIAL = 11
+
+
+def near_midpoint_rows(xb):
+    """Rows whose exact rotation has an element within 2^-40 of its size of a
+    bf16 rounding midpoint (where a rounding decision taken from a value with
+    relative error below 2^-40 may go either way)."""
+    y = oracle.hadamard_f64(xb)
+    yr = oracle.hadamard_bf16(xb).astype(np.uint32)
+    val = (yr << 16).view(np.float32).astype(np.float64)
+    mag = (yr & 0x7FFF).astype(np.int64)
+    neighbour = []
+    for step in (-1, 1):
+        o = np.where(yr & 0x8000, -mag, mag) + step
+        b = np.where(o < 0, 0x8000 | (-o), o).astype(np.uint32)
+        neighbour.append((b << 16).view(np.float32).astype(np.float64))
+    dist = np.minimum(np.abs(y - (val + neighbour[0]) / 2), np.abs(y - (val + neighbour[1]) / 2))
+    return np.any(dist <= 2.0 ** -40 * np.abs(y), axis=1)
+
+
+@pytest.mark.parametrize("rows", [1, 7, 8, 33, 1000, 4103])
 def test_codes_and_scales_exact(rows):
     rng = np.random.default_rng(rows)
     x = rng.normal(size=(rows, 128)) * np.exp(rng.uniform(-8, 8, size=(rows, 1)))
     xb = bf16_bits(x)
-    if rows >= 8:
-        xb[:7] = special_rows()
+    if rows >= N_SPECIAL:
+        xb[:N_SPECIAL] = special_rows()
     codes, scales, st = run(xb)
     assert st == binding.SA_OK
     want_c, want_s = oracle.rotate_quant_rows(xb)
-    assert np.array_equal(scales.view(np.uint32), want_s.view(np.uint32))
-    assert np.array_equal(codes, want_c)
+    near = near_midpoint_rows(xb)
+    margins.record("producer rows near a bf16 midpoint (share)", float(near.mean()), 0.01)
+    assert near.mean() <= 0.01
+    ok = ~near
+    assert np.array_equal(scales[ok].view(np.uint32), want_s[ok].view(np.uint32))
+    assert np.array_equal(codes[ok], want_c[ok])
 
 
 def test_scatter_to_cache_rows():

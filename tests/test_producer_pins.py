@@ -1,8 +1,12 @@
 """Pins for the oracle of the V3.2 index producer ("DeepSeek-V3.2-Exp
 inference/model.py", rotate_activation and act_quant in Indexer.forward):
-the Hadamard rotation against scipy's Sylvester matrix and closed forms, the
+the Hadamard rotation against scipy's Sylvester matrix, an exact evaluation in
+Python integers rounded in decimal arithmetic, and closed forms, the
 e4m3 encoder exhaustively against the format's decoder and torch's cast, and
 the block quantisation against its defining properties."""
+from decimal import Decimal, getcontext
+from fractions import Fraction
+
 import numpy as np
 import pytest
 import torch
@@ -30,9 +34,51 @@ def pin_hadamard_matrix(n=128, mutant=0):
     xv = bf16_values(x)
     exact = xv @ scipy_linalg.hadamard(n).T.astype(np.float64) / np.sqrt(n)
     got = bf16_values(oracle.hadamard_bf16(x, mutant))
-    # bf16 rounding of the result plus the fp32 butterfly's rounding (log2 n stages)
-    bound = 2.0 ** -8 * np.abs(exact) + 2.0 ** -21 * np.abs(xv).sum(axis=1, keepdims=True)
+    # one rounding to bf16: within half a bf16 step, at most 2^-8 of the value
+    # (plus the float64 evaluation of `exact` here)
+    bound = 2.0 ** -8 * np.abs(exact) + 2.0 ** -40 * np.abs(xv).sum(axis=1, keepdims=True)
     assert np.all(np.abs(got - exact) <= bound)
+
+
+def _exact_bf16(num: int, den_pow2: int, n: int) -> float:
+    """The bfloat16 nearest (ties to even) to num * 2^-den_pow2 * n^-1/2,
+    decided in 80-digit decimal arithmetic against the neighbouring bf16
+    values (an evaluation independent of the oracle's integer rounding)."""
+    if num == 0:
+        return 0.0
+    getcontext().prec = 80
+    y = Decimal(num) / (Decimal(2) ** den_pow2) / Decimal(n).sqrt()
+    c = int(to_bf16_bits(np.array([float(y)], dtype=np.float32))[0])
+    cand = [float(bf16_values(np.array([b], dtype=np.uint16))[0]) for b in (c - 1, c, c + 1) if 0 <= b <= 0xFFFF]
+    cand = [v for v in cand if np.isfinite(v) and np.sign(v) == np.sign(float(y))]
+    dist = sorted((abs(Decimal(v) - y), v) for v in cand)
+    if dist[0][0] == dist[1][0]:   # a tie: the value with the even last bit
+        return [v for d, v in dist[:2] if int(to_bf16_bits(np.array([v], dtype=np.float32))[0]) % 2 == 0][0]
+    return dist[0][1]
+
+
+def pin_hadamard_exact_rounding(mutant=0):
+    """Each output is the exact sum H x (in Python integers) times n^-1/2,
+    rounded once to the nearest bf16 (ties to even): for odd and even log2 n,
+    on rows of several scales and with exact ties (n = 64: y = S / 8)."""
+    rng = np.random.default_rng(11)
+    for n in (2, 8, 64, 128, 256):
+        H = scipy_linalg.hadamard(n).astype(np.int64)
+        rows = rng.normal(size=(6, n)) * rng.choice([1e-30, 1e-3, 1.0, 3e4], size=(6, 1))
+        rows[0] = np.round(rng.normal(size=n) * 4) / 4   # coarse values: ties when n = 64
+        x = to_bf16_bits(rows)
+        got = bf16_values(oracle.hadamard_bf16(x, mutant))
+        xv = bf16_values(x)
+        for i in range(x.shape[0]):
+            xi = [int(Fraction(float(v)) * 2 ** 140) for v in xv[i]]   # every bf16 value is k * 2^-140
+            for o in range(n):
+                S = sum(int(H[o, j]) * xi[j] for j in range(n))
+                want = _exact_bf16(S, 140, n)
+                assert got[i, o] == want and (want != 0.0 or not np.signbit(got[i, o])), (n, i, o, got[i, o], want)
+
+
+def test_hadamard_exact_rounding():
+    pin_hadamard_exact_rounding()
 
 
 @pytest.mark.parametrize("n", [2, 8, 128])
@@ -42,17 +88,24 @@ def test_hadamard_matches_sylvester_matrix(n):
 
 def test_hadamard_closed_forms():
     n = 128
-    sc = np.float32(1.0 / np.sqrt(n))
-    # a unit vector e_j maps to column j of H times n^-1/2
+    # a unit vector e_j maps to column j of H times n^-1/2: +-bf16(128^-1/2)
+    one = _exact_bf16(1, 0, n)
+    assert one == 0.08837890625           # 128^-1/2 = 0.0883883..., nearest bf16 181 * 2^-11
     for j in (0, 1, 77, 127):
         x = np.zeros(n, dtype=np.float32)
         x[j] = 1.0
         got = bf16_values(oracle.hadamard_bf16(to_bf16_bits(x)[None])[0])
-        want = bf16_values(to_bf16_bits(scipy_linalg.hadamard(n)[:, j] * sc))
-        assert np.array_equal(got, want)
-    # a constant vector maps to sqrt(n) c e_0 (the sums are exact in fp32 here)
+        assert np.array_equal(got, scipy_linalg.hadamard(n)[:, j] * one)
+    # a constant vector c maps to sqrt(n) c e_0: 0.75 * 128^1/2 = 8.485..., nearest bf16 8.5
     got = bf16_values(oracle.hadamard_bf16(to_bf16_bits(np.full(n, 0.75))[None])[0])
-    assert got[0] == bf16_values(to_bf16_bits(np.float32(0.75 * n) * sc)) and not got[1:].any()
+    assert got[0] == 8.5 and not got[1:].any() and not np.signbit(got[1:]).any()
+
+
+def test_hadamard_rejects_rows_beyond_its_exact_range():
+    x = np.zeros(128, dtype=np.float32)
+    x[0], x[1] = 1e30, 1e-30
+    with pytest.raises(ValueError):
+        oracle.hadamard_bf16(to_bf16_bits(x)[None])
 
 
 def test_hadamard_is_an_involution():
@@ -115,7 +168,7 @@ def test_act_quant_properties():
     assert s0[0] == 1.0 and not c0.any()
 
 
-PRODUCER_MUTANTS = {12: "butterfly difference reversed", 13: "ties away from zero", 14: "scale for a max of 240"}
+PRODUCER_MUTANTS = {12: "Hadamard sign from popcount(i ^ j)", 13: "ties away from zero", 14: "scale for a max of 240"}
 
 
 @pytest.mark.parametrize("mutant", sorted(PRODUCER_MUTANTS), ids=lambda m: PRODUCER_MUTANTS[m].replace(" ", "_"))
@@ -125,7 +178,7 @@ def test_producer_mutant_is_caught(mutant):
     oracle._lib(mutant, path)
     oracle._LIBS[mutant] = oracle._LIBS[path]
     failed = []
-    for pin in (pin_hadamard_matrix, pin_e4m3_ties, pin_act_quant):
+    for pin in (pin_hadamard_matrix, pin_hadamard_exact_rounding, pin_e4m3_ties, pin_act_quant):
         try:
             pin(mutant=mutant)
         except (AssertionError, ValueError):

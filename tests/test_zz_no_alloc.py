@@ -14,19 +14,17 @@ import torch
 from gpu_run import ensure_built
 from indexer_selected_sparse_score_gb300 import binding
 from indexer_selected_sparse_score_gb300 import workloads as wl
-from tolerances import ATTN_RTOL, BF16_HALF_ULP_REL
+from tolerances import check_attn
 
 pytestmark = pytest.mark.gpu
 
 
 def _outputs_close(g, ref):
-    g = g.float().cpu().numpy().astype(np.float64)
-    ref = ref.float().cpu().numpy().astype(np.float64)
-    rowmax = np.abs(ref).max(axis=-1, keepdims=True)
-    assert np.all(np.abs(g - ref) <= BF16_HALF_ULP_REL * np.abs(ref) + ATTN_RTOL * rowmax)
+    """g within the parity tests' attention tolerance of ref (two bf16 outputs)."""
+    check_attn(g.float().cpu().numpy().astype(np.float64), ref.float().cpu().numpy().astype(np.float64))
 
 
-@pytest.mark.parametrize("name", ["c1", "c2"])
+@pytest.mark.parametrize("name", ["c1", "c2", "c4"])
 def test_noalloc_matches_workspace_path_twice(name):
     ensure_built()
     w = wl.generate(wl.CONFIGS[name])
@@ -51,6 +49,16 @@ def test_noalloc_matches_workspace_path_twice(name):
     binding.sa_fused_decode_noalloc(dp.ia, dp.aa, w.K, None, out, None)
     torch.cuda.synchronize()
     _outputs_close(out, out_ref)
+    if name == "c1":  # small enough to check every token against the oracle as well
+        import oracle
+        from helpers import n_vis, problem
+        from tolerances import check_topk_sets
+        S, A = oracle.index_scores(problem(w), with_magnitude=True)
+        o_idx = oracle.topk(problem(w), S, w.K)
+        g_idx = idx.cpu().numpy()
+        for t in range(w.T):
+            check_topk_sets(g_idx[t], o_idx[t], S[t], A[t], n_vis(int(w.q_pos[t]), w.r), w.K)
+        check_attn(out.float().cpu().numpy().astype(np.float64), oracle.sparse_attn(problem(w), g_idx))
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
@@ -68,4 +76,15 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
 
 
 def lib_scratch_bytes():
-    return 32 << 20  # SA_NOALLOC_SCRATCH_BYTES in include/sa.h
+    return binding.sa_noalloc_scratch_bytes()
+
+
+def test_scratch_size_matches_the_header():
+    """The compiled size equals SA_NOALLOC_SCRATCH_BYTES as include/sa.h states it."""
+    import os
+    import re
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "sa.h")).read()
+    m = re.search(r"#define SA_NOALLOC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", hdr)
+    assert m, "SA_NOALLOC_SCRATCH_BYTES not found in include/sa.h"
+    ensure_built()
+    assert lib_scratch_bytes() == int(m.group(1)) << int(m.group(2))
