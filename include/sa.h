@@ -84,9 +84,16 @@ typedef struct {
   const float *w;      /* [T, H_I] head weights, used as given (callers fold
                           softmax_scale * H_I^-0.5 and any q scale into them
                           or pass q_scale) */
-  const void *k_I;     /* [B, N_c, D_I] index keys, bf16 or fp8-e4m3fn */
+  const void *k_I;     /* [B, N_c, D_I] index keys, bf16 or fp8-e4m3fn (rows of sequence b
+                          start k_seq_stride elements after those of b - 1) */
   int32_t k_dtype;     /* sa_dtype of k_I */
-  const float *k_scale; /* [B, N_c] dequantisation scale of each key row (> 0), or NULL for 1 */
+  const float *k_scale; /* [B, N_c] dequantisation scale of each key row (> 0), or NULL for 1;
+                           sequence stride k_seq_stride / D_I */
+  int64_t k_seq_stride; /* elements of k_I between consecutive sequences: 0 for dense
+                           (N_c * D_I), else a multiple of D_I of at least N_c * D_I -- e.g. a
+                           cache allocated for max_seq_len / r rows of which N_c are in use
+                           ("DeepSeek-V4.1-Flash-NVFP4 inference/model.py", Indexer.__init__
+                           k_cache and Indexer.forward index_k[:bsz, :end_pos // ratio]) */
 } sa_index_args;
 
 /* Attention inputs: one shared KV head across H query heads
@@ -107,6 +114,12 @@ typedef struct {
                           and Vc == Kc -- V4.1's single kv -- each row is read once) */
   const float *sink;   /* [H] per-head attention sink logit, or NULL for none */
   float scale;         /* softmax scale applied to Q.K (e.g. D^-0.5) */
+  int64_t w_seq_stride; /* elements of Kw / Vw between consecutive sequences: 0 for dense
+                           (R * D), else a multiple of D of at least R * D */
+  int64_t c_seq_stride; /* elements of Kc / Vc between consecutive sequences: 0 for dense
+                           (N_c * D), else a multiple of D of at least N_c * D ("DeepSeek-V4.1-
+                           Flash-NVFP4 inference/model.py", Attention.__init__ compress_kv_cache
+                           of max_seq_len / ratio rows) */
 } sa_attn_args;
 
 /* Bytes of workspace the calls below need for these shapes and this K
@@ -125,10 +138,12 @@ SA_API sa_status sa_workspace_init(void *ws, size_t ws_bytes, sa_stream_t stream
  *   scores[t, s] = sum_h w[t,h] * ReLU( sum_d q[t,h,d] q_scale[t,h] * k[b,s,d] k_scale[b,s] )
  *
  * for s < n_vis(t) (b = q_seq[t]) and -inf for n_vis(t) <= s < N_c.
- * scores: [T, N_c] fp32, device, written in full.  Arithmetic: the products
- * are exact in fp32 and accumulated in fp32. */
-SA_API sa_status sa_indexer_scores(const sa_index_args *ia, float *scores, void *ws, size_t ws_bytes,
-                            sa_stream_t stream);
+ * scores: [T, ld] fp32, device; columns 0 .. N_c - 1 of every row are written,
+ * the rest untouched.  ld >= N_c (a multiple of 4 keeps rows 16-byte aligned,
+ * which the top-k entry points read fastest).  Arithmetic: the products are
+ * exact in fp32 and accumulated in fp32. */
+SA_API sa_status sa_indexer_scores(const sa_index_args *ia, float *scores, int64_t ld, void *ws,
+                                   size_t ws_bytes, sa_stream_t stream);
 
 /* Per-query top-k ("DeepSeek-V4.1-Flash-NVFP4 inference/model.py",
  * Indexer.forward: topk = min(index_topk, n_vis); the picks re-sorted into
@@ -136,10 +151,11 @@ SA_API sa_status sa_indexer_scores(const sa_index_args *ia, float *scores, void 
  * K_eff = min(K, n_vis(t)) positions s < n_vis(t) with the highest
  * scores[t, s] (ties: the lower position wins) and writes them in ascending
  * order to idx[t, 0 .. K_eff), then -1 to idx[t, K_eff .. K).
- * scores: [T, N_c] fp32 (only s < n_vis(t) is read); idx: [T, K] int32.
- * K may be 0.  The selection is exact on the fp32 values (no tolerance). */
-SA_API sa_status sa_topk(const float *scores, const sa_index_args *ia, int32_t K, int32_t *idx, void *ws,
-                  size_t ws_bytes, sa_stream_t stream);
+ * scores: [T, ld] fp32, ld >= N_c (only s < n_vis(t) is read); idx: [T, K]
+ * int32.  K may be 0.  The selection is exact on the fp32 values (no
+ * tolerance). */
+SA_API sa_status sa_topk(const float *scores, int64_t ld, const sa_index_args *ia, int32_t K, int32_t *idx,
+                         void *ws, size_t ws_bytes, sa_stream_t stream);
 
 /* Two-level top-k, level one ("DeepSeek-V4.1-Flash-NVFP4 inference/model.py",
  * select_candidate_blocks, called by Indexer.forward in the layer that is the
@@ -151,12 +167,12 @@ SA_API sa_status sa_topk(const float *scores, const sa_index_args *ia, int32_t K
  * highest-scoring blocks are taken (ties: the lower block wins) and those
  * scoring -inf are dropped.  A kept block b sets bit b % 32 of cand[t, b / 32];
  * every other bit of the row, those past nb included, is 0.
- * scores: [T, N_c] fp32 (only s < n_vis(t) is read; NaN scores give
+ * scores: [T, ld] fp32, ld >= N_c (only s < n_vis(t) is read; NaN scores give
  * unspecified picks); cand: [T, sa_candidate_words(N_c, block_size)] uint32,
  * written in full.  block_size >= 1, topk_blocks >= 0; nb > 32768 or
  * N_c > 2^30 returns SA_ERR_UNSUPPORTED.  The selection is exact on the fp32 values.  The
  * workspace needs only its 256-byte header (the status word). */
-SA_API sa_status sa_candidate_blocks(const float *scores, const sa_index_args *ia, int32_t block_size,
+SA_API sa_status sa_candidate_blocks(const float *scores, int64_t ld, const sa_index_args *ia, int32_t block_size,
                                      int32_t topk_blocks, uint32_t *cand, void *ws, size_t ws_bytes,
                                      sa_stream_t stream);
 
@@ -175,7 +191,7 @@ SA_API int32_t sa_candidate_words(int32_t N_c, int32_t block_size);
  * sa_candidate_blocks (of this or another layer's scores).  N_c > 2^30
  * returns SA_ERR_UNSUPPORTED.  Other arguments and the output as for
  * sa_topk. */
-SA_API sa_status sa_topk_candidates(const float *scores, const sa_index_args *ia, int32_t K,
+SA_API sa_status sa_topk_candidates(const float *scores, int64_t ld, const sa_index_args *ia, int32_t K,
                                     const uint32_t *cand, int32_t block_size, int32_t *idx, void *ws,
                                     size_t ws_bytes, sa_stream_t stream);
 

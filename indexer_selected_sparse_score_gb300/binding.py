@@ -45,6 +45,7 @@ class IndexArgs(ctypes.Structure):
         ("q_I", ctypes.c_void_p), ("q_dtype", ctypes.c_int32), ("q_scale", ctypes.c_void_p),
         ("w", ctypes.c_void_p),
         ("k_I", ctypes.c_void_p), ("k_dtype", ctypes.c_int32), ("k_scale", ctypes.c_void_p),
+        ("k_seq_stride", ctypes.c_int64),
     ]
 
 
@@ -54,6 +55,7 @@ class AttnArgs(ctypes.Structure):
         ("Q", ctypes.c_void_p), ("Kw", ctypes.c_void_p), ("Vw", ctypes.c_void_p),
         ("Kc", ctypes.c_void_p), ("Vc", ctypes.c_void_p),
         ("sink", ctypes.c_void_p), ("scale", ctypes.c_float),
+        ("w_seq_stride", ctypes.c_int64), ("c_seq_stride", ctypes.c_int64),
     ]
 
 
@@ -81,12 +83,13 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.sa_workspace_size.argtypes = [IA, AA, i32]
     lib.sa_workspace_size.restype = sz
     lib.sa_workspace_init.argtypes = [vp, sz, vp]
-    lib.sa_indexer_scores.argtypes = [IA, vp, vp, sz, vp]
-    lib.sa_topk.argtypes = [vp, IA, i32, vp, vp, sz, vp]
-    lib.sa_candidate_blocks.argtypes = [vp, IA, i32, i32, vp, vp, sz, vp]
+    i64 = ctypes.c_int64
+    lib.sa_indexer_scores.argtypes = [IA, vp, i64, vp, sz, vp]
+    lib.sa_topk.argtypes = [vp, i64, IA, i32, vp, vp, sz, vp]
+    lib.sa_candidate_blocks.argtypes = [vp, i64, IA, i32, i32, vp, vp, sz, vp]
     lib.sa_candidate_words.argtypes = [i32, i32]
     lib.sa_candidate_words.restype = i32
-    lib.sa_topk_candidates.argtypes = [vp, IA, i32, vp, i32, vp, vp, sz, vp]
+    lib.sa_topk_candidates.argtypes = [vp, i64, IA, i32, vp, i32, vp, vp, sz, vp]
     lib.sa_rotate_quant.argtypes = [vp, i32, i32, vp, ctypes.c_int64, vp, vp, vp, sz, vp]
     lib.sa_compress_prefill.argtypes = [vp, vp, i32, i32, i32, i32, vp, ctypes.c_float, vp, vp]
     lib.sa_sparse_attn.argtypes = [IA, AA, vp, i32, vp, vp, sz, vp]
@@ -147,14 +150,23 @@ def sa_workspace_init(ws, stream=None) -> None:
     _check(load().sa_workspace_init(p, n, _s(stream)))
 
 
-def sa_indexer_scores(ia: IndexArgs, scores, ws, stream=None) -> None:
-    p, n = _ws(ws)
-    _check(load().sa_indexer_scores(ctypes.byref(ia), _p(scores), p, n, _s(stream)))
+def _ld(scores, ld, ia) -> int:
+    """Row stride of a score matrix: as given, else that of a 2-D tensor, else N_c."""
+    if ld is not None:
+        return int(ld)
+    if isinstance(scores, torch.Tensor) and scores.dim() == 2:
+        return int(scores.stride(0))
+    return int(ia.N_c)
 
 
-def sa_topk(scores, ia: IndexArgs, K: int, idx, ws, stream=None) -> None:
+def sa_indexer_scores(ia: IndexArgs, scores, ws, stream=None, ld=None) -> None:
     p, n = _ws(ws)
-    _check(load().sa_topk(_p(scores), ctypes.byref(ia), K, _p(idx), p, n, _s(stream)))
+    _check(load().sa_indexer_scores(ctypes.byref(ia), _p(scores), _ld(scores, ld, ia), p, n, _s(stream)))
+
+
+def sa_topk(scores, ia: IndexArgs, K: int, idx, ws, stream=None, ld=None) -> None:
+    p, n = _ws(ws)
+    _check(load().sa_topk(_p(scores), _ld(scores, ld, ia), ctypes.byref(ia), K, _p(idx), p, n, _s(stream)))
 
 
 def sa_candidate_words(N_c: int, block_size: int) -> int:
@@ -162,19 +174,20 @@ def sa_candidate_words(N_c: int, block_size: int) -> int:
 
 
 def sa_candidate_blocks(scores, ia: IndexArgs, block_size: int, topk_blocks: int, cand, ws,
-                        stream=None) -> None:
+                        stream=None, ld=None) -> None:
     """Level one of the two-level top-k: ``cand`` ([T, sa_candidate_words] int32
     or uint32) receives one bit per kept block."""
     p, n = _ws(ws)
-    _check(load().sa_candidate_blocks(_p(scores), ctypes.byref(ia), block_size, topk_blocks, _p(cand), p, n,
-                                      _s(stream)))
+    _check(load().sa_candidate_blocks(_p(scores), _ld(scores, ld, ia), ctypes.byref(ia), block_size, topk_blocks,
+                                      _p(cand), p, n, _s(stream)))
 
 
-def sa_topk_candidates(scores, ia: IndexArgs, K: int, cand, block_size: int, idx, ws, stream=None) -> None:
+def sa_topk_candidates(scores, ia: IndexArgs, K: int, cand, block_size: int, idx, ws, stream=None,
+                       ld=None) -> None:
     """Level two: sa_topk with the scores outside the kept blocks of ``cand`` at -inf."""
     p, n = _ws(ws)
-    _check(load().sa_topk_candidates(_p(scores), ctypes.byref(ia), K, _p(cand), block_size, _p(idx), p, n,
-                                     _s(stream)))
+    _check(load().sa_topk_candidates(_p(scores), _ld(scores, ld, ia), ctypes.byref(ia), K, _p(cand), block_size,
+                                     _p(idx), p, n, _s(stream)))
 
 
 def sa_rotate_quant(x, rows: int, codes, scales, ws, dst=None, dst_rows: int = 0, dim: int = 128,
@@ -255,15 +268,40 @@ class DeviceProblem:
     D: int
 
 
-def upload(w, device="cuda", K: Optional[int] = None) -> DeviceProblem:
-    """Copy a workload (host numpy arrays in storage formats) to the device."""
-    names = ("q_seq", "q_pos", "q_I", "q_scale", "w", "k_I", "k_scale", "Q", "Kw", "Vw", "Kc", "Vc", "sink")
+def _padded(a: Optional[np.ndarray], rows: int, device, fill: int = 0x55):
+    """[B, n, ...] host array into a device tensor of [B, rows, ...] (rows >= n),
+    the extra rows filled with a byte pattern; returns (tensor, view of the used rows)."""
+    if a is None:
+        return None, None
+    src = torch.from_numpy(np.ascontiguousarray(a))
+    full = torch.empty((a.shape[0], rows) + tuple(a.shape[2:]), dtype=src.dtype, device=device)
+    full.view(torch.uint8).fill_(fill)
+    full[:, :a.shape[1]].copy_(src.to(device))
+    return full, full[:, :a.shape[1]]
+
+
+def upload(w, device="cuda", K: Optional[int] = None, pad: Optional[dict] = None) -> DeviceProblem:
+    """Copy a workload (host numpy arrays in storage formats) to the device.
+
+    ``pad`` places caches in larger allocations, as a model keeps them:
+    {"k": rows, "w": rows, "c": rows} allocates that many rows per sequence for
+    the index keys (and their scales), the raw ring and the compressed cache,
+    and passes the matching sequence strides."""
+    pad = pad or {}
+    names = ("q_seq", "q_pos", "q_I", "q_scale", "w", "Q", "sink")
     t = {n: _dev(getattr(w, n), device) for n in names}
+    kr, wr, cr = pad.get("k", w.N_c), pad.get("w", w.R), pad.get("c", w.N_c)
+    t["k_I"], _ = _padded(w.k_I, kr, device)
+    t["k_scale"], _ = _padded(w.k_scale, kr, device)
+    for n in ("Kw", "Vw"):
+        t[n], _ = _padded(getattr(w, n), wr, device)
+    for n in ("Kc", "Vc"):
+        t[n], _ = _padded(getattr(w, n), cr, device)
     ia = IndexArgs(w.B, w.T, w.H_I, w.D_I, w.N_c, w.r, _p(t["q_seq"]), _p(t["q_pos"]),
                    _p(t["q_I"]), w.q_dtype, _p(t["q_scale"]), _p(t["w"]),
-                   _p(t["k_I"]), w.k_dtype, _p(t["k_scale"]))
+                   _p(t["k_I"]), w.k_dtype, _p(t["k_scale"]), kr * w.D_I if "k" in pad else 0)
     aa = AttnArgs(w.H, w.D, w.W, w.R, _p(t["Q"]), _p(t["Kw"]), _p(t["Vw"]), _p(t["Kc"]), _p(t["Vc"]),
-                  _p(t["sink"]), float(w.scale))
+                  _p(t["sink"]), float(w.scale), wr * w.D if "w" in pad else 0, cr * w.D if "c" in pad else 0)
     return DeviceProblem(t, ia, aa, w.K if K is None else K, w.T, w.H, w.D)
 
 

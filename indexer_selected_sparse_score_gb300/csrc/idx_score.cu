@@ -23,7 +23,7 @@ constexpr int kScoreThreads = 128;
 
 template <int DI, bool QFP8, bool KFP8>
 __global__ void __launch_bounds__(kScoreThreads)
-idx_score_simt_kernel(int B, int H_I, int N_c, int r, const int32_t *__restrict__ q_seq,
+idx_score_simt_kernel(int B, int H_I, int N_c, int64_t kseq, int r, const int32_t *__restrict__ q_seq,
                       const int32_t *__restrict__ q_pos, const void *__restrict__ q_I,
                       const float *__restrict__ q_scale, const float *__restrict__ w,
                       const void *__restrict__ k_I, const float *__restrict__ k_scale,
@@ -66,7 +66,7 @@ idx_score_simt_kernel(int B, int H_I, int N_c, int r, const int32_t *__restrict_
     return;
   }
 
-  const int64_t krow = static_cast<int64_t>(tk.b) * N_c + s;
+  const int64_t krow = static_cast<int64_t>(tk.b) * kseq + s;  // kseq: key rows per sequence
   float kf[DI];
   if (KFP8) {
     const uint4 *kp = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(k_I) + krow * DI);
@@ -124,7 +124,7 @@ cudaError_t launch_simt(const sa_index_args &ia, float *scores, int64_t ld, bool
     if (e != cudaSuccess) return e;
   }
   dim3 grid((ia.N_c + kScoreThreads - 1) / kScoreThreads, ia.T);
-  kern<<<grid, kScoreThreads, smem, stream>>>(ia.B, ia.H_I, ia.N_c, ia.r, ia.q_seq, ia.q_pos,
+  kern<<<grid, kScoreThreads, smem, stream>>>(ia.B, ia.H_I, ia.N_c, k_rows_per_seq(ia), ia.r, ia.q_seq, ia.q_pos,
                                               ia.q_I, ia.q_scale, ia.w, ia.k_I, ia.k_scale,
                                               scores, ld, write_masked ? 1 : 0, status);
   return cudaGetLastError();

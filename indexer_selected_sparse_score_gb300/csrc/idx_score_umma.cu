@@ -313,6 +313,7 @@ idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq
 
 struct ScoreParams {
   int B, T, N_c, r;
+  int kseq;  // key rows between consecutive sequences (k_I and k_scale)
   const int32_t *q_seq, *q_pos;
   const int32_t *prefix;  // tiles before each token, written by the prep kernel
   const uint8_t *qpack;
@@ -509,11 +510,11 @@ idx_score_umma_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreParam
       if (lane == 0) {
         info[k] = make_int4(t, s0, nv, qn);
         mbar_expect_tx(&kfull[s], kKeyTileBytes);
-        tma_load_2d_hint(keys + s * kKeyTileBytes, &kmap, &kfull[s], 0, b * p.N_c + s0, kpol);
+        tma_load_2d_hint(keys + s * kKeyTileBytes, &kmap, &kfull[s], 0, b * p.kseq + s0, kpol);
       }
       if (p.k_scale) {
         const int pos = s0 + 4 * lane;
-        const float *src = p.k_scale + static_cast<int64_t>(b) * p.N_c + pos;
+        const float *src = p.k_scale + static_cast<int64_t>(b) * p.kseq + pos;
         float *dst = ksc + k * kTileKeys + 4 * lane;
         if (pos + 3 < nv && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
           cp_async16(dst, src, kpol);
@@ -860,7 +861,11 @@ cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld,
   auto encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap kmap;
-  const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(ia.B) * ia.N_c};
+  // rows of the last sequence end at (B - 1) * kseq + N_c; a tile reaching
+  // past that reads zeros (and past a token's visible rows is never used)
+  const int64_t kseq = k_rows_per_seq(ia);
+  if ((static_cast<int64_t>(ia.B) - 1) * kseq + ia.N_c + kTileKeys >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
+  const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>((static_cast<int64_t>(ia.B) - 1) * kseq + ia.N_c)};
   const cuuint64_t strides[1] = {128};
   const cuuint32_t box[2] = {128, kTileKeys};
   const cuuint32_t estr[2] = {1, 1};
@@ -869,8 +874,8 @@ cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
-  ScoreParams sp{ia.B,  ia.T,   ia.N_c, ia.r, ia.q_seq, ia.q_pos, prefix, qpack, wq, ia.k_scale, scores,
-                 ld,    status, pool,   ia.T <= ia.B ? 1 : 0};
+  ScoreParams sp{ia.B,  ia.T,   ia.N_c, ia.r,   static_cast<int>(kseq), ia.q_seq, ia.q_pos, prefix, qpack,
+                 wq,    ia.k_scale, scores, ld, status, pool, ia.T <= ia.B ? 1 : 0};
   auto kern = idx_score_umma_kernel<NH, P>;
   const size_t smem = L::total + 1024;  // + alignment slack for the 1024-byte swizzle atoms
   static bool attr_done[64] = {};

@@ -124,6 +124,16 @@ sa_status fused_with_scratch(const sa_index_args *ia, const sa_attn_args *aa, in
                              uint32_t *status, cudaStream_t stream);
 
 bool attn_shape_supported(int H, int D);
+
+// Rows between consecutive sequences of each cache (the strides of the
+// argument structs, 0 meaning dense).
+inline int64_t k_rows_per_seq(const sa_index_args &ia) {
+  return ia.k_seq_stride ? ia.k_seq_stride / ia.D_I : ia.N_c;
+}
+inline int64_t w_rows_per_seq(const sa_attn_args &aa) { return aa.w_seq_stride ? aa.w_seq_stride / aa.D : aa.R; }
+inline int64_t c_rows_per_seq(const sa_index_args &ia, const sa_attn_args &aa) {
+  return aa.c_seq_stride ? aa.c_seq_stride / aa.D : ia.N_c;
+}
 bool index_shape_supported(int H_I, int D_I);
 
 }  // namespace sa

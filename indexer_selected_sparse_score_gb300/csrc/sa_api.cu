@@ -1,5 +1,6 @@
 // The C ABI declared in include/sa.h: argument checks on the host, workspace
 // carve-up, and the launch sequence of each entry point.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -32,6 +33,16 @@ bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 
 size_t round_up(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+sa_status check_k_stride(const sa_index_args *ia) {
+  if (ia->k_seq_stride != 0 &&
+      (ia->k_seq_stride % ia->D_I != 0 || ia->k_seq_stride < static_cast<int64_t>(ia->N_c) * ia->D_I))
+    return fail(SA_ERR_INVALID_ARG, "k_seq_stride %lld: need 0 or a multiple of D_I = %d of at least N_c * D_I",
+                static_cast<long long>(ia->k_seq_stride), ia->D_I);
+  if (static_cast<int64_t>(ia->B - 1) * sa::k_rows_per_seq(*ia) + ia->N_c >= (int64_t{1} << 31) - 256)
+    return fail(SA_ERR_UNSUPPORTED, "index key cache rows must fit in 31 bits");
+  return SA_OK;
+}
+
 sa_status check_index(const sa_index_args *ia, bool need_index_inputs) {
   if (!ia) return fail(SA_ERR_INVALID_ARG, "index args pointer is NULL");
   if (ia->B < 1 || ia->T < 0 || ia->N_c < 1 || ia->r < 1)
@@ -55,6 +66,13 @@ sa_status check_index(const sa_index_args *ia, bool need_index_inputs) {
     return fail(SA_ERR_INVALID_ARG, "q_I and k_I must be 16-byte aligned");
   if (!aligned4(ia->w) || !aligned4(ia->q_scale) || !aligned4(ia->k_scale))
     return fail(SA_ERR_INVALID_ARG, "w, q_scale and k_scale must be 4-byte aligned");
+  return check_k_stride(ia);
+}
+
+sa_status check_ld(int64_t ld, const sa_index_args *ia) {
+  if (ld < ia->N_c)
+    return fail(SA_ERR_INVALID_ARG, "score row stride ld = %lld is below N_c = %d", static_cast<long long>(ld),
+                ia->N_c);
   return SA_OK;
 }
 
@@ -73,6 +91,24 @@ sa_status check_attn(const sa_attn_args *aa, int T) {
       !aligned16(aa->Vc))
     return fail(SA_ERR_INVALID_ARG, "Q, Kw, Vw, Kc, Vc must be 16-byte aligned");
   if (!aligned4(aa->sink)) return fail(SA_ERR_INVALID_ARG, "sink must be 4-byte aligned");
+  if (aa->w_seq_stride != 0 &&
+      (aa->w_seq_stride % aa->D != 0 || aa->w_seq_stride < static_cast<int64_t>(aa->R) * aa->D))
+    return fail(SA_ERR_INVALID_ARG, "w_seq_stride %lld: need 0 or a multiple of D = %d of at least R * D",
+                static_cast<long long>(aa->w_seq_stride), aa->D);
+  return SA_OK;
+}
+
+sa_status check_c_stride(const sa_attn_args *aa, const sa_index_args *ia) {
+  if (aa->c_seq_stride != 0 &&
+      (aa->c_seq_stride % aa->D != 0 || aa->c_seq_stride < static_cast<int64_t>(ia->N_c) * aa->D))
+    return fail(SA_ERR_INVALID_ARG, "c_seq_stride %lld: need 0 or a multiple of D = %d of at least N_c * D",
+                static_cast<long long>(aa->c_seq_stride), aa->D);
+  // row indices of the caches are 32-bit
+  const int64_t last = static_cast<int64_t>(ia->B - 1) *
+                       std::max(sa::w_rows_per_seq(*aa), sa::c_rows_per_seq(*ia, *aa)) +
+                       std::max<int64_t>(aa->R, ia->N_c);
+  if (last >= (int64_t{1} << 31) - 256)
+    return fail(SA_ERR_UNSUPPORTED, "caches of %lld rows: row indices must fit in 31 bits", static_cast<long long>(last));
   return SA_OK;
 }
 
@@ -140,6 +176,7 @@ sa_status fused_with_scratch(const sa_index_args *ia, const sa_attn_args *aa, in
                              uint32_t *status, cudaStream_t st) {
   if (sa_status s = check_index(ia, true)) return s;
   if (sa_status s = check_attn(aa, ia->T)) return s;
+  if (sa_status s = check_c_stride(aa, ia)) return s;
   if (K < 0) return fail(SA_ERR_INVALID_ARG, "K must be >= 0 (got %d)", K);
   if (ia->T > 0 && !out) return fail(SA_ERR_INVALID_ARG, "out must be a device pointer");
   if (!aligned4(idx_out) || !aligned16(out))
@@ -166,7 +203,8 @@ extern "C" {
 
 size_t sa_workspace_size(const sa_index_args *ia, const sa_attn_args *aa, int32_t K) {
   if (check_index(ia, false) != SA_OK || K < 0) return 0;
-  if (aa && check_attn(aa, 0) != SA_OK) return 0;
+  if (sa::index_shape_supported(ia->H_I, ia->D_I) && check_k_stride(ia) != SA_OK) return 0;
+  if (aa && (check_attn(aa, 0) != SA_OK || check_c_stride(aa, ia) != SA_OK)) return 0;
   return sa::ws_layout(*ia, aa, K).total;
 }
 
@@ -176,28 +214,30 @@ sa_status sa_workspace_init(void *ws, size_t ws_bytes, sa_stream_t stream) {
   return e == cudaSuccess ? SA_OK : cuda_fail(e, "cudaMemsetAsync");
 }
 
-sa_status sa_indexer_scores(const sa_index_args *ia, float *scores, void *ws, size_t ws_bytes,
+sa_status sa_indexer_scores(const sa_index_args *ia, float *scores, int64_t ld, void *ws, size_t ws_bytes,
                             sa_stream_t stream) {
   if (sa_status s = check_index(ia, true)) return s;
+  if (sa_status s = check_ld(ld, ia)) return s;
   if (ia->T > 0 && !scores) return fail(SA_ERR_INVALID_ARG, "scores must be a device pointer");
   if (!aligned4(scores)) return fail(SA_ERR_INVALID_ARG, "scores must be 4-byte aligned");
   const sa::WsLayout L = sa::ws_layout(*ia, nullptr, 0);
   if (sa_status s = check_ws(ws, ws_bytes, L.total)) return s;
-  cudaError_t e = sa::launch_idx_score(*ia, scores, ia->N_c, true, at<void>(ws, L.score_scratch),
+  cudaError_t e = sa::launch_idx_score(*ia, scores, ld, true, at<void>(ws, L.score_scratch),
                                        at<uint32_t>(ws, 0), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SA_OK : cuda_fail(e, "index score launch");
 }
 
-sa_status sa_topk(const float *scores, const sa_index_args *ia, int32_t K, int32_t *idx, void *ws,
+sa_status sa_topk(const float *scores, int64_t ld, const sa_index_args *ia, int32_t K, int32_t *idx, void *ws,
                   size_t ws_bytes, sa_stream_t stream) {
   if (sa_status s = check_index(ia, false)) return s;
+  if (sa_status s = check_ld(ld, ia)) return s;
   if (K < 0) return fail(SA_ERR_INVALID_ARG, "K must be >= 0 (got %d)", K);
   if (ia->T > 0 && K > 0 && (!scores || !idx))
     return fail(SA_ERR_INVALID_ARG, "scores and idx must be device pointers");
   if (!aligned4(scores) || !aligned4(idx))
     return fail(SA_ERR_INVALID_ARG, "scores and idx must be 4-byte aligned");
   if (sa_status s = check_ws(ws, ws_bytes, 256)) return s;
-  cudaError_t e = sa::launch_topk(scores, ia->N_c, *ia, K, idx, at<uint32_t>(ws, 0),
+  cudaError_t e = sa::launch_topk(scores, ld, *ia, K, idx, at<uint32_t>(ws, 0),
                                   reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SA_OK : cuda_fail(e, "top-k launch");
 }
@@ -237,9 +277,10 @@ int32_t sa_candidate_words(int32_t N_c, int32_t block_size) {
   return sa::candidate_words(N_c, block_size);
 }
 
-sa_status sa_candidate_blocks(const float *scores, const sa_index_args *ia, int32_t block_size,
+sa_status sa_candidate_blocks(const float *scores, int64_t ld, const sa_index_args *ia, int32_t block_size,
                               int32_t topk_blocks, uint32_t *cand, void *ws, size_t ws_bytes, sa_stream_t stream) {
   if (sa_status s = check_index(ia, false)) return s;
+  if (sa_status s = check_ld(ld, ia)) return s;
   if (block_size < 1 || topk_blocks < 0)
     return fail(SA_ERR_INVALID_ARG, "need block_size >= 1 and topk_blocks >= 0 (got %d, %d)", block_size,
                 topk_blocks);
@@ -253,14 +294,16 @@ sa_status sa_candidate_blocks(const float *scores, const sa_index_args *ia, int3
   if (!aligned4(scores) || !aligned4(cand))
     return fail(SA_ERR_INVALID_ARG, "scores and cand must be 4-byte aligned");
   if (sa_status s = check_ws(ws, ws_bytes, 256)) return s;
-  cudaError_t e = sa::launch_candidate_blocks(scores, ia->N_c, *ia, block_size, topk_blocks, cand,
+  cudaError_t e = sa::launch_candidate_blocks(scores, ld, *ia, block_size, topk_blocks, cand,
                                               at<uint32_t>(ws, 0), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SA_OK : cuda_fail(e, "candidate block launch");
 }
 
-sa_status sa_topk_candidates(const float *scores, const sa_index_args *ia, int32_t K, const uint32_t *cand,
-                             int32_t block_size, int32_t *idx, void *ws, size_t ws_bytes, sa_stream_t stream) {
+sa_status sa_topk_candidates(const float *scores, int64_t ld, const sa_index_args *ia, int32_t K,
+                             const uint32_t *cand, int32_t block_size, int32_t *idx, void *ws, size_t ws_bytes,
+                             sa_stream_t stream) {
   if (sa_status s = check_index(ia, false)) return s;
+  if (sa_status s = check_ld(ld, ia)) return s;
   if (K < 0) return fail(SA_ERR_INVALID_ARG, "K must be >= 0 (got %d)", K);
   if (block_size < 1) return fail(SA_ERR_INVALID_ARG, "block_size must be >= 1 (got %d)", block_size);
   if (ia->N_c > (1 << 30)) return fail(SA_ERR_UNSUPPORTED, "N_c %d above 2^30", ia->N_c);
@@ -269,7 +312,7 @@ sa_status sa_topk_candidates(const float *scores, const sa_index_args *ia, int32
   if (!aligned4(scores) || !aligned4(idx) || !aligned4(cand))
     return fail(SA_ERR_INVALID_ARG, "scores, cand and idx must be 4-byte aligned");
   if (sa_status s = check_ws(ws, ws_bytes, 256)) return s;
-  cudaError_t e = sa::launch_topk(scores, ia->N_c, *ia, K, idx, at<uint32_t>(ws, 0),
+  cudaError_t e = sa::launch_topk(scores, ld, *ia, K, idx, at<uint32_t>(ws, 0),
                                   reinterpret_cast<cudaStream_t>(stream), cand,
                                   sa::candidate_words(ia->N_c, block_size), block_size);
   return e == cudaSuccess ? SA_OK : cuda_fail(e, "top-k launch");
@@ -279,6 +322,8 @@ sa_status sa_sparse_attn(const sa_index_args *ia, const sa_attn_args *aa, const 
                          int32_t K, void *out, void *ws, size_t ws_bytes, sa_stream_t stream) {
   if (sa_status s = check_index(ia, false)) return s;
   if (sa_status s = check_attn(aa, ia->T)) return s;
+  if (sa_status s = check_c_stride(aa, ia)) return s;
+  if (sa_status s = check_c_stride(aa, ia)) return s;
   if (K < 0) return fail(SA_ERR_INVALID_ARG, "K must be >= 0 (got %d)", K);
   if (ia->T > 0 && (!out || (K > 0 && !idx)))
     return fail(SA_ERR_INVALID_ARG, "out and idx must be device pointers");
@@ -298,6 +343,7 @@ static sa_status fused_impl(const sa_index_args *ia, const sa_attn_args *aa, int
                             sa_stream_t stream, void *const *ev) {
   if (sa_status s = check_index(ia, true)) return s;
   if (sa_status s = check_attn(aa, ia->T)) return s;
+  if (sa_status s = check_c_stride(aa, ia)) return s;
   if (K < 0) return fail(SA_ERR_INVALID_ARG, "K must be >= 0 (got %d)", K);
   if (ia->T > 0 && !out) return fail(SA_ERR_INVALID_ARG, "out must be a device pointer");
   if (!aligned4(idx_out) || !aligned16(out))
@@ -346,7 +392,8 @@ sa_status sa_fused_decode_staged(const sa_index_args *ia, const sa_attn_args *aa
 }
 
 int32_t sa_fused_decode_launch_count(const sa_index_args *ia, const sa_attn_args *aa, int32_t K) {
-  if (check_index(ia, true) != SA_OK || check_attn(aa, 0) != SA_OK || K < 0) return 0;
+  if (check_index(ia, true) != SA_OK || check_attn(aa, 0) != SA_OK || check_c_stride(aa, ia) != SA_OK || K < 0)
+    return 0;
   if (ia->T == 0) return 0;
   const sa::SplitPlan plan = sa::plan_splits(ia->T, aa->W, K);
   return sa::fused_launch_count(*ia, *aa, K, plan);

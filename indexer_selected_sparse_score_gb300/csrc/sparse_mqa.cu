@@ -36,6 +36,7 @@ struct AttnParams {
   int B, T, N_c, r;
   const int32_t *q_seq, *q_pos;
   int W, R;
+  int wseq, cseq;  // rows between consecutive sequences of the ring and of the compressed cache
   const uint16_t *Q, *Kw, *Vw, *Kc, *Vc;
   const float *sink;
   float qk_scale;  // scale * log2(e)
@@ -111,11 +112,11 @@ __global__ void __launch_bounds__(AttnShape<D, kSameKV>::kThreads) sparse_mqa_si
       if (kk < k_end) {
         if (kk < n_w) {
           const int pos = tk.pos - n_w + 1 + kk;
-          row = tk.b * p.R + pos % p.R;
+          row = tk.b * p.wseq + pos % p.R;
         } else {
           const int c = p.idx[static_cast<int64_t>(t) * p.K + (kk - n_w)];
           if (c >= 0 && c < tk.nv) {
-            row = tk.b * p.N_c + c;
+            row = tk.b * p.cseq + c;
             src = 1;
           } else if (c != -1) {
             raise_flag(p.status, kFlagBadIndex);
@@ -425,11 +426,11 @@ __global__ void __launch_bounds__(kMmaThreads) sparse_mqa_mma512_kernel(AttnPara
     if (kk < k_end) {
       if (kk < n_w) {
         const int pos = tk.pos - n_w + 1 + kk;
-        row = tk.b * p.R + pos % p.R;
+        row = tk.b * p.wseq + pos % p.R;
       } else {
         const int c = p.idx[static_cast<int64_t>(t) * p.K + (kk - n_w)];
         if (c >= 0 && c < tk.nv) {
-          row = tk.b * p.N_c + c;
+          row = tk.b * p.cseq + c;
           src = 1;
         } else if (c != -1) {
           raise_flag(p.status, kFlagBadIndex);
@@ -655,6 +656,8 @@ cudaError_t launch_sparse_mqa(const sa_index_args &ia, const sa_attn_args &aa, c
   p.q_pos = ia.q_pos;
   p.W = aa.W;
   p.R = aa.R;
+  p.wseq = static_cast<int>(w_rows_per_seq(aa));
+  p.cseq = static_cast<int>(c_rows_per_seq(ia, aa));
   p.Q = static_cast<const uint16_t *>(aa.Q);
   p.Kw = static_cast<const uint16_t *>(aa.Kw);
   p.Vw = static_cast<const uint16_t *>(aa.Vw);

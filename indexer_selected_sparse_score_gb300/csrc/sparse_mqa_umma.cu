@@ -79,6 +79,7 @@ struct AttnSmem {
 
 struct AttnUmmaParams {
   int B, T, N_c, r, W, R, K;
+  int wseq, cseq;                 // rows between consecutive sequences of the ring and of the compressed cache
   int WT, TPT;                    // window tiles per token, tiles per token
   int split, PT0;                 // CTAs per token (1, or a 2-CTA cluster with one token), tiles of rank 0's part
   int evict_first;                // nonzero: K/V rows are read once per call (at most one token per sequence)
@@ -474,11 +475,11 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
               const int q = j * kTile + 4 * lane + e;
               if (q < n_w) {
                 const int pos = tk.pos - n_w + 1 + q;
-                rows[e] = tk.b * p.R + pos % p.R;
+                rows[e] = tk.b * p.wseq + pos % p.R;
                 valid[e] = true;
               }
             } else if (cidx[e] >= 0 && cidx[e] < tk.nv) {
-              rows[e] = tk.b * p.N_c + cidx[e];
+              rows[e] = tk.b * p.cseq + cidx[e];
               valid[e] = true;
             } else if (cidx[e] != -1 && warp == kKWarp0) {
               raise_flag(p.status, kFlagBadIndex);
@@ -886,6 +887,8 @@ cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &
   p.W = aa.W;
   p.R = aa.R;
   p.K = K;
+  p.wseq = static_cast<int>(w_rows_per_seq(aa));
+  p.cseq = static_cast<int>(c_rows_per_seq(ia, aa));
   p.WT = (aa.W + kTile - 1) / kTile;
   p.TPT = p.WT + (K + kTile - 1) / kTile;
   p.q_seq = ia.q_seq;
@@ -899,10 +902,10 @@ cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &
   p.status = status;
   CUtensorMap qmap, kwmap, kcmap, vwmap, vcmap;
   if (!encode_rows(&qmap, aa.Q, static_cast<uint64_t>(ia.T) * kH, 16) ||
-      !encode_rows(&kwmap, aa.Kw, static_cast<uint64_t>(ia.B) * aa.R, 1) ||
-      !encode_rows(&kcmap, aa.Kc, static_cast<uint64_t>(ia.B) * ia.N_c, 1) ||
-      !encode_rows(&vwmap, aa.Vw, static_cast<uint64_t>(ia.B) * aa.R, 1) ||
-      !encode_rows(&vcmap, aa.Vc, static_cast<uint64_t>(ia.B) * ia.N_c, 1))
+      !encode_rows(&kwmap, aa.Kw, static_cast<uint64_t>(ia.B - 1) * p.wseq + aa.R, 1) ||
+      !encode_rows(&kcmap, aa.Kc, static_cast<uint64_t>(ia.B - 1) * p.cseq + ia.N_c, 1) ||
+      !encode_rows(&vwmap, aa.Vw, static_cast<uint64_t>(ia.B - 1) * p.wseq + aa.R, 1) ||
+      !encode_rows(&vcmap, aa.Vc, static_cast<uint64_t>(ia.B - 1) * p.cseq + ia.N_c, 1))
     return cudaErrorInvalidValue;
   const size_t smem = attn_smem_bytes();
   // the register split above assumes the kernel launches with kLaunchRegs

@@ -38,13 +38,14 @@ def test_every_declared_symbol_is_exported(lib):
 
 def _ia(**kw):
     base = dict(B=2, T=3, H_I=16, D_I=64, N_c=100, r=2, q_seq=16, q_pos=16, q_I=16, q_dtype=0,
-                q_scale=None, w=16, k_I=16, k_dtype=1, k_scale=16)
+                q_scale=None, w=16, k_I=16, k_dtype=1, k_scale=16, k_seq_stride=0)
     base.update(kw)
     return binding.IndexArgs(*[base[f] for f, _ in binding.IndexArgs._fields_])
 
 
 def _aa(**kw):
-    base = dict(H=16, D=128, W=8, R=8, Q=16, Kw=16, Vw=16, Kc=16, Vc=16, sink=None, scale=0.088)
+    base = dict(H=16, D=128, W=8, R=8, Q=16, Kw=16, Vw=16, Kc=16, Vc=16, sink=None, scale=0.088,
+                w_seq_stride=0, c_seq_stride=0)
     base.update(kw)
     return binding.AttnArgs(*[base[f] for f, _ in binding.AttnArgs._fields_])
 
@@ -123,11 +124,13 @@ def test_candidate_words(lib):
     (dict(ws=None), binding.SA_ERR_WORKSPACE),
     (dict(ws_bytes=64), binding.SA_ERR_WORKSPACE),
     (dict(ia=_ia(r=0)), binding.SA_ERR_INVALID_ARG),
+    (dict(ld=99), binding.SA_ERR_INVALID_ARG),                        # score rows shorter than N_c
 ])
 def test_candidate_blocks_rejects_bad_arguments(lib, kw, status):
-    a = dict(scores=256, ia=_ia(), block_size=8, topk_blocks=4, cand=256, ws=256, ws_bytes=256)
+    a = dict(scores=256, ld=None, ia=_ia(), block_size=8, topk_blocks=4, cand=256, ws=256, ws_bytes=256)
     a.update(kw)
-    st = lib.sa_candidate_blocks(a["scores"], ctypes.byref(a["ia"]), a["block_size"], a["topk_blocks"],
+    ld = a["ia"].N_c if a["ld"] is None else a["ld"]
+    st = lib.sa_candidate_blocks(a["scores"], ld, ctypes.byref(a["ia"]), a["block_size"], a["topk_blocks"],
                                  a["cand"], a["ws"], a["ws_bytes"], None)
     assert st == status
     assert lib.sa_last_error_detail()
@@ -141,11 +144,13 @@ def test_candidate_blocks_rejects_bad_arguments(lib, kw, status):
     (dict(cand=258), binding.SA_ERR_INVALID_ARG),
     (dict(ws=None), binding.SA_ERR_WORKSPACE),
     (dict(ia=_ia(N_c=(1 << 30) + 1)), binding.SA_ERR_UNSUPPORTED),
+    (dict(ld=50), binding.SA_ERR_INVALID_ARG),
 ])
 def test_topk_candidates_rejects_bad_arguments(lib, kw, status):
-    a = dict(scores=256, ia=_ia(), K=8, cand=256, block_size=8, idx=256, ws=256, ws_bytes=256)
+    a = dict(scores=256, ld=None, ia=_ia(), K=8, cand=256, block_size=8, idx=256, ws=256, ws_bytes=256)
     a.update(kw)
-    st = lib.sa_topk_candidates(a["scores"], ctypes.byref(a["ia"]), a["K"], a["cand"], a["block_size"],
+    ld = a["ia"].N_c if a["ld"] is None else a["ld"]
+    st = lib.sa_topk_candidates(a["scores"], ld, ctypes.byref(a["ia"]), a["K"], a["cand"], a["block_size"],
                                 a["idx"], a["ws"], a["ws_bytes"], None)
     assert st == status
 
@@ -153,8 +158,40 @@ def test_topk_candidates_rejects_bad_arguments(lib, kw, status):
 def test_candidate_calls_with_no_tokens_enqueue_nothing(lib):
     # T = 0: valid arguments and nothing to do (no device is touched)
     ia = _ia(T=0, q_seq=None, q_pos=None)
-    assert lib.sa_candidate_blocks(None, ctypes.byref(ia), 8, 4, None, 256, 256, None) == binding.SA_OK
-    assert lib.sa_topk_candidates(None, ctypes.byref(ia), 8, None, 8, None, 256, 256, None) == binding.SA_OK
+    assert lib.sa_candidate_blocks(None, 100, ctypes.byref(ia), 8, 4, None, 256, 256, None) == binding.SA_OK
+    assert lib.sa_topk_candidates(None, 100, ctypes.byref(ia), 8, None, 8, None, 256, 256, None) == binding.SA_OK
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(ia=_ia(k_seq_stride=100 * 64 - 64)), binding.SA_ERR_INVALID_ARG),    # below N_c * D_I
+    (dict(ia=_ia(k_seq_stride=100 * 64 + 32)), binding.SA_ERR_INVALID_ARG),    # not whole rows
+    (dict(aa=_aa(w_seq_stride=7 * 128)), binding.SA_ERR_INVALID_ARG),         # below R * D
+    (dict(aa=_aa(w_seq_stride=8 * 128 + 8)), binding.SA_ERR_INVALID_ARG),
+    (dict(aa=_aa(c_seq_stride=99 * 128)), binding.SA_ERR_INVALID_ARG),        # below N_c * D
+    (dict(aa=_aa(c_seq_stride=100 * 128 + 64)), binding.SA_ERR_INVALID_ARG),
+    (dict(aa=_aa(c_seq_stride=(1 << 31) * 128)), binding.SA_ERR_UNSUPPORTED),  # rows past 31 bits
+])
+def test_sequence_strides_are_checked(lib, kw, status):
+    a = dict(ia=_ia(), aa=_aa())
+    a.update(kw)
+    assert _call_fused(lib, a["ia"], a["aa"]) == status
+    assert lib.sa_last_error_detail()
+    assert lib.sa_workspace_size(ctypes.byref(a["ia"]), ctypes.byref(a["aa"]), 8) == 0
+
+
+def test_padded_strides_are_accepted(lib):
+    # a cache with room for 4 x more rows per sequence than are in use
+    n = lib.sa_workspace_size(ctypes.byref(_ia(k_seq_stride=400 * 64)),
+                              ctypes.byref(_aa(w_seq_stride=32 * 128, c_seq_stride=400 * 128)), 8)
+    assert n == lib.sa_workspace_size(ctypes.byref(_ia()), ctypes.byref(_aa()), 8)
+
+
+def test_score_row_stride_is_checked(lib):
+    ia = _ia()
+    assert lib.sa_topk(256, 99, ctypes.byref(ia), 8, 256, 256, 256, None) == binding.SA_ERR_INVALID_ARG
+    assert lib.sa_indexer_scores(ctypes.byref(ia), 256, 64, 256, 1 << 20, None) == binding.SA_ERR_INVALID_ARG
+    ia0 = _ia(T=0, q_seq=None, q_pos=None)
+    assert lib.sa_topk(None, 128, ctypes.byref(ia0), 8, None, 256, 256, None) == binding.SA_OK
 
 
 def test_attention_head_dims(lib):
