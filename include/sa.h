@@ -219,11 +219,72 @@ SA_API sa_status sa_rotate_quant(const void *x, int32_t rows, int32_t dim, const
  * group g < S / r (tokens g*r .. g*r + r - 1):
  *   c[d] = bf16( sum_j softmax_j(score[b, g*r + j, d]) kv[b, g*r + j, d] )
  *   out[b, g, d] = bf16( weight[d] * c[d] / sqrt(mean_d c[d]^2 + eps) )
- * in fp32.  out: [B, S / r, D] bf16.  The trailing S % r tokens are not read:
- * the caller keeps them as the partial group that decode steps complete.
+ * in fp32.  out: [B, S / r, D] bf16.  The trailing S % r tokens are the
+ * partial group that decode steps complete: with kv_state and score_state
+ * ([B, r, D] fp32, both or neither) they are copied to slots 0 .. S % r - 1,
+ * as the page splits them into kv_state / score_state.
  * r >= 2; D a multiple of 32 in [32, 1024]; B <= 65535; eps >= 0. */
 SA_API sa_status sa_compress_prefill(const float *kv, const float *score, int32_t B, int32_t S, int32_t D, int32_t r,
-                                     const float *weight, float eps, void *out, sa_stream_t stream);
+                                     const float *weight, float eps, void *out, float *kv_state, float *score_state,
+                                     sa_stream_t stream);
+
+/* One compressor decode step ("DeepSeek-V4.1-Flash-NVFP4 inference/model.py",
+ * Compressor.forward with start_pos > 0): for every sequence b, the token at
+ * absolute position pos[b] (its projections kv[b], score[b]: [B, D] fp32)
+ * fills slot pos[b] % r of the state (kv_state, score_state: [B, r, D] fp32,
+ * caller-owned and kept across steps; a sequence that starts without a
+ * prefill begins with kv_state 0 and score_state -inf, as the page's buffers
+ * do).  When the group has just completed, (pos[b] + 1) % r == 0, its r slots
+ * are pooled and normalised exactly as in sa_compress_prefill and written to
+ * out[b] ([B, D] bf16); the other rows of out are left untouched.  A negative
+ * pos[b] is skipped and flagged in the workspace status word
+ * (sa_check_device_status reports SA_ERR_DEVICE_DATA); the workspace needs
+ * only its 256-byte header.  Same limits on r, D, B and eps as
+ * sa_compress_prefill. */
+SA_API sa_status sa_compress_decode(const float *kv, const float *score, const int32_t *pos, int32_t B, int32_t D,
+                                    int32_t r, float *kv_state, float *score_state, const float *weight, float eps,
+                                    void *out, void *ws, size_t ws_bytes, sa_stream_t stream);
+
+/* Rotary embedding parameters ("DeepSeek-V4.1-Flash-NVFP4 inference/model.py",
+ * precompute_freqs_cis and apply_rotary_emb): pair i < dim / 2 of the rotated
+ * values turns by pos * f_i with f_i = base^(-2i / dim), and, when
+ * original_seq_len > 0, YaRN's correction: pairs below the corrected dimension
+ * of beta_fast keep f_i, those above that of beta_slow take f_i / factor, and
+ * a linear ramp fades between (the page's low / high bounds, span at least
+ * 1e-3).  Pairs are adjacent values (x[2i], x[2i + 1]) taken as complex
+ * numbers. */
+typedef struct {
+  int32_t dim;              /* rotated values at the end of the row (rope_head_dim) */
+  double base;              /* rope theta (compress_rope_theta for compressed rows) */
+  double factor;            /* YaRN factor */
+  int32_t original_seq_len; /* > 0 applies YaRN */
+  double beta_fast, beta_slow;
+} sa_rope_args;
+
+/* Index keys of the layer that owns them ("DeepSeek-V4.1-Flash-NVFP4
+ * inference/model.py", Indexer.forward: k = k_norm(wk(latent)),
+ * apply_rotary_emb on its last rope_head_dim values at the position of the
+ * group's first token, the key quantisation, k_cache[:, start_pos // ratio]).
+ * kproj: [n, D_I] bf16, row i = wk(latent) of compressed row grp[i] of
+ * sequence seq[i] (the projection stays with the caller).  For each row:
+ *   k = bf16( weight * x / sqrt(mean(x^2) + eps) )        (RMSNorm.forward)
+ *   k[D_I - dim ..] rotated at position grp[i] * r, rounded to bf16
+ *   scale = amax|k| / 448 (1 for a zero row), codes = e4m3(k / scale)
+ * written to k_I at element seq[i] * k_seq_stride + grp[i] * D_I (128 codes)
+ * and to k_scale at seq[i] * (k_seq_stride / D_I) + grp[i].  The page
+ * quantises these keys to fp4; here they take the e4m3 codes with one fp32
+ * scale per position that sa_indexer_scores reads.  Norm and rotation are
+ * evaluated in double and each bf16 result is one rounding of it; the
+ * quotients are correctly rounded fp32.  D_I = 128, dim a multiple of 4 in
+ * [0, 128]; k_seq_stride 0 (dense: N_rows * D_I) or a multiple of D_I of at
+ * least N_rows * D_I; seq[i] outside [0, B) or grp[i] outside [0, N_rows) is
+ * skipped and flagged (SA_ERR_DEVICE_DATA).  The workspace needs only its
+ * 256-byte header. */
+SA_API sa_status sa_index_key_publish(const void *kproj, int32_t n, int32_t D_I, const int32_t *seq,
+                                      const int32_t *grp, int32_t r, const float *weight, float eps,
+                                      const sa_rope_args *rope, uint8_t *k_I, float *k_scale, int32_t B,
+                                      int32_t N_rows, int64_t k_seq_stride, void *ws, size_t ws_bytes,
+                                      sa_stream_t stream);
 
 /* Sparse MQA over the window and the selected compressed rows
  * ("DeepSeek-V4.1-Flash-NVFP4 inference/model.py", Attention.forward and

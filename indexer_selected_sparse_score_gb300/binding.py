@@ -59,9 +59,16 @@ class AttnArgs(ctypes.Structure):
     ]
 
 
+class RopeArgs(ctypes.Structure):
+    _fields_ = [
+        ("dim", ctypes.c_int32), ("base", ctypes.c_double), ("factor", ctypes.c_double),
+        ("original_seq_len", ctypes.c_int32), ("beta_fast", ctypes.c_double), ("beta_slow", ctypes.c_double),
+    ]
+
+
 EXPORTED = ("sa_workspace_size", "sa_workspace_init", "sa_indexer_scores", "sa_topk",
             "sa_candidate_blocks", "sa_candidate_words", "sa_topk_candidates", "sa_rotate_quant",
-            "sa_compress_prefill",
+            "sa_compress_prefill", "sa_compress_decode", "sa_index_key_publish",
             "sa_sparse_attn", "sa_fused_decode", "sa_fused_decode_staged",
             "sa_fused_decode_launch_count", "sa_check_device_status", "sa_status_string",
             "sa_last_error_detail", "sa_fused_decode_noalloc", "sa_noalloc_scratch_bytes")
@@ -91,7 +98,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.sa_candidate_words.restype = i32
     lib.sa_topk_candidates.argtypes = [vp, i64, IA, i32, vp, i32, vp, vp, sz, vp]
     lib.sa_rotate_quant.argtypes = [vp, i32, i32, vp, ctypes.c_int64, vp, vp, vp, sz, vp]
-    lib.sa_compress_prefill.argtypes = [vp, vp, i32, i32, i32, i32, vp, ctypes.c_float, vp, vp]
+    lib.sa_compress_prefill.argtypes = [vp, vp, i32, i32, i32, i32, vp, ctypes.c_float, vp, vp, vp, vp]
+    lib.sa_compress_decode.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, ctypes.c_float, vp, vp, sz, vp]
+    lib.sa_index_key_publish.argtypes = [vp, i32, i32, vp, vp, i32, vp, ctypes.c_float, ctypes.POINTER(RopeArgs),
+                                         vp, vp, i32, i32, i64, vp, sz, vp]
     lib.sa_sparse_attn.argtypes = [IA, AA, vp, i32, vp, vp, sz, vp]
     lib.sa_fused_decode.argtypes = [IA, AA, i32, vp, vp, vp, sz, vp]
     lib.sa_fused_decode_staged.argtypes = [IA, AA, i32, vp, vp, vp, sz, vp, ctypes.POINTER(vp)]
@@ -106,7 +116,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.sa_status_string.restype = ctypes.c_char_p
     lib.sa_last_error_detail.restype = ctypes.c_char_p
     for name in ("sa_workspace_init", "sa_indexer_scores", "sa_topk", "sa_candidate_blocks",
-                 "sa_topk_candidates", "sa_rotate_quant", "sa_compress_prefill", "sa_sparse_attn",
+                 "sa_topk_candidates", "sa_rotate_quant", "sa_compress_prefill", "sa_compress_decode",
+                 "sa_index_key_publish", "sa_sparse_attn",
                  "sa_fused_decode", "sa_fused_decode_staged", "sa_check_device_status"):
         getattr(lib, name).restype = i32
     if path == LIB:
@@ -198,9 +209,30 @@ def sa_rotate_quant(x, rows: int, codes, scales, ws, dst=None, dst_rows: int = 0
     _check(load().sa_rotate_quant(_p(x), rows, dim, _p(dst), dst_rows, _p(codes), _p(scales), p, n, _s(stream)))
 
 
-def sa_compress_prefill(kv, score, B: int, S: int, D: int, r: int, weight, eps: float, out, stream=None) -> None:
-    """V4.1 compressor from position 0: [B, S // r, D] bf16 pooled, normalised rows."""
-    _check(load().sa_compress_prefill(_p(kv), _p(score), B, S, D, r, _p(weight), eps, _p(out), _s(stream)))
+def sa_compress_prefill(kv, score, B: int, S: int, D: int, r: int, weight, eps: float, out, stream=None,
+                        kv_state=None, score_state=None) -> None:
+    """V4.1 compressor from position 0: [B, S // r, D] bf16 pooled, normalised
+    rows; the trailing S % r tokens go to the states when given."""
+    _check(load().sa_compress_prefill(_p(kv), _p(score), B, S, D, r, _p(weight), eps, _p(out), _p(kv_state),
+                                      _p(score_state), _s(stream)))
+
+
+def sa_compress_decode(kv, score, pos, B: int, D: int, r: int, kv_state, score_state, weight, eps: float, out, ws,
+                       stream=None) -> None:
+    """One V4.1 compressor decode step: row b of ``out`` is written when the
+    group of sequence b completes at position pos[b]."""
+    p, n = _ws(ws)
+    _check(load().sa_compress_decode(_p(kv), _p(score), _p(pos), B, D, r, _p(kv_state), _p(score_state), _p(weight),
+                                     eps, _p(out), p, n, _s(stream)))
+
+
+def sa_index_key_publish(kproj, n: int, seq, grp, r: int, weight, eps: float, rope: "RopeArgs", k_I, k_scale,
+                         B: int, N_rows: int, ws, k_seq_stride: int = 0, D_I: int = 128, stream=None) -> None:
+    """V4.1 index keys: k_norm, rotary embedding at the group start, e4m3 codes
+    and a scale per position, written into the key cache."""
+    p, nb = _ws(ws)
+    _check(load().sa_index_key_publish(_p(kproj), n, D_I, _p(seq), _p(grp), r, _p(weight), eps, ctypes.byref(rope),
+                                       _p(k_I), _p(k_scale), B, N_rows, k_seq_stride, p, nb, _s(stream)))
 
 
 def sa_sparse_attn(ia: IndexArgs, aa: AttnArgs, idx, K: int, out, ws, stream=None) -> None:

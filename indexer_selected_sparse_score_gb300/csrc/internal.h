@@ -63,7 +63,17 @@ cudaError_t launch_rotate_quant(const void *x, int rows, const int32_t *dst, int
                                 float *scales, uint32_t *status, cudaStream_t stream);
 // V4.1 compressor from position 0: S / r pooled, normalised bf16 rows per sequence.
 cudaError_t launch_compress_prefill(const float *kv, const float *score, int B, int S, int D, int r,
-                                    const float *weight, float eps, void *out, cudaStream_t stream);
+                                    const float *weight, float eps, void *out, float *kv_state, float *score_state,
+                                    cudaStream_t stream);
+cudaError_t launch_compress_decode(const float *kv, const float *score, const int32_t *pos, int B, int D, int r,
+                                   float *kv_state, float *score_state, const float *weight, float eps, void *out,
+                                   uint32_t *status, cudaStream_t stream);
+// V4.1 index keys of a compressing layer: k_norm, rotary embedding of the last
+// rope.dim values at position grp * r, e4m3 block quantisation, cache write.
+cudaError_t launch_index_key_publish(const void *kproj, int n, const int32_t *seq, const int32_t *grp, int r,
+                                     const float *weight, float eps, const sa_rope_args &rope, uint8_t *k_I,
+                                     float *k_scale, int B, int N_rows, int64_t k_seq_stride, uint32_t *status,
+                                     cudaStream_t stream);
 cudaError_t launch_candidate_blocks(const float *scores, int64_t ld, const sa_index_args &ia, int block_size,
                                    int topk_blocks, uint32_t *cand, uint32_t *status, cudaStream_t stream);
 

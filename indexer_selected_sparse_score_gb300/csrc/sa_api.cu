@@ -242,19 +242,76 @@ sa_status sa_topk(const float *scores, int64_t ld, const sa_index_args *ia, int3
   return e == cudaSuccess ? SA_OK : cuda_fail(e, "top-k launch");
 }
 
-sa_status sa_compress_prefill(const float *kv, const float *score, int32_t B, int32_t S, int32_t D, int32_t r,
-                              const float *weight, float eps, void *out, sa_stream_t stream) {
-  if (B < 0 || S < 0 || B > 65535) return fail(SA_ERR_INVALID_ARG, "need 0 <= B <= 65535 and S >= 0");
+static sa_status check_compressor(int32_t B, int32_t D, int32_t r, float eps) {
+  if (B < 0 || B > 65535) return fail(SA_ERR_INVALID_ARG, "need 0 <= B <= 65535 (got %d)", B);
   if (r < 2) return fail(SA_ERR_INVALID_ARG, "compression ratio must be >= 2 (got %d)", r);
   if (D < 32 || D > 1024 || D % 32) return fail(SA_ERR_UNSUPPORTED, "head dim %d: need a multiple of 32 in [32, 1024]", D);
   if (!std::isfinite(eps) || eps < 0.f) return fail(SA_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  return SA_OK;
+}
+
+sa_status sa_compress_prefill(const float *kv, const float *score, int32_t B, int32_t S, int32_t D, int32_t r,
+                              const float *weight, float eps, void *out, float *kv_state, float *score_state,
+                              sa_stream_t stream) {
+  if (sa_status s = check_compressor(B, D, r, eps)) return s;
+  if (S < 0) return fail(SA_ERR_INVALID_ARG, "need S >= 0 (got %d)", S);
   if (B > 0 && S >= r && (!kv || !score || !weight || !out))
     return fail(SA_ERR_INVALID_ARG, "kv, score, weight and out must be device pointers");
-  if (!aligned4(kv) || !aligned4(score) || !aligned4(weight) || !aligned4(out))
-    return fail(SA_ERR_INVALID_ARG, "kv, score, weight and out must be 4-byte aligned");
-  cudaError_t e = sa::launch_compress_prefill(kv, score, B, S, D, r, weight, eps, out,
+  if ((kv_state == nullptr) != (score_state == nullptr))
+    return fail(SA_ERR_INVALID_ARG, "kv_state and score_state go together");
+  if (B > 0 && S % r && kv_state && (!kv || !score))
+    return fail(SA_ERR_INVALID_ARG, "kv and score must be device pointers");
+  if (!aligned4(kv) || !aligned4(score) || !aligned4(weight) || !aligned4(out) || !aligned4(kv_state) ||
+      !aligned4(score_state))
+    return fail(SA_ERR_INVALID_ARG, "kv, score, weight, out and the states must be 4-byte aligned");
+  cudaError_t e = sa::launch_compress_prefill(kv, score, B, S, D, r, weight, eps, out, kv_state, score_state,
                                               reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SA_OK : cuda_fail(e, "compressor launch");
+}
+
+sa_status sa_compress_decode(const float *kv, const float *score, const int32_t *pos, int32_t B, int32_t D,
+                             int32_t r, float *kv_state, float *score_state, const float *weight, float eps,
+                             void *out, void *ws, size_t ws_bytes, sa_stream_t stream) {
+  if (sa_status s = check_compressor(B, D, r, eps)) return s;
+  if (B > 0 && (!kv || !score || !pos || !kv_state || !score_state || !weight || !out))
+    return fail(SA_ERR_INVALID_ARG, "kv, score, pos, the states, weight and out must be device pointers");
+  if (!aligned4(kv) || !aligned4(score) || !aligned4(pos) || !aligned4(kv_state) || !aligned4(score_state) ||
+      !aligned4(weight) || !aligned4(out))
+    return fail(SA_ERR_INVALID_ARG, "every pointer must be 4-byte aligned");
+  if (sa_status s = check_ws(ws, ws_bytes, 256)) return s;
+  cudaError_t e = sa::launch_compress_decode(kv, score, pos, B, D, r, kv_state, score_state, weight, eps, out,
+                                             at<uint32_t>(ws, 0), reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SA_OK : cuda_fail(e, "compressor decode launch");
+}
+
+sa_status sa_index_key_publish(const void *kproj, int32_t n, int32_t D_I, const int32_t *seq, const int32_t *grp,
+                               int32_t r, const float *weight, float eps, const sa_rope_args *rope, uint8_t *k_I,
+                               float *k_scale, int32_t B, int32_t N_rows, int64_t k_seq_stride, void *ws,
+                               size_t ws_bytes, sa_stream_t stream) {
+  if (n < 0 || B < 1 || N_rows < 1 || r < 1)
+    return fail(SA_ERR_INVALID_ARG, "need n >= 0, B >= 1, N_rows >= 1, r >= 1");
+  if (D_I != 128) return fail(SA_ERR_UNSUPPORTED, "index head dim %d: the key producer takes 128", D_I);
+  if (!rope) return fail(SA_ERR_INVALID_ARG, "rope args pointer is NULL");
+  if (rope->dim < 0 || rope->dim > D_I || rope->dim % 4)
+    return fail(SA_ERR_INVALID_ARG, "rope dim %d: need a multiple of 4 in [0, %d]", rope->dim, D_I);
+  if (rope->dim > 0 && (!std::isfinite(rope->base) || rope->base <= 1.0 || !std::isfinite(rope->factor) ||
+                        rope->factor <= 0.0 ||
+                        (rope->original_seq_len > 0 && !(rope->beta_fast > 0.0 && rope->beta_slow > 0.0))))
+    return fail(SA_ERR_INVALID_ARG, "rope base > 1, factor > 0 and, with YaRN, beta_fast and beta_slow > 0");
+  if (!std::isfinite(eps) || eps < 0.f) return fail(SA_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (k_seq_stride != 0 && (k_seq_stride % D_I || k_seq_stride < static_cast<int64_t>(N_rows) * D_I))
+    return fail(SA_ERR_INVALID_ARG, "k_seq_stride %lld: need 0 or a multiple of D_I of at least N_rows * D_I",
+                static_cast<long long>(k_seq_stride));
+  if (n > 0 && (!kproj || !seq || !grp || !weight || !k_I || !k_scale))
+    return fail(SA_ERR_INVALID_ARG, "kproj, seq, grp, weight, k_I and k_scale must be device pointers");
+  if (!aligned16(kproj) || !aligned4(k_I) || !aligned4(seq) || !aligned4(grp) || !aligned4(weight) ||
+      !aligned4(k_scale))
+    return fail(SA_ERR_INVALID_ARG, "kproj must be 16-byte aligned; k_I and the other arrays 4-byte aligned");
+  if (sa_status s = check_ws(ws, ws_bytes, 256)) return s;
+  cudaError_t e = sa::launch_index_key_publish(kproj, n, seq, grp, r, weight, eps, *rope, k_I, k_scale, B, N_rows,
+                                               k_seq_stride, at<uint32_t>(ws, 0),
+                                               reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SA_OK : cuda_fail(e, "index key launch");
 }
 
 sa_status sa_rotate_quant(const void *x, int32_t rows, int32_t dim, const int32_t *dst, int64_t dst_rows,

@@ -106,6 +106,9 @@ def _lib(mutant: int = 0, path: Optional[str] = None):
         lib.orc_apply_rope.argtypes = [vp, i32, ctypes.c_int64, ctypes.c_double, ctypes.c_double, i32,
                                        ctypes.c_double, ctypes.c_double, i32]
         lib.orc_candidate_blocks.restype = i32
+        lib.orc_index_key.argtypes = [vp, i32, vp, ctypes.c_double, ctypes.c_int64, i32, ctypes.c_double,
+                                      ctypes.c_double, i32, ctypes.c_double, ctypes.c_double, vp, vp, vp]
+        lib.orc_index_key.restype = i32
         lib.orc_sparse_attn.argtypes = [P, vp, i32, vp, i32, vp]
         lib.orc_sparse_attn.restype = i32
         lib.orc_fused.argtypes = [P, i32, vp, i32, vp, vp]
@@ -376,6 +379,25 @@ def compress_decode(kv_tok: np.ndarray, score_tok: np.ndarray, pos: int, r: int,
     if rc < 0:
         raise ValueError("oracle: invalid compressor arguments")
     return out if rc == 1 else None
+
+
+def index_key(x_bits: np.ndarray, weight: np.ndarray, eps: float, pos: int, rope: Rope, mutant: int = 0):
+    """The index key of one compressed row ("DeepSeek-V4.1-Flash-NVFP4
+    inference/model.py", Indexer.forward, the key-owning layer): x_bits is a row
+    of wk(latent) as bf16 bits; returns (codes uint8 [D], scale float32, the
+    bf16 key before quantisation as bits [D]).  The rotation takes `pos`, the
+    position of the group's first token."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16).reshape(-1)
+    w = np.ascontiguousarray(weight, dtype=np.float32)
+    D = x.size
+    codes = np.empty(D, dtype=np.uint8)
+    scale = np.empty(1, dtype=np.float32)
+    k = np.empty(D, dtype=np.uint16)
+    if _lib(mutant).orc_index_key(x.ctypes.data, D, w.ctypes.data, eps, pos, rope.dim, rope.base, rope.factor,
+                                  rope.original_seq_len, rope.beta_fast, rope.beta_slow, codes.ctypes.data,
+                                  scale.ctypes.data, k.ctypes.data) != 0:
+        raise ValueError("oracle: invalid index-key arguments")
+    return codes, scale[0], k
 
 
 def sparse_attn(p: Problem, idx: np.ndarray, rows=None, mutant: int = 0) -> np.ndarray:

@@ -617,6 +617,77 @@ void orc_apply_rope(double *x, int32_t dim, int64_t pos, double base, double fac
   }
 }
 
+/* ---- V4.1 index keys of a compressing layer ------------------------------- */
+
+/* The bfloat16 nearest (ties to even) to a finite double, rounded once. */
+static uint16_t bf16_nearest_d(double v) {
+  const uint16_t sign = signbit(v) ? 0x8000u : 0u;
+  const double a = fabs(v);
+  if (a == 0.0) return sign;
+  int e;
+  (void)frexp(a, &e); /* a = f 2^e, f in [0.5, 1): the leading bit has weight 2^(e-1) */
+  int q = e - 1 - 7;  /* quantum of 8 significant bits */
+  if (q < -133) q = -133; /* subnormal range */
+  double c = rint(ldexp(a, -q)); /* exact scaling, one rounding (ties to even) */
+  if (c >= 256.0) { /* carried into the next binade */
+    c = 128.0;
+    q += 1;
+  }
+  uint16_t bits;
+  if (c < 128.0) {
+    bits = (uint16_t)c; /* subnormal */
+  } else {
+    const int bexp = q + 7 + 127;
+    bits = bexp >= 255 ? 0x7F80u : (uint16_t)((bexp << 7) | (int)(c - 128.0));
+  }
+  return sign | bits;
+}
+
+/* "DeepSeek-V4.1-Flash-NVFP4 inference/model.py", Indexer.forward in a layer
+ * that owns the index keys: k = k_norm(wk(latent)), then apply_rotary_emb on
+ * the last rope_dim values at the position of the group's first token, then
+ * the key's quantisation, then the write to the key cache at row
+ * start_pos // ratio.  Here x is one row of wk(latent) (bf16, D values):
+ *   RMSNorm.forward: y = weight * x / sqrt(mean(x^2) + eps), cast to bf16;
+ *   the rotation of pairs (y[D - rope_dim + 2i], y[D - rope_dim + 2i + 1]) by
+ *   the angle of pair i at `pos` (orc_rope_angle), cast back to bf16;
+ *   the page's fp4 block quantisation read as the V3.2 act_quant of one
+ *   128-value block: scale = amax / 448 and e4m3 codes (orc_act_quant_row).
+ * Arithmetic in double between the two bf16 roundings, each a single
+ * rounding of the exact value; the quantiser in fp32.  k_bf16 (optional)
+ * receives the bf16 key before quantisation. */
+int32_t orc_index_key(const uint16_t *x, int32_t D, const float *weight, double eps, int64_t pos, int32_t rope_dim,
+                      double base, double factor, int32_t original_seq_len, double beta_fast, double beta_slow,
+                      uint8_t *codes, float *scale, uint16_t *k_bf16) {
+  if (D < 1 || rope_dim < 0 || rope_dim > D || (rope_dim & 1) || pos < 0) return -1;
+  double *v = (double *)malloc(sizeof(double) * (size_t)D);
+  uint16_t *k = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)D);
+  double ss = 0.0;
+  for (int32_t d = 0; d < D; ++d) {
+    v[d] = orc_bf16_value(x[d]);
+    ss += v[d] * v[d];
+  }
+#if ORC_MUTANT == 23
+  const double inv = 1.0 / sqrt(ss / (double)D); /* eps left out */
+#else
+  const double inv = 1.0 / sqrt(ss / (double)D + eps);
+#endif
+  for (int32_t d = 0; d < D; ++d) k[d] = bf16_nearest_d((double)weight[d] * (v[d] * inv));
+#if ORC_MUTANT == 22
+  const int32_t r0 = 0; /* the rotation applied to the first rope_dim values */
+#else
+  const int32_t r0 = D - rope_dim;
+#endif
+  for (int32_t d = 0; d < rope_dim; ++d) v[d] = orc_bf16_value(k[r0 + d]);
+  orc_apply_rope(v, rope_dim, pos, base, factor, original_seq_len, beta_fast, beta_slow, 0);
+  for (int32_t d = 0; d < rope_dim; ++d) k[r0 + d] = bf16_nearest_d(v[d]);
+  if (k_bf16) memcpy(k_bf16, k, sizeof(uint16_t) * (size_t)D);
+  orc_act_quant_row(k, D, codes, scale);
+  free(k);
+  free(v);
+  return 0;
+}
+
 /* ---- sparse attention ---------------------------------------------------- */
 
 /* For query token t (sequence b, position p) the key set J is the window rows

@@ -66,6 +66,9 @@ double orc_rope_angle(int32_t dim, int32_t i, int64_t pos, double base, double f
                       double beta_fast, double beta_slow);
 void orc_apply_rope(double *x, int32_t dim, int64_t pos, double base, double factor, int32_t original_seq_len,
                     double beta_fast, double beta_slow, int32_t inverse);
+int32_t orc_index_key(const uint16_t *x, int32_t D, const float *weight, double eps, int64_t pos, int32_t rope_dim,
+                      double base, double factor, int32_t original_seq_len, double beta_fast, double beta_slow,
+                      uint8_t *codes, float *scale, uint16_t *k_bf16);
 int32_t orc_compress_decode(const float *kv_tok, const float *score_tok, int32_t pos, int32_t D, int32_t r,
                             float *kv_state, float *score_state, const float *weight, double eps, double *out);
 int32_t orc_sparse_attn(const orc_problem *P, const int32_t *idx /*[T,K]*/, int32_t K,

@@ -233,12 +233,60 @@ def test_rotate_quant_with_no_rows_enqueues_nothing(lib):
     (dict(out=258), binding.SA_ERR_INVALID_ARG),
 ])
 def test_compress_prefill_rejects_bad_arguments(lib, kw, status):
-    a = dict(kv=256, score=256, B=2, S=8, D=64, r=4, weight=256, eps=1e-6, out=256)
+    a = dict(kv=256, score=256, B=2, S=8, D=64, r=4, weight=256, eps=1e-6, out=256, kvs=None, scs=None)
     a.update(kw)
     st = lib.sa_compress_prefill(a["kv"], a["score"], a["B"], a["S"], a["D"], a["r"], a["weight"], a["eps"], a["out"],
-                                 None)
+                                 a["kvs"], a["scs"], None)
     assert st == status
 
 
+def test_compress_prefill_states_go_together(lib):
+    assert lib.sa_compress_prefill(256, 256, 2, 9, 64, 4, 256, 1e-6, 256, 256, None, None) == binding.SA_ERR_INVALID_ARG
+
+
 def test_compress_prefill_with_no_group_enqueues_nothing(lib):
-    assert lib.sa_compress_prefill(None, None, 2, 3, 64, 4, None, 1e-6, None, None) == binding.SA_OK
+    assert lib.sa_compress_prefill(None, None, 2, 3, 64, 4, None, 1e-6, None, None, None, None) == binding.SA_OK
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(r=1), binding.SA_ERR_INVALID_ARG),
+    (dict(D=40), binding.SA_ERR_UNSUPPORTED),
+    (dict(pos=None), binding.SA_ERR_INVALID_ARG),
+    (dict(kvs=258), binding.SA_ERR_INVALID_ARG),
+    (dict(ws=None), binding.SA_ERR_WORKSPACE),
+])
+def test_compress_decode_rejects_bad_arguments(lib, kw, status):
+    a = dict(kv=256, score=256, pos=256, B=2, D=64, r=4, kvs=256, scs=256, weight=256, eps=1e-6, out=256, ws=256,
+             ws_bytes=256)
+    a.update(kw)
+    st = lib.sa_compress_decode(a["kv"], a["score"], a["pos"], a["B"], a["D"], a["r"], a["kvs"], a["scs"],
+                                a["weight"], a["eps"], a["out"], a["ws"], a["ws_bytes"], None)
+    assert st == status
+
+
+def _rope(**kw):
+    base = dict(dim=64, base=160000.0, factor=16.0, original_seq_len=65536, beta_fast=32.0, beta_slow=1.0)
+    base.update(kw)
+    return binding.RopeArgs(*[base[f] for f, _ in binding.RopeArgs._fields_])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D_I=64), binding.SA_ERR_UNSUPPORTED),
+    (dict(rope=_rope(dim=66)), binding.SA_ERR_INVALID_ARG),
+    (dict(rope=_rope(dim=132)), binding.SA_ERR_INVALID_ARG),
+    (dict(rope=_rope(base=1.0)), binding.SA_ERR_INVALID_ARG),
+    (dict(rope=None), binding.SA_ERR_INVALID_ARG),
+    (dict(stride=100 * 128 - 128), binding.SA_ERR_INVALID_ARG),
+    (dict(kproj=264), binding.SA_ERR_INVALID_ARG),
+    (dict(seq=None), binding.SA_ERR_INVALID_ARG),
+    (dict(ws=None), binding.SA_ERR_WORKSPACE),
+    (dict(n=-1), binding.SA_ERR_INVALID_ARG),
+])
+def test_index_key_publish_rejects_bad_arguments(lib, kw, status):
+    a = dict(kproj=256, n=4, D_I=128, seq=256, grp=256, r=4, weight=256, eps=1e-6, rope=_rope(), k_I=256,
+             k_scale=256, B=2, N_rows=100, stride=0, ws=256, ws_bytes=256)
+    a.update(kw)
+    st = lib.sa_index_key_publish(a["kproj"], a["n"], a["D_I"], a["seq"], a["grp"], a["r"], a["weight"], a["eps"],
+                                  ctypes.byref(a["rope"]) if a["rope"] is not None else None, a["k_I"], a["k_scale"],
+                                  a["B"], a["N_rows"], a["stride"], a["ws"], a["ws_bytes"], None)
+    assert st == status
