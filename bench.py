@@ -55,6 +55,7 @@ def parse():
     ap.add_argument("--no-v41", action="store_true", help="skip the V4.1-shape measurement")
     ap.add_argument("--v41-only", action="store_true", help="print only the V4.1-shape measurement")
     ap.add_argument("--producer-only", action="store_true", help="print only the index-producer measurement")
+    ap.add_argument("--compressor-only", action="store_true", help="print only the compressor measurement")
     return ap.parse_args()
 
 
@@ -584,6 +585,74 @@ def workload_field(binding, torch, wl, name, steps, warmup, n_copies, peak):
     return res
 
 
+def compressor_field(binding, torch, steps, peak):
+    """Device time of the V4.1 compressor (row f3) on synthetic inputs, L2
+    flushed before each launch: the prefill of a 4096-token chunk (D 512,
+    r 4: 1024 groups), one decode step of 128 sequences whose groups all
+    complete, and the index-key producer on the chunk's 1024 compressed rows
+    and on the decode step's 128."""
+    gen = torch.Generator(device="cuda").manual_seed(44)
+    D, r, S = 512, 4, 4096
+    G = S // r
+    kv = torch.randn((1, S, D), device="cuda", generator=gen)
+    sc = torch.randn((1, S, D), device="cuda", generator=gen)
+    w = torch.rand(D, device="cuda", generator=gen) + 0.5
+    latent = torch.empty((1, G, D), dtype=torch.bfloat16, device="cuda")
+    B = 128
+    kv_d = torch.randn((B, D), device="cuda", generator=gen)
+    sc_d = torch.randn((B, D), device="cuda", generator=gen)
+    kvs = torch.randn((B, r, D), device="cuda", generator=gen)
+    scs = torch.randn((B, r, D), device="cuda", generator=gen)
+    pos = torch.full((B,), 4 * 8191 + 3, dtype=torch.int32, device="cuda")  # every group completes
+    out_d = torch.empty((B, D), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    binding.sa_workspace_init(ws)
+    rope = binding.RopeArgs(64, 160000.0, 16.0, 65536, 32.0, 1.0)
+    kn = torch.rand(128, device="cuda", generator=gen) + 0.5
+    kproj = torch.randn((G, 128), device="cuda", generator=gen).bfloat16()
+    kI = torch.empty((B, 32768, 128), dtype=torch.uint8, device="cuda")
+    ks = torch.empty((B, 32768), dtype=torch.float32, device="cuda")
+    seq_p = torch.zeros(G, dtype=torch.int32, device="cuda")
+    grp_p = torch.arange(G, dtype=torch.int32, device="cuda")
+    seq_d = torch.arange(B, dtype=torch.int32, device="cuda")
+    grp_d = torch.full((B,), 8191, dtype=torch.int32, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    calls = {
+        "prefill_4096x512": (lambda: binding.sa_compress_prefill(kv, sc, 1, S, D, r, w, 1e-6, latent),
+                             2 * S * D * 4 + G * D * 2),
+        "decode_b128x512": (lambda: binding.sa_compress_decode(kv_d, sc_d, pos, B, D, r, kvs, scs, w, 1e-6, out_d, ws),
+                            B * (2 * D * 4 + 2 * D * 4 + 2 * r * D * 4 + D * 2)),
+        "index_keys_1024_rows": (lambda: binding.sa_index_key_publish(kproj, G, seq_p, grp_p, r, kn, 1e-6, rope, kI,
+                                                                      ks, B, 32768, ws),
+                                 G * (128 * 2 + 128 + 4 + 8)),
+        "index_keys_128_rows": (lambda: binding.sa_index_key_publish(kproj[:B], B, seq_d, grp_d, r, kn, 1e-6, rope, kI,
+                                                                     ks, B, 32768, ws),
+                                B * (128 * 2 + 128 + 4 + 8)),
+    }
+    res = {"workload": "prefill chunk of 4096 tokens (D 512, r 4); decode step of 128 sequences whose groups all "
+                       "complete; index keys (128 values, rope 64, YaRN) for 1024 and 128 rows; N(0,1) inputs; "
+                       "L2 flushed per launch"}
+    for name, (f, alg) in calls.items():
+        for _ in range(3):
+            f()
+        tot, n = 0.0, max(5, steps)
+        for _ in range(n):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            f()
+            e1.record()
+            torch.cuda.synchronize()
+            tot += e0.elapsed_time(e1)
+        us = tot / n * 1000.0
+        gbs = alg / (us / 1e6) / 1e9
+        res[name] = {"us": round(us, 2), "algorithmic_bytes": alg, "GB_s": round(gbs, 1),
+                     "frac_of_hbm_peak": round(gbs / peak, 4)}
+    if binding.sa_check_device_status(ws) != binding.SA_OK:
+        raise RuntimeError("device status not OK after the compressor")
+    return res
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -604,6 +673,10 @@ def run_ours(args):
     if args.producer_only:
         if rank == 0:
             print(json.dumps({"index_producer": index_producer(binding, torch, args.steps, peaks()[0])}), flush=True)
+        return
+    if args.compressor_only:
+        if rank == 0:
+            print(json.dumps({"compressor": compressor_field(binding, torch, args.steps, peaks()[0])}), flush=True)
         return
     if args.v41_only:
         if rank == 0:
@@ -738,6 +811,7 @@ def run_ours(args):
     two_level = None if args.no_two_level else two_level_topk(binding, torch, wl, args.steps, peak)
     v41 = None if args.no_v41 else v41_decode(binding, torch, args.steps, peak)
     producer = index_producer(binding, torch, args.steps, peak)
+    compressor = compressor_field(binding, torch, args.steps, peak)
     extra = {}
     for name in [x for x in args.extra.split(",") if x and x != spec.name]:
         extra[name] = workload_field(binding, torch, wl, name, args.steps, args.warmup, args.copies, peak)
@@ -771,6 +845,7 @@ def run_ours(args):
         "two_level_topk": two_level,
         "v41_decode": v41,
         "index_producer": producer,
+        "compressor": compressor,
         "workloads": extra,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

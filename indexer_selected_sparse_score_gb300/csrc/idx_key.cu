@@ -9,9 +9,11 @@
 // rotation run in double, so that each of the two bf16 results (after the
 // norm, after the rotation) is one rounding of a value whose error is far
 // below a bf16 step; the block quantisation (scale = amax / 448, e4m3 codes of
-// k / scale) takes correctly rounded fp32 quotients.  The rows are few (one
-// per sequence every r decode steps, S / r per prefilled sequence), so the
-// double arithmetic costs nothing that matters; the kernel is latency-bound.
+// k / scale) takes correctly rounded fp32 quotients.  The rotation
+// frequencies depend on the rotary parameters only and are tabled per launch
+// on the host (as precompute_freqs_cis tables them once); each pair's angle
+// and its sine and cosine are taken in double in the kernel.
+#include <algorithm>
 #include <cmath>
 
 #include "common.cuh"
@@ -24,26 +26,20 @@ constexpr int kKeyDim = 128;
 constexpr int kKeyWarps = 4;
 constexpr double kPi = 3.14159265358979323846;
 
-// Frequency of rotation pair i (YaRN-corrected when original_seq_len > 0).
-__device__ double rope_frequency(int i, const sa_rope_args &a) {
-  const double f = 1.0 / pow(a.base, static_cast<double>(2 * i) / a.dim);
-  if (a.original_seq_len <= 0) return f;
-  // the dimension whose wavelength completes `turns` rotations over the
-  // training context
-  auto corrected = [&](double turns) {
-    return a.dim * log(a.original_seq_len / (turns * 2.0 * kPi)) / (2.0 * log(a.base));
-  };
-  const double low = fmax(floor(corrected(a.beta_fast)), 0.0);
-  const double high = fmin(ceil(corrected(a.beta_slow)), static_cast<double>(a.dim - 1));
-  const double ramp = fmin(fmax((i - low) / fmax(high - low, 1e-3), 0.0), 1.0);
-  return f / a.factor * ramp + f * (1.0 - ramp);
-}
+constexpr int kMaxPairs = kKeyDim / 2;
+
+// Rotation frequencies of the launch, one per pair (precompute_freqs_cis's
+// table, computed once per launch on the host: they depend on the rotary
+// parameters only).
+struct RopeFreqs {
+  double f[kMaxPairs];
+};
 
 __global__ void __launch_bounds__(32 * kKeyWarps)
 index_key_kernel(const uint16_t *__restrict__ kproj, int n, const int32_t *__restrict__ seq,
-                 const int32_t *__restrict__ grp, int r, const float *__restrict__ weight, float eps,
-                 const sa_rope_args rope, uint8_t *__restrict__ k_I, float *__restrict__ k_scale, int B, int N_rows,
-                 int64_t kseq_rows, uint32_t *status) {
+                 const int32_t *__restrict__ grp, int r, const float *__restrict__ weight, float eps, int rope_dim,
+                 const __grid_constant__ RopeFreqs freqs, uint8_t *__restrict__ k_I, float *__restrict__ k_scale,
+                 int B, int N_rows, int64_t kseq_rows, uint32_t *status) {
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kKeyWarps + (threadIdx.x >> 5);
   if (row >= n) return;
@@ -67,14 +63,14 @@ index_key_kernel(const uint16_t *__restrict__ kproj, int n, const int32_t *__res
   for (int e = 0; e < 4; ++e)
     k[e] = __bfloat162float(__double2bfloat16(static_cast<double>(weight[4 * lane + e]) * (x[e] * inv)));
   // rotation of the last rope.dim values: pairs (first + 2i, first + 2i + 1)
-  const int first = kKeyDim - rope.dim;
+  const int first = kKeyDim - rope_dim;
   if (4 * lane >= first) {
     const double pos = static_cast<double>(j) * r;  // a latent stands for its group's first token
 #pragma unroll
     for (int e = 0; e < 4; e += 2) {
       const int i = (4 * lane + e - first) / 2;
       double sn, cs;
-      sincos(pos * rope_frequency(i, rope), &sn, &cs);
+      sincos(pos * freqs.f[i], &sn, &cs);
       const double re = k[e], im = k[e + 1];
       k[e] = __bfloat162float(__double2bfloat16(re * cs - im * sn));
       k[e + 1] = __bfloat162float(__double2bfloat16(re * sn + im * cs));
@@ -104,9 +100,32 @@ cudaError_t launch_index_key_publish(const void *kproj, int n, const int32_t *se
                                      cudaStream_t stream) {
   if (n == 0) return cudaSuccess;
   const int64_t kseq_rows = k_seq_stride ? k_seq_stride / kKeyDim : N_rows;
+  // f_i = base^(-2i / dim); with original_seq_len > 0 (YaRN) the pairs below
+  // the corrected dimension of beta_fast keep it, those above that of
+  // beta_slow are divided by factor, and a linear ramp fades between (the
+  // corrected dimension: the one whose wavelength completes `turns` rotations
+  // over the training context)
+  RopeFreqs fr{};
+  const int pairs = rope.dim / 2;
+  double low = 0.0, high = 0.0;
+  if (rope.original_seq_len > 0) {
+    auto corrected = [&](double turns) {
+      return rope.dim * std::log(rope.original_seq_len / (turns * 2.0 * kPi)) / (2.0 * std::log(rope.base));
+    };
+    low = std::max(std::floor(corrected(rope.beta_fast)), 0.0);
+    high = std::min(std::ceil(corrected(rope.beta_slow)), static_cast<double>(rope.dim - 1));
+  }
+  for (int i = 0; i < pairs; ++i) {
+    double f = 1.0 / std::pow(rope.base, static_cast<double>(2 * i) / rope.dim);
+    if (rope.original_seq_len > 0) {
+      const double ramp = std::min(std::max((i - low) / std::max(high - low, 1e-3), 0.0), 1.0);
+      f = f / rope.factor * ramp + f * (1.0 - ramp);
+    }
+    fr.f[i] = f;
+  }
   return launch_ex(false, index_key_kernel, dim3((n + kKeyWarps - 1) / kKeyWarps), dim3(32 * kKeyWarps), 0, stream, 1,
-                   static_cast<const uint16_t *>(kproj), n, seq, grp, r, weight, eps, rope, k_I, k_scale, B, N_rows,
-                   kseq_rows, status);
+                   static_cast<const uint16_t *>(kproj), n, seq, grp, r, weight, eps, rope.dim, fr, k_I, k_scale, B,
+                   N_rows, kseq_rows, status);
 }
 
 }  // namespace sa

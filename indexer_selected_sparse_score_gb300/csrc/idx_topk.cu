@@ -270,15 +270,26 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
   __shared__ uint32_t sel_gt[kRegMax / 32], sel_eq[kRegMax / 32];  // pick bitmaps by position
   pdl_trigger();
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the token arrays are inputs of the call, not outputs of the previous
+  // kernel: read them before waiting for it, so that the score loads can stop
+  // at the visible count
+  Token tk;
+  const bool ok = load_token(q_seq, q_pos, t, B, N_c, r, status, tk, tid == 0);
+  const int nv = ok ? tk.nv : 0;
+  int32_t *out = idx + static_cast<int64_t>(t) * K;
   pdl_wait();  // the scores come from the previous kernel
-  // the row's raw scores: chunk q of this thread is positions 4096 q + 4 tid .. + 3
+  if (nv <= K) {  // every visible position is kept
+    for (int i = tid; i < K; i += NT) out[i] = i < nv ? i : -1;
+    return;
+  }
+  // the row's visible scores: chunk q of this thread is positions 4096 q + 4 tid .. + 3
   const float *row = scores + static_cast<int64_t>(t) * ld;
   uint32_t key[E];
   if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
 #pragma unroll
     for (int q = 0; q < E / 4; ++q) {
       const int p0 = kChunkSpan * q + 4 * tid;
-      if (p0 + 3 < N_c) {
+      if (p0 + 3 < nv) {
         const uint4 u = *reinterpret_cast<const uint4 *>(row + p0);
         key[4 * q] = u.x;
         key[4 * q + 1] = u.y;
@@ -286,14 +297,14 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
         key[4 * q + 3] = u.w;
       } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) key[4 * q + j] = p0 + j < N_c ? __float_as_uint(row[p0 + j]) : 0u;
+        for (int j = 0; j < 4; ++j) key[4 * q + j] = p0 + j < nv ? __float_as_uint(row[p0 + j]) : 0u;
       }
     }
   } else {
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const int p0 = kChunkSpan * (e >> 2) + 4 * tid + (e & 3);
-      key[e] = p0 < N_c ? __float_as_uint(row[p0]) : 0u;
+      key[e] = p0 < nv ? __float_as_uint(row[p0]) : 0u;
     }
   }
   // the row's candidate mask (kCand) goes to shared memory with one load per
@@ -302,14 +313,6 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
   if constexpr (kCand) {
     const uint32_t *crow = cmask + static_cast<int64_t>(t) * cand_words;
     for (int i = tid; i < cand_words; i += NT) cwords[i] = crow[i];
-  }
-  Token tk;
-  const bool ok = load_token(q_seq, q_pos, t, B, N_c, r, status, tk, tid == 0);
-  const int nv = ok ? tk.nv : 0;
-  int32_t *out = idx + static_cast<int64_t>(t) * K;
-  if (nv <= K) {  // every visible position is kept
-    for (int i = tid; i < K; i += NT) out[i] = i < nv ? i : -1;
-    return;
   }
 #pragma unroll
   for (int w = 0; w < kSelWords; ++w) {
