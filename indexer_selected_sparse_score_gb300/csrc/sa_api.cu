@@ -143,6 +143,8 @@ WsLayout ws_layout(const sa_index_args &ia, const sa_attn_args *aa, int K) {
   L.attn_scratch = L.part_m = L.part_l = L.part_o = off;
   if (aa && attn_umma_supported(*aa)) {
     off += round_up(attn_umma_scratch(ia, aa ? *aa : sa_attn_args{}, K));
+  } else if (aa && attn_umma512_supported(*aa)) {
+    // the head-dim-512 tensor-core attention keeps nothing in global memory
   } else if (aa) {
     const SplitPlan plan = plan_splits(ia.T, aa->W, K);
     const size_t th = static_cast<size_t>(ia.T) * aa->H * plan.splits;

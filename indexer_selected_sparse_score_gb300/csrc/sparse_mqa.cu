@@ -624,7 +624,7 @@ int fused_launch_count(const sa_index_args &ia, const sa_attn_args &aa, int K,
                        const SplitPlan &plan) {
   const int score = idx_score_umma_supported(ia) ? 2 : 1;  // (query packing +) scoring
   const int topk = K > 0 ? 1 : 0;
-  const int attn = attn_umma_supported(aa) ? 1 : (plan.splits > 1 ? 2 : 1);
+  const int attn = (attn_umma_supported(aa) || attn_umma512_supported(aa)) ? 1 : (plan.splits > 1 ? 2 : 1);
   return ia.T > 0 ? score + topk + attn : 0;
 }
 
@@ -647,6 +647,7 @@ cudaError_t launch_sparse_mqa(const sa_index_args &ia, const sa_attn_args &aa, c
   if (ia.T == 0) return cudaSuccess;
   if (attn_umma_supported(aa))
     return launch_sparse_mqa_umma(ia, aa, idx, K, out, attn_scratch, status, stream);
+  if (attn_umma512_supported(aa)) return launch_sparse_mqa_umma512(ia, aa, idx, K, out, status, stream);
   AttnParams p;
   p.B = ia.B;
   p.T = ia.T;

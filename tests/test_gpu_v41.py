@@ -74,3 +74,19 @@ def test_fused_dim512(case):
     for t in range(w.T):
         check_topk_sets(g_idx[t], o_idx[t], S[t], A[t], n_vis(int(w.q_pos[t]), w.r), w.K)
     check_attn(g_out, oracle.sparse_attn(problem(w), g_idx))
+
+
+def test_attn_dim512_one_kv_on_oracle_indices(case):
+    """sa_sparse_attn on the oracle's indices with K and V as one device tensor:
+    at 64 heads this is the tensor-core (tcgen05) kernel of the released shape."""
+    import torch
+    name, w, same, S, A = case
+    if not same:
+        pytest.skip("K and V are separate tensors in this case")
+    o_idx = oracle.topk(problem(w), S, w.K)
+    dp = share_kv(w, binding.upload(w))
+    ws = binding.new_workspace(dp)
+    out = torch.empty((w.T, w.H, w.D), dtype=torch.bfloat16, device="cuda")
+    binding.sa_sparse_attn(dp.ia, dp.aa, torch.from_numpy(o_idx).cuda(), w.K, out, ws)
+    assert binding.sa_check_device_status(ws) == binding.SA_OK
+    check_attn(out.float().cpu().numpy().astype(np.float64), oracle.sparse_attn(problem(w), o_idx))
