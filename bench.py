@@ -427,7 +427,7 @@ def v41_decode(binding, torch, steps, peak):
             "sparse_mqa_GB_s": round(attn_bytes / (st["sparse_mqa"] / 1000.0) / 1e9, 1),
             "sparse_mqa_TFLOP_s": round(attn_flop / (st["sparse_mqa"] / 1000.0) / 1e12, 2),
             "sparse_mqa_traffic": recorded_traffic("sparse_mqa", "v41"),
-            "note": "attention at head dim 512 runs on the warp-level bf16 MMA (mma.sync) kernel"}
+            "note": "attention at head dim 512 runs on the tcgen05 kernel (sparse_mqa_umma512): one token per 2-CTA cluster, the parts merged over distributed shared memory"}
 
 
 def index_producer(binding, torch, steps, peak):

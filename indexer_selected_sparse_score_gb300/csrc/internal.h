@@ -79,17 +79,20 @@ cudaError_t launch_candidate_blocks(const float *scores, int64_t ld, const sa_in
 
 // Attention + combine.  The tensor-core kernel (64 heads of dim 128) uses
 // `attn_scratch` (attn_umma_scratch bytes); the CUDA-core kernel uses the
-// split partials part_m/part_l/part_o laid out by `plan`.
+// split partials part_m/part_l/part_o laid out by `plan`.  `inputs_ready`:
+// the previous kernel on the stream is an ordinary (not programmatic) launch
+// made after every input but idx was written, so the tensor-core kernels may
+// read those inputs before waiting for it.
 cudaError_t launch_sparse_mqa(const sa_index_args &ia, const sa_attn_args &aa, const int32_t *idx,
                               int K, void *out, float *part_m, float *part_l, float *part_o,
-                              void *attn_scratch, const SplitPlan &plan, uint32_t *status,
+                              void *attn_scratch, const SplitPlan &plan, bool inputs_ready, uint32_t *status,
                               cudaStream_t stream);
 bool attn_umma_supported(const sa_attn_args &aa);
 // Tensor-core (tcgen05) attention at the released V4.1 shape: 64 heads of dim
 // 512 over one kv tensor (Kw == Vw, Kc == Vc); no scratch.
 bool attn_umma512_supported(const sa_attn_args &aa);
 cudaError_t launch_sparse_mqa_umma512(const sa_index_args &ia, const sa_attn_args &aa, const int32_t *idx, int K,
-                                      void *out, uint32_t *status, cudaStream_t stream);
+                                      void *out, bool inputs_ready, uint32_t *status, cudaStream_t stream);
 size_t attn_umma_scratch(const sa_index_args &ia, const sa_attn_args &aa, int K);
 cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &aa, const int32_t *idx,
                                    int K, void *out, void *scratch, uint32_t *status,

@@ -193,9 +193,10 @@ sa_status fused_with_scratch(const sa_index_args *ia, const sa_attn_args *aa, in
   e = launch_topk(scores, ia->N_c, *ia, K, idx, status, st);
   if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
   const SplitPlan plan = plan_splits(ia->T, aa->W, K);
+  // the top-k launch is an ordinary one, made after every input was written
   e = launch_sparse_mqa(*ia, *aa, idx, K, out, at<float>(scratch, L.part_m),
                         at<float>(scratch, L.part_l), at<float>(scratch, L.part_o),
-                        at<void>(scratch, L.attn_scratch), plan, status, st);
+                        at<void>(scratch, L.attn_scratch), plan, true, status, st);
   return e == cudaSuccess ? SA_OK : cuda_fail(e, "sparse attention launch");
 }
 
@@ -382,7 +383,6 @@ sa_status sa_sparse_attn(const sa_index_args *ia, const sa_attn_args *aa, const 
   if (sa_status s = check_index(ia, false)) return s;
   if (sa_status s = check_attn(aa, ia->T)) return s;
   if (sa_status s = check_c_stride(aa, ia)) return s;
-  if (sa_status s = check_c_stride(aa, ia)) return s;
   if (K < 0) return fail(SA_ERR_INVALID_ARG, "K must be >= 0 (got %d)", K);
   if (ia->T > 0 && (!out || (K > 0 && !idx)))
     return fail(SA_ERR_INVALID_ARG, "out and idx must be device pointers");
@@ -393,7 +393,7 @@ sa_status sa_sparse_attn(const sa_index_args *ia, const sa_attn_args *aa, const 
   const sa::SplitPlan plan = sa::plan_splits(ia->T, aa->W, K);
   cudaError_t e = sa::launch_sparse_mqa(*ia, *aa, idx, K, out, at<float>(ws, L.part_m),
                                         at<float>(ws, L.part_l), at<float>(ws, L.part_o), at<void>(ws, L.attn_scratch), plan,
-                                        at<uint32_t>(ws, 0), reinterpret_cast<cudaStream_t>(stream));
+                                        false, at<uint32_t>(ws, 0), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SA_OK : cuda_fail(e, "sparse attention launch");
 }
 
@@ -430,7 +430,7 @@ static sa_status fused_impl(const sa_index_args *ia, const sa_attn_args *aa, int
   e = mark(2);
   if (e == cudaSuccess)
     e = sa::launch_sparse_mqa(*ia, *aa, idx, K, out, at<float>(ws, L.part_m), at<float>(ws, L.part_l),
-                              at<float>(ws, L.part_o), at<void>(ws, L.attn_scratch), plan, status, st);
+                              at<float>(ws, L.part_o), at<void>(ws, L.attn_scratch), plan, true, status, st);
   if (e == cudaSuccess) e = mark(3);
   return e == cudaSuccess ? SA_OK : cuda_fail(e, "sparse attention launch");
 }

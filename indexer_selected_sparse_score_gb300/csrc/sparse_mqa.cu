@@ -642,12 +642,13 @@ SplitPlan plan_splits(int T, int W, int K) {
 
 cudaError_t launch_sparse_mqa(const sa_index_args &ia, const sa_attn_args &aa, const int32_t *idx,
                               int K, void *out, float *part_m, float *part_l, float *part_o,
-                              void *attn_scratch, const SplitPlan &plan, uint32_t *status,
+                              void *attn_scratch, const SplitPlan &plan, bool inputs_ready, uint32_t *status,
                               cudaStream_t stream) {
   if (ia.T == 0) return cudaSuccess;
   if (attn_umma_supported(aa))
     return launch_sparse_mqa_umma(ia, aa, idx, K, out, attn_scratch, status, stream);
-  if (attn_umma512_supported(aa)) return launch_sparse_mqa_umma512(ia, aa, idx, K, out, status, stream);
+  if (attn_umma512_supported(aa))
+    return launch_sparse_mqa_umma512(ia, aa, idx, K, out, inputs_ready, status, stream);
   AttnParams p;
   p.B = ia.B;
   p.T = ia.T;

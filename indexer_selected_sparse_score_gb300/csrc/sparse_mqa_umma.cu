@@ -176,61 +176,6 @@ __device__ __forceinline__ uint64_t desc_sw128_mnmajor(uint32_t addr, uint32_t l
   return d;
 }
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Every thread of every CTA of the cluster: a barrier with release/acquire
-// ordering at cluster scope.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Arrives (release, cluster scope) on the mbarrier at the same shared-memory
-// offset as `bar` in the cluster's CTA `rank`.
-__device__ __forceinline__ void mbar_arrive_remote(uint64_t *bar, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(bar)), "r"(rank));
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
-}
-
-// Shared-memory address of the same offset in the cluster's CTA `rank`.
-__device__ __forceinline__ uint32_t cluster_map(const void *p, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
-  return remote;
-}
-
-__device__ __forceinline__ void st_cluster_f4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-
-// Bounded wait with acquire at cluster scope (for phases completed by the
-// other CTA of the cluster); the result is the same in every lane.
-__device__ __forceinline__ bool mbar_wait_cluster_warp(uint64_t *bar, uint32_t parity) {
-  auto test = [&]() {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
-        : "memory");
-    return ok != 0;
-  };
-  bool ok = test();
-  if (!ok) {
-    const long long t0 = clock64();
-    while (!(ok = test()))
-      if (clock64() - t0 > kWaitBudgetCycles) break;
-  }
-  return __all_sync(0xffffffffu, ok);
-}
-
 // Key q (0..63) of a thread's 64 keys is present iff bit q/4 of mw[q%4] is
 // set, mw = the tile's mask words shifted to the thread's half (bit g of word
 // e = key 4g+e of the tile).

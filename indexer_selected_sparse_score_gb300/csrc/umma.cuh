@@ -56,6 +56,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// mbar_try_wait with a suspend hint of `ns` nanoseconds: the thread wakes
+// when the phase completes or the hint runs out (for polling several
+// barriers without spinning).
+__device__ __forceinline__ bool mbar_try_wait_ns(uint64_t *bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // True in exactly one lane of the (converged) warp.  Operands computed by the
 // whole warp before an elected issue stay warp-uniform.
 __device__ __forceinline__ bool elect_one() {
@@ -288,6 +303,80 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 // whose rows are 128 bytes long.
 __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t kbyte) {
   return (row >> 3) * 1024u + (row & 7u) * 128u + ((((kbyte >> 4) ^ (row & 7u)) << 4) | (kbyte & 15u));
+}
+
+// ------------------------------------------------------------------ clusters --
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster: a barrier with release/acquire
+// ordering at cluster scope.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrives (release, cluster scope) on the mbarrier at the same shared-memory
+// offset as `bar` in the cluster's CTA `rank`.
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t *bar, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(bar)), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
+// Shared-memory address of the same offset in the cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_map(const void *p, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+  return remote;
+}
+
+__device__ __forceinline__ void st_cluster_f4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// Bounded wait with acquire at cluster scope (for phases completed by the
+// other CTA of the cluster); false if the budget ran out.  The waiting thread
+// polls (no suspend hint): these phases complete once per token.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity) {
+  auto test = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+  };
+  if (test()) return true;
+  const long long t0 = clock64();
+  while (!test())
+    if (clock64() - t0 > kWaitBudgetCycles) return false;
+  return true;
+}
+
+// mbar_wait_cluster in every lane; the result is the same in every lane.
+__device__ __forceinline__ bool mbar_wait_cluster_warp(uint64_t *bar, uint32_t parity) {
+  const bool ok = mbar_wait_cluster(bar, parity);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// this CTA's shared memory to shared memory of a CTA of the cluster
+// (`dst_cluster`, from cluster_map), completing `bytes` of transactions on the
+// mbarrier at `bar_cluster` (from cluster_map) in that CTA.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, const void *src, uint32_t bytes,
+                                                     uint32_t bar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+               : "memory");
 }
 
 }  // namespace umma
