@@ -366,6 +366,20 @@ SA_API sa_status sa_fused_decode_noalloc(const sa_index_args *ia, const sa_attn_
  * or SA_ERR_TIMEOUT. */
 SA_API sa_status sa_check_device_status(void *ws, sa_stream_t stream);
 
+/* Bound on each pipeline wait of the tensor-core attention kernels (heads of
+ * dim 128 and of dim 512, as sa_sparse_attn, sa_fused_decode and
+ * sa_fused_decode_noalloc launch them), in SM clock cycles; 0 restores the
+ * default of 2e9 cycles (about a second).  A wait between the kernel's own
+ * stages (copies, products, softmax, the hand-off between the two CTAs of a
+ * split token) that runs out makes the kernel set the timeout flag of the
+ * status word (sa_check_device_status then returns SA_ERR_TIMEOUT), wait for
+ * the copies and products it already started (those waits keep the default
+ * bound), and return; its outputs are then undefined and the CUDA context
+ * stays usable.  Meant for testing that path and for callers that prefer an
+ * early error to a long stall.  Process-wide; applies to launches made after
+ * it returns.  Returns SA_ERR_INVALID_ARG for a negative value. */
+SA_API sa_status sa_set_wait_budget(int64_t cycles);
+
 /* Text for a status code (static storage). */
 SA_API const char *sa_status_string(sa_status s);
 

@@ -71,7 +71,7 @@ EXPORTED = ("sa_workspace_size", "sa_workspace_init", "sa_indexer_scores", "sa_t
             "sa_compress_prefill", "sa_compress_decode", "sa_index_key_publish",
             "sa_sparse_attn", "sa_fused_decode", "sa_fused_decode_staged",
             "sa_fused_decode_launch_count", "sa_check_device_status", "sa_status_string",
-            "sa_last_error_detail", "sa_fused_decode_noalloc", "sa_noalloc_scratch_bytes")
+            "sa_last_error_detail", "sa_fused_decode_noalloc", "sa_noalloc_scratch_bytes", "sa_set_wait_budget")
 
 _LIB = None
 
@@ -112,6 +112,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.sa_noalloc_scratch_bytes.argtypes = []
     lib.sa_noalloc_scratch_bytes.restype = sz
     lib.sa_check_device_status.argtypes = [vp, vp]
+    lib.sa_set_wait_budget.argtypes = [i64]
+    lib.sa_set_wait_budget.restype = i32
     lib.sa_status_string.argtypes = [i32]
     lib.sa_status_string.restype = ctypes.c_char_p
     lib.sa_last_error_detail.restype = ctypes.c_char_p
@@ -275,6 +277,11 @@ def sa_noalloc_scratch_bytes() -> int:
 def sa_check_device_status(ws, stream=None) -> int:
     """Synchronise, read and clear the sticky device status; returns the sa status."""
     return int(load().sa_check_device_status(_p(ws), _s(stream)))
+
+
+def sa_set_wait_budget(cycles: int) -> None:
+    """Bound (SM cycles, 0 = default) on each pipeline wait of the tensor-core attention kernels."""
+    _check(load().sa_set_wait_budget(int(cycles)))
 
 
 # ------------------------------------------------------ device marshalling ---

@@ -91,12 +91,14 @@ bool attn_umma_supported(const sa_attn_args &aa);
 // Tensor-core (tcgen05) attention at the released V4.1 shape: 64 heads of dim
 // 512 over one kv tensor (Kw == Vw, Kc == Vc); no scratch.
 bool attn_umma512_supported(const sa_attn_args &aa);
+// The wait bound set by sa_set_wait_budget (SM cycles; 0 = the default).
+long long attn_wait_budget();
+
 cudaError_t launch_sparse_mqa_umma512(const sa_index_args &ia, const sa_attn_args &aa, const int32_t *idx, int K,
                                       void *out, bool inputs_ready, uint32_t *status, cudaStream_t stream);
 size_t attn_umma_scratch(const sa_index_args &ia, const sa_attn_args &aa, int K);
-cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &aa, const int32_t *idx,
-                                   int K, void *out, void *scratch, uint32_t *status,
-                                   cudaStream_t stream);
+cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &aa, const int32_t *idx, int K,
+                                   void *out, void *scratch, bool inputs_ready, uint32_t *status, cudaStream_t stream);
 
 // Kernel launches of one fused call (index score, top-k, attention, combine).
 int fused_launch_count(const sa_index_args &ia, const sa_attn_args &aa, int K,

@@ -1,6 +1,7 @@
 // The C ABI declared in include/sa.h: argument checks on the host, workspace
 // carve-up, and the launch sequence of each entry point.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -162,6 +163,9 @@ WsLayout ws_layout(const sa_index_args &ia, const sa_attn_args *aa, int K) {
 }  // namespace sa
 
 namespace sa {
+
+std::atomic<long long> g_wait_budget{0};
+long long attn_wait_budget() { return g_wait_budget.load(); }
 
 sa_status set_error(sa_status s, const char *fmt, ...) {
   char buf[512];
@@ -456,6 +460,12 @@ int32_t sa_fused_decode_launch_count(const sa_index_args *ia, const sa_attn_args
   if (ia->T == 0) return 0;
   const sa::SplitPlan plan = sa::plan_splits(ia->T, aa->W, K);
   return sa::fused_launch_count(*ia, *aa, K, plan);
+}
+
+sa_status sa_set_wait_budget(int64_t cycles) {
+  if (cycles < 0) return fail(SA_ERR_INVALID_ARG, "wait budget must be >= 0 (got %lld)", static_cast<long long>(cycles));
+  sa::g_wait_budget.store(static_cast<long long>(cycles));
+  return SA_OK;
 }
 
 sa_status sa_check_device_status(void *ws, sa_stream_t stream) {

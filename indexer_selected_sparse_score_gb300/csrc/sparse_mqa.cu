@@ -646,7 +646,7 @@ cudaError_t launch_sparse_mqa(const sa_index_args &ia, const sa_attn_args &aa, c
                               cudaStream_t stream) {
   if (ia.T == 0) return cudaSuccess;
   if (attn_umma_supported(aa))
-    return launch_sparse_mqa_umma(ia, aa, idx, K, out, attn_scratch, status, stream);
+    return launch_sparse_mqa_umma(ia, aa, idx, K, out, attn_scratch, inputs_ready, status, stream);
   if (attn_umma512_supported(aa))
     return launch_sparse_mqa_umma512(ia, aa, idx, K, out, inputs_ready, status, stream);
   AttnParams p;

@@ -82,6 +82,8 @@ struct AttnUmmaParams {
   int wseq, cseq;                 // rows between consecutive sequences of the ring and of the compressed cache
   int WT, TPT;                    // window tiles per token, tiles per token
   int split, PT0;                 // CTAs per token (1, or a 2-CTA cluster with one token), tiles of rank 0's part
+  int early;                      // nonzero: every input but idx is complete at launch, so only idx waits for the predecessor
+  long long budget;               // SM cycles a pipeline wait may take before the kernel gives up (drains keep the full budget)
   int evict_first;                // nonzero: K/V rows are read once per call (at most one token per sequence)
   const int32_t *q_seq, *q_pos, *idx;
   const __nv_bfloat16 *Vw, *Vc;   // V rows (window ring, compressed), 128 bf16 each
@@ -319,7 +321,10 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
   __syncthreads();
   if (split > 1) cluster_sync();  // the partner's barriers are initialised before any remote arrival
   tc_fence_after();
-  pdl_wait();  // the selected indices come from the previous kernel
+  // The selected indices come from the previous kernel.  When every other
+  // input is known complete at launch, only the reads of idx wait for it, so
+  // the queries and the window rows load while the previous kernel finishes.
+  if (!p.early) pdl_wait();
   const uint32_t tmem = *tmem_base_s;
   auto fail = [&]() {
     raise_flag(p.status, kFlagTimeout);
@@ -360,12 +365,16 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         }
         int qn = -1, prev_t = -1, issued = 0;
         Token tk{0, 0, 0};
-        bool tok_ok = false;
+        bool tok_ok = false, waited = !p.early;
         int n_w = 0;
         // idx entries of keys 4*lane .. 4*lane+3 of a compressed tile, loaded one
         // tile ahead so their latency overlaps the current tile's copies
         auto load_idx = [&](int n, int32_t (&cc)[4]) {
           const int t = t0 + n / PT, j = J0 + n % PT;
+          if (j >= p.WT && !waited) {
+            pdl_wait();
+            waited = true;
+          }
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             cc[e] = -1;
@@ -373,40 +382,40 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
             if (j >= p.WT && k < p.K) cc[e] = p.idx[static_cast<int64_t>(t) * p.K + k];
           }
         };
+        // a new token: its (sequence, position), and its queries into a Q buffer
+        auto begin_token = [&](int t) -> bool {
+          tok_ok = load_token(p.q_seq, p.q_pos, t, p.B, p.N_c, p.r, p.status, tk, warp == kKWarp0 && lane == 0);
+          n_w = tok_ok ? min(p.W, tk.pos + 1) : 0;
+          ++qn;
+          prev_t = t;
+          if (warp != kKWarp0) return true;
+          const int qb = qn & 1;
+          bool ok = true;
+          if (lane == 0) {
+            ok = mbar_wait(&qempty[qb], ((qn >> 1) & 1) ^ 1, p.budget);
+            if (ok) {
+              // heads 16w..16w+15 -> rows 32w+16qb .. +15, both 64-column halves
+              mbar_expect_tx(&qfull[qb], 2 * kH * 128);
+#pragma unroll
+              for (int w = 0; w < 4; ++w)
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+                  tma_load_2d(qs + kb * 16384 + (32 * w + 16 * qb) * 128, &qmap, &qfull[qb], 64 * kb,
+                              t * kH + 16 * w);
+            } else {
+              fail();
+            }
+          }
+          return __shfl_sync(0xffffffffu, ok, 0);
+        };
+        bool run = begin_token(t0);
         int32_t cnext[4];
         load_idx(0, cnext);
         for (int n = 0; n < count; ++n) {
-          if (__any_sync(0xffffffffu, aborted())) break;
           const int t = t0 + n / PT, j = J0 + n % PT;
           int32_t cidx[4] = {cnext[0], cnext[1], cnext[2], cnext[3]};
-          if (n + 1 < count) load_idx(n + 1, cnext);
-          if (t != prev_t) {
-            tok_ok = load_token(p.q_seq, p.q_pos, t, p.B, p.N_c, p.r, p.status, tk,
-                                warp == kKWarp0 && lane == 0 && j == J0);
-            n_w = tok_ok ? min(p.W, tk.pos + 1) : 0;
-            ++qn;
-            if (warp == kKWarp0) {
-              const int qb = qn & 1;
-              bool ok = true;
-              if (lane == 0) {
-                ok = mbar_wait(&qempty[qb], ((qn >> 1) & 1) ^ 1);
-                if (ok) {
-                  // heads 16w..16w+15 -> rows 32w+16qb .. +15, both 64-column halves
-                  mbar_expect_tx(&qfull[qb], 2 * kH * 128);
-#pragma unroll
-                  for (int w = 0; w < 4; ++w)
-#pragma unroll
-                    for (int kb = 0; kb < 2; ++kb)
-                      tma_load_2d(qs + kb * 16384 + (32 * w + 16 * qb) * 128, &qmap, &qfull[qb], 64 * kb,
-                                  t * kH + 16 * w);
-                } else {
-                  fail();
-                }
-              }
-              if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-            }
-            prev_t = t;
-          }
+          bool ok = run;
+          if (ok && t != prev_t) ok = begin_token(t);
           // rows and presence of keys 4*lane .. 4*lane+3
           const bool window = j < p.WT;
           int rows[4];
@@ -431,10 +440,13 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
             }
           }
           const int s = n % kStages;
-          if (!mbar_wait_warp(&ring_empty[s], ((n / kStages) & 1) ^ 1)) {
-            if (lane == 0) fail();
+          if (ok) ok = mbar_wait_warp(&ring_empty[s], ((n / kStages) & 1) ^ 1, p.budget);
+          if (!ok && lane == 0) fail();
+          // the warps of a ring take the same decision, so that a tile's copies
+          // are issued by all of them or by none: its barrier then completes
+          // and the drain below ends once they land
+          if (is_k ? barrier_any(3, 32 * kKWarps, !ok || aborted()) : barrier_any(1, 32 * kVWarps, !ok || aborted()))
             break;
-          }
           if (warp == kKWarp0) {  // key mask of the tile: bit g of word e = key 4g+e exists
             uint32_t m4[4];
 #pragma unroll
@@ -469,6 +481,8 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
             }
           }
           ++issued;
+          // the next tile's indices load while this tile's rows are in flight
+          if (n + 1 < count) load_idx(n + 1, cnext);
         }
         if ((warp == kKWarp0 || warp == kVWarp0) && lane == 0) {  // drain: every issued copy lands before the CTA exits
           for (int n = max(0, issued - kStages); n < issued; ++n)
@@ -499,10 +513,10 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
           if (t != prev_t_s) {
             ++qn_s;
             prev_t_s = t;
-            if (!mbar_wait_warp(&qfull[qn_s & 1], (qn_s >> 1) & 1)) return false;
+            if (!mbar_wait_warp(&qfull[qn_s & 1], (qn_s >> 1) & 1, p.budget)) return false;
           }
-          if (!mbar_wait_warp(&kfull[s], (n / kStages) & 1) ||
-              !mbar_wait_warp(&sempty[b], ((n / kSBufs) & 1) ^ 1))
+          if (!mbar_wait_warp(&kfull[s], (n / kStages) & 1, p.budget) ||
+              !mbar_wait_warp(&sempty[b], ((n / kSBufs) & 1) ^ 1, p.budget))
             return false;
           tc_fence_after();
           const uint32_t a0 = smem_u32(qs + (qn_s & 1) * 2048), b0 = smem_u32(ks + s * 32768);
@@ -526,8 +540,9 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         auto issue_pv = [&](int n) -> bool {
           const bool first = n % PT == 0;
           const int s = n % kStages, b = n % kSBufs;
-          if (first && tok_pv >= 0 && !mbar_wait_warp(oempty, tok_pv & 1)) return false;
-          if (!mbar_wait_warp(&pfull[b], (n / kSBufs) & 1) || !mbar_wait_warp(&vfull[s], (n / kStages) & 1))
+          if (first && tok_pv >= 0 && !mbar_wait_warp(oempty, tok_pv & 1, p.budget)) return false;
+          if (!mbar_wait_warp(&pfull[b], (n / kSBufs) & 1, p.budget) ||
+              !mbar_wait_warp(&vfull[s], (n / kStages) & 1, p.budget))
             return false;
           if (first) ++tok_pv;
           tc_fence_after();
@@ -579,8 +594,8 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         l = 0.f;
       }
       const int b = n % kSBufs;
-      if (!(mbar_wait_warp(&mfull[n % kMaskSlots], (n / kMaskSlots) & 1) &&
-            mbar_wait_warp(&sfull[b], (n / kSBufs) & 1))) {
+      if (!(mbar_wait_warp(&mfull[n % kMaskSlots], (n / kMaskSlots) & 1, p.budget) &&
+            mbar_wait_warp(&sfull[b], (n / kSBufs) & 1, p.budget))) {
         if (lane == 0) fail();
         break;
       }
@@ -615,7 +630,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         // O holds P.V of tiles up to n-1: wait for P.V(n-1), then scale this
         // warp's rows (factor 1 for heads that keep their reference)
         const int pn = n - 1;
-        if (!mbar_wait_warp(&sempty[pn % kSBufs], (pn / kSBufs) & 1)) {
+        if (!mbar_wait_warp(&sempty[pn % kSBufs], (pn / kSBufs) & 1, p.budget)) {
           if (lane == 0) fail();
           break;
         }
@@ -647,7 +662,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
 
       if (last) {
         // O is complete once P.V(n) is done
-        if (!mbar_wait_warp(&sempty[b], (n / kSBufs) & 1)) {
+        if (!mbar_wait_warp(&sempty[b], (n / kSBufs) & 1, p.budget)) {
           if (lane == 0) fail();
           break;
         }
@@ -659,7 +674,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
           // it is free, laid out by softmax thread (the same thread of rank 0
           // reads them): O chunk q (4 columns) of thread i at 16 (128 q + i),
           // so a warp's store covers 512 contiguous bytes; (m, l) at 32 KB + 8 i
-          if (!mbar_wait_cluster_warp(xempty, 0)) {
+          if (!mbar_wait_cluster_warp(xempty, 0, p.budget)) {
             if (lane == 0) fail();
             break;
           }
@@ -690,7 +705,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
           float m1 = -INFINITY, l1 = 0.f;
           const float4 *xo = reinterpret_cast<const float4 *>(ks) + tid;  // chunk q at xo[128 q]
           if (split > 1) {
-            if (!mbar_wait_cluster_warp(xfull, 0)) {
+            if (!mbar_wait_cluster_warp(xfull, 0, p.budget)) {
               if (lane == 0) fail();
               break;
             }
@@ -751,6 +766,9 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
     }
   }
 
+  // a CTA whose part had no compressed tile never waited for the previous
+  // kernel: it does so before leaving, so that this kernel completes after it
+  if (p.early) pdl_wait();
   tc_fence_before();
   __syncthreads();
   // neither CTA of a cluster leaves while the other may still arrive on its barriers
@@ -822,7 +840,7 @@ bool attn_umma_supported(const sa_attn_args &aa) { return aa.H == kH && aa.D == 
 size_t attn_umma_scratch(const sa_index_args &, const sa_attn_args &, int) { return 0; }
 
 cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &aa, const int32_t *idx, int K,
-                                   void *out, void *, uint32_t *status, cudaStream_t stream) {
+                                   void *out, void *, bool inputs_ready, uint32_t *status, cudaStream_t stream) {
   if (ia.T == 0) return cudaSuccess;
   AttnUmmaParams p;
   p.B = ia.B;
@@ -868,6 +886,9 @@ cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &
   if (e != cudaSuccess) return e;
   p.split = attn_split(ia, p.TPT);
   p.evict_first = ia.T <= ia.B ? 1 : 0;
+  p.early = inputs_ready ? 1 : 0;
+  const long long budget = attn_wait_budget();
+  p.budget = budget > 0 ? budget : kWaitBudgetCycles;
   p.PT0 = (p.TPT + 1) / 2;  // rank 0 takes the larger half (window included); rank 1's hand-off costs about its merge
   const int sms = sm_count();
   // whole tokens (at most one CTA per SM), or one cluster pair per token

@@ -100,6 +100,7 @@ struct Attn512Params {
   int wseq, cseq;    // rows between consecutive sequences of the ring and of the compressed cache
   int evict_first;   // nonzero: rows are read once per call (at most one token per sequence)
   int early;         // nonzero: every input but idx is complete at launch, so only idx waits for the predecessor
+  long long budget;  // SM cycles a pipeline wait may take before the kernel gives up (drains keep the full budget)
   const int32_t *q_seq, *q_pos, *idx;
   const float *sink;
   float qk_scale;    // scale * log2(e)
@@ -311,7 +312,7 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
           if (warp != kCopyWarp0) return true;
           bool ok = true;
           if (lane == 0) {
-            ok = mbar_wait(qempty, (qn & 1) ^ 1);
+            ok = mbar_wait(qempty, (qn & 1) ^ 1, p.budget);
             if (ok) {
               mbar_expect_tx(qfull, kH * kD * 2);
 #pragma unroll
@@ -325,11 +326,11 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
         bool run = begin_token(t0);
         int32_t cnext[4];
         load_idx(0, cnext);
-        for (int n = 0; run && n < count; ++n) {
-          if (__any_sync(0xffffffffu, aborted())) break;
+        for (int n = 0; n < count; ++n) {
           const int t = t0 + n / PT, j = J0 + n % PT;
           int32_t cidx[4] = {cnext[0], cnext[1], cnext[2], cnext[3]};
-          if (t != prev_t && !begin_token(t)) break;
+          bool ok = run;
+          if (ok && t != prev_t) ok = begin_token(t);
           // rows and presence of keys 4 g_own .. 4 g_own + 3
           const bool window = j < p.WT;
           int rows[4];
@@ -354,10 +355,12 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
             }
           }
           const int s = n % kSlots;
-          if (!mbar_wait_warp(&kvempty[s], ((n / kSlots) & 1) ^ 1)) {
-            if (lane == 0) fail();
-            break;
-          }
+          if (ok) ok = mbar_wait_warp(&kvempty[s], ((n / kSlots) & 1) ^ 1, p.budget);
+          if (!ok && lane == 0) fail();
+          // every copy warp takes the same decision, so that a tile's copies are
+          // issued by all of them or by none: its barrier then completes and
+          // the drain below ends once they land
+          if (barrier_any(1, 32 * kCopyWarps, !ok || aborted())) break;
           if (warp == kCopyWarp0) {  // key mask: bit g of word e = key 4g+e exists
             uint32_t m4[4];
 #pragma unroll
@@ -424,9 +427,10 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
           if (t != prev_t_s) {
             ++tok_s;
             prev_t_s = t;
-            if (!mbar_wait_warp(qfull, tok_s & 1)) return false;
+            if (!mbar_wait_warp(qfull, tok_s & 1, p.budget)) return false;
           }
-          if (!mbar_wait_warp(&kvfull[s], (n / kSlots) & 1) || !mbar_wait_warp(&sempty[b], ((n / kSBufs) & 1) ^ 1))
+          if (!mbar_wait_warp(&kvfull[s], (n / kSlots) & 1, p.budget) ||
+              !mbar_wait_warp(&sempty[b], ((n / kSBufs) & 1) ^ 1, p.budget))
             return false;
           tc_fence_after();
           if (leader) {
@@ -449,8 +453,8 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
         auto issue_o = [&](int n) -> bool {
           const bool first = n % PT == 0;
           const int s = n % kSlots, pb = n % kPBufs;
-          if (first && tok_o >= 0 && !mbar_wait_warp(oempty, tok_o & 1)) return false;
-          if (!mbar_wait_warp(&pfull[pb], (n / kPBufs) & 1)) return false;
+          if (first && tok_o >= 0 && !mbar_wait_warp(oempty, tok_o & 1, p.budget)) return false;
+          if (!mbar_wait_warp(&pfull[pb], (n / kPBufs) & 1, p.budget)) return false;
           if (first) ++tok_o;
           tc_fence_after();
           if (leader) {
@@ -509,7 +513,7 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
               ok = issue_o(n);
               o_left = false;
               t_idle = clock64();
-            } else if (__shfl_sync(0xffffffffu, clock64() - t_idle > kWaitBudgetCycles, leader_lane)) {
+            } else if (__shfl_sync(0xffffffffu, clock64() - t_idle > p.budget, leader_lane)) {
               ok = false;
             } else if (leader) {
               // nothing ready: sleep in the barrier of P(n) (or of tile
@@ -548,13 +552,17 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
 #pragma unroll
     for (int h = 0; h < 32; ++h) l[h] = 0.f;
     bool bad = false;  // a wait of this warp gave up (the group leaves together after a barrier)
+    // thread 0 of a split token's CTA, once it has told the partner that its
+    // ring may take the partner's hand-off: the partner may then be copying
+    // into this CTA, so this CTA does not leave before the copy has landed
+    bool x_armed = false;
     int jj = 0, tok = 0;
     for (int n = 0; n < count; ++n, jj = (jj + 1 == PT) ? 0 : jj + 1, tok += jj == 0) {
       const bool first = jj == 0, last = jj == PT - 1;
       const int b = n % kSBufs, pb = n % kPBufs;
       uint32_t sv[32];  // this key's logits (raw dot products) for the warp's 32 heads
       bool present = false;
-      if (!mbar_wait_warp(&mfull[n % kMaskSlots], (n / kMaskSlots) & 1)) {
+      if (!mbar_wait_warp(&mfull[n % kMaskSlots], (n / kMaskSlots) & 1, p.budget)) {
         bad = true;
       } else {
         const uint32_t mw = mask_s[(n % kMaskSlots) * 4 + (key & 3)];
@@ -564,11 +572,11 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
       // heads 32-63 from the key warps, which alone reach the S^T lanes, to
       // warps 2 and 3: fp32 [64 keys][32 heads] in its lower half, 16-byte
       // chunk c of key k's row at chunk position c ^ (k & 7)
-      if (!bad && !mbar_wait_warp(&pempty[pb], ((n / kPBufs) & 1) ^ 1)) bad = true;
+      if (!bad && !mbar_wait_warp(&pempty[pb], ((n / kPBufs) & 1) ^ 1, p.budget)) bad = true;
       uint8_t *xrow = pts + pb * 16384 + 8192 + 128 * key;
       bool over = false;  // does a present logit pass its head's reference by the lazy margin?
       if (keyw && !bad) {
-        if (!mbar_wait_warp(&sfull[b], (n / kSBufs) & 1)) {
+        if (!mbar_wait_warp(&sfull[b], (n / kSBufs) & 1, p.budget)) {
           bad = true;
         } else {
           tc_fence_after();
@@ -632,7 +640,7 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
         if (!first) {
           // O^T holds the products of tiles up to n - 1: wait for the last, then
           // scale this warp's lanes of every block, column h by factor h
-          if (!mbar_wait_warp(&pempty[(n - 1) % kPBufs], ((n - 1) / kPBufs) & 1)) {
+          if (!mbar_wait_warp(&pempty[(n - 1) % kPBufs], ((n - 1) / kPBufs) & 1, p.budget)) {
             if (lane == 0) fail();
           } else {
             tc_fence_after();
@@ -689,7 +697,7 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
       }
       if (last) {
         // ---- end of the token: O^T complete once the tile's product is done
-        if (!bad && !mbar_wait_warp(&pempty[pb], (n / kPBufs) & 1)) {
+        if (!bad && !mbar_wait_warp(&pempty[pb], (n / kPBufs) & 1, p.budget)) {
           if (lane == 0) fail();
           bad = true;
         }
@@ -700,6 +708,7 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
         if (split > 1 && tid == 0 && !bad) {
           mbar_expect_tx(xfull, kXferBytes);
           mbar_arrive_remote(xempty, rank ^ 1);
+          x_armed = true;
         }
         // the sums per head (lane l: head 32 hg + l over the warp's keys)
         red_s[32 * warp + lane] = warp_reduce_scatter32<false>(l, lane);
@@ -736,7 +745,7 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
         group_sync();  // (6) the part's (m_ref, sum) and the hand-off staged, or a failure flagged
         if (split > 1) {
           if (tid == 0) {
-            if (!aborted() && mbar_wait_cluster(xempty, 0)) {
+            if (!aborted() && mbar_wait_cluster(xempty, 0, p.budget)) {
               const uint32_t peer = static_cast<uint32_t>(rank ^ 1);
               const uint32_t bar = cluster_map(xfull, peer);
 #pragma unroll 1
@@ -748,7 +757,7 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
               fail();
             }
           }
-          if (!mbar_wait_cluster_warp(xfull, 0) && lane == 0) fail();
+          if (!mbar_wait_cluster_warp(xfull, 0, p.budget) && lane == 0) fail();
         }
         // O = (a0 O0 + a1 O1) / L against M = max(m0, m1), L = a0 l0 + a1 l1
         // (part 0 = this CTA's, part 1 = the partner's, absent for a whole token)
@@ -809,6 +818,8 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
         if (lane == 0) mbar_arrive(oempty);
       }
     }
+    // the hand-off into this CTA has landed, or (partner failed) a second has passed
+    if (x_armed && !mbar_wait_cluster(xfull, 0)) raise_flag(p.status, kFlagTimeout);
   }
 
   // a CTA whose part had no compressed tile never waited for the previous
@@ -879,6 +890,7 @@ bool attn_umma512_supported(const sa_attn_args &aa) {
 
 cudaError_t launch_sparse_mqa_umma512(const sa_index_args &ia, const sa_attn_args &aa, const int32_t *idx, int K,
                                       void *out, bool inputs_ready, uint32_t *status, cudaStream_t stream) {
+  const long long budget = attn_wait_budget();
   if (ia.T == 0) return cudaSuccess;
   Attn512Params p;
   p.B = ia.B;
@@ -894,6 +906,7 @@ cudaError_t launch_sparse_mqa_umma512(const sa_index_args &ia, const sa_attn_arg
   p.cseq = static_cast<int>(c_rows_per_seq(ia, aa));
   p.evict_first = ia.T <= ia.B ? 1 : 0;
   p.early = inputs_ready ? 1 : 0;
+  p.budget = budget > 0 ? budget : kWaitBudgetCycles;
   p.q_seq = ia.q_seq;
   p.q_pos = ia.q_pos;
   p.idx = idx;

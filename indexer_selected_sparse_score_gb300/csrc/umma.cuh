@@ -71,6 +71,22 @@ __device__ __forceinline__ bool mbar_try_wait_ns(uint64_t *bar, uint32_t parity,
   return ok != 0;
 }
 
+// Named barrier `id` over `nthreads` threads (whole warps) that returns, in
+// every participating thread, whether any of them passed true: a decision
+// that all the participating warps take alike.
+__device__ __forceinline__ bool barrier_any(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // True in exactly one lane of the (converged) warp.  Operands computed by the
 // whole warp before an elected issue stay warp-uniform.
 __device__ __forceinline__ bool elect_one() {
@@ -99,20 +115,29 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
 // About one second of SM cycles: no wait in these kernels may take longer.
 constexpr long long kWaitBudgetCycles = 2000000000ll;
 
-// Waits for the phase of `parity` to complete; false if the budget ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Waits for the phase of `parity` to complete; false if `budget` SM cycles
+// ran out first.  At the default budget a waiting thread sleeps in the
+// barrier (suspend hint); a budget far below the hint's scale is kept by
+// polling without blocking (the hint only bounds a sleep approximately).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long budget = kWaitBudgetCycles) {
+  if (budget >= 4ll * kSuspendHintNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+      if (clock64() - t0 > budget) return false;
+    return true;
+  }
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity))
-    if (clock64() - t0 > kWaitBudgetCycles) return false;
+  while (!mbar_test_wait(bar, parity))
+    if (clock64() - t0 > budget) return false;
   return true;
 }
 
 // Every lane of the warp waits; the result is the same in every lane (false
 // if any lane ran out of budget), so a warp never splits before a
 // .sync.aligned instruction.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity) {
-  const bool ok = mbar_wait(bar, parity);
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, long long budget = kWaitBudgetCycles) {
+  const bool ok = mbar_wait(bar, parity, budget);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -342,28 +367,39 @@ __device__ __forceinline__ void st_cluster_f4(uint32_t addr, float a, float b, f
 // Bounded wait with acquire at cluster scope (for phases completed by the
 // other CTA of the cluster); false if the budget ran out.  The waiting thread
 // polls (no suspend hint): these phases complete once per token.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, long long budget = kWaitBudgetCycles) {
+  const bool block = budget >= 4ll * kSuspendHintNs;  // else poll without blocking, as mbar_wait
   auto test = [&]() {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
+    if (block)
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t"
+          "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(ok)
+          : "r"(smem_u32(bar)), "r"(parity)
+          : "memory");
+    else
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t"
+          "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(ok)
+          : "r"(smem_u32(bar)), "r"(parity)
+          : "memory");
     return ok != 0;
   };
   if (test()) return true;
   const long long t0 = clock64();
   while (!test())
-    if (clock64() - t0 > kWaitBudgetCycles) return false;
+    if (clock64() - t0 > budget) return false;
   return true;
 }
 
 // mbar_wait_cluster in every lane; the result is the same in every lane.
-__device__ __forceinline__ bool mbar_wait_cluster_warp(uint64_t *bar, uint32_t parity) {
-  const bool ok = mbar_wait_cluster(bar, parity);
+__device__ __forceinline__ bool mbar_wait_cluster_warp(uint64_t *bar, uint32_t parity,
+                                                       long long budget = kWaitBudgetCycles) {
+  const bool ok = mbar_wait_cluster(bar, parity, budget);
   return __all_sync(0xffffffffu, ok);
 }
 

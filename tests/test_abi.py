@@ -290,3 +290,11 @@ def test_index_key_publish_rejects_bad_arguments(lib, kw, status):
                                   ctypes.byref(a["rope"]) if a["rope"] is not None else None, a["k_I"], a["k_scale"],
                                   a["B"], a["N_rows"], a["stride"], a["ws"], a["ws_bytes"], None)
     assert st == status
+
+
+def test_wait_budget_argument_check():
+    """sa_set_wait_budget touches no device: a negative bound is refused, 0 restores the default."""
+    lib = binding.load()
+    assert lib.sa_set_wait_budget(-5) == binding.SA_ERR_INVALID_ARG
+    assert lib.sa_set_wait_budget(1000) == binding.SA_OK
+    assert lib.sa_set_wait_budget(0) == binding.SA_OK
