@@ -109,7 +109,8 @@ STAGE_SOURCES = {"idx_score": ("idx_score.cu", "idx_score_umma.cu", "umma.cuh", 
                  "level_one": ("idx_candidates.cu", "common.cuh"),
                  "level_two": ("idx_topk.cu", "common.cuh"),
                  "index_producer": ("idx_producer.cu", "common.cuh"),
-                 "sparse_mqa": ("sparse_mqa.cu", "sparse_mqa_umma.cu", "umma.cuh", "common.cuh")}
+                 "sparse_mqa": ("sparse_mqa.cu", "sparse_mqa_umma.cu", "sparse_mqa_umma512.cu", "umma.cuh",
+                                "common.cuh")}
 
 
 def kernel_source_hash(stage):
