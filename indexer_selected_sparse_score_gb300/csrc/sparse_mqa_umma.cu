@@ -251,6 +251,9 @@ __device__ __forceinline__ void exp_store64(const uint32_t (&v)[64], const uint3
   tmem_st_16x2_x8(s_col + 56, lo);
 }
 
+// kShort: the waits between stages take the bound of sa_set_wait_budget (and
+// the copy warps vote on stopping); otherwise the default bound, a constant
+template <bool kShort>
 __global__ void __launch_bounds__(kThreads, 1)
 sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kwmap,
                        const __grid_constant__ CUtensorMap kcmap, const __grid_constant__ CUtensorMap vwmap,
@@ -276,6 +279,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
   int *abort_s = reinterpret_cast<int *>(smem + L::misc + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long budget = kShort ? p.budget : kWaitBudgetCycles;  // bound of a wait between stages
   // Work: cluster c (of G) takes whole tokens [T*c/G, T*(c+1)/G); with a
   // 2-CTA cluster, rank 0 takes tiles [0, PT0) of each and rank 1 the rest.
   const int split = p.split;
@@ -392,7 +396,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
           const int qb = qn & 1;
           bool ok = true;
           if (lane == 0) {
-            ok = mbar_wait(&qempty[qb], ((qn >> 1) & 1) ^ 1, p.budget);
+            ok = mbar_wait(&qempty[qb], ((qn >> 1) & 1) ^ 1, budget);
             if (ok) {
               // heads 16w..16w+15 -> rows 32w+16qb .. +15, both 64-column halves
               mbar_expect_tx(&qfull[qb], 2 * kH * 128);
@@ -440,13 +444,18 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
             }
           }
           const int s = n % kStages;
-          if (ok) ok = mbar_wait_warp(&ring_empty[s], ((n / kStages) & 1) ^ 1, p.budget);
+          if (ok) ok = mbar_wait_warp(&ring_empty[s], ((n / kStages) & 1) ^ 1, budget);
           if (!ok && lane == 0) fail();
-          // the warps of a ring take the same decision, so that a tile's copies
-          // are issued by all of them or by none: its barrier then completes
-          // and the drain below ends once they land
-          if (is_k ? barrier_any(3, 32 * kKWarps, !ok || aborted()) : barrier_any(1, 32 * kVWarps, !ok || aborted()))
-            break;
+          // Under a short wait bound the warps of a ring take the same
+          // decision (a reducing barrier per tile), so that a tile's copies are
+          // issued by all of them or by none: its barrier then completes and
+          // the drain below ends as soon as they land.  At the default bound
+          // (a stop is then all but impossible) each warp decides alone, and a
+          // drain may wait out its own bound.
+          const bool stop = kShort ? (is_k ? barrier_any(3, 32 * kKWarps, !ok || aborted())
+                                           : barrier_any(1, 32 * kVWarps, !ok || aborted()))
+                                   : __any_sync(0xffffffffu, !ok || aborted());
+          if (stop) break;
           if (warp == kKWarp0) {  // key mask of the tile: bit g of word e = key 4g+e exists
             uint32_t m4[4];
 #pragma unroll
@@ -513,10 +522,10 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
           if (t != prev_t_s) {
             ++qn_s;
             prev_t_s = t;
-            if (!mbar_wait_warp(&qfull[qn_s & 1], (qn_s >> 1) & 1, p.budget)) return false;
+            if (!mbar_wait_warp(&qfull[qn_s & 1], (qn_s >> 1) & 1, budget)) return false;
           }
-          if (!mbar_wait_warp(&kfull[s], (n / kStages) & 1, p.budget) ||
-              !mbar_wait_warp(&sempty[b], ((n / kSBufs) & 1) ^ 1, p.budget))
+          if (!mbar_wait_warp(&kfull[s], (n / kStages) & 1, budget) ||
+              !mbar_wait_warp(&sempty[b], ((n / kSBufs) & 1) ^ 1, budget))
             return false;
           tc_fence_after();
           const uint32_t a0 = smem_u32(qs + (qn_s & 1) * 2048), b0 = smem_u32(ks + s * 32768);
@@ -540,9 +549,9 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         auto issue_pv = [&](int n) -> bool {
           const bool first = n % PT == 0;
           const int s = n % kStages, b = n % kSBufs;
-          if (first && tok_pv >= 0 && !mbar_wait_warp(oempty, tok_pv & 1, p.budget)) return false;
-          if (!mbar_wait_warp(&pfull[b], (n / kSBufs) & 1, p.budget) ||
-              !mbar_wait_warp(&vfull[s], (n / kStages) & 1, p.budget))
+          if (first && tok_pv >= 0 && !mbar_wait_warp(oempty, tok_pv & 1, budget)) return false;
+          if (!mbar_wait_warp(&pfull[b], (n / kSBufs) & 1, budget) ||
+              !mbar_wait_warp(&vfull[s], (n / kStages) & 1, budget))
             return false;
           if (first) ++tok_pv;
           tc_fence_after();
@@ -594,8 +603,8 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         l = 0.f;
       }
       const int b = n % kSBufs;
-      if (!(mbar_wait_warp(&mfull[n % kMaskSlots], (n / kMaskSlots) & 1, p.budget) &&
-            mbar_wait_warp(&sfull[b], (n / kSBufs) & 1, p.budget))) {
+      if (!(mbar_wait_warp(&mfull[n % kMaskSlots], (n / kMaskSlots) & 1, budget) &&
+            mbar_wait_warp(&sfull[b], (n / kSBufs) & 1, budget))) {
         if (lane == 0) fail();
         break;
       }
@@ -630,7 +639,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         // O holds P.V of tiles up to n-1: wait for P.V(n-1), then scale this
         // warp's rows (factor 1 for heads that keep their reference)
         const int pn = n - 1;
-        if (!mbar_wait_warp(&sempty[pn % kSBufs], (pn / kSBufs) & 1, p.budget)) {
+        if (!mbar_wait_warp(&sempty[pn % kSBufs], (pn / kSBufs) & 1, budget)) {
           if (lane == 0) fail();
           break;
         }
@@ -662,7 +671,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
 
       if (last) {
         // O is complete once P.V(n) is done
-        if (!mbar_wait_warp(&sempty[b], (n / kSBufs) & 1, p.budget)) {
+        if (!mbar_wait_warp(&sempty[b], (n / kSBufs) & 1, budget)) {
           if (lane == 0) fail();
           break;
         }
@@ -674,7 +683,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
           // it is free, laid out by softmax thread (the same thread of rank 0
           // reads them): O chunk q (4 columns) of thread i at 16 (128 q + i),
           // so a warp's store covers 512 contiguous bytes; (m, l) at 32 KB + 8 i
-          if (!mbar_wait_cluster_warp(xempty, 0, p.budget)) {
+          if (!mbar_wait_cluster_warp(xempty, 0, budget)) {
             if (lane == 0) fail();
             break;
           }
@@ -705,7 +714,7 @@ sparse_mqa_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
           float m1 = -INFINITY, l1 = 0.f;
           const float4 *xo = reinterpret_cast<const float4 *>(ks) + tid;  // chunk q at xo[128 q]
           if (split > 1) {
-            if (!mbar_wait_cluster_warp(xfull, 0, p.budget)) {
+            if (!mbar_wait_cluster_warp(xfull, 0, budget)) {
               if (lane == 0) fail();
               break;
             }
@@ -813,7 +822,7 @@ int max_pair_clusters() {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, sparse_mqa_umma_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, sparse_mqa_umma_kernel<false>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
@@ -871,24 +880,31 @@ cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &
       !encode_rows(&vcmap, aa.Vc, static_cast<uint64_t>(ia.B - 1) * p.cseq + ia.N_c, 1))
     return cudaErrorInvalidValue;
   const size_t smem = attn_smem_bytes();
+  const long long budget = attn_wait_budget();
+  const bool short_budget = budget > 0 && budget < kWaitBudgetCycles;
+  auto kern = short_budget ? sparse_mqa_umma_kernel<true> : sparse_mqa_umma_kernel<false>;
   // the register split above assumes the kernel launches with kLaunchRegs
   // registers per thread; anything else could leave a raise waiting forever
-  static int regs = -1;
-  if (regs < 0) {
+  static int regs[2] = {-1, -1};
+  if (regs[short_budget] < 0) {
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void *>(sparse_mqa_umma_kernel));
+    cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void *>(kern));
     if (e != cudaSuccess) return e;
-    regs = fa.numRegs;
+    regs[short_budget] = fa.numRegs;
   }
-  if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  static bool attr_done[64] = {};
-  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(sparse_mqa_umma_kernel), smem, attr_done);
+  if (regs[short_budget] != kLaunchRegs) return cudaErrorInvalidConfiguration;
+  static bool attr_done[2][64] = {};
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), smem, attr_done[short_budget]);
   if (e != cudaSuccess) return e;
+  if (short_budget) {  // the occupancy query of attn_split runs on the default kernel
+    static bool attr_done_default[64] = {};
+    e = set_smem_once(reinterpret_cast<const void *>(sparse_mqa_umma_kernel<false>), smem, attr_done_default);
+    if (e != cudaSuccess) return e;
+  }
   p.split = attn_split(ia, p.TPT);
   p.evict_first = ia.T <= ia.B ? 1 : 0;
   p.early = inputs_ready ? 1 : 0;
-  const long long budget = attn_wait_budget();
-  p.budget = budget > 0 ? budget : kWaitBudgetCycles;
+  p.budget = short_budget ? budget : kWaitBudgetCycles;
   p.PT0 = (p.TPT + 1) / 2;  // rank 0 takes the larger half (window included); rank 1's hand-off costs about its merge
   const int sms = sm_count();
   // whole tokens (at most one CTA per SM), or one cluster pair per token
@@ -896,8 +912,7 @@ cudaError_t launch_sparse_mqa_umma(const sa_index_args &ia, const sa_attn_args &
   // a programmatic dependent launch: CTAs that find a free SM set up (barriers,
   // tensor memory) while the top-k kernel finishes, and wait for it before
   // reading the indices
-  return launch_ex(true, sparse_mqa_umma_kernel, dim3(grid), dim3(kThreads), smem, stream, p.split, qmap, kwmap, kcmap,
-                    vwmap, vcmap, p);
+  return launch_ex(true, kern, dim3(grid), dim3(kThreads), smem, stream, p.split, qmap, kwmap, kcmap, vwmap, vcmap, p);
 }
 
 }  // namespace sa

@@ -175,6 +175,9 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane)
 // Named barrier of the softmax warpgroup (warps 0-3).
 __device__ __forceinline__ void group_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
+// kShort: the waits between stages take the bound of sa_set_wait_budget (and
+// the copy warps vote on stopping); otherwise the default bound, a constant
+template <bool kShort>
 __global__ void __launch_bounds__(kThreads, 1)
 sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
                           const __grid_constant__ CUtensorMap cmap, const Attn512Params p) {
@@ -210,6 +213,7 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
   uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem + L::misc);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long budget = kShort ? p.budget : kWaitBudgetCycles;  // bound of a wait between stages
   // cluster c (of G) takes tokens [T c / G, T (c + 1) / G); with a 2-CTA
   // cluster (one token each), rank 0 takes tiles [0, PT0) and rank 1 the rest
   const int split = p.split;
@@ -312,7 +316,7 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
           if (warp != kCopyWarp0) return true;
           bool ok = true;
           if (lane == 0) {
-            ok = mbar_wait(qempty, (qn & 1) ^ 1, p.budget);
+            ok = mbar_wait(qempty, (qn & 1) ^ 1, budget);
             if (ok) {
               mbar_expect_tx(qfull, kH * kD * 2);
 #pragma unroll
@@ -355,12 +359,17 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
             }
           }
           const int s = n % kSlots;
-          if (ok) ok = mbar_wait_warp(&kvempty[s], ((n / kSlots) & 1) ^ 1, p.budget);
+          if (ok) ok = mbar_wait_warp(&kvempty[s], ((n / kSlots) & 1) ^ 1, budget);
           if (!ok && lane == 0) fail();
-          // every copy warp takes the same decision, so that a tile's copies are
-          // issued by all of them or by none: its barrier then completes and
-          // the drain below ends once they land
-          if (barrier_any(1, 32 * kCopyWarps, !ok || aborted())) break;
+          // Under a short wait bound every copy warp takes the same decision (a
+          // reducing barrier per tile), so that a tile's copies are issued by
+          // all of them or by none: its barrier then completes and the drain
+          // below ends as soon as they land.  At the default bound (a stop is
+          // then all but impossible) each warp decides alone, and a drain may
+          // wait out its own bound.
+          const bool stop = kShort ? barrier_any(1, 32 * kCopyWarps, !ok || aborted())
+                                   : __any_sync(0xffffffffu, !ok || aborted());
+          if (stop) break;
           if (warp == kCopyWarp0) {  // key mask: bit g of word e = key 4g+e exists
             uint32_t m4[4];
 #pragma unroll
@@ -427,10 +436,10 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
           if (t != prev_t_s) {
             ++tok_s;
             prev_t_s = t;
-            if (!mbar_wait_warp(qfull, tok_s & 1, p.budget)) return false;
+            if (!mbar_wait_warp(qfull, tok_s & 1, budget)) return false;
           }
-          if (!mbar_wait_warp(&kvfull[s], (n / kSlots) & 1, p.budget) ||
-              !mbar_wait_warp(&sempty[b], ((n / kSBufs) & 1) ^ 1, p.budget))
+          if (!mbar_wait_warp(&kvfull[s], (n / kSlots) & 1, budget) ||
+              !mbar_wait_warp(&sempty[b], ((n / kSBufs) & 1) ^ 1, budget))
             return false;
           tc_fence_after();
           if (leader) {
@@ -453,8 +462,8 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
         auto issue_o = [&](int n) -> bool {
           const bool first = n % PT == 0;
           const int s = n % kSlots, pb = n % kPBufs;
-          if (first && tok_o >= 0 && !mbar_wait_warp(oempty, tok_o & 1, p.budget)) return false;
-          if (!mbar_wait_warp(&pfull[pb], (n / kPBufs) & 1, p.budget)) return false;
+          if (first && tok_o >= 0 && !mbar_wait_warp(oempty, tok_o & 1, budget)) return false;
+          if (!mbar_wait_warp(&pfull[pb], (n / kPBufs) & 1, budget)) return false;
           if (first) ++tok_o;
           tc_fence_after();
           if (leader) {
@@ -513,7 +522,7 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
               ok = issue_o(n);
               o_left = false;
               t_idle = clock64();
-            } else if (__shfl_sync(0xffffffffu, clock64() - t_idle > p.budget, leader_lane)) {
+            } else if (__shfl_sync(0xffffffffu, clock64() - t_idle > budget, leader_lane)) {
               ok = false;
             } else if (leader) {
               // nothing ready: sleep in the barrier of P(n) (or of tile
@@ -562,7 +571,7 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
       const int b = n % kSBufs, pb = n % kPBufs;
       uint32_t sv[32];  // this key's logits (raw dot products) for the warp's 32 heads
       bool present = false;
-      if (!mbar_wait_warp(&mfull[n % kMaskSlots], (n / kMaskSlots) & 1, p.budget)) {
+      if (!mbar_wait_warp(&mfull[n % kMaskSlots], (n / kMaskSlots) & 1, budget)) {
         bad = true;
       } else {
         const uint32_t mw = mask_s[(n % kMaskSlots) * 4 + (key & 3)];
@@ -572,11 +581,11 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
       // heads 32-63 from the key warps, which alone reach the S^T lanes, to
       // warps 2 and 3: fp32 [64 keys][32 heads] in its lower half, 16-byte
       // chunk c of key k's row at chunk position c ^ (k & 7)
-      if (!bad && !mbar_wait_warp(&pempty[pb], ((n / kPBufs) & 1) ^ 1, p.budget)) bad = true;
+      if (!bad && !mbar_wait_warp(&pempty[pb], ((n / kPBufs) & 1) ^ 1, budget)) bad = true;
       uint8_t *xrow = pts + pb * 16384 + 8192 + 128 * key;
       bool over = false;  // does a present logit pass its head's reference by the lazy margin?
       if (keyw && !bad) {
-        if (!mbar_wait_warp(&sfull[b], (n / kSBufs) & 1, p.budget)) {
+        if (!mbar_wait_warp(&sfull[b], (n / kSBufs) & 1, budget)) {
           bad = true;
         } else {
           tc_fence_after();
@@ -640,7 +649,7 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
         if (!first) {
           // O^T holds the products of tiles up to n - 1: wait for the last, then
           // scale this warp's lanes of every block, column h by factor h
-          if (!mbar_wait_warp(&pempty[(n - 1) % kPBufs], ((n - 1) / kPBufs) & 1, p.budget)) {
+          if (!mbar_wait_warp(&pempty[(n - 1) % kPBufs], ((n - 1) / kPBufs) & 1, budget)) {
             if (lane == 0) fail();
           } else {
             tc_fence_after();
@@ -697,7 +706,7 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
       }
       if (last) {
         // ---- end of the token: O^T complete once the tile's product is done
-        if (!bad && !mbar_wait_warp(&pempty[pb], (n / kPBufs) & 1, p.budget)) {
+        if (!bad && !mbar_wait_warp(&pempty[pb], (n / kPBufs) & 1, budget)) {
           if (lane == 0) fail();
           bad = true;
         }
@@ -745,7 +754,7 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
         group_sync();  // (6) the part's (m_ref, sum) and the hand-off staged, or a failure flagged
         if (split > 1) {
           if (tid == 0) {
-            if (!aborted() && mbar_wait_cluster(xempty, 0, p.budget)) {
+            if (!aborted() && mbar_wait_cluster(xempty, 0, budget)) {
               const uint32_t peer = static_cast<uint32_t>(rank ^ 1);
               const uint32_t bar = cluster_map(xfull, peer);
 #pragma unroll 1
@@ -757,7 +766,7 @@ sparse_mqa_umma512_kernel(const __grid_constant__ CUtensorMap qmap, const __grid
               fail();
             }
           }
-          if (!mbar_wait_cluster_warp(xfull, 0, p.budget) && lane == 0) fail();
+          if (!mbar_wait_cluster_warp(xfull, 0, budget) && lane == 0) fail();
         }
         // O = (a0 O0 + a1 O1) / L against M = max(m0, m1), L = a0 l0 + a1 l1
         // (part 0 = this CTA's, part 1 = the partner's, absent for a whole token)
@@ -872,7 +881,7 @@ int max_pair_clusters512() {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, sparse_mqa_umma512_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, sparse_mqa_umma512_kernel<false>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
@@ -906,7 +915,9 @@ cudaError_t launch_sparse_mqa_umma512(const sa_index_args &ia, const sa_attn_arg
   p.cseq = static_cast<int>(c_rows_per_seq(ia, aa));
   p.evict_first = ia.T <= ia.B ? 1 : 0;
   p.early = inputs_ready ? 1 : 0;
-  p.budget = budget > 0 ? budget : kWaitBudgetCycles;
+  const bool short_budget = budget > 0 && budget < kWaitBudgetCycles;
+  auto kern = short_budget ? sparse_mqa_umma512_kernel<true> : sparse_mqa_umma512_kernel<false>;
+  p.budget = short_budget ? budget : kWaitBudgetCycles;
   p.q_seq = ia.q_seq;
   p.q_pos = ia.q_pos;
   p.idx = idx;
@@ -921,26 +932,30 @@ cudaError_t launch_sparse_mqa_umma512(const sa_index_args &ia, const sa_attn_arg
     return cudaErrorInvalidValue;
   // the register split assumes kLaunchRegs registers per thread at launch;
   // anything else could leave a raise waiting forever
-  static int regs = -1;
-  if (regs < 0) {
+  static int regs[2] = {-1, -1};
+  if (regs[short_budget] < 0) {
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void *>(sparse_mqa_umma512_kernel));
+    cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void *>(kern));
     if (e != cudaSuccess) return e;
-    regs = fa.numRegs;
+    regs[short_budget] = fa.numRegs;
   }
-  if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+  if (regs[short_budget] != kLaunchRegs) return cudaErrorInvalidConfiguration;
   const size_t smem = attn512_smem_bytes();
-  static bool attr_done[64] = {};
-  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(sparse_mqa_umma512_kernel), smem, attr_done);
+  static bool attr_done[2][64] = {};
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), smem, attr_done[short_budget]);
   if (e != cudaSuccess) return e;
+  if (short_budget) {  // the occupancy query below runs on the default kernel
+    static bool attr_done_default[64] = {};
+    e = set_smem_once(reinterpret_cast<const void *>(sparse_mqa_umma512_kernel<false>), smem, attr_done_default);
+    if (e != cudaSuccess) return e;
+  }
   // a 2-CTA cluster per token when every token can have one at once (each CTA
   // half of the token's tiles), else whole tokens with at most one CTA per SM
   p.split = (p.TPT >= 2 && ia.T <= max_pair_clusters512()) ? 2 : 1;
   p.PT0 = (p.TPT + 1) / 2;  // rank 0 takes the larger half (window first); rank 1's hand-off costs about the merge
   const int sms = sm_count();
   const int grid = p.split == 1 ? (ia.T < sms ? ia.T : sms) : 2 * ia.T;
-  return launch_ex(true, sparse_mqa_umma512_kernel, dim3(grid), dim3(kThreads), smem, stream, p.split, qmap, wmap,
-                   cmap, p);
+  return launch_ex(true, kern, dim3(grid), dim3(kThreads), smem, stream, p.split, qmap, wmap, cmap, p);
 }
 
 }  // namespace sa
