@@ -176,6 +176,34 @@ idx_qprep_kernel(int B, int T, int N_c, int r, const int32_t *__restrict__ q_seq
     // CTAs, which start early and fill the SMs' shared memory)
     __shared__ int warp_sums[32];
     if (threadIdx.x == 0) *pool = 0;  // no pool chunk handed out yet
+    if (T <= 4 * kPrepThreads) {
+      // up to four tokens per thread, in order: the counts stay in registers
+      // (one round trip for the inputs, one block scan)
+      const int base = 4 * static_cast<int>(threadIdx.x);
+      int sq[4], ps[4], cnt[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int tt = min(base + k, T - 1);
+        sq[k] = q_seq[tt];
+        ps[k] = q_pos[tt];
+      }
+      int sum = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        cnt[k] = base + k < T ? tiles_of(B, N_c, r, sq[k], ps[k]) : 0;
+        sum += cnt[k];
+      }
+      const int incl = plan_block_scan(sum, warp_sums);
+      int run = incl - sum;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (base + k < T) {
+          prefix[base + k] = run;
+          run += cnt[k];
+        }
+      if (threadIdx.x == kPrepThreads - 1) prefix[T] = incl;
+      return;
+    }
     int *cnt_s = prefix;  // tile counts, then their prefix, staged in global memory
     // (a) tile count of every token, one token per thread, coalesced, four loads in flight
     for (int t0 = threadIdx.x; t0 < T; t0 += 4 * kPrepThreads) {
@@ -852,6 +880,21 @@ cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld,
   constexpr int P = QFP8 ? 1 : 2;
   using L = ScoreSmem<NH, P>;
   const int grid = sm_count() * kCtasPerSm<NH>;
+  // The prep kernel takes the largest shared-memory carveout, as the main
+  // kernel does: an SM holding a prep CTA configured for less shared memory
+  // could not take a main-kernel CTA until the prep CTA had left, and the main
+  // kernel's CTAs start while the prep kernel runs.
+  {
+    static bool carveout_done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64 && !carveout_done[dev]) {
+      cudaError_t ce = cudaFuncSetAttribute(reinterpret_cast<const void *>(idx_qprep_kernel<NH, QFP8>),
+                                            cudaFuncAttributePreferredSharedMemoryCarveout,
+                                            cudaSharedmemCarveoutMaxShared);
+      if (ce != cudaSuccess) return ce;
+      carveout_done[dev] = true;
+    }
+  }
   idx_qprep_kernel<NH, QFP8><<<ia.T + 1, kPrepThreads, 0, stream>>>(
       ia.B, ia.T, ia.N_c, ia.r, ia.q_seq, ia.q_pos, ia.q_I, ia.q_scale, ia.w, qpack, wq, scores, ld,
       write_masked ? 1 : 0, prefix, pool, status);
