@@ -925,7 +925,7 @@ cudaError_t launch_umma_impl(const sa_index_args &ia, float *scores, int64_t ld,
   e = set_smem_once(reinterpret_cast<const void *>(kern), smem, attr_done);
   if (e != cudaSuccess) return e;
   // the prep kernel is short: overlapping this kernel's launch and set-up
-  // with it pays (the top-k kernel, which needs whole SMs, starts normally)
+  // with it pays
   return launch_ex(true, kern, dim3(grid), dim3(kMainThreads), smem, stream, 1, kmap, sp);
 }
 

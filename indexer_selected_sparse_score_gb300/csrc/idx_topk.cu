@@ -471,16 +471,19 @@ RegKern pick_reg_kernel(int N_c, bool many_rows) {
 
 cudaError_t launch_topk(const float *scores, int64_t ld, const sa_index_args &ia, int K,
                         int32_t *idx, uint32_t *status, cudaStream_t stream, const uint32_t *cand,
-                        int cand_words, int block_size) {
+                        int cand_words, int block_size, bool programmatic) {
   if (ia.T == 0 || K == 0) return cudaSuccess;
   const FastDiv dbs = make_fastdiv(static_cast<uint32_t>(block_size));
   // a row holds at most N_c visible scores
   if (ia.N_c > kRegMax)
-    return launch_ex(false, topk_radix_kernel, dim3(ia.T), dim3(kTopkThreads), 0, stream, 1, scores, ld, ia.B, ia.N_c,
-                     ia.r, ia.q_seq, ia.q_pos, K, idx, status, cand, cand_words, dbs);
+    return launch_ex(programmatic, topk_radix_kernel, dim3(ia.T), dim3(kTopkThreads), 0, stream, 1, scores, ld, ia.B,
+                     ia.N_c, ia.r, ia.q_seq, ia.q_pos, K, idx, status, cand, cand_words, dbs);
   const bool many_rows = ia.T > 2 * sm_count();
   const RegKern kern = cand ? pick_reg_kernel<true>(ia.N_c, many_rows) : pick_reg_kernel<false>(ia.N_c, many_rows);
-  return launch_ex(false, kern, dim3(ia.T), dim3(many_rows ? 512 : 1024), 0, stream, 1, scores, ld, ia.B, ia.N_c, ia.r,
+  // programmatic (after the scoring kernel of the fused step): the CTAs take
+  // SMs as the scoring kernel's CTAs finish (they all started before any of
+  // these can) and wait for it before reading the scores
+  return launch_ex(programmatic, kern, dim3(ia.T), dim3(many_rows ? 512 : 1024), 0, stream, 1, scores, ld, ia.B, ia.N_c, ia.r,
                    ia.q_seq, ia.q_pos, K, idx, status, cand, cand_words, dbs);
 }
 

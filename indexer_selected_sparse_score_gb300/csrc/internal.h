@@ -48,9 +48,13 @@ cudaError_t launch_idx_score_umma(const sa_index_args &ia, float *scores, int64_
 
 // Per-query top-k.  With `cand` ([T, cand_words] block mask, blocks of
 // block_size positions) the positions outside kept blocks count as -inf.
+// `programmatic`: the previous kernel on the stream is one this library
+// launched that writes no token array (the kernel reads those before it waits
+// for the previous kernel), so the launch may overlap its end.
 cudaError_t launch_topk(const float *scores, int64_t ld, const sa_index_args &ia, int K,
                         int32_t *idx, uint32_t *status, cudaStream_t stream,
-                        const uint32_t *cand = nullptr, int cand_words = 0, int block_size = 1);
+                        const uint32_t *cand = nullptr, int cand_words = 0, int block_size = 1,
+                        bool programmatic = false);
 
 // Level one of the two-level top-k: per token, the block mask of the kept
 // candidate blocks ([T, candidate_words(N_c, block_size)] uint32).
@@ -80,9 +84,11 @@ cudaError_t launch_candidate_blocks(const float *scores, int64_t ld, const sa_in
 // Attention + combine.  The tensor-core kernel (64 heads of dim 128) uses
 // `attn_scratch` (attn_umma_scratch bytes); the CUDA-core kernel uses the
 // split partials part_m/part_l/part_o laid out by `plan`.  `inputs_ready`:
-// the previous kernel on the stream is an ordinary (not programmatic) launch
-// made after every input but idx was written, so the tensor-core kernels may
-// read those inputs before waiting for it.
+// the chain of programmatic launches this one ends began with an ordinary
+// launch made after every input but idx was written (each kernel of the chain
+// starts only after every CTA of its predecessor has started), so the
+// tensor-core kernels may read those inputs before waiting for the previous
+// kernel.
 cudaError_t launch_sparse_mqa(const sa_index_args &ia, const sa_attn_args &aa, const int32_t *idx,
                               int K, void *out, float *part_m, float *part_l, float *part_o,
                               void *attn_scratch, const SplitPlan &plan, bool inputs_ready, uint32_t *status,

@@ -194,10 +194,10 @@ sa_status fused_with_scratch(const sa_index_args *ia, const sa_attn_args *aa, in
   cudaError_t e =
       launch_idx_score(*ia, scores, ia->N_c, false, at<void>(scratch, L.score_scratch), status, st);
   if (e != cudaSuccess) return cuda_fail(e, "index score launch");
-  e = launch_topk(scores, ia->N_c, *ia, K, idx, status, st);
+  e = launch_topk(scores, ia->N_c, *ia, K, idx, status, st, nullptr, 0, 1, true);
   if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
   const SplitPlan plan = plan_splits(ia->T, aa->W, K);
-  // the top-k launch is an ordinary one, made after every input was written
+  // the chain began with an ordinary launch made after every input was written
   e = launch_sparse_mqa(*ia, *aa, idx, K, out, at<float>(scratch, L.part_m),
                         at<float>(scratch, L.part_l), at<float>(scratch, L.part_o),
                         at<void>(scratch, L.attn_scratch), plan, true, status, st);
@@ -428,7 +428,7 @@ static sa_status fused_impl(const sa_index_args *ia, const sa_attn_args *aa, int
     e = sa::launch_idx_score(*ia, scores, ia->N_c, false, at<void>(ws, L.score_scratch), status, st);
   if (e != cudaSuccess) return cuda_fail(e, "index score launch");
   e = mark(1);
-  if (e == cudaSuccess) e = sa::launch_topk(scores, ia->N_c, *ia, K, idx, status, st);
+  if (e == cudaSuccess) e = sa::launch_topk(scores, ia->N_c, *ia, K, idx, status, st, nullptr, 0, 1, !ev);
   if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
   const sa::SplitPlan plan = sa::plan_splits(ia->T, aa->W, K);
   e = mark(2);

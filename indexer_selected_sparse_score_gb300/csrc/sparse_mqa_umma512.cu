@@ -952,7 +952,9 @@ cudaError_t launch_sparse_mqa_umma512(const sa_index_args &ia, const sa_attn_arg
   // a 2-CTA cluster per token when every token can have one at once (each CTA
   // half of the token's tiles), else whole tokens with at most one CTA per SM
   p.split = (p.TPT >= 2 && ia.T <= max_pair_clusters512()) ? 2 : 1;
-  p.PT0 = (p.TPT + 1) / 2;  // rank 0 takes the larger half (window first); rank 1's hand-off costs about the merge
+  // rank 0 takes the larger half, window first (in the fused step its rows
+  // load before the wait for the indices)
+  p.PT0 = (p.TPT + 1) / 2;
   const int sms = sm_count();
   const int grid = p.split == 1 ? (ia.T < sms ? ia.T : sms) : 2 * ia.T;
   return launch_ex(true, kern, dim3(grid), dim3(kThreads), smem, stream, p.split, qmap, wmap, cmap, p);
