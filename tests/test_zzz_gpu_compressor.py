@@ -169,6 +169,35 @@ def test_index_key_publish_codes_exact():
     assert np.array_equal(kI.cpu().numpy(), gc)
 
 
+def test_index_key_publish_codes_exact_long_positions():
+    """4096 rows at positions up to 131068 (angles of up to ~1.3e5 radians for
+    the fastest pair, where the argument reduction of the rotation matters):
+    codes and scales equal the oracle's bit for bit."""
+    ensure_built()
+    rng = np.random.default_rng(29)
+    B, N_rows, n, r = 1, 32768, 4096, 4
+    rope = oracle.Rope()
+    seq = np.zeros(n, dtype=np.int32)
+    grp = rng.choice(N_rows, size=n, replace=False).astype(np.int32)
+    x = _bf16_bits(rng.normal(size=(n, 128)) * rng.choice([1e-2, 1.0, 7.0], size=(n, 1)))
+    w = rng.uniform(0.5, 2.0, size=128).astype(np.float32)
+    eps = float(np.float32(1e-6))
+    kI = torch.zeros((B, N_rows, 128), dtype=torch.uint8, device="cuda")
+    ks = torch.zeros((B, N_rows), dtype=torch.float32, device="cuda")
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    binding.sa_workspace_init(ws)
+    ra = binding.RopeArgs(rope.dim, rope.base, rope.factor, rope.original_seq_len, rope.beta_fast, rope.beta_slow)
+    binding.sa_index_key_publish(torch.from_numpy(x.view(np.int16)).cuda(), n, torch.from_numpy(seq).cuda(),
+                                 torch.from_numpy(grp).cuda(), r, torch.from_numpy(w).cuda(), eps, ra, kI, ks, B,
+                                 N_rows, ws)
+    assert binding.sa_check_device_status(ws) == binding.SA_OK
+    gc, gs = kI.cpu().numpy(), ks.cpu().numpy()
+    for i in range(n):
+        codes, scale, _ = oracle.index_key(x[i], w, eps, int(grp[i]) * r, rope)
+        assert np.array_equal(gc[0, grp[i]], codes), i
+        assert np.float32(gs[0, grp[i]]).view(np.uint32) == np.float32(scale).view(np.uint32), i
+
+
 def test_compressed_keys_feed_the_scorer():
     """The f3 path end to end on the GPU: compressor prefill of one sequence,
     the caller's key projection (a random bf16 matrix here), the key publisher
