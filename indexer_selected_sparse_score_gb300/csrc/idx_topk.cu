@@ -149,17 +149,21 @@ topk_radix_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, 
 }
 
 // ---------------------------------------------------------------------------
-// Register-resident variant for rows of up to kRegMax scores: thread i holds
-// positions 4096 q + 4 i + j (j < 4) for q < E / 4, so the row's loads depend
-// only on N_c and go out at once (before the token's visible count is known),
-// and any row length spreads evenly over the threads.  The keys are first
-// reduced to their range (key - min, an order-preserving shift), so the radix
-// digits cover only the L = bit length of (max - min) bits the row actually
-// uses: the first pass spreads the row over its bins (plain shared atomics,
-// little contention) and a bin of at most kFinish keys is ranked directly.
-// The picks go into two position bitmaps in shared memory (above the k-th key,
-// equal to it); one block scan over 32-position words then writes them in
-// ascending order, the equal ones lowest position first.
+// Register-resident variant for rows of up to kRegMax scores: slot e of
+// thread i holds position NT e + i, so the row's loads depend only on N_c and
+// go out at once (before the token's visible count is known), any row length
+// spreads evenly over the threads, and slot e of a warp covers 32 consecutive
+// positions: one word of a position bitmap, formed by one ballot.  The keys are
+// first reduced to their range (key - min, an order-preserving shift), so the
+// radix digits cover only the L = bit length of (max - min) bits the row
+// actually uses: the first pass spreads the row over its bins (plain shared
+// atomics, little contention) and a bin of at most kFinish keys is ranked
+// directly.  Slots past the visible count hold key 0, the smallest: with more
+// than K visible keys they change neither the k-th largest value nor, as they
+// sit at the highest positions, which of the keys equal to it are taken, so no
+// pass tests them.  The picks go into two position bitmaps in shared memory
+// (above the k-th key, equal to it); one block scan over the words then writes
+// them in ascending order, the equal ones lowest position first.
 
 constexpr int kRegMax = 32768;
 constexpr int kDigitBits = 11;                 // radix digit width
@@ -167,15 +171,8 @@ constexpr int kDigitBins = 1 << kDigitBits;
 constexpr int kFinish = 256;                   // a bin this small is ranked directly
 // The register top-k runs with NT threads: 1024 when each SM holds about one
 // row (one row's latency is the step's), 512 when rows outnumber the SMs (two
-// CTAs per SM keep more rows in flight).  Per NT: keys per thread at most,
-// positions one chunk q of all threads covers, bitmap words per thread.
-template <int NT>
-struct RegShape {
-  static constexpr int kWarps = NT / 32;
-  static constexpr int kE = kRegMax / NT;
-  static constexpr int kChunkSpan = 4 * NT;
-  static constexpr int kSelWords = kRegMax / 32 / NT;
-};
+// CTAs per SM keep more rows in flight); E keys per thread cover E * NT
+// positions.
 
 // Block-wide exclusive scan of one uint32 per thread; returns the prefix and
 // writes the total to *total.
@@ -207,24 +204,43 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_s
   return r;
 }
 
+// Shared state of one register top-k CTA.
+struct RegSel {
+  uint32_t warp_sums[33];
+  uint32_t digit, above, count;    // the pass's chosen bin
+  uint32_t ncand, fin_above;
+  uint32_t cand[kFinish];          // the last bin's keys and positions
+  int32_t cpos[kFinish];
+};
+
 // One radix pass: histogram of digit (key >> shift) & (nbins-1) over the keys
 // that match `prefix` under `mask`, then locate the bin holding the
 // `remaining`-th largest.  Returns the digit; `remaining` becomes the rank
-// within that bin.
-template <int E, int NT>
-__device__ __forceinline__ uint32_t radix_pass(const uint32_t (&key)[E], int cnt, uint32_t prefix, uint32_t mask,
-                                               int shift, int nbins, uint32_t *hist, uint32_t *warp_sums,
-                                               int &remaining, uint32_t &in_bin) {
-  constexpr int R = kDigitBins / NT;  // ranks (bins) per thread in the scan
-  const int tid = threadIdx.x;
-  for (int i = tid; i < nbins; i += NT) hist[i] = 0;
-  __syncthreads();
+// within that bin.  kFirst: the first pass, whose keys all match (they are
+// below 2^L and shift + log2(nbins) = L) and whose histogram was zeroed before
+// the block's first barrier.  Each warp sums its threads' bins; every warp then
+// finds, from the warp totals, the warp whose bins hold the rank, and that
+// warp alone locates the bin.
+template <int E, int NT, bool kFirst>
+__device__ __forceinline__ uint32_t radix_pass(const uint32_t (&key)[E], uint32_t prefix, uint32_t mask, int shift,
+                                               int nbins, uint32_t *hist, RegSel &rs, int &remaining,
+                                               uint32_t &in_bin) {
+  constexpr int R = kDigitBins / NT;  // ranks (bins) per thread
+  constexpr int kWarps = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if constexpr (!kFirst) {
+    for (int i = tid; i < nbins; i += NT) hist[i] = 0;
+    __syncthreads();
+  }
 #pragma unroll
-  for (int e = 0; e < E; ++e)
-    if (e < cnt && (key[e] & mask) == prefix)
+  for (int e = 0; e < E; ++e) {
+    if constexpr (kFirst)
+      atomicAdd(&hist[key[e] >> shift], 1u);
+    else if ((key[e] & mask) == prefix)
       atomicAdd(&hist[(key[e] >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
+  }
   __syncthreads();
-  // bins in descending order: thread t owns ranks r = R t .. R t + R - 1 (bin = nbins-1-r)
+  // bins in descending order: thread t owns ranks R t .. R t + R - 1 (bin nbins-1-rank)
   uint32_t c[R], sum = 0;
 #pragma unroll
   for (int k = 0; k < R; ++k) {
@@ -232,42 +248,67 @@ __device__ __forceinline__ uint32_t radix_pass(const uint32_t (&key)[E], int cnt
     c[k] = rk < nbins ? hist[nbins - 1 - rk] : 0u;
     sum += c[k];
   }
-  uint32_t total;
-  const uint32_t before = block_excl_scan(sum, warp_sums, &total);
-  __shared__ uint32_t sel_digit, sel_above, sel_count;
+  const uint32_t wsum = __reduce_add_sync(0xffffffffu, sum);
+  if (lane == 0) rs.warp_sums[warp] = wsum;
+  __syncthreads();
   const uint32_t rem = static_cast<uint32_t>(remaining);
-  if (before < rem && rem <= before + sum) {
-    uint32_t run = before;
+  const uint32_t wv = lane < kWarps ? rs.warp_sums[lane] : 0u;
+  uint32_t wincl = wv;
 #pragma unroll
-    for (int k = 0; k < R; ++k) {
-      if (run < rem && rem <= run + c[k]) {
-        sel_digit = nbins - 1 - (R * tid + k);
-        sel_above = run;
-        sel_count = c[k];
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, wincl, o);
+    if (lane >= o) wincl += y;
+  }
+  // the ranks above `rem` exist (rem <= the keys counted), so some warp reaches it
+  const int sw = __ffs(__ballot_sync(0xffffffffu, wincl >= rem)) - 1;
+  if (warp == sw) {
+    const uint32_t before = __shfl_sync(0xffffffffu, wincl - wv, sw);
+    uint32_t li = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, li, o);
+      if (lane >= o) li += y;
+    }
+    if (lane == __ffs(__ballot_sync(0xffffffffu, before + li >= rem)) - 1) {
+      uint32_t run = before + li - sum;
+#pragma unroll
+      for (int k = 0; k < R; ++k) {
+        if (run < rem && rem <= run + c[k]) {
+          rs.digit = static_cast<uint32_t>(nbins - 1 - (R * tid + k));
+          rs.above = run;
+          rs.count = c[k];
+        }
+        run += c[k];
       }
-      run += c[k];
     }
   }
   __syncthreads();
-  remaining -= static_cast<int>(sel_above);
-  const uint32_t d = sel_digit;
-  in_bin = sel_count;
-  __syncthreads();
-  return d;
+  // rs is rewritten only after the next pass's first barrier, which every
+  // thread reaches after these reads
+  remaining -= static_cast<int>(rs.above);
+  in_bin = rs.count;
+  return rs.digit;
 }
 
+// Resident CTAs per SM the register budget is set for: two at 512 threads
+// (while E keys fit in half the register file), else one.
+template <int E, int NT>
+constexpr int kRegCtasPerSm = (NT <= 512 && E <= 32) ? 2 : 1;
+
 template <int E, int NT, bool kCand>
-__global__ void __launch_bounds__(NT)
+__global__ void __launch_bounds__(NT, (kRegCtasPerSm<E, NT>))
 topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, int r,
                 const int32_t *__restrict__ q_seq, const int32_t *__restrict__ q_pos, int K,
                 int32_t *__restrict__ idx, uint32_t *status, const uint32_t *__restrict__ cmask,
                 int cand_words, FastDiv dbs) {
-  static_assert(E % 4 == 0 && E * NT <= kRegMax, "keys per thread");
-  using S = RegShape<NT>;
-  constexpr int kChunkSpan = S::kChunkSpan, kSelWords = S::kSelWords, kRegWarps = S::kWarps;
+  static_assert(E % 8 == 0 && E * NT <= kRegMax, "keys per thread");
+  constexpr int kWarps = NT / 32;
+  constexpr int kWords = E * NT / 32;                       // bitmap words: one per (slot, warp)
+  constexpr int kWordsPerThread = (kWords + NT - 1) / NT;   // in the ordered write-out
   __shared__ uint32_t hist[kDigitBins];
-  __shared__ uint32_t warp_sums[33];
-  __shared__ uint32_t sel_gt[kRegMax / 32], sel_eq[kRegMax / 32];  // pick bitmaps by position
+  __shared__ uint32_t sel_gt[kWords], sel_eq[kWords];       // pick bitmaps by position
+  __shared__ RegSel rs;
+  __shared__ uint32_t wmin[kWarps], wmax[kWarps];
   pdl_trigger();
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // the token arrays are inputs of the call, not outputs of the previous
@@ -282,31 +323,12 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
     for (int i = tid; i < K; i += NT) out[i] = i < nv ? i : -1;
     return;
   }
-  // the row's visible scores: chunk q of this thread is positions 4096 q + 4 tid .. + 3
-  const float *row = scores + static_cast<int64_t>(t) * ld;
+  // the visible slots of a thread are a prefix of its E
+  const int cnt = tid < nv ? min(E, (nv - tid + NT - 1) / NT) : 0;
+  const float *row = scores + static_cast<int64_t>(t) * ld + tid;
   uint32_t key[E];
-  if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
 #pragma unroll
-    for (int q = 0; q < E / 4; ++q) {
-      const int p0 = kChunkSpan * q + 4 * tid;
-      if (p0 + 3 < nv) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(row + p0);
-        key[4 * q] = u.x;
-        key[4 * q + 1] = u.y;
-        key[4 * q + 2] = u.z;
-        key[4 * q + 3] = u.w;
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) key[4 * q + j] = p0 + j < nv ? __float_as_uint(row[p0 + j]) : 0u;
-      }
-    }
-  } else {
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const int p0 = kChunkSpan * (e >> 2) + 4 * tid + (e & 3);
-      key[e] = p0 < nv ? __float_as_uint(row[p0]) : 0u;
-    }
-  }
+  for (int e = 0; e < E; ++e) key[e] = e < cnt ? __float_as_uint(row[NT * e]) : 0u;
   // the row's candidate mask (kCand) goes to shared memory with one load per
   // thread, issued beside the score loads
   __shared__ uint32_t cwords[kCand ? kRegMax / 32 : 1];
@@ -314,130 +336,145 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
     const uint32_t *crow = cmask + static_cast<int64_t>(t) * cand_words;
     for (int i = tid; i < cand_words; i += NT) cwords[i] = crow[i];
   }
-#pragma unroll
-  for (int w = 0; w < kSelWords; ++w) {
-    sel_gt[kSelWords * tid + w] = 0u;
-    sel_eq[kSelWords * tid + w] = 0u;
-  }
+  for (int i = tid; i < kDigitBins; i += NT) hist[i] = 0;  // the first pass's histogram
+  for (int i = tid; i < kWords; i += NT) sel_eq[i] = 0u;
+  if (tid == 0) rs.ncand = 0;
   if constexpr (kCand) {
-    // positions outside the kept candidate blocks score -inf; a chunk of four
-    // positions inside one block needs one look-up
+    // positions outside the kept candidate blocks score -inf
     __syncthreads();  // the mask words are in shared memory
+    if (NT % (32 * dbs.d) == 0) {
+      // blocks of 32 words' worth divide a slot's span: slot e of this thread
+      // is block NT e / size + tid / size, the same bit of every slot's word
+      const uint32_t tb = fast_div(static_cast<uint32_t>(tid), dbs);
+      const uint32_t *cw = cwords + (tb >> 5), bit = 1u << (tb & 31u);
+      const int step = NT / (32 * static_cast<int>(dbs.d));
 #pragma unroll
-    for (int q = 0; q < E / 4; ++q) {
-      const int p0 = kChunkSpan * q + 4 * tid;
-      if (p0 < nv) {
-        if (dbs.d % 4u == 0u || fast_div(p0, dbs) == fast_div(p0 + 3, dbs)) {
-          if (!cand_kept(cwords, p0, dbs)) {
+      for (int e = 0; e < E; ++e)
+        if (e < cnt && !(cw[step * e] & bit)) key[e] = kNegInfBits;
+    } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) key[4 * q + j] = kNegInfBits;
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (p0 + j < nv && !cand_kept(cwords, p0 + j, dbs)) key[4 * q + j] = kNegInfBits;
-        }
-      }
+      for (int e = 0; e < E; ++e)
+        if (e < cnt && !cand_kept(cwords, NT * e + tid, dbs)) key[e] = kNegInfBits;
     }
   }
-  // the visible keys of a thread are a prefix of its E: positions grow with e
-  const int rem = nv - 4 * tid;
-  const int cnt = rem <= 0 ? 0 : min(E, 4 * (rem / kChunkSpan) + min(4, rem % kChunkSpan));
-  auto pos_of = [&](int e) { return kChunkSpan * (e >> 2) + 4 * tid + (e & 3); };
-#pragma unroll
-  for (int e = 0; e < E; ++e) key[e] = e < cnt ? ordered_key(__uint_as_float(key[e])) : 0u;
-
   // the row's key range: keys become key - min (< 2^L)
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
 #pragma unroll
   for (int e = 0; e < E; ++e)
     if (e < cnt) {
+      key[e] = ordered_key(__uint_as_float(key[e]));
       kmin = min(kmin, key[e]);
       kmax = max(kmax, key[e]);
     }
   kmin = __reduce_min_sync(0xffffffffu, kmin);
   kmax = __reduce_max_sync(0xffffffffu, kmax);
-  __shared__ uint32_t wmin[kRegWarps], wmax[kRegWarps];
   if (lane == 0) {
     wmin[warp] = kmin;
     wmax[warp] = kmax;
   }
   __syncthreads();
-  kmin = __reduce_min_sync(0xffffffffu, lane < kRegWarps ? wmin[lane] : 0xFFFFFFFFu);
-  kmax = __reduce_max_sync(0xffffffffu, lane < kRegWarps ? wmax[lane] : 0u);
+  kmin = __reduce_min_sync(0xffffffffu, lane < kWarps ? wmin[lane] : 0xFFFFFFFFu);
+  kmax = __reduce_max_sync(0xffffffffu, lane < kWarps ? wmax[lane] : 0u);
 #pragma unroll
   for (int e = 0; e < E; ++e) key[e] = e < cnt ? key[e] - kmin : 0u;
   const int L = kmax > kmin ? 32 - __clz(kmax - kmin) : 0;
 
-  // radix select over bits [0, L), kDigitBits at a time from the top; once
-  // the chosen bin holds at most kFinish keys, they are ranked directly
-  int remaining = K;
-  uint32_t thr = 0u;
-  __shared__ uint32_t cand[kFinish], ncand, fin_thr, fin_above;
-  for (int hi = L; hi > 0;) {
+  // radix select over bits [0, L), kDigitBits at a time from the top, until
+  // the chosen bin holds at most kFinish keys or every bit is fixed
+  int remaining = K, hi = L;
+  uint32_t thr = 0u, in_bin = 0u;
+  if (hi > 0) {
     const int nb = hi < kDigitBits ? hi : kDigitBits, shift = hi - nb;
-    const uint32_t mask = hi >= 32 ? 0u : ~((1u << hi) - 1u);  // bits already fixed
-    uint32_t in_bin;
-    const uint32_t d = radix_pass<E, NT>(key, cnt, thr, mask, shift, 1 << nb, hist, warp_sums, remaining, in_bin);
-    thr |= d << shift;
+    thr = radix_pass<E, NT, true>(key, 0u, 0u, shift, 1 << nb, hist, rs, remaining, in_bin) << shift;
     hi = shift;
-    if (hi > 0 && in_bin <= static_cast<uint32_t>(kFinish)) {
-      // gather the bin's keys (those matching every fixed bit)
-      if (tid == 0) ncand = 0;
-      __syncthreads();
-      const uint32_t fixed = ~((1u << hi) - 1u);
+  }
+  while (hi > 0 && in_bin > static_cast<uint32_t>(kFinish)) {
+    const int nb = hi < kDigitBits ? hi : kDigitBits, shift = hi - nb;
+    const uint32_t mask = ~((1u << hi) - 1u);  // bits already fixed (hi < 32 after the first pass)
+    thr |= radix_pass<E, NT, false>(key, thr, mask, shift, 1 << nb, hist, rs, remaining, in_bin) << shift;
+    hi = shift;
+  }
+  uint32_t need_eq;
+  if (hi > 0) {
+    // keys above the chosen bin are picks: one ballot per slot fills the
+    // bitmap word of the warp's 32 positions; the bin's keys (at most
+    // kFinish) are gathered with their positions and ranked directly
+    const uint32_t fixed = ~((1u << hi) - 1u);
 #pragma unroll
-      for (int e = 0; e < E; ++e)
-        if (e < cnt && (key[e] & fixed) == thr) cand[atomicAdd(&ncand, 1u)] = key[e];
-      __syncthreads();
-      {
-        // the remaining-th largest among the candidates: the value v with
-        // #(> v) < remaining <= #(> v) + #(== v); thread i ranks candidate i
-        const uint32_t n = ncand, rem2 = static_cast<uint32_t>(remaining);
-        if (static_cast<uint32_t>(tid) < n) {
-          const uint32_t v = cand[tid];
-          uint32_t gt = 0, eq = 0;
-          for (uint32_t j = 0; j < n; ++j) {
-            const uint32_t u = cand[j];
-            gt += u > v;
-            eq += u == v;
-          }
-          if (gt < rem2 && rem2 <= gt + eq) {  // every thread holding that value agrees
-            fin_thr = v;
-            fin_above = gt;
-          }
+    for (int e = 0; e < E; ++e) {
+      const uint32_t kf = key[e] & fixed;
+      const uint32_t above = __ballot_sync(0xffffffffu, kf > thr);
+      if (lane == 0) sel_gt[kWarps * e + warp] = above;
+      const uint32_t inb = __ballot_sync(0xffffffffu, kf == thr);
+      if (inb != 0u) {
+        uint32_t base = 0;
+        if (lane == 0) base = atomicAdd(&rs.ncand, static_cast<uint32_t>(__popc(inb)));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if ((inb >> lane) & 1u) {
+          const uint32_t i = base + __popc(inb & lanemask_lt());
+          rs.cand[i] = key[e];
+          rs.cpos[i] = NT * e + tid;
         }
       }
-      __syncthreads();
-      thr = fin_thr;
-      remaining -= static_cast<int>(fin_above);
-      break;
     }
-  }
-  const uint32_t need_eq = static_cast<uint32_t>(remaining);
-
-  // picks into the bitmaps (few: K of nv keys)
+    __syncthreads();
+    // the remaining-th largest among the candidates is the value v with
+    // #(> v) < remaining <= #(>= v); candidate i is above it exactly when
+    // #(>= its key) < remaining, equal to it when #(> its key) < remaining <=
+    // #(>= its key), so each candidate places its own bit
+    const uint32_t n = rs.ncand, rem2 = static_cast<uint32_t>(remaining);
+    if (static_cast<uint32_t>(tid) < n) {
+      const uint32_t v = rs.cand[tid];
+      uint32_t gt = 0, ge = 0;
+      for (uint32_t j = 0; j < n; ++j) {
+        const uint32_t u = rs.cand[j];
+        gt += u > v;
+        ge += u >= v;
+      }
+      const int p = rs.cpos[tid];
+      if (ge < rem2)
+        atomicOr(&sel_gt[p >> 5], 1u << (p & 31));
+      else if (gt < rem2) {
+        atomicOr(&sel_eq[p >> 5], 1u << (p & 31));
+        rs.fin_above = gt;  // the same from every candidate equal to the k-th key
+      }
+    }
+    __syncthreads();
+    need_eq = rem2 - rs.fin_above;
+  } else {
+    // every bit fixed: thr is the k-th largest key itself
 #pragma unroll
-  for (int e = 0; e < E; ++e)
-    if (e < cnt && key[e] >= thr) {
-      const int p0 = pos_of(e);
-      atomicOr(key[e] > thr ? &sel_gt[p0 >> 5] : &sel_eq[p0 >> 5], 1u << (p0 & 31));
+    for (int e = 0; e < E; ++e) {
+      const uint32_t gt = __ballot_sync(0xffffffffu, key[e] > thr);
+      const uint32_t eq = __ballot_sync(0xffffffffu, key[e] == thr);
+      if (lane == 0) {
+        sel_gt[kWarps * e + warp] = gt;
+        sel_eq[kWarps * e + warp] = eq;
+      }
     }
-  __syncthreads();
-  // thread i writes the picks among its kSelWords words of 32 positions, in order
+    __syncthreads();
+    need_eq = static_cast<uint32_t>(remaining);
+  }
+
+  // thread i writes the picks among its words of 32 positions, in order
   uint32_t ng = 0, ne = 0;
 #pragma unroll
-  for (int w = 0; w < kSelWords; ++w) {
-    ng += __popc(sel_gt[kSelWords * tid + w]);
-    ne += __popc(sel_eq[kSelWords * tid + w]);
+  for (int w = 0; w < kWordsPerThread; ++w) {
+    const int wi = kWordsPerThread * tid + w;
+    if (wi < kWords) {
+      ng += __popc(sel_gt[wi]);
+      ne += __popc(sel_eq[wi]);
+    }
   }
   uint32_t tot;
-  const uint32_t pre = block_excl_scan((ng << 16) | ne, warp_sums, &tot);
+  const uint32_t pre = block_excl_scan((ng << 16) | ne, rs.warp_sums, &tot);
   uint32_t eq_seen = pre & 0xFFFFu;  // equal keys at lower positions
   uint32_t o = (pre >> 16) + min(eq_seen, need_eq);
 #pragma unroll
-  for (int w = 0; w < kSelWords; ++w) {
-    uint32_t take = sel_gt[kSelWords * tid + w], x = sel_eq[kSelWords * tid + w];
+  for (int w = 0; w < kWordsPerThread; ++w) {
+    const int wi = kWordsPerThread * tid + w;
+    if (wi >= kWords) break;
+    uint32_t take = sel_gt[wi], x = sel_eq[wi];
     for (; x != 0u && eq_seen < need_eq; ++eq_seen) {  // equal keys, lowest positions first
       take |= x & (0u - x);
       x &= x - 1u;
@@ -445,7 +482,7 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
     eq_seen += __popc(x);  // equal keys past the quota
     while (take != 0u) {
       const int bit = __ffs(take) - 1;
-      if (o < static_cast<uint32_t>(K)) out[o] = 32 * (kSelWords * tid + w) + bit;
+      if (o < static_cast<uint32_t>(K)) out[o] = 32 * wi + bit;
       ++o;
       take &= take - 1u;
     }
@@ -457,7 +494,7 @@ using RegKern = void (*)(const float *, int64_t, int, int, int, const int32_t *,
 
 template <bool kCand>
 RegKern pick_reg_kernel(int N_c, bool many_rows) {
-  constexpr int kE = RegShape<1024>::kE;  // 32 keys per thread at most with 1024 threads
+  constexpr int kE = kRegMax / 1024;  // 32 keys per thread at most with 1024 threads
   if (many_rows)
     return N_c <= kRegMax / 4 ? topk_reg_kernel<kE / 2, 512, kCand>
          : N_c <= kRegMax / 2 ? topk_reg_kernel<kE, 512, kCand>

@@ -100,6 +100,20 @@ def run_candidates(scores: np.ndarray, q_seq, q_pos, B: int, r: int, block_size:
     return cand.cpu().numpy().view(np.uint32)
 
 
+def run_topk_rows(scores: np.ndarray, q_seq, q_pos, B: int, r: int, K: int):
+    """sa_topk on given score rows and token arrays alone: [T, K] indices."""
+    ensure_built()
+    T, N_c = scores.shape
+    ia, keep = _token_args(B, N_c, r, q_seq, q_pos)
+    ws = _small_ws()
+    s = torch.from_numpy(np.ascontiguousarray(scores, dtype=np.float32)).cuda()
+    idx = torch.full((T, max(K, 1)), -7, dtype=torch.int32, device="cuda")
+    binding.sa_topk(s, ia, K, idx, ws)
+    assert binding.sa_check_device_status(ws) == binding.SA_OK
+    del keep
+    return idx[:, :K].cpu().numpy()
+
+
 def run_topk_candidates(scores: np.ndarray, q_seq, q_pos, B: int, r: int, K: int, cand: np.ndarray,
                         block_size: int):
     """Level two on the GPU: [T, K] indices."""

@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 import oracle
-from gpu_run import run_attn, run_fused, run_scores, run_topk
+from gpu_run import run_attn, run_fused, run_scores, run_topk, run_topk_rows
 from helpers import n_vis, problem
 from indexer_selected_sparse_score_gb300 import binding
 from indexer_selected_sparse_score_gb300 import workloads as wl
@@ -133,6 +133,48 @@ def test_topk_ties_and_sizes(N_c):
         nv = n_vis(int(w.q_pos[t]), w.r)
         ref = oracle.topk_row(scores[t].astype(np.float64), nv, spec.K)
         assert idx[t].tolist() == ref.tolist(), t
+
+
+@pytest.mark.parametrize("T", [6, 320])
+@pytest.mark.parametrize("N_c", [5000, 12000, 30000])
+def test_topk_threshold_at_the_row_minimum(N_c, T):
+    """Rows whose k-th largest score is at or next to the row's minimum, so the
+    selection meets the slots past the visible count (key 0, the smallest after
+    the range shift), plus rows of two or three levels and a constant row: exact
+    match with the oracle, for every register top-k shape (6 rows: 1024 threads
+    per row; 320 rows: 512 threads).  Scores past the visible count are large,
+    so reading any of them would show."""
+    K = 700
+    rng = np.random.default_rng(N_c + T)
+    nv = np.empty(T, dtype=np.int64)
+    scores = np.full((T, N_c), 100.0, dtype=np.float32)
+    for t in range(T):
+        kind = t % 6
+        if kind == 0:    # one position left out: the k-th largest is the second smallest
+            nv[t] = K + 1
+            row = rng.normal(size=nv[t])
+        elif kind == 1:  # the ten smallest tie at the row minimum; five of them are taken
+            nv[t] = K + 5
+            row = rng.normal(size=nv[t])
+            row[rng.choice(nv[t], 10, replace=False)] = row.min() - 1.0
+        elif kind == 2:  # three levels over the whole row
+            nv[t] = N_c
+            row = rng.integers(0, 3, size=nv[t]).astype(np.float64)
+        elif kind == 3:  # quarter steps (ties everywhere) at a random visible count
+            nv[t] = rng.integers(K + 1, N_c + 1)
+            row = np.round(rng.normal(size=nv[t]) * 4) / 4
+        elif kind == 4:  # a constant row
+            nv[t] = rng.integers(K + 1, N_c + 1)
+            row = np.full(nv[t], -1.0)
+        else:            # two levels, the upper one held by fewer than K positions
+            nv[t] = rng.integers(2 * K, N_c + 1)
+            row = np.zeros(nv[t])
+            row[rng.choice(nv[t], K // 3, replace=False)] = 2.0
+        scores[t, :nv[t]] = row
+    idx = run_topk_rows(scores, np.arange(T, dtype=np.int32), (nv - 1).astype(np.int32), T, 1, K)
+    for t in range(T):
+        ref = oracle.topk_row(scores[t].astype(np.float64), int(nv[t]), K)
+        assert idx[t].tolist() == ref.tolist(), (t, t % 6, int(nv[t]))
 
 
 @pytest.mark.parametrize("H", [16, 64])
