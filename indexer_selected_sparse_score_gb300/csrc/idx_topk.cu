@@ -343,8 +343,9 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
     // positions outside the kept candidate blocks score -inf
     __syncthreads();  // the mask words are in shared memory
     if (NT % (32 * dbs.d) == 0) {
-      // blocks of 32 words' worth divide a slot's span: slot e of this thread
-      // is block NT e / size + tid / size, the same bit of every slot's word
+      // NT a multiple of 32 block sizes: position NT e + tid lies in block
+      // NT e / size + tid / size, i.e. the same bit of a mask word that moves
+      // NT / (32 size) words per slot
       const uint32_t tb = fast_div(static_cast<uint32_t>(tid), dbs);
       const uint32_t *cw = cwords + (tb >> 5), bit = 1u << (tb & 31u);
       const int step = NT / (32 * static_cast<int>(dbs.d));
