@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -113,11 +114,19 @@ STAGE_SOURCES = {"idx_score": ("idx_score.cu", "idx_score_umma.cu", "umma.cuh", 
                                 "common.cuh")}
 
 
+def _code_only(text):
+    """Source text without comments, blank lines or trailing blanks: an edit to
+    a comment leaves the hash (and so a recorded capture) unchanged."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash(stage):
     h = hashlib.sha256()
     for src in STAGE_SOURCES[stage]:
-        with open(os.path.join(ROOT, "indexer_selected_sparse_score_gb300", "csrc", src), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "indexer_selected_sparse_score_gb300", "csrc", src)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
