@@ -326,8 +326,18 @@ def two_level_topk(binding, torch, wl, steps, peak):
     if binding.sa_check_device_status(ws) != binding.SA_OK:
         raise RuntimeError("device status not OK after the two-level top-k")
     nb = (nv + CAND_BLOCK - 1) // CAND_BLOCK
+    # level two reads the scores of the kept visible positions (blocks of 8 are
+    # compacted), counted from level one's mask
+    bits = np.unpackbits(cand.cpu().numpy().view(np.uint8), axis=1, bitorder="little")
+    kept_vis = 0
+    for t in range(T):
+        kb = np.nonzero(bits[t, :nb[t]])[0]
+        c = len(kb) * CAND_BLOCK
+        if len(kb) and kb[-1] == nb[t] - 1:
+            c -= int(nb[t]) * CAND_BLOCK - int(nv[t])
+        kept_vis += c
     alg = {"level_one": int(nv.sum() * 4 + T * words * 4),          # visible scores read, mask written
-           "level_two": int(nv.sum() * 4 + T * words * 4 + T * K * 4),  # scores and mask read, indices written
+           "level_two": int(kept_vis * 4 + T * words * 4 + T * K * 4),  # kept scores and mask read, indices written
            "one_level_topk": int(nv.sum() * 4 + T * K * 4)}
     res = {"workload": "128 tokens, N_c 32768, lengths U[8192,131072], r 4 (the ragged long-context decode "
                        "geometry); N(0,1) fp32 scores; blocks of 8, 2048 kept; K 2048; L2 flushed per launch",

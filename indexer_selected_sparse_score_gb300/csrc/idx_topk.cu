@@ -218,13 +218,14 @@ struct RegSel {
 // `remaining`-th largest.  Returns the digit; `remaining` becomes the rank
 // within that bin.  kFirst: the first pass, whose keys all match (they are
 // below 2^L and shift + log2(nbins) = L) and whose histogram was zeroed before
-// the block's first barrier.  Each warp sums its threads' bins; every warp then
+// the block's first barrier.  kBounded: only slots below `nslots` (the same for
+// every thread) are counted.  Each warp sums its threads' bins; every warp then
 // finds, from the warp totals, the warp whose bins hold the rank, and that
 // warp alone locates the bin.
-template <int E, int NT, bool kFirst>
+template <int E, int NT, bool kFirst, bool kBounded = false>
 __device__ __forceinline__ uint32_t radix_pass(const uint32_t (&key)[E], uint32_t prefix, uint32_t mask, int shift,
                                                int nbins, uint32_t *hist, RegSel &rs, int &remaining,
-                                               uint32_t &in_bin) {
+                                               uint32_t &in_bin, int nslots = E) {
   constexpr int R = kDigitBins / NT;  // ranks (bins) per thread
   constexpr int kWarps = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -234,6 +235,7 @@ __device__ __forceinline__ uint32_t radix_pass(const uint32_t (&key)[E], uint32_
   }
 #pragma unroll
   for (int e = 0; e < E; ++e) {
+    if (kBounded && e >= nslots) break;  // kBounded: slots from nslots on hold no key of any thread
     if constexpr (kFirst)
       atomicAdd(&hist[key[e] >> shift], 1u);
     else if ((key[e] & mask) == prefix)
@@ -490,6 +492,265 @@ topk_reg_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, in
   }
 }
 
+// ---------------------------------------------------------------------------
+// Level two with compaction, for candidate blocks of at least kCompactMinBlock
+// positions: the selection runs over the kept visible positions alone, listed
+// in ascending order (kept block ids in shared memory; candidate c is position
+// list[c / size] * size + c % size), so its slots stop at the row's candidate
+// count instead of the row's length.  The row the selection stands for is the
+// visible row with -inf outside the kept blocks.  Its k-th largest value is a
+// candidate's while at least K candidates score above -inf (nfin >= K): the
+// radix select then runs over the candidates' keys, and every other position
+// lies below it.  Otherwise it is -inf: every candidate above -inf is a pick,
+// and the rest are the lowest-positioned of the positions that score -inf
+// (candidates at -inf and the visible positions outside the kept blocks).
+// Candidate slots past the count hold key 0 and set no bit: as with the
+// register kernel, they sit below every candidate and are never needed to fill
+// the picks of the value they may tie.
+constexpr int kCompactMinBlock = 4;                    // the block list fits 8192 uint16 entries
+constexpr uint32_t kNegInfKey = ~kNegInfBits;          // ordered key of -inf
+
+template <int E, int NT>
+__global__ void __launch_bounds__(NT, (kRegCtasPerSm<E, NT>))
+topk_cand_kernel(const float *__restrict__ scores, int64_t ld, int B, int N_c, int r,
+                 const int32_t *__restrict__ q_seq, const int32_t *__restrict__ q_pos, int K,
+                 int32_t *__restrict__ idx, uint32_t *status, const uint32_t *__restrict__ cmask,
+                 int cand_words, FastDiv dbs) {
+  static_assert(E % 8 == 0 && E * NT <= kRegMax, "keys per thread");
+  constexpr int kWarps = NT / 32;
+  constexpr int kWords = E * NT / 32;                       // position bitmap words
+  constexpr int kWordsPerThread = (kWords + NT - 1) / NT;
+  constexpr int kMaxBlocks = kRegMax / kCompactMinBlock;
+  __shared__ uint32_t hist[kDigitBins];
+  __shared__ uint32_t sel_gt[kWords], sel_eq[kWords];
+  __shared__ RegSel rs;
+  __shared__ uint32_t wred[3][kWarps];
+  __shared__ uint32_t cwords[kRegMax / 32];
+  __shared__ uint16_t blist[kMaxBlocks];                    // kept visible blocks, ascending
+  pdl_trigger();
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  Token tk;
+  const bool ok = load_token(q_seq, q_pos, t, B, N_c, r, status, tk, tid == 0);
+  const int nv = ok ? tk.nv : 0;
+  int32_t *out = idx + static_cast<int64_t>(t) * K;
+  pdl_wait();  // the scores and the block mask come from the previous kernels
+  if (nv <= K) {  // every visible position is kept
+    for (int i = tid; i < K; i += NT) out[i] = i < nv ? i : -1;
+    return;
+  }
+  const uint32_t bs = dbs.d;
+  const int nbv = static_cast<int>(fast_div(static_cast<uint32_t>(nv) + bs - 1u, dbs));  // blocks holding a visible position
+  const int nwv = (nbv + 31) >> 5;                                                      // their mask words
+  const uint32_t *crow = cmask + static_cast<int64_t>(t) * cand_words;
+  for (int i = tid; i < kDigitBins; i += NT) hist[i] = 0;  // the first pass's histogram
+  for (int i = tid; i < kWords; i += NT) {
+    sel_gt[i] = 0u;
+    sel_eq[i] = 0u;
+  }
+  if (tid == 0) rs.ncand = 0;
+  // the kept visible blocks in ascending order: a block scan of the mask words'
+  // counts, then each thread lists its words' blocks (one word per thread per round)
+  uint32_t listed = 0;  // blocks listed by earlier rounds
+  for (int w0 = 0; w0 < nwv; w0 += NT) {
+    const int w = w0 + tid;
+    uint32_t m = 0u;
+    if (w < nwv) {
+      m = crow[w];
+      if (w == nwv - 1 && (nbv & 31)) m &= (1u << (nbv & 31)) - 1u;  // blocks past the visible end
+      cwords[w] = m;
+    }
+    uint32_t tot;
+    uint32_t o = listed + block_excl_scan(static_cast<uint32_t>(__popc(m)), rs.warp_sums, &tot);
+    for (uint32_t x = m; x != 0u; x &= x - 1u) blist[o++] = static_cast<uint16_t>(32 * w + __ffs(x) - 1);
+    listed += tot;
+  }
+  __syncthreads();  // the list and the mask words are in shared memory
+  const int nkept = static_cast<int>(listed);
+  // candidate count: the kept blocks' positions below nv (only the block
+  // holding position nv - 1 can be cut short, and it is listed last)
+  int ncv = nkept * static_cast<int>(bs);
+  if (nkept > 0 && static_cast<int>(blist[nkept - 1]) == nbv - 1) ncv -= nbv * static_cast<int>(bs) - nv;
+  ncv = min(ncv, E * NT);
+  const int nslots = (ncv + NT - 1) / NT;                   // slots holding a candidate of some thread
+  const float *row = scores + static_cast<int64_t>(t) * ld;
+  uint32_t key[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) key[e] = 0u;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if (e >= nslots) break;
+    const int c = NT * e + tid;
+    if (c < ncv) {
+      const uint32_t kb = fast_div(static_cast<uint32_t>(c), dbs);
+      const int pos = static_cast<int>(blist[kb] * bs + (static_cast<uint32_t>(c) - kb * bs));
+      key[e] = __float_as_uint(row[pos]);
+    }
+  }
+  auto pos_of = [&](int c) -> int {
+    const uint32_t kb = fast_div(static_cast<uint32_t>(c), dbs);
+    return static_cast<int>(blist[kb] * bs + (static_cast<uint32_t>(c) - kb * bs));
+  };
+  // keys, the candidates' range, and how many score above -inf
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u, nf = 0u;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if (e >= nslots) break;
+    if (NT * e + tid < ncv) {
+      key[e] = ordered_key(__uint_as_float(key[e]));
+      kmin = min(kmin, key[e]);
+      kmax = max(kmax, key[e]);
+      nf += key[e] > kNegInfKey;
+    }
+  }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  nf = __reduce_add_sync(0xffffffffu, nf);
+  if (lane == 0) {
+    wred[0][warp] = kmin;
+    wred[1][warp] = kmax;
+    wred[2][warp] = nf;
+  }
+  __syncthreads();
+  kmin = __reduce_min_sync(0xffffffffu, lane < kWarps ? wred[0][lane] : 0xFFFFFFFFu);
+  kmax = __reduce_max_sync(0xffffffffu, lane < kWarps ? wred[1][lane] : 0u);
+  const uint32_t nfin = __reduce_add_sync(0xffffffffu, lane < kWarps ? wred[2][lane] : 0u);
+  uint32_t need_eq;
+  if (nfin < static_cast<uint32_t>(K)) {
+    // the k-th value is -inf: candidates above it are picks; the rest come,
+    // lowest position first, from the candidates at -inf and the visible
+    // positions outside the kept blocks
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if (e >= nslots) break;
+      const int c = NT * e + tid;
+      if (c < ncv) {
+        const int p = pos_of(c);
+        atomicOr(key[e] > kNegInfKey ? &sel_gt[p >> 5] : &sel_eq[p >> 5], 1u << (p & 31));
+      }
+    }
+    const int nwp = (nv + 31) >> 5;  // words of visible positions
+    for (int w = tid; w < nwp; w += NT) {
+      uint32_t outside = 0u;
+      for (int b = 0; b < 32; ++b) {
+        const int p = 32 * w + b;
+        if (p < nv) {
+          const uint32_t blk = fast_div(static_cast<uint32_t>(p), dbs);
+          if (!((cwords[blk >> 5] >> (blk & 31)) & 1u)) outside |= 1u << b;
+        }
+      }
+      atomicOr(&sel_eq[w], outside);
+    }
+    __syncthreads();
+    need_eq = static_cast<uint32_t>(K) - nfin;
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if (e >= nslots) break;
+      key[e] = NT * e + tid < ncv ? key[e] - kmin : 0u;
+    }
+    const int L = kmax > kmin ? 32 - __clz(kmax - kmin) : 0;
+    int remaining = K, hi = L;
+    uint32_t thr = 0u, in_bin = 0u;
+    if (hi > 0) {
+      const int nb = hi < kDigitBits ? hi : kDigitBits, shift = hi - nb;
+      thr = radix_pass<E, NT, true, true>(key, 0u, 0u, shift, 1 << nb, hist, rs, remaining, in_bin, nslots) << shift;
+      hi = shift;
+    }
+    while (hi > 0 && in_bin > static_cast<uint32_t>(kFinish)) {
+      const int nb = hi < kDigitBits ? hi : kDigitBits, shift = hi - nb;
+      const uint32_t mask = ~((1u << hi) - 1u);
+      thr |= radix_pass<E, NT, false, true>(key, thr, mask, shift, 1 << nb, hist, rs, remaining, in_bin, nslots)
+             << shift;
+      hi = shift;
+    }
+    if (hi > 0) {
+      // the chosen bin's keys (at most kFinish) are gathered with their
+      // positions and rank themselves; keys above the bin are picks
+      const uint32_t fixed = ~((1u << hi) - 1u);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        if (e >= nslots) break;
+        const int c = NT * e + tid;
+        const uint32_t kf = key[e] & fixed;
+        if (c < ncv) {
+          if (kf > thr) {
+            const int p = pos_of(c);
+            atomicOr(&sel_gt[p >> 5], 1u << (p & 31));
+          } else if (kf == thr) {
+            const uint32_t i = atomicAdd(&rs.ncand, 1u);
+            rs.cand[i] = key[e];
+            rs.cpos[i] = pos_of(c);
+          }
+        }
+      }
+      __syncthreads();
+      const uint32_t n = rs.ncand, rem2 = static_cast<uint32_t>(remaining);
+      if (static_cast<uint32_t>(tid) < n) {
+        const uint32_t v = rs.cand[tid];
+        uint32_t gt = 0, ge = 0;
+        for (uint32_t j = 0; j < n; ++j) {
+          const uint32_t u = rs.cand[j];
+          gt += u > v;
+          ge += u >= v;
+        }
+        const int p = rs.cpos[tid];
+        if (ge < rem2)
+          atomicOr(&sel_gt[p >> 5], 1u << (p & 31));
+        else if (gt < rem2) {
+          atomicOr(&sel_eq[p >> 5], 1u << (p & 31));
+          rs.fin_above = gt;  // the same from every candidate equal to the k-th key
+        }
+      }
+      __syncthreads();
+      need_eq = rem2 - rs.fin_above;
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        if (e >= nslots) break;
+        const int c = NT * e + tid;
+        if (c < ncv && key[e] >= thr) {
+          const int p = pos_of(c);
+          atomicOr(key[e] > thr ? &sel_gt[p >> 5] : &sel_eq[p >> 5], 1u << (p & 31));
+        }
+      }
+      __syncthreads();
+      need_eq = static_cast<uint32_t>(remaining);
+    }
+  }
+
+  // thread i writes the picks among its words of 32 positions, in order
+  uint32_t ng = 0, ne = 0;
+#pragma unroll
+  for (int w = 0; w < kWordsPerThread; ++w) {
+    const int wi = kWordsPerThread * tid + w;
+    if (wi < kWords) {
+      ng += __popc(sel_gt[wi]);
+      ne += __popc(sel_eq[wi]);
+    }
+  }
+  uint32_t tot;
+  const uint32_t pre = block_excl_scan((ng << 16) | ne, rs.warp_sums, &tot);
+  uint32_t eq_seen = pre & 0xFFFFu;
+  uint32_t o = (pre >> 16) + min(eq_seen, need_eq);
+#pragma unroll
+  for (int w = 0; w < kWordsPerThread; ++w) {
+    const int wi = kWordsPerThread * tid + w;
+    if (wi >= kWords) break;
+    uint32_t take = sel_gt[wi], x = sel_eq[wi];
+    for (; x != 0u && eq_seen < need_eq; ++eq_seen) {
+      take |= x & (0u - x);
+      x &= x - 1u;
+    }
+    eq_seen += __popc(x);
+    while (take != 0u) {
+      const int bit = __ffs(take) - 1;
+      if (o < static_cast<uint32_t>(K)) out[o] = 32 * wi + bit;
+      ++o;
+      take &= take - 1u;
+    }
+  }
+}
+
 using RegKern = void (*)(const float *, int64_t, int, int, int, const int32_t *, const int32_t *, int, int32_t *,
                          uint32_t *, const uint32_t *, int, FastDiv);
 
@@ -505,6 +766,18 @@ RegKern pick_reg_kernel(int N_c, bool many_rows) {
                             : topk_reg_kernel<kE, 1024, kCand>;
 }
 
+template <int Dummy = 0>
+RegKern pick_cand_kernel(int N_c, bool many_rows) {
+  constexpr int kE = kRegMax / 1024;
+  if (many_rows)
+    return N_c <= kRegMax / 4 ? topk_cand_kernel<kE / 2, 512>
+         : N_c <= kRegMax / 2 ? topk_cand_kernel<kE, 512>
+                              : topk_cand_kernel<2 * kE, 512>;
+  return N_c <= kRegMax / 4 ? topk_cand_kernel<kE / 4, 1024>
+       : N_c <= kRegMax / 2 ? topk_cand_kernel<kE / 2, 1024>
+                            : topk_cand_kernel<kE, 1024>;
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const float *scores, int64_t ld, const sa_index_args &ia, int K,
@@ -517,7 +790,11 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const sa_index_args &ia
     return launch_ex(programmatic, topk_radix_kernel, dim3(ia.T), dim3(kTopkThreads), 0, stream, 1, scores, ld, ia.B,
                      ia.N_c, ia.r, ia.q_seq, ia.q_pos, K, idx, status, cand, cand_words, dbs);
   const bool many_rows = ia.T > 2 * sm_count();
-  const RegKern kern = cand ? pick_reg_kernel<true>(ia.N_c, many_rows) : pick_reg_kernel<false>(ia.N_c, many_rows);
+  // level two: blocks of kCompactMinBlock positions or more are compacted
+  // (the selection runs over the kept positions), smaller ones masked in place
+  const RegKern kern = !cand ? pick_reg_kernel<false>(ia.N_c, many_rows)
+                       : block_size >= kCompactMinBlock ? pick_cand_kernel(ia.N_c, many_rows)
+                                                        : pick_reg_kernel<true>(ia.N_c, many_rows);
   // programmatic (after the scoring kernel of the fused step): the CTAs take
   // SMs as the scoring kernel's CTAs finish (they all started before any of
   // these can) and wait for it before reading the scores
