@@ -37,3 +37,15 @@ def test_step_bytes_match_the_per_query_formula(name, mean_mb):
 def test_peak_source():
     peak, src = bench.peaks()
     assert peak > 1000 and src in ("measured", "fallback")
+
+
+def test_recorded_traffic_survives_comment_edits_only():
+    """A capture stays attached to a kernel while only its comments change:
+    the source hash ignores comments and blank lines but not code."""
+    src = "int f(int x) {  // doubles x\n  /* a block\n     comment */\n  return 2 * x;\n}\n"
+    same = "int f(int x) {  // twice x\n\n  return 2 * x;  // result\n}\n"
+    other = "int f(int x) {  // doubles x\n  return 3 * x;\n}\n"
+    assert bench._code_only(src) == bench._code_only(same)
+    assert bench._code_only(src) != bench._code_only(other)
+    for stage in bench.STAGE_SOURCES:
+        assert len(bench.kernel_source_hash(stage)) == 16
