@@ -112,6 +112,26 @@ def test_level_two_arbitrary_mask():
     check_level_two(scores, nv, K, keep, bs, q_seq, q_pos)
 
 
+@pytest.mark.parametrize("bs", [1, 2, 3, 4])
+@pytest.mark.parametrize("T,N_c,K", [(12, 5000, 300), (12, 30000, 700), (320, 12000, 300)])
+def test_level_two_block_sizes_around_compaction(T, N_c, K, bs):
+    """Blocks of 1-3 positions take the masked register kernel and blocks of 4
+    the compacting one: both exact against the oracle, with level one's masks
+    (few and many blocks kept) and with random masks (about a tenth and half of
+    the blocks), at 1024 and 512 threads per row."""
+    scores = planted(T, N_c, seed=T + N_c + bs)
+    nv = visible_counts(T, N_c, bs, seed=T * N_c + bs)
+    q_seq, q_pos = tokens_for(nv)
+    nb = (N_c + bs - 1) // bs
+    for tb in (K // bs // 4 + 1, nb // 2):
+        cand, keep, q_seq1, q_pos1 = check_level_one(scores, nv, bs, tb)
+        check_level_two(scores, nv, K, keep, bs, q_seq1, q_pos1, cand=cand)
+    rng = np.random.default_rng(bs)
+    for frac in (0.1, 0.5):
+        keep = rng.random((T, nb)) < frac
+        check_level_two(scores, nv, K, keep, bs, q_seq, q_pos)
+
+
 @pytest.mark.parametrize("name", ["i64x128_fp8k", "umma_many"])
 def test_two_level_on_indexer_scores(name):
     """Index scores from the GPU's indexer, then level one (blocks of 8) and
