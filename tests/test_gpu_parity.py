@@ -177,6 +177,29 @@ def test_topk_threshold_at_the_row_minimum(N_c, T):
         assert idx[t].tolist() == ref.tolist(), (t, t % 6, int(nv[t]))
 
 
+@pytest.mark.parametrize("K", [1, 2, 31, 255, 256, 257, 4095, 9000])
+def test_topk_k_sweep(K):
+    """K from one pick to most of the row, around the 256-key bin that is ranked
+    directly, on rows of normal scores, of ties (quarter steps) and of two
+    levels: exact against the oracle (rows shorter than K keep all of theirs)."""
+    T, N_c = 9, 12000
+    rng = np.random.default_rng(K)
+    nv = np.array([N_c, N_c - 1, 10000, 5000, max(1, K - 1), K, K + 1, 3, N_c], dtype=np.int64)
+    nv = np.minimum(nv, N_c)
+    scores = np.full((T, N_c), 50.0, dtype=np.float32)
+    for t in range(T):
+        row = rng.normal(size=N_c)
+        if t % 3 == 1:
+            row = np.round(row * 4) / 4
+        elif t % 3 == 2:
+            row = (rng.random(N_c) < 0.3).astype(np.float64)
+        scores[t, :nv[t]] = row[:nv[t]]
+    idx = run_topk_rows(scores, np.arange(T, dtype=np.int32), (nv - 1).astype(np.int32), T, 1, K)
+    for t in range(T):
+        ref = oracle.topk_row(scores[t].astype(np.float64), int(nv[t]), K)
+        assert idx[t].tolist() == ref.tolist(), (K, t, int(nv[t]))
+
+
 @pytest.mark.parametrize("H", [16, 64])
 def test_k_zero_is_window_only(H):
     w = wl.generate(wl.small("k0", K=0, H=H, W=130, R=130), seed=5)
